@@ -1,0 +1,255 @@
+"""CPU oracle for batch-1 decoder decode (ctypes wrapper over lf_oracle.c).
+
+TEST INFRASTRUCTURE ONLY: tests/, __graft_entry__.smoke() and bench.py's
+cpu_baseline / reference leg are the only users.  Nothing in the
+persistent_monokernel_gb300 package imports this module, and this module
+imports nothing from that package.
+
+Precision: FP32 activations and FP32 sums in index order (the KOG monokernel
+write-up, shivam2003.com, "The fused operations, briefly": FP32-accumulated
+GEMV partial products), FP16 weights and an FP16 KV cache.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "lf_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+CFLAGS = ["-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared", "-Wall"]
+
+
+def build(force: bool = False) -> str:
+    """Compile liboracle.so with gcc (plain C11 + OpenMP)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+class _Config(C.Structure):
+    _fields_ = [("n_layers", C.c_int), ("d_model", C.c_int), ("n_heads", C.c_int), ("n_kv_heads", C.c_int),
+                ("head_dim", C.c_int), ("ffn_dim", C.c_int), ("vocab", C.c_int), ("max_seq", C.c_int),
+                ("rope_theta", C.c_float), ("rms_eps", C.c_float)]
+
+
+_WNAMES = ("embed", "attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down",
+           "final_norm", "lm_head")
+
+
+class _Weights(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in _WNAMES]
+
+
+def lib():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            L = C.CDLL(_LIB)
+            f32p = C.POINTER(C.c_float)
+            u16p = C.POINTER(C.c_uint16)
+            L.orc_half_to_float.argtypes = [C.c_uint16]
+            L.orc_half_to_float.restype = C.c_float
+            L.orc_float_to_half.argtypes = [C.c_float]
+            L.orc_float_to_half.restype = C.c_uint16
+            L.orc_rmsnorm.argtypes = [f32p, u16p, C.c_int, C.c_float, f32p]
+            L.orc_matvec.argtypes = [u16p, f32p, C.c_int, C.c_int, f32p]
+            L.orc_rope.argtypes = [f32p, C.c_int, C.c_int, C.c_float]
+            L.orc_attend_head.argtypes = [f32p, u16p, u16p, C.c_int, C.c_int, C.c_float, f32p, f32p]
+            L.orc_silu.argtypes = [C.c_float]
+            L.orc_silu.restype = C.c_float
+            L.orc_philox4x32_10.argtypes = [C.POINTER(C.c_uint32), C.POINTER(C.c_uint32), C.POINTER(C.c_uint32)]
+            L.orc_gumbel.argtypes = [C.c_uint64, C.c_int, C.c_int]
+            L.orc_gumbel.restype = C.c_float
+            L.orc_sample.argtypes = [f32p, C.c_int, C.c_float, C.c_int, C.c_uint64, C.c_int]
+            L.orc_sample.restype = C.c_int
+            L.orc_create.argtypes = [C.POINTER(_Config), C.POINTER(_Weights)]
+            L.orc_create.restype = C.c_void_p
+            L.orc_destroy.argtypes = [C.c_void_p]
+            L.orc_reset.argtypes = [C.c_void_p]
+            L.orc_pos.argtypes = [C.c_void_p]
+            L.orc_pending.argtypes = [C.c_void_p]
+            L.orc_kcache.argtypes = [C.c_void_p]
+            L.orc_kcache.restype = C.c_void_p
+            L.orc_vcache.argtypes = [C.c_void_p]
+            L.orc_vcache.restype = C.c_void_p
+            L.orc_forward.argtypes = [C.c_void_p, C.c_int, f32p]
+            L.orc_prefill.argtypes = [C.c_void_p, C.POINTER(C.c_int32), C.c_int]
+            L.orc_decode.argtypes = [C.c_void_p, C.c_int, C.c_float, C.c_int, C.c_uint64,
+                                     C.POINTER(C.c_int32), C.POINTER(C.c_int32), f32p]
+            _lib = L
+    return _lib
+
+
+def _f32(a):
+    return a.ctypes.data_as(C.POINTER(C.c_float))
+
+
+def _u16(a):
+    return a.ctypes.data_as(C.POINTER(C.c_uint16))
+
+
+def _i32(a):
+    return a.ctypes.data_as(C.POINTER(C.c_int32))
+
+
+def _as_u16(a) -> np.ndarray:
+    """FP16 data (numpy float16 / torch float16 CPU tensor) viewed as uint16, C-contiguous."""
+    if hasattr(a, "numpy"):
+        a = a.detach().cpu().contiguous().numpy()
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.float16:
+        a = a.view(np.uint16)
+    if a.dtype != np.uint16:
+        raise TypeError("expected FP16 data")
+    return a
+
+
+# ---------------------------------------------------------------- op level
+
+def half_to_float(bits: int) -> float:
+    return lib().orc_half_to_float(bits)
+
+
+def float_to_half(x: float) -> int:
+    return lib().orc_float_to_half(x)
+
+
+def rmsnorm(x, g, eps):
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    g = _as_u16(g)
+    out = np.empty_like(x)
+    lib().orc_rmsnorm(_f32(x), _u16(g), x.size, eps, _f32(out))
+    return out
+
+
+def matvec(W, x):
+    W = _as_u16(W)
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    y = np.empty(W.shape[0], dtype=np.float32)
+    lib().orc_matvec(_u16(W), _f32(x), W.shape[0], W.shape[1], _f32(y))
+    return y
+
+
+def rope(v, pos, base):
+    v = np.array(v, dtype=np.float32, copy=True)
+    lib().orc_rope(_f32(v), v.size, pos, base)
+    return v
+
+
+def attend_head(q, K, V, scale):
+    q = np.ascontiguousarray(q, dtype=np.float32)
+    K = _as_u16(K)
+    V = _as_u16(V)
+    ctx, hd = K.shape
+    scores = np.empty(ctx, dtype=np.float32)
+    out = np.empty(hd, dtype=np.float32)
+    lib().orc_attend_head(_f32(q), _u16(K), _u16(V), ctx, hd, scale, _f32(scores), _f32(out))
+    return out, scores
+
+
+def silu(z: float) -> float:
+    return lib().orc_silu(z)
+
+
+def philox4x32_10(ctr, key):
+    c = (C.c_uint32 * 4)(*[int(v) & 0xFFFFFFFF for v in ctr])
+    k = (C.c_uint32 * 2)(*[int(v) & 0xFFFFFFFF for v in key])
+    o = (C.c_uint32 * 4)()
+    lib().orc_philox4x32_10(c, k, o)
+    return [int(v) for v in o]
+
+
+def gumbel(seed: int, pos: int, i: int) -> float:
+    return lib().orc_gumbel(seed, pos, i)
+
+
+def sample(logits, temperature: float, top_k: int, seed: int, pos: int) -> int:
+    lg = np.ascontiguousarray(logits, dtype=np.float32)
+    return lib().orc_sample(_f32(lg), lg.size, temperature, top_k, seed, pos)
+
+
+def num_threads() -> int:
+    return lib().orc_num_threads()
+
+
+# ------------------------------------------------------------- the decoder
+
+class OracleDecoder:
+    """The whole decoder on the CPU.  `weights` maps the synthetic tensor
+    names to FP16 arrays (numpy float16 or CPU torch.float16)."""
+
+    def __init__(self, cfg, weights: dict, max_seq: int):
+        self.cfg = cfg
+        self.max_seq = max_seq
+        self._keep = {n: _as_u16(weights[n]) for n in _WNAMES}
+        c = _Config(cfg.n_layers, cfg.d_model, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim, cfg.ffn_dim,
+                    cfg.vocab, max_seq, cfg.rope_theta, cfg.rms_eps)
+        w = _Weights(*[self._keep[n].ctypes.data for n in _WNAMES])
+        self._h = lib().orc_create(C.byref(c), C.byref(w))
+        if not self._h:
+            raise ValueError("orc_create rejected the configuration")
+
+    def close(self):
+        if getattr(self, "_h", None):
+            lib().orc_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        self.close()
+
+    def reset(self):
+        lib().orc_reset(self._h)
+
+    @property
+    def pos(self) -> int:
+        return lib().orc_pos(self._h)
+
+    @property
+    def pending(self) -> int:
+        return lib().orc_pending(self._h)
+
+    def kv_cache(self):
+        c = self.cfg
+        n = c.n_layers * c.n_kv_heads * self.max_seq * c.head_dim
+        shape = (c.n_layers, c.n_kv_heads, self.max_seq, c.head_dim)
+        k = np.ctypeslib.as_array(C.cast(lib().orc_kcache(self._h), C.POINTER(C.c_uint16)), (n,))
+        v = np.ctypeslib.as_array(C.cast(lib().orc_vcache(self._h), C.POINTER(C.c_uint16)), (n,))
+        return k.reshape(shape).view(np.float16).copy(), v.reshape(shape).view(np.float16).copy()
+
+    def forward(self, token: int, want_logits: bool = True):
+        lg = np.empty(self.cfg.vocab, dtype=np.float32) if want_logits else None
+        rc = lib().orc_forward(self._h, int(token), _f32(lg) if want_logits else None)
+        if rc:
+            raise ValueError("orc_forward failed (cache full or bad token)")
+        return lg
+
+    def prefill(self, tokens):
+        t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        if lib().orc_prefill(self._h, _i32(t), t.size):
+            raise ValueError("orc_prefill failed (cache full or empty prompt)")
+
+    def decode(self, n_steps: int, temperature: float = 0.0, top_k: int = 0, seed: int = 0,
+               force_tokens=None, want_logits: bool = True):
+        out = np.empty(n_steps, dtype=np.int32)
+        lg = np.empty((n_steps, self.cfg.vocab), dtype=np.float32) if want_logits else None
+        ft = None
+        if force_tokens is not None:
+            ft = np.ascontiguousarray(np.asarray(force_tokens, dtype=np.int32))
+            assert ft.size >= n_steps
+        rc = lib().orc_decode(self._h, n_steps, temperature, top_k, seed,
+                              _i32(ft) if ft is not None else None, _i32(out),
+                              _f32(lg) if want_logits else None)
+        if rc:
+            raise ValueError("orc_decode failed (no pending token or cache full)")
+        return out, lg

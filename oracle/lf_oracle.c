@@ -1,0 +1,418 @@
+/*
+ * lf_oracle.c -- plain, slow CPU reference of batch-1 decoder decode.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and the
+ * cpu_baseline / reference leg of bench.py may load or call this library.  It
+ * shares no code, header, table or constant generator with the CUDA library,
+ * and the CUDA library never calls it.
+ *
+ * What it computes follows the KOG monokernel write-up (shivam2003.com,
+ * "KOG LaneFormer-2B & the monokernel"):
+ *   - batch-1 decode, one token per step, FP16 weights streamed once per
+ *     token ("A worked bandwidth ceiling"; model table "Precision: FP16");
+ *   - GEMV partial products accumulated in FP32 ("The fused operations,
+ *     briefly", QKV-projection bullet);
+ *   - Gumbel-max sampling, argmax_i(logit_i + g_i) ("The fused operations,
+ *     briefly", sampling bullet);
+ * and, where those pages are silent, the plain Llama-style decoder that the
+ * workload definitions name: pre-norm RMSNorm blocks, rotate-half RoPE,
+ * causal GQA attention over an FP16 KV cache, SwiGLU FFN, final RMSNorm and an
+ * untied LM head.  Every reading taken where the pages are silent is listed in
+ * the repository's design notes.
+ *
+ * Precision: activations and every accumulation are IEEE FP32, each dot
+ * product summed left to right in index order; K and V are rounded to FP16
+ * (round to nearest even) when stored in the cache.  Build with
+ * -ffp-contract=off so that no multiply-add is fused and the result is the
+ * same on x86-64 and aarch64.  OpenMP only splits independent output rows or
+ * heads across threads; it does not change any sum.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORC_API __attribute__((visibility("default")))
+
+/* ------------------------------------------------------------------------ */
+/* IEEE binary16 <-> binary32, written from the IEEE 754 encoding.           */
+/* ------------------------------------------------------------------------ */
+
+ORC_API float orc_half_to_float(uint16_t h)
+{
+    uint32_t sign = (uint32_t)(h >> 15) & 1u;
+    uint32_t expo = (uint32_t)(h >> 10) & 0x1Fu;
+    uint32_t mant = (uint32_t)h & 0x3FFu;
+    float mag;
+    if (expo == 0) {
+        mag = ldexpf((float)mant, -24);                  /* subnormal: m * 2^-24 */
+    } else if (expo == 31) {
+        mag = mant ? NAN : INFINITY;
+    } else {
+        mag = ldexpf((float)(mant | 0x400u), (int)expo - 25);  /* (1024+m) * 2^(e-25) */
+    }
+    return sign ? -mag : mag;
+}
+
+/* Round a float to the nearest binary16, ties to even. */
+ORC_API uint16_t orc_float_to_half(float f)
+{
+    uint32_t bits;
+    memcpy(&bits, &f, 4);
+    uint16_t sign = (uint16_t)((bits >> 16) & 0x8000u);
+    if (isnan(f)) return (uint16_t)(sign | 0x7E00u);
+    float a = fabsf(f);
+    if (a >= 65520.0f) return (uint16_t)(sign | 0x7C00u);  /* rounds to infinity */
+    if (a < ldexpf(1.0f, -14)) {
+        /* subnormal range: quantum 2^-24; rint rounds half to even */
+        float q = rintf(ldexpf(a, 24));
+        return (uint16_t)(sign | (uint16_t)q);           /* q == 1024 gives the smallest normal */
+    }
+    int e;
+    frexpf(a, &e);                                       /* a = fr * 2^e, fr in [0.5, 1) */
+    /* a in [2^(e-1), 2^e); binary16 quantum there is 2^(e-1-10) */
+    float q = rintf(ldexpf(a, 11 - e));                  /* in [1024, 2048] */
+    int expo = e - 1 + 15;
+    uint32_t m = (uint32_t)q;
+    if (m == 2048u) { m = 1024u; expo += 1; }
+    if (expo >= 31) return (uint16_t)(sign | 0x7C00u);
+    return (uint16_t)(sign | (uint16_t)(expo << 10) | (uint16_t)(m - 1024u));
+}
+
+/* ------------------------------------------------------------------------ */
+/* Building blocks                                                           */
+/* ------------------------------------------------------------------------ */
+
+/* RMSNorm: out_i = x_i * (1 / sqrt(sum_j x_j^2 / d + eps)) * g_i. */
+ORC_API void orc_rmsnorm(const float *x, const uint16_t *g, int d, float eps, float *out)
+{
+    float ss = 0.0f;
+    for (int i = 0; i < d; ++i) ss += x[i] * x[i];
+    float inv = 1.0f / sqrtf(ss / (float)d + eps);
+    for (int i = 0; i < d; ++i) out[i] = (x[i] * inv) * orc_half_to_float(g[i]);
+}
+
+/* y_r = sum_k W[r, k] * x_k, W row-major FP16 [n_rows, k_dim], FP32 sum in index order. */
+ORC_API void orc_matvec(const uint16_t *W, const float *x, int n_rows, int k_dim, float *y)
+{
+    #pragma omp parallel for schedule(static)
+    for (int r = 0; r < n_rows; ++r) {
+        const uint16_t *row = W + (size_t)r * (size_t)k_dim;
+        float acc = 0.0f;
+        for (int k = 0; k < k_dim; ++k) acc += orc_half_to_float(row[k]) * x[k];
+        y[r] = acc;
+    }
+}
+
+/* Rotate-half RoPE of one head vector v[hd] at position pos:
+ * for i < hd/2, theta_i = pos * base^(-2i/hd) (in double), and
+ *   v[i]        <- v[i] cos - v[i+hd/2] sin
+ *   v[i+hd/2]   <- v[i+hd/2] cos + v[i] sin      (FP32 arithmetic). */
+ORC_API void orc_rope(float *v, int hd, int pos, float base)
+{
+    int half = hd / 2;
+    for (int i = 0; i < half; ++i) {
+        double inv_freq = pow((double)base, -2.0 * (double)i / (double)hd);
+        double ang = (double)pos * inv_freq;
+        float c = (float)cos(ang), s = (float)sin(ang);
+        float a = v[i], b = v[i + half];
+        v[i] = a * c - b * s;
+        v[i + half] = b * c + a * s;
+    }
+}
+
+/* Softmax-weighted sum for one query head over ctx cached positions:
+ *   s_j = (q . K_j) * scale,  p = softmax(s) (max subtracted),  o = sum_j p_j V_j.
+ * K, V: FP16 rows of hd values, row j at K + j*hd.  scores: scratch [ctx]. */
+ORC_API void orc_attend_head(const float *q, const uint16_t *K, const uint16_t *V, int ctx, int hd,
+                             float scale, float *scores, float *out)
+{
+    float m = -INFINITY;
+    for (int j = 0; j < ctx; ++j) {
+        const uint16_t *kj = K + (size_t)j * hd;
+        float dot = 0.0f;
+        for (int i = 0; i < hd; ++i) dot += q[i] * orc_half_to_float(kj[i]);
+        scores[j] = dot * scale;
+        if (scores[j] > m) m = scores[j];
+    }
+    float sum = 0.0f;
+    for (int j = 0; j < ctx; ++j) { scores[j] = expf(scores[j] - m); sum += scores[j]; }
+    for (int j = 0; j < ctx; ++j) scores[j] = scores[j] / sum;
+    for (int i = 0; i < hd; ++i) out[i] = 0.0f;
+    for (int j = 0; j < ctx; ++j) {
+        const uint16_t *vj = V + (size_t)j * hd;
+        for (int i = 0; i < hd; ++i) out[i] += scores[j] * orc_half_to_float(vj[i]);
+    }
+}
+
+/* SiLU(z) = z / (1 + e^-z). */
+ORC_API float orc_silu(float z) { return z / (1.0f + expf(-z)); }
+
+/* ------------------------------------------------------------------------ */
+/* Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As   */
+/* Easy as 1, 2, 3", SC'11): ten rounds of two 32x32->64 multiplies with     */
+/* Weyl key bumps between rounds.                                            */
+/* ------------------------------------------------------------------------ */
+
+#define ORC_PHILOX_M0 0xD2511F53u
+#define ORC_PHILOX_M1 0xCD9E8D57u
+#define ORC_PHILOX_W0 0x9E3779B9u
+#define ORC_PHILOX_W1 0xBB67AE85u
+
+ORC_API void orc_philox4x32_10(const uint32_t ctr_in[4], const uint32_t key_in[2], uint32_t out[4])
+{
+    uint32_t c0 = ctr_in[0], c1 = ctr_in[1], c2 = ctr_in[2], c3 = ctr_in[3];
+    uint32_t k0 = key_in[0], k1 = key_in[1];
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) { k0 += ORC_PHILOX_W0; k1 += ORC_PHILOX_W1; }
+        uint64_t p0 = (uint64_t)ORC_PHILOX_M0 * (uint64_t)c0;
+        uint64_t p1 = (uint64_t)ORC_PHILOX_M1 * (uint64_t)c2;
+        uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+        uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+        uint32_t n0 = hi1 ^ c1 ^ k0;
+        uint32_t n2 = hi0 ^ c3 ^ k1;
+        c0 = n0; c1 = lo1; c2 = n2; c3 = lo0;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* Gumbel noise for vocabulary entry i of the step at position pos:
+ *   r = word (i mod 4) of Philox4x32-10(counter = (i div 4, pos, 0, 0), key = seed),
+ *   u = (2 * (r >> 9) + 1) * 2^-24 in (0, 1)   (exact in FP32),
+ *   g = -log(-log(u)). */
+ORC_API float orc_gumbel(uint64_t seed, int pos, int i)
+{
+    uint32_t ctr[4] = {(uint32_t)i >> 2, (uint32_t)pos, 0u, 0u};
+    uint32_t key[2] = {(uint32_t)(seed & 0xFFFFFFFFu), (uint32_t)(seed >> 32)};
+    uint32_t r[4];
+    orc_philox4x32_10(ctr, key, r);
+    uint32_t w = r[i & 3];
+    float u = (float)((w >> 9) * 2u + 1u) * 0x1p-24f;
+    return -logf(-logf(u));
+}
+
+/* Order used for "largest logits": larger value first, equal values by lower index. */
+static const float *g_sort_logits;
+static int orc_cmp_desc(const void *a, const void *b)
+{
+    int ia = *(const int *)a, ib = *(const int *)b;
+    float va = g_sort_logits[ia], vb = g_sort_logits[ib];
+    if (va > vb) return -1;
+    if (va < vb) return 1;
+    return (ia < ib) ? -1 : (ia > ib);
+}
+
+/* Token choice for one step.
+ *   temperature <= 0 or top_k == 1: greedy argmax (lowest index among equal maxima).
+ *   otherwise: S = the top_k largest logits (top_k <= 0 or >= V: all of them);
+ *   token = argmax_{i in S} (logit_i / T + g_i), equal scores resolved to the lower index. */
+ORC_API int orc_sample(const float *logits, int V, float temperature, int top_k, uint64_t seed, int pos)
+{
+    if (temperature <= 0.0f || top_k == 1) {
+        int best = 0;
+        for (int i = 1; i < V; ++i) if (logits[i] > logits[best]) best = i;
+        return best;
+    }
+    int k = (top_k <= 0 || top_k >= V) ? V : top_k;
+    int *idx = (int *)malloc(sizeof(int) * (size_t)V);
+    for (int i = 0; i < V; ++i) idx[i] = i;
+    if (k < V) {
+        g_sort_logits = logits;
+        qsort(idx, (size_t)V, sizeof(int), orc_cmp_desc);
+    }
+    int tok = -1;
+    float best = -INFINITY;
+    for (int j = 0; j < k; ++j) {
+        int i = idx[j];
+        float score = logits[i] / temperature + orc_gumbel(seed, pos, i);
+        if (tok < 0 || score > best || (score == best && i < tok)) { best = score; tok = i; }
+    }
+    free(idx);
+    return tok;
+}
+
+/* ------------------------------------------------------------------------ */
+/* The decoder                                                               */
+/* ------------------------------------------------------------------------ */
+
+typedef struct {
+    int n_layers, d_model, n_heads, n_kv_heads, head_dim, ffn_dim, vocab, max_seq;
+    float rope_theta, rms_eps;
+} orc_config;
+
+typedef struct {
+    const uint16_t *embed;      /* [V, d] */
+    const uint16_t *attn_norm;  /* [L, d] */
+    const uint16_t *wq;         /* [L, Q, d] */
+    const uint16_t *wk;         /* [L, KV, d] */
+    const uint16_t *wv;         /* [L, KV, d] */
+    const uint16_t *wo;         /* [L, d, Q] */
+    const uint16_t *ffn_norm;   /* [L, d] */
+    const uint16_t *w_gate;     /* [L, F, d] */
+    const uint16_t *w_up;       /* [L, F, d] */
+    const uint16_t *w_down;     /* [L, d, F] */
+    const uint16_t *final_norm; /* [d] */
+    const uint16_t *lm_head;    /* [V, d] */
+} orc_weights;
+
+typedef struct {
+    orc_config c;
+    orc_weights w;
+    uint16_t *kcache;   /* [L][H_kv][max_seq][hd] FP16 */
+    uint16_t *vcache;
+    int pos;            /* position of the pending token */
+    int pending;        /* token fed to the next forward pass, -1 if none */
+    /* activations */
+    float *x, *xn, *q, *k, *v, *attn, *tmp, *gate, *up, *hbuf, *scores;
+} orc_model;
+
+ORC_API orc_model *orc_create(const orc_config *c, const orc_weights *w)
+{
+    if (!c || !w || c->n_heads % c->n_kv_heads != 0 || c->head_dim % 2 != 0) return NULL;
+    orc_model *m = (orc_model *)calloc(1, sizeof(orc_model));
+    m->c = *c;
+    m->w = *w;
+    size_t kv = (size_t)c->n_layers * c->n_kv_heads * (size_t)c->max_seq * c->head_dim;
+    m->kcache = (uint16_t *)calloc(kv, 2);
+    m->vcache = (uint16_t *)calloc(kv, 2);
+    int d = c->d_model, Q = c->n_heads * c->head_dim, KV = c->n_kv_heads * c->head_dim, F = c->ffn_dim;
+    m->x = (float *)calloc((size_t)d, 4);
+    m->xn = (float *)calloc((size_t)d, 4);
+    m->q = (float *)calloc((size_t)Q, 4);
+    m->k = (float *)calloc((size_t)KV, 4);
+    m->v = (float *)calloc((size_t)KV, 4);
+    m->attn = (float *)calloc((size_t)Q, 4);
+    m->tmp = (float *)calloc((size_t)(d > c->vocab ? d : c->vocab), 4);
+    m->gate = (float *)calloc((size_t)F, 4);
+    m->up = (float *)calloc((size_t)F, 4);
+    m->hbuf = (float *)calloc((size_t)F, 4);
+    m->scores = (float *)calloc((size_t)c->n_heads * (size_t)c->max_seq, 4);
+    if (!m->kcache || !m->vcache || !m->scores) { free(m); return NULL; }
+    m->pos = 0;
+    m->pending = -1;
+    return m;
+}
+
+ORC_API void orc_destroy(orc_model *m)
+{
+    if (!m) return;
+    free(m->kcache); free(m->vcache);
+    free(m->x); free(m->xn); free(m->q); free(m->k); free(m->v); free(m->attn);
+    free(m->tmp); free(m->gate); free(m->up); free(m->hbuf); free(m->scores);
+    free(m);
+}
+
+ORC_API void orc_reset(orc_model *m) { m->pos = 0; m->pending = -1; }
+ORC_API int orc_pos(const orc_model *m) { return m->pos; }
+ORC_API int orc_pending(const orc_model *m) { return m->pending; }
+ORC_API const uint16_t *orc_kcache(const orc_model *m) { return m->kcache; }
+ORC_API const uint16_t *orc_vcache(const orc_model *m) { return m->vcache; }
+
+ORC_API int orc_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* One forward pass of `token` at position m->pos.  Appends K and V of this
+ * position to the cache, writes the V logits if `logits` is not NULL, and
+ * advances the position.  Returns 0, or -1 if the cache is full. */
+ORC_API int orc_forward(orc_model *m, int token, float *logits)
+{
+    const orc_config *c = &m->c;
+    const orc_weights *w = &m->w;
+    int L = c->n_layers, d = c->d_model, Hq = c->n_heads, Hkv = c->n_kv_heads, hd = c->head_dim;
+    int F = c->ffn_dim, Q = Hq * hd, KV = Hkv * hd, group = Hq / Hkv;
+    int p = m->pos;
+    if (p >= c->max_seq || token < 0 || token >= c->vocab) return -1;
+    float scale = 1.0f / sqrtf((float)hd);
+
+    for (int i = 0; i < d; ++i) m->x[i] = orc_half_to_float(w->embed[(size_t)token * d + i]);
+
+    for (int l = 0; l < L; ++l) {
+        /* attention block */
+        orc_rmsnorm(m->x, w->attn_norm + (size_t)l * d, d, c->rms_eps, m->xn);
+        orc_matvec(w->wq + (size_t)l * Q * d, m->xn, Q, d, m->q);
+        orc_matvec(w->wk + (size_t)l * KV * d, m->xn, KV, d, m->k);
+        orc_matvec(w->wv + (size_t)l * KV * d, m->xn, KV, d, m->v);
+        for (int h = 0; h < Hq; ++h) orc_rope(m->q + h * hd, hd, p, c->rope_theta);
+        for (int g = 0; g < Hkv; ++g) orc_rope(m->k + g * hd, hd, p, c->rope_theta);
+        for (int g = 0; g < Hkv; ++g) {
+            size_t base = (((size_t)l * Hkv + g) * (size_t)c->max_seq + (size_t)p) * hd;
+            for (int i = 0; i < hd; ++i) {
+                m->kcache[base + i] = orc_float_to_half(m->k[g * hd + i]);
+                m->vcache[base + i] = orc_float_to_half(m->v[g * hd + i]);
+            }
+        }
+        #pragma omp parallel for schedule(static)
+        for (int h = 0; h < Hq; ++h) {
+            int g = h / group;
+            size_t base = ((size_t)l * Hkv + g) * (size_t)c->max_seq * hd;
+            orc_attend_head(m->q + h * hd, m->kcache + base, m->vcache + base, p + 1, hd, scale,
+                            m->scores + (size_t)h * c->max_seq, m->attn + h * hd);
+        }
+        orc_matvec(w->wo + (size_t)l * d * Q, m->attn, d, Q, m->tmp);
+        for (int i = 0; i < d; ++i) m->x[i] = m->x[i] + m->tmp[i];
+
+        /* FFN block */
+        orc_rmsnorm(m->x, w->ffn_norm + (size_t)l * d, d, c->rms_eps, m->xn);
+        orc_matvec(w->w_gate + (size_t)l * F * d, m->xn, F, d, m->gate);
+        orc_matvec(w->w_up + (size_t)l * F * d, m->xn, F, d, m->up);
+        for (int i = 0; i < F; ++i) m->hbuf[i] = orc_silu(m->gate[i]) * m->up[i];
+        orc_matvec(w->w_down + (size_t)l * d * F, m->hbuf, d, F, m->tmp);
+        for (int i = 0; i < d; ++i) m->x[i] = m->x[i] + m->tmp[i];
+    }
+    if (logits) {
+        orc_rmsnorm(m->x, w->final_norm, d, c->rms_eps, m->xn);
+        orc_matvec(w->lm_head, m->xn, c->vocab, d, logits);
+    }
+    m->pos = p + 1;
+    return 0;
+}
+
+/* Prefill: forward passes of tokens[0 .. n-2]; tokens[n-1] becomes the pending
+ * token.  Returns 0, or -1 on a bad argument or a full cache. */
+ORC_API int orc_prefill(orc_model *m, const int32_t *tokens, int n)
+{
+    /* positions used: the pending token (if any), tokens[0 .. n-2], and one
+     * more for tokens[n-1] when it is later decoded */
+    if (n < 1 || m->pos + (m->pending >= 0 ? 1 : 0) + n > m->c.max_seq) return -1;
+    if (m->pending >= 0) {
+        /* a pending token from an earlier call is consumed first */
+        if (orc_forward(m, m->pending, NULL)) return -1;
+    }
+    for (int i = 0; i < n - 1; ++i)
+        if (orc_forward(m, tokens[i], NULL)) return -1;
+    m->pending = tokens[n - 1];
+    return 0;
+}
+
+/* n_steps decode steps.  Step i runs the forward pass of the pending token at
+ * position pos, chooses a token from its logits (orc_sample, keyed by that
+ * position), writes it to out_tokens[i] and makes it the pending token -- or,
+ * if force_tokens is not NULL, makes force_tokens[i] the pending token
+ * instead (teacher forcing on a fixed input sequence).  If logits_out is not
+ * NULL, step i's logits go to logits_out[i * V ...].  Returns 0 or -1. */
+ORC_API int orc_decode(orc_model *m, int n_steps, float temperature, int top_k, uint64_t seed,
+                       const int32_t *force_tokens, int32_t *out_tokens, float *logits_out)
+{
+    int V = m->c.vocab;
+    if (m->pending < 0 || m->pos + n_steps > m->c.max_seq) return -1;
+    float *lg = logits_out ? NULL : (float *)malloc(sizeof(float) * (size_t)V);
+    for (int i = 0; i < n_steps; ++i) {
+        float *dst = logits_out ? logits_out + (size_t)i * V : lg;
+        int p = m->pos;
+        if (orc_forward(m, m->pending, dst)) { free(lg); return -1; }
+        int tok = orc_sample(dst, V, temperature, top_k, seed, p);
+        out_tokens[i] = tok;
+        m->pending = force_tokens ? force_tokens[i] : tok;
+    }
+    free(lg);
+    return 0;
+}

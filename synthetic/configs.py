@@ -1,0 +1,100 @@
+"""Workload shapes: Llama-style decoder-only transformers decoded at batch 1.
+
+The five workloads are the decode configurations this library is measured on:
+a tiny and a small decoder, a ~2.3B-parameter decoder at short and at 32k
+context, and an 8B-shaped decoder sampled at temperature 0.8 / top-k 50.
+The ~2.3B size is the one the KOG LaneFormer write-up (shivam2003.com,
+"A worked bandwidth ceiling") quotes: 2.3B FP16 parameters, 4.6 GB streamed
+per token.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, replace
+
+
+@dataclass(frozen=True)
+class ModelConfig:
+    name: str
+    n_layers: int
+    d_model: int
+    n_heads: int
+    n_kv_heads: int
+    head_dim: int
+    ffn_dim: int
+    vocab: int
+    rope_theta: float = 10000.0
+    rms_eps: float = 1e-5
+
+    @property
+    def q_dim(self) -> int:
+        return self.n_heads * self.head_dim
+
+    @property
+    def kv_dim(self) -> int:
+        return self.n_kv_heads * self.head_dim
+
+    def n_params(self) -> int:
+        L, d, F, V = self.n_layers, self.d_model, self.ffn_dim, self.vocab
+        per_layer = (self.q_dim + 2 * self.kv_dim) * d + d * self.q_dim + 3 * d * F + 2 * d
+        return V * d * 2 + L * per_layer + d
+
+    def weight_bytes_per_token(self) -> int:
+        """FP16 bytes every decode step must stream: all layer matrices and
+        norm gains, the final norm, the LM head and one embedding row."""
+        L, d, F, V = self.n_layers, self.d_model, self.ffn_dim, self.vocab
+        per_layer = (self.q_dim + 2 * self.kv_dim) * d + d * self.q_dim + 3 * d * F + 2 * d
+        return 2 * (L * per_layer + d + V * d + d)
+
+    def kv_bytes_per_position(self) -> int:
+        """FP16 K and V bytes of one cached position over all layers."""
+        return 2 * 2 * self.n_layers * self.kv_dim
+
+    def with_(self, **kw) -> "ModelConfig":
+        return replace(self, **kw)
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    model: ModelConfig
+    weight_seed: int
+    prompt_seed: int
+    prompt_len: int
+    decode_steps: int
+    temperature: float = 0.0
+    top_k: int = 0
+    sample_seed: int = 0
+
+    @property
+    def max_seq(self) -> int:
+        return self.prompt_len + self.decode_steps
+
+    def bytes_per_step(self, pos: int) -> int:
+        """Algorithmic HBM bytes of the decode step whose input token sits at
+        position `pos`: weights, the KV read over ctx = pos + 1 positions and
+        the KV write of one position."""
+        m = self.model
+        return m.weight_bytes_per_token() + (pos + 1) * m.kv_bytes_per_position() + m.kv_bytes_per_position()
+
+    def decode_bytes(self, first_pos: int, n_steps: int) -> int:
+        return sum(self.bytes_per_step(first_pos + i) for i in range(n_steps))
+
+
+MODELS = {
+    "tiny": ModelConfig("tiny", 2, 256, 4, 4, 64, 1024, 4096),
+    "small": ModelConfig("small", 16, 1024, 16, 4, 64, 4096, 32000),
+    "2.3b": ModelConfig("2.3b", 25, 2560, 20, 5, 128, 8192, 64000),
+    "8b": ModelConfig("8b", 32, 4096, 32, 8, 128, 14336, 128256),
+}
+
+WORKLOADS = {
+    "tiny": Workload("tiny", MODELS["tiny"], 0, 1000, 64, 32),
+    "small": Workload("small", MODELS["small"], 1, 1001, 128, 256),
+    "2.3b": Workload("2.3b", MODELS["2.3b"], 2, 1002, 512, 1024),
+    "2.3b-32k": Workload("2.3b-32k", MODELS["2.3b"], 2, 1003, 32768, 256),
+    "8b": Workload("8b", MODELS["8b"], 3, 1004, 2048, 512, temperature=0.8, top_k=50, sample_seed=1234),
+}
+
+
+def workload(name: str) -> Workload:
+    return WORKLOADS[name]

@@ -1,0 +1,140 @@
+"""Seeded FP16 weights and prompt ids, bit-identical on CPU and CUDA.
+
+Every weight is one entry of a fixed table of 65,536 FP16 values: the
+quantiles 0.02 * Phi^-1((k + 0.5) / 65536) of N(0, 0.02), each rounded to FP16.
+A counter-based integer hash of (seed, tensor, layer, element index) picks the
+entry.  Only integer operations and a gather are used, with every intermediate
+product below 2**63, so torch gives the same bits on the CPU and on a GPU.  The
+weights therefore follow N(0, 0.02) to within FP16 rounding.
+
+Tensor layouts are row-major, nn.Linear style ([out, in]), stacked over layers:
+  embed [V, d], attn_norm [L, d], wq [L, Q, d], wk [L, KV, d], wv [L, KV, d],
+  wo [L, d, Q], ffn_norm [L, d], w_gate [L, F, d], w_up [L, F, d],
+  w_down [L, d, F], final_norm [d], lm_head [V, d].
+"""
+from __future__ import annotations
+
+from statistics import NormalDist
+
+import torch
+
+from .configs import ModelConfig
+
+MASK32 = 0xFFFFFFFF
+# Odd multipliers below 2**31, so that a 32-bit value times one stays below 2**63.
+_C1 = 0x7FEB352D
+_C2 = 0x2C1B3C6D
+_C3 = 0x297A2D39
+_C4 = 0x5BD1E995 & 0x7FFFFFFF
+
+WEIGHT_ORDER = ("embed", "wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down", "lm_head",
+                "attn_norm", "ffn_norm", "final_norm")
+_TENSOR_ID = {name: i + 1 for i, name in enumerate(WEIGHT_ORDER)}
+
+_TABLE_CACHE: dict = {}
+
+
+def normal_table(std: float = 0.02) -> torch.Tensor:
+    """FP16 table of the 65,536 mid-quantiles of N(0, std)."""
+    key = float(std)
+    if key not in _TABLE_CACHE:
+        nd = NormalDist(0.0, 1.0)
+        vals = [std * nd.inv_cdf((k + 0.5) / 65536.0) for k in range(65536)]
+        _TABLE_CACHE[key] = torch.tensor(vals, dtype=torch.float64).to(torch.float16)
+    return _TABLE_CACHE[key]
+
+
+def _mix32(x: torch.Tensor) -> torch.Tensor:
+    """Integer avalanche mix of int64 tensors that hold 32-bit values."""
+    x = x ^ (x >> 16)
+    x = (x * _C1) & MASK32
+    x = x ^ (x >> 15)
+    x = (x * _C2) & MASK32
+    x = x ^ (x >> 16)
+    return x
+
+
+def _mix_scalar(x: int) -> int:
+    x &= MASK32
+    x ^= x >> 16
+    x = (x * _C1) & MASK32
+    x ^= x >> 15
+    x = (x * _C2) & MASK32
+    x ^= x >> 16
+    return x
+
+
+def _stream_key(seed: int, tensor_id: int, layer: int) -> tuple:
+    k1 = _mix_scalar((seed * _C3 + tensor_id) & MASK32)
+    k1 = _mix_scalar(k1 ^ ((layer * _C4) & MASK32))
+    k2 = _mix_scalar(k1 + 0x9E3779B9)
+    return k1, k2
+
+
+def hashed_indices(seed: int, tensor_id: int, layer: int, start: int, n: int, device) -> torch.Tensor:
+    """16-bit table indices for elements [start, start + n) of one stream."""
+    k1, k2 = _stream_key(seed, tensor_id, layer)
+    i = torch.arange(start, start + n, dtype=torch.int64, device=device)
+    h = _mix32((i & MASK32) ^ k1)
+    h = _mix32((h + k2) & MASK32)
+    return (h >> 16) & 0xFFFF
+
+
+_CHUNK = 1 << 20
+
+
+def _fill(out: torch.Tensor, table: torch.Tensor, seed: int, tensor_id: int, layer: int) -> None:
+    flat = out.view(-1)
+    n = flat.numel()
+    for s in range(0, n, _CHUNK):
+        m = min(_CHUNK, n - s)
+        idx = hashed_indices(seed, tensor_id, layer, s, m, flat.device)
+        flat[s:s + m] = table[idx]
+
+
+def make_weights(cfg: ModelConfig, seed: int, device="cpu", gains: str = "ones") -> dict:
+    """All FP16 tensors of one decoder.
+
+    gains="ones" gives RMSNorm gains of exactly 1.0 (the configured
+    workloads); gains="random" gives 1 + N(0, 0.1)-distributed gains, used by
+    tests to exercise the gain multiply.
+    """
+    device = torch.device(device)
+    table = normal_table(0.02).to(device)
+    L, d, F, V = cfg.n_layers, cfg.d_model, cfg.ffn_dim, cfg.vocab
+    Q, KV = cfg.q_dim, cfg.kv_dim
+    shapes = {
+        "embed": (V, d), "wq": (L, Q, d), "wk": (L, KV, d), "wv": (L, KV, d), "wo": (L, d, Q),
+        "w_gate": (L, F, d), "w_up": (L, F, d), "w_down": (L, d, F), "lm_head": (V, d),
+    }
+    w = {}
+    for name in WEIGHT_ORDER[:9]:
+        shp = shapes[name]
+        t = torch.empty(shp, dtype=torch.float16, device=device)
+        if len(shp) == 3:
+            for layer in range(shp[0]):
+                _fill(t[layer], table, seed, _TENSOR_ID[name], layer)
+        else:
+            _fill(t, table, seed, _TENSOR_ID[name], 0)
+        w[name] = t
+    norm_shapes = {"attn_norm": (L, d), "ffn_norm": (L, d), "final_norm": (d,)}
+    for name, shp in norm_shapes.items():
+        if gains == "ones":
+            w[name] = torch.ones(shp, dtype=torch.float16, device=device)
+        elif gains == "random":
+            t = torch.empty(shp, dtype=torch.float16, device=device)
+            _fill(t, table, seed, _TENSOR_ID[name], 0)
+            # 1 + 5 * N(0, 0.02) = 1 + N(0, 0.1), rounded to FP16
+            w[name] = (1.0 + 5.0 * t.to(torch.float32)).to(torch.float16)
+        else:
+            raise ValueError(f"gains must be 'ones' or 'random', not {gains!r}")
+    return w
+
+
+def make_prompt(vocab: int, n: int, seed: int, device="cpu") -> torch.Tensor:
+    """n token ids, uniform on [0, vocab) (up to a 2**-32 modulo bias), int32."""
+    k1, k2 = _stream_key(seed, 0x50524F4D, 0)  # tensor id "PROM"
+    i = torch.arange(n, dtype=torch.int64, device=device)
+    h = _mix32((i & MASK32) ^ k1)
+    h = _mix32((h + k2) & MASK32)
+    return (h % vocab).to(torch.int32)
