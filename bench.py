@@ -1,0 +1,412 @@
+#!/usr/bin/env python3
+"""Batch-1 decode benchmark: tokens/s and achieved HBM GB/s on one GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 2.3b] [--impl ours|reference]
+
+A step is one decode token: the whole per-token pass (embedding, every layer,
+LM head, sampling) over the workload's synthetic weights.  The timed region is
+ONE lf_decode launch of K steps that continues the workload's prompt, timed
+with CUDA events on the launching stream, bracketed by a barrier and a device
+synchronize on both sides.  The weights (4.3 GB for the ~2.3B workload) are far
+larger than the 129 MB L2, so every step streams them from HBM.
+
+Multi-GPU: replicas only.  Each rank decodes its own request on its own GPU
+(torchrun, one process per GPU); `value` is the tokens of all ranks divided by
+the slowest rank's time.
+
+--impl reference times the CPU oracle (oracle/, plain C, FP32) on the host
+cores instead, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "batch-1 decode tokens/s and achieved HBM GB/s (fraction of ~8 TB/s) at 1 GB300"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+KERNEL_SOURCES = ("persistent_monokernel_gb300/csrc/lf_kernel.cu", "persistent_monokernel_gb300/csrc/lf_internal.cuh",
+                  "persistent_monokernel_gb300/csrc/lf_ptx.cuh", "persistent_monokernel_gb300/csrc/lf_api.cu")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None, help="timed decode steps (default: the workload's)")
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="2.3b")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-ablations", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_traffic(workload: str):
+    """DRAM bytes per decode step from the committed ncu summary, if it was
+    taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        if rec.get("kernel_source_hash") != kernel_source_hash():
+            return None
+        return rec["per_step_bytes"].get(workload)
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+               "-f", self.path]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def gpu_uuid(torch, dev: int):
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def workload_desc(wl, K):
+    m = wl.model
+    samp = "greedy" if not wl.temperature > 0 else f"T={wl.temperature}, top-k {wl.top_k}, Philox seed {wl.sample_seed}"
+    return (f"{wl.name}: {m.n_layers} layers, d_model {m.d_model}, {m.n_heads}/{m.n_kv_heads} heads x {m.head_dim}, "
+            f"SwiGLU FFN {m.ffn_dim}, vocab {m.vocab}, FP16 weights ~N(0,0.02); prompt {wl.prompt_len}, "
+            f"{K} decode steps ({samp})")
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+
+def time_oracle(cfg, weights_cpu, prompt, budget_s: float, max_steps: int, warmup: int = 1):
+    """Decode steps of the CPU oracle after a short prompt; returns (tok/s, steps, seconds, threads)."""
+    import oracle
+    n_prompt = len(prompt)
+    cap = n_prompt + warmup + max_steps + 1
+    orc = oracle.OracleDecoder(cfg, weights_cpu, cap)
+    orc.prefill(prompt)
+    if warmup:
+        orc.decode(warmup, want_logits=False)
+    t0 = time.perf_counter()
+    orc.decode(1, want_logits=False)
+    one = time.perf_counter() - t0
+    n = int(max(1, min(max_steps - 1, budget_s / max(one, 1e-6) - 1)))
+    t0 = time.perf_counter()
+    orc.decode(n, want_logits=False)
+    dt = time.perf_counter() - t0
+    threads = oracle.num_threads()
+    orc.close()
+    return (n + 1) / (dt + one), n + 1, dt + one, threads
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args):
+    import torch
+
+    import persistent_monokernel_gb300 as pm
+    from persistent_monokernel_gb300 import build as pm_build
+    from synthetic import WORKLOADS, make_prompt, make_weights
+
+    world, rank, local = dist_setup()
+    if world != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if rank == 0:
+        pm_build.build()
+    if dist:
+        dist.barrier()
+
+    wl = WORKLOADS[args.workload]
+    cfg = wl.model
+    K = args.steps or wl.decode_steps
+    W = max(3, args.warmup)
+    max_seq = wl.prompt_len + max(K, W, 128)
+    weights = make_weights(cfg, wl.weight_seed, device="cuda")
+    prompt = make_prompt(cfg.vocab, wl.prompt_len, wl.prompt_seed).cuda()
+    dec = pm.Decoder(cfg, weights, max_seq)
+    info = dec.info()
+    stream = torch.cuda.current_stream()
+    samp = dict(temperature=wl.temperature, top_k=wl.top_k, seed=wl.sample_seed)
+
+    def barrier():
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def timed_decode(n_steps):
+        dec.reset()
+        dec.prefill(prompt)
+        out = torch.empty(n_steps, dtype=torch.int32, device="cuda")
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        dec.decode(n_steps, out=out, **samp)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        st = dec.sync()
+        if st != 0:
+            raise RuntimeError(f"device status {pm.error_string(st)}")
+        return e0.elapsed_time(e1) / 1e3
+
+    # ---- warm-up: W untimed steps from the same prompt
+    dec.prefill(prompt)
+    dec.decode(W, **samp)
+    if dec.sync() != 0:
+        raise RuntimeError("warm-up failed")
+
+    # ---- timed region
+    clocks = ClockSampler(gpu_uuid(torch, local))
+    clocks.start()
+    t = timed_decode(K)
+    clk = clocks.stop()
+    t_max = t
+    if dist:
+        tt = torch.tensor([t], device="cuda", dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t_max = float(tt.item())
+
+    peak, peak_kind = hbm_peak()
+    first_pos = wl.prompt_len - 1
+    bytes_launch = wl.decode_bytes(first_pos, K)
+    achieved = bytes_launch / t / 1e9
+    tok_s_rank = K / t
+    value = world * K / t_max
+
+    result = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "tok/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(t_max / K * 1e3, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "weights_dtype": "fp16",
+        "data": "synthetic: seeded FP16 weights ~N(0,0.02), seeded uniform prompt ids",
+        "config": {
+            "workload": workload_desc(wl, K),
+            "prompt_len": wl.prompt_len,
+            "decode_positions": [first_pos, first_pos + K - 1],
+            "parallelism": f"replicas x{world} (no sharding)",
+            "l2": f"inputs larger than L2: {cfg.weight_bytes_per_token() / 1e9:.2f} GB of weights streamed per step",
+            "schedule": "monokernel, per-dependency flags",
+            "grid": f"{info['n_ctas']} CTAs x {info['threads_per_cta']} threads, {info['smem_bytes']} B smem "
+                    f"({info['ring_bytes']} B weight ring)",
+        },
+        "hbm_gbs": round(achieved, 1),
+        "hbm_frac_of_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
+        "bytes_per_step": round(bytes_launch / K),
+        "gpu_launches": 1,
+    }
+    traffic_step = measured_traffic(args.workload)
+    result["roofline"] = {
+        "bound": "hbm",
+        "achieved": round(achieved, 1),
+        "peak": peak,
+        "unit": "GB/s",
+        "frac": round(achieved / peak, 4),
+        "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+        else "fallback 6.8 TB/s",
+        "traffic": round(traffic_step * K) if traffic_step else None,
+        "kernel": "lfk::lf_monokernel (one launch = all K steps)",
+    }
+    result["clocks"] = clk
+
+    if rank == 0 and world == 1 and not args.no_ablations:
+        n_ab = min(K, 64)
+        ab = {"steps": n_ab}
+        for name, sched in (("monokernel_flags", pm.SCHED_FLAGS), ("grid_barrier", pm.SCHED_GRID_BARRIER),
+                            ("multi_kernel", pm.SCHED_MULTI_KERNEL)):
+            dec.set_schedule(sched)
+            ab[name + "_tok_s"] = round(n_ab / timed_decode(n_ab), 2)
+        dec.set_schedule(pm.SCHED_FLAGS)
+        ab["launches_per_step_multi_kernel"] = 5 * cfg.n_layers + 1
+        result["ablations"] = ab
+
+    if not args.no_e2e:
+        import numpy as np
+        dec.reset()
+        host_prompt = make_prompt(cfg.vocab, wl.prompt_len, wl.prompt_seed).pin_memory()
+        barrier()
+        t0 = time.perf_counter()
+        out = dec.generate(host_prompt.numpy(), K, **samp)
+        t_e2e = time.perf_counter() - t0
+        assert out.shape == (K,) and np.all((out >= 0) & (out < cfg.vocab))
+        if dist:
+            tt = torch.tensor([t_e2e], device="cuda", dtype=torch.float64)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            t_e2e = float(tt.item())
+        result["e2e"] = {
+            "value": round(world * K / t_e2e, 2),
+            "unit": "tok/s",
+            "h2d_bytes_per_step": round(4 * wl.prompt_len / K, 3),
+            "d2h_bytes_per_step": 4,
+            "what": f"lf_generate with host buffers: prompt upload ({wl.prompt_len} ids), prefill of the prompt "
+                    f"(repeated decode steps), {K} decode steps, token download, synchronize",
+            "request_ms": round(t_e2e * 1e3, 3),
+        }
+
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        wc = {k: v.cpu() for k, v in weights.items()}
+        pr = make_prompt(cfg.vocab, 8, wl.prompt_seed).numpy()
+        tok_s, n, dt, threads = time_oracle(cfg, wc, pr, budget_s=15.0, max_steps=256)
+        result["cpu_baseline"] = {
+            "value": round(tok_s, 4),
+            "unit": "tok/s",
+            "cores": threads,
+            "kind": "oracle",
+            "sample": f"{n} greedy decode steps of the same decoder after an 8-token prompt "
+                      f"(context 8..{8 + n}; the GPU run decodes at context {wl.prompt_len}..{wl.prompt_len + K}), "
+                      f"{dt:.1f} s on {threads} OpenMP threads",
+        }
+        del wc
+
+    dec.close()
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ reference arm (the CPU oracle)
+
+def run_reference(args):
+    world, rank, local = dist_setup()
+    if rank != 0:
+        return
+    import torch
+
+    from synthetic import WORKLOADS, make_prompt, make_weights
+    import oracle
+
+    oracle.build()
+    wl = WORKLOADS[args.workload]
+    cfg = wl.model
+    K = args.steps or wl.decode_steps
+    W = max(3, args.warmup)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    wc = {k: v.cpu() for k, v in make_weights(cfg, wl.weight_seed, device=dev).items()}
+    pr = make_prompt(cfg.vocab, 8, wl.prompt_seed).numpy()
+    tok_s, n, dt, threads = time_oracle(cfg, wc, pr, budget_s=60.0, max_steps=K, warmup=min(W, 3))
+    sample = (f"{n} of the {K} requested decode steps of the same decoder after an 8-token prompt "
+              f"(context 8..{8 + n}), {dt:.1f} s on {threads} OpenMP threads; warm-up {min(W, 3)} steps")
+    print(json.dumps({
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(tok_s, 4),
+        "unit": "tok/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(dt / n * 1e3, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic: seeded FP16 weights ~N(0,0.02), seeded uniform prompt ids",
+        "config": {"workload": workload_desc(wl, K)},
+        "cpu_baseline": {"value": round(tok_s, 4), "unit": "tok/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(tok_s, 4), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

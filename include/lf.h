@@ -1,0 +1,222 @@
+/*
+ * lf.h -- C ABI of the batch-1 decode monokernel library (liblf.so).
+ *
+ * One handle holds one decoder (weights, FP16 KV cache, decode state) on one
+ * GPU.  The whole per-token pass -- embedding gather, RMSNorm, QKV GEMV, RoPE,
+ * KV append, attention over the cache, output projection, SwiGLU FFN, final
+ * norm, LM-head GEMV and sampling -- runs inside ONE persistent kernel per
+ * lf_decode / lf_prefill call, with no kernel launch and no host round trip
+ * between tokens.  This follows the "monokernel" of the KOG LaneFormer
+ * write-up (shivam2003.com, "KOG LaneFormer-2B & the monokernel", section
+ * "Pillar 3 -- the monokernel runtime": the kernel launches once and stays
+ * resident until the token is produced), extended here to n_steps tokens per
+ * launch.
+ *
+ * Conventions for every entry point:
+ *   - Pointers named *_dev are device pointers; *_host are host pointers.
+ *     The caller owns every buffer it passes.  Device buffers must stay
+ *     valid until the work queued on `stream` has finished.
+ *   - `stream` is a cudaStream_t passed as void*; NULL is the legacy default
+ *     stream.  Calls are asynchronous on it unless stated otherwise.
+ *   - A handle is single-threaded and single-stream: do not call into one
+ *     handle from two threads at once, or queue work for it on two streams.
+ *   - Every call returns an lf_status.  No entry point aborts the process,
+ *     throws, or traps on the device.  Errors found on the host are returned
+ *     at once and leave the handle unchanged.  An error found on the device
+ *     (a bounded wait that ran out) is latched in the handle: lf_sync
+ *     returns it, and every later call returns LF_ERR_STATE until lf_reset.
+ *   - All tensors are row-major.  Weight matrices use the nn.Linear layout
+ *     [out_features, in_features] and are FP16 (IEEE binary16).
+ */
+#ifndef LF_H
+#define LF_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define LF_API __attribute__((visibility("default")))
+#else
+#define LF_API
+#endif
+
+#define LF_ABI_VERSION 1
+#define LF_MAX_TOP_K 64          /* largest top_k that lf_decode accepts (besides 0) */
+
+typedef enum {
+    LF_OK = 0,
+    LF_ERR_INVALID_ARG = 1,      /* NULL pointer, bad size or shape */
+    LF_ERR_OUT_OF_MEMORY = 2,    /* a device or host allocation failed */
+    LF_ERR_CAPACITY = 3,         /* the request needs more than max_seq positions */
+    LF_ERR_NOT_RESIDENT = 4,     /* the persistent grid cannot be co-resident on this GPU */
+    LF_ERR_CUDA = 5,             /* a CUDA runtime call failed */
+    LF_ERR_TIMEOUT = 6,          /* a device-side wait ran past wait_timeout_ns (latched) */
+    LF_ERR_NOT_SUPPORTED = 7,    /* shape outside what the kernels handle (see lf_config) */
+    LF_ERR_STATE = 8             /* call not valid in the current state (no pending token, latched error) */
+} lf_status;
+
+/* Schedules: how the stages of the per-token pass wait for each other.
+ * LF_SCHED_FLAGS is the library's design; the other two are ablations that
+ * reproduce the overheads the monokernel write-up removes. */
+typedef enum {
+    /* One persistent launch; every stage waits only for the counters of the
+     * data it reads (per-dependency waits: stackfutures.com, "The
+     * Monokernel", "Targeted synchronization"). */
+    LF_SCHED_FLAGS = 0,
+    /* One persistent launch; a grid-wide arrival-counter barrier after every
+     * stage (the atomic-counter grid sync that shivam2003.com, "Cross-GPU
+     * synchronization without atomics", measured at 7.59-7.88 us). */
+    LF_SCHED_GRID_BARRIER = 1,
+    /* One kernel launch per stage and layer, on the stream (the generic
+     * stack of shivam2003.com, "Why standard frameworks leave the bandwidth
+     * on the table": one kernel per stage/layer). */
+    LF_SCHED_MULTI_KERNEL = 2
+} lf_schedule;
+
+/* Decoder shape.  Supported: head_dim 64 or 128; n_heads a multiple of
+ * n_kv_heads with n_heads / n_kv_heads <= 8; d_model, n_heads * head_dim and
+ * ffn_dim multiples of 256; vocab >= 1; max_seq >= 1. */
+typedef struct {
+    int32_t n_layers;
+    int32_t d_model;
+    int32_t n_heads;         /* query heads */
+    int32_t n_kv_heads;      /* key/value heads (GQA groups are contiguous: query head h uses KV head h / (n_heads / n_kv_heads)) */
+    int32_t head_dim;
+    int32_t ffn_dim;
+    int32_t vocab;
+    int32_t max_seq;         /* KV-cache capacity in positions */
+    float rope_theta;        /* RoPE base, e.g. 10000 */
+    float rms_eps;           /* RMSNorm epsilon, e.g. 1e-5 */
+    int64_t wait_timeout_ns; /* bound of every device-side wait; 0 selects 2e9 (2 s) */
+    int32_t n_ctas;          /* persistent grid size; 0 selects one CTA per SM (capped at d_model) */
+    int32_t fault_step;      /* test hook: -1 (off), or the decode step (within one lf_decode call)
+                                at which layer 0's QKV stage withholds its readiness signal, so
+                                that the consumers' bounded waits run out */
+} lf_config;
+
+/* Device pointers to the caller's FP16 weights (row-major, stacked over
+ * layers).  L = n_layers, d = d_model, Q = n_heads*head_dim,
+ * KV = n_kv_heads*head_dim, F = ffn_dim, V = vocab.
+ * lf_create copies the projection matrices and the LM head into a
+ * library-owned, per-CTA streaming layout; the caller may free those after
+ * lf_create returns.  embed and the three norm-gain tensors are read in
+ * place by every decode step and must outlive the handle. */
+typedef struct {
+    const void *embed;       /* [V, d]      read in place */
+    const void *attn_norm;   /* [L, d]      read in place */
+    const void *wq;          /* [L, Q, d]   copied */
+    const void *wk;          /* [L, KV, d]  copied */
+    const void *wv;          /* [L, KV, d]  copied */
+    const void *wo;          /* [L, d, Q]   copied */
+    const void *ffn_norm;    /* [L, d]      read in place */
+    const void *w_gate;      /* [L, F, d]   copied */
+    const void *w_up;        /* [L, F, d]   copied */
+    const void *w_down;      /* [L, d, F]   copied */
+    const void *final_norm;  /* [d]         read in place */
+    const void *lm_head;     /* [V, d]      copied (untied from embed) */
+} lf_weights;
+
+/* Token choice, after the Gumbel-max trick of shivam2003.com ("The fused
+ * operations, briefly", sampling: argmax_i(logit_i + g_i) samples the
+ * softmax without normalising):
+ *   temperature <= 0 or top_k == 1: greedy argmax (lowest index among equal maxima);
+ *   otherwise S = the top_k largest logits (all of them if top_k == 0; equal
+ *   logits ordered by lower index) and the token is
+ *   argmax_{i in S} (logit_i / temperature + g_i), equal scores to the lower index,
+ *   g_i = -log(-log(u_i)), u_i = (2 * (r_i >> 9) + 1) * 2^-24, r_i = word (i mod 4) of
+ *   Philox4x32-10(counter = (i / 4, p, 0, 0), key = (seed low 32, seed high 32)),
+ *   p = position of the token whose logits are sampled.
+ * top_k must be 0 or in [1, LF_MAX_TOP_K]. */
+typedef struct {
+    float temperature;
+    int32_t top_k;
+    float *debug_logits_dev;          /* NULL, or [n_steps, V] FP32: every step's logits */
+    const int32_t *force_tokens_dev;  /* NULL, or [n_steps]: step i feeds force_tokens[i] to step
+                                         i+1 instead of its own choice (the choice is still
+                                         written to out_tokens); teacher forcing for tests */
+} lf_sampling;
+
+typedef struct lf_handle lf_handle;
+
+typedef struct {
+    int32_t n_ctas;              /* persistent grid size */
+    int32_t threads_per_cta;
+    int32_t smem_bytes;          /* dynamic shared memory per CTA */
+    int32_t ring_bytes;          /* weight-ring bytes per CTA */
+    int32_t sm_count;
+    int32_t position;            /* position of the pending token (tokens decoded or prefilled so far) */
+    int32_t has_pending;         /* 1 if a pending token is set */
+    int32_t schedule;            /* current lf_schedule */
+    int64_t weight_stream_bytes; /* bytes of the library's repacked weight copy */
+    int64_t kv_cache_bytes;      /* bytes of the FP16 K and V caches */
+} lf_info;
+
+/* Validate cfg, allocate the KV cache, activations, counters and the
+ * repacked weight copy on the current device, build the RoPE table and the
+ * static work partition, and check that the persistent grid fits.  Runs one
+ * repack kernel on the legacy default stream and synchronizes.  On success
+ * *out receives a handle with no pending token at position 0.
+ * Errors: INVALID_ARG (NULL, non-positive sizes), NOT_SUPPORTED (shape),
+ * OUT_OF_MEMORY, NOT_RESIDENT, CUDA. */
+LF_API lf_status lf_create(const lf_config *cfg, const lf_weights *weights, lf_handle **out);
+
+/* Release every library-owned allocation.  Synchronizes the device first.
+ * Accepts NULL. */
+LF_API void lf_destroy(lf_handle *h);
+
+/* Prefill, implemented as repeated decode steps in one persistent launch:
+ * runs the forward pass of the pending token (if any) and of
+ * tokens_dev[0 .. n-2] at consecutive positions, appending their K and V to
+ * the cache, and makes tokens_dev[n-1] the pending token.  No logits are
+ * computed.  tokens_dev: device int32 [n], each in [0, vocab).
+ * Errors: INVALID_ARG (n < 1, NULL), CAPACITY (not enough positions left for
+ * these tokens plus the pending one), STATE (latched device error). */
+LF_API lf_status lf_prefill(lf_handle *h, const int32_t *tokens_dev, int32_t n, void *stream);
+
+/* n_steps decode steps in one persistent launch.  Step i runs the forward
+ * pass of the pending token at the current position, chooses a token from
+ * its logits (lf_sampling), writes it to out_tokens_dev[i] (device int32
+ * [n_steps]) and makes it the pending token.  The position advances by
+ * n_steps.  Errors: INVALID_ARG, NOT_SUPPORTED (top_k), CAPACITY (position +
+ * n_steps > max_seq), STATE (no pending token, or latched device error). */
+LF_API lf_status lf_decode(lf_handle *h, int32_t n_steps, const lf_sampling *sp, uint64_t seed,
+                    int32_t *out_tokens_dev, void *stream);
+
+/* Host-buffer convenience: copies prompt_host[0 .. n_prompt-1] to the device,
+ * prefills it, decodes n_steps tokens and copies them to out_host, then
+ * synchronizes `stream` and returns the device status.  Uses library-owned
+ * staging buffers; both host buffers may be pageable or pinned. */
+LF_API lf_status lf_generate(lf_handle *h, const int32_t *prompt_host, int32_t n_prompt, int32_t n_steps,
+                      const lf_sampling *sp, uint64_t seed, int32_t *out_host, void *stream);
+
+/* Synchronize the stream of the last call and return the latched device
+ * status: LF_OK; LF_ERR_TIMEOUT if a bounded wait ran out; LF_ERR_INVALID_ARG
+ * if a token id fed to a forward pass was outside [0, vocab) (the kernel
+ * substituted 0 for it and stopped). */
+LF_API lf_status lf_sync(lf_handle *h);
+
+/* Forget the sequence: position 0, no pending token, counters and the
+ * latched device error cleared.  Synchronizes the device. */
+LF_API lf_status lf_reset(lf_handle *h);
+
+/* Select the schedule used by later lf_prefill / lf_decode calls. */
+LF_API lf_status lf_set_schedule(lf_handle *h, int32_t schedule);
+
+/* Fill *out with the handle's launch geometry and state. */
+LF_API lf_status lf_get_info(const lf_handle *h, lf_info *out);
+
+/* Static string naming a status code. */
+LF_API const char *lf_error_string(lf_status s);
+
+/* LF_ABI_VERSION of the built library. */
+LF_API int32_t lf_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LF_H */

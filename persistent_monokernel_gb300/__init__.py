@@ -1,0 +1,199 @@
+"""Python binding of liblf.so, the batch-1 decode monokernel (include/lf.h).
+
+The binding marshals arguments only: every step of the decode pass runs in the
+CUDA library.  PyTorch provides the device memory and the streams.  Importing
+this module loads the in-tree liblf.so and fails loudly if it is missing (build
+it with `python -m persistent_monokernel_gb300.build`); there is no CPU path.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "liblf.so")
+
+LF_OK = 0
+STATUS_NAMES = {0: "LF_OK", 1: "LF_ERR_INVALID_ARG", 2: "LF_ERR_OUT_OF_MEMORY", 3: "LF_ERR_CAPACITY",
+                4: "LF_ERR_NOT_RESIDENT", 5: "LF_ERR_CUDA", 6: "LF_ERR_TIMEOUT", 7: "LF_ERR_NOT_SUPPORTED",
+                8: "LF_ERR_STATE"}
+SCHED_FLAGS, SCHED_GRID_BARRIER, SCHED_MULTI_KERNEL = 0, 1, 2
+MAX_TOP_K = 64
+
+# Every symbol include/lf.h declares.
+EXPORTS = ("lf_create", "lf_destroy", "lf_prefill", "lf_decode", "lf_generate", "lf_sync", "lf_reset",
+           "lf_set_schedule", "lf_get_info", "lf_error_string", "lf_abi_version")
+
+
+class LFError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
+
+
+class lf_config(C.Structure):
+    _fields_ = [("n_layers", C.c_int32), ("d_model", C.c_int32), ("n_heads", C.c_int32),
+                ("n_kv_heads", C.c_int32), ("head_dim", C.c_int32), ("ffn_dim", C.c_int32), ("vocab", C.c_int32),
+                ("max_seq", C.c_int32), ("rope_theta", C.c_float), ("rms_eps", C.c_float),
+                ("wait_timeout_ns", C.c_int64), ("n_ctas", C.c_int32), ("fault_step", C.c_int32)]
+
+
+WEIGHT_FIELDS = ("embed", "attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down",
+                 "final_norm", "lm_head")
+
+
+class lf_weights(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in WEIGHT_FIELDS]
+
+
+class lf_sampling(C.Structure):
+    _fields_ = [("temperature", C.c_float), ("top_k", C.c_int32), ("debug_logits_dev", C.c_void_p),
+                ("force_tokens_dev", C.c_void_p)]
+
+
+class lf_info(C.Structure):
+    _fields_ = [("n_ctas", C.c_int32), ("threads_per_cta", C.c_int32), ("smem_bytes", C.c_int32),
+                ("ring_bytes", C.c_int32), ("sm_count", C.c_int32), ("position", C.c_int32),
+                ("has_pending", C.c_int32), ("schedule", C.c_int32), ("weight_stream_bytes", C.c_int64),
+                ("kv_cache_bytes", C.c_int64)]
+
+
+_lib = None
+
+
+def lib() -> C.CDLL:
+    """Load liblf.so (raises OSError if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise OSError(f"{LIB_PATH} is missing: build it with `python -m persistent_monokernel_gb300.build`")
+        L = C.CDLL(LIB_PATH)
+        vp = C.c_void_p
+        L.lf_create.argtypes = [C.POINTER(lf_config), C.POINTER(lf_weights), C.POINTER(vp)]
+        L.lf_destroy.argtypes = [vp]
+        L.lf_destroy.restype = None
+        L.lf_prefill.argtypes = [vp, vp, C.c_int32, vp]
+        L.lf_decode.argtypes = [vp, C.c_int32, C.POINTER(lf_sampling), C.c_uint64, vp, vp]
+        L.lf_generate.argtypes = [vp, C.POINTER(C.c_int32), C.c_int32, C.c_int32, C.POINTER(lf_sampling),
+                                  C.c_uint64, C.POINTER(C.c_int32), vp]
+        L.lf_sync.argtypes = [vp]
+        L.lf_reset.argtypes = [vp]
+        L.lf_set_schedule.argtypes = [vp, C.c_int32]
+        L.lf_get_info.argtypes = [vp, C.POINTER(lf_info)]
+        L.lf_error_string.argtypes = [C.c_int]
+        L.lf_error_string.restype = C.c_char_p
+        L.lf_abi_version.restype = C.c_int32
+        for name in ("lf_create", "lf_prefill", "lf_decode", "lf_generate", "lf_sync", "lf_reset",
+                     "lf_set_schedule", "lf_get_info"):
+            getattr(L, name).restype = C.c_int
+        _lib = L
+    return _lib
+
+
+def _check(status: int, where: str) -> None:
+    if status != LF_OK:
+        raise LFError(status, where)
+
+
+def _stream_ptr(stream) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _dptr(t) -> int:
+    return 0 if t is None else int(t.data_ptr())
+
+
+class Decoder:
+    """One decoder on the current CUDA device.
+
+    `model` is any object with the attributes n_layers, d_model, n_heads,
+    n_kv_heads, head_dim, ffn_dim, vocab, rope_theta and rms_eps; `weights`
+    maps the lf_weights field names to contiguous CUDA float16 tensors.
+    """
+
+    def __init__(self, model, weights: dict, max_seq: int, n_ctas: int = 0, wait_timeout_ns: int = 0,
+                 fault_step: int = -1):
+        import torch
+        self.model = model
+        self.max_seq = int(max_seq)
+        for n in WEIGHT_FIELDS:
+            t = weights[n]
+            if not (t.is_cuda and t.dtype == torch.float16 and t.is_contiguous()):
+                raise ValueError(f"weight {n} must be a contiguous CUDA float16 tensor")
+        # embed and the norm gains are read in place by every step: keep them alive
+        self._keep = {n: weights[n] for n in ("embed", "attn_norm", "ffn_norm", "final_norm")}
+        cfg = lf_config(model.n_layers, model.d_model, model.n_heads, model.n_kv_heads, model.head_dim,
+                        model.ffn_dim, model.vocab, self.max_seq, model.rope_theta, model.rms_eps,
+                        int(wait_timeout_ns), int(n_ctas), int(fault_step))
+        w = lf_weights(*[_dptr(weights[n]) for n in WEIGHT_FIELDS])
+        h = C.c_void_p()
+        _check(lib().lf_create(C.byref(cfg), C.byref(w), C.byref(h)), "lf_create")
+        self._h = h
+
+    # ---- lifetime
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            lib().lf_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        self.close()
+
+    # ---- calls
+    def prefill(self, tokens, stream=None) -> None:
+        import torch
+        assert tokens.is_cuda and tokens.dtype == torch.int32 and tokens.is_contiguous()
+        _check(lib().lf_prefill(self._h, _dptr(tokens), tokens.numel(), _stream_ptr(stream)), "lf_prefill")
+
+    def decode(self, n_steps: int, temperature: float = 0.0, top_k: int = 0, seed: int = 0, out=None,
+               debug_logits=None, force_tokens=None, stream=None):
+        import torch
+        if out is None:
+            out = torch.empty(n_steps, dtype=torch.int32, device="cuda")
+        sp = lf_sampling(float(temperature), int(top_k), _dptr(debug_logits), _dptr(force_tokens))
+        _check(lib().lf_decode(self._h, int(n_steps), C.byref(sp), int(seed) & (2 ** 64 - 1), _dptr(out),
+                               _stream_ptr(stream)), "lf_decode")
+        return out
+
+    def generate(self, prompt_host, n_steps: int, temperature: float = 0.0, top_k: int = 0, seed: int = 0,
+                 stream=None):
+        """Host buffers in and out (lf_generate): returns a numpy int32 array."""
+        import numpy as np
+        p = np.ascontiguousarray(np.asarray(prompt_host, dtype=np.int32))
+        out = np.empty(n_steps, dtype=np.int32)
+        sp = lf_sampling(float(temperature), int(top_k), 0, 0)
+        _check(lib().lf_generate(self._h, p.ctypes.data_as(C.POINTER(C.c_int32)), p.size, int(n_steps),
+                                 C.byref(sp), int(seed) & (2 ** 64 - 1), out.ctypes.data_as(C.POINTER(C.c_int32)),
+                                 _stream_ptr(stream)), "lf_generate")
+        return out
+
+    def sync(self) -> int:
+        """lf_sync: returns the status code (0, or 6 for a device timeout)."""
+        return int(lib().lf_sync(self._h))
+
+    def reset(self) -> None:
+        _check(lib().lf_reset(self._h), "lf_reset")
+
+    def set_schedule(self, schedule: int) -> None:
+        _check(lib().lf_set_schedule(self._h, int(schedule)), "lf_set_schedule")
+
+    def info(self) -> dict:
+        i = lf_info()
+        _check(lib().lf_get_info(self._h, C.byref(i)), "lf_get_info")
+        return {f: getattr(i, f) for f, _ in lf_info._fields_}
+
+
+def error_string(status: int) -> str:
+    return lib().lf_error_string(int(status)).decode()

@@ -1,0 +1,542 @@
+// lf_api.cu -- host runtime behind include/lf.h: validation, the static work
+// partition, allocation, the repack of the weights into per-CTA streams, the
+// RoPE table, and the launches of the persistent kernel.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/lf.h"
+#include "lf_internal.cuh"
+
+extern "C" cudaError_t lfk_set_smem(int smem_bytes);
+extern "C" cudaError_t lfk_launch_monokernel(const lfk::Params *p, int smem_bytes, cudaStream_t stream,
+                                             int cooperative);
+extern "C" cudaError_t lfk_occupancy(int smem_bytes, int *blocks_per_sm);
+extern "C" unsigned lfk_smem_bytes(int ring_bytes, int act_floats, int lm_rows_max);
+extern "C" cudaError_t lfk_launch_repack(lfk::Geo g, int P, const lfk::CtaPlan *plans, const void *wq,
+                                         const void *wk, const void *wv, const void *wo, const void *wg,
+                                         const void *wu, const void *wd, const void *head, void *dst,
+                                         cudaStream_t stream);
+
+namespace {
+
+constexpr int kAttnMinLen = 32;         // fewest positions per split-KV piece
+constexpr long long kDefaultTimeoutNs = 2000000000LL;
+
+}  // namespace
+
+struct lf_handle {
+    lf_config cfg;
+    lfk::Geo g;
+    int P = 0, sm_count = 0;
+    std::vector<lfk::CtaPlan> plans;
+    lfk::CtaPlan *d_plans = nullptr;
+    uint8_t *wstream = nullptr;
+    size_t wstream_bytes = 0;
+    const __half *embed = nullptr, *attn_norm = nullptr, *ffn_norm = nullptr, *final_norm = nullptr;
+    __half *kc = nullptr, *vc = nullptr;
+    float2 *rope = nullptr;
+    float *qbuf = nullptr, *attn = nullptr, *xattn = nullptr, *hbuf = nullptr, *xout = nullptr, *apart = nullptr;
+    int max_split = 1;
+    unsigned *counters = nullptr;  // one allocation: layer counters, attn_done, lm_done, tok_cnt, gbar
+    size_t counters_bytes = 0;
+    unsigned *cnt = nullptr, *attn_done = nullptr, *lm_done = nullptr, *tok_cnt = nullptr, *gbar = nullptr;
+    unsigned n_prod[4] = {0, 0, 0, 0};
+    unsigned long long *lm_part = nullptr;
+    int *tok_buf = nullptr, *tok_seq = nullptr;
+    unsigned *status = nullptr, *abort_flag = nullptr;
+    int ring_bytes = 0, act_floats = 0, lm_rows_max = 0, smem_bytes = 0;
+    // sequence state
+    int pos = 0;
+    int has_pending = 0;
+    unsigned epoch = 0, tok_count = 0, gbar_count = 0;
+    int sched = LF_SCHED_FLAGS;
+    lf_status latched = LF_OK;
+    cudaStream_t last_stream = nullptr;
+    // lf_generate staging
+    int32_t *stage_in = nullptr, *stage_out = nullptr;
+    int stage_cap = 0;
+};
+
+namespace {
+
+template <class T>
+cudaError_t dalloc(T **p, size_t count)
+{
+    return cudaMalloc(reinterpret_cast<void **>(p), std::max<size_t>(count, 1) * sizeof(T));
+}
+
+void free_all(lf_handle *h)
+{
+    void *ptrs[] = {h->d_plans, h->wstream, h->kc, h->vc, h->rope, h->qbuf, h->attn, h->xattn, h->hbuf,
+                    h->xout, h->apart, h->counters, h->lm_part, h->tok_buf, h->tok_seq, h->status,
+                    h->stage_in, h->stage_out};
+    for (void *p : ptrs)
+        if (p) cudaFree(p);
+}
+
+lf_status from_cuda(cudaError_t e)
+{
+    if (e == cudaSuccess) return LF_OK;
+    if (e == cudaErrorMemoryAllocation) return LF_ERR_OUT_OF_MEMORY;
+    if (e == cudaErrorCooperativeLaunchTooLarge) return LF_ERR_NOT_RESIDENT;
+    return LF_ERR_CUDA;
+}
+
+lf_status validate_config(const lf_config &c)
+{
+    if (c.n_layers <= 0 || c.d_model <= 0 || c.n_heads <= 0 || c.n_kv_heads <= 0 || c.head_dim <= 0 ||
+        c.ffn_dim <= 0 || c.vocab <= 0 || c.max_seq <= 0 || !(c.rms_eps >= 0.f) || !(c.rope_theta > 0.f) ||
+        c.n_ctas < 0 || c.wait_timeout_ns < 0)
+        return LF_ERR_INVALID_ARG;
+    if (c.head_dim != 64 && c.head_dim != 128) return LF_ERR_NOT_SUPPORTED;
+    if (c.n_heads % c.n_kv_heads != 0 || c.n_heads / c.n_kv_heads > lfk::MAX_GROUP) return LF_ERR_NOT_SUPPORTED;
+    const long long Q = (long long)c.n_heads * c.head_dim;
+    if (c.d_model % lfk::KC || Q % lfk::KC || c.ffn_dim % lfk::KC) return LF_ERR_NOT_SUPPORTED;
+    return LF_OK;
+}
+
+// Attention scratch (floats) inside the activation region: q of a group,
+// scores and probabilities of one sub-block, three per-head vectors and the
+// staged fresh K/V row.
+int attn_scratch_floats(const lfk::Geo &g)
+{
+    const int S = lfk::attn_sub_positions(g.hd);
+    return g.group * g.hd + 2 * g.group * S + 3 * lfk::MAX_GROUP + g.hd;
+}
+
+lf_status launch(lf_handle *h, const lfk::Params &p, cudaStream_t stream)
+{
+    const int coop = (p.sched == lfk::SCHED_MULTI) ? 0 : 1;
+    cudaError_t e = lfk_launch_monokernel(&p, h->smem_bytes, stream, coop);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return from_cuda(e);
+    }
+    return LF_OK;
+}
+
+lfk::Params base_params(lf_handle *h)
+{
+    lfk::Params p;
+    std::memset(&p, 0, sizeof(p));
+    p.g = h->g;
+    p.P = h->P;
+    p.eps = h->cfg.rms_eps;
+    p.plans = h->d_plans;
+    p.wstream = h->wstream;
+    p.embed = h->embed;
+    p.attn_norm = h->attn_norm;
+    p.ffn_norm = h->ffn_norm;
+    p.final_norm = h->final_norm;
+    p.kc = h->kc;
+    p.vc = h->vc;
+    p.rope = h->rope;
+    p.qbuf = h->qbuf;
+    p.attn = h->attn;
+    p.xattn = h->xattn;
+    p.hbuf = h->hbuf;
+    p.xout = h->xout;
+    p.apart = h->apart;
+    p.max_split = h->max_split;
+    p.cnt = h->cnt;
+    p.attn_done = h->attn_done;
+    p.lm_done = h->lm_done;
+    p.tok_cnt = h->tok_cnt;
+    p.gbar = h->gbar;
+    for (int i = 0; i < 4; ++i) p.n_prod[i] = h->n_prod[i];
+    p.lm_part = h->lm_part;
+    p.tok_buf = h->tok_buf;
+    p.tok_seq = h->tok_seq;
+    p.status = h->status;
+    p.abort_flag = h->abort_flag;
+    p.timeout_ns = h->cfg.wait_timeout_ns > 0 ? h->cfg.wait_timeout_ns : kDefaultTimeoutNs;
+    p.fault_step = h->cfg.fault_step;
+    p.ring_bytes = h->ring_bytes;
+    p.act_floats = h->act_floats;
+    p.lm_rows_max = h->lm_rows_max;
+    p.attn_min_len = kAttnMinLen;
+    p.sched = h->sched;
+    p.only_layer = -1;
+    p.only_stage = -1;
+    return p;
+}
+
+// Runs the steps of one prefill or decode call under the current schedule.
+lf_status run_steps(lf_handle *h, lfk::Params p, cudaStream_t stream)
+{
+    if (p.sched != lfk::SCHED_MULTI) return launch(h, p, stream);
+    // multi-kernel ablation: one launch per (step, layer, stage) + one for the LM head
+    const int L = h->g.L;
+    const int n = p.n_steps;
+    for (int i = 0; i < n; ++i) {
+        lfk::Params q = p;
+        q.n_steps = 1;
+        q.pos0 = p.pos0 + i;
+        q.epoch0 = p.epoch0 + (unsigned)i;
+        q.tok_base = p.tok_base + (unsigned)i;
+        q.fault_step = -1;
+        if (p.mode == lfk::MODE_PREFILL) {
+            q.has_pending = (p.has_pending && i == 0) ? 1 : 0;
+            q.prompt = p.prompt + (i - (p.has_pending ? 1 : 0));
+            if (q.has_pending) q.prompt = p.prompt;
+        } else {
+            q.out_tokens = p.out_tokens + i;
+            q.debug_logits = p.debug_logits ? p.debug_logits + (size_t)i * h->g.V : nullptr;
+            q.force_tokens = p.force_tokens ? p.force_tokens + i : nullptr;
+        }
+        for (int l = 0; l < L; ++l) {
+            for (int s = 0; s < 5; ++s) {
+                q.only_layer = l;
+                q.only_stage = s;
+                lf_status st = launch(h, q, stream);
+                if (st != LF_OK) return st;
+            }
+        }
+        if (p.mode == lfk::MODE_DECODE) {
+            q.only_layer = 0;
+            q.only_stage = 5;
+            lf_status st = launch(h, q, stream);
+            if (st != LF_OK) return st;
+        }
+    }
+    return LF_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t lf_abi_version(void) { return LF_ABI_VERSION; }
+
+const char *lf_error_string(lf_status s)
+{
+    switch (s) {
+    case LF_OK: return "LF_OK";
+    case LF_ERR_INVALID_ARG: return "LF_ERR_INVALID_ARG: invalid argument";
+    case LF_ERR_OUT_OF_MEMORY: return "LF_ERR_OUT_OF_MEMORY: allocation failed";
+    case LF_ERR_CAPACITY: return "LF_ERR_CAPACITY: not enough KV-cache positions left";
+    case LF_ERR_NOT_RESIDENT: return "LF_ERR_NOT_RESIDENT: the persistent grid cannot be co-resident";
+    case LF_ERR_CUDA: return "LF_ERR_CUDA: a CUDA runtime call failed";
+    case LF_ERR_TIMEOUT: return "LF_ERR_TIMEOUT: a device-side wait ran out";
+    case LF_ERR_NOT_SUPPORTED: return "LF_ERR_NOT_SUPPORTED: shape or option not supported";
+    case LF_ERR_STATE: return "LF_ERR_STATE: call not valid in the current state";
+    }
+    return "unknown lf_status";
+}
+
+lf_status lf_create(const lf_config *cfg, const lf_weights *w, lf_handle **out)
+{
+    if (!cfg || !w || !out) return LF_ERR_INVALID_ARG;
+    *out = nullptr;
+    lf_status st = validate_config(*cfg);
+    if (st != LF_OK) return st;
+    const void *need[] = {w->embed, w->attn_norm, w->wq, w->wk, w->wv, w->wo, w->ffn_norm,
+                          w->w_gate, w->w_up, w->w_down, w->final_norm, w->lm_head};
+    for (const void *p : need)
+        if (!p) return LF_ERR_INVALID_ARG;
+
+    lf_handle *h = new (std::nothrow) lf_handle();
+    if (!h) return LF_ERR_OUT_OF_MEMORY;
+    h->cfg = *cfg;
+    lfk::Geo &g = h->g;
+    g.L = cfg->n_layers;
+    g.d = cfg->d_model;
+    g.Hq = cfg->n_heads;
+    g.Hkv = cfg->n_kv_heads;
+    g.hd = cfg->head_dim;
+    g.F = cfg->ffn_dim;
+    g.V = cfg->vocab;
+    g.Q = g.Hq * g.hd;
+    g.KV = g.Hkv * g.hd;
+    g.group = g.Hq / g.Hkv;
+    g.max_seq = cfg->max_seq;
+
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, dev);
+    int optin = 0;
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) {
+        delete h;
+        return from_cuda(e);
+    }
+
+    // ---- grid size: one CTA per SM, and every CTA owns rows of every GEMV stage
+    int P = cfg->n_ctas > 0 ? std::min(cfg->n_ctas, h->sm_count) : h->sm_count;
+    for (int s = 0; s < lfk::N_GEMV; ++s) P = std::min(P, lfk::stage_geom(g, s).units);
+    h->P = P;
+
+    // ---- static partition and per-CTA stream offsets
+    h->plans.resize(P);
+    unsigned long long base = 0;
+    int lm_rows_max = 0;
+    for (int b = 0; b < P; ++b) {
+        lfk::CtaPlan &pl = h->plans[b];
+        for (int s = 0; s < lfk::N_GEMV; ++s) {
+            const int U = lfk::stage_geom(g, s).units;
+            pl.u0[s] = lfk::cta_unit_start(U, P, b);
+            pl.u1[s] = lfk::cta_unit_start(U, P, b + 1);
+        }
+        unsigned long long off = 0;
+        for (int s = 0; s < 4; ++s) {
+            const lfk::StageGeom sg = lfk::stage_geom(g, s);
+            pl.stage_off[s] = off;
+            off += (unsigned long long)(pl.u1[s] - pl.u0[s]) * sg.rows_per_unit * sg.K * 2ull;
+        }
+        pl.layer_bytes = off;
+        pl.lm_off = off * (unsigned long long)g.L;
+        const unsigned long long lm_bytes = (unsigned long long)(pl.u1[lfk::ST_LM] - pl.u0[lfk::ST_LM]) * g.d * 2ull;
+        pl.base = base;
+        base += pl.lm_off + lm_bytes;
+        lm_rows_max = std::max(lm_rows_max, pl.u1[lfk::ST_LM] - pl.u0[lfk::ST_LM]);
+        for (int s = 0; s < 4; ++s)
+            if (pl.u1[s] > pl.u0[s]) h->n_prod[s]++;
+    }
+    h->wstream_bytes = base;
+    h->lm_rows_max = lm_rows_max;
+
+    // ---- shared memory: everything but the ring, then the largest ring that fits
+    h->act_floats = std::max(std::max(g.d, g.Q), std::max(g.F, attn_scratch_floats(g)));
+    h->act_floats = (h->act_floats + 3) / 4 * 4;
+    const unsigned rest = lfk_smem_bytes(0, h->act_floats, lm_rows_max);
+    if ((int)rest + 2 * lfk::ATT_CHUNK_BYTES > optin) {
+        delete h;
+        return LF_ERR_NOT_SUPPORTED;
+    }
+    h->ring_bytes = (int)(((unsigned)optin - rest) / 1024u * 1024u);
+    while ((int)lfk_smem_bytes(h->ring_bytes, h->act_floats, lm_rows_max) > optin) h->ring_bytes -= 1024;
+    h->smem_bytes = (int)lfk_smem_bytes(h->ring_bytes, h->act_floats, lm_rows_max);
+    if (h->ring_bytes < 2 * lfk::ATT_CHUNK_BYTES) {
+        delete h;
+        return LF_ERR_NOT_SUPPORTED;
+    }
+    int per_sm = 0;
+    e = lfk_occupancy(h->smem_bytes, &per_sm);
+    if (e != cudaSuccess) {
+        delete h;
+        return from_cuda(e);
+    }
+    if (per_sm < 1 || per_sm * h->sm_count < P) {
+        delete h;
+        return LF_ERR_NOT_RESIDENT;
+    }
+
+    // ---- allocations
+    h->max_split = std::max(1, P / g.Hkv);
+    const size_t kv_elems = (size_t)g.L * g.Hkv * (size_t)g.max_seq * g.hd;
+    const size_t n_layer_cnt = (size_t)g.L * lfk::N_LAYER_CNT;
+    const size_t n_attn_done = (size_t)g.L * g.Hkv;
+    const size_t n_words = (n_layer_cnt + n_attn_done + 3) * lfk::CNT_STRIDE;
+    h->counters_bytes = n_words * sizeof(unsigned);
+    if ((e = dalloc(&h->d_plans, (size_t)P)) != cudaSuccess || (e = dalloc(&h->wstream, h->wstream_bytes)) != cudaSuccess ||
+        (e = dalloc(&h->kc, kv_elems)) != cudaSuccess || (e = dalloc(&h->vc, kv_elems)) != cudaSuccess ||
+        (e = dalloc(&h->rope, (size_t)g.max_seq * (g.hd / 2))) != cudaSuccess ||
+        (e = dalloc(&h->qbuf, (size_t)g.L * g.Q)) != cudaSuccess ||
+        (e = dalloc(&h->attn, (size_t)g.L * g.Q)) != cudaSuccess ||
+        (e = dalloc(&h->xattn, (size_t)g.L * g.d)) != cudaSuccess ||
+        (e = dalloc(&h->hbuf, (size_t)g.L * g.F)) != cudaSuccess ||
+        (e = dalloc(&h->xout, (size_t)g.L * g.d)) != cudaSuccess ||
+        (e = dalloc(&h->apart, (size_t)g.L * g.Hq * h->max_split * (g.hd + 2))) != cudaSuccess ||
+        (e = dalloc(&h->counters, n_words)) != cudaSuccess ||
+        (e = dalloc(&h->lm_part, (size_t)P * lfk::MAX_TOPK)) != cudaSuccess ||
+        (e = dalloc(&h->tok_buf, 1)) != cudaSuccess || (e = dalloc(&h->tok_seq, (size_t)g.max_seq)) != cudaSuccess ||
+        (e = dalloc(&h->status, 8)) != cudaSuccess) {
+        free_all(h);
+        delete h;
+        return from_cuda(e);
+    }
+    h->cnt = h->counters;
+    h->attn_done = h->counters + n_layer_cnt * lfk::CNT_STRIDE;
+    h->lm_done = h->attn_done + n_attn_done * lfk::CNT_STRIDE;
+    h->tok_cnt = h->lm_done + lfk::CNT_STRIDE;
+    h->gbar = h->tok_cnt + lfk::CNT_STRIDE;
+    h->abort_flag = h->status + 4;
+    h->embed = static_cast<const __half *>(w->embed);
+    h->attn_norm = static_cast<const __half *>(w->attn_norm);
+    h->ffn_norm = static_cast<const __half *>(w->ffn_norm);
+    h->final_norm = static_cast<const __half *>(w->final_norm);
+
+    // ---- RoPE table: theta_i = pos * base^(-2i/hd) in double, cos/sin rounded to FP32
+    std::vector<float2> rope((size_t)g.max_seq * (g.hd / 2));
+    for (int pos = 0; pos < g.max_seq; ++pos)
+        for (int i = 0; i < g.hd / 2; ++i) {
+            const double inv_freq = std::pow((double)cfg->rope_theta, -2.0 * (double)i / (double)g.hd);
+            const double ang = (double)pos * inv_freq;
+            rope[(size_t)pos * (g.hd / 2) + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+        }
+    e = cudaMemcpy(h->rope, rope.data(), rope.size() * sizeof(float2), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemcpy(h->d_plans, h->plans.data(), P * sizeof(lfk::CtaPlan), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = cudaMemset(h->counters, 0, h->counters_bytes);
+    if (e == cudaSuccess) e = cudaMemset(h->status, 0, 8 * sizeof(unsigned));
+    if (e == cudaSuccess) e = cudaMemset(h->tok_buf, 0, sizeof(int));
+    if (e == cudaSuccess)
+        e = lfk_launch_repack(g, P, h->d_plans, w->wq, w->wk, w->wv, w->wo, w->w_gate, w->w_up, w->w_down,
+                              w->lm_head, h->wstream, nullptr);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = lfk_set_smem(h->smem_bytes);
+    if (e != cudaSuccess) {
+        free_all(h);
+        delete h;
+        return from_cuda(e);
+    }
+    *out = h;
+    return LF_OK;
+}
+
+void lf_destroy(lf_handle *h)
+{
+    if (!h) return;
+    cudaDeviceSynchronize();
+    free_all(h);
+    delete h;
+}
+
+lf_status lf_prefill(lf_handle *h, const int32_t *tokens_dev, int32_t n, void *stream)
+{
+    if (!h || !tokens_dev || n < 1) return LF_ERR_INVALID_ARG;
+    if (h->latched != LF_OK) return LF_ERR_STATE;
+    const int steps = (h->has_pending ? 1 : 0) + n - 1;
+    if ((long long)h->pos + steps + 1 > h->g.max_seq) return LF_ERR_CAPACITY;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (steps > 0) {
+        lfk::Params p = base_params(h);
+        p.mode = lfk::MODE_PREFILL;
+        p.n_steps = steps;
+        p.pos0 = h->pos;
+        p.has_pending = h->has_pending;
+        p.prompt = tokens_dev;
+        p.epoch0 = h->epoch;
+        p.tok_base = h->tok_count;
+        p.gbar_base = h->gbar_count;
+        p.fault_step = -1;
+        lf_status st = run_steps(h, p, s);
+        if (st != LF_OK) return st;
+        h->epoch += (unsigned)steps;
+        h->pos += steps;
+        if (h->sched == LF_SCHED_GRID_BARRIER) h->gbar_count += (unsigned)steps * 5u * (unsigned)h->g.L;
+    }
+    cudaError_t e = cudaMemcpyAsync(h->tok_buf, tokens_dev + (n - 1), sizeof(int32_t), cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return from_cuda(e);
+    h->has_pending = 1;
+    h->last_stream = s;
+    return LF_OK;
+}
+
+lf_status lf_decode(lf_handle *h, int32_t n_steps, const lf_sampling *sp, uint64_t seed, int32_t *out_tokens_dev,
+                    void *stream)
+{
+    if (!h || !sp || !out_tokens_dev || n_steps < 1) return LF_ERR_INVALID_ARG;
+    if (sp->top_k < 0 || sp->top_k > LF_MAX_TOP_K) return LF_ERR_NOT_SUPPORTED;
+    if (h->latched != LF_OK || !h->has_pending) return LF_ERR_STATE;
+    if ((long long)h->pos + n_steps > h->g.max_seq) return LF_ERR_CAPACITY;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    lfk::Params p = base_params(h);
+    p.mode = lfk::MODE_DECODE;
+    p.n_steps = n_steps;
+    p.pos0 = h->pos;
+    p.out_tokens = out_tokens_dev;
+    p.debug_logits = sp->debug_logits_dev;
+    p.force_tokens = sp->force_tokens_dev;
+    p.temperature = sp->temperature;
+    p.top_k = sp->top_k;
+    p.seed = seed;
+    p.epoch0 = h->epoch;
+    p.tok_base = h->tok_count;
+    p.gbar_base = h->gbar_count;
+    lf_status st = run_steps(h, p, s);
+    if (st != LF_OK) return st;
+    h->epoch += (unsigned)n_steps;
+    h->tok_count += (unsigned)n_steps;
+    h->pos += n_steps;
+    if (h->sched == LF_SCHED_GRID_BARRIER) h->gbar_count += (unsigned)n_steps * (5u * (unsigned)h->g.L + 1u);
+    h->last_stream = s;
+    return LF_OK;
+}
+
+lf_status lf_sync(lf_handle *h)
+{
+    if (!h) return LF_ERR_INVALID_ARG;
+    cudaError_t e = cudaStreamSynchronize(h->last_stream);
+    if (e != cudaSuccess) return from_cuda(e);
+    unsigned st[4] = {0, 0, 0, 0};
+    e = cudaMemcpy(st, h->status, sizeof(st), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return from_cuda(e);
+    if (st[0] == (unsigned)lfk::STATUS_TIMEOUT) h->latched = LF_ERR_TIMEOUT;
+    else if (st[0] != 0u) h->latched = LF_ERR_INVALID_ARG;
+    return h->latched;
+}
+
+lf_status lf_reset(lf_handle *h)
+{
+    if (!h) return LF_ERR_INVALID_ARG;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemset(h->counters, 0, h->counters_bytes);
+    if (e == cudaSuccess) e = cudaMemset(h->status, 0, 8 * sizeof(unsigned));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return from_cuda(e);
+    h->pos = 0;
+    h->has_pending = 0;
+    h->epoch = h->tok_count = h->gbar_count = 0;
+    h->latched = LF_OK;
+    return LF_OK;
+}
+
+lf_status lf_set_schedule(lf_handle *h, int32_t schedule)
+{
+    if (!h) return LF_ERR_INVALID_ARG;
+    if (schedule != LF_SCHED_FLAGS && schedule != LF_SCHED_GRID_BARRIER && schedule != LF_SCHED_MULTI_KERNEL)
+        return LF_ERR_INVALID_ARG;
+    h->sched = schedule;
+    return LF_OK;
+}
+
+lf_status lf_get_info(const lf_handle *h, lf_info *out)
+{
+    if (!h || !out) return LF_ERR_INVALID_ARG;
+    out->n_ctas = h->P;
+    out->threads_per_cta = lfk::NTHREADS;
+    out->smem_bytes = h->smem_bytes;
+    out->ring_bytes = h->ring_bytes;
+    out->sm_count = h->sm_count;
+    out->position = h->pos;
+    out->has_pending = h->has_pending;
+    out->schedule = h->sched;
+    out->weight_stream_bytes = (int64_t)h->wstream_bytes;
+    out->kv_cache_bytes = (int64_t)(2ull * h->g.L * h->g.Hkv * (size_t)h->g.max_seq * h->g.hd * 2ull);
+    return LF_OK;
+}
+
+lf_status lf_generate(lf_handle *h, const int32_t *prompt_host, int32_t n_prompt, int32_t n_steps,
+                      const lf_sampling *sp, uint64_t seed, int32_t *out_host, void *stream)
+{
+    if (!h || !prompt_host || !out_host || !sp || n_prompt < 1 || n_steps < 1) return LF_ERR_INVALID_ARG;
+    const int need = std::max(n_prompt, n_steps);
+    if (need > h->stage_cap) {
+        if (h->stage_in) cudaFree(h->stage_in);
+        if (h->stage_out) cudaFree(h->stage_out);
+        h->stage_in = h->stage_out = nullptr;
+        h->stage_cap = 0;
+        cudaError_t e = dalloc(&h->stage_in, (size_t)need);
+        if (e == cudaSuccess) e = dalloc(&h->stage_out, (size_t)need);
+        if (e != cudaSuccess) return from_cuda(e);
+        h->stage_cap = need;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(h->stage_in, prompt_host, sizeof(int32_t) * n_prompt, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return from_cuda(e);
+    lf_status st = lf_prefill(h, h->stage_in, n_prompt, stream);
+    if (st != LF_OK) return st;
+    st = lf_decode(h, n_steps, sp, seed, h->stage_out, stream);
+    if (st != LF_OK) return st;
+    e = cudaMemcpyAsync(out_host, h->stage_out, sizeof(int32_t) * n_steps, cudaMemcpyDeviceToHost, s);
+    if (e != cudaSuccess) return from_cuda(e);
+    return lf_sync(h);
+}
+
+}  // extern "C"

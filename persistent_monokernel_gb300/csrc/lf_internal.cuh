@@ -1,0 +1,160 @@
+// lf_internal.cuh -- shapes, static work partition and the kernel parameter
+// block, shared by the host runtime (lf_api.cu) and the kernels (lf_kernel.cu).
+//
+// The partition is fixed when a handle is created, in the spirit of the
+// "compile-time work partition" of the KOG monokernel (shivam2003.com,
+// "Compile-time work partition (no scheduler)"): every CTA of the persistent
+// grid knows, for every stage, which weight rows it owns and where their
+// bytes sit in its own contiguous weight stream.
+#pragma once
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+namespace lfk {
+
+constexpr int KC = 256;               // weight columns per streamed chunk
+constexpr int KC_BYTES = KC * 2;      // bytes of one row segment in a chunk
+constexpr int TILE_ROWS = 32;         // rows of one GEMV tile (4 per consumer warp)
+constexpr int NCW = 8;                // consumer warps
+constexpr int NCT = NCW * 32;         // consumer threads
+constexpr int NTHREADS = NCT + 32;    // + one producer warp
+constexpr int TICKETS = 32;           // ring slots in flight (mbarrier pairs)
+constexpr int ATT_CHUNK_BYTES = 16384;// K + V bytes of one attention sub-block
+constexpr int MAX_TOPK = 64;
+constexpr int MAX_GROUP = 8;          // query heads per KV head
+constexpr int CNT_STRIDE = 32;        // uint32 words between counters (one 128-byte line each)
+
+enum Stage { ST_QKV = 0, ST_O = 1, ST_GU = 2, ST_D = 3, ST_LM = 4, N_GEMV = 5 };
+enum LayerCounter { C_QKV = 0, C_ATTN = 1, C_O = 2, C_GU = 3, C_D = 4, N_LAYER_CNT = 5 };
+enum Mode { MODE_PREFILL = 0, MODE_DECODE = 1 };
+enum Sched { SCHED_FLAGS = 0, SCHED_GRID = 1, SCHED_MULTI = 2 };
+enum StatusCode { STATUS_OK = 0, STATUS_BAD_TOKEN = 1, STATUS_TIMEOUT = 6 };
+
+struct Geo {
+    int L, d, Hq, Hkv, hd, F, V, Q, KV, group, max_seq;
+};
+
+struct StageGeom {
+    int units;          // work units of the stage
+    int rows_per_unit;  // 2 for RoPE pairs (QKV) and gate/up pairs (GU), else 1
+    int K;              // columns (input length)
+};
+
+__host__ __device__ inline int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// QKV units are row pairs (i, i + hd/2) of one head of the fused [q; k; v]
+// row space, so that RoPE's rotate-half partners land in the same tile.
+// GU units are (gate row r, up row r) pairs, so that SiLU(gate) * up is
+// formed where both rows were computed.
+__host__ __device__ inline StageGeom stage_geom(const Geo &g, int s)
+{
+    switch (s) {
+    case ST_QKV: return {(g.Q + 2 * g.KV) / 2, 2, g.d};
+    case ST_O: return {g.d, 1, g.Q};
+    case ST_GU: return {g.F, 2, g.d};
+    case ST_D: return {g.d, 1, g.F};
+    default: return {g.V, 1, g.d};
+    }
+}
+
+__host__ __device__ inline int units_per_tile(int rpu) { return TILE_ROWS / rpu; }
+__host__ __device__ inline int tiles_of(int n_units, int rpu)
+{
+    return n_units <= 0 ? 0 : ceil_div(n_units, units_per_tile(rpu));
+}
+// Units [a, b) of tile t when n units starting at u0 are split into nt near-equal tiles.
+__host__ __device__ inline void tile_range(int u0, int n, int nt, int t, int &a, int &b)
+{
+    a = u0 + (int)((long long)t * n / nt);
+    b = u0 + (int)((long long)(t + 1) * n / nt);
+}
+// First unit owned by CTA b when U units are split contiguously over P CTAs.
+__host__ __device__ inline int cta_unit_start(int U, int P, int b) { return (int)((long long)b * U / P); }
+
+// Split-KV attention: the ctx positions of each KV head are cut into n_split
+// contiguous pieces of `per` positions (the last may be shorter; none is
+// empty), at most P / Hkv pieces per head, at least min_len positions each.
+struct AttnSplit { int n_split, per; };
+__host__ __device__ inline AttnSplit attn_split(int ctx, int P, int Hkv, int min_len)
+{
+    int maxs = P / Hkv;
+    if (maxs < 1) maxs = 1;
+    int n0 = ceil_div(ctx, min_len);
+    if (n0 > maxs) n0 = maxs;
+    if (n0 < 1) n0 = 1;
+    int per = ceil_div(ctx, n0);
+    return {ceil_div(ctx, per), per};
+}
+// Attention unit u of layer l (u in [0, U), U = Hkv * n_split) runs on CTA (u + l*U) mod P.
+__host__ __device__ inline int attn_unit_first(int b, int l, int U, int P)
+{
+    long long r = ((long long)b - (long long)l * U) % P;
+    if (r < 0) r += P;
+    return (int)r;
+}
+__host__ __device__ inline int attn_sub_positions(int hd) { return ATT_CHUNK_BYTES / (4 * hd); }
+
+// Per-CTA plan: unit ranges of the five GEMV stages and the byte offsets of
+// this CTA's weight stream.  The stream of CTA b is laid out as
+//   [layer 0: QKV tiles | O tiles | GU tiles | D tiles] ... [layer L-1: ...] [LM-head tiles]
+// and each tile as K/256 chunks of (R rows x 256 columns), row-major inside a chunk.
+struct CtaPlan {
+    int u0[N_GEMV], u1[N_GEMV];
+    unsigned long long base;          // byte offset of the stream in the repacked buffer
+    unsigned long long layer_bytes;   // bytes of one layer's four stages
+    unsigned long long stage_off[4];  // offset of each stage inside a layer
+    unsigned long long lm_off;        // offset of the LM-head tiles from base
+};
+
+struct Params {
+    Geo g;
+    int P;                       // persistent CTAs
+    float eps;
+    const CtaPlan *plans;
+    const uint8_t *wstream;      // repacked FP16 weights
+    const __half *embed, *attn_norm, *ffn_norm, *final_norm;
+    __half *kc, *vc;             // [L][Hkv][max_seq][hd]
+    const float2 *rope;          // [max_seq][hd/2] (cos, sin)
+    float *qbuf;                 // [L][Q]   RoPE'd queries
+    float *attn;                 // [L][Q]   attention output
+    float *xattn;                // [L][d]   residual after attention
+    float *hbuf;                 // [L][F]   SiLU(gate) * up
+    float *xout;                 // [L][d]   residual after FFN
+    float *apart;                // [L][Hq][max_split][hd + 2]  (o[hd], m, l) per piece
+    int max_split;
+    unsigned *cnt;               // [L][N_LAYER_CNT] counters
+    unsigned *attn_done;         // [L][Hkv]
+    unsigned *lm_done, *tok_cnt, *gbar;
+    unsigned n_prod[4];          // CTAs that publish each GEMV stage (QKV, O, GU, D)
+    unsigned long long *lm_part; // [P][MAX_TOPK] 64-bit selection keys
+    int *tok_buf;                // [1] pending token
+    int *tok_seq;                // [max_seq] token fed to step i + 1
+    unsigned *status;            // first error code (0 = none)
+    unsigned *abort_flag;
+    // per call
+    int mode;
+    int n_steps;
+    int pos0;                    // position of step 0's input token
+    int has_pending;             // prefill: step 0 consumes the pending token first
+    const int *prompt;
+    int *out_tokens;
+    float *debug_logits;
+    const int *force_tokens;
+    float temperature;
+    int top_k;                   // 0 = whole vocabulary
+    unsigned long long seed;
+    unsigned epoch0;             // forward passes since the counters were cleared
+    unsigned tok_base;           // sampled tokens since the counters were cleared
+    unsigned gbar_base;          // grid barriers since the counters were cleared
+    long long timeout_ns;
+    int fault_step;
+    int ring_bytes;
+    int act_floats;
+    int lm_rows_max;
+    int attn_min_len;
+    int sched;
+    // multi-kernel schedule: run only stage `only_stage` of layer `only_layer` of step 0
+    int only_layer, only_stage;
+};
+
+}  // namespace lfk

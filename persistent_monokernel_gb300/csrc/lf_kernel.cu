@@ -1,0 +1,1151 @@
+// lf_kernel.cu -- the persistent decode monokernel for sm_103a.
+//
+// One CTA per SM runs every stage of every decode step, as in the KOG
+// monokernel (shivam2003.com, "Pillar 3 -- the monokernel runtime"):
+//
+//   for step:                                    (one token)
+//     for layer:
+//       QKV   rmsnorm(x) . [Wq;Wk;Wv] -> RoPE -> q, K/V cache append (FP16)
+//       ATTN  split-KV attention pieces -> the last piece of a KV head combines
+//       O     x += Wo . attn
+//       GU    h = SiLU(Wg . rmsnorm(x)) * (Wu . rmsnorm(x))
+//       D     x += Wd . h
+//     LM      logits = Whead . rmsnorm(x) -> per-CTA candidates -> the last CTA samples
+//
+// Warp roles.  Warp NCW (the producer) streams this CTA's weights -- repacked
+// at handle creation into one contiguous per-CTA stream in consumption order
+// -- and the K/V sub-blocks of its attention pieces through a shared-memory
+// byte ring with 1-D TMA bulk copies carrying an L2 evict-first hint
+// (shivam2003.com, "Weight streaming -- keeping HBM saturated": non-temporal
+// weight loads, and weights for the next stages fetched while the current
+// one still runs).  It never waits for activations, so the ring fills ahead
+// across stage, layer and token boundaries.  Warps 0..NCW-1 (the consumers)
+// compute.
+//
+// Synchronisation.  In the default schedule a stage waits only for the
+// counters of the data it reads (stackfutures.com, "The Monokernel":
+// per-dependency waits instead of a global barrier).  Producers publish with
+// red.release.gpu; consumers poll with ld.acquire.gpu.  Counters only grow:
+// stage s of layer l is complete for forward pass e when its counter reaches
+// (e + 1) * (number of CTAs that publish it).  Every wait is bounded by a
+// %globaltimer deadline; on expiry the kernel records the error, raises an
+// abort flag that every other wait also polls, drains its in-flight copies
+// and returns.
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "lf_internal.cuh"
+#include "lf_ptx.cuh"
+
+namespace lfk {
+
+// ---------------------------------------------------------------- shared memory
+
+struct SmemLayout {
+    unsigned ring, act, lmkeys, res, full, empty, chunk_end, red, hist, misc, total;
+};
+
+__host__ __device__ inline unsigned align_up(unsigned x, unsigned a) { return (x + a - 1) / a * a; }
+
+__host__ __device__ inline SmemLayout smem_layout(int ring_bytes, int act_floats, int lm_rows_max)
+{
+    SmemLayout s;
+    unsigned o = 0;
+    s.ring = o;      o = align_up(o + (unsigned)ring_bytes, 128);
+    s.act = o;       o = align_up(o + 4u * (unsigned)act_floats, 128);
+    s.lmkeys = o;    o = align_up(o + 8u * (unsigned)lm_rows_max, 128);
+    s.res = o;       o = align_up(o + 4u * 2u * TILE_ROWS, 128);
+    s.full = o;      o += 8u * TICKETS;
+    s.empty = o;     o += 8u * TICKETS;
+    s.chunk_end = o; o += 8u * TICKETS;
+    s.red = o;       o = align_up(o + 4u * 64u, 16);
+    s.hist = o;      o = align_up(o + 4u * 256u, 16);
+    s.misc = o;      o = align_up(o + 4u * 64u, 128);
+    s.total = o;
+    return s;
+}
+
+// misc word indices
+enum { M_FLAG = 0, M_TOKEN = 1, M_DIGIT = 2, M_REMAIN = 3, M_INV = 4 };
+
+struct Ctx {
+    const Params *p;
+    uint8_t *ring;
+    float *act;
+    unsigned long long *lmkeys;
+    float *res;
+    uint64_t *full, *empty;
+    unsigned long long *chunk_end;
+    float *red;
+    unsigned *hist;
+    unsigned *misc;
+    int b;            // CTA index
+    int tid, warp, lane;
+};
+
+// Stage ids for the multi-kernel schedule's stage filter.
+enum { SID_QKV = 0, SID_ATTN = 1, SID_O = 2, SID_GU = 3, SID_D = 4, SID_LM = 5 };
+
+__device__ __forceinline__ bool stage_active(const Params &p, int layer, int sid)
+{
+    if (p.only_stage < 0) return true;
+    return p.only_stage == sid && (sid == SID_LM || p.only_layer == layer);
+}
+
+// ---------------------------------------------------------------- bounded waits
+
+__device__ __forceinline__ void raise_error(const Params &p, unsigned code, unsigned where, unsigned layer,
+                                            unsigned step)
+{
+    if (atomicCAS(p.status, 0u, code) == 0u) {
+        p.status[1] = where;
+        p.status[2] = layer;
+        p.status[3] = step;
+    }
+    atomicExch(p.abort_flag, 1u);
+}
+
+// Spin until (int)(*ctr - target) >= 0.  Returns false on timeout or abort.
+__device__ bool wait_counter(const Params &p, const unsigned *ctr, unsigned target, unsigned where,
+                             unsigned layer, unsigned step)
+{
+    unsigned long long t0 = 0;
+    for (unsigned it = 0;; ++it) {
+        if ((int)(ld_acquire(ctr) - target) >= 0) return true;
+        if ((it & 31u) == 31u) {
+            if (ld_relaxed(p.abort_flag)) return false;
+            unsigned long long now = globaltimer_ns();
+            if (t0 == 0) t0 = now;
+            else if ((long long)(now - t0) > p.timeout_ns) {
+                raise_error(p, STATUS_TIMEOUT, where, layer, step);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ bool wait_mbar(const Params &p, uint64_t *bar, unsigned parity, unsigned where)
+{
+    unsigned long long t0 = 0;
+    for (unsigned it = 0;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 15u) == 15u) {
+            if (ld_relaxed(p.abort_flag)) return false;
+            unsigned long long now = globaltimer_ns();
+            if (t0 == 0) t0 = now;
+            else if ((long long)(now - t0) > p.timeout_ns) {
+                raise_error(p, STATUS_TIMEOUT, where, 0xFFFFu, 0xFFFFu);
+                return false;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- ring cursors
+
+// Both sides place chunks identically: a chunk that would cross the end of the
+// ring starts at offset 0 instead.
+struct ConsRing {
+    unsigned n = 0;    // chunks consumed
+    unsigned off = 0;  // read offset
+    __device__ const uint8_t *acquire(const Ctx &c, unsigned bytes, bool &ab)
+    {
+        if (off + bytes > (unsigned)c.p->ring_bytes) off = 0;
+        const uint8_t *ptr = c.ring + off;
+        off += bytes;
+        bool fail = ab;
+        if (!fail) fail = !wait_mbar(*c.p, &c.full[n % TICKETS], (n / TICKETS) & 1u, 100);
+        if (__any_sync(0xffffffffu, fail)) {
+            ab = true;
+            return nullptr;
+        }
+        return ptr;
+    }
+    __device__ void release(const Ctx &c)
+    {
+        __syncwarp();
+        if (c.lane == 0) mbar_arrive(&c.empty[n % TICKETS]);
+        ++n;
+    }
+};
+
+struct ProdRing {
+    unsigned n = 0, off = 0, tail_n = 0;
+    unsigned long long alloc = 0, tail_b = 0;
+    uint64_t pol = 0;     // weights: read once per token, L2 evict-first
+    uint64_t pol_kv = 0;  // KV cache
+    // Reserve `bytes` of ring and a ticket; returns the ring offset or -1 on abort.
+    __device__ int reserve(const Ctx &c, unsigned bytes)
+    {
+        const unsigned RB = (unsigned)c.p->ring_bytes;
+        if (off + bytes > RB) {
+            alloc += RB - off;
+            off = 0;
+        }
+        while (n - tail_n >= (unsigned)TICKETS || alloc + bytes - tail_b > RB) {
+            if (!wait_mbar(*c.p, &c.empty[tail_n % TICKETS], (tail_n / TICKETS) & 1u, 101)) return -1;
+            tail_b = c.chunk_end[tail_n % TICKETS];
+            ++tail_n;
+        }
+        c.chunk_end[n % TICKETS] = alloc + bytes;
+        int o = (int)off;
+        off += bytes;
+        alloc += bytes;
+        return o;
+    }
+    __device__ bool emit(const Ctx &c, const void *src, unsigned bytes)
+    {
+        int o = reserve(c, bytes);
+        if (o < 0) return false;
+        uint64_t *bar = &c.full[n % TICKETS];
+        mbar_arrive_expect_tx(bar, bytes);
+        bulk_g2s(c.ring + o, src, bytes, bar, pol);
+        ++n;
+        return true;
+    }
+    // K and V rows of one attention sub-block: re-read every step, so they
+    // keep the normal L2 priority.
+    __device__ bool emit2(const Ctx &c, const void *src0, const void *src1, unsigned half_bytes)
+    {
+        int o = reserve(c, 2 * half_bytes);
+        if (o < 0) return false;
+        uint64_t *bar = &c.full[n % TICKETS];
+        mbar_arrive_expect_tx(bar, 2 * half_bytes);
+        bulk_g2s(c.ring + o, src0, half_bytes, bar, pol_kv);
+        bulk_g2s(c.ring + o + half_bytes, src1, half_bytes, bar, pol_kv);
+        ++n;
+        return true;
+    }
+    // After an abort: wait (bounded) until every issued copy has landed, so
+    // that no TMA write into shared memory is in flight when the CTA exits.
+    __device__ void drain(const Ctx &c)
+    {
+        unsigned first = (n > (unsigned)TICKETS && n - TICKETS > tail_n) ? n - TICKETS : tail_n;
+        for (unsigned k = first; k < n; ++k) {
+            unsigned long long t0 = globaltimer_ns();
+            while (!mbar_try_wait(&c.full[k % TICKETS], (k / TICKETS) & 1u)) {
+                if ((long long)(globaltimer_ns() - t0) > c.p->timeout_ns) break;
+            }
+        }
+    }
+};
+
+// ---------------------------------------------------------------- helpers
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v)
+{
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        unsigned long long w = __shfl_xor_sync(0xffffffffu, v, o);
+        v = w > v ? w : v;
+    }
+    return v;
+}
+
+__device__ __forceinline__ float dot8(uint4 w, float4 xa, float4 xb, float acc)
+{
+    float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&w.x));
+    float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&w.y));
+    float2 f2 = __half22float2(*reinterpret_cast<const __half2 *>(&w.z));
+    float2 f3 = __half22float2(*reinterpret_cast<const __half2 *>(&w.w));
+    acc = fmaf(f0.x, xa.x, acc);
+    acc = fmaf(f0.y, xa.y, acc);
+    acc = fmaf(f1.x, xa.z, acc);
+    acc = fmaf(f1.y, xa.w, acc);
+    acc = fmaf(f2.x, xb.x, acc);
+    acc = fmaf(f2.y, xb.y, acc);
+    acc = fmaf(f3.x, xb.z, acc);
+    acc = fmaf(f3.y, xb.w, acc);
+    return acc;
+}
+
+__device__ __forceinline__ float gumbel_dev(unsigned long long seed, int pos, int i)
+{
+    uint4 r = philox4x32_10(make_uint4((unsigned)i >> 2, (unsigned)pos, 0u, 0u),
+                            make_uint2((unsigned)(seed & 0xFFFFFFFFull), (unsigned)(seed >> 32)));
+    unsigned w = (i & 3) == 0 ? r.x : (i & 3) == 1 ? r.y : (i & 3) == 2 ? r.z : r.w;
+    float u = (float)((w >> 9) * 2u + 1u) * 0x1p-24f;
+    return -logf(-logf(u));
+}
+
+// ---------------------------------------------------------------- stage plumbing
+
+__device__ __forceinline__ unsigned *layer_cnt(const Params &p, int l, int which)
+{
+    return p.cnt + ((size_t)l * N_LAYER_CNT + which) * CNT_STRIDE;
+}
+
+// Grid-barrier schedule: index of the barrier that closes (step, layer, slot).
+// Slots 0..4 close QKV, attention, O, GU and D of a layer; slot 5 closes the
+// LM head and sampling of a decode step.
+__device__ __forceinline__ unsigned gbar_index(const Params &p, int step, int l, int slot)
+{
+    const unsigned per_step = 5u * (unsigned)p.g.L + (p.mode == MODE_DECODE ? 1u : 0u);
+    const unsigned in_step = slot == 5 ? 5u * (unsigned)p.g.L : (unsigned)l * 5u + (unsigned)slot;
+    return p.gbar_base + (unsigned)step * per_step + in_step;
+}
+
+// Consumer-side dependency wait: thread 0 polls, then the consumer warps
+// meet at a named barrier that also ORs the abort state.  Returns true if
+// the CTA must stop.
+__device__ bool cons_wait(const Ctx &c, const unsigned *ctr, unsigned target, unsigned where, int l, int step,
+                          bool ab)
+{
+    if (c.tid == 0 && !ab) ab = !wait_counter(*c.p, ctr, target, where, l, step);
+    return cons_sync_or(ab);
+}
+
+// Publish the end of a stage: all consumer writes are ordered before thread
+// 0's release by the named barrier plus a gpu-scope fence.
+__device__ bool cons_publish(const Ctx &c, unsigned *ctr, bool do_cnt, unsigned *gbar, bool ab)
+{
+    ab = cons_sync_or(ab);
+    if (ab) return true;
+    if (c.tid == 0) {
+        fence_acq_rel_gpu();
+        if (do_cnt) red_release_add(ctr, 1u);
+        if (gbar) red_release_add(gbar, 1u);
+    }
+    return false;
+}
+
+// Stage input wait in the three schedules: the producer counter `ctr` in the
+// flag schedule, the grid barrier (gstep, gl, gslot) in the barrier schedule,
+// nothing in the multi-kernel schedule (the previous launch has finished).
+__device__ bool stage_wait(const Ctx &c, const unsigned *ctr, unsigned target, int gstep, int gl, int gslot,
+                           int step, int l, unsigned where, bool ab)
+{
+    const Params &p = *c.p;
+    if (p.sched == SCHED_MULTI) return cons_sync_or(ab);
+    if (p.sched == SCHED_GRID) {
+        if (gslot < 0) return cons_sync_or(ab);
+        const unsigned idx = gbar_index(p, gstep, gl, gslot);
+        return cons_wait(c, p.gbar, (idx + 1u) * (unsigned)p.P, where, l, step, ab);
+    }
+    if (!ctr) return cons_sync_or(ab);
+    return cons_wait(c, ctr, target, where, l, step, ab);
+}
+
+// Load an activation vector into shared memory, times the RMSNorm gain if
+// given, and return 1/sqrt(mean(x^2) + eps) (or 1 if norm == false).  The
+// input is FP32 from global memory (read at L2, never a stale L1 line) or,
+// for layer 0, the FP16 embedding row.
+__device__ bool load_act(const Ctx &c, const float *src32, const __half *src16, const __half *gain, int K, bool norm,
+                         float &inv, bool ab)
+{
+    const Params &p = *c.p;
+    float ss = 0.f;
+    float4 *xs = reinterpret_cast<float4 *>(c.act);
+    if (!ab) {
+        for (int i = c.tid; i < K / 4; i += NCT) {
+            float4 v;
+            if (src32) {
+                v = __ldcg(reinterpret_cast<const float4 *>(src32) + i);
+            } else {
+                uint2 hv = __ldg(reinterpret_cast<const uint2 *>(src16) + i);
+                float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&hv.x));
+                float2 b2 = __half22float2(*reinterpret_cast<const __half2 *>(&hv.y));
+                v = make_float4(a.x, a.y, b2.x, b2.y);
+            }
+            if (norm) ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+            if (gain) {
+                uint2 gv = __ldg(reinterpret_cast<const uint2 *>(gain) + i);
+                float2 ga = __half22float2(*reinterpret_cast<const __half2 *>(&gv.x));
+                float2 gb = __half22float2(*reinterpret_cast<const __half2 *>(&gv.y));
+                v.x *= ga.x;
+                v.y *= ga.y;
+                v.z *= gb.x;
+                v.w *= gb.y;
+            }
+            xs[i] = v;
+        }
+    }
+    inv = 1.f;
+    if (norm) {
+        ss = warp_sum(ss);
+        if (c.lane == 0) c.red[c.warp] = ss;
+        if (cons_sync_or(ab)) return true;
+        float tot = 0.f;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) tot += c.red[w];
+        inv = 1.0f / sqrtf(tot / (float)K + p.eps);
+    }
+    return cons_sync_or(ab);
+}
+
+// One GEMV tile: R rows (stored rows w, w+8, w+16, w+24 belong to warp w),
+// K columns in chunks of 256 from the ring.  Writes the R dot products to res.
+__device__ void gemv_tile(const Ctx &c, ConsRing &rc, int R, int K, float *res, bool &ab)
+{
+    const int w = c.warp, ln = c.lane;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    const int nkc = K / KC;
+    const float4 *xs = reinterpret_cast<const float4 *>(c.act);
+    for (int kc = 0; kc < nkc; ++kc) {
+        const uint8_t *ch = rc.acquire(c, (unsigned)R * KC_BYTES, ab);
+        if (ab) break;
+        const float4 xa = xs[kc * 64 + ln * 2];
+        const float4 xb = xs[kc * 64 + ln * 2 + 1];
+        const uint4 *wp = reinterpret_cast<const uint4 *>(ch) + ln;
+        if (w < R) a0 = dot8(wp[w * 32], xa, xb, a0);
+        if (w + 8 < R) a1 = dot8(wp[(w + 8) * 32], xa, xb, a1);
+        if (w + 16 < R) a2 = dot8(wp[(w + 16) * 32], xa, xb, a2);
+        if (w + 24 < R) a3 = dot8(wp[(w + 24) * 32], xa, xb, a3);
+        rc.release(c);
+    }
+    a0 = warp_sum(a0);
+    a1 = warp_sum(a1);
+    a2 = warp_sum(a2);
+    a3 = warp_sum(a3);
+    if (ln == 0) {
+        if (w < R) res[w] = a0;
+        if (w + 8 < R) res[w + 8] = a1;
+        if (w + 16 < R) res[w + 16] = a2;
+        if (w + 24 < R) res[w + 24] = a3;
+    }
+}
+
+// Token fed to forward pass `step` (decode: after its counter was acquired).
+// An id outside [0, V) is reported (LF_ERR_INVALID_ARG via lf_sync) and
+// replaced by 0, so that no embedding read leaves the table.
+__device__ __forceinline__ int step_token(const Params &p, int step)
+{
+    int t;
+    if (p.mode == MODE_PREFILL) {
+        if (p.has_pending) t = step == 0 ? __ldcg(p.tok_buf) : __ldg(p.prompt + step - 1);
+        else t = __ldg(p.prompt + step);
+    } else {
+        t = step == 0 ? __ldcg(p.tok_buf) : __ldcg(p.tok_seq + step - 1);
+    }
+    if ((unsigned)t >= (unsigned)p.g.V) {
+        raise_error(p, STATUS_BAD_TOKEN, 300, 0, (unsigned)step);
+        t = 0;
+    }
+    return t;
+}
+
+// ---------------------------------------------------------------- GEMV stages
+
+__device__ bool stage_gemv(const Ctx &c, ConsRing &rc, int s, int l, int step, bool ab)
+{
+    const Params &p = *c.p;
+    const Geo &g = p.g;
+    const CtaPlan &pl = p.plans[c.b];
+    const StageGeom sg = stage_geom(g, s);
+    const int pos = p.pos0 + step;
+    // layer 0 reads the embedding row of the step's token (after the stage's wait)
+    const int tok = (l == 0 && (s == ST_QKV || s == ST_O)) ? step_token(p, step) : 0;
+
+    // ---- inputs
+    float inv = 1.f;
+    if (s == ST_QKV) {
+        ab = load_act(c, l == 0 ? nullptr : p.xout + (size_t)(l - 1) * g.d,
+                      l == 0 ? p.embed + (size_t)tok * g.d : nullptr, p.attn_norm + (size_t)l * g.d, g.d, true, inv,
+                      ab);
+    } else if (s == ST_O) {
+        ab = load_act(c, p.attn + (size_t)l * g.Q, nullptr, nullptr, g.Q, false, inv, ab);
+    } else if (s == ST_GU) {
+        ab = load_act(c, p.xattn + (size_t)l * g.d, nullptr, p.ffn_norm + (size_t)l * g.d, g.d, true, inv, ab);
+    } else if (s == ST_D) {
+        ab = load_act(c, p.hbuf + (size_t)l * g.F, nullptr, nullptr, g.F, false, inv, ab);
+    } else {
+        ab = load_act(c, p.xout + (size_t)(g.L - 1) * g.d, nullptr, p.final_norm, g.d, true, inv, ab);
+    }
+    if (ab) return true;
+
+    const int u0 = pl.u0[s], n = pl.u1[s] - u0;
+    const int nt = tiles_of(n, sg.rows_per_unit);
+    for (int t = 0; t < nt; ++t) {
+        int a, bnd;
+        tile_range(u0, n, nt, t, a, bnd);
+        const int nu = bnd - a;
+        const int R = nu * sg.rows_per_unit;
+        float *res = c.res + (t & 1) * TILE_ROWS;
+        gemv_tile(c, rc, R, sg.K, res, ab);
+        if (cons_sync_or(ab)) return true;
+        // ---- epilogue
+        for (int i = c.tid; i < nu; i += NCT) {
+            const int u = a + i;
+            if (s == ST_QKV) {
+                const int half = g.hd / 2;
+                const int hh = u / half, j = u % half;
+                const float v0 = res[i] * inv, v1 = res[i + nu] * inv;
+                if (hh < g.Hq + g.Hkv) {
+                    const float2 cs = __ldg(p.rope + (size_t)pos * half + j);
+                    const float r0 = v0 * cs.x - v1 * cs.y;
+                    const float r1 = v1 * cs.x + v0 * cs.y;
+                    if (hh < g.Hq) {
+                        float *q = p.qbuf + (size_t)l * g.Q + (size_t)hh * g.hd;
+                        q[j] = r0;
+                        q[j + half] = r1;
+                    } else {
+                        const int kvh = hh - g.Hq;
+                        __half *k = p.kc + (((size_t)l * g.Hkv + kvh) * g.max_seq + pos) * g.hd;
+                        k[j] = __float2half_rn(r0);
+                        k[j + half] = __float2half_rn(r1);
+                    }
+                } else {
+                    const int kvh = hh - g.Hq - g.Hkv;
+                    __half *v = p.vc + (((size_t)l * g.Hkv + kvh) * g.max_seq + pos) * g.hd;
+                    v[j] = __float2half_rn(v0);
+                    v[j + half] = __float2half_rn(v1);
+                }
+            } else if (s == ST_O) {
+                const float xin = (l == 0) ? __half2float(p.embed[(size_t)tok * g.d + u])
+                                           : __ldcg(p.xout + (size_t)(l - 1) * g.d + u);
+                p.xattn[(size_t)l * g.d + u] = xin + res[i];
+            } else if (s == ST_GU) {
+                const float gt = res[i] * inv, up = res[i + nu] * inv;
+                p.hbuf[(size_t)l * g.F + u] = gt / (1.0f + expf(-gt)) * up;
+            } else if (s == ST_D) {
+                p.xout[(size_t)l * g.d + u] = __ldcg(p.xattn + (size_t)l * g.d + u) + res[i];
+            } else {
+                const float logit = res[i] * inv;
+                if (p.debug_logits) p.debug_logits[(size_t)step * g.V + u] = logit;
+                float keyv = logit;
+                const bool all_vocab = p.temperature > 0.f && p.top_k != 1 && (p.top_k <= 0 || p.top_k >= g.V);
+                if (all_vocab) keyv = logit / p.temperature + gumbel_dev(p.seed, pos, u);
+                c.lmkeys[u - u0] = sel_key(keyv, u);
+            }
+        }
+        if (s == ST_QKV) fence_proxy_async_global();  // K/V rows are read by TMA in later steps
+    }
+    return false;
+}
+
+// ---------------------------------------------------------------- attention
+
+template <int HD>
+__device__ bool attn_piece(const Ctx &c, ConsRing &rc, int l, int step, int gkv, int cpiece, const AttnSplit &sp,
+                           bool ab)
+{
+    constexpr int E = HD / 32;           // K elements per lane
+    constexpr int S = ATT_CHUNK_BYTES / (4 * HD);
+    const Params &p = *c.p;
+    const Geo &g = p.g;
+    const int G = g.group;
+    const int pos = p.pos0 + step;
+    const int ctx = pos + 1;
+    const int j0 = cpiece * sp.per;
+    const int j1 = min(j0 + sp.per, ctx);
+    const int jr = min(j1, pos);          // ring positions are [j0, jr); pos itself is read fresh
+    const float scale = 1.0f / sqrtf((float)HD);
+
+    float *qs = c.act;                    // [G][HD]
+    float *sc = qs + G * HD;              // [G][S]
+    float *pb = sc + G * S;               // [G][S]
+    float *mrun = pb + G * S;             // [G]
+    float *lrun = mrun + MAX_GROUP;       // [G]
+    float *alph = lrun + MAX_GROUP;       // [G]
+    __half *fresh = reinterpret_cast<__half *>(alph + MAX_GROUP);  // [2][HD]
+
+    const float *qsrc = p.qbuf + (size_t)l * g.Q + (size_t)gkv * G * HD;
+    for (int i = c.tid; i < G * HD; i += NCT) qs[i] = __ldcg(qsrc + i);
+    if (c.tid < G) {
+        mrun[c.tid] = -INFINITY;
+        lrun[c.tid] = 0.f;
+    }
+    if (cons_sync_or(ab)) return true;
+
+    float qreg[MAX_GROUP][E];
+#pragma unroll
+    for (int h = 0; h < MAX_GROUP; ++h)
+#pragma unroll
+        for (int e = 0; e < E; ++e) qreg[h][e] = (h < G) ? qs[h * HD + c.lane * E + e] : 0.f;
+
+    constexpr int OMAX = (MAX_GROUP * HD + NCT - 1) / NCT;
+    float o[OMAX];
+#pragma unroll
+    for (int k = 0; k < OMAX; ++k) o[k] = 0.f;
+
+    const size_t kvbase = ((size_t)l * g.Hkv + gkv) * g.max_seq;
+    const int nring = jr > j0 ? ceil_div(jr - j0, S) : 0;
+    const bool has_fresh = (pos >= j0 && pos < j1);
+    const int nblocks = nring + (has_fresh ? 1 : 0);
+
+    for (int blk = 0; blk < nblocks; ++blk) {
+        const __half *Kb, *Vb;
+        int nb;
+        const bool is_ring = blk < nring;
+        if (is_ring) {
+            nb = min(S, jr - (j0 + blk * S));
+            const uint8_t *ch = rc.acquire(c, 4u * (unsigned)nb * HD, ab);
+            Kb = reinterpret_cast<const __half *>(ch);
+            Vb = Kb + (size_t)nb * HD;
+        } else {
+            nb = 1;
+            const __half *ksrc = p.kc + (kvbase + pos) * HD;
+            const __half *vsrc = p.vc + (kvbase + pos) * HD;
+            for (int i = c.tid; i < HD; i += NCT) {
+                fresh[i] = __ushort_as_half(__ldcg(reinterpret_cast<const unsigned short *>(ksrc) + i));
+                fresh[HD + i] = __ushort_as_half(__ldcg(reinterpret_cast<const unsigned short *>(vsrc) + i));
+            }
+            if (cons_sync_or(ab)) return true;
+            Kb = fresh;
+            Vb = fresh + HD;
+        }
+        // scores: one position per warp at a time, lanes split the head dim
+        if (!ab) {
+            for (int jj = c.warp; jj < nb; jj += NCW) {
+                float kv[E];
+                const __half *kr = Kb + (size_t)jj * HD + c.lane * E;
+                if constexpr (E == 4) {
+                    const uint2 raw = *reinterpret_cast<const uint2 *>(kr);
+                    const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
+                    const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
+                    kv[0] = f0.x;
+                    kv[1] = f0.y;
+                    kv[2] = f1.x;
+                    kv[3] = f1.y;
+                } else {
+                    const unsigned raw = *reinterpret_cast<const unsigned *>(kr);
+                    const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&raw));
+                    kv[0] = f0.x;
+                    kv[1] = f0.y;
+                }
+#pragma unroll
+                for (int h = 0; h < MAX_GROUP; ++h) {
+                    if (h < G) {
+                        float d = 0.f;
+#pragma unroll
+                        for (int e = 0; e < E; ++e) d = fmaf(qreg[h][e], kv[e], d);
+                        d = warp_sum(d);
+                        if (c.lane == 0) sc[h * S + jj] = d * scale;
+                    }
+                }
+            }
+        }
+        if (cons_sync_or(ab)) return true;
+        // per-head running max / sum (one warp per head)
+        for (int h = c.warp; h < G; h += NCW) {
+            float s0 = c.lane < nb ? sc[h * S + c.lane] : -INFINITY;
+            float s1 = c.lane + 32 < nb ? sc[h * S + c.lane + 32] : -INFINITY;
+            const float mx = warp_max(fmaxf(s0, s1));
+            const float mold = mrun[h];
+            const float mnew = fmaxf(mold, mx);
+            const float alpha = (mold == -INFINITY) ? 0.f : expf(mold - mnew);
+            const float p0 = c.lane < nb ? expf(s0 - mnew) : 0.f;
+            const float p1 = c.lane + 32 < nb ? expf(s1 - mnew) : 0.f;
+            if (c.lane < nb) pb[h * S + c.lane] = p0;
+            if (c.lane + 32 < nb) pb[h * S + c.lane + 32] = p1;
+            const float ls = warp_sum(p0 + p1);
+            __syncwarp();
+            if (c.lane == 0) {
+                lrun[h] = lrun[h] * alpha + ls;
+                mrun[h] = mnew;
+                alph[h] = alpha;
+            }
+        }
+        if (cons_sync_or(ab)) return true;
+        // o = o * alpha + sum_j p_j V_j
+#pragma unroll
+        for (int k = 0; k < OMAX; ++k) {
+            const int eidx = c.tid + k * NCT;
+            if (eidx < G * HD) {
+                const int h = eidx / HD, i = eidx % HD;
+                float acc = o[k] * alph[h];
+                for (int jj = 0; jj < nb; ++jj) acc = fmaf(pb[h * S + jj], __half2float(Vb[(size_t)jj * HD + i]), acc);
+                o[k] = acc;
+            }
+        }
+        if (is_ring && !ab) rc.release(c);
+        if (cons_sync_or(ab)) return true;
+    }
+
+    // ---- write this piece's partial (o, m, l) per query head of the group
+    const int hq0 = gkv * G;
+#pragma unroll
+    for (int k = 0; k < OMAX; ++k) {
+        const int eidx = c.tid + k * NCT;
+        if (eidx < G * HD) {
+            const int h = eidx / HD, i = eidx % HD;
+            float *dst = p.apart + (((size_t)l * g.Hq + hq0 + h) * p.max_split + cpiece) * (HD + 2);
+            dst[i] = o[k];
+            if (i == 0) {
+                dst[HD] = mrun[h];
+                dst[HD + 1] = lrun[h];
+            }
+        }
+    }
+    if (cons_sync_or(ab)) return true;
+    if (c.tid == 0) {
+        fence_acq_rel_gpu();
+        unsigned old = atom_add_acq_rel(p.attn_done + ((size_t)l * g.Hkv + gkv) * CNT_STRIDE, 1u);
+        c.misc[M_FLAG] = (old == (unsigned)sp.n_split - 1u) ? 1u : 0u;
+    }
+    if (cons_sync_or(ab)) return true;
+    if (c.misc[M_FLAG] == 0u) return false;
+
+    // ---- this CTA holds the last piece of KV head gkv: combine all pieces
+    if (c.tid == 0) st_relaxed(p.attn_done + ((size_t)l * g.Hkv + gkv) * CNT_STRIDE, 0u);
+#pragma unroll
+    for (int k = 0; k < OMAX; ++k) {
+        const int eidx = c.tid + k * NCT;
+        if (eidx < G * HD) {
+            const int h = eidx / HD, i = eidx % HD;
+            const float *src = p.apart + (((size_t)l * g.Hq + hq0 + h) * p.max_split) * (HD + 2);
+            float M = -INFINITY;
+            for (int cc = 0; cc < sp.n_split; ++cc) M = fmaxf(M, __ldcg(src + (size_t)cc * (HD + 2) + HD));
+            float num = 0.f, den = 0.f;
+            for (int cc = 0; cc < sp.n_split; ++cc) {
+                const float *pc = src + (size_t)cc * (HD + 2);
+                const float wgt = expf(__ldcg(pc + HD) - M);
+                num = fmaf(wgt, __ldcg(pc + i), num);
+                den = fmaf(wgt, __ldcg(pc + HD + 1), den);
+            }
+            p.attn[(size_t)l * g.Q + (size_t)(hq0 + h) * HD + i] = num / den;
+        }
+    }
+    return cons_publish(c, layer_cnt(p, l, C_ATTN), true, nullptr, ab);
+}
+
+// ---------------------------------------------------------------- LM head selection
+
+// k-th largest of n distinct 64-bit keys (k >= 1, k <= n), by an 8-pass
+// most-significant-digit radix select over the consumer threads.  `keys`
+// may be shared or global memory; stride/width describe a [rows][stride]
+// array of which the first `width` entries of each row are used.
+__device__ bool radix_select(const Ctx &c, const unsigned long long *keys, int rows, int stride, int width, int k,
+                             bool global_mem, unsigned long long &tau, bool ab)
+{
+    unsigned long long prefix = 0ull, mask = 0ull;
+    unsigned remain = (unsigned)k;
+    const int n = rows * width;
+    for (int pass = 0; pass < 8; ++pass) {
+        const int shift = 56 - 8 * pass;
+        for (int i = c.tid; i < 256; i += NCT) c.hist[i] = 0u;
+        if (cons_sync_or(ab)) return true;
+        for (int i = c.tid; i < n; i += NCT) {
+            const int r = i / width, j = i % width;
+            const unsigned long long key = global_mem ? __ldcg(keys + (size_t)r * stride + j) : keys[(size_t)r * stride + j];
+            if ((key & mask) == prefix) atomicAdd(&c.hist[(key >> shift) & 255u], 1u);
+        }
+        if (cons_sync_or(ab)) return true;
+        if (c.warp == 0) {
+            // lane L covers bins 255-8L .. 248-8L (high to low)
+            unsigned cnt[8];
+            unsigned tot = 0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                cnt[q] = c.hist[255 - 8 * c.lane - q];
+                tot += cnt[q];
+            }
+            unsigned incl = tot;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                unsigned v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (c.lane >= o) incl += v;
+            }
+            const unsigned excl = incl - tot;
+            if (excl < remain && remain <= incl) {
+                unsigned cum = excl;
+                for (int q = 0; q < 8; ++q) {
+                    if (cum + cnt[q] >= remain) {
+                        c.misc[M_DIGIT] = 255u - 8u * c.lane - q;
+                        c.misc[M_REMAIN] = remain - cum;
+                        break;
+                    }
+                    cum += cnt[q];
+                }
+            }
+        }
+        if (cons_sync_or(ab)) return true;
+        const unsigned digit = c.misc[M_DIGIT];
+        remain = c.misc[M_REMAIN];
+        prefix |= (unsigned long long)digit << shift;
+        mask |= 0xFFull << shift;
+    }
+    tau = prefix;
+    return false;
+}
+
+__device__ bool stage_lm_sample(const Ctx &c, ConsRing &rc, int step, bool ab)
+{
+    const Params &p = *c.p;
+    const Geo &g = p.g;
+    const CtaPlan &pl = p.plans[c.b];
+    const int pos = p.pos0 + step;
+    ab = stage_gemv(c, rc, ST_LM, g.L - 1, step, ab);
+    if (cons_sync_or(ab)) return true;
+
+    const bool greedy = !(p.temperature > 0.f) || p.top_k == 1;
+    const bool all_vocab = !greedy && (p.top_k <= 0 || p.top_k >= g.V);
+    const int nloc = pl.u1[ST_LM] - pl.u0[ST_LM];
+    unsigned long long *part = p.lm_part + (size_t)c.b * MAX_TOPK;
+    if (greedy || all_vocab) {
+        unsigned long long best = 0ull;
+        for (int i = c.tid; i < nloc; i += NCT) best = c.lmkeys[i] > best ? c.lmkeys[i] : best;
+        best = warp_max_u64(best);
+        if (c.lane == 0) reinterpret_cast<unsigned long long *>(c.red)[c.warp] = best;
+        if (cons_sync_or(ab)) return true;
+        if (c.tid == 0) {
+            unsigned long long m = 0ull;
+            for (int w = 0; w < NCW; ++w) {
+                unsigned long long v = reinterpret_cast<unsigned long long *>(c.red)[w];
+                m = v > m ? v : m;
+            }
+            part[0] = m;
+        }
+    } else {
+        const int k = p.top_k;
+        const int kloc = min(k, nloc);
+        unsigned long long tau;
+        if (radix_select(c, c.lmkeys, 1, nloc, nloc, kloc, false, tau, ab)) return true;
+        if (c.tid == 0) c.misc[M_FLAG] = 0u;
+        if (cons_sync_or(ab)) return true;
+        for (int i = c.tid; i < nloc; i += NCT) {
+            const unsigned long long key = c.lmkeys[i];
+            if (key >= tau) part[atomicAdd(&c.misc[M_FLAG], 1u)] = key;
+        }
+        for (int j = kloc + c.tid; j < k; j += NCT) part[j] = 0ull;
+    }
+    if (cons_sync_or(ab)) return true;
+    if (c.tid == 0) {
+        fence_acq_rel_gpu();
+        const unsigned old = atom_add_acq_rel(p.lm_done, 1u);
+        c.misc[M_FLAG] = (old == (unsigned)p.P - 1u) ? 1u : 0u;
+    }
+    if (cons_sync_or(ab)) return true;
+    const bool last = c.misc[M_FLAG] != 0u;
+    if (last) {
+        if (c.tid == 0) st_relaxed(p.lm_done, 0u);
+        unsigned long long best = 0ull;
+        if (greedy || all_vocab) {
+            for (int i = c.tid; i < p.P; i += NCT) {
+                const unsigned long long v = __ldcg(p.lm_part + (size_t)i * MAX_TOPK);
+                best = v > best ? v : best;
+            }
+        } else {
+            const int k = p.top_k;
+            unsigned long long tau;
+            if (radix_select(c, p.lm_part, p.P, MAX_TOPK, k, k, true, tau, ab)) return true;
+            for (int i = c.tid; i < p.P * k; i += NCT) {
+                const unsigned long long key = __ldcg(p.lm_part + (size_t)(i / k) * MAX_TOPK + (i % k));
+                if (key >= tau) {
+                    const int idx = sel_key_index(key);
+                    const float score = sel_key_value(key) / p.temperature + gumbel_dev(p.seed, pos, idx);
+                    const unsigned long long sk = sel_key(score, idx);
+                    best = sk > best ? sk : best;
+                }
+            }
+        }
+        best = warp_max_u64(best);
+        if (c.lane == 0) reinterpret_cast<unsigned long long *>(c.red)[c.warp] = best;
+        if (cons_sync_or(ab)) return true;
+        if (c.tid == 0) {
+            unsigned long long m = 0ull;
+            for (int w = 0; w < NCW; ++w) {
+                unsigned long long v = reinterpret_cast<unsigned long long *>(c.red)[w];
+                m = v > m ? v : m;
+            }
+            const int tok = sel_key_index(m);
+            p.out_tokens[step] = tok;
+            const int next = p.force_tokens ? __ldg(p.force_tokens + step) : tok;
+            p.tok_seq[step] = next;
+            if (step == p.n_steps - 1) p.tok_buf[0] = next;
+            fence_acq_rel_gpu();
+            red_release_add(p.tok_cnt, 1u);
+        }
+    }
+    if (p.sched == SCHED_GRID) {
+        if (cons_sync_or(ab)) return true;
+        if (c.tid == 0) red_release_add(p.gbar, 1u);
+    }
+    return cons_sync_or(ab);
+}
+
+// ---------------------------------------------------------------- consumer
+
+__device__ void consumer(const Ctx &c)
+{
+    const Params &p = *c.p;
+    const Geo &g = p.g;
+    ConsRing rc;
+    const bool ab = false;
+    const bool grid = p.sched == SCHED_GRID;
+    const bool decode = p.mode == MODE_DECODE;
+    for (int step = 0; step < p.n_steps; ++step) {
+        const unsigned e = p.epoch0 + (unsigned)step;
+        // decode: the input token of step > 0 is the previous step's choice
+        if (decode && step > 0 && p.sched == SCHED_FLAGS && stage_active(p, 0, SID_QKV)) {
+            if (cons_wait(c, p.tok_cnt, p.tok_base + (unsigned)step, 200, 0, step, ab)) return;
+        }
+        for (int l = 0; l < g.L; ++l) {
+            if (stage_active(p, l, SID_QKV)) {
+                // QKV(l) reads x_out(l-1), or for l = 0 the embedding of the step's token
+                int gstep = step, gl = l - 1, gslot = 4;
+                if (l == 0) {
+                    gstep = step - 1;
+                    gl = g.L - 1;
+                    gslot = step > 0 ? (decode ? 5 : 4) : -1;
+                }
+                if (stage_wait(c, l > 0 ? layer_cnt(p, l - 1, C_D) : nullptr, (e + 1u) * p.n_prod[ST_D], gstep, gl,
+                               gslot, step, l, 1, ab))
+                    return;
+                if (stage_gemv(c, rc, ST_QKV, l, step, ab)) return;
+                const bool withhold = decode && step == p.fault_step && l == 0;
+                if (cons_publish(c, layer_cnt(p, l, C_QKV), !withhold, (grid && !withhold) ? p.gbar : nullptr, ab))
+                    return;
+            }
+            if (stage_active(p, l, SID_ATTN)) {
+                if (stage_wait(c, layer_cnt(p, l, C_QKV), (e + 1u) * p.n_prod[ST_QKV], step, l, 0, step, l, 2, ab))
+                    return;
+                const int ctx = p.pos0 + step + 1;
+                const AttnSplit sp = attn_split(ctx, p.P, g.Hkv, p.attn_min_len);
+                const int U = g.Hkv * sp.n_split;
+                for (int u = attn_unit_first(c.b, l, U, p.P); u < U; u += p.P) {
+                    const int gkv = u / sp.n_split, cp = u % sp.n_split;
+                    const bool stop = (g.hd == 128) ? attn_piece<128>(c, rc, l, step, gkv, cp, sp, ab)
+                                                    : attn_piece<64>(c, rc, l, step, gkv, cp, sp, ab);
+                    if (stop) return;
+                }
+                if (grid && cons_publish(c, nullptr, false, p.gbar, ab)) return;
+            }
+            if (stage_active(p, l, SID_O)) {
+                if (stage_wait(c, layer_cnt(p, l, C_ATTN), (e + 1u) * (unsigned)g.Hkv, step, l, 1, step, l, 3, ab))
+                    return;
+                if (stage_gemv(c, rc, ST_O, l, step, ab)) return;
+                if (cons_publish(c, layer_cnt(p, l, C_O), true, grid ? p.gbar : nullptr, ab)) return;
+            }
+            if (stage_active(p, l, SID_GU)) {
+                if (stage_wait(c, layer_cnt(p, l, C_O), (e + 1u) * p.n_prod[ST_O], step, l, 2, step, l, 4, ab))
+                    return;
+                if (stage_gemv(c, rc, ST_GU, l, step, ab)) return;
+                if (cons_publish(c, layer_cnt(p, l, C_GU), true, grid ? p.gbar : nullptr, ab)) return;
+            }
+            if (stage_active(p, l, SID_D)) {
+                if (stage_wait(c, layer_cnt(p, l, C_GU), (e + 1u) * p.n_prod[ST_GU], step, l, 3, step, l, 5, ab))
+                    return;
+                if (stage_gemv(c, rc, ST_D, l, step, ab)) return;
+                if (cons_publish(c, layer_cnt(p, l, C_D), true, grid ? p.gbar : nullptr, ab)) return;
+            }
+        }
+        if (decode && stage_active(p, 0, SID_LM)) {
+            if (stage_wait(c, layer_cnt(p, g.L - 1, C_D), (e + 1u) * p.n_prod[ST_D], step, g.L - 1, 4, step, g.L - 1,
+                           6, ab))
+                return;
+            if (stage_lm_sample(c, rc, step, ab)) return;
+        }
+    }
+}
+
+// ---------------------------------------------------------------- producer
+
+__device__ bool produce_tiles(const Ctx &c, ProdRing &pr, int s, int l)
+{
+    const Params &p = *c.p;
+    const CtaPlan &pl = p.plans[c.b];
+    const StageGeom sg = stage_geom(p.g, s);
+    const int u0 = pl.u0[s], n = pl.u1[s] - u0;
+    const int nt = tiles_of(n, sg.rows_per_unit);
+    const uint8_t *src = p.wstream + pl.base +
+                         (s == ST_LM ? pl.lm_off : (unsigned long long)l * pl.layer_bytes + pl.stage_off[s]);
+    const int nkc = sg.K / KC;
+    for (int t = 0; t < nt; ++t) {
+        int a, bnd;
+        tile_range(u0, n, nt, t, a, bnd);
+        const unsigned bytes = (unsigned)((bnd - a) * sg.rows_per_unit) * KC_BYTES;
+        for (int kc = 0; kc < nkc; ++kc) {
+            if (!pr.emit(c, src, bytes)) return false;
+            src += bytes;
+        }
+    }
+    return true;
+}
+
+__device__ void producer(const Ctx &c)
+{
+    const Params &p = *c.p;
+    const Geo &g = p.g;
+    ProdRing pr;
+    pr.pol = policy_evict_first();
+    pr.pol_kv = policy_evict_normal();
+    bool ok = true;
+    for (int step = 0; step < p.n_steps && ok; ++step) {
+        const unsigned e = p.epoch0 + (unsigned)step;
+        const int pos = p.pos0 + step;
+        for (int l = 0; l < g.L && ok; ++l) {
+            if (stage_active(p, l, SID_QKV)) ok = produce_tiles(c, pr, ST_QKV, l);
+            if (ok && stage_active(p, l, SID_ATTN)) {
+                const AttnSplit sp = attn_split(pos + 1, p.P, g.Hkv, p.attn_min_len);
+                const int U = g.Hkv * sp.n_split;
+                const int S = attn_sub_positions(g.hd);
+                bool guarded = (step == 0);
+                for (int u = attn_unit_first(c.b, l, U, p.P); u < U && ok; u += p.P) {
+                    const int gkv = u / sp.n_split, cp = u % sp.n_split;
+                    const int j0 = cp * sp.per;
+                    const int jr = min(min(j0 + sp.per, pos + 1), pos);
+                    if (jr > j0 && !guarded) {
+                        // positions < pos of step > 0 were written by the previous step's QKV stage
+                        ok = wait_counter(p, layer_cnt(p, l, C_QKV), e * p.n_prod[ST_QKV], 102, l, step);
+                        fence_proxy_async_global();
+                        guarded = true;
+                    }
+                    const size_t base = (((size_t)l * g.Hkv + gkv) * g.max_seq) * g.hd;
+                    for (int jb = j0; jb < jr && ok; jb += S) {
+                        const int nb = min(S, jr - jb);
+                        const unsigned hb = (unsigned)nb * g.hd * 2u;
+                        ok = pr.emit2(c, p.kc + base + (size_t)jb * g.hd, p.vc + base + (size_t)jb * g.hd, hb);
+                    }
+                }
+            }
+            if (ok && stage_active(p, l, SID_O)) ok = produce_tiles(c, pr, ST_O, l);
+            if (ok && stage_active(p, l, SID_GU)) ok = produce_tiles(c, pr, ST_GU, l);
+            if (ok && stage_active(p, l, SID_D)) ok = produce_tiles(c, pr, ST_D, l);
+        }
+        if (ok && p.mode == MODE_DECODE && stage_active(p, 0, SID_LM)) ok = produce_tiles(c, pr, ST_LM, 0);
+    }
+    if (!ok) pr.drain(c);
+}
+
+// ---------------------------------------------------------------- kernel
+
+__global__ void __launch_bounds__(NTHREADS, 1) lf_monokernel(const __grid_constant__ Params p)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    const SmemLayout L = smem_layout(p.ring_bytes, p.act_floats, p.lm_rows_max);
+    Ctx c;
+    c.p = &p;
+    c.ring = smem + L.ring;
+    c.act = reinterpret_cast<float *>(smem + L.act);
+    c.lmkeys = reinterpret_cast<unsigned long long *>(smem + L.lmkeys);
+    c.res = reinterpret_cast<float *>(smem + L.res);
+    c.full = reinterpret_cast<uint64_t *>(smem + L.full);
+    c.empty = reinterpret_cast<uint64_t *>(smem + L.empty);
+    c.chunk_end = reinterpret_cast<unsigned long long *>(smem + L.chunk_end);
+    c.red = reinterpret_cast<float *>(smem + L.red);
+    c.hist = reinterpret_cast<unsigned *>(smem + L.hist);
+    c.misc = reinterpret_cast<unsigned *>(smem + L.misc);
+    c.b = blockIdx.x;
+    c.tid = threadIdx.x;
+    c.warp = threadIdx.x >> 5;
+    c.lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < TICKETS; ++i) {
+            mbar_init(&c.full[i], 1);
+            mbar_init(&c.empty[i], NCW);
+        }
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (c.warp == NCW) {
+        if (c.lane == 0) producer(c);
+        return;
+    }
+    consumer(c);
+}
+
+// ---------------------------------------------------------------- repack
+
+// Copy the caller's weights into the per-CTA streams, using the same tile
+// enumeration as the producer.  One block per CTA stream.
+struct RepackSrc {
+    const __half *wq, *wk, *wv, *wo, *wg, *wu, *wd, *head;
+};
+
+__device__ const __half *src_row(const Geo &g, const RepackSrc &w, int s, int l, int unit, int part)
+{
+    switch (s) {
+    case ST_QKV: {
+        const int half = g.hd / 2;
+        const int hh = unit / half, j = unit % half;
+        const int r = hh * g.hd + j + part * half;  // row of the fused [q; k; v] space
+        if (r < g.Q) return w.wq + ((size_t)l * g.Q + r) * g.d;
+        if (r < g.Q + g.KV) return w.wk + ((size_t)l * g.KV + (r - g.Q)) * g.d;
+        return w.wv + ((size_t)l * g.KV + (r - g.Q - g.KV)) * g.d;
+    }
+    case ST_O: return w.wo + ((size_t)l * g.d + unit) * g.Q;
+    case ST_GU: return (part ? w.wu : w.wg) + ((size_t)l * g.F + unit) * g.d;
+    case ST_D: return w.wd + ((size_t)l * g.d + unit) * g.F;
+    default: return w.head + (size_t)unit * g.d;
+    }
+}
+
+__global__ void lf_repack_kernel(Geo g, const CtaPlan *plans, RepackSrc w, uint8_t *dst)
+{
+    const CtaPlan pl = plans[blockIdx.x];
+    for (int l = 0; l < g.L + 1; ++l) {
+        const int s_lo = (l < g.L) ? ST_QKV : ST_LM;
+        const int s_hi = (l < g.L) ? ST_D : ST_LM;
+        for (int s = s_lo; s <= s_hi; ++s) {
+            const StageGeom sg = stage_geom(g, s);
+            const int u0 = pl.u0[s], n = pl.u1[s] - u0;
+            const int nt = tiles_of(n, sg.rows_per_unit);
+            uint8_t *out = dst + pl.base + (s == ST_LM ? pl.lm_off : (unsigned long long)l * pl.layer_bytes + pl.stage_off[s]);
+            const int nkc = sg.K / KC;
+            for (int t = 0; t < nt; ++t) {
+                int a, bnd;
+                tile_range(u0, n, nt, t, a, bnd);
+                const int nu = bnd - a;
+                const int R = nu * sg.rows_per_unit;
+                for (int kc = 0; kc < nkc; ++kc) {
+                    // chunk: R rows x 256 columns, stored row r -> (unit a + r % nu, part r / nu)
+                    for (int q = threadIdx.x; q < R * 32; q += blockDim.x) {
+                        const int r = q / 32, seg = q % 32;
+                        const int unit = a + (sg.rows_per_unit == 2 ? r % nu : r);
+                        const int part = sg.rows_per_unit == 2 ? r / nu : 0;
+                        const uint4 *srow = reinterpret_cast<const uint4 *>(src_row(g, w, s, l < g.L ? l : 0, unit, part) +
+                                                                            (size_t)kc * KC);
+                        reinterpret_cast<uint4 *>(out)[q] = srow[seg];
+                    }
+                    out += (size_t)R * KC_BYTES;
+                }
+            }
+        }
+    }
+}
+
+}  // namespace lfk
+
+// ---------------------------------------------------------------- launch hooks used by lf_api.cu
+
+extern "C" cudaError_t lfk_set_smem(int smem_bytes)
+{
+    return cudaFuncSetAttribute(lfk::lf_monokernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+}
+
+extern "C" cudaError_t lfk_launch_monokernel(const lfk::Params *p, int smem_bytes, cudaStream_t stream,
+                                             int cooperative)
+{
+    void *args[] = {const_cast<lfk::Params *>(p)};
+    if (cooperative)
+        return cudaLaunchCooperativeKernel((const void *)lfk::lf_monokernel, dim3(p->P), dim3(lfk::NTHREADS), args,
+                                           (size_t)smem_bytes, stream);
+    return cudaLaunchKernel((const void *)lfk::lf_monokernel, dim3(p->P), dim3(lfk::NTHREADS), args,
+                            (size_t)smem_bytes, stream);
+}
+
+extern "C" cudaError_t lfk_occupancy(int smem_bytes, int *blocks_per_sm)
+{
+    cudaError_t e = lfk_set_smem(smem_bytes);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, lfk::lf_monokernel, lfk::NTHREADS,
+                                                        (size_t)smem_bytes);
+}
+
+extern "C" unsigned lfk_smem_bytes(int ring_bytes, int act_floats, int lm_rows_max)
+{
+    return lfk::smem_layout(ring_bytes, act_floats, lm_rows_max).total;
+}
+
+extern "C" cudaError_t lfk_launch_repack(lfk::Geo g, int P, const lfk::CtaPlan *plans, const void *wq, const void *wk,
+                                         const void *wv, const void *wo, const void *wg, const void *wu,
+                                         const void *wd, const void *head, void *dst, cudaStream_t stream)
+{
+    lfk::RepackSrc w{(const __half *)wq, (const __half *)wk, (const __half *)wv, (const __half *)wo,
+                     (const __half *)wg, (const __half *)wu, (const __half *)wd, (const __half *)head};
+    lfk::lf_repack_kernel<<<P, 256, 0, stream>>>(g, plans, w, (uint8_t *)dst);
+    return cudaGetLastError();
+}

@@ -1,0 +1,71 @@
+"""The C-ABI library loads and exports every symbol include/lf.h declares;
+host-side argument checks (no GPU needed, no compute call)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "lf.h")
+
+
+def _declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"LF_API\s+[\w\s\*]*?\b(lf_\w+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def pm():
+    import persistent_monokernel_gb300 as pm
+    from persistent_monokernel_gb300 import build
+    build.build()
+    return pm
+
+
+def test_header_declares_the_public_entry_points():
+    syms = _declared_symbols()
+    for name in ("lf_create", "lf_prefill", "lf_decode", "lf_destroy", "lf_sync", "lf_reset"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(pm):
+    L = pm.lib()
+    for name in _declared_symbols():
+        assert hasattr(L, name), name
+    assert set(pm.EXPORTS) == set(_declared_symbols())
+
+
+def test_abi_version_and_error_strings(pm):
+    assert pm.lib().lf_abi_version() == 1
+    for code, name in pm.STATUS_NAMES.items():
+        assert pm.error_string(code).startswith(name)
+
+
+def test_create_rejects_bad_arguments_before_touching_the_gpu(pm):
+    L = pm.lib()
+    h = C.c_void_p()
+    w = pm.lf_weights(*([0x1000] * 12))
+    assert L.lf_create(None, C.byref(w), C.byref(h)) == 1
+    good = dict(n_layers=2, d_model=256, n_heads=4, n_kv_heads=4, head_dim=64, ffn_dim=1024, vocab=4096,
+                max_seq=64, rope_theta=10000.0, rms_eps=1e-5, wait_timeout_ns=0, n_ctas=0, fault_step=-1)
+    cases = [(dict(head_dim=96), 7), (dict(n_kv_heads=3), 7), (dict(d_model=300), 7), (dict(ffn_dim=1000), 7),
+             (dict(n_layers=0), 1), (dict(max_seq=0), 1), (dict(n_heads=64, n_kv_heads=4), 7)]
+    for change, expect in cases:
+        cfg = pm.lf_config(**{**good, **change})
+        assert L.lf_create(C.byref(cfg), C.byref(w), C.byref(h)) == expect, change
+    wnull = pm.lf_weights(*([0x1000] * 11 + [0]))
+    cfg = pm.lf_config(**good)
+    assert L.lf_create(C.byref(cfg), C.byref(wnull), C.byref(h)) == 1
+
+
+def test_calls_on_a_null_handle_are_rejected(pm):
+    L = pm.lib()
+    sp = pm.lf_sampling(0.0, 0, None, None)
+    assert L.lf_prefill(None, None, 4, None) == 1
+    assert L.lf_decode(None, 4, C.byref(sp), 0, None, None) == 1
+    assert L.lf_sync(None) == 1
+    assert L.lf_reset(None) == 1
+    assert L.lf_set_schedule(None, 0) == 1
+    L.lf_destroy(None)
