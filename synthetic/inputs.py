@@ -80,14 +80,16 @@ def hashed_indices(seed: int, tensor_id: int, layer: int, start: int, n: int, de
     return (h >> 16) & 0xFFFF
 
 
-_CHUNK = 1 << 20
+_CHUNK = 1 << 20        # CPU: keeps the int64 temporaries in cache
+_CHUNK_CUDA = 1 << 26   # GPU: few launches
 
 
 def _fill(out: torch.Tensor, table: torch.Tensor, seed: int, tensor_id: int, layer: int) -> None:
     flat = out.view(-1)
     n = flat.numel()
-    for s in range(0, n, _CHUNK):
-        m = min(_CHUNK, n - s)
+    chunk = _CHUNK_CUDA if flat.is_cuda else _CHUNK
+    for s in range(0, n, chunk):
+        m = min(chunk, n - s)
         idx = hashed_indices(seed, tensor_id, layer, s, m, flat.device)
         flat[s:s + m] = table[idx]
 
