@@ -209,6 +209,42 @@ LF_API lf_status lf_set_schedule(lf_handle *h, int32_t schedule);
 /* Fill *out with the handle's launch geometry and state. */
 LF_API lf_status lf_get_info(const lf_handle *h, lf_info *out);
 
+/* Size of the device array that lf_generate_noalloc uses as scratch. */
+#define LF_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* One whole request -- prefill of prompt_dev[0 .. n_prompt-1], then n_steps
+ * decode steps written to out_tokens_dev -- that makes no device allocation.
+ * The write-up these kernels follow has no counterpart of this entry point:
+ * it exists for callers that cannot call cudaMalloc when a request arrives,
+ * such as a plugin inside a host framework that owns every device allocation
+ * through its own pool, or a process whose device memory is reserved up front.
+ *
+ * cfg and w are as for lf_create, but nothing is copied: the kernels stream
+ * the projection matrices and the LM head straight from the caller's buffers
+ * (row-major, nn.Linear layout), so every buffer in w must stay valid until
+ * the call returns.  prompt_dev (device int32 [n_prompt]) and out_tokens_dev
+ * (device int32 [n_steps]) belong to the caller; sp works as for lf_decode.
+ * cfg->max_seq bounds n_prompt + n_steps; cfg->fault_step is ignored.
+ *
+ * All scratch -- partition, RoPE table, FP16 KV cache, activations, counters,
+ * attention partials, sampling candidates -- lives in one file-scope device
+ * array of LF_NOALLOC_SCRATCH_BYTES (8 MiB), which every GPU that loads the
+ * library holds until the process exits.  A request whose scratch would not
+ * fit (mainly the KV cache: 4 * n_layers * n_kv_heads * max_seq * head_dim
+ * bytes) is rejected with LF_ERR_CAPACITY before any work is queued.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) and sets the kernel's shared-memory limit; make that
+ * first call before any stream capture.  Every call reuses the same array and
+ * clears the counters it relies on; calls whose work overlaps on the GPU, or
+ * calls from two host threads at once, race on the array: serialise them.
+ * The call synchronizes `stream` and returns the device status (LF_OK,
+ * LF_ERR_TIMEOUT, or LF_ERR_INVALID_ARG for a token id outside [0, vocab)).
+ * Other errors: INVALID_ARG, NOT_SUPPORTED, CAPACITY, NOT_RESIDENT, CUDA. */
+LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_weights *w, const int32_t *prompt_dev,
+                                     int32_t n_prompt, int32_t n_steps, const lf_sampling *sp, uint64_t seed,
+                                     int32_t *out_tokens_dev, void *stream);
+
 /* Static string naming a status code. */
 LF_API const char *lf_error_string(lf_status s);
 

@@ -22,7 +22,7 @@ MAX_TOP_K = 64
 
 # Every symbol include/lf.h declares.
 EXPORTS = ("lf_create", "lf_destroy", "lf_prefill", "lf_decode", "lf_generate", "lf_sync", "lf_reset",
-           "lf_set_schedule", "lf_get_info", "lf_error_string", "lf_abi_version")
+           "lf_set_schedule", "lf_get_info", "lf_error_string", "lf_abi_version", "lf_generate_noalloc")
 
 
 class LFError(RuntimeError):
@@ -83,6 +83,9 @@ def lib() -> C.CDLL:
         L.lf_error_string.argtypes = [C.c_int]
         L.lf_error_string.restype = C.c_char_p
         L.lf_abi_version.restype = C.c_int32
+        L.lf_generate_noalloc.argtypes = [C.POINTER(lf_config), C.POINTER(lf_weights), vp, C.c_int32, C.c_int32,
+                                          C.POINTER(lf_sampling), C.c_uint64, vp, vp]
+        L.lf_generate_noalloc.restype = C.c_int
         for name in ("lf_create", "lf_prefill", "lf_decode", "lf_generate", "lf_sync", "lf_reset",
                      "lf_set_schedule", "lf_get_info"):
             getattr(L, name).restype = C.c_int

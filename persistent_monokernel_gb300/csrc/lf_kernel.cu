@@ -941,6 +941,30 @@ __device__ void consumer(const Ctx &c)
     }
 }
 
+// ---------------------------------------------------------------- caller-layout weight rows
+
+struct RepackSrc {
+    const __half *wq, *wk, *wv, *wo, *wg, *wu, *wd, *head;
+};
+
+__device__ const __half *src_row(const Geo &g, const RepackSrc &w, int s, int l, int unit, int part)
+{
+    switch (s) {
+    case ST_QKV: {
+        const int half = g.hd / 2;
+        const int hh = unit / half, j = unit % half;
+        const int r = hh * g.hd + j + part * half;  // row of the fused [q; k; v] space
+        if (r < g.Q) return w.wq + ((size_t)l * g.Q + r) * g.d;
+        if (r < g.Q + g.KV) return w.wk + ((size_t)l * g.KV + (r - g.Q)) * g.d;
+        return w.wv + ((size_t)l * g.KV + (r - g.Q - g.KV)) * g.d;
+    }
+    case ST_O: return w.wo + ((size_t)l * g.d + unit) * g.Q;
+    case ST_GU: return (part ? w.wu : w.wg) + ((size_t)l * g.F + unit) * g.d;
+    case ST_D: return w.wd + ((size_t)l * g.d + unit) * g.F;
+    default: return w.head + (size_t)unit * g.d;
+    }
+}
+
 // ---------------------------------------------------------------- producer
 
 __device__ bool produce_tiles(const Ctx &c, ProdRing &pr, int s, int l)
@@ -965,11 +989,49 @@ __device__ bool produce_tiles(const Ctx &c, ProdRing &pr, int s, int l)
     return true;
 }
 
-__device__ void producer(const Ctx &c)
+// Producer variant used by lf_generate_noalloc, whose weights stay in the
+// caller's row-major layout: each chunk (R rows x 256 columns) is gathered with
+// one 512-byte bulk copy per row segment into the same ring layout.
+__device__ bool produce_tiles_direct(const Ctx &c, ProdRing &pr, const RepackSrc &w, int s, int l)
+{
+    const Params &p = *c.p;
+    const CtaPlan &pl = p.plans[c.b];
+    const StageGeom sg = stage_geom(p.g, s);
+    const int u0 = pl.u0[s], n = pl.u1[s] - u0;
+    const int nt = tiles_of(n, sg.rows_per_unit);
+    const int nkc = sg.K / KC;
+    for (int t = 0; t < nt; ++t) {
+        int a, bnd;
+        tile_range(u0, n, nt, t, a, bnd);
+        const int nu = bnd - a;
+        const int R = nu * sg.rows_per_unit;
+        for (int kc = 0; kc < nkc; ++kc) {
+            const int o = pr.reserve(c, (unsigned)R * KC_BYTES);
+            if (o < 0) return false;
+            uint64_t *bar = &c.full[pr.n % TICKETS];
+            mbar_arrive_expect_tx(bar, (unsigned)R * KC_BYTES);
+            for (int r = 0; r < R; ++r) {
+                const int unit = a + (sg.rows_per_unit == 2 ? r % nu : r);
+                const int part = sg.rows_per_unit == 2 ? r / nu : 0;
+                const __half *src = src_row(p.g, w, s, l, unit, part) + (size_t)kc * KC;
+                bulk_g2s(c.ring + o + r * KC_BYTES, src, KC_BYTES, bar, pr.pol);
+            }
+            ++pr.n;
+        }
+    }
+    return true;
+}
+
+template <bool kDirect>
+__device__ void producer(const Ctx &c, const RepackSrc *w)
 {
     const Params &p = *c.p;
     const Geo &g = p.g;
     ProdRing pr;
+    auto tiles = [](const Ctx &cc, ProdRing &r, const RepackSrc *ws, int s, int l) {
+        if constexpr (kDirect) return produce_tiles_direct(cc, r, *ws, s, l);
+        else return produce_tiles(cc, r, s, l);
+    };
     pr.pol = policy_evict_first();
     pr.pol_kv = policy_evict_normal();
     bool ok = true;
@@ -977,7 +1039,7 @@ __device__ void producer(const Ctx &c)
         const unsigned e = p.epoch0 + (unsigned)step;
         const int pos = p.pos0 + step;
         for (int l = 0; l < g.L && ok; ++l) {
-            if (stage_active(p, l, SID_QKV)) ok = produce_tiles(c, pr, ST_QKV, l);
+            if (stage_active(p, l, SID_QKV)) ok = tiles(c, pr, w, ST_QKV, l);
             if (ok && stage_active(p, l, SID_ATTN)) {
                 const AttnSplit sp = attn_split(pos + 1, p.P, g.Hkv, p.attn_min_len);
                 const int U = g.Hkv * sp.n_split;
@@ -1001,18 +1063,19 @@ __device__ void producer(const Ctx &c)
                     }
                 }
             }
-            if (ok && stage_active(p, l, SID_O)) ok = produce_tiles(c, pr, ST_O, l);
-            if (ok && stage_active(p, l, SID_GU)) ok = produce_tiles(c, pr, ST_GU, l);
-            if (ok && stage_active(p, l, SID_D)) ok = produce_tiles(c, pr, ST_D, l);
+            if (ok && stage_active(p, l, SID_O)) ok = tiles(c, pr, w, ST_O, l);
+            if (ok && stage_active(p, l, SID_GU)) ok = tiles(c, pr, w, ST_GU, l);
+            if (ok && stage_active(p, l, SID_D)) ok = tiles(c, pr, w, ST_D, l);
         }
-        if (ok && p.mode == MODE_DECODE && stage_active(p, 0, SID_LM)) ok = produce_tiles(c, pr, ST_LM, 0);
+        if (ok && p.mode == MODE_DECODE && stage_active(p, 0, SID_LM)) ok = tiles(c, pr, w, ST_LM, 0);
     }
     if (!ok) pr.drain(c);
 }
 
 // ---------------------------------------------------------------- kernel
 
-__global__ void __launch_bounds__(NTHREADS, 1) lf_monokernel(const __grid_constant__ Params p)
+template <bool kDirect>
+__device__ __forceinline__ void monokernel_body(const Params &p, const RepackSrc *w)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     const SmemLayout L = smem_layout(p.ring_bytes, p.act_floats, p.lm_rows_max);
@@ -1041,38 +1104,28 @@ __global__ void __launch_bounds__(NTHREADS, 1) lf_monokernel(const __grid_consta
     }
     __syncthreads();
     if (c.warp == NCW) {
-        if (c.lane == 0) producer(c);
+        if (c.lane == 0) producer<kDirect>(c, w);
         return;
     }
     consumer(c);
+}
+
+__global__ void __launch_bounds__(NTHREADS, 1) lf_monokernel(const __grid_constant__ Params p)
+{
+    monokernel_body<false>(p, nullptr);
+}
+
+// Same kernel, streaming weights from the caller's layout (lf_generate_noalloc).
+__global__ void __launch_bounds__(NTHREADS, 1) lf_monokernel_direct(const __grid_constant__ Params p,
+                                                                   const __grid_constant__ RepackSrc w)
+{
+    monokernel_body<true>(p, &w);
 }
 
 // ---------------------------------------------------------------- repack
 
 // Copy the caller's weights into the per-CTA streams, using the same tile
 // enumeration as the producer.  One block per CTA stream.
-struct RepackSrc {
-    const __half *wq, *wk, *wv, *wo, *wg, *wu, *wd, *head;
-};
-
-__device__ const __half *src_row(const Geo &g, const RepackSrc &w, int s, int l, int unit, int part)
-{
-    switch (s) {
-    case ST_QKV: {
-        const int half = g.hd / 2;
-        const int hh = unit / half, j = unit % half;
-        const int r = hh * g.hd + j + part * half;  // row of the fused [q; k; v] space
-        if (r < g.Q) return w.wq + ((size_t)l * g.Q + r) * g.d;
-        if (r < g.Q + g.KV) return w.wk + ((size_t)l * g.KV + (r - g.Q)) * g.d;
-        return w.wv + ((size_t)l * g.KV + (r - g.Q - g.KV)) * g.d;
-    }
-    case ST_O: return w.wo + ((size_t)l * g.d + unit) * g.Q;
-    case ST_GU: return (part ? w.wu : w.wg) + ((size_t)l * g.F + unit) * g.d;
-    case ST_D: return w.wd + ((size_t)l * g.d + unit) * g.F;
-    default: return w.head + (size_t)unit * g.d;
-    }
-}
-
 __global__ void lf_repack_kernel(Geo g, const CtaPlan *plans, RepackSrc w, uint8_t *dst)
 {
     const CtaPlan pl = plans[blockIdx.x];
@@ -1148,4 +1201,21 @@ extern "C" cudaError_t lfk_launch_repack(lfk::Geo g, int P, const lfk::CtaPlan *
                      (const __half *)wg, (const __half *)wu, (const __half *)wd, (const __half *)head};
     lfk::lf_repack_kernel<<<P, 256, 0, stream>>>(g, plans, w, (uint8_t *)dst);
     return cudaGetLastError();
+}
+
+extern "C" cudaError_t lfk_set_smem_direct(int smem_bytes)
+{
+    return cudaFuncSetAttribute(lfk::lf_monokernel_direct, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+}
+
+extern "C" cudaError_t lfk_launch_monokernel_direct(const lfk::Params *p, const void *wq, const void *wk,
+                                                    const void *wv, const void *wo, const void *wg, const void *wu,
+                                                    const void *wd, const void *head, int smem_bytes,
+                                                    cudaStream_t stream)
+{
+    lfk::RepackSrc w{(const __half *)wq, (const __half *)wk, (const __half *)wv, (const __half *)wo,
+                     (const __half *)wg, (const __half *)wu, (const __half *)wd, (const __half *)head};
+    void *args[] = {const_cast<lfk::Params *>(p), &w};
+    return cudaLaunchCooperativeKernel((const void *)lfk::lf_monokernel_direct, dim3(p->P), dim3(lfk::NTHREADS),
+                                       args, (size_t)smem_bytes, stream);
 }
