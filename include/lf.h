@@ -209,6 +209,20 @@ LF_API lf_status lf_set_schedule(lf_handle *h, int32_t schedule);
 /* Fill *out with the handle's launch geometry and state. */
 LF_API lf_status lf_get_info(const lf_handle *h, lf_info *out);
 
+/* Stage trace (profiling aid).  lf_enable_trace(h, n) makes every later
+ * lf_prefill / lf_decode launch of the persistent schedules record, for its
+ * first n steps, six %globaltimer stamps (ns) per (step, slot, CTA): [0] the
+ * stage was entered, [1] its inputs were ready, [2] its inputs were loaded,
+ * [3] it was published, [4] GEMV: first tile done / attention: K/V positions
+ * done, [5] attention: piece partial published.  slot = 5 * layer + {0 QKV,
+ * 1 attention, 2 O, 3 gate/up, 4 down}; slot 5 * n_layers is the LM head and
+ * sampling.  Layout: [step][slot][cta][6] uint64, zero where nothing was
+ * recorded.  n = 0 disables tracing.  lf_read_trace synchronizes the device,
+ * sets *n_out to the number of words and, if host_out is not NULL, copies
+ * them there (capacity in words). */
+LF_API lf_status lf_enable_trace(lf_handle *h, int32_t max_steps);
+LF_API lf_status lf_read_trace(lf_handle *h, uint64_t *host_out, int64_t capacity, int64_t *n_out);
+
 /* Size of the device array that lf_generate_noalloc uses as scratch. */
 #define LF_NOALLOC_SCRATCH_BYTES (8u << 20)
 

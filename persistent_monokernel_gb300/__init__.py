@@ -19,10 +19,12 @@ STATUS_NAMES = {0: "LF_OK", 1: "LF_ERR_INVALID_ARG", 2: "LF_ERR_OUT_OF_MEMORY", 
                 8: "LF_ERR_STATE"}
 SCHED_FLAGS, SCHED_GRID_BARRIER, SCHED_MULTI_KERNEL = 0, 1, 2
 MAX_TOP_K = 64
+TRACE_STAMPS = 6
 
 # Every symbol include/lf.h declares.
 EXPORTS = ("lf_create", "lf_destroy", "lf_prefill", "lf_decode", "lf_generate", "lf_sync", "lf_reset",
-           "lf_set_schedule", "lf_get_info", "lf_error_string", "lf_abi_version", "lf_generate_noalloc")
+           "lf_set_schedule", "lf_get_info", "lf_error_string", "lf_abi_version", "lf_generate_noalloc",
+           "lf_enable_trace", "lf_read_trace")
 
 
 class LFError(RuntimeError):
@@ -86,6 +88,10 @@ def lib() -> C.CDLL:
         L.lf_generate_noalloc.argtypes = [C.POINTER(lf_config), C.POINTER(lf_weights), vp, C.c_int32, C.c_int32,
                                           C.POINTER(lf_sampling), C.c_uint64, vp, vp]
         L.lf_generate_noalloc.restype = C.c_int
+        L.lf_enable_trace.argtypes = [vp, C.c_int32]
+        L.lf_enable_trace.restype = C.c_int
+        L.lf_read_trace.argtypes = [vp, vp, C.c_int64, C.POINTER(C.c_int64)]
+        L.lf_read_trace.restype = C.c_int
         for name in ("lf_create", "lf_prefill", "lf_decode", "lf_generate", "lf_sync", "lf_reset",
                      "lf_set_schedule", "lf_get_info"):
             getattr(L, name).restype = C.c_int
@@ -191,6 +197,19 @@ class Decoder:
 
     def set_schedule(self, schedule: int) -> None:
         _check(lib().lf_set_schedule(self._h, int(schedule)), "lf_set_schedule")
+
+    def enable_trace(self, max_steps: int) -> None:
+        _check(lib().lf_enable_trace(self._h, int(max_steps)), "lf_enable_trace")
+
+    def read_trace(self):
+        """Stage trace as a uint64 array [steps, slots, ctas, 6] (ns stamps)."""
+        import numpy as np
+        n = C.c_int64()
+        _check(lib().lf_read_trace(self._h, None, 0, C.byref(n)), "lf_read_trace")
+        buf = np.zeros(n.value, dtype=np.uint64)
+        _check(lib().lf_read_trace(self._h, buf.ctypes.data, n.value, C.byref(n)), "lf_read_trace")
+        slots = 5 * self.model.n_layers + 1
+        return buf.reshape(-1, slots, self.info()["n_ctas"], TRACE_STAMPS)
 
     def info(self) -> dict:
         i = lf_info()

@@ -27,6 +27,17 @@ namespace {
 
 constexpr int kAttnMinLen = 32;         // fewest positions per split-KV piece
 constexpr long long kDefaultTimeoutNs = 2000000000LL;
+constexpr int kL2PrefetchKB = 0;        // weight-stream lookahead into L2 per CTA (measured: no gain)
+
+// Tuning override of the L2 lookahead, LF_L2_PREFETCH_KB (0 disables it).
+int l2_prefetch_bytes_from_env()
+{
+    const char *v = std::getenv("LF_L2_PREFETCH_KB");
+    long kb = v ? std::strtol(v, nullptr, 10) : kL2PrefetchKB;
+    if (kb < 0) kb = 0;
+    if (kb > 8192) kb = 8192;
+    return (int)kb * 1024;
+}
 
 }  // namespace
 
@@ -61,6 +72,11 @@ struct lf_handle {
     // lf_generate staging
     int32_t *stage_in = nullptr, *stage_out = nullptr;
     int stage_cap = 0;
+    // optional stage trace
+    unsigned long long *trace = nullptr;
+    int trace_steps = 0;
+    int l2_prefetch_bytes = 0;
+    int l2_prefetch_last = 0;
 };
 
 namespace {
@@ -75,7 +91,7 @@ void free_all(lf_handle *h)
 {
     void *ptrs[] = {h->d_plans, h->wstream, h->kc, h->vc, h->rope, h->qbuf, h->attn, h->xattn, h->hbuf,
                     h->xout, h->apart, h->counters, h->lm_part, h->tok_buf, h->tok_seq, h->status,
-                    h->stage_in, h->stage_out};
+                    h->stage_in, h->stage_out, h->trace};
     for (void *p : ptrs)
         if (p) cudaFree(p);
 }
@@ -95,19 +111,18 @@ lf_status validate_config(const lf_config &c)
         c.n_ctas < 0 || c.wait_timeout_ns < 0)
         return LF_ERR_INVALID_ARG;
     if (c.head_dim != 64 && c.head_dim != 128) return LF_ERR_NOT_SUPPORTED;
-    if (c.n_heads % c.n_kv_heads != 0 || c.n_heads / c.n_kv_heads > lfk::MAX_GROUP) return LF_ERR_NOT_SUPPORTED;
+    if (c.n_heads % c.n_kv_heads != 0 || lfk::MAX_GROUP % (c.n_heads / c.n_kv_heads) != 0) return LF_ERR_NOT_SUPPORTED;
     const long long Q = (long long)c.n_heads * c.head_dim;
     if (c.d_model % lfk::KC || Q % lfk::KC || c.ffn_dim % lfk::KC) return LF_ERR_NOT_SUPPORTED;
     return LF_OK;
 }
 
-// Attention scratch (floats) inside the activation region: q of a group,
-// scores and probabilities of one sub-block, three per-head vectors and the
-// staged fresh K/V row.
+// Attention scratch (floats) inside the activation region: q of the group
+// [G][hd], the staged fresh K and V rows (hd floats' worth of FP16) and the
+// eight warp states [NCW][hd + 2].
 int attn_scratch_floats(const lfk::Geo &g)
 {
-    const int S = lfk::attn_sub_positions(g.hd);
-    return g.group * g.hd + 2 * g.group * S + 3 * lfk::MAX_GROUP + g.hd;
+    return lfk::MAX_GROUP * g.hd + g.hd + lfk::NCW * (g.hd + 2);
 }
 
 lf_status launch(lf_handle *h, const lfk::Params &p, cudaStream_t stream)
@@ -164,6 +179,10 @@ lfk::Params base_params(lf_handle *h)
     p.sched = h->sched;
     p.only_layer = -1;
     p.only_stage = -1;
+    p.trace = h->trace;
+    p.trace_steps = h->trace_steps;
+    p.l2_prefetch_bytes = h->l2_prefetch_bytes;
+    p.l2_prefetch_last = h->l2_prefetch_last;
     return p;
 }
 
@@ -181,6 +200,7 @@ lf_status run_steps(lf_handle *h, lfk::Params p, cudaStream_t stream)
         q.epoch0 = p.epoch0 + (unsigned)i;
         q.tok_base = p.tok_base + (unsigned)i;
         q.fault_step = -1;
+        q.trace = nullptr;
         if (p.mode == lfk::MODE_PREFILL) {
             q.has_pending = (p.has_pending && i == 0) ? 1 : 0;
             q.prompt = p.prompt + (i - (p.has_pending ? 1 : 0));
@@ -244,6 +264,8 @@ lf_status lf_create(const lf_config *cfg, const lf_weights *w, lf_handle **out)
     lf_handle *h = new (std::nothrow) lf_handle();
     if (!h) return LF_ERR_OUT_OF_MEMORY;
     h->cfg = *cfg;
+    h->l2_prefetch_bytes = l2_prefetch_bytes_from_env();
+    h->l2_prefetch_last = std::getenv("LF_L2_PREFETCH_LAST") ? 1 : 0;
     lfk::Geo &g = h->g;
     g.L = cfg->n_layers;
     g.d = cfg->d_model;
@@ -302,6 +324,7 @@ lf_status lf_create(const lf_config *cfg, const lf_weights *w, lf_handle **out)
     h->lm_rows_max = lm_rows_max;
 
     // ---- shared memory: everything but the ring, then the largest ring that fits
+    h->max_split = std::max(1, P / g.Hkv);
     h->act_floats = std::max(std::max(g.d, g.Q), std::max(g.F, attn_scratch_floats(g)));
     h->act_floats = (h->act_floats + 3) / 4 * 4;
     const unsigned rest = lfk_smem_bytes(0, h->act_floats, lm_rows_max);
@@ -328,7 +351,6 @@ lf_status lf_create(const lf_config *cfg, const lf_weights *w, lf_handle **out)
     }
 
     // ---- allocations
-    h->max_split = std::max(1, P / g.Hkv);
     const size_t kv_elems = (size_t)g.L * g.Hkv * (size_t)g.max_seq * g.hd;
     const size_t n_layer_cnt = (size_t)g.L * lfk::N_LAYER_CNT;
     const size_t n_attn_done = (size_t)g.L * g.Hkv;
@@ -537,6 +559,39 @@ lf_status lf_generate(lf_handle *h, const int32_t *prompt_host, int32_t n_prompt
     e = cudaMemcpyAsync(out_host, h->stage_out, sizeof(int32_t) * n_steps, cudaMemcpyDeviceToHost, s);
     if (e != cudaSuccess) return from_cuda(e);
     return lf_sync(h);
+}
+
+}  // extern "C"
+
+extern "C" {
+
+lf_status lf_enable_trace(lf_handle *h, int32_t max_steps)
+{
+    if (!h || max_steps < 0) return LF_ERR_INVALID_ARG;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return from_cuda(e);
+    if (h->trace) cudaFree(h->trace);
+    h->trace = nullptr;
+    h->trace_steps = 0;
+    if (max_steps == 0) return LF_OK;
+    const size_t n = (size_t)max_steps * lfk::trace_slots(h->g.L) * h->P * lfk::TR_N;
+    e = dalloc(&h->trace, n);
+    if (e == cudaSuccess) e = cudaMemset(h->trace, 0, n * sizeof(unsigned long long));
+    if (e != cudaSuccess) return from_cuda(e);
+    h->trace_steps = max_steps;
+    return LF_OK;
+}
+
+lf_status lf_read_trace(lf_handle *h, uint64_t *host_out, int64_t capacity, int64_t *n_out)
+{
+    if (!h || !n_out) return LF_ERR_INVALID_ARG;
+    const size_t n = h->trace ? (size_t)h->trace_steps * lfk::trace_slots(h->g.L) * h->P * lfk::TR_N : 0;
+    *n_out = (int64_t)n;
+    if (!host_out) return LF_OK;
+    if (capacity < (int64_t)n) return LF_ERR_INVALID_ARG;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess && n) e = cudaMemcpy(host_out, h->trace, n * sizeof(uint64_t), cudaMemcpyDeviceToHost);
+    return from_cuda(e);
 }
 
 }  // extern "C"

@@ -12,8 +12,9 @@
 
 namespace lfk {
 
-constexpr int KC = 256;               // weight columns per streamed chunk
-constexpr int KC_BYTES = KC * 2;      // bytes of one row segment in a chunk
+constexpr int KC = 256;               // weight columns per column group (32 lanes x 8 FP16)
+constexpr int KC_BYTES = KC * 2;      // bytes of one row of one column group
+constexpr int CHUNK_MAX = 32768;      // largest streamed GEMV chunk (bytes)
 constexpr int TILE_ROWS = 32;         // rows of one GEMV tile (4 per consumer warp)
 constexpr int NCW = 8;                // consumer warps
 constexpr int NCT = NCW * 32;         // consumer threads
@@ -58,6 +59,17 @@ __host__ __device__ inline StageGeom stage_geom(const Geo &g, int s)
 }
 
 __host__ __device__ inline int units_per_tile(int rpu) { return TILE_ROWS / rpu; }
+// Column groups per streamed chunk of a tile with R rows and K columns: the
+// largest m in {8, 4, 2, 1} that divides K/256 and keeps R x 256m FP16 values
+// within CHUNK_MAX bytes.  Larger chunks amortise the per-chunk cost of the
+// ring (one TMA issue, one mbarrier round trip).
+__host__ __device__ inline int chunk_groups(int R, int K)
+{
+    const int ng = K / KC;
+    for (int m = 8; m > 1; m >>= 1)
+        if (ng % m == 0 && R * m * KC_BYTES <= CHUNK_MAX) return m;
+    return 1;
+}
 __host__ __device__ inline int tiles_of(int n_units, int rpu)
 {
     return n_units <= 0 ? 0 : ceil_div(n_units, units_per_tile(rpu));
@@ -97,7 +109,8 @@ __host__ __device__ inline int attn_sub_positions(int hd) { return ATT_CHUNK_BYT
 // Per-CTA plan: unit ranges of the five GEMV stages and the byte offsets of
 // this CTA's weight stream.  The stream of CTA b is laid out as
 //   [layer 0: QKV tiles | O tiles | GU tiles | D tiles] ... [layer L-1: ...] [LM-head tiles]
-// and each tile as K/256 chunks of (R rows x 256 columns), row-major inside a chunk.
+// and each tile as K/(256m) chunks of (R rows x 256m columns), row-major inside
+// a chunk, m = chunk_groups(R, K).
 struct CtaPlan {
     int u0[N_GEMV], u1[N_GEMV];
     unsigned long long base;          // byte offset of the stream in the repacked buffer
@@ -155,6 +168,19 @@ struct Params {
     int sched;
     // multi-kernel schedule: run only stage `only_stage` of layer `only_layer` of step 0
     int only_layer, only_stage;
+    // optional %globaltimer trace: [step][slot][cta][4] (slot = 5 * layer + stage, LM = 5 * L)
+    unsigned long long *trace;
+    int trace_steps;
+    // bytes of this CTA's weight stream kept in flight into L2 ahead of the ring (0 = off)
+    int l2_prefetch_bytes;
+    int l2_prefetch_last;        // 1: the lookahead marks lines evict-last, 0: evict-normal
 };
+
+// Trace stamps per (step, slot, CTA): stage entered, inputs ready, inputs
+// loaded, stage published, and two stage-specific points (GEMV: first chunk
+// acquired, last chunk released; attention: K/V positions done, piece partial
+// published).
+enum TraceStamp { TR_ENTER = 0, TR_READY = 1, TR_LOADED = 2, TR_DONE = 3, TR_X1 = 4, TR_X2 = 5, TR_N = 6 };
+__host__ __device__ inline int trace_slots(int L) { return 5 * L + 1; }
 
 }  // namespace lfk

@@ -92,6 +92,13 @@ __device__ __forceinline__ bool stage_active(const Params &p, int layer, int sid
     return p.only_stage == sid && (sid == SID_LM || p.only_layer == layer);
 }
 
+__device__ __forceinline__ void trace_mark(const Ctx &c, int step, int slot, int stamp)
+{
+    const Params &p = *c.p;
+    if (p.trace && c.tid == 0 && step < p.trace_steps)
+        p.trace[(((size_t)step * trace_slots(p.g.L) + slot) * p.P + c.b) * TR_N + stamp] = globaltimer_ns();
+}
+
 // ---------------------------------------------------------------- bounded waits
 
 __device__ __forceinline__ void raise_error(const Params &p, unsigned code, unsigned where, unsigned layer,
@@ -106,8 +113,10 @@ __device__ __forceinline__ void raise_error(const Params &p, unsigned code, unsi
 }
 
 // Spin until (int)(*ctr - target) >= 0.  Returns false on timeout or abort.
-__device__ bool wait_counter(const Params &p, const unsigned *ctr, unsigned target, unsigned where,
-                             unsigned layer, unsigned step)
+// The spin loops live out of line (one copy each) to keep the kernel's
+// executed code small; callers try once inline first.
+__device__ __forceinline__ bool wait_counter_slow(const Params &p, const unsigned *ctr, unsigned target, unsigned where,
+                                               unsigned layer, unsigned step)
 {
     unsigned long long t0 = 0;
     for (unsigned it = 0;; ++it) {
@@ -123,8 +132,14 @@ __device__ bool wait_counter(const Params &p, const unsigned *ctr, unsigned targ
         }
     }
 }
+__device__ __forceinline__ bool wait_counter(const Params &p, const unsigned *ctr, unsigned target, unsigned where,
+                                             unsigned layer, unsigned step)
+{
+    if ((int)(ld_acquire(ctr) - target) >= 0) return true;
+    return wait_counter_slow(p, ctr, target, where, layer, step);
+}
 
-__device__ bool wait_mbar(const Params &p, uint64_t *bar, unsigned parity, unsigned where)
+__device__ __forceinline__ bool wait_mbar_slow(const Params &p, uint64_t *bar, unsigned parity, unsigned where)
 {
     unsigned long long t0 = 0;
     for (unsigned it = 0;; ++it) {
@@ -140,6 +155,11 @@ __device__ bool wait_mbar(const Params &p, uint64_t *bar, unsigned parity, unsig
         }
     }
 }
+__device__ __forceinline__ bool wait_mbar(const Params &p, uint64_t *bar, unsigned parity, unsigned where)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_mbar_slow(p, bar, parity, where);
+}
 
 // ---------------------------------------------------------------- ring cursors
 
@@ -148,7 +168,7 @@ __device__ bool wait_mbar(const Params &p, uint64_t *bar, unsigned parity, unsig
 struct ConsRing {
     unsigned n = 0;    // chunks consumed
     unsigned off = 0;  // read offset
-    __device__ const uint8_t *acquire(const Ctx &c, unsigned bytes, bool &ab)
+    __device__ __forceinline__ const uint8_t *acquire(const Ctx &c, unsigned bytes, bool &ab)
     {
         if (off + bytes > (unsigned)c.p->ring_bytes) off = 0;
         const uint8_t *ptr = c.ring + off;
@@ -161,7 +181,7 @@ struct ConsRing {
         }
         return ptr;
     }
-    __device__ void release(const Ctx &c)
+    __device__ __forceinline__ void release(const Ctx &c)
     {
         __syncwarp();
         if (c.lane == 0) mbar_arrive(&c.empty[n % TICKETS]);
@@ -174,8 +194,24 @@ struct ProdRing {
     unsigned long long alloc = 0, tail_b = 0;
     uint64_t pol = 0;     // weights: read once per token, L2 evict-first
     uint64_t pol_kv = 0;  // KV cache
+    // L2 lookahead over the weight stream, in "virtual" offsets step * token_bytes + offset
+    const uint8_t *stream_base = nullptr;
+    unsigned long long token_bytes = 0, pf_next = 0, pf_limit = 0, pf_dist = 0;
+    uint64_t pol_pf = 0;
+    __device__ void prefetch_to(unsigned long long target)
+    {
+        if (target > pf_limit) target = pf_limit;
+        while (pf_next < target) {
+            const unsigned long long off = pf_next % token_bytes;
+            unsigned long long n = token_bytes - off;
+            if (n > 32768ull) n = 32768ull;
+            if (n > pf_limit - pf_next) n = pf_limit - pf_next;
+            bulk_prefetch_l2(stream_base + off, (unsigned)n, pol_pf);
+            pf_next += n;
+        }
+    }
     // Reserve `bytes` of ring and a ticket; returns the ring offset or -1 on abort.
-    __device__ int reserve(const Ctx &c, unsigned bytes)
+    __device__ __forceinline__ int reserve(const Ctx &c, unsigned bytes)
     {
         const unsigned RB = (unsigned)c.p->ring_bytes;
         if (off + bytes > RB) {
@@ -193,7 +229,7 @@ struct ProdRing {
         alloc += bytes;
         return o;
     }
-    __device__ bool emit(const Ctx &c, const void *src, unsigned bytes)
+    __device__ __forceinline__ bool emit(const Ctx &c, const void *src, unsigned bytes)
     {
         int o = reserve(c, bytes);
         if (o < 0) return false;
@@ -300,7 +336,7 @@ __device__ __forceinline__ unsigned gbar_index(const Params &p, int step, int l,
 // Consumer-side dependency wait: thread 0 polls, then the consumer warps
 // meet at a named barrier that also ORs the abort state.  Returns true if
 // the CTA must stop.
-__device__ bool cons_wait(const Ctx &c, const unsigned *ctr, unsigned target, unsigned where, int l, int step,
+__device__ __forceinline__ bool cons_wait(const Ctx &c, const unsigned *ctr, unsigned target, unsigned where, int l, int step,
                           bool ab)
 {
     if (c.tid == 0 && !ab) ab = !wait_counter(*c.p, ctr, target, where, l, step);
@@ -309,7 +345,7 @@ __device__ bool cons_wait(const Ctx &c, const unsigned *ctr, unsigned target, un
 
 // Publish the end of a stage: all consumer writes are ordered before thread
 // 0's release by the named barrier plus a gpu-scope fence.
-__device__ bool cons_publish(const Ctx &c, unsigned *ctr, bool do_cnt, unsigned *gbar, bool ab)
+__device__ __forceinline__ bool cons_publish(const Ctx &c, unsigned *ctr, bool do_cnt, unsigned *gbar, bool ab)
 {
     ab = cons_sync_or(ab);
     if (ab) return true;
@@ -324,7 +360,7 @@ __device__ bool cons_publish(const Ctx &c, unsigned *ctr, bool do_cnt, unsigned 
 // Stage input wait in the three schedules: the producer counter `ctr` in the
 // flag schedule, the grid barrier (gstep, gl, gslot) in the barrier schedule,
 // nothing in the multi-kernel schedule (the previous launch has finished).
-__device__ bool stage_wait(const Ctx &c, const unsigned *ctr, unsigned target, int gstep, int gl, int gslot,
+__device__ __forceinline__ bool stage_wait(const Ctx &c, const unsigned *ctr, unsigned target, int gstep, int gl, int gslot,
                            int step, int l, unsigned where, bool ab)
 {
     const Params &p = *c.p;
@@ -342,7 +378,7 @@ __device__ bool stage_wait(const Ctx &c, const unsigned *ctr, unsigned target, i
 // given, and return 1/sqrt(mean(x^2) + eps) (or 1 if norm == false).  The
 // input is FP32 from global memory (read at L2, never a stale L1 line) or,
 // for layer 0, the FP16 embedding row.
-__device__ bool load_act(const Ctx &c, const float *src32, const __half *src16, const __half *gain, int K, bool norm,
+__device__ __forceinline__ bool load_act(const Ctx &c, const float *src32, const __half *src16, const __half *gain, int K, bool norm,
                          float &inv, bool ab)
 {
     const Params &p = *c.p;
@@ -386,23 +422,29 @@ __device__ bool load_act(const Ctx &c, const float *src32, const __half *src16, 
 }
 
 // One GEMV tile: R rows (stored rows w, w+8, w+16, w+24 belong to warp w),
-// K columns in chunks of 256 from the ring.  Writes the R dot products to res.
-__device__ void gemv_tile(const Ctx &c, ConsRing &rc, int R, int K, float *res, bool &ab)
+// K columns in chunks of 256m columns from the ring.  Writes the R dot
+// products to res.
+__device__ __forceinline__ void gemv_tile(const Ctx &c, ConsRing &rc, int R, int K, float *res, bool &ab)
 {
     const int w = c.warp, ln = c.lane;
     float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-    const int nkc = K / KC;
+    const int m = chunk_groups(R, K);
+    const int nch = K / (KC * m);
     const float4 *xs = reinterpret_cast<const float4 *>(c.act);
-    for (int kc = 0; kc < nkc; ++kc) {
-        const uint8_t *ch = rc.acquire(c, (unsigned)R * KC_BYTES, ab);
+    for (int ch_i = 0; ch_i < nch; ++ch_i) {
+        const uint8_t *ch = rc.acquire(c, (unsigned)(R * m) * KC_BYTES, ab);
         if (ab) break;
-        const float4 xa = xs[kc * 64 + ln * 2];
-        const float4 xb = xs[kc * 64 + ln * 2 + 1];
         const uint4 *wp = reinterpret_cast<const uint4 *>(ch) + ln;
-        if (w < R) a0 = dot8(wp[w * 32], xa, xb, a0);
-        if (w + 8 < R) a1 = dot8(wp[(w + 8) * 32], xa, xb, a1);
-        if (w + 16 < R) a2 = dot8(wp[(w + 16) * 32], xa, xb, a2);
-        if (w + 24 < R) a3 = dot8(wp[(w + 24) * 32], xa, xb, a3);
+        for (int gi = 0; gi < m; ++gi) {
+            const int gcol = ch_i * m + gi;
+            const float4 xa = xs[gcol * 64 + ln * 2];
+            const float4 xb = xs[gcol * 64 + ln * 2 + 1];
+            const uint4 *wg = wp + gi * 32;
+            if (w < R) a0 = dot8(wg[(size_t)w * 32 * m], xa, xb, a0);
+            if (w + 8 < R) a1 = dot8(wg[(size_t)(w + 8) * 32 * m], xa, xb, a1);
+            if (w + 16 < R) a2 = dot8(wg[(size_t)(w + 16) * 32 * m], xa, xb, a2);
+            if (w + 24 < R) a3 = dot8(wg[(size_t)(w + 24) * 32 * m], xa, xb, a3);
+        }
         rc.release(c);
     }
     a0 = warp_sum(a0);
@@ -438,7 +480,7 @@ __device__ __forceinline__ int step_token(const Params &p, int step)
 
 // ---------------------------------------------------------------- GEMV stages
 
-__device__ bool stage_gemv(const Ctx &c, ConsRing &rc, int s, int l, int step, bool ab)
+__device__ __forceinline__ bool stage_gemv(const Ctx &c, ConsRing &rc, int s, int l, int step, bool ab)
 {
     const Params &p = *c.p;
     const Geo &g = p.g;
@@ -448,22 +490,35 @@ __device__ bool stage_gemv(const Ctx &c, ConsRing &rc, int s, int l, int step, b
     // layer 0 reads the embedding row of the step's token (after the stage's wait)
     const int tok = (l == 0 && (s == ST_QKV || s == ST_O)) ? step_token(p, step) : 0;
 
-    // ---- inputs
-    float inv = 1.f;
+    // ---- inputs (one call site: the stage picks source, gain and length)
+    const float *src32 = nullptr;
+    const __half *src16 = nullptr, *gain = nullptr;
+    int K = g.d;
+    bool norm = true;
     if (s == ST_QKV) {
-        ab = load_act(c, l == 0 ? nullptr : p.xout + (size_t)(l - 1) * g.d,
-                      l == 0 ? p.embed + (size_t)tok * g.d : nullptr, p.attn_norm + (size_t)l * g.d, g.d, true, inv,
-                      ab);
+        if (l == 0) src16 = p.embed + (size_t)tok * g.d;
+        else src32 = p.xout + (size_t)(l - 1) * g.d;
+        gain = p.attn_norm + (size_t)l * g.d;
     } else if (s == ST_O) {
-        ab = load_act(c, p.attn + (size_t)l * g.Q, nullptr, nullptr, g.Q, false, inv, ab);
+        src32 = p.attn + (size_t)l * g.Q;
+        K = g.Q;
+        norm = false;
     } else if (s == ST_GU) {
-        ab = load_act(c, p.xattn + (size_t)l * g.d, nullptr, p.ffn_norm + (size_t)l * g.d, g.d, true, inv, ab);
+        src32 = p.xattn + (size_t)l * g.d;
+        gain = p.ffn_norm + (size_t)l * g.d;
     } else if (s == ST_D) {
-        ab = load_act(c, p.hbuf + (size_t)l * g.F, nullptr, nullptr, g.F, false, inv, ab);
+        src32 = p.hbuf + (size_t)l * g.F;
+        K = g.F;
+        norm = false;
     } else {
-        ab = load_act(c, p.xout + (size_t)(g.L - 1) * g.d, nullptr, p.final_norm, g.d, true, inv, ab);
+        src32 = p.xout + (size_t)(g.L - 1) * g.d;
+        gain = p.final_norm;
     }
+    float inv = 1.f;
+    ab = load_act(c, src32, src16, gain, K, norm, inv, ab);
     if (ab) return true;
+    const int tslot = s == ST_LM ? 5 * g.L : 5 * l + (s == ST_QKV ? 0 : s + 1);
+    trace_mark(c, step, tslot, TR_LOADED);
 
     const int u0 = pl.u0[s], n = pl.u1[s] - u0;
     const int nt = tiles_of(n, sg.rows_per_unit);
@@ -474,6 +529,7 @@ __device__ bool stage_gemv(const Ctx &c, ConsRing &rc, int s, int l, int step, b
         const int R = nu * sg.rows_per_unit;
         float *res = c.res + (t & 1) * TILE_ROWS;
         gemv_tile(c, rc, R, sg.K, res, ab);
+        if (t == 0) trace_mark(c, step, tslot, TR_X1);
         if (cons_sync_or(ab)) return true;
         // ---- epilogue
         for (int i = c.tid; i < nu; i += NCT) {
@@ -527,186 +583,193 @@ __device__ bool stage_gemv(const Ctx &c, ConsRing &rc, int s, int l, int step, b
 
 // ---------------------------------------------------------------- attention
 
+// One split-KV piece: positions [j0, j1) of KV head gkv for the G query heads
+// that share it.  Warp w owns query head w mod G and every (8/G)-th slab of 32
+// positions, and keeps an online-softmax state (running max m, sum l, output
+// o) for it.  Per slab, lanes first take one position each and compute its full
+// score q . k over the head dimension (element index rotated by the lane, so
+// the 32 rows are read from distinct shared-memory banks), then take E = hd/32
+// output elements each and accumulate p_j * v_j with p_j broadcast by shuffle.
+// Positions < pos come from the ring; position pos (written by this step's QKV
+// stage) is staged from the cache.  The warps of a head are merged at the end.
 template <int HD>
-__device__ bool attn_piece(const Ctx &c, ConsRing &rc, int l, int step, int gkv, int cpiece, const AttnSplit &sp,
-                           bool ab)
+__device__ __forceinline__ bool attn_piece(const Ctx &c, ConsRing &rc, int l, int step, int gkv, int cpiece,
+                                        const AttnSplit &sp, bool ab)
 {
-    constexpr int E = HD / 32;           // K elements per lane
-    constexpr int S = ATT_CHUNK_BYTES / (4 * HD);
+    constexpr int E = HD / 32;
+    constexpr int S = ATT_CHUNK_BYTES / (4 * HD);     // positions per ring sub-block
+    constexpr int SLABS = S / 32;                       // 32-position slabs per sub-block
+    constexpr int H2 = HD / 2;
     const Params &p = *c.p;
     const Geo &g = p.g;
-    const int G = g.group;
+    const int G = g.group;                              // divides NCW
+    const int WPH = NCW / G;                            // warps per head
     const int pos = p.pos0 + step;
     const int ctx = pos + 1;
     const int j0 = cpiece * sp.per;
     const int j1 = min(j0 + sp.per, ctx);
-    const int jr = min(j1, pos);          // ring positions are [j0, jr); pos itself is read fresh
+    const int jr = min(j1, pos);
     const float scale = 1.0f / sqrtf((float)HD);
+    const int hq0 = gkv * G;
+    const int myh = c.warp % G, mys = c.warp / G;       // head, slab residue of this warp
 
-    float *qs = c.act;                    // [G][HD]
-    float *sc = qs + G * HD;              // [G][S]
-    float *pb = sc + G * S;               // [G][S]
-    float *mrun = pb + G * S;             // [G]
-    float *lrun = mrun + MAX_GROUP;       // [G]
-    float *alph = lrun + MAX_GROUP;       // [G]
-    __half *fresh = reinterpret_cast<__half *>(alph + MAX_GROUP);  // [2][HD]
-
-    const float *qsrc = p.qbuf + (size_t)l * g.Q + (size_t)gkv * G * HD;
-    for (int i = c.tid; i < G * HD; i += NCT) qs[i] = __ldcg(qsrc + i);
-    if (c.tid < G) {
-        mrun[c.tid] = -INFINITY;
-        lrun[c.tid] = 0.f;
+    // ---- shared scratch: q [G][HD] FP32, fresh K and V rows [2][HD] FP16, warp states [NCW][HD + 2]
+    float *qs = c.act;
+    __half *fresh = reinterpret_cast<__half *>(qs + G * HD);
+    float *ws = qs + G * HD + HD;
+    const size_t kvbase = ((size_t)l * g.Hkv + gkv) * g.max_seq;
+    const bool has_fresh = pos >= j0 && pos < j1;
+    if (!ab) {
+        const float *qsrc = p.qbuf + (size_t)l * g.Q + (size_t)hq0 * HD;
+        for (int i = c.tid; i < G * HD / 4; i += NCT)
+            reinterpret_cast<float4 *>(qs)[i] = __ldcg(reinterpret_cast<const float4 *>(qsrc) + i);
+        if (has_fresh) {
+            const unsigned *ksrc = reinterpret_cast<const unsigned *>(p.kc + (kvbase + pos) * HD);
+            const unsigned *vsrc = reinterpret_cast<const unsigned *>(p.vc + (kvbase + pos) * HD);
+            for (int i = c.tid; i < H2; i += NCT) {
+                reinterpret_cast<unsigned *>(fresh)[i] = __ldcg(ksrc + i);
+                reinterpret_cast<unsigned *>(fresh)[H2 + i] = __ldcg(vsrc + i);
+            }
+        }
     }
     if (cons_sync_or(ab)) return true;
 
-    float qreg[MAX_GROUP][E];
+    float m = -INFINITY, lsum = 0.f, o[E];
 #pragma unroll
-    for (int h = 0; h < MAX_GROUP; ++h)
-#pragma unroll
-        for (int e = 0; e < E; ++e) qreg[h][e] = (h < G) ? qs[h * HD + c.lane * E + e] : 0.f;
+    for (int e = 0; e < E; ++e) o[e] = 0.f;
+    const float2 *q2 = reinterpret_cast<const float2 *>(qs + myh * HD);
 
-    constexpr int OMAX = (MAX_GROUP * HD + NCT - 1) / NCT;
-    float o[OMAX];
+    // one slab of n (1..32) positions: K rows at Kb, V rows at Vb (row stride HD)
+    auto slab = [&](const __half *Kb, const __half *Vb, int n) {
+        float sc = -INFINITY;
+        if (c.lane < n) {
+            const __half2 *kr = reinterpret_cast<const __half2 *>(Kb + (size_t)c.lane * HD);
+            float d0 = 0.f, d1 = 0.f;
+#pragma unroll 8
+            for (int it = 0; it < H2; ++it) {
+                const int e2 = (it + c.lane) & (H2 - 1);
+                const float2 kv = __half22float2(kr[e2]);
+                const float2 qv = q2[e2];
+                d0 = fmaf(qv.x, kv.x, d0);
+                d1 = fmaf(qv.y, kv.y, d1);
+            }
+            sc = (d0 + d1) * scale;
+        }
+        const float mn = fmaxf(m, warp_max(sc));
+        const float corr = __expf(m - mn);           // 0 while m is -inf
+        const float pe = c.lane < n ? __expf(sc - mn) : 0.f;
+        lsum = fmaf(lsum, corr, warp_sum(pe));
 #pragma unroll
-    for (int k = 0; k < OMAX; ++k) o[k] = 0.f;
+        for (int e = 0; e < E; ++e) o[e] *= corr;
+        for (int jj = 0; jj < n; ++jj) {
+            const float pj = __shfl_sync(0xffffffffu, pe, jj);
+            const __half *vr = Vb + (size_t)jj * HD + c.lane * E;
+            if constexpr (E == 4) {
+                const uint2 w = *reinterpret_cast<const uint2 *>(vr);
+                const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&w.x));
+                const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&w.y));
+                o[0] = fmaf(pj, a.x, o[0]);
+                o[1] = fmaf(pj, a.y, o[1]);
+                o[2] = fmaf(pj, b.x, o[2]);
+                o[3] = fmaf(pj, b.y, o[3]);
+            } else {
+                const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(vr));
+                o[0] = fmaf(pj, a.x, o[0]);
+                o[1] = fmaf(pj, a.y, o[1]);
+            }
+        }
+        m = mn;
+    };
 
-    const size_t kvbase = ((size_t)l * g.Hkv + gkv) * g.max_seq;
     const int nring = jr > j0 ? ceil_div(jr - j0, S) : 0;
-    const bool has_fresh = (pos >= j0 && pos < j1);
-    const int nblocks = nring + (has_fresh ? 1 : 0);
-
-    for (int blk = 0; blk < nblocks; ++blk) {
-        const __half *Kb, *Vb;
-        int nb;
-        const bool is_ring = blk < nring;
-        if (is_ring) {
-            nb = min(S, jr - (j0 + blk * S));
-            const uint8_t *ch = rc.acquire(c, 4u * (unsigned)nb * HD, ab);
-            Kb = reinterpret_cast<const __half *>(ch);
-            Vb = Kb + (size_t)nb * HD;
-        } else {
-            nb = 1;
-            const __half *ksrc = p.kc + (kvbase + pos) * HD;
-            const __half *vsrc = p.vc + (kvbase + pos) * HD;
-            for (int i = c.tid; i < HD; i += NCT) {
-                fresh[i] = __ushort_as_half(__ldcg(reinterpret_cast<const unsigned short *>(ksrc) + i));
-                fresh[HD + i] = __ushort_as_half(__ldcg(reinterpret_cast<const unsigned short *>(vsrc) + i));
-            }
-            if (cons_sync_or(ab)) return true;
-            Kb = fresh;
-            Vb = fresh + HD;
-        }
-        // scores: one position per warp at a time, lanes split the head dim
-        if (!ab) {
-            for (int jj = c.warp; jj < nb; jj += NCW) {
-                float kv[E];
-                const __half *kr = Kb + (size_t)jj * HD + c.lane * E;
-                if constexpr (E == 4) {
-                    const uint2 raw = *reinterpret_cast<const uint2 *>(kr);
-                    const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.x));
-                    const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&raw.y));
-                    kv[0] = f0.x;
-                    kv[1] = f0.y;
-                    kv[2] = f1.x;
-                    kv[3] = f1.y;
-                } else {
-                    const unsigned raw = *reinterpret_cast<const unsigned *>(kr);
-                    const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&raw));
-                    kv[0] = f0.x;
-                    kv[1] = f0.y;
-                }
+    for (int blk = 0; blk < nring; ++blk) {
+        const int nb = min(S, jr - (j0 + blk * S));
+        const uint8_t *ch = rc.acquire(c, 4u * (unsigned)nb * HD, ab);
+        if (ab) break;
+        const __half *Kb = reinterpret_cast<const __half *>(ch);
+        const __half *Vb = Kb + (size_t)nb * HD;
 #pragma unroll
-                for (int h = 0; h < MAX_GROUP; ++h) {
-                    if (h < G) {
-                        float d = 0.f;
-#pragma unroll
-                        for (int e = 0; e < E; ++e) d = fmaf(qreg[h][e], kv[e], d);
-                        d = warp_sum(d);
-                        if (c.lane == 0) sc[h * S + jj] = d * scale;
-                    }
-                }
-            }
+        for (int sl = 0; sl < SLABS; ++sl) {
+            const int gslab = blk * SLABS + sl;
+            const int n = min(32, nb - sl * 32);
+            if (n > 0 && gslab % WPH == mys) slab(Kb + (size_t)sl * 32 * HD, Vb + (size_t)sl * 32 * HD, n);
         }
-        if (cons_sync_or(ab)) return true;
-        // per-head running max / sum (one warp per head)
-        for (int h = c.warp; h < G; h += NCW) {
-            float s0 = c.lane < nb ? sc[h * S + c.lane] : -INFINITY;
-            float s1 = c.lane + 32 < nb ? sc[h * S + c.lane + 32] : -INFINITY;
-            const float mx = warp_max(fmaxf(s0, s1));
-            const float mold = mrun[h];
-            const float mnew = fmaxf(mold, mx);
-            const float alpha = (mold == -INFINITY) ? 0.f : expf(mold - mnew);
-            const float p0 = c.lane < nb ? expf(s0 - mnew) : 0.f;
-            const float p1 = c.lane + 32 < nb ? expf(s1 - mnew) : 0.f;
-            if (c.lane < nb) pb[h * S + c.lane] = p0;
-            if (c.lane + 32 < nb) pb[h * S + c.lane + 32] = p1;
-            const float ls = warp_sum(p0 + p1);
-            __syncwarp();
-            if (c.lane == 0) {
-                lrun[h] = lrun[h] * alpha + ls;
-                mrun[h] = mnew;
-                alph[h] = alpha;
-            }
-        }
-        if (cons_sync_or(ab)) return true;
-        // o = o * alpha + sum_j p_j V_j
-#pragma unroll
-        for (int k = 0; k < OMAX; ++k) {
-            const int eidx = c.tid + k * NCT;
-            if (eidx < G * HD) {
-                const int h = eidx / HD, i = eidx % HD;
-                float acc = o[k] * alph[h];
-                for (int jj = 0; jj < nb; ++jj) acc = fmaf(pb[h * S + jj], __half2float(Vb[(size_t)jj * HD + i]), acc);
-                o[k] = acc;
-            }
-        }
-        if (is_ring && !ab) rc.release(c);
-        if (cons_sync_or(ab)) return true;
+        rc.release(c);
     }
+    if (!ab && has_fresh && (nring * SLABS) % WPH == mys) slab(fresh, fresh + HD, 1);
+    trace_mark(c, step, 5 * l + 1, TR_X1);
 
-    // ---- write this piece's partial (o, m, l) per query head of the group
-    const int hq0 = gkv * G;
+    // ---- merge the warps of each head: ws[warp][HD + 2] = (o, m, l)
+    {
+        float *dst = ws + (size_t)c.warp * (HD + 2);
 #pragma unroll
-    for (int k = 0; k < OMAX; ++k) {
-        const int eidx = c.tid + k * NCT;
-        if (eidx < G * HD) {
-            const int h = eidx / HD, i = eidx % HD;
-            float *dst = p.apart + (((size_t)l * g.Hq + hq0 + h) * p.max_split + cpiece) * (HD + 2);
-            dst[i] = o[k];
-            if (i == 0) {
-                dst[HD] = mrun[h];
-                dst[HD + 1] = lrun[h];
-            }
+        for (int e = 0; e < E; ++e) dst[c.lane * E + e] = o[e];
+        if (c.lane == 0) {
+            dst[HD] = m;
+            dst[HD + 1] = lsum;
+        }
+    }
+    if (cons_sync_or(ab)) return true;
+    for (int eidx = c.tid; eidx < G * HD; eidx += NCT) {
+        const int h = eidx / HD, i = eidx % HD;
+        float M = -INFINITY;
+        for (int k = 0; k < WPH; ++k) M = fmaxf(M, ws[(size_t)(h + k * G) * (HD + 2) + HD]);
+        float num = 0.f, den = 0.f;
+        for (int k = 0; k < WPH; ++k) {
+            const float *src = ws + (size_t)(h + k * G) * (HD + 2);
+            const float wgt = (src[HD] == -INFINITY) ? 0.f : __expf(src[HD] - M);
+            num = fmaf(wgt, src[i], num);
+            den = fmaf(wgt, src[HD + 1], den);
+        }
+        float *dst = p.apart + (((size_t)l * g.Hq + hq0 + h) * p.max_split + cpiece) * (HD + 2);
+        dst[i] = num;
+        if (i == 0) {
+            dst[HD] = M;
+            dst[HD + 1] = den;
         }
     }
     if (cons_sync_or(ab)) return true;
     if (c.tid == 0) {
-        fence_acq_rel_gpu();
-        unsigned old = atom_add_acq_rel(p.attn_done + ((size_t)l * g.Hkv + gkv) * CNT_STRIDE, 1u);
+        const unsigned old = atom_add_acq_rel(p.attn_done + ((size_t)l * g.Hkv + gkv) * CNT_STRIDE, 1u);
         c.misc[M_FLAG] = (old == (unsigned)sp.n_split - 1u) ? 1u : 0u;
     }
     if (cons_sync_or(ab)) return true;
+    trace_mark(c, step, 5 * l + 1, TR_X2);
     if (c.misc[M_FLAG] == 0u) return false;
 
-    // ---- this CTA holds the last piece of KV head gkv: combine all pieces
+    // ---- this CTA holds the last piece of KV head gkv: combine all pieces in one
+    // online pass per output element, with the loads of four pieces in flight at once
     if (c.tid == 0) st_relaxed(p.attn_done + ((size_t)l * g.Hkv + gkv) * CNT_STRIDE, 0u);
+    const int ns = sp.n_split;
+    const float *base = p.apart + ((size_t)l * g.Hq + hq0) * p.max_split * (HD + 2);
+    for (int eidx = c.tid; eidx < G * HD; eidx += NCT) {
+        const int h = eidx / HD, i = eidx % HD;
+        const float *src = base + (size_t)h * p.max_split * (HD + 2);
+        float M = -INFINITY, num = 0.f, den = 0.f;
+        for (int c0 = 0; c0 < ns; c0 += 4) {
+            float mc[4], lc[4], oc[4];
 #pragma unroll
-    for (int k = 0; k < OMAX; ++k) {
-        const int eidx = c.tid + k * NCT;
-        if (eidx < G * HD) {
-            const int h = eidx / HD, i = eidx % HD;
-            const float *src = p.apart + (((size_t)l * g.Hq + hq0 + h) * p.max_split) * (HD + 2);
-            float M = -INFINITY;
-            for (int cc = 0; cc < sp.n_split; ++cc) M = fmaxf(M, __ldcg(src + (size_t)cc * (HD + 2) + HD));
-            float num = 0.f, den = 0.f;
-            for (int cc = 0; cc < sp.n_split; ++cc) {
-                const float *pc = src + (size_t)cc * (HD + 2);
-                const float wgt = expf(__ldcg(pc + HD) - M);
-                num = fmaf(wgt, __ldcg(pc + i), num);
-                den = fmaf(wgt, __ldcg(pc + HD + 1), den);
+            for (int k = 0; k < 4; ++k) {
+                if (c0 + k < ns) {
+                    const float *pc = src + (size_t)(c0 + k) * (HD + 2);
+                    const float2 ml = __ldcg(reinterpret_cast<const float2 *>(pc + HD));
+                    mc[k] = ml.x;
+                    lc[k] = ml.y;
+                    oc[k] = __ldcg(pc + i);
+                }
             }
-            p.attn[(size_t)l * g.Q + (size_t)(hq0 + h) * HD + i] = num / den;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                if (c0 + k < ns) {
+                    const float Mn = fmaxf(M, mc[k]);
+                    const float a = __expf(M - Mn), b = __expf(mc[k] - Mn);
+                    num = fmaf(num, a, b * oc[k]);
+                    den = fmaf(den, a, b * lc[k]);
+                    M = Mn;
+                }
+            }
         }
+        p.attn[(size_t)l * g.Q + (size_t)(hq0 + h) * HD + i] = num / den;
     }
     return cons_publish(c, layer_cnt(p, l, C_ATTN), true, nullptr, ab);
 }
@@ -717,7 +780,7 @@ __device__ bool attn_piece(const Ctx &c, ConsRing &rc, int l, int step, int gkv,
 // most-significant-digit radix select over the consumer threads.  `keys`
 // may be shared or global memory; stride/width describe a [rows][stride]
 // array of which the first `width` entries of each row are used.
-__device__ bool radix_select(const Ctx &c, const unsigned long long *keys, int rows, int stride, int width, int k,
+__device__ __forceinline__ bool radix_select(const Ctx &c, const unsigned long long *keys, int rows, int stride, int width, int k,
                              bool global_mem, unsigned long long &tau, bool ab)
 {
     unsigned long long prefix = 0ull, mask = 0ull;
@@ -771,7 +834,7 @@ __device__ bool radix_select(const Ctx &c, const unsigned long long *keys, int r
     return false;
 }
 
-__device__ bool stage_lm_sample(const Ctx &c, ConsRing &rc, int step, bool ab)
+__device__ __forceinline__ bool stage_lm_sample(const Ctx &c, ConsRing &rc, int step, bool ab)
 {
     const Params &p = *c.p;
     const Geo &g = p.g;
@@ -884,6 +947,7 @@ __device__ void consumer(const Ctx &c)
         }
         for (int l = 0; l < g.L; ++l) {
             if (stage_active(p, l, SID_QKV)) {
+                trace_mark(c, step, 5 * l + 0, TR_ENTER);
                 // QKV(l) reads x_out(l-1), or for l = 0 the embedding of the step's token
                 int gstep = step, gl = l - 1, gslot = 4;
                 if (l == 0) {
@@ -894,14 +958,18 @@ __device__ void consumer(const Ctx &c)
                 if (stage_wait(c, l > 0 ? layer_cnt(p, l - 1, C_D) : nullptr, (e + 1u) * p.n_prod[ST_D], gstep, gl,
                                gslot, step, l, 1, ab))
                     return;
+                trace_mark(c, step, 5 * l + 0, TR_READY);
                 if (stage_gemv(c, rc, ST_QKV, l, step, ab)) return;
                 const bool withhold = decode && step == p.fault_step && l == 0;
                 if (cons_publish(c, layer_cnt(p, l, C_QKV), !withhold, (grid && !withhold) ? p.gbar : nullptr, ab))
                     return;
+                trace_mark(c, step, 5 * l + 0, TR_DONE);
             }
             if (stage_active(p, l, SID_ATTN)) {
+                trace_mark(c, step, 5 * l + 1, TR_ENTER);
                 if (stage_wait(c, layer_cnt(p, l, C_QKV), (e + 1u) * p.n_prod[ST_QKV], step, l, 0, step, l, 2, ab))
                     return;
+                trace_mark(c, step, 5 * l + 1, TR_READY);
                 const int ctx = p.pos0 + step + 1;
                 const AttnSplit sp = attn_split(ctx, p.P, g.Hkv, p.attn_min_len);
                 const int U = g.Hkv * sp.n_split;
@@ -912,31 +980,44 @@ __device__ void consumer(const Ctx &c)
                     if (stop) return;
                 }
                 if (grid && cons_publish(c, nullptr, false, p.gbar, ab)) return;
+                trace_mark(c, step, 5 * l + 1, TR_DONE);
             }
             if (stage_active(p, l, SID_O)) {
+                trace_mark(c, step, 5 * l + 2, TR_ENTER);
                 if (stage_wait(c, layer_cnt(p, l, C_ATTN), (e + 1u) * (unsigned)g.Hkv, step, l, 1, step, l, 3, ab))
                     return;
+                trace_mark(c, step, 5 * l + 2, TR_READY);
                 if (stage_gemv(c, rc, ST_O, l, step, ab)) return;
                 if (cons_publish(c, layer_cnt(p, l, C_O), true, grid ? p.gbar : nullptr, ab)) return;
+                trace_mark(c, step, 5 * l + 2, TR_DONE);
             }
             if (stage_active(p, l, SID_GU)) {
+                trace_mark(c, step, 5 * l + 3, TR_ENTER);
                 if (stage_wait(c, layer_cnt(p, l, C_O), (e + 1u) * p.n_prod[ST_O], step, l, 2, step, l, 4, ab))
                     return;
+                trace_mark(c, step, 5 * l + 3, TR_READY);
                 if (stage_gemv(c, rc, ST_GU, l, step, ab)) return;
                 if (cons_publish(c, layer_cnt(p, l, C_GU), true, grid ? p.gbar : nullptr, ab)) return;
+                trace_mark(c, step, 5 * l + 3, TR_DONE);
             }
             if (stage_active(p, l, SID_D)) {
+                trace_mark(c, step, 5 * l + 4, TR_ENTER);
                 if (stage_wait(c, layer_cnt(p, l, C_GU), (e + 1u) * p.n_prod[ST_GU], step, l, 3, step, l, 5, ab))
                     return;
+                trace_mark(c, step, 5 * l + 4, TR_READY);
                 if (stage_gemv(c, rc, ST_D, l, step, ab)) return;
                 if (cons_publish(c, layer_cnt(p, l, C_D), true, grid ? p.gbar : nullptr, ab)) return;
+                trace_mark(c, step, 5 * l + 4, TR_DONE);
             }
         }
         if (decode && stage_active(p, 0, SID_LM)) {
+            trace_mark(c, step, 5 * g.L, TR_ENTER);
             if (stage_wait(c, layer_cnt(p, g.L - 1, C_D), (e + 1u) * p.n_prod[ST_D], step, g.L - 1, 4, step, g.L - 1,
                            6, ab))
                 return;
+            trace_mark(c, step, 5 * g.L, TR_READY);
             if (stage_lm_sample(c, rc, step, ab)) return;
+            trace_mark(c, step, 5 * g.L, TR_DONE);
         }
     }
 }
@@ -967,7 +1048,7 @@ __device__ const __half *src_row(const Geo &g, const RepackSrc &w, int s, int l,
 
 // ---------------------------------------------------------------- producer
 
-__device__ bool produce_tiles(const Ctx &c, ProdRing &pr, int s, int l)
+__device__ __forceinline__ bool produce_tiles(const Ctx &c, ProdRing &pr, int s, int l, int step)
 {
     const Params &p = *c.p;
     const CtaPlan &pl = p.plans[c.b];
@@ -976,12 +1057,17 @@ __device__ bool produce_tiles(const Ctx &c, ProdRing &pr, int s, int l)
     const int nt = tiles_of(n, sg.rows_per_unit);
     const uint8_t *src = p.wstream + pl.base +
                          (s == ST_LM ? pl.lm_off : (unsigned long long)l * pl.layer_bytes + pl.stage_off[s]);
-    const int nkc = sg.K / KC;
     for (int t = 0; t < nt; ++t) {
         int a, bnd;
         tile_range(u0, n, nt, t, a, bnd);
-        const unsigned bytes = (unsigned)((bnd - a) * sg.rows_per_unit) * KC_BYTES;
-        for (int kc = 0; kc < nkc; ++kc) {
+        const int R = (bnd - a) * sg.rows_per_unit;
+        const int m = chunk_groups(R, sg.K);
+        const unsigned bytes = (unsigned)(R * m) * KC_BYTES;
+        const int nch = sg.K / (KC * m);
+        for (int k = 0; k < nch; ++k) {
+            if (pr.pf_dist)
+                pr.prefetch_to((unsigned long long)step * pr.token_bytes + (unsigned long long)(src - pr.stream_base) +
+                               bytes + pr.pf_dist);
             if (!pr.emit(c, src, bytes)) return false;
             src += bytes;
         }
@@ -990,31 +1076,33 @@ __device__ bool produce_tiles(const Ctx &c, ProdRing &pr, int s, int l)
 }
 
 // Producer variant used by lf_generate_noalloc, whose weights stay in the
-// caller's row-major layout: each chunk (R rows x 256 columns) is gathered with
-// one 512-byte bulk copy per row segment into the same ring layout.
-__device__ bool produce_tiles_direct(const Ctx &c, ProdRing &pr, const RepackSrc &w, int s, int l)
+// caller's row-major layout: each chunk (R rows x 256m columns) is gathered
+// with one bulk copy of 512m bytes per row into the same ring layout.
+__device__ __forceinline__ bool produce_tiles_direct(const Ctx &c, ProdRing &pr, const RepackSrc &w, int s, int l, int step)
 {
     const Params &p = *c.p;
     const CtaPlan &pl = p.plans[c.b];
     const StageGeom sg = stage_geom(p.g, s);
     const int u0 = pl.u0[s], n = pl.u1[s] - u0;
     const int nt = tiles_of(n, sg.rows_per_unit);
-    const int nkc = sg.K / KC;
     for (int t = 0; t < nt; ++t) {
         int a, bnd;
         tile_range(u0, n, nt, t, a, bnd);
         const int nu = bnd - a;
         const int R = nu * sg.rows_per_unit;
-        for (int kc = 0; kc < nkc; ++kc) {
-            const int o = pr.reserve(c, (unsigned)R * KC_BYTES);
+        const int m = chunk_groups(R, sg.K);
+        const unsigned row_bytes = (unsigned)m * KC_BYTES;
+        const int nch = sg.K / (KC * m);
+        for (int k = 0; k < nch; ++k) {
+            const int o = pr.reserve(c, (unsigned)R * row_bytes);
             if (o < 0) return false;
             uint64_t *bar = &c.full[pr.n % TICKETS];
-            mbar_arrive_expect_tx(bar, (unsigned)R * KC_BYTES);
+            mbar_arrive_expect_tx(bar, (unsigned)R * row_bytes);
             for (int r = 0; r < R; ++r) {
                 const int unit = a + (sg.rows_per_unit == 2 ? r % nu : r);
                 const int part = sg.rows_per_unit == 2 ? r / nu : 0;
-                const __half *src = src_row(p.g, w, s, l, unit, part) + (size_t)kc * KC;
-                bulk_g2s(c.ring + o + r * KC_BYTES, src, KC_BYTES, bar, pr.pol);
+                const __half *src = src_row(p.g, w, s, l, unit, part) + (size_t)k * KC * m;
+                bulk_g2s(c.ring + o + r * row_bytes, src, row_bytes, bar, pr.pol);
             }
             ++pr.n;
         }
@@ -1028,14 +1116,26 @@ __device__ void producer(const Ctx &c, const RepackSrc *w)
     const Params &p = *c.p;
     const Geo &g = p.g;
     ProdRing pr;
-    auto tiles = [](const Ctx &cc, ProdRing &r, const RepackSrc *ws, int s, int l) {
-        if constexpr (kDirect) return produce_tiles_direct(cc, r, *ws, s, l);
-        else return produce_tiles(cc, r, s, l);
+    int step_now = 0;
+    auto tiles = [&step_now](const Ctx &cc, ProdRing &r, const RepackSrc *ws, int s, int l) {
+        if constexpr (kDirect) return produce_tiles_direct(cc, r, *ws, s, l, step_now);
+        else return produce_tiles(cc, r, s, l, step_now);
     };
     pr.pol = policy_evict_first();
     pr.pol_kv = policy_evict_normal();
+    pr.pol_pf = p.l2_prefetch_last ? policy_evict_last() : policy_evict_normal();
+    if (!kDirect && p.only_stage < 0 && p.l2_prefetch_bytes > 0) {
+        const CtaPlan &pl = p.plans[c.b];
+        pr.stream_base = p.wstream + pl.base;
+        pr.token_bytes = pl.lm_off;
+        if (p.mode == MODE_DECODE)
+            pr.token_bytes += (unsigned long long)(pl.u1[ST_LM] - pl.u0[ST_LM]) * g.d * 2ull;
+        pr.pf_limit = pr.token_bytes * (unsigned long long)p.n_steps;
+        pr.pf_dist = (unsigned long long)p.l2_prefetch_bytes;
+    }
     bool ok = true;
     for (int step = 0; step < p.n_steps && ok; ++step) {
+        step_now = step;
         const unsigned e = p.epoch0 + (unsigned)step;
         const int pos = p.pos0 + step;
         for (int l = 0; l < g.L && ok; ++l) {
@@ -1137,23 +1237,24 @@ __global__ void lf_repack_kernel(Geo g, const CtaPlan *plans, RepackSrc w, uint8
             const int u0 = pl.u0[s], n = pl.u1[s] - u0;
             const int nt = tiles_of(n, sg.rows_per_unit);
             uint8_t *out = dst + pl.base + (s == ST_LM ? pl.lm_off : (unsigned long long)l * pl.layer_bytes + pl.stage_off[s]);
-            const int nkc = sg.K / KC;
             for (int t = 0; t < nt; ++t) {
                 int a, bnd;
                 tile_range(u0, n, nt, t, a, bnd);
                 const int nu = bnd - a;
                 const int R = nu * sg.rows_per_unit;
-                for (int kc = 0; kc < nkc; ++kc) {
-                    // chunk: R rows x 256 columns, stored row r -> (unit a + r % nu, part r / nu)
-                    for (int q = threadIdx.x; q < R * 32; q += blockDim.x) {
-                        const int r = q / 32, seg = q % 32;
+                const int m = chunk_groups(R, sg.K);
+                const int nch = sg.K / (KC * m);
+                for (int k = 0; k < nch; ++k) {
+                    // chunk: R rows x 256m columns, stored row r -> (unit a + r % nu, part r / nu)
+                    for (int q = threadIdx.x; q < R * 32 * m; q += blockDim.x) {
+                        const int r = q / (32 * m), rem = q % (32 * m);
                         const int unit = a + (sg.rows_per_unit == 2 ? r % nu : r);
                         const int part = sg.rows_per_unit == 2 ? r / nu : 0;
-                        const uint4 *srow = reinterpret_cast<const uint4 *>(src_row(g, w, s, l < g.L ? l : 0, unit, part) +
-                                                                            (size_t)kc * KC);
-                        reinterpret_cast<uint4 *>(out)[q] = srow[seg];
+                        const uint4 *srow =
+                            reinterpret_cast<const uint4 *>(src_row(g, w, s, l < g.L ? l : 0, unit, part));
+                        reinterpret_cast<uint4 *>(out)[q] = srow[(size_t)k * 32 * m + rem];
                     }
-                    out += (size_t)R * KC_BYTES;
+                    out += (size_t)R * m * KC_BYTES;
                 }
             }
         }

@@ -74,7 +74,7 @@ extern "C" LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_w
         cfg->vocab <= 0 || cfg->max_seq <= 0 || cfg->n_ctas < 0 || !(cfg->rope_theta > 0.f) || !(cfg->rms_eps >= 0.f))
         return LF_ERR_INVALID_ARG;
     if (cfg->head_dim != 64 && cfg->head_dim != 128) return LF_ERR_NOT_SUPPORTED;
-    if (cfg->n_heads % cfg->n_kv_heads || cfg->n_heads / cfg->n_kv_heads > lfk::MAX_GROUP) return LF_ERR_NOT_SUPPORTED;
+    if (cfg->n_heads % cfg->n_kv_heads || lfk::MAX_GROUP % (cfg->n_heads / cfg->n_kv_heads)) return LF_ERR_NOT_SUPPORTED;
     if (cfg->d_model % lfk::KC || (cfg->n_heads * cfg->head_dim) % lfk::KC || cfg->ffn_dim % lfk::KC)
         return LF_ERR_NOT_SUPPORTED;
     if (sp->top_k < 0 || sp->top_k > LF_MAX_TOP_K) return LF_ERR_NOT_SUPPORTED;
@@ -115,8 +115,8 @@ extern "C" LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_w
         const int n_lm = pl.u1[lfk::ST_LM] - pl.u0[lfk::ST_LM];
         lm_rows_max = n_lm > lm_rows_max ? n_lm : lm_rows_max;
     }
-    const int S = lfk::attn_sub_positions(g.hd);
-    int act = g.group * g.hd + 2 * g.group * S + 3 * lfk::MAX_GROUP + g.hd;
+    const int max_split = P / g.Hkv > 1 ? P / g.Hkv : 1;
+    int act = lfk::MAX_GROUP * g.hd + g.hd + lfk::NCW * (g.hd + 2);
     const int dims[] = {g.d, g.Q, g.F};
     for (int v : dims) act = v > act ? v : act;
     act = (act + 3) / 4 * 4;
@@ -127,7 +127,6 @@ extern "C" LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_w
     const int smem = (int)lfk_smem_bytes(ring, act, lm_rows_max);
 
     // ---- scratch layout inside the static array
-    const int max_split = P / g.Hkv > 1 ? P / g.Hkv : 1;
     const size_t kv_elems = (size_t)g.L * g.Hkv * (size_t)g.max_seq * g.hd;
     const size_t n_layer_cnt = (size_t)g.L * lfk::N_LAYER_CNT, n_attn_done = (size_t)g.L * g.Hkv;
     const size_t cnt_words = (n_layer_cnt + n_attn_done + 3) * lfk::CNT_STRIDE;

@@ -75,9 +75,33 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
+// Wait primitive for one mbarrier phase.  LF_MBAR_WAIT selects the form:
+// 0 try_wait (may suspend the thread until the phase completes or a
+// hardware time limit passes), 1 test_wait (never suspends), 2 try_wait with a
+// short suspend-time hint.
+#ifndef LF_MBAR_WAIT
+#define LF_MBAR_WAIT 0
+#endif
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity)
 {
     unsigned ok;
+#if LF_MBAR_WAIT == 1
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+#elif LF_MBAR_WAIT == 2
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(100u)
+        : "memory");
+#else
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
@@ -85,6 +109,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity)
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
+#endif
     return ok != 0;
 }
 
@@ -93,6 +118,12 @@ __device__ __forceinline__ uint64_t policy_evict_first()
 {
     uint64_t pol;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint64_t policy_evict_last()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
     return pol;
 }
 __device__ __forceinline__ uint64_t policy_evict_normal()
@@ -108,6 +139,13 @@ __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src, unsign
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
         ::"r"(smem_u32(dst_smem)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
+}
+
+// Prefetch global bytes into L2 (no shared-memory destination, no completion).
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, unsigned bytes, uint64_t policy)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(src), "r"(bytes), "l"(policy)
+                 : "memory");
 }
 
 // ---- named barrier over the consumer warps, with an OR-reduction of a predicate
