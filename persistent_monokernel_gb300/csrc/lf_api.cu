@@ -25,7 +25,7 @@ extern "C" cudaError_t lfk_launch_repack(lfk::Geo g, int P, const lfk::CtaPlan *
 
 namespace {
 
-constexpr int kAttnMinLen = 32;         // fewest positions per split-KV piece
+constexpr int kAttnMinLen = 64;         // fewest positions per split-KV piece
 constexpr long long kDefaultTimeoutNs = 2000000000LL;
 constexpr int kL2PrefetchKB = 0;        // weight-stream lookahead into L2 per CTA (measured: no gain)
 
@@ -119,10 +119,13 @@ lf_status validate_config(const lf_config &c)
 
 // Attention scratch (floats) inside the activation region: q of the group
 // [G][hd], the staged fresh K and V rows (hd floats' worth of FP16) and the
-// eight warp states [NCW][hd + 2].
-int attn_scratch_floats(const lfk::Geo &g)
+// eight warp states [NCW][hd + 2]; or, in the combine, the (m, l) table of
+// every piece [G][max_split].
+int attn_scratch_floats(const lfk::Geo &g, int max_split)
 {
-    return lfk::MAX_GROUP * g.hd + g.hd + lfk::NCW * (g.hd + 2);
+    const int piece = lfk::MAX_GROUP * g.hd + g.hd + lfk::NCW * (g.hd + 2);
+    const int combine = 2 * g.group * max_split;
+    return piece > combine ? piece : combine;
 }
 
 lf_status launch(lf_handle *h, const lfk::Params &p, cudaStream_t stream)
@@ -325,7 +328,7 @@ lf_status lf_create(const lf_config *cfg, const lf_weights *w, lf_handle **out)
 
     // ---- shared memory: everything but the ring, then the largest ring that fits
     h->max_split = std::max(1, P / g.Hkv);
-    h->act_floats = std::max(std::max(g.d, g.Q), std::max(g.F, attn_scratch_floats(g)));
+    h->act_floats = std::max(std::max(g.d, g.Q), std::max(g.F, attn_scratch_floats(g, h->max_split)));
     h->act_floats = (h->act_floats + 3) / 4 * 4;
     const unsigned rest = lfk_smem_bytes(0, h->act_floats, lm_rows_max);
     if ((int)rest + 2 * lfk::ATT_CHUNK_BYTES > optin) {

@@ -737,39 +737,64 @@ __device__ __forceinline__ bool attn_piece(const Ctx &c, ConsRing &rc, int l, in
     trace_mark(c, step, 5 * l + 1, TR_X2);
     if (c.misc[M_FLAG] == 0u) return false;
 
-    // ---- this CTA holds the last piece of KV head gkv: combine all pieces in one
-    // online pass per output element, with the loads of four pieces in flight at once
+    // ---- this CTA holds the last piece of KV head gkv: combine all pieces,
+    // attn = sum_c e^(m_c - M) o_c / sum_c e^(m_c - M) l_c, M = max_c m_c.
+    // The (m, l) table goes to shared memory while each thread loads o of 16
+    // pieces for two output elements at once: one L2 round trip per 16 pieces.
     if (c.tid == 0) st_relaxed(p.attn_done + ((size_t)l * g.Hkv + gkv) * CNT_STRIDE, 0u);
+    constexpr int PB = 16;
     const int ns = sp.n_split;
     const float *base = p.apart + ((size_t)l * g.Hq + hq0) * p.max_split * (HD + 2);
-    for (int eidx = c.tid; eidx < G * HD; eidx += NCT) {
-        const int h = eidx / HD, i = eidx % HD;
-        const float *src = base + (size_t)h * p.max_split * (HD + 2);
-        float M = -INFINITY, num = 0.f, den = 0.f;
-        for (int c0 = 0; c0 < ns; c0 += 4) {
-            float mc[4], lc[4], oc[4];
+    float2 *mls = reinterpret_cast<float2 *>(c.act);   // [G][ns] (m, l); act is free after the merge
+    const int n_el = G * HD;
+    const int n_it = ceil_div(n_el, 2 * NCT);           // the same for every thread
+    float o0[PB], o1[PB];
+    auto load_batch = [&](int it, int c0) {
+        const int e0 = c.tid + it * 2 * NCT, e1 = e0 + NCT;
+        const float *s0 = base + (size_t)(e0 / HD) * p.max_split * (HD + 2) + e0 % HD;
+        const float *s1 = base + (size_t)(e1 / HD) * p.max_split * (HD + 2) + e1 % HD;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                if (c0 + k < ns) {
-                    const float *pc = src + (size_t)(c0 + k) * (HD + 2);
-                    const float2 ml = __ldcg(reinterpret_cast<const float2 *>(pc + HD));
-                    mc[k] = ml.x;
-                    lc[k] = ml.y;
-                    oc[k] = __ldcg(pc + i);
-                }
-            }
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                if (c0 + k < ns) {
-                    const float Mn = fmaxf(M, mc[k]);
-                    const float a = __expf(M - Mn), b = __expf(mc[k] - Mn);
-                    num = fmaf(num, a, b * oc[k]);
-                    den = fmaf(den, a, b * lc[k]);
-                    M = Mn;
-                }
-            }
+        for (int k = 0; k < PB; ++k) {
+            if (c0 + k < ns && e0 < n_el) o0[k] = __ldcg(s0 + (size_t)(c0 + k) * (HD + 2));
+            if (c0 + k < ns && e1 < n_el) o1[k] = __ldcg(s1 + (size_t)(c0 + k) * (HD + 2));
         }
-        p.attn[(size_t)l * g.Q + (size_t)(hq0 + h) * HD + i] = num / den;
+    };
+    load_batch(0, 0);                                   // in flight while the table loads
+    for (int idx = c.tid; idx < G * ns; idx += NCT) {
+        const int h = idx / ns, cc = idx % ns;
+        mls[idx] = __ldcg(reinterpret_cast<const float2 *>(base + ((size_t)h * p.max_split + cc) * (HD + 2) + HD));
+    }
+    if (cons_sync_or(ab)) return true;
+    for (int it = 0; it < n_it; ++it) {
+        const int e0 = c.tid + it * 2 * NCT, e1 = e0 + NCT;
+        const int h0 = min(e0, n_el - 1) / HD, h1 = min(e1, n_el - 1) / HD;
+        float M0 = -INFINITY, n0 = 0.f, d0 = 0.f, M1 = -INFINITY, n1 = 0.f, d1 = 0.f;
+        for (int c0 = 0; c0 < ns; c0 += PB) {
+            if (it > 0 || c0 > 0) load_batch(it, c0);
+            float B0 = M0, B1 = M1;
+#pragma unroll
+            for (int k = 0; k < PB; ++k) {
+                if (c0 + k < ns) {
+                    B0 = fmaxf(B0, mls[h0 * ns + c0 + k].x);
+                    B1 = fmaxf(B1, mls[h1 * ns + c0 + k].x);
+                }
+            }
+            const float a0 = __expf(M0 - B0), a1 = __expf(M1 - B1);
+            n0 *= a0; d0 *= a0; n1 *= a1; d1 *= a1;
+#pragma unroll
+            for (int k = 0; k < PB; ++k) {
+                if (c0 + k < ns) {
+                    const float2 q0 = mls[h0 * ns + c0 + k], q1 = mls[h1 * ns + c0 + k];
+                    const float w0 = __expf(q0.x - B0), w1 = __expf(q1.x - B1);
+                    if (e0 < n_el) { n0 = fmaf(w0, o0[k], n0); d0 = fmaf(w0, q0.y, d0); }
+                    if (e1 < n_el) { n1 = fmaf(w1, o1[k], n1); d1 = fmaf(w1, q1.y, d1); }
+                }
+            }
+            M0 = B0;
+            M1 = B1;
+        }
+        if (e0 < n_el) p.attn[(size_t)l * g.Q + (size_t)hq0 * HD + e0] = n0 / d0;
+        if (e1 < n_el) p.attn[(size_t)l * g.Q + (size_t)hq0 * HD + e1] = n1 / d1;
     }
     return cons_publish(c, layer_cnt(p, l, C_ATTN), true, nullptr, ab);
 }

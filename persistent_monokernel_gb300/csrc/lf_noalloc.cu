@@ -37,7 +37,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 constexpr int kMaxCtas = 1024;
-constexpr int kAttnMinLen = 32;
+constexpr int kAttnMinLen = 64;
 constexpr long long kTimeoutNs = 2000000000LL;
 
 // The scratch.  Every GPU that loads the library holds these bytes until the
@@ -117,6 +117,7 @@ extern "C" LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_w
     }
     const int max_split = P / g.Hkv > 1 ? P / g.Hkv : 1;
     int act = lfk::MAX_GROUP * g.hd + g.hd + lfk::NCW * (g.hd + 2);
+    if (2 * g.group * max_split > act) act = 2 * g.group * max_split;
     const int dims[] = {g.d, g.Q, g.F};
     for (int v : dims) act = v > act ? v : act;
     act = (act + 3) / 4 * 4;

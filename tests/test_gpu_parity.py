@@ -225,3 +225,43 @@ def test_bounded_wait_runs_out_and_the_handle_recovers(pm):
     got = dec.decode(6).cpu().numpy()
     assert dec.sync() == 0
     assert np.array_equal(got, want)
+
+
+@pytest.mark.parametrize("cfg,prompt_len,wseed", [
+    (MODELS["tiny"], 3000, 0),                                        # 38 pieces per KV head
+    (ModelConfig("gqa128-long", 1, 512, 8, 2, 128, 1024, 2000), 2000, 24),
+])
+def test_long_context_parity(pm, cfg, prompt_len, wseed):
+    """Split-KV attention over thousands of cached positions: many pieces,
+    several combine batches, hd 64 (MHA) and hd 128 (GQA)."""
+    n = 12
+    dec, orc, _ = _setup(pm, cfg, wseed, prompt_len + n)
+    prompt = make_prompt(cfg.vocab, prompt_len, wseed + 100)
+    toks, lg, ref = _forced_run(pm, dec, orc, cfg, prompt, n, wseed + 200)
+    compare_logits(lg, ref)
+    check_tokens(toks, ref, 0.0, 0, 0, prompt_len - 1)
+
+
+def test_full_size_2p3b_decoder_parity(pm):
+    """The ~2.3B workload's decoder at its full size and launch configuration
+    (the bench's grid), on a short sequence the oracle can follow."""
+    wl = WORKLOADS["2.3b"]
+    cfg = wl.model
+    dec, orc, _ = _setup(pm, cfg, wl.weight_seed, 64)
+    prompt = make_prompt(cfg.vocab, 24, wl.prompt_seed)
+    toks, lg, ref = _forced_run(pm, dec, orc, cfg, prompt, 8, 55)
+    compare_logits(lg, ref)
+    assert check_tokens(toks, ref, 0.0, 0, 0, 23) >= 6
+
+
+def test_full_size_8b_sampled_parity(pm):
+    """The 8B-shape workload's decoder at full size, sampled in-kernel at
+    T = 0.8, top-k 50 with its Philox seed, against the oracle's choice."""
+    wl = WORKLOADS["8b"]
+    cfg = wl.model
+    dec, orc, _ = _setup(pm, cfg, wl.weight_seed, 32)
+    prompt = make_prompt(cfg.vocab, 8, wl.prompt_seed)
+    toks, lg, ref = _forced_run(pm, dec, orc, cfg, prompt, 6, 56, T=wl.temperature, top_k=wl.top_k,
+                                seed=wl.sample_seed)
+    compare_logits(lg, ref)
+    check_tokens(toks, ref, wl.temperature, wl.top_k, wl.sample_seed, 7)
