@@ -211,12 +211,15 @@ LF_API lf_status lf_get_info(const lf_handle *h, lf_info *out);
 
 /* Stage trace (profiling aid).  lf_enable_trace(h, n) makes every later
  * lf_prefill / lf_decode launch of the persistent schedules record, for its
- * first n steps, six %globaltimer stamps (ns) per (step, slot, CTA): [0] the
+ * first n steps, eight %globaltimer stamps (ns) per (step, slot, CTA): [0] the
  * stage was entered, [1] its inputs were ready, [2] its inputs were loaded,
  * [3] it was published, [4] GEMV: first tile done / attention: K/V positions
- * done, [5] attention: piece partial published.  slot = 5 * layer + {0 QKV,
+ * done, [5] GEMV: first weight chunk in hand / attention: piece partial
+ * published, [6] and [7] the producer warp issued the stage's first and last
+ * weight (or K/V) chunk, [8] (a count, not a time) GEMV chunks that had not
+ * landed in shared memory when first asked for.  slot = 5 * layer + {0 QKV,
  * 1 attention, 2 O, 3 gate/up, 4 down}; slot 5 * n_layers is the LM head and
- * sampling.  Layout: [step][slot][cta][6] uint64, zero where nothing was
+ * sampling.  Layout: [step][slot][cta][9] uint64, zero where nothing was
  * recorded.  n = 0 disables tracing.  lf_read_trace synchronizes the device,
  * sets *n_out to the number of words and, if host_out is not NULL, copies
  * them there (capacity in words). */

@@ -14,7 +14,6 @@ namespace lfk {
 
 constexpr int KC = 256;               // weight columns per column group (32 lanes x 8 FP16)
 constexpr int KC_BYTES = KC * 2;      // bytes of one row of one column group
-constexpr int CHUNK_MAX = 32768;      // largest streamed GEMV chunk (bytes)
 constexpr int TILE_ROWS = 32;         // rows of one GEMV tile (4 per consumer warp)
 constexpr int NCW = 8;                // consumer warps
 constexpr int NCT = NCW * 32;         // consumer threads
@@ -24,6 +23,7 @@ constexpr int ATT_CHUNK_BYTES = 16384;// K + V bytes of one attention sub-block
 constexpr int MAX_TOPK = 64;
 constexpr int MAX_GROUP = 8;          // query heads per KV head
 constexpr int CNT_STRIDE = 32;        // uint32 words between counters (one 128-byte line each)
+constexpr int PART_BUFS = 8;          // rotating per-tile partial-sum buffers of a GEMV stage
 
 enum Stage { ST_QKV = 0, ST_O = 1, ST_GU = 2, ST_D = 3, ST_LM = 4, N_GEMV = 5 };
 enum LayerCounter { C_QKV = 0, C_ATTN = 1, C_O = 2, C_GU = 3, C_D = 4, N_LAYER_CNT = 5 };
@@ -59,17 +59,6 @@ __host__ __device__ inline StageGeom stage_geom(const Geo &g, int s)
 }
 
 __host__ __device__ inline int units_per_tile(int rpu) { return TILE_ROWS / rpu; }
-// Column groups per streamed chunk of a tile with R rows and K columns: the
-// largest m in {8, 4, 2, 1} that divides K/256 and keeps R x 256m FP16 values
-// within CHUNK_MAX bytes.  Larger chunks amortise the per-chunk cost of the
-// ring (one TMA issue, one mbarrier round trip).
-__host__ __device__ inline int chunk_groups(int R, int K)
-{
-    const int ng = K / KC;
-    for (int m = 8; m > 1; m >>= 1)
-        if (ng % m == 0 && R * m * KC_BYTES <= CHUNK_MAX) return m;
-    return 1;
-}
 __host__ __device__ inline int tiles_of(int n_units, int rpu)
 {
     return n_units <= 0 ? 0 : ceil_div(n_units, units_per_tile(rpu));
@@ -109,8 +98,8 @@ __host__ __device__ inline int attn_sub_positions(int hd) { return ATT_CHUNK_BYT
 // Per-CTA plan: unit ranges of the five GEMV stages and the byte offsets of
 // this CTA's weight stream.  The stream of CTA b is laid out as
 //   [layer 0: QKV tiles | O tiles | GU tiles | D tiles] ... [layer L-1: ...] [LM-head tiles]
-// and each tile as K/(256m) chunks of (R rows x 256m columns), row-major inside
-// a chunk, m = chunk_groups(R, K).
+// and each tile as K/256 chunks of (R rows x 256 columns), row-major inside
+// a chunk.
 struct CtaPlan {
     int u0[N_GEMV], u1[N_GEMV];
     unsigned long long base;          // byte offset of the stream in the repacked buffer
@@ -180,7 +169,11 @@ struct Params {
 // loaded, stage published, and two stage-specific points (GEMV: first chunk
 // acquired, last chunk released; attention: K/V positions done, piece partial
 // published).
-enum TraceStamp { TR_ENTER = 0, TR_READY = 1, TR_LOADED = 2, TR_DONE = 3, TR_X1 = 4, TR_X2 = 5, TR_N = 6 };
+// The producer adds when it issued the first and the last chunk of the sub-stage.
+// TR_WAITS is a count, not a time: the stage's weight chunks that were not yet
+// in shared memory when thread 0 first asked for them.
+enum TraceStamp { TR_ENTER = 0, TR_READY = 1, TR_LOADED = 2, TR_DONE = 3, TR_X1 = 4, TR_X2 = 5, TR_P0 = 6, TR_P1 = 7,
+                  TR_WAITS = 8, TR_N = 9 };
 __host__ __device__ inline int trace_slots(int L) { return 5 * L + 1; }
 
 }  // namespace lfk

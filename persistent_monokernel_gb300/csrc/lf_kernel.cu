@@ -42,34 +42,43 @@ namespace lfk {
 // ---------------------------------------------------------------- shared memory
 
 struct SmemLayout {
-    unsigned ring, act, lmkeys, res, full, empty, chunk_end, red, hist, misc, total;
+    unsigned ring, act, lmkeys, res, full, empty, chunk_end, red, hist, misc, plan, total;
 };
 
 __host__ __device__ inline unsigned align_up(unsigned x, unsigned a) { return (x + a - 1) / a * a; }
 
 __host__ __device__ inline SmemLayout smem_layout(int ring_bytes, int act_floats, int lm_rows_max)
 {
+    // Fixed-size parts first: their offsets are compile-time constants, so
+    // their addresses cost no registers; the ring, the activation vector and
+    // the LM keys follow at offsets that depend on the model.
     SmemLayout s;
     unsigned o = 0;
-    s.ring = o;      o = align_up(o + (unsigned)ring_bytes, 128);
-    s.act = o;       o = align_up(o + 4u * (unsigned)act_floats, 128);
-    s.lmkeys = o;    o = align_up(o + 8u * (unsigned)lm_rows_max, 128);
-    s.res = o;       o = align_up(o + 4u * 2u * TILE_ROWS, 128);
+    s.res = o;       o = align_up(o + 4u * PART_BUFS * NCW * TILE_ROWS, 128);
     s.full = o;      o += 8u * TICKETS;
     s.empty = o;     o += 8u * TICKETS;
     s.chunk_end = o; o += 8u * TICKETS;
     s.red = o;       o = align_up(o + 4u * 64u, 16);
     s.hist = o;      o = align_up(o + 4u * 256u, 16);
     s.misc = o;      o = align_up(o + 4u * 64u, 128);
-    s.total = o;
+    s.plan = o;      o = align_up(o + (unsigned)sizeof(CtaPlan), 128);
+    s.ring = o;      o = align_up(o + (unsigned)ring_bytes, 128);
+    s.act = o;       o = align_up(o + 4u * (unsigned)act_floats, 128);
+    s.lmkeys = o;    o = align_up(o + 8u * (unsigned)lm_rows_max, 128);
+    // the GEMV reads whole 8-row blocks: keep 7 rows of readable bytes after the ring
+    const unsigned slack_end = s.ring + (unsigned)ring_bytes + 7u * KC_BYTES;
+    s.total = o > slack_end ? o : align_up(slack_end, 128);
     return s;
 }
 
-// misc word indices
-enum { M_FLAG = 0, M_TOKEN = 1, M_DIGIT = 2, M_REMAIN = 3, M_INV = 4 };
+// misc word indices; M_TCNT + b / M_TRED + b: arrivals at / reductions of
+// partial-sum buffer b (cumulative)
+enum { M_FLAG = 0, M_TOKEN = 1, M_DIGIT = 2, M_REMAIN = 3, M_INV = 4, M_TSEQ = 8, M_TCNT = 16, M_TRED = 24 };
 
 struct Ctx {
     const Params *p;
+    const CtaPlan *plan;  // this CTA's partition, copied to shared memory (global reads
+                          // after an ld.acquire miss L1 and cost an L2 round trip)
     uint8_t *ring;
     float *act;
     unsigned long long *lmkeys;
@@ -96,6 +105,12 @@ __device__ __forceinline__ void trace_mark(const Ctx &c, int step, int slot, int
 {
     const Params &p = *c.p;
     if (p.trace && c.tid == 0 && step < p.trace_steps)
+        p.trace[(((size_t)step * trace_slots(p.g.L) + slot) * p.P + c.b) * TR_N + stamp] = globaltimer_ns();
+}
+__device__ __forceinline__ void trace_mark_producer(const Ctx &c, int step, int slot, int stamp)
+{
+    const Params &p = *c.p;
+    if (p.trace && step < p.trace_steps)
         p.trace[(((size_t)step * trace_slots(p.g.L) + slot) * p.P + c.b) * TR_N + stamp] = globaltimer_ns();
 }
 
@@ -166,15 +181,19 @@ __device__ __forceinline__ bool wait_mbar(const Params &p, uint64_t *bar, unsign
 // Both sides place chunks identically: a chunk that would cross the end of the
 // ring starts at offset 0 instead.
 struct ConsRing {
-    unsigned n = 0;    // chunks consumed
-    unsigned off = 0;  // read offset
+    unsigned n = 0;       // chunks consumed
+    unsigned off = 0;     // read offset
+    unsigned waited = 0;  // chunks that had not landed when first asked for (for the trace)
     __device__ __forceinline__ const uint8_t *acquire(const Ctx &c, unsigned bytes, bool &ab)
     {
         if (off + bytes > (unsigned)c.p->ring_bytes) off = 0;
         const uint8_t *ptr = c.ring + off;
         off += bytes;
         bool fail = ab;
-        if (!fail) fail = !wait_mbar(*c.p, &c.full[n % TICKETS], (n / TICKETS) & 1u, 100);
+        if (!fail && !mbar_try_wait(&c.full[n % TICKETS], (n / TICKETS) & 1u)) {
+            ++waited;
+            fail = !wait_mbar(*c.p, &c.full[n % TICKETS], (n / TICKETS) & 1u, 100);
+        }
         if (__any_sync(0xffffffffu, fail)) {
             ab = true;
             return nullptr;
@@ -185,6 +204,20 @@ struct ConsRing {
     {
         __syncwarp();
         if (c.lane == 0) mbar_arrive(&c.empty[n % TICKETS]);
+        ++n;
+    }
+    // A chunk owned by one warp: the other warps only advance their cursor;
+    // the owner releases it for all NCW consumer warps at once.
+    __device__ __forceinline__ void skip(const Ctx &c, unsigned bytes)
+    {
+        if (off + bytes > (unsigned)c.p->ring_bytes) off = 0;
+        off += bytes;
+        ++n;
+    }
+    __device__ __forceinline__ void release_own(const Ctx &c)
+    {
+        __syncwarp();
+        if (c.lane == 0) mbar_arrive_cnt(&c.empty[n % TICKETS], NCW);
         ++n;
     }
 };
@@ -421,42 +454,51 @@ __device__ __forceinline__ bool load_act(const Ctx &c, const float *src32, const
     return cons_sync_or(ab);
 }
 
-// One GEMV tile: R rows (stored rows w, w+8, w+16, w+24 belong to warp w),
-// K columns in chunks of 256m columns from the ring.  Writes the R dot
-// products to res.
-__device__ __forceinline__ void gemv_tile(const Ctx &c, ConsRing &rc, int R, int K, float *res, bool &ab)
+// One weight chunk (R rows x 256 columns, row-major, R <= 32; column group
+// gcol of the tile) consumed by one warp: lane l takes columns 8l..8l+7 and
+// accumulates all R rows, so each lane carries R independent FMA chains.
+__device__ __forceinline__ void gemv_chunk(const Ctx &c, const uint8_t *ch, int R, int gcol,
+                                           float (&acc)[TILE_ROWS])
 {
-    const int w = c.warp, ln = c.lane;
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-    const int m = chunk_groups(R, K);
-    const int nch = K / (KC * m);
-    const float4 *xs = reinterpret_cast<const float4 *>(c.act);
-    for (int ch_i = 0; ch_i < nch; ++ch_i) {
-        const uint8_t *ch = rc.acquire(c, (unsigned)(R * m) * KC_BYTES, ab);
-        if (ab) break;
-        const uint4 *wp = reinterpret_cast<const uint4 *>(ch) + ln;
-        for (int gi = 0; gi < m; ++gi) {
-            const int gcol = ch_i * m + gi;
-            const float4 xa = xs[gcol * 64 + ln * 2];
-            const float4 xb = xs[gcol * 64 + ln * 2 + 1];
-            const uint4 *wg = wp + gi * 32;
-            if (w < R) a0 = dot8(wg[(size_t)w * 32 * m], xa, xb, a0);
-            if (w + 8 < R) a1 = dot8(wg[(size_t)(w + 8) * 32 * m], xa, xb, a1);
-            if (w + 16 < R) a2 = dot8(wg[(size_t)(w + 16) * 32 * m], xa, xb, a2);
-            if (w + 24 < R) a3 = dot8(wg[(size_t)(w + 24) * 32 * m], xa, xb, a3);
+    // 32-bit shared addresses: the lane's 16 bytes of row r sit at
+    // chunk + r * 512 + lane * 16, its 8 x values at act + gcol * 1024 + lane * 32.
+    const uint32_t xs = smem_u32(c.act) + (uint32_t)gcol * 1024u + (uint32_t)c.lane * 32u;
+    const float4 xa = lds_f4(xs);
+    const float4 xb = lds_f4(xs + 16u);
+    const uint32_t a0 = smem_u32(ch) + (uint32_t)c.lane * 16u;
+    // Rows in blocks of 8 at constant offsets: one branch per block, so the 8
+    // loads issue together and the 8 FMA chains interleave.  The last block
+    // may read up to 7 rows past the chunk (inside the ring, or in the slack
+    // the shared-memory layout keeps after it); those sums land in lanes
+    // >= R after the row reduction and are never used.
+#pragma unroll
+    for (int rb = 0; rb < TILE_ROWS; rb += 8) {
+        if (rb < R) {
+            uint4 wv[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) wv[r] = lds_u4(a0 + (uint32_t)(rb + r) * KC_BYTES);
+#pragma unroll
+            for (int r = 0; r < 8; ++r) acc[rb + r] = dot8(wv[r], xa, xb, acc[rb + r]);
         }
-        rc.release(c);
     }
-    a0 = warp_sum(a0);
-    a1 = warp_sum(a1);
-    a2 = warp_sum(a2);
-    a3 = warp_sum(a3);
-    if (ln == 0) {
-        if (w < R) res[w] = a0;
-        if (w + 8 < R) res[w + 8] = a1;
-        if (w + 16 < R) res[w + 16] = a2;
-        if (w + 24 < R) res[w + 24] = a3;
+}
+
+// Sum each of 32 per-lane values over the warp; afterwards lane r holds the
+// sum of value r (31 shuffles: each level hands half of the values to the
+// partner lane).
+__device__ __forceinline__ float reduce_rows32(float (&v)[TILE_ROWS], int lane)
+{
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        const bool upper = (lane & off) != 0;
+#pragma unroll
+        for (int i = 0; i < off; ++i) {
+            const float send = upper ? v[i] : v[i + off];
+            const float keep = upper ? v[i + off] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
     }
+    return v[0];
 }
 
 // Token fed to forward pass `step` (decode: after its counter was acquired).
@@ -484,7 +526,7 @@ __device__ __forceinline__ bool stage_gemv(const Ctx &c, ConsRing &rc, int s, in
 {
     const Params &p = *c.p;
     const Geo &g = p.g;
-    const CtaPlan &pl = p.plans[c.b];
+    const CtaPlan &pl = *c.plan;
     const StageGeom sg = stage_geom(g, s);
     const int pos = p.pos0 + step;
     // layer 0 reads the embedding row of the step's token (after the stage's wait)
@@ -519,25 +561,88 @@ __device__ __forceinline__ bool stage_gemv(const Ctx &c, ConsRing &rc, int s, in
     if (ab) return true;
     const int tslot = s == ST_LM ? 5 * g.L : 5 * l + (s == ST_QKV ? 0 : s + 1);
     trace_mark(c, step, tslot, TR_LOADED);
+    const unsigned waited0 = rc.waited;
 
     const int u0 = pl.u0[s], n = pl.u1[s] - u0;
     const int nt = tiles_of(n, sg.rows_per_unit);
+    int jc = 0;   // chunk index within the stage: chunk jc belongs to warp jc mod NCW
     for (int t = 0; t < nt; ++t) {
         int a, bnd;
         tile_range(u0, n, nt, t, a, bnd);
         const int nu = bnd - a;
         const int R = nu * sg.rows_per_unit;
-        float *res = c.res + (t & 1) * TILE_ROWS;
-        gemv_tile(c, rc, R, sg.K, res, ab);
-        if (t == 0) trace_mark(c, step, tslot, TR_X1);
-        if (cons_sync_or(ab)) return true;
-        // ---- epilogue
-        for (int i = c.tid; i < nu; i += NCT) {
+        const int nch = sg.K / KC;
+        const unsigned bytes = (unsigned)R * KC_BYTES;
+        float acc[TILE_ROWS];
+#pragma unroll
+        for (int r = 0; r < TILE_ROWS; ++r) acc[r] = 0.f;
+        bool mine = false;
+        for (int k = 0; k < nch; ++k, ++jc) {
+            if (jc % NCW != c.warp) {
+                rc.skip(c, bytes);
+                continue;
+            }
+            const uint8_t *ch = rc.acquire(c, bytes, ab);
+            if (ab) break;
+            if (t == 0 && !mine) trace_mark(c, step, tslot, TR_X2);
+            gemv_chunk(c, ch, R, k, acc);
+            mine = true;
+            rc.release_own(c);
+        }
+        if (ab) break;
+        // ---- per-warp row sums -> partial buffer; the last warp to arrive reduces
+        const float v = mine ? reduce_rows32(acc, c.lane) : 0.f;
+        const unsigned seq = c.misc[M_TSEQ] + (unsigned)t;      // tile sequence number (kernel-wide)
+        const int buf = (int)(seq % PART_BUFS);
+        const unsigned use = seq / PART_BUFS;
+        // the buffer's previous use must have been reduced before it is overwritten
+        bool stuck = false;
+        if (c.lane == 0) {
+            unsigned long long t0 = 0;
+            for (unsigned it = 0; *reinterpret_cast<volatile unsigned *>(&c.misc[M_TRED + buf]) != use; ++it) {
+                if ((it & 255u) != 255u) continue;
+                if (ld_relaxed(p.abort_flag)) { stuck = true; break; }
+                const unsigned long long now = globaltimer_ns();
+                if (t0 == 0) t0 = now;
+                else if ((long long)(now - t0) > p.timeout_ns) {
+                    raise_error(p, STATUS_TIMEOUT, 110, l, step);
+                    stuck = true;
+                    break;
+                }
+            }
+        }
+        if (__shfl_sync(0xffffffffu, (int)stuck, 0)) {
+            ab = true;
+            break;
+        }
+        float *part = c.res + (size_t)buf * NCW * TILE_ROWS;
+        part[c.warp * TILE_ROWS + c.lane] = v;
+        __syncwarp();
+        unsigned old = 0;
+        if (c.lane == 0) {
+            __threadfence_block();
+            old = atomicAdd(&c.misc[M_TCNT + buf], 1u);
+        }
+        old = __shfl_sync(0xffffffffu, old, 0);
+        if (old != use * NCW + (NCW - 1)) continue;
+        __threadfence_block();
+        float sum = 0.f;
+#pragma unroll
+        for (int w = 0; w < NCW; ++w) sum += *reinterpret_cast<volatile float *>(&part[w * TILE_ROWS + c.lane]);
+        __syncwarp();
+        if (c.lane == 0) {
+            __threadfence_block();
+            *reinterpret_cast<volatile unsigned *>(&c.misc[M_TRED + buf]) = use + 1;
+        }
+        // ---- epilogue: lane i handles unit a + i (pair stages: rows i and i + nu)
+        const float partner = __shfl_sync(0xffffffffu, sum, (c.lane + nu) & 31);
+        const int i = c.lane;
+        if (i < nu) {
             const int u = a + i;
             if (s == ST_QKV) {
                 const int half = g.hd / 2;
                 const int hh = u / half, j = u % half;
-                const float v0 = res[i] * inv, v1 = res[i + nu] * inv;
+                const float v0 = sum * inv, v1 = partner * inv;
                 if (hh < g.Hq + g.Hkv) {
                     const float2 cs = __ldg(p.rope + (size_t)pos * half + j);
                     const float r0 = v0 * cs.x - v1 * cs.y;
@@ -548,27 +653,28 @@ __device__ __forceinline__ bool stage_gemv(const Ctx &c, ConsRing &rc, int s, in
                         q[j + half] = r1;
                     } else {
                         const int kvh = hh - g.Hq;
-                        __half *k = p.kc + (((size_t)l * g.Hkv + kvh) * g.max_seq + pos) * g.hd;
-                        k[j] = __float2half_rn(r0);
-                        k[j + half] = __float2half_rn(r1);
+                        __half *kr = p.kc + (((size_t)l * g.Hkv + kvh) * g.max_seq + pos) * g.hd;
+                        kr[j] = __float2half_rn(r0);
+                        kr[j + half] = __float2half_rn(r1);
                     }
                 } else {
                     const int kvh = hh - g.Hq - g.Hkv;
-                    __half *v = p.vc + (((size_t)l * g.Hkv + kvh) * g.max_seq + pos) * g.hd;
-                    v[j] = __float2half_rn(v0);
-                    v[j + half] = __float2half_rn(v1);
+                    __half *vr = p.vc + (((size_t)l * g.Hkv + kvh) * g.max_seq + pos) * g.hd;
+                    vr[j] = __float2half_rn(v0);
+                    vr[j + half] = __float2half_rn(v1);
                 }
+                fence_proxy_async_global();   // K/V rows are read by TMA in later steps
             } else if (s == ST_O) {
                 const float xin = (l == 0) ? __half2float(p.embed[(size_t)tok * g.d + u])
                                            : __ldcg(p.xout + (size_t)(l - 1) * g.d + u);
-                p.xattn[(size_t)l * g.d + u] = xin + res[i];
+                p.xattn[(size_t)l * g.d + u] = xin + sum;
             } else if (s == ST_GU) {
-                const float gt = res[i] * inv, up = res[i + nu] * inv;
+                const float gt = sum * inv, up = partner * inv;
                 p.hbuf[(size_t)l * g.F + u] = gt / (1.0f + expf(-gt)) * up;
             } else if (s == ST_D) {
-                p.xout[(size_t)l * g.d + u] = __ldcg(p.xattn + (size_t)l * g.d + u) + res[i];
+                p.xout[(size_t)l * g.d + u] = __ldcg(p.xattn + (size_t)l * g.d + u) + sum;
             } else {
-                const float logit = res[i] * inv;
+                const float logit = sum * inv;
                 if (p.debug_logits) p.debug_logits[(size_t)step * g.V + u] = logit;
                 float keyv = logit;
                 const bool all_vocab = p.temperature > 0.f && p.top_k != 1 && (p.top_k <= 0 || p.top_k >= g.V);
@@ -576,8 +682,13 @@ __device__ __forceinline__ bool stage_gemv(const Ctx &c, ConsRing &rc, int s, in
                 c.lmkeys[u - u0] = sel_key(keyv, u);
             }
         }
-        if (s == ST_QKV) fence_proxy_async_global();  // K/V rows are read by TMA in later steps
     }
+    // every warp counts the same tiles: advance the kernel-wide tile sequence
+    // (after the stage's closing barrier nobody reads the old value)
+    if (cons_sync_or(ab)) return true;
+    if (c.tid == 0) c.misc[M_TSEQ] += (unsigned)nt;
+    if (p.trace && c.tid == 0 && step < p.trace_steps)
+        p.trace[(((size_t)step * trace_slots(g.L) + tslot) * p.P + c.b) * TR_N + TR_WAITS] = rc.waited - waited0;
     return false;
 }
 
@@ -859,13 +970,15 @@ __device__ __forceinline__ bool radix_select(const Ctx &c, const unsigned long l
     return false;
 }
 
-__device__ __forceinline__ bool stage_lm_sample(const Ctx &c, ConsRing &rc, int step, bool ab)
+// Token choice after the LM-head tiles of this CTA have put their selection
+// keys in shared memory: per-CTA candidates, then the last CTA to arrive picks
+// the token and publishes it.
+__device__ __forceinline__ bool stage_lm_sample(const Ctx &c, int step, bool ab)
 {
     const Params &p = *c.p;
     const Geo &g = p.g;
-    const CtaPlan &pl = p.plans[c.b];
+    const CtaPlan &pl = *c.plan;
     const int pos = p.pos0 + step;
-    ab = stage_gemv(c, rc, ST_LM, g.L - 1, step, ab);
     if (cons_sync_or(ab)) return true;
 
     const bool greedy = !(p.temperature > 0.f) || p.top_k == 1;
@@ -956,6 +1069,10 @@ __device__ __forceinline__ bool stage_lm_sample(const Ctx &c, ConsRing &rc, int 
 
 // ---------------------------------------------------------------- consumer
 
+// The consumer walks the sub-stages of every step -- for each layer QKV,
+// attention, O, gate/up, down, then the LM head -- through ONE loop body, so
+// that each stage's code exists once in the kernel and stays warm in the
+// instruction cache from one layer to the next.
 __device__ void consumer(const Ctx &c)
 {
     const Params &p = *c.p;
@@ -964,37 +1081,56 @@ __device__ void consumer(const Ctx &c)
     const bool ab = false;
     const bool grid = p.sched == SCHED_GRID;
     const bool decode = p.mode == MODE_DECODE;
+    const int n_sub = 5 * g.L + (decode ? 1 : 0);
     for (int step = 0; step < p.n_steps; ++step) {
         const unsigned e = p.epoch0 + (unsigned)step;
-        // decode: the input token of step > 0 is the previous step's choice
-        if (decode && step > 0 && p.sched == SCHED_FLAGS && stage_active(p, 0, SID_QKV)) {
-            if (cons_wait(c, p.tok_cnt, p.tok_base + (unsigned)step, 200, 0, step, ab)) return;
-        }
-        for (int l = 0; l < g.L; ++l) {
-            if (stage_active(p, l, SID_QKV)) {
-                trace_mark(c, step, 5 * l + 0, TR_ENTER);
-                // QKV(l) reads x_out(l-1), or for l = 0 the embedding of the step's token
-                int gstep = step, gl = l - 1, gslot = 4;
-                if (l == 0) {
+        for (int k = 0; k < n_sub; ++k) {
+            const bool lm = k == 5 * g.L;
+            const int l = lm ? g.L - 1 : k / 5;
+            const int sid = lm ? SID_LM : k % 5;
+            if (!stage_active(p, l, sid)) continue;
+            trace_mark(c, step, k, TR_ENTER);
+            // ---- what this sub-stage waits for: the producer counter (flag
+            // schedule) or the grid barrier that closes the previous sub-stage
+            const unsigned *ctr = nullptr;
+            unsigned target = 0;
+            int gstep = step, gl = l, gslot = sid - 1;
+            if (sid == SID_QKV) {
+                if (l > 0) {
+                    ctr = layer_cnt(p, l - 1, C_D);
+                    target = (e + 1u) * p.n_prod[ST_D];
+                    gl = l - 1;
+                    gslot = 4;
+                } else {
+                    if (decode && step > 0) {
+                        ctr = p.tok_cnt;                        // the previous step's token
+                        target = p.tok_base + (unsigned)step;
+                    }
                     gstep = step - 1;
                     gl = g.L - 1;
                     gslot = step > 0 ? (decode ? 5 : 4) : -1;
                 }
-                if (stage_wait(c, l > 0 ? layer_cnt(p, l - 1, C_D) : nullptr, (e + 1u) * p.n_prod[ST_D], gstep, gl,
-                               gslot, step, l, 1, ab))
-                    return;
-                trace_mark(c, step, 5 * l + 0, TR_READY);
-                if (stage_gemv(c, rc, ST_QKV, l, step, ab)) return;
-                const bool withhold = decode && step == p.fault_step && l == 0;
-                if (cons_publish(c, layer_cnt(p, l, C_QKV), !withhold, (grid && !withhold) ? p.gbar : nullptr, ab))
-                    return;
-                trace_mark(c, step, 5 * l + 0, TR_DONE);
+            } else if (sid == SID_ATTN) {
+                ctr = layer_cnt(p, l, C_QKV);
+                target = (e + 1u) * p.n_prod[ST_QKV];
+            } else if (sid == SID_O) {
+                ctr = layer_cnt(p, l, C_ATTN);
+                target = (e + 1u) * (unsigned)g.Hkv;
+            } else if (sid == SID_GU) {
+                ctr = layer_cnt(p, l, C_O);
+                target = (e + 1u) * p.n_prod[ST_O];
+            } else if (sid == SID_D) {
+                ctr = layer_cnt(p, l, C_GU);
+                target = (e + 1u) * p.n_prod[ST_GU];
+            } else {
+                ctr = layer_cnt(p, g.L - 1, C_D);
+                target = (e + 1u) * p.n_prod[ST_D];
+                gslot = 4;
             }
-            if (stage_active(p, l, SID_ATTN)) {
-                trace_mark(c, step, 5 * l + 1, TR_ENTER);
-                if (stage_wait(c, layer_cnt(p, l, C_QKV), (e + 1u) * p.n_prod[ST_QKV], step, l, 0, step, l, 2, ab))
-                    return;
-                trace_mark(c, step, 5 * l + 1, TR_READY);
+            if (stage_wait(c, ctr, target, gstep, gl, gslot, step, l, 1 + sid, ab)) return;
+            trace_mark(c, step, k, TR_READY);
+
+            if (sid == SID_ATTN) {
                 const int ctx = p.pos0 + step + 1;
                 const AttnSplit sp = attn_split(ctx, p.P, g.Hkv, p.attn_min_len);
                 const int U = g.Hkv * sp.n_split;
@@ -1005,44 +1141,19 @@ __device__ void consumer(const Ctx &c)
                     if (stop) return;
                 }
                 if (grid && cons_publish(c, nullptr, false, p.gbar, ab)) return;
-                trace_mark(c, step, 5 * l + 1, TR_DONE);
+            } else {
+                const int st = sid == SID_QKV ? ST_QKV : sid == SID_O ? ST_O : sid == SID_GU ? ST_GU
+                                                       : sid == SID_D ? ST_D : ST_LM;
+                if (stage_gemv(c, rc, st, l, step, ab)) return;
+                if (lm) {
+                    if (stage_lm_sample(c, step, ab)) return;
+                } else {
+                    const bool withhold = decode && step == p.fault_step && l == 0 && sid == SID_QKV;
+                    if (cons_publish(c, layer_cnt(p, l, sid), !withhold, (grid && !withhold) ? p.gbar : nullptr, ab))
+                        return;
+                }
             }
-            if (stage_active(p, l, SID_O)) {
-                trace_mark(c, step, 5 * l + 2, TR_ENTER);
-                if (stage_wait(c, layer_cnt(p, l, C_ATTN), (e + 1u) * (unsigned)g.Hkv, step, l, 1, step, l, 3, ab))
-                    return;
-                trace_mark(c, step, 5 * l + 2, TR_READY);
-                if (stage_gemv(c, rc, ST_O, l, step, ab)) return;
-                if (cons_publish(c, layer_cnt(p, l, C_O), true, grid ? p.gbar : nullptr, ab)) return;
-                trace_mark(c, step, 5 * l + 2, TR_DONE);
-            }
-            if (stage_active(p, l, SID_GU)) {
-                trace_mark(c, step, 5 * l + 3, TR_ENTER);
-                if (stage_wait(c, layer_cnt(p, l, C_O), (e + 1u) * p.n_prod[ST_O], step, l, 2, step, l, 4, ab))
-                    return;
-                trace_mark(c, step, 5 * l + 3, TR_READY);
-                if (stage_gemv(c, rc, ST_GU, l, step, ab)) return;
-                if (cons_publish(c, layer_cnt(p, l, C_GU), true, grid ? p.gbar : nullptr, ab)) return;
-                trace_mark(c, step, 5 * l + 3, TR_DONE);
-            }
-            if (stage_active(p, l, SID_D)) {
-                trace_mark(c, step, 5 * l + 4, TR_ENTER);
-                if (stage_wait(c, layer_cnt(p, l, C_GU), (e + 1u) * p.n_prod[ST_GU], step, l, 3, step, l, 5, ab))
-                    return;
-                trace_mark(c, step, 5 * l + 4, TR_READY);
-                if (stage_gemv(c, rc, ST_D, l, step, ab)) return;
-                if (cons_publish(c, layer_cnt(p, l, C_D), true, grid ? p.gbar : nullptr, ab)) return;
-                trace_mark(c, step, 5 * l + 4, TR_DONE);
-            }
-        }
-        if (decode && stage_active(p, 0, SID_LM)) {
-            trace_mark(c, step, 5 * g.L, TR_ENTER);
-            if (stage_wait(c, layer_cnt(p, g.L - 1, C_D), (e + 1u) * p.n_prod[ST_D], step, g.L - 1, 4, step, g.L - 1,
-                           6, ab))
-                return;
-            trace_mark(c, step, 5 * g.L, TR_READY);
-            if (stage_lm_sample(c, rc, step, ab)) return;
-            trace_mark(c, step, 5 * g.L, TR_DONE);
+            trace_mark(c, step, k, TR_DONE);
         }
     }
 }
@@ -1076,7 +1187,7 @@ __device__ const __half *src_row(const Geo &g, const RepackSrc &w, int s, int l,
 __device__ __forceinline__ bool produce_tiles(const Ctx &c, ProdRing &pr, int s, int l, int step)
 {
     const Params &p = *c.p;
-    const CtaPlan &pl = p.plans[c.b];
+    const CtaPlan &pl = *c.plan;
     const StageGeom sg = stage_geom(p.g, s);
     const int u0 = pl.u0[s], n = pl.u1[s] - u0;
     const int nt = tiles_of(n, sg.rows_per_unit);
@@ -1086,9 +1197,8 @@ __device__ __forceinline__ bool produce_tiles(const Ctx &c, ProdRing &pr, int s,
         int a, bnd;
         tile_range(u0, n, nt, t, a, bnd);
         const int R = (bnd - a) * sg.rows_per_unit;
-        const int m = chunk_groups(R, sg.K);
-        const unsigned bytes = (unsigned)(R * m) * KC_BYTES;
-        const int nch = sg.K / (KC * m);
+        const unsigned bytes = (unsigned)R * KC_BYTES;
+        const int nch = sg.K / KC;
         for (int k = 0; k < nch; ++k) {
             if (pr.pf_dist)
                 pr.prefetch_to((unsigned long long)step * pr.token_bytes + (unsigned long long)(src - pr.stream_base) +
@@ -1101,12 +1211,12 @@ __device__ __forceinline__ bool produce_tiles(const Ctx &c, ProdRing &pr, int s,
 }
 
 // Producer variant used by lf_generate_noalloc, whose weights stay in the
-// caller's row-major layout: each chunk (R rows x 256m columns) is gathered
-// with one bulk copy of 512m bytes per row into the same ring layout.
+// caller's row-major layout: each chunk (R rows x 256 columns) is gathered
+// with one 512-byte bulk copy per row into the same ring layout.
 __device__ __forceinline__ bool produce_tiles_direct(const Ctx &c, ProdRing &pr, const RepackSrc &w, int s, int l, int step)
 {
     const Params &p = *c.p;
-    const CtaPlan &pl = p.plans[c.b];
+    const CtaPlan &pl = *c.plan;
     const StageGeom sg = stage_geom(p.g, s);
     const int u0 = pl.u0[s], n = pl.u1[s] - u0;
     const int nt = tiles_of(n, sg.rows_per_unit);
@@ -1115,9 +1225,8 @@ __device__ __forceinline__ bool produce_tiles_direct(const Ctx &c, ProdRing &pr,
         tile_range(u0, n, nt, t, a, bnd);
         const int nu = bnd - a;
         const int R = nu * sg.rows_per_unit;
-        const int m = chunk_groups(R, sg.K);
-        const unsigned row_bytes = (unsigned)m * KC_BYTES;
-        const int nch = sg.K / (KC * m);
+        const unsigned row_bytes = KC_BYTES;
+        const int nch = sg.K / KC;
         for (int k = 0; k < nch; ++k) {
             const int o = pr.reserve(c, (unsigned)R * row_bytes);
             if (o < 0) return false;
@@ -1126,7 +1235,7 @@ __device__ __forceinline__ bool produce_tiles_direct(const Ctx &c, ProdRing &pr,
             for (int r = 0; r < R; ++r) {
                 const int unit = a + (sg.rows_per_unit == 2 ? r % nu : r);
                 const int part = sg.rows_per_unit == 2 ? r / nu : 0;
-                const __half *src = src_row(p.g, w, s, l, unit, part) + (size_t)k * KC * m;
+                const __half *src = src_row(p.g, w, s, l, unit, part) + (size_t)k * KC;
                 bulk_g2s(c.ring + o + r * row_bytes, src, row_bytes, bar, pr.pol);
             }
             ++pr.n;
@@ -1150,7 +1259,7 @@ __device__ void producer(const Ctx &c, const RepackSrc *w)
     pr.pol_kv = policy_evict_normal();
     pr.pol_pf = p.l2_prefetch_last ? policy_evict_last() : policy_evict_normal();
     if (!kDirect && p.only_stage < 0 && p.l2_prefetch_bytes > 0) {
-        const CtaPlan &pl = p.plans[c.b];
+        const CtaPlan &pl = *c.plan;
         pr.stream_base = p.wstream + pl.base;
         pr.token_bytes = pl.lm_off;
         if (p.mode == MODE_DECODE)
@@ -1159,40 +1268,47 @@ __device__ void producer(const Ctx &c, const RepackSrc *w)
         pr.pf_dist = (unsigned long long)p.l2_prefetch_bytes;
     }
     bool ok = true;
+    const int n_sub = 5 * g.L + (p.mode == MODE_DECODE ? 1 : 0);
     for (int step = 0; step < p.n_steps && ok; ++step) {
         step_now = step;
         const unsigned e = p.epoch0 + (unsigned)step;
         const int pos = p.pos0 + step;
-        for (int l = 0; l < g.L && ok; ++l) {
-            if (stage_active(p, l, SID_QKV)) ok = tiles(c, pr, w, ST_QKV, l);
-            if (ok && stage_active(p, l, SID_ATTN)) {
-                const AttnSplit sp = attn_split(pos + 1, p.P, g.Hkv, p.attn_min_len);
-                const int U = g.Hkv * sp.n_split;
-                const int S = attn_sub_positions(g.hd);
-                bool guarded = (step == 0);
-                for (int u = attn_unit_first(c.b, l, U, p.P); u < U && ok; u += p.P) {
-                    const int gkv = u / sp.n_split, cp = u % sp.n_split;
-                    const int j0 = cp * sp.per;
-                    const int jr = min(min(j0 + sp.per, pos + 1), pos);
-                    if (jr > j0 && !guarded) {
-                        // positions < pos of step > 0 were written by the previous step's QKV stage
-                        ok = wait_counter(p, layer_cnt(p, l, C_QKV), e * p.n_prod[ST_QKV], 102, l, step);
-                        fence_proxy_async_global();
-                        guarded = true;
-                    }
-                    const size_t base = (((size_t)l * g.Hkv + gkv) * g.max_seq) * g.hd;
-                    for (int jb = j0; jb < jr && ok; jb += S) {
-                        const int nb = min(S, jr - jb);
-                        const unsigned hb = (unsigned)nb * g.hd * 2u;
-                        ok = pr.emit2(c, p.kc + base + (size_t)jb * g.hd, p.vc + base + (size_t)jb * g.hd, hb);
-                    }
+        for (int k = 0; k < n_sub && ok; ++k) {
+            const bool lm = k == 5 * g.L;
+            const int l = lm ? 0 : k / 5;
+            const int sid = lm ? SID_LM : k % 5;
+            if (!stage_active(p, l, sid)) continue;
+            trace_mark_producer(c, step, k, TR_P0);
+            if (sid != SID_ATTN) {
+                const int st = sid == SID_QKV ? ST_QKV : sid == SID_O ? ST_O : sid == SID_GU ? ST_GU
+                                                       : sid == SID_D ? ST_D : ST_LM;
+                ok = tiles(c, pr, w, st, l);
+                trace_mark_producer(c, step, k, TR_P1);
+                continue;
+            }
+            const AttnSplit sp = attn_split(pos + 1, p.P, g.Hkv, p.attn_min_len);
+            const int U = g.Hkv * sp.n_split;
+            const int S = attn_sub_positions(g.hd);
+            bool guarded = (step == 0);
+            for (int u = attn_unit_first(c.b, l, U, p.P); u < U && ok; u += p.P) {
+                const int gkv = u / sp.n_split, cp = u % sp.n_split;
+                const int j0 = cp * sp.per;
+                const int jr = min(min(j0 + sp.per, pos + 1), pos);
+                if (jr > j0 && !guarded) {
+                    // positions < pos of step > 0 were written by the previous step's QKV stage
+                    ok = wait_counter(p, layer_cnt(p, l, C_QKV), e * p.n_prod[ST_QKV], 102, l, step);
+                    fence_proxy_async_global();
+                    guarded = true;
+                }
+                const size_t base = (((size_t)l * g.Hkv + gkv) * g.max_seq) * g.hd;
+                for (int jb = j0; jb < jr && ok; jb += S) {
+                    const int nb = min(S, jr - jb);
+                    const unsigned hb = (unsigned)nb * g.hd * 2u;
+                    ok = pr.emit2(c, p.kc + base + (size_t)jb * g.hd, p.vc + base + (size_t)jb * g.hd, hb);
                 }
             }
-            if (ok && stage_active(p, l, SID_O)) ok = tiles(c, pr, w, ST_O, l);
-            if (ok && stage_active(p, l, SID_GU)) ok = tiles(c, pr, w, ST_GU, l);
-            if (ok && stage_active(p, l, SID_D)) ok = tiles(c, pr, w, ST_D, l);
+            trace_mark_producer(c, step, k, TR_P1);
         }
-        if (ok && p.mode == MODE_DECODE && stage_active(p, 0, SID_LM)) ok = tiles(c, pr, w, ST_LM, 0);
     }
     if (!ok) pr.drain(c);
 }
@@ -1216,6 +1332,8 @@ __device__ __forceinline__ void monokernel_body(const Params &p, const RepackSrc
     c.red = reinterpret_cast<float *>(smem + L.red);
     c.hist = reinterpret_cast<unsigned *>(smem + L.hist);
     c.misc = reinterpret_cast<unsigned *>(smem + L.misc);
+    CtaPlan *plan_s = reinterpret_cast<CtaPlan *>(smem + L.plan);
+    c.plan = plan_s;
     c.b = blockIdx.x;
     c.tid = threadIdx.x;
     c.warp = threadIdx.x >> 5;
@@ -1226,6 +1344,8 @@ __device__ __forceinline__ void monokernel_body(const Params &p, const RepackSrc
             mbar_init(&c.empty[i], NCW);
         }
         mbar_fence_init();
+        *plan_s = p.plans[blockIdx.x];
+        for (int i = 0; i < 64; ++i) c.misc[i] = 0u;
     }
     __syncthreads();
     if (c.warp == NCW) {
@@ -1267,19 +1387,18 @@ __global__ void lf_repack_kernel(Geo g, const CtaPlan *plans, RepackSrc w, uint8
                 tile_range(u0, n, nt, t, a, bnd);
                 const int nu = bnd - a;
                 const int R = nu * sg.rows_per_unit;
-                const int m = chunk_groups(R, sg.K);
-                const int nch = sg.K / (KC * m);
+                const int nch = sg.K / KC;
                 for (int k = 0; k < nch; ++k) {
-                    // chunk: R rows x 256m columns, stored row r -> (unit a + r % nu, part r / nu)
-                    for (int q = threadIdx.x; q < R * 32 * m; q += blockDim.x) {
-                        const int r = q / (32 * m), rem = q % (32 * m);
+                    // chunk: R rows x 256 columns, stored row r -> (unit a + r % nu, part r / nu)
+                    for (int q = threadIdx.x; q < R * 32; q += blockDim.x) {
+                        const int r = q / 32, rem = q % 32;
                         const int unit = a + (sg.rows_per_unit == 2 ? r % nu : r);
                         const int part = sg.rows_per_unit == 2 ? r / nu : 0;
                         const uint4 *srow =
                             reinterpret_cast<const uint4 *>(src_row(g, w, s, l < g.L ? l : 0, unit, part));
-                        reinterpret_cast<uint4 *>(out)[q] = srow[(size_t)k * 32 * m + rem];
+                        reinterpret_cast<uint4 *>(out)[q] = srow[(size_t)k * 32 + rem];
                     }
-                    out += (size_t)R * m * KC_BYTES;
+                    out += (size_t)R * KC_BYTES;
                 }
             }
         }
