@@ -104,7 +104,8 @@ typedef struct {
  * lf_create copies the projection matrices and the LM head into a
  * library-owned, per-CTA streaming layout; the caller may free those after
  * lf_create returns.  embed and the three norm-gain tensors are read in
- * place by every decode step and must outlive the handle. */
+ * place by every decode step and must outlive the handle.  Every pointer
+ * must be 16-byte aligned (the kernels read them with bulk copies). */
 typedef struct {
     const void *embed;       /* [V, d]      read in place */
     const void *attn_norm;   /* [L, d]      read in place */
@@ -160,7 +161,9 @@ typedef struct {
  * static work partition, and check that the persistent grid fits.  Runs one
  * repack kernel on the legacy default stream and synchronizes.  On success
  * *out receives a handle with no pending token at position 0.
- * Errors: INVALID_ARG (NULL, non-positive sizes), NOT_SUPPORTED (shape),
+ * Errors: INVALID_ARG (NULL or not 16-byte aligned weight pointers,
+ * non-positive sizes), NOT_SUPPORTED (shape: head_dim other than 64 or 128,
+ * d_model, n_heads*head_dim or ffn_dim not a multiple of 256 or above 16384),
  * OUT_OF_MEMORY, NOT_RESIDENT, CUDA. */
 LF_API lf_status lf_create(const lf_config *cfg, const lf_weights *weights, lf_handle **out);
 

@@ -17,7 +17,7 @@ extern "C" cudaError_t lfk_set_smem(int smem_bytes);
 extern "C" cudaError_t lfk_launch_monokernel(const lfk::Params *p, int smem_bytes, cudaStream_t stream,
                                              int cooperative);
 extern "C" cudaError_t lfk_occupancy(int smem_bytes, int *blocks_per_sm);
-extern "C" unsigned lfk_smem_bytes(int ring_bytes, int act_floats, int lm_rows_max);
+extern "C" unsigned lfk_smem_bytes(int ring_bytes, int a_floats, int b_slots, int d, int lm_rows_max);
 extern "C" cudaError_t lfk_launch_repack(lfk::Geo g, int P, const lfk::CtaPlan *plans, const void *wq,
                                          const void *wk, const void *wv, const void *wo, const void *wg,
                                          const void *wu, const void *wd, const void *head, void *dst,
@@ -54,14 +54,13 @@ struct lf_handle {
     float2 *rope = nullptr;
     float *qbuf = nullptr, *attn = nullptr, *xattn = nullptr, *hbuf = nullptr, *xout = nullptr, *apart = nullptr;
     int max_split = 1;
-    unsigned *counters = nullptr;  // one allocation: layer counters, attn_done, lm_done, tok_cnt, gbar
+    unsigned *counters = nullptr;  // one allocation: slice counters, attn_done, lm_done, tok_cnt, gbar
     size_t counters_bytes = 0;
-    unsigned *cnt = nullptr, *attn_done = nullptr, *lm_done = nullptr, *tok_cnt = nullptr, *gbar = nullptr;
-    unsigned n_prod[4] = {0, 0, 0, 0};
+    unsigned *sig = nullptr, *attn_done = nullptr, *lm_done = nullptr, *tok_cnt = nullptr, *gbar = nullptr;
     unsigned long long *lm_part = nullptr;
     int *tok_buf = nullptr, *tok_seq = nullptr;
     unsigned *status = nullptr, *abort_flag = nullptr;
-    int ring_bytes = 0, act_floats = 0, lm_rows_max = 0, smem_bytes = 0;
+    int ring_bytes = 0, a_floats = 0, b_slots = 0, lm_rows_max = 0, smem_bytes = 0;
     // sequence state
     int pos = 0;
     int has_pending = 0;
@@ -114,18 +113,9 @@ lf_status validate_config(const lf_config &c)
     if (c.n_heads % c.n_kv_heads != 0 || lfk::MAX_GROUP % (c.n_heads / c.n_kv_heads) != 0) return LF_ERR_NOT_SUPPORTED;
     const long long Q = (long long)c.n_heads * c.head_dim;
     if (c.d_model % lfk::KC || Q % lfk::KC || c.ffn_dim % lfk::KC) return LF_ERR_NOT_SUPPORTED;
+    const long long most = (long long)lfk::MAX_SLICES * lfk::KC;
+    if (c.d_model > most || Q > most || c.ffn_dim > most) return LF_ERR_NOT_SUPPORTED;
     return LF_OK;
-}
-
-// Attention scratch (floats) inside the activation region: q of the group
-// [G][hd], the staged fresh K and V rows (hd floats' worth of FP16) and the
-// eight warp states [NCW][hd + 2]; or, in the combine, the (m, l) table of
-// every piece [G][max_split].
-int attn_scratch_floats(const lfk::Geo &g, int max_split)
-{
-    const int piece = lfk::MAX_GROUP * g.hd + g.hd + lfk::NCW * (g.hd + 2);
-    const int combine = 2 * g.group * max_split;
-    return piece > combine ? piece : combine;
 }
 
 lf_status launch(lf_handle *h, const lfk::Params &p, cudaStream_t stream)
@@ -162,12 +152,11 @@ lfk::Params base_params(lf_handle *h)
     p.xout = h->xout;
     p.apart = h->apart;
     p.max_split = h->max_split;
-    p.cnt = h->cnt;
+    p.sig = h->sig;
     p.attn_done = h->attn_done;
     p.lm_done = h->lm_done;
     p.tok_cnt = h->tok_cnt;
     p.gbar = h->gbar;
-    for (int i = 0; i < 4; ++i) p.n_prod[i] = h->n_prod[i];
     p.lm_part = h->lm_part;
     p.tok_buf = h->tok_buf;
     p.tok_seq = h->tok_seq;
@@ -176,7 +165,8 @@ lfk::Params base_params(lf_handle *h)
     p.timeout_ns = h->cfg.wait_timeout_ns > 0 ? h->cfg.wait_timeout_ns : kDefaultTimeoutNs;
     p.fault_step = h->cfg.fault_step;
     p.ring_bytes = h->ring_bytes;
-    p.act_floats = h->act_floats;
+    p.a_floats = h->a_floats;
+    p.b_slots = h->b_slots;
     p.lm_rows_max = h->lm_rows_max;
     p.attn_min_len = kAttnMinLen;
     p.sched = h->sched;
@@ -262,7 +252,7 @@ lf_status lf_create(const lf_config *cfg, const lf_weights *w, lf_handle **out)
     const void *need[] = {w->embed, w->attn_norm, w->wq, w->wk, w->wv, w->wo, w->ffn_norm,
                           w->w_gate, w->w_up, w->w_down, w->final_norm, w->lm_head};
     for (const void *p : need)
-        if (!p) return LF_ERR_INVALID_ARG;
+        if (!p || (reinterpret_cast<uintptr_t>(p) & 15u)) return LF_ERR_INVALID_ARG;   // bulk copies need 16 B
 
     lf_handle *h = new (std::nothrow) lf_handle();
     if (!h) return LF_ERR_OUT_OF_MEMORY;
@@ -320,24 +310,22 @@ lf_status lf_create(const lf_config *cfg, const lf_weights *w, lf_handle **out)
         pl.base = base;
         base += pl.lm_off + lm_bytes;
         lm_rows_max = std::max(lm_rows_max, pl.u1[lfk::ST_LM] - pl.u0[lfk::ST_LM]);
-        for (int s = 0; s < 4; ++s)
-            if (pl.u1[s] > pl.u0[s]) h->n_prod[s]++;
     }
     h->wstream_bytes = base;
     h->lm_rows_max = lm_rows_max;
 
     // ---- shared memory: everything but the ring, then the largest ring that fits
     h->max_split = std::max(1, P / g.Hkv);
-    h->act_floats = std::max(std::max(g.d, g.Q), std::max(g.F, attn_scratch_floats(g, h->max_split)));
-    h->act_floats = (h->act_floats + 3) / 4 * 4;
-    const unsigned rest = lfk_smem_bytes(0, h->act_floats, lm_rows_max);
+    lfk::act_sizes(g, h->plans.data(), P, h->max_split, h->a_floats, h->b_slots);
+    const unsigned rest = lfk_smem_bytes(0, h->a_floats, h->b_slots, g.d, lm_rows_max);
     if ((int)rest + 2 * lfk::ATT_CHUNK_BYTES > optin) {
         delete h;
         return LF_ERR_NOT_SUPPORTED;
     }
     h->ring_bytes = (int)(((unsigned)optin - rest) / 1024u * 1024u);
-    while ((int)lfk_smem_bytes(h->ring_bytes, h->act_floats, lm_rows_max) > optin) h->ring_bytes -= 1024;
-    h->smem_bytes = (int)lfk_smem_bytes(h->ring_bytes, h->act_floats, lm_rows_max);
+    while ((int)lfk_smem_bytes(h->ring_bytes, h->a_floats, h->b_slots, g.d, lm_rows_max) > optin)
+        h->ring_bytes -= 1024;
+    h->smem_bytes = (int)lfk_smem_bytes(h->ring_bytes, h->a_floats, h->b_slots, g.d, lm_rows_max);
     if (h->ring_bytes < 2 * lfk::ATT_CHUNK_BYTES) {
         delete h;
         return LF_ERR_NOT_SUPPORTED;
@@ -355,9 +343,9 @@ lf_status lf_create(const lf_config *cfg, const lf_weights *w, lf_handle **out)
 
     // ---- allocations
     const size_t kv_elems = (size_t)g.L * g.Hkv * (size_t)g.max_seq * g.hd;
-    const size_t n_layer_cnt = (size_t)g.L * lfk::N_LAYER_CNT;
+    const size_t sig_words = (size_t)g.L * lfk::sig_layout(g).per_layer * lfk::SIG_STRIDE;
     const size_t n_attn_done = (size_t)g.L * g.Hkv;
-    const size_t n_words = (n_layer_cnt + n_attn_done + 3) * lfk::CNT_STRIDE;
+    const size_t n_words = sig_words + (n_attn_done + 3) * lfk::CNT_STRIDE;
     h->counters_bytes = n_words * sizeof(unsigned);
     if ((e = dalloc(&h->d_plans, (size_t)P)) != cudaSuccess || (e = dalloc(&h->wstream, h->wstream_bytes)) != cudaSuccess ||
         (e = dalloc(&h->kc, kv_elems)) != cudaSuccess || (e = dalloc(&h->vc, kv_elems)) != cudaSuccess ||
@@ -376,8 +364,8 @@ lf_status lf_create(const lf_config *cfg, const lf_weights *w, lf_handle **out)
         delete h;
         return from_cuda(e);
     }
-    h->cnt = h->counters;
-    h->attn_done = h->counters + n_layer_cnt * lfk::CNT_STRIDE;
+    h->sig = h->counters;
+    h->attn_done = h->counters + sig_words;
     h->lm_done = h->attn_done + n_attn_done * lfk::CNT_STRIDE;
     h->tok_cnt = h->lm_done + lfk::CNT_STRIDE;
     h->gbar = h->tok_cnt + lfk::CNT_STRIDE;

@@ -17,16 +17,23 @@ constexpr int KC_BYTES = KC * 2;      // bytes of one row of one column group
 constexpr int TILE_ROWS = 32;         // rows of one GEMV tile (4 per consumer warp)
 constexpr int NCW = 8;                // consumer warps
 constexpr int NCT = NCW * 32;         // consumer threads
-constexpr int NTHREADS = NCT + 32;    // + one producer warp
+// Warp roles after the consumers: the producer streams weights into the ring,
+// the loader brings activation slices into shared memory as they become
+// ready, the reducer sums tile partials and runs the stage epilogues.
+constexpr int W_PROD = NCW, W_LOAD = NCW + 1, W_RED = NCW + 2;
+constexpr int NTHREADS = NCT + 96;
 constexpr int TICKETS = 32;           // ring slots in flight (mbarrier pairs)
 constexpr int ATT_CHUNK_BYTES = 16384;// K + V bytes of one attention sub-block
 constexpr int MAX_TOPK = 64;
 constexpr int MAX_GROUP = 8;          // query heads per KV head
 constexpr int CNT_STRIDE = 32;        // uint32 words between counters (one 128-byte line each)
+constexpr int SIG_STRIDE = 8;         // uint32 words between slice readiness counters (one 32-byte sector)
 constexpr int PART_BUFS = 8;          // rotating per-tile partial-sum buffers of a GEMV stage
+constexpr int PART_STRIDE = TILE_ROWS + 1;  // per warp: 32 row sums + the sum of squares of x
+constexpr int MAX_SLICES = 64;        // 256-element slices of one activation vector (length <= 16384)
+constexpr int B_RING_SLOTS = 16;      // slots of the O / down-projection input ring
 
 enum Stage { ST_QKV = 0, ST_O = 1, ST_GU = 2, ST_D = 3, ST_LM = 4, N_GEMV = 5 };
-enum LayerCounter { C_QKV = 0, C_ATTN = 1, C_O = 2, C_GU = 3, C_D = 4, N_LAYER_CNT = 5 };
 enum Mode { MODE_PREFILL = 0, MODE_DECODE = 1 };
 enum Sched { SCHED_FLAGS = 0, SCHED_GRID = 1, SCHED_MULTI = 2 };
 enum StatusCode { STATUS_OK = 0, STATUS_BAD_TOKEN = 1, STATUS_TIMEOUT = 6 };
@@ -100,6 +107,40 @@ __host__ __device__ inline int attn_sub_positions(int hd) { return ATT_CHUNK_BYT
 //   [layer 0: QKV tiles | O tiles | GU tiles | D tiles] ... [layer L-1: ...] [LM-head tiles]
 // and each tile as K/256 chunks of (R rows x 256 columns), row-major inside
 // a chunk.
+// Readiness counters of one layer, cumulative over forward passes (cleared by
+// lf_create and lf_reset).  Every slot is a uint32 SIG_STRIDE words apart.
+//   qkvh[h]   RoPE pair-units of head h written by the QKV stage (query heads,
+//             then key heads, then value heads): hd/2 per pass
+//   attn[k]   elements of slice k (256 elements) of the attention output [Q]
+//   xattn[k]  elements of slice k of the residual after attention [d]
+//   h[k]      elements of slice k of SiLU(gate) * up [F]
+//   xout[k]   elements of slice k of the residual after the FFN [d]
+// A GEMV chunk over columns 256k..256k+255 waits only for slice k of its input.
+struct SigLayout {
+    int qkvh, attn, xattn, h, xout, per_layer;
+};
+__host__ __device__ inline SigLayout sig_layout(const Geo &g)
+{
+    SigLayout s;
+    s.qkvh = 0;
+    s.attn = s.qkvh + g.Hq + 2 * g.Hkv;
+    s.xattn = s.attn + g.Q / KC;
+    s.h = s.xattn + g.d / KC;
+    s.xout = s.h + g.F / KC;
+    s.per_layer = s.xout + g.d / KC;
+    return s;
+}
+
+// Attention scratch (floats) in activation buffer A: q of the group [G][hd],
+// the staged fresh K and V rows (hd floats' worth of FP16) and the eight warp
+// states [NCW][hd + 2]; or, in the combine, the (m, l) table [G][max_split].
+__host__ __device__ inline int attn_scratch_floats(const Geo &g, int max_split)
+{
+    const int piece = MAX_GROUP * g.hd + g.hd + NCW * (g.hd + 2);
+    const int combine = 2 * g.group * max_split;
+    return piece > combine ? piece : combine;
+}
+
 struct CtaPlan {
     int u0[N_GEMV], u1[N_GEMV];
     unsigned long long base;          // byte offset of the stream in the repacked buffer
@@ -107,6 +148,25 @@ struct CtaPlan {
     unsigned long long stage_off[4];  // offset of each stage inside a layer
     unsigned long long lm_off;        // offset of the LM-head tiles from base
 };
+
+// Activation buffer sizes (host side): A holds a d-vector (QKV, gate/up and
+// LM-head inputs) or the attention scratch; B holds the O and down inputs, as
+// a ring of B_RING_SLOTS 256-float slots when every CTA has a single O tile
+// and a single down tile (each slice then has one reader), else as the whole
+// longer input (Q or F).
+inline void act_sizes(const Geo &g, const CtaPlan *plans, int P, int max_split, int &a_floats, int &b_slots)
+{
+    int a = attn_scratch_floats(g, max_split);
+    a = a > g.d ? a : g.d;
+    a_floats = (a + 3) / 4 * 4;
+    const int nb = (g.Q > g.F ? g.Q : g.F) / KC;
+    bool single = true;
+    for (int b = 0; b < P; ++b) {
+        if (tiles_of(plans[b].u1[ST_O] - plans[b].u0[ST_O], 1) > 1) single = false;
+        if (tiles_of(plans[b].u1[ST_D] - plans[b].u0[ST_D], 1) > 1) single = false;
+    }
+    b_slots = single ? (nb < B_RING_SLOTS ? nb : B_RING_SLOTS) : nb;
+}
 
 struct Params {
     Geo g;
@@ -124,10 +184,9 @@ struct Params {
     float *xout;                 // [L][d]   residual after FFN
     float *apart;                // [L][Hq][max_split][hd + 2]  (o[hd], m, l) per piece
     int max_split;
-    unsigned *cnt;               // [L][N_LAYER_CNT] counters
-    unsigned *attn_done;         // [L][Hkv]
+    unsigned *sig;               // [L][sig_layout().per_layer] readiness counters
+    unsigned *attn_done;         // [L][Hkv] pieces of each KV head that have published
     unsigned *lm_done, *tok_cnt, *gbar;
-    unsigned n_prod[4];          // CTAs that publish each GEMV stage (QKV, O, GU, D)
     unsigned long long *lm_part; // [P][MAX_TOPK] 64-bit selection keys
     int *tok_buf;                // [1] pending token
     int *tok_seq;                // [max_seq] token fed to step i + 1
@@ -151,7 +210,8 @@ struct Params {
     long long timeout_ns;
     int fault_step;
     int ring_bytes;
-    int act_floats;
+    int a_floats;                // activation buffer A (QKV / gate-up / LM inputs, attention scratch)
+    int b_slots;                 // 256-float slots of activation buffer B (O / down inputs)
     int lm_rows_max;
     int attn_min_len;
     int sched;
@@ -165,13 +225,14 @@ struct Params {
     int l2_prefetch_last;        // 1: the lookahead marks lines evict-last, 0: evict-normal
 };
 
-// Trace stamps per (step, slot, CTA): stage entered, inputs ready, inputs
-// loaded, stage published, and two stage-specific points (GEMV: first chunk
-// acquired, last chunk released; attention: K/V positions done, piece partial
-// published).
-// The producer adds when it issued the first and the last chunk of the sub-stage.
-// TR_WAITS is a count, not a time: the stage's weight chunks that were not yet
-// in shared memory when thread 0 first asked for them.
+// Trace stamps per (step, slot, CTA), %globaltimer ns.  GEMV stages: consumer
+// warp 0 entered the stage, its first input slice landed, the loader had
+// issued every slice, the reducer published the last tile, consumer warp 0
+// finished its last chunk (X1), the last tile's partials were complete (X2).
+// Attention: entered, inputs ready, K/V positions done (X1), piece partial
+// published (X2), stage done.  The producer adds when it issued the first and
+// the last chunk of the sub-stage (P0, P1).  TR_WAITS is a count: weight
+// chunks of the stage that had not landed when warp 0 first asked for them.
 enum TraceStamp { TR_ENTER = 0, TR_READY = 1, TR_LOADED = 2, TR_DONE = 3, TR_X1 = 4, TR_X2 = 5, TR_P0 = 6, TR_P1 = 7,
                   TR_WAITS = 8, TR_N = 9 };
 __host__ __device__ inline int trace_slots(int L) { return 5 * L + 1; }

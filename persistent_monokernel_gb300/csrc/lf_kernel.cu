@@ -42,28 +42,36 @@ namespace lfk {
 // ---------------------------------------------------------------- shared memory
 
 struct SmemLayout {
-    unsigned ring, act, lmkeys, res, full, empty, chunk_end, red, hist, misc, plan, total;
+    unsigned res, full, empty, chunk_end, afull, bfull, gfull, brel, red, hist, misc, plan;
+    unsigned ring, acta, actb, gain, lmkeys, total;
 };
 
 __host__ __device__ inline unsigned align_up(unsigned x, unsigned a) { return (x + a - 1) / a * a; }
 
-__host__ __device__ inline SmemLayout smem_layout(int ring_bytes, int act_floats, int lm_rows_max)
+__host__ __device__ inline SmemLayout smem_layout(int ring_bytes, int a_floats, int b_slots, int d, int lm_rows_max)
 {
     // Fixed-size parts first: their offsets are compile-time constants, so
-    // their addresses cost no registers; the ring, the activation vector and
-    // the LM keys follow at offsets that depend on the model.
+    // their addresses cost no registers; the ring, the two activation buffers,
+    // the RMSNorm gain row and the LM keys follow at offsets that depend on
+    // the model.
     SmemLayout s;
     unsigned o = 0;
-    s.res = o;       o = align_up(o + 4u * PART_BUFS * NCW * TILE_ROWS, 128);
+    s.res = o;       o = align_up(o + 4u * PART_BUFS * NCW * PART_STRIDE, 128);
     s.full = o;      o += 8u * TICKETS;
     s.empty = o;     o += 8u * TICKETS;
     s.chunk_end = o; o += 8u * TICKETS;
+    s.afull = o;     o += 8u * MAX_SLICES;   // slice k of buffer A landed
+    s.bfull = o;     o += 8u * MAX_SLICES;   // slot j of buffer B landed
+    s.gfull = o;     o += 16u;               // gain row landed
+    s.brel = o;      o = align_up(o + 4u * MAX_SLICES, 16);   // consumer releases of B slots
     s.red = o;       o = align_up(o + 4u * 64u, 16);
     s.hist = o;      o = align_up(o + 4u * 256u, 16);
     s.misc = o;      o = align_up(o + 4u * 64u, 128);
     s.plan = o;      o = align_up(o + (unsigned)sizeof(CtaPlan), 128);
     s.ring = o;      o = align_up(o + (unsigned)ring_bytes, 128);
-    s.act = o;       o = align_up(o + 4u * (unsigned)act_floats, 128);
+    s.acta = o;      o = align_up(o + 4u * (unsigned)a_floats, 128);
+    s.actb = o;      o = align_up(o + 4u * KC * (unsigned)b_slots, 128);
+    s.gain = o;      o = align_up(o + 2u * (unsigned)d, 128);
     s.lmkeys = o;    o = align_up(o + 8u * (unsigned)lm_rows_max, 128);
     // the GEMV reads whole 8-row blocks: keep 7 rows of readable bytes after the ring
     const unsigned slack_end = s.ring + (unsigned)ring_bytes + 7u * KC_BYTES;
@@ -71,20 +79,26 @@ __host__ __device__ inline SmemLayout smem_layout(int ring_bytes, int act_floats
     return s;
 }
 
-// misc word indices; M_TCNT + b / M_TRED + b: arrivals at / reductions of
-// partial-sum buffer b (cumulative)
-enum { M_FLAG = 0, M_TOKEN = 1, M_DIGIT = 2, M_REMAIN = 3, M_INV = 4, M_TSEQ = 8, M_TCNT = 16, M_TRED = 24 };
+// misc word indices.  M_TCNT + b / M_TRED + b: consumer arrivals at / reducer
+// passes over partial-sum buffer b (cumulative).  M_AREL: consumer warps done
+// with an input in buffer A; M_ASCR: attention stages done with their scratch
+// in buffer A; M_LMDONE: decode steps whose LM-head keys are complete.
+enum { M_FLAG = 0, M_TOKEN = 1, M_DIGIT = 2, M_REMAIN = 3, M_AREL = 4, M_ASCR = 5, M_LMDONE = 6, M_TCNT = 16,
+       M_TRED = 24 };
 
 struct Ctx {
     const Params *p;
     const CtaPlan *plan;  // this CTA's partition, copied to shared memory (global reads
                           // after an ld.acquire miss L1 and cost an L2 round trip)
     uint8_t *ring;
-    float *act;
+    float *acta, *actb;
+    __half *gain;
     unsigned long long *lmkeys;
     float *res;
     uint64_t *full, *empty;
     unsigned long long *chunk_end;
+    uint64_t *afull, *bfull, *gfull;
+    unsigned *brel;
     float *red;
     unsigned *hist;
     unsigned *misc;
@@ -351,9 +365,45 @@ __device__ __forceinline__ float gumbel_dev(unsigned long long seed, int pos, in
 
 // ---------------------------------------------------------------- stage plumbing
 
-__device__ __forceinline__ unsigned *layer_cnt(const Params &p, int l, int which)
+__device__ __forceinline__ unsigned *sig_ptr(const Params &p, int l, int idx)
 {
-    return p.cnt + ((size_t)l * N_LAYER_CNT + which) * CNT_STRIDE;
+    return p.sig + ((size_t)l * sig_layout(p.g).per_layer + idx) * SIG_STRIDE;
+}
+
+// Spin (one thread) until the cumulative shared-memory count *w reaches
+// target.  Returns false on timeout or abort.
+__device__ __forceinline__ bool wait_smem_ge(const Params &p, const unsigned *w, unsigned target, unsigned where,
+                                             unsigned layer, unsigned step)
+{
+    unsigned long long t0 = 0;
+    for (unsigned it = 0;; ++it) {
+        if ((int)(*reinterpret_cast<const volatile unsigned *>(w) - target) >= 0) return true;
+        if ((it & 255u) == 255u) {
+            if (ld_relaxed(p.abort_flag)) return false;
+            const unsigned long long now = globaltimer_ns();
+            if (t0 == 0) t0 = now;
+            else if ((long long)(now - t0) > p.timeout_ns) {
+                raise_error(p, STATUS_TIMEOUT, where, layer, step);
+                return false;
+            }
+        }
+    }
+}
+
+// Count the outputs [e0, e0 + n) of a stage in the readiness counters of the
+// groups of `per` elements they fall in (`base`: counter of group 0).  Called
+// by one lane after __syncwarp or a barrier; the single gpu-scope fence turns
+// the relaxed adds into releases of every store the group made before.
+__device__ __forceinline__ void publish_range(unsigned *base, int e0, int n, int per)
+{
+    fence_acq_rel_gpu();
+    const int end = e0 + n;
+    for (int e = e0; e < end;) {
+        const int grp = e / per;
+        const int stop = min(end, (grp + 1) * per);
+        red_relaxed_add(base + (size_t)grp * SIG_STRIDE, (unsigned)(stop - e));
+        e = stop;
+    }
 }
 
 // Grid-barrier schedule: index of the barrier that closes (step, layer, slot).
@@ -366,6 +416,30 @@ __device__ __forceinline__ unsigned gbar_index(const Params &p, int step, int l,
     return p.gbar_base + (unsigned)step * per_step + in_step;
 }
 
+// The grid barrier a sub-stage waits for in the barrier schedule: the one
+// that closes the previous sub-stage (false: none, the first sub-stage of the
+// call).
+__device__ __forceinline__ bool grid_barrier_before(const Params &p, int step, int l, int sid, unsigned &idx)
+{
+    int gstep = step, gl = l, gslot = sid - 1;
+    if (sid == SID_QKV) {
+        if (l > 0) {
+            gl = l - 1;
+            gslot = 4;
+        } else {
+            if (step == 0) return false;
+            gstep = step - 1;
+            gl = p.g.L - 1;
+            gslot = p.mode == MODE_DECODE ? 5 : 4;
+        }
+    } else if (sid == SID_LM) {
+        gl = p.g.L - 1;
+        gslot = 4;
+    }
+    idx = gbar_index(p, gstep, gl, gslot);
+    return true;
+}
+
 // Consumer-side dependency wait: thread 0 polls, then the consumer warps
 // meet at a named barrier that also ORs the abort state.  Returns true if
 // the CTA must stop.
@@ -376,95 +450,254 @@ __device__ __forceinline__ bool cons_wait(const Ctx &c, const unsigned *ctr, uns
     return cons_sync_or(ab);
 }
 
-// Publish the end of a stage: all consumer writes are ordered before thread
-// 0's release by the named barrier plus a gpu-scope fence.
-__device__ __forceinline__ bool cons_publish(const Ctx &c, unsigned *ctr, bool do_cnt, unsigned *gbar, bool ab)
+// Arrival of this CTA at the grid barrier (barrier schedule), after all
+// consumer writes of the sub-stage.
+__device__ __forceinline__ bool cons_grid_arrive(const Ctx &c, bool ab)
 {
     ab = cons_sync_or(ab);
     if (ab) return true;
     if (c.tid == 0) {
         fence_acq_rel_gpu();
-        if (do_cnt) red_release_add(ctr, 1u);
-        if (gbar) red_release_add(gbar, 1u);
+        red_release_add(c.p->gbar, 1u);
     }
     return false;
 }
 
-// Stage input wait in the three schedules: the producer counter `ctr` in the
-// flag schedule, the grid barrier (gstep, gl, gslot) in the barrier schedule,
-// nothing in the multi-kernel schedule (the previous launch has finished).
-__device__ __forceinline__ bool stage_wait(const Ctx &c, const unsigned *ctr, unsigned target, int gstep, int gl, int gslot,
-                           int step, int l, unsigned where, bool ab)
+__device__ __forceinline__ int stage_of(int sid)
 {
-    const Params &p = *c.p;
-    if (p.sched == SCHED_MULTI) return cons_sync_or(ab);
-    if (p.sched == SCHED_GRID) {
-        if (gslot < 0) return cons_sync_or(ab);
-        const unsigned idx = gbar_index(p, gstep, gl, gslot);
-        return cons_wait(c, p.gbar, (idx + 1u) * (unsigned)p.P, where, l, step, ab);
-    }
-    if (!ctr) return cons_sync_or(ab);
-    return cons_wait(c, ctr, target, where, l, step, ab);
+    return sid == SID_QKV ? ST_QKV : sid == SID_O ? ST_O : sid == SID_GU ? ST_GU : sid == SID_D ? ST_D : ST_LM;
 }
 
-// Load an activation vector into shared memory, times the RMSNorm gain if
-// given, and return 1/sqrt(mean(x^2) + eps) (or 1 if norm == false).  The
-// input is FP32 from global memory (read at L2, never a stale L1 line) or,
-// for layer 0, the FP16 embedding row.
-__device__ __forceinline__ bool load_act(const Ctx &c, const float *src32, const __half *src16, const __half *gain, int K, bool norm,
-                         float &inv, bool ab)
+// Input of a GEMV stage: the FP32 vector (null for layer 0's QKV, which reads
+// the FP16 embedding row of the step's token), the RMSNorm gain row (null for
+// the O and down projections), the readiness counter of input slice 0 (slice
+// k at + k * SIG_STRIDE), and which activation buffer holds it: B for the O
+// and down projections, A otherwise.
+struct StageIn {
+    const float *src32;
+    const __half *gain;
+    unsigned *sig;
+    bool bufb;
+};
+
+__device__ __forceinline__ StageIn stage_input(const Params &p, int s, int l)
+{
+    const Geo &g = p.g;
+    const SigLayout sl = sig_layout(g);
+    StageIn in;
+    in.src32 = nullptr;
+    in.gain = nullptr;
+    in.sig = nullptr;
+    in.bufb = false;
+    if (s == ST_QKV) {
+        in.gain = p.attn_norm + (size_t)l * g.d;
+        if (l > 0) {
+            in.src32 = p.xout + (size_t)(l - 1) * g.d;
+            in.sig = sig_ptr(p, l - 1, sl.xout);
+        }
+    } else if (s == ST_O) {
+        in.src32 = p.attn + (size_t)l * g.Q;
+        in.sig = sig_ptr(p, l, sl.attn);
+        in.bufb = true;
+    } else if (s == ST_GU) {
+        in.src32 = p.xattn + (size_t)l * g.d;
+        in.sig = sig_ptr(p, l, sl.xattn);
+        in.gain = p.ffn_norm + (size_t)l * g.d;
+    } else if (s == ST_D) {
+        in.src32 = p.hbuf + (size_t)l * g.F;
+        in.sig = sig_ptr(p, l, sl.h);
+        in.bufb = true;
+    } else {
+        in.src32 = p.xout + (size_t)(g.L - 1) * g.d;
+        in.sig = sig_ptr(p, g.L - 1, sl.xout);
+        in.gain = p.final_norm;
+    }
+    return in;
+}
+
+// A warp's position in the CTA's sequence of sub-stages, advanced identically
+// by the consumer warps, the loader and the reducer: tiles passed (the
+// partial-sum buffer sequence), fills of buffer A, phases of buffer B's slots,
+// inputs of buffer A handed back by the consumers, attention stages passed.
+struct PipeState {
+    unsigned seq = 0, afill = 0, bphase = 0, a_uses = 0, attn_uses = 0;
+};
+
+// Token fed to forward pass `step` (decode: after its counter was acquired).
+// An id outside [0, V) is reported (LF_ERR_INVALID_ARG via lf_sync) and
+// replaced by 0, so that no embedding read leaves the table.
+__device__ __forceinline__ int step_token(const Params &p, int step)
+{
+    int t;
+    if (p.mode == MODE_PREFILL) {
+        if (p.has_pending) t = step == 0 ? __ldcg(p.tok_buf) : __ldg(p.prompt + step - 1);
+        else t = __ldg(p.prompt + step);
+    } else {
+        t = step == 0 ? __ldcg(p.tok_buf) : __ldcg(p.tok_seq + step - 1);
+    }
+    if ((unsigned)t >= (unsigned)p.g.V) {
+        raise_error(p, STATUS_BAD_TOKEN, 300, 0, (unsigned)step);
+        t = 0;
+    }
+    return t;
+}
+
+// ---------------------------------------------------------------- loader warp
+
+// Brings each GEMV stage's input into shared memory, one 256-element slice at
+// a time, as soon as the slice's readiness counter shows it complete (flag
+// schedule), after the grid barrier (barrier schedule) or at once (multi-kernel
+// schedule).  Buffer A (QKV, gate/up and LM-head inputs) holds the whole
+// vector: every tile of those stages reads every slice.  Buffer B (O and down
+// inputs, one tile per CTA) is a ring of b_slots slots: slice k goes to slot
+// k mod b_slots once the consumer of the slot's previous slice released it;
+// slots without a slice in a round get a plain arrival, so that every slot's
+// mbarrier advances one phase per round.  The RMSNorm gain row of the A
+// stages goes to its own area.  Lanes work on different slices in parallel.
+__device__ void loader(const Ctx &c)
 {
     const Params &p = *c.p;
-    float ss = 0.f;
-    float4 *xs = reinterpret_cast<float4 *>(c.act);
-    if (!ab) {
-        for (int i = c.tid; i < K / 4; i += NCT) {
-            float4 v;
-            if (src32) {
-                v = __ldcg(reinterpret_cast<const float4 *>(src32) + i);
+    const Geo &g = p.g;
+    const CtaPlan &pl = *c.plan;
+    const bool decode = p.mode == MODE_DECODE;
+    const int n_sub = 5 * g.L + (decode ? 1 : 0);
+    const uint64_t pol = policy_evict_normal();
+    const uint64_t pol_gain = policy_evict_last();
+    PipeState ps;
+    unsigned bexp[2] = {0u, 0u};     // releases of B slots lane and lane + 32 owed before their next fill
+    // slots this lane armed last (for the drain after an abort): A slots lane
+    // and lane + 32 (bits of a_mask) in fill a_par, B slots in phase b_ph[h],
+    // the gain row (lane 0) in fill g_par
+    unsigned a_mask = 0u, a_par = 0u, g_par = 0u, b_ph[2] = {0u, 0u};
+    bool g_arm = false, b_arm[2] = {false, false};
+    bool ok = true;
+    for (int step = 0; step < p.n_steps && ok; ++step) {
+        const unsigned e = p.epoch0 + (unsigned)step;
+        for (int k = 0; k < n_sub && ok; ++k) {
+            const bool lm = k == 5 * g.L;
+            const int l = lm ? g.L - 1 : k / 5;
+            const int sid = lm ? SID_LM : k % 5;
+            if (!stage_active(p, l, sid)) continue;
+            if (sid == SID_ATTN) {
+                ps.attn_uses++;
+                continue;
+            }
+            const int s = stage_of(sid);
+            const StageGeom sg = stage_geom(g, s);
+            const StageIn in = stage_input(p, s, l);
+            const int n = sg.K / KC;
+            const bool flags = p.sched == SCHED_FLAGS;
+            // ---- barrier schedule: the whole previous sub-stage, everywhere
+            if (p.sched == SCHED_GRID) {
+                unsigned idx;
+                if (c.lane == 0 && grid_barrier_before(p, step, l, sid, idx))
+                    ok = wait_counter(p, p.gbar, (idx + 1u) * (unsigned)p.P, 130, l, step);
+                ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
+                if (!ok) break;
+            }
+            if (!in.bufb) {
+                // ---- buffer A: every consumer warp is done with its previous
+                // input and the attention stages with their scratch
+                if (c.lane == 0)
+                    ok = wait_smem_ge(p, &c.misc[M_AREL], (unsigned)NCW * ps.a_uses, 131, l, step) &&
+                         wait_smem_ge(p, &c.misc[M_ASCR], ps.attn_uses, 132, l, step);
+                ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
+                if (!ok) break;
+                ps.a_uses++;
+                a_mask = 0u;
+                a_par = ps.afill & 1u;
+                if (c.lane == 0) {
+                    mbar_arrive_expect_tx(c.gfull, 2u * (unsigned)g.d);
+                    bulk_g2s(c.gain, in.gain, 2u * (unsigned)g.d, c.gfull, pol_gain);
+                    g_arm = true;
+                    g_par = a_par;
+                }
+                if (!in.src32) {
+                    // layer 0: the FP16 embedding row of the step's token
+                    int tok = 0;
+                    if (c.lane == 0) {
+                        if (flags && decode && step > 0)
+                            ok = wait_counter(p, p.tok_cnt, p.tok_base + (unsigned)step, 133, l, step);
+                        if (ok) tok = step_token(p, step);
+                    }
+                    ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
+                    tok = __shfl_sync(0xffffffffu, tok, 0);
+                    if (!ok) break;
+                    const __half *row = p.embed + (size_t)tok * g.d;
+                    for (int kk = c.lane; kk < n; kk += 32) {
+                        mbar_arrive_expect_tx(c.afull + kk, 2u * KC);
+                        bulk_g2s(c.acta + (size_t)kk * (KC / 2), row + (size_t)kk * KC, 2u * KC, c.afull + kk, pol);
+                        a_mask |= 1u << (kk >> 5);
+                    }
+                } else {
+                    for (int kk = c.lane; kk < n && ok; kk += 32) {
+                        if (flags) ok = wait_counter(p, in.sig + (size_t)kk * SIG_STRIDE, (unsigned)KC * (e + 1u), 134, l, step);
+                        if (!ok) break;
+                        fence_proxy_async_global();
+                        mbar_arrive_expect_tx(c.afull + kk, 4u * KC);
+                        bulk_g2s(c.acta + (size_t)kk * KC, in.src32 + (size_t)kk * KC, 4u * KC, c.afull + kk, pol);
+                        a_mask |= 1u << (kk >> 5);
+                    }
+                }
+                ps.afill++;
             } else {
-                uint2 hv = __ldg(reinterpret_cast<const uint2 *>(src16) + i);
-                float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&hv.x));
-                float2 b2 = __half22float2(*reinterpret_cast<const __half2 *>(&hv.y));
-                v = make_float4(a.x, a.y, b2.x, b2.y);
+                // ---- buffer B: slots in rounds
+                const int bs = p.b_slots;
+                const int nt = tiles_of(pl.u1[s] - pl.u0[s], sg.rows_per_unit);
+                const int rounds = ceil_div(n, bs);
+                for (int r = 0; r < rounds && ok; ++r) {
+                    for (int h = 0; h < 2 && ok; ++h) {
+                        const int j = c.lane + 32 * h;
+                        if (j >= bs) break;
+                        const int kk = r * bs + j;
+                        ok = wait_smem_ge(p, c.brel + j, bexp[h], 135, l, step);
+                        if (!ok) break;
+                        if (kk < n) {
+                            if (flags) ok = wait_counter(p, in.sig + (size_t)kk * SIG_STRIDE, (unsigned)KC * (e + 1u), 136, l, step);
+                            if (!ok) break;
+                            fence_proxy_async_global();
+                            mbar_arrive_expect_tx(c.bfull + j, 4u * KC);
+                            bulk_g2s(c.actb + (size_t)j * KC, in.src32 + (size_t)kk * KC, 4u * KC, c.bfull + j, pol);
+                            bexp[h] += (unsigned)nt;
+                            b_arm[h] = true;
+                            b_ph[h] = (ps.bphase + (unsigned)r) & 1u;
+                        } else {
+                            mbar_arrive(c.bfull + j);
+                        }
+                    }
+                }
+                ps.bphase += (unsigned)rounds;
             }
-            if (norm) ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-            if (gain) {
-                uint2 gv = __ldg(reinterpret_cast<const uint2 *>(gain) + i);
-                float2 ga = __half22float2(*reinterpret_cast<const __half2 *>(&gv.x));
-                float2 gb = __half22float2(*reinterpret_cast<const __half2 *>(&gv.y));
-                v.x *= ga.x;
-                v.y *= ga.y;
-                v.z *= gb.x;
-                v.w *= gb.y;
-            }
-            xs[i] = v;
+            ok = __all_sync(0xffffffffu, ok);
+            if (c.lane == 0) trace_mark_producer(c, step, k, TR_LOADED);
         }
     }
-    inv = 1.f;
-    if (norm) {
-        ss = warp_sum(ss);
-        if (c.lane == 0) c.red[c.warp] = ss;
-        if (cons_sync_or(ab)) return true;
-        float tot = 0.f;
-#pragma unroll
-        for (int w = 0; w < NCW; ++w) tot += c.red[w];
-        inv = 1.0f / sqrtf(tot / (float)K + p.eps);
+    if (!ok) {
+        // No bulk copy may still be writing shared memory when the CTA exits:
+        // wait (bounded) until the last copy into each slot this lane armed
+        // has landed.
+        const unsigned long long t0 = globaltimer_ns();
+        auto settle = [&](uint64_t *bar, unsigned par) {
+            while (!mbar_try_wait(bar, par))
+                if ((long long)(globaltimer_ns() - t0) > p.timeout_ns) return;
+        };
+        for (int h = 0; h < 2; ++h) {
+            if (a_mask & (1u << h)) settle(c.afull + c.lane + 32 * h, a_par);
+            if (b_arm[h]) settle(c.bfull + c.lane + 32 * h, b_ph[h]);
+        }
+        if (g_arm) settle(c.gfull, g_par);
     }
-    return cons_sync_or(ab);
 }
 
-// One weight chunk (R rows x 256 columns, row-major, R <= 32; column group
-// gcol of the tile) consumed by one warp: lane l takes columns 8l..8l+7 and
+// ---------------------------------------------------------------- GEMV stages
+
+// One weight chunk (R rows x 256 columns, row-major, R <= 32) consumed by one
+// warp: lane l holds the 8 input values of columns 8l..8l+7 (xa, xb) and
 // accumulates all R rows, so each lane carries R independent FMA chains.
-__device__ __forceinline__ void gemv_chunk(const Ctx &c, const uint8_t *ch, int R, int gcol,
+__device__ __forceinline__ void gemv_chunk(const Ctx &c, const uint8_t *ch, int R, const float4 &xa, const float4 &xb,
                                            float (&acc)[TILE_ROWS])
 {
-    // 32-bit shared addresses: the lane's 16 bytes of row r sit at
-    // chunk + r * 512 + lane * 16, its 8 x values at act + gcol * 1024 + lane * 32.
-    const uint32_t xs = smem_u32(c.act) + (uint32_t)gcol * 1024u + (uint32_t)c.lane * 32u;
-    const float4 xa = lds_f4(xs);
-    const float4 xb = lds_f4(xs + 16u);
+    // 32-bit shared addresses: the lane's 16 bytes of row r sit at chunk + r * 512 + lane * 16.
     const uint32_t a0 = smem_u32(ch) + (uint32_t)c.lane * 16u;
     // Rows in blocks of 8 at constant offsets: one branch per block, so the 8
     // loads issue together and the 8 FMA chains interleave.  The last block
@@ -501,150 +734,214 @@ __device__ __forceinline__ float reduce_rows32(float (&v)[TILE_ROWS], int lane)
     return v[0];
 }
 
-// Token fed to forward pass `step` (decode: after its counter was acquired).
-// An id outside [0, V) is reported (LF_ERR_INVALID_ARG via lf_sync) and
-// replaced by 0, so that no embedding read leaves the table.
-__device__ __forceinline__ int step_token(const Params &p, int step)
-{
-    int t;
-    if (p.mode == MODE_PREFILL) {
-        if (p.has_pending) t = step == 0 ? __ldcg(p.tok_buf) : __ldg(p.prompt + step - 1);
-        else t = __ldg(p.prompt + step);
-    } else {
-        t = step == 0 ? __ldcg(p.tok_buf) : __ldcg(p.tok_seq + step - 1);
-    }
-    if ((unsigned)t >= (unsigned)p.g.V) {
-        raise_error(p, STATUS_BAD_TOKEN, 300, 0, (unsigned)step);
-        t = 0;
-    }
-    return t;
-}
+__device__ __forceinline__ float2 h2f(unsigned w) { return __half22float2(*reinterpret_cast<const __half2 *>(&w)); }
 
-// ---------------------------------------------------------------- GEMV stages
-
-__device__ __forceinline__ bool stage_gemv(const Ctx &c, ConsRing &rc, int s, int l, int step, bool ab)
+// Consumer side of a GEMV stage.  Chunk j of the stage (tile by tile, column
+// group by column group, as the producer streams them) belongs to warp
+// j mod NCW.  Before a chunk the warp waits only for the input slice of its
+// column group, takes the lane's 8 input values, adds their squares to the
+// RMSNorm sum (tile 0 covers every slice once) and applies the gain.  After
+// each tile the warp reduces its 32 row sums over the lanes and hands them to
+// the reducer through a rotating partial-sum buffer.
+__device__ __forceinline__ bool stage_gemv(const Ctx &c, ConsRing &rc, PipeState &ps, int s, int l, int step, bool ab)
 {
     const Params &p = *c.p;
     const Geo &g = p.g;
     const CtaPlan &pl = *c.plan;
     const StageGeom sg = stage_geom(g, s);
-    const int pos = p.pos0 + step;
-    // layer 0 reads the embedding row of the step's token (after the stage's wait)
-    const int tok = (l == 0 && (s == ST_QKV || s == ST_O)) ? step_token(p, step) : 0;
-
-    // ---- inputs (one call site: the stage picks source, gain and length)
-    const float *src32 = nullptr;
-    const __half *src16 = nullptr, *gain = nullptr;
-    int K = g.d;
-    bool norm = true;
-    if (s == ST_QKV) {
-        if (l == 0) src16 = p.embed + (size_t)tok * g.d;
-        else src32 = p.xout + (size_t)(l - 1) * g.d;
-        gain = p.attn_norm + (size_t)l * g.d;
-    } else if (s == ST_O) {
-        src32 = p.attn + (size_t)l * g.Q;
-        K = g.Q;
-        norm = false;
-    } else if (s == ST_GU) {
-        src32 = p.xattn + (size_t)l * g.d;
-        gain = p.ffn_norm + (size_t)l * g.d;
-    } else if (s == ST_D) {
-        src32 = p.hbuf + (size_t)l * g.F;
-        K = g.F;
-        norm = false;
-    } else {
-        src32 = p.xout + (size_t)(g.L - 1) * g.d;
-        gain = p.final_norm;
-    }
-    float inv = 1.f;
-    ab = load_act(c, src32, src16, gain, K, norm, inv, ab);
-    if (ab) return true;
+    const StageIn in = stage_input(p, s, l);
+    const bool fp16 = in.src32 == nullptr;
+    const bool norm = in.gain != nullptr;
     const int tslot = s == ST_LM ? 5 * g.L : 5 * l + (s == ST_QKV ? 0 : s + 1);
-    trace_mark(c, step, tslot, TR_LOADED);
-    const unsigned waited0 = rc.waited;
-
+    const uint32_t xbase = smem_u32(in.bufb ? (const void *)c.actb : (const void *)c.acta) +
+                           (uint32_t)c.lane * (fp16 ? 16u : 32u);
+    const uint32_t gbase = smem_u32(c.gain) + (uint32_t)c.lane * 16u;
+    const int nslices = sg.K / KC;
+    const int bs = p.b_slots;
+    const unsigned apar = ps.afill & 1u;
+    if (norm && !ab) {
+        bool fail = false;
+        if (!mbar_try_wait(c.gfull, apar)) fail = !wait_mbar(p, c.gfull, apar, 120);
+        ab = __any_sync(0xffffffffu, fail);
+    }
     const int u0 = pl.u0[s], n = pl.u1[s] - u0;
     const int nt = tiles_of(n, sg.rows_per_unit);
-    int jc = 0;   // chunk index within the stage: chunk jc belongs to warp jc mod NCW
-    for (int t = 0; t < nt; ++t) {
+    int jc = 0;
+    bool first = true;
+    for (int t = 0; t < nt && !ab; ++t) {
         int a, bnd;
         tile_range(u0, n, nt, t, a, bnd);
-        const int nu = bnd - a;
-        const int R = nu * sg.rows_per_unit;
-        const int nch = sg.K / KC;
+        const int R = (bnd - a) * sg.rows_per_unit;
         const unsigned bytes = (unsigned)R * KC_BYTES;
         float acc[TILE_ROWS];
 #pragma unroll
         for (int r = 0; r < TILE_ROWS; ++r) acc[r] = 0.f;
+        float ss = 0.f;
         bool mine = false;
-        for (int k = 0; k < nch; ++k, ++jc) {
+        for (int k = 0; k < nslices; ++k, ++jc) {
             if (jc % NCW != c.warp) {
                 rc.skip(c, bytes);
                 continue;
             }
+            // the input slice: buffer A slot k, or buffer B slot k mod bs in round k / bs
+            uint64_t *bar;
+            unsigned par;
+            uint32_t xaddr;
+            if (in.bufb) {
+                const int j = k % bs;
+                bar = c.bfull + j;
+                par = (ps.bphase + (unsigned)(k / bs)) & 1u;
+                xaddr = xbase + (uint32_t)j * 4u * KC;
+            } else {
+                bar = c.afull + k;
+                par = apar;
+                xaddr = xbase + (uint32_t)k * (fp16 ? 2u : 4u) * KC;
+            }
+            bool fail = false;
+            if (!mbar_try_wait(bar, par)) fail = !wait_mbar(p, bar, par, 121);
+            if (__any_sync(0xffffffffu, fail)) {
+                ab = true;
+                break;
+            }
+            if (first) {
+                trace_mark(c, step, tslot, TR_READY);
+                first = false;
+            }
+            float4 xa, xb;
+            if (fp16) {
+                const uint4 hv = lds_u4(xaddr);
+                const float2 f0 = h2f(hv.x), f1 = h2f(hv.y), f2 = h2f(hv.z), f3 = h2f(hv.w);
+                xa = make_float4(f0.x, f0.y, f1.x, f1.y);
+                xb = make_float4(f2.x, f2.y, f3.x, f3.y);
+            } else {
+                xa = lds_f4(xaddr);
+                xb = lds_f4(xaddr + 16u);
+            }
+            if (norm) {
+                if (t == 0) {
+                    ss = fmaf(xa.x, xa.x, ss); ss = fmaf(xa.y, xa.y, ss);
+                    ss = fmaf(xa.z, xa.z, ss); ss = fmaf(xa.w, xa.w, ss);
+                    ss = fmaf(xb.x, xb.x, ss); ss = fmaf(xb.y, xb.y, ss);
+                    ss = fmaf(xb.z, xb.z, ss); ss = fmaf(xb.w, xb.w, ss);
+                }
+                const uint4 gv = lds_u4(gbase + (uint32_t)k * 2u * KC);
+                const float2 g0 = h2f(gv.x), g1 = h2f(gv.y), g2 = h2f(gv.z), g3 = h2f(gv.w);
+                xa.x *= g0.x; xa.y *= g0.y; xa.z *= g1.x; xa.w *= g1.y;
+                xb.x *= g2.x; xb.y *= g2.y; xb.z *= g3.x; xb.w *= g3.y;
+            }
             const uint8_t *ch = rc.acquire(c, bytes, ab);
             if (ab) break;
-            if (t == 0 && !mine) trace_mark(c, step, tslot, TR_X2);
-            gemv_chunk(c, ch, R, k, acc);
+            gemv_chunk(c, ch, R, xa, xb, acc);
             mine = true;
             rc.release_own(c);
-        }
-        if (ab) break;
-        // ---- per-warp row sums -> partial buffer; the last warp to arrive reduces
-        const float v = mine ? reduce_rows32(acc, c.lane) : 0.f;
-        const unsigned seq = c.misc[M_TSEQ] + (unsigned)t;      // tile sequence number (kernel-wide)
-        const int buf = (int)(seq % PART_BUFS);
-        const unsigned use = seq / PART_BUFS;
-        // the buffer's previous use must have been reduced before it is overwritten
-        bool stuck = false;
-        if (c.lane == 0) {
-            unsigned long long t0 = 0;
-            for (unsigned it = 0; *reinterpret_cast<volatile unsigned *>(&c.misc[M_TRED + buf]) != use; ++it) {
-                if ((it & 255u) != 255u) continue;
-                if (ld_relaxed(p.abort_flag)) { stuck = true; break; }
-                const unsigned long long now = globaltimer_ns();
-                if (t0 == 0) t0 = now;
-                else if ((long long)(now - t0) > p.timeout_ns) {
-                    raise_error(p, STATUS_TIMEOUT, 110, l, step);
-                    stuck = true;
-                    break;
-                }
+            if (in.bufb) {
+                __syncwarp();
+                if (c.lane == 0) atomicAdd(c.brel + (k % bs), 1u);
             }
         }
-        if (__shfl_sync(0xffffffffu, (int)stuck, 0)) {
+        if (ab) break;
+        // ---- per-warp row sums -> partial buffer of this tile
+        const float v = mine ? reduce_rows32(acc, c.lane) : 0.f;
+        const float ssw = (norm && t == 0) ? warp_sum(ss) : 0.f;
+        const unsigned seq = ps.seq++;
+        const int buf = (int)(seq % PART_BUFS);
+        const unsigned use = seq / PART_BUFS;
+        // the reducer must be done with the buffer's previous use
+        bool ok = true;
+        if (c.lane == 0 && use > 0) ok = wait_smem_ge(p, &c.misc[M_TRED + buf], use, 110, l, step);
+        if (!__shfl_sync(0xffffffffu, (int)ok, 0)) {
             ab = true;
             break;
         }
-        float *part = c.res + (size_t)buf * NCW * TILE_ROWS;
-        part[c.warp * TILE_ROWS + c.lane] = v;
+        float *part = c.res + ((size_t)buf * NCW + c.warp) * PART_STRIDE;
+        part[c.lane] = v;
+        if (c.lane == 0) part[TILE_ROWS] = ssw;
         __syncwarp();
-        unsigned old = 0;
         if (c.lane == 0) {
             __threadfence_block();
-            old = atomicAdd(&c.misc[M_TCNT + buf], 1u);
+            atomicAdd(&c.misc[M_TCNT + buf], 1u);
         }
-        old = __shfl_sync(0xffffffffu, old, 0);
-        if (old != use * NCW + (NCW - 1)) continue;
+    }
+    if (ab) return true;
+    if (c.warp == 0 && c.lane == 0) trace_mark_producer(c, step, tslot, TR_X1);
+    if (in.bufb) {
+        ps.bphase += (unsigned)ceil_div(nslices, bs);
+    } else {
+        ps.afill++;
+        __syncwarp();
+        if (c.lane == 0) atomicAdd(&c.misc[M_AREL], 1u);
+    }
+    return false;
+}
+
+// Reducer side of a GEMV stage: for each tile, in the consumers' order, wait
+// for the eight warps' partials, sum them in warp order, run the stage
+// epilogue (lane i: unit a + i; pair stages: rows i and i + nu) and count the
+// outputs in the readiness counters of the slices (or heads) they belong to.
+__device__ __forceinline__ bool reduce_stage(const Ctx &c, PipeState &ps, int s, int l, int step, bool ab)
+{
+    const Params &p = *c.p;
+    const Geo &g = p.g;
+    const CtaPlan &pl = *c.plan;
+    const StageGeom sg = stage_geom(g, s);
+    const SigLayout sl = sig_layout(g);
+    const int pos = p.pos0 + step;
+    const bool norm = s != ST_O && s != ST_D;
+    const int tslot = s == ST_LM ? 5 * g.L : 5 * l + (s == ST_QKV ? 0 : s + 1);
+    // layer 0's O residual is the embedding row of the step's token
+    const int tok = (l == 0 && s == ST_O) ? __shfl_sync(0xffffffffu, c.lane == 0 ? step_token(p, step) : 0, 0) : 0;
+    const bool withhold = p.mode == MODE_DECODE && step == p.fault_step && l == 0 && s == ST_QKV;
+    const int u0 = pl.u0[s], n = pl.u1[s] - u0;
+    const int nt = tiles_of(n, sg.rows_per_unit);
+    float inv = 1.f;
+    for (int t = 0; t < nt; ++t) {
+        int a, bnd;
+        tile_range(u0, n, nt, t, a, bnd);
+        const int nu = bnd - a;
+        const unsigned seq = ps.seq++;
+        const int buf = (int)(seq % PART_BUFS);
+        const unsigned use = seq / PART_BUFS;
+        // the epilogue's other inputs (RoPE row, residual) do not depend on
+        // the partials: load them while the consumers finish the tile
+        const int u = a + min(c.lane, nu - 1);
+        float2 pre = make_float2(0.f, 0.f);
+        if (s == ST_QKV) {
+            const int half = g.hd / 2;
+            if (u / half < g.Hq + g.Hkv) pre = __ldg(p.rope + (size_t)pos * half + u % half);
+        } else if (s == ST_O) {
+            pre.x = (l == 0) ? __half2float(p.embed[(size_t)tok * g.d + u]) : __ldcg(p.xout + (size_t)(l - 1) * g.d + u);
+        } else if (s == ST_D) {
+            pre.x = __ldcg(p.xattn + (size_t)l * g.d + u);
+        }
+        bool ok = true;
+        if (c.lane == 0) ok = wait_smem_ge(p, &c.misc[M_TCNT + buf], (use + 1u) * NCW, 111, l, step);
+        if (!__shfl_sync(0xffffffffu, (int)ok, 0)) return true;
+        if (t == nt - 1 && c.lane == 0) trace_mark_producer(c, step, tslot, TR_X2);
         __threadfence_block();
+        const volatile float *part = c.res + (size_t)buf * NCW * PART_STRIDE;
         float sum = 0.f;
 #pragma unroll
-        for (int w = 0; w < NCW; ++w) sum += *reinterpret_cast<volatile float *>(&part[w * TILE_ROWS + c.lane]);
+        for (int w = 0; w < NCW; ++w) sum += part[w * PART_STRIDE + c.lane];
+        if (norm && t == 0) {
+            float tot = 0.f;
+#pragma unroll
+            for (int w = 0; w < NCW; ++w) tot += part[w * PART_STRIDE + TILE_ROWS];
+            inv = 1.0f / sqrtf(tot / (float)sg.K + p.eps);
+        }
         __syncwarp();
         if (c.lane == 0) {
             __threadfence_block();
-            *reinterpret_cast<volatile unsigned *>(&c.misc[M_TRED + buf]) = use + 1;
+            *reinterpret_cast<volatile unsigned *>(&c.misc[M_TRED + buf]) = use + 1u;
         }
         // ---- epilogue: lane i handles unit a + i (pair stages: rows i and i + nu)
         const float partner = __shfl_sync(0xffffffffu, sum, (c.lane + nu) & 31);
-        const int i = c.lane;
-        if (i < nu) {
-            const int u = a + i;
+        if (c.lane < nu) {
             if (s == ST_QKV) {
                 const int half = g.hd / 2;
                 const int hh = u / half, j = u % half;
                 const float v0 = sum * inv, v1 = partner * inv;
                 if (hh < g.Hq + g.Hkv) {
-                    const float2 cs = __ldg(p.rope + (size_t)pos * half + j);
+                    const float2 cs = pre;
                     const float r0 = v0 * cs.x - v1 * cs.y;
                     const float r1 = v1 * cs.x + v0 * cs.y;
                     if (hh < g.Hq) {
@@ -663,16 +960,14 @@ __device__ __forceinline__ bool stage_gemv(const Ctx &c, ConsRing &rc, int s, in
                     vr[j] = __float2half_rn(v0);
                     vr[j + half] = __float2half_rn(v1);
                 }
-                fence_proxy_async_global();   // K/V rows are read by TMA in later steps
+                if (hh >= g.Hq) fence_proxy_async_global();   // K/V rows are read by TMA in later steps
             } else if (s == ST_O) {
-                const float xin = (l == 0) ? __half2float(p.embed[(size_t)tok * g.d + u])
-                                           : __ldcg(p.xout + (size_t)(l - 1) * g.d + u);
-                p.xattn[(size_t)l * g.d + u] = xin + sum;
+                p.xattn[(size_t)l * g.d + u] = pre.x + sum;
             } else if (s == ST_GU) {
                 const float gt = sum * inv, up = partner * inv;
                 p.hbuf[(size_t)l * g.F + u] = gt / (1.0f + expf(-gt)) * up;
             } else if (s == ST_D) {
-                p.xout[(size_t)l * g.d + u] = __ldcg(p.xattn + (size_t)l * g.d + u) + sum;
+                p.xout[(size_t)l * g.d + u] = pre.x + sum;
             } else {
                 const float logit = sum * inv;
                 if (p.debug_logits) p.debug_logits[(size_t)step * g.V + u] = logit;
@@ -682,14 +977,44 @@ __device__ __forceinline__ bool stage_gemv(const Ctx &c, ConsRing &rc, int s, in
                 c.lmkeys[u - u0] = sel_key(keyv, u);
             }
         }
+        __syncwarp();
+        if (c.lane == 0 && s != ST_LM && !withhold) {
+            if (s == ST_QKV) publish_range(sig_ptr(p, l, sl.qkvh), a, nu, g.hd / 2);
+            else if (s == ST_O) publish_range(sig_ptr(p, l, sl.xattn), a, nu, KC);
+            else if (s == ST_GU) publish_range(sig_ptr(p, l, sl.h), a, nu, KC);
+            else publish_range(sig_ptr(p, l, sl.xout), a, nu, KC);
+        }
     }
-    // every warp counts the same tiles: advance the kernel-wide tile sequence
-    // (after the stage's closing barrier nobody reads the old value)
-    if (cons_sync_or(ab)) return true;
-    if (c.tid == 0) c.misc[M_TSEQ] += (unsigned)nt;
-    if (p.trace && c.tid == 0 && step < p.trace_steps)
-        p.trace[(((size_t)step * trace_slots(g.L) + tslot) * p.P + c.b) * TR_N + TR_WAITS] = rc.waited - waited0;
-    return false;
+    if (c.lane == 0) {
+        trace_mark_producer(c, step, tslot, TR_DONE);
+        if (s == ST_LM) {
+            __threadfence_block();
+            *reinterpret_cast<volatile unsigned *>(&c.misc[M_LMDONE]) = (unsigned)step + 1u;
+        } else if (p.sched == SCHED_GRID && !withhold) {
+            fence_acq_rel_gpu();
+            red_release_add(p.gbar, 1u);
+        }
+    }
+    __syncwarp();
+    return ab;
+}
+
+// The reducer warp walks the same sub-stages as the consumers.
+__device__ void reducer(const Ctx &c)
+{
+    const Params &p = *c.p;
+    const Geo &g = p.g;
+    const int n_sub = 5 * g.L + (p.mode == MODE_DECODE ? 1 : 0);
+    PipeState ps;
+    for (int step = 0; step < p.n_steps; ++step) {
+        for (int k = 0; k < n_sub; ++k) {
+            const bool lm = k == 5 * g.L;
+            const int l = lm ? g.L - 1 : k / 5;
+            const int sid = lm ? SID_LM : k % 5;
+            if (!stage_active(p, l, sid) || sid == SID_ATTN) continue;
+            if (reduce_stage(c, ps, stage_of(sid), l, step, false)) return;
+        }
+    }
 }
 
 // ---------------------------------------------------------------- attention
@@ -725,11 +1050,22 @@ __device__ __forceinline__ bool attn_piece(const Ctx &c, ConsRing &rc, int l, in
     const int myh = c.warp % G, mys = c.warp / G;       // head, slab residue of this warp
 
     // ---- shared scratch: q [G][HD] FP32, fresh K and V rows [2][HD] FP16, warp states [NCW][HD + 2]
-    float *qs = c.act;
+    float *qs = c.acta;
     __half *fresh = reinterpret_cast<__half *>(qs + G * HD);
     float *ws = qs + G * HD + HD;
     const size_t kvbase = ((size_t)l * g.Hkv + gkv) * g.max_seq;
     const bool has_fresh = pos >= j0 && pos < j1;
+    // ---- flag schedule: wait for the query heads of the group and the key and
+    // value heads of gkv (this step's QKV outputs), one thread per counter
+    if (p.sched == SCHED_FLAGS) {
+        const SigLayout sl = sig_layout(g);
+        const unsigned target = (unsigned)H2 * (p.epoch0 + (unsigned)step + 1u);
+        if (c.tid < G + 2 && !ab) {
+            const int hh = c.tid < G ? hq0 + c.tid : (c.tid == G ? g.Hq + gkv : g.Hq + g.Hkv + gkv);
+            ab = !wait_counter(p, sig_ptr(p, l, sl.qkvh + hh), target, 140, l, step);
+        }
+        if (cons_sync_or(ab)) return true;
+    }
     if (!ab) {
         const float *qsrc = p.qbuf + (size_t)l * g.Q + (size_t)hq0 * HD;
         for (int i = c.tid; i < G * HD / 4; i += NCT)
@@ -856,7 +1192,7 @@ __device__ __forceinline__ bool attn_piece(const Ctx &c, ConsRing &rc, int l, in
     constexpr int PB = 16;
     const int ns = sp.n_split;
     const float *base = p.apart + ((size_t)l * g.Hq + hq0) * p.max_split * (HD + 2);
-    float2 *mls = reinterpret_cast<float2 *>(c.act);   // [G][ns] (m, l); act is free after the merge
+    float2 *mls = reinterpret_cast<float2 *>(c.acta);  // [G][ns] (m, l); the scratch is free after the merge
     const int n_el = G * HD;
     const int n_it = ceil_div(n_el, 2 * NCT);           // the same for every thread
     float o0[PB], o1[PB];
@@ -907,7 +1243,10 @@ __device__ __forceinline__ bool attn_piece(const Ctx &c, ConsRing &rc, int l, in
         if (e0 < n_el) p.attn[(size_t)l * g.Q + (size_t)hq0 * HD + e0] = n0 / d0;
         if (e1 < n_el) p.attn[(size_t)l * g.Q + (size_t)hq0 * HD + e1] = n1 / d1;
     }
-    return cons_publish(c, layer_cnt(p, l, C_ATTN), true, nullptr, ab);
+    // ---- count the group's G x hd outputs in the attention-output slices
+    if (cons_sync_or(ab)) return true;
+    if (c.tid == 0) publish_range(sig_ptr(p, l, sig_layout(g).attn), hq0 * HD, G * HD, KC);
+    return false;
 }
 
 // ---------------------------------------------------------------- LM head selection
@@ -1078,59 +1417,25 @@ __device__ void consumer(const Ctx &c)
     const Params &p = *c.p;
     const Geo &g = p.g;
     ConsRing rc;
+    PipeState ps;
     const bool ab = false;
-    const bool grid = p.sched == SCHED_GRID;
     const bool decode = p.mode == MODE_DECODE;
     const int n_sub = 5 * g.L + (decode ? 1 : 0);
     for (int step = 0; step < p.n_steps; ++step) {
-        const unsigned e = p.epoch0 + (unsigned)step;
         for (int k = 0; k < n_sub; ++k) {
             const bool lm = k == 5 * g.L;
             const int l = lm ? g.L - 1 : k / 5;
             const int sid = lm ? SID_LM : k % 5;
             if (!stage_active(p, l, sid)) continue;
             trace_mark(c, step, k, TR_ENTER);
-            // ---- what this sub-stage waits for: the producer counter (flag
-            // schedule) or the grid barrier that closes the previous sub-stage
-            const unsigned *ctr = nullptr;
-            unsigned target = 0;
-            int gstep = step, gl = l, gslot = sid - 1;
-            if (sid == SID_QKV) {
-                if (l > 0) {
-                    ctr = layer_cnt(p, l - 1, C_D);
-                    target = (e + 1u) * p.n_prod[ST_D];
-                    gl = l - 1;
-                    gslot = 4;
-                } else {
-                    if (decode && step > 0) {
-                        ctr = p.tok_cnt;                        // the previous step's token
-                        target = p.tok_base + (unsigned)step;
-                    }
-                    gstep = step - 1;
-                    gl = g.L - 1;
-                    gslot = step > 0 ? (decode ? 5 : 4) : -1;
-                }
-            } else if (sid == SID_ATTN) {
-                ctr = layer_cnt(p, l, C_QKV);
-                target = (e + 1u) * p.n_prod[ST_QKV];
-            } else if (sid == SID_O) {
-                ctr = layer_cnt(p, l, C_ATTN);
-                target = (e + 1u) * (unsigned)g.Hkv;
-            } else if (sid == SID_GU) {
-                ctr = layer_cnt(p, l, C_O);
-                target = (e + 1u) * p.n_prod[ST_O];
-            } else if (sid == SID_D) {
-                ctr = layer_cnt(p, l, C_GU);
-                target = (e + 1u) * p.n_prod[ST_GU];
-            } else {
-                ctr = layer_cnt(p, g.L - 1, C_D);
-                target = (e + 1u) * p.n_prod[ST_D];
-                gslot = 4;
-            }
-            if (stage_wait(c, ctr, target, gstep, gl, gslot, step, l, 1 + sid, ab)) return;
-            trace_mark(c, step, k, TR_READY);
-
             if (sid == SID_ATTN) {
+                // barrier schedule: the whole QKV stage, everywhere (the flag
+                // schedule waits per unit inside attn_piece)
+                unsigned idx;
+                if (p.sched == SCHED_GRID && grid_barrier_before(p, step, l, sid, idx)) {
+                    if (cons_wait(c, p.gbar, (idx + 1u) * (unsigned)p.P, 2, l, step, ab)) return;
+                }
+                trace_mark(c, step, k, TR_READY);
                 const int ctx = p.pos0 + step + 1;
                 const AttnSplit sp = attn_split(ctx, p.P, g.Hkv, p.attn_min_len);
                 const int U = g.Hkv * sp.n_split;
@@ -1140,20 +1445,24 @@ __device__ void consumer(const Ctx &c)
                                                     : attn_piece<64>(c, rc, l, step, gkv, cp, sp, ab);
                     if (stop) return;
                 }
-                if (grid && cons_publish(c, nullptr, false, p.gbar, ab)) return;
+                // hand the scratch in buffer A back to the loader
+                if (cons_sync_or(ab)) return;
+                if (c.tid == 0) {
+                    __threadfence_block();
+                    atomicAdd(&c.misc[M_ASCR], 1u);
+                }
+                if (p.sched == SCHED_GRID && cons_grid_arrive(c, ab)) return;
+                trace_mark(c, step, k, TR_DONE);
             } else {
-                const int st = sid == SID_QKV ? ST_QKV : sid == SID_O ? ST_O : sid == SID_GU ? ST_GU
-                                                       : sid == SID_D ? ST_D : ST_LM;
-                if (stage_gemv(c, rc, st, l, step, ab)) return;
+                if (stage_gemv(c, rc, ps, stage_of(sid), l, step, ab)) return;
                 if (lm) {
+                    // the reducer's keys of every LM-head tile of this CTA
+                    bool fail = false;
+                    if (c.tid == 0) fail = !wait_smem_ge(p, &c.misc[M_LMDONE], (unsigned)step + 1u, 112, l, step);
+                    if (cons_sync_or(fail)) return;
                     if (stage_lm_sample(c, step, ab)) return;
-                } else {
-                    const bool withhold = decode && step == p.fault_step && l == 0 && sid == SID_QKV;
-                    if (cons_publish(c, layer_cnt(p, l, sid), !withhold, (grid && !withhold) ? p.gbar : nullptr, ab))
-                        return;
                 }
             }
-            trace_mark(c, step, k, TR_DONE);
         }
     }
 }
@@ -1289,16 +1598,18 @@ __device__ void producer(const Ctx &c, const RepackSrc *w)
             const AttnSplit sp = attn_split(pos + 1, p.P, g.Hkv, p.attn_min_len);
             const int U = g.Hkv * sp.n_split;
             const int S = attn_sub_positions(g.hd);
-            bool guarded = (step == 0);
             for (int u = attn_unit_first(c.b, l, U, p.P); u < U && ok; u += p.P) {
                 const int gkv = u / sp.n_split, cp = u % sp.n_split;
                 const int j0 = cp * sp.per;
                 const int jr = min(min(j0 + sp.per, pos + 1), pos);
-                if (jr > j0 && !guarded) {
-                    // positions < pos of step > 0 were written by the previous step's QKV stage
-                    ok = wait_counter(p, layer_cnt(p, l, C_QKV), e * p.n_prod[ST_QKV], 102, l, step);
+                if (jr > j0 && step > 0) {
+                    // position pos - 1 of step > 0 was written by the previous
+                    // step's QKV stage: its key and value heads of gkv
+                    const SigLayout sl = sig_layout(g);
+                    const unsigned prev = (unsigned)(g.hd / 2) * e;
+                    ok = wait_counter(p, sig_ptr(p, l, sl.qkvh + g.Hq + gkv), prev, 102, l, step) &&
+                         wait_counter(p, sig_ptr(p, l, sl.qkvh + g.Hq + g.Hkv + gkv), prev, 103, l, step);
                     fence_proxy_async_global();
-                    guarded = true;
                 }
                 const size_t base = (((size_t)l * g.Hkv + gkv) * g.max_seq) * g.hd;
                 for (int jb = j0; jb < jr && ok; jb += S) {
@@ -1319,16 +1630,22 @@ template <bool kDirect>
 __device__ __forceinline__ void monokernel_body(const Params &p, const RepackSrc *w)
 {
     extern __shared__ __align__(128) uint8_t smem[];
-    const SmemLayout L = smem_layout(p.ring_bytes, p.act_floats, p.lm_rows_max);
+    const SmemLayout L = smem_layout(p.ring_bytes, p.a_floats, p.b_slots, p.g.d, p.lm_rows_max);
     Ctx c;
     c.p = &p;
     c.ring = smem + L.ring;
-    c.act = reinterpret_cast<float *>(smem + L.act);
+    c.acta = reinterpret_cast<float *>(smem + L.acta);
+    c.actb = reinterpret_cast<float *>(smem + L.actb);
+    c.gain = reinterpret_cast<__half *>(smem + L.gain);
     c.lmkeys = reinterpret_cast<unsigned long long *>(smem + L.lmkeys);
     c.res = reinterpret_cast<float *>(smem + L.res);
     c.full = reinterpret_cast<uint64_t *>(smem + L.full);
     c.empty = reinterpret_cast<uint64_t *>(smem + L.empty);
     c.chunk_end = reinterpret_cast<unsigned long long *>(smem + L.chunk_end);
+    c.afull = reinterpret_cast<uint64_t *>(smem + L.afull);
+    c.bfull = reinterpret_cast<uint64_t *>(smem + L.bfull);
+    c.gfull = reinterpret_cast<uint64_t *>(smem + L.gfull);
+    c.brel = reinterpret_cast<unsigned *>(smem + L.brel);
     c.red = reinterpret_cast<float *>(smem + L.red);
     c.hist = reinterpret_cast<unsigned *>(smem + L.hist);
     c.misc = reinterpret_cast<unsigned *>(smem + L.misc);
@@ -1343,13 +1660,27 @@ __device__ __forceinline__ void monokernel_body(const Params &p, const RepackSrc
             mbar_init(&c.full[i], 1);
             mbar_init(&c.empty[i], NCW);
         }
+        for (int i = 0; i < MAX_SLICES; ++i) {
+            mbar_init(&c.afull[i], 1);
+            mbar_init(&c.bfull[i], 1);
+        }
+        mbar_init(c.gfull, 1);
         mbar_fence_init();
         *plan_s = p.plans[blockIdx.x];
         for (int i = 0; i < 64; ++i) c.misc[i] = 0u;
+        for (int i = 0; i < MAX_SLICES; ++i) c.brel[i] = 0u;
     }
     __syncthreads();
-    if (c.warp == NCW) {
+    if (c.warp == W_PROD) {
         if (c.lane == 0) producer<kDirect>(c, w);
+        return;
+    }
+    if (c.warp == W_LOAD) {
+        loader(c);
+        return;
+    }
+    if (c.warp == W_RED) {
+        reducer(c);
         return;
     }
     consumer(c);
@@ -1433,9 +1764,9 @@ extern "C" cudaError_t lfk_occupancy(int smem_bytes, int *blocks_per_sm)
                                                         (size_t)smem_bytes);
 }
 
-extern "C" unsigned lfk_smem_bytes(int ring_bytes, int act_floats, int lm_rows_max)
+extern "C" unsigned lfk_smem_bytes(int ring_bytes, int a_floats, int b_slots, int d, int lm_rows_max)
 {
-    return lfk::smem_layout(ring_bytes, act_floats, lm_rows_max).total;
+    return lfk::smem_layout(ring_bytes, a_floats, b_slots, d, lm_rows_max).total;
 }
 
 extern "C" cudaError_t lfk_launch_repack(lfk::Geo g, int P, const lfk::CtaPlan *plans, const void *wq, const void *wk,

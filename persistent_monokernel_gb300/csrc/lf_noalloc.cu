@@ -26,7 +26,7 @@
 #include "../../include/lf.h"
 #include "lf_internal.cuh"
 
-extern "C" unsigned lfk_smem_bytes(int ring_bytes, int act_floats, int lm_rows_max);
+extern "C" unsigned lfk_smem_bytes(int ring_bytes, int a_floats, int b_slots, int d, int lm_rows_max);
 extern "C" cudaError_t lfk_set_smem_direct(int smem_bytes);
 extern "C" cudaError_t lfk_launch_monokernel_direct(const lfk::Params *p, const void *wq, const void *wk,
                                                     const void *wv, const void *wo, const void *wg, const void *wu,
@@ -69,13 +69,16 @@ extern "C" LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_w
     const void *need[] = {w->embed, w->attn_norm, w->wq, w->wk, w->wv, w->wo, w->ffn_norm,
                           w->w_gate, w->w_up, w->w_down, w->final_norm, w->lm_head};
     for (const void *p : need)
-        if (!p) return LF_ERR_INVALID_ARG;
+        if (!p || (reinterpret_cast<uintptr_t>(p) & 15u)) return LF_ERR_INVALID_ARG;   // bulk copies need 16 B
     if (cfg->n_layers <= 0 || cfg->d_model <= 0 || cfg->n_heads <= 0 || cfg->n_kv_heads <= 0 || cfg->ffn_dim <= 0 ||
         cfg->vocab <= 0 || cfg->max_seq <= 0 || cfg->n_ctas < 0 || !(cfg->rope_theta > 0.f) || !(cfg->rms_eps >= 0.f))
         return LF_ERR_INVALID_ARG;
     if (cfg->head_dim != 64 && cfg->head_dim != 128) return LF_ERR_NOT_SUPPORTED;
     if (cfg->n_heads % cfg->n_kv_heads || lfk::MAX_GROUP % (cfg->n_heads / cfg->n_kv_heads)) return LF_ERR_NOT_SUPPORTED;
     if (cfg->d_model % lfk::KC || (cfg->n_heads * cfg->head_dim) % lfk::KC || cfg->ffn_dim % lfk::KC)
+        return LF_ERR_NOT_SUPPORTED;
+    const long long most = (long long)lfk::MAX_SLICES * lfk::KC;
+    if (cfg->d_model > most || (long long)cfg->n_heads * cfg->head_dim > most || cfg->ffn_dim > most)
         return LF_ERR_NOT_SUPPORTED;
     if (sp->top_k < 0 || sp->top_k > LF_MAX_TOP_K) return LF_ERR_NOT_SUPPORTED;
     if ((long long)n_prompt + n_steps > cfg->max_seq) return LF_ERR_CAPACITY;
@@ -116,21 +119,19 @@ extern "C" LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_w
         lm_rows_max = n_lm > lm_rows_max ? n_lm : lm_rows_max;
     }
     const int max_split = P / g.Hkv > 1 ? P / g.Hkv : 1;
-    int act = lfk::MAX_GROUP * g.hd + g.hd + lfk::NCW * (g.hd + 2);
-    if (2 * g.group * max_split > act) act = 2 * g.group * max_split;
-    const int dims[] = {g.d, g.Q, g.F};
-    for (int v : dims) act = v > act ? v : act;
-    act = (act + 3) / 4 * 4;
-    const unsigned rest = lfk_smem_bytes(0, act, lm_rows_max);
+    int a_floats = 0, b_slots = 0;
+    lfk::act_sizes(g, h_plans, P, max_split, a_floats, b_slots);
+    const unsigned rest = lfk_smem_bytes(0, a_floats, b_slots, g.d, lm_rows_max);
     if ((int)rest + 2 * lfk::ATT_CHUNK_BYTES > optin) return LF_ERR_NOT_SUPPORTED;
     int ring = (int)(((unsigned)optin - rest) / 1024u * 1024u);
-    while ((int)lfk_smem_bytes(ring, act, lm_rows_max) > optin) ring -= 1024;
-    const int smem = (int)lfk_smem_bytes(ring, act, lm_rows_max);
+    while ((int)lfk_smem_bytes(ring, a_floats, b_slots, g.d, lm_rows_max) > optin) ring -= 1024;
+    const int smem = (int)lfk_smem_bytes(ring, a_floats, b_slots, g.d, lm_rows_max);
 
     // ---- scratch layout inside the static array
     const size_t kv_elems = (size_t)g.L * g.Hkv * (size_t)g.max_seq * g.hd;
-    const size_t n_layer_cnt = (size_t)g.L * lfk::N_LAYER_CNT, n_attn_done = (size_t)g.L * g.Hkv;
-    const size_t cnt_words = (n_layer_cnt + n_attn_done + 3) * lfk::CNT_STRIDE;
+    const size_t sig_words = (size_t)g.L * lfk::sig_layout(g).per_layer * lfk::SIG_STRIDE;
+    const size_t n_attn_done = (size_t)g.L * g.Hkv;
+    const size_t cnt_words = sig_words + (n_attn_done + 3) * lfk::CNT_STRIDE;
     const size_t rope_elems = (size_t)g.max_seq * (g.hd / 2);
     size_t off = 0;
     const size_t o_plans = carve(off, sizeof(lfk::CtaPlan) * P);
@@ -193,12 +194,11 @@ extern "C" LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_w
     p.apart = reinterpret_cast<float *>(base + o_apart);
     p.max_split = max_split;
     unsigned *cnt = reinterpret_cast<unsigned *>(base + o_cnt);
-    p.cnt = cnt;
-    p.attn_done = cnt + n_layer_cnt * lfk::CNT_STRIDE;
+    p.sig = cnt;
+    p.attn_done = cnt + sig_words;
     p.lm_done = p.attn_done + n_attn_done * lfk::CNT_STRIDE;
     p.tok_cnt = p.lm_done + lfk::CNT_STRIDE;
     p.gbar = p.tok_cnt + lfk::CNT_STRIDE;
-    for (int s = 0; s < 4; ++s) p.n_prod[s] = (unsigned)P;
     p.lm_part = reinterpret_cast<unsigned long long *>(base + o_lm);
     p.tok_buf = reinterpret_cast<int *>(base + o_tok);
     p.tok_seq = p.tok_buf + 1;
@@ -207,7 +207,8 @@ extern "C" LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_w
     p.timeout_ns = cfg->wait_timeout_ns > 0 ? cfg->wait_timeout_ns : kTimeoutNs;
     p.fault_step = -1;
     p.ring_bytes = ring;
-    p.act_floats = act;
+    p.a_floats = a_floats;
+    p.b_slots = b_slots;
     p.lm_rows_max = lm_rows_max;
     p.attn_min_len = kAttnMinLen;
     p.sched = lfk::SCHED_FLAGS;

@@ -51,6 +51,11 @@ __device__ __forceinline__ void red_release_add(unsigned *p, unsigned v)
 {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+// Relaxed add at gpu scope; a preceding fence.acq_rel.gpu makes it a release.
+__device__ __forceinline__ void red_relaxed_add(unsigned *p, unsigned v)
+{
+    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 __device__ __forceinline__ unsigned atom_add_acq_rel(unsigned *p, unsigned v)
 {
     unsigned old;
