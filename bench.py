@@ -308,9 +308,40 @@ def run_ours(args):
                             ("multi_kernel", pm.SCHED_MULTI_KERNEL)):
             dec.set_schedule(sched)
             ab[name + "_tok_s"] = round(n_ab / timed_decode(n_ab), 2)
+        # the multi-kernel launches captured once into a CUDA graph and replayed:
+        # the graph removes the host launch overhead, not the kernel boundaries
+        # (replays recompute the same positions, so the work per replay is fixed)
+        dec.set_schedule(pm.SCHED_MULTI_KERNEL)
+        dec.reset()
+        dec.prefill(prompt)
+        out_g = torch.empty(n_ab, dtype=torch.int32, device="cuda")
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            dec.decode(n_ab, out=out_g, **samp)
+        graph.replay()
+        torch.cuda.synchronize()
+        reps = 3
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            graph.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ab["multi_kernel_cuda_graph_tok_s"] = round(n_ab * reps / (e0.elapsed_time(e1) / 1e3), 2)
+        del graph
+        if dec.sync() != 0:
+            raise RuntimeError("multi-kernel graph ablation failed")
         dec.set_schedule(pm.SCHED_FLAGS)
         ab["launches_per_step_multi_kernel"] = 5 * cfg.n_layers + 1
         result["ablations"] = ab
+        # one-hop readiness flag vs grid barrier over the same number of CTAs
+        n_ctas = info["n_ctas"]
+        result["sync_latency_ns"] = {
+            "ctas": n_ctas,
+            "flag_hop": round(pm.sync_latency_ns(0, n_ctas, 200), 1),
+            "grid_barrier": round(pm.sync_latency_ns(1, n_ctas, 200), 1),
+        }
 
     if not args.no_e2e:
         import numpy as np

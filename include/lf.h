@@ -268,6 +268,18 @@ LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_weights *w, 
 /* Static string naming a status code. */
 LF_API const char *lf_error_string(lf_status s);
 
+/* Microbenchmark of grid synchronisation on the current device (no handle).
+ * mode 0: one-hop readiness flag -- a token is passed round a ring of n_ctas
+ * CTAs `iters` times, each hop a gpu-scope release add by one CTA and an
+ * acquire poll by the next; *ns_out = nanoseconds per hop.
+ * mode 1: arrival-counter grid barrier over n_ctas CTAs, `iters` times;
+ * *ns_out = nanoseconds per barrier.
+ * Both run as one cooperative launch of n_ctas one-warp CTAs on the legacy
+ * default stream and synchronize the device.  Waits are bounded (1 s).
+ * Errors: INVALID_ARG (mode, n_ctas < 2, iters < 1, NULL), NOT_RESIDENT
+ * (n_ctas above the SM count), OUT_OF_MEMORY, TIMEOUT, CUDA. */
+LF_API lf_status lf_sync_latency(int32_t mode, int32_t n_ctas, int32_t iters, double *ns_out);
+
 /* LF_ABI_VERSION of the built library. */
 LF_API int32_t lf_abi_version(void);
 

@@ -24,7 +24,7 @@ TRACE_STAMPS = 9
 # Every symbol include/lf.h declares.
 EXPORTS = ("lf_create", "lf_destroy", "lf_prefill", "lf_decode", "lf_generate", "lf_sync", "lf_reset",
            "lf_set_schedule", "lf_get_info", "lf_error_string", "lf_abi_version", "lf_generate_noalloc",
-           "lf_enable_trace", "lf_read_trace")
+           "lf_enable_trace", "lf_read_trace", "lf_sync_latency")
 
 
 class LFError(RuntimeError):
@@ -92,6 +92,8 @@ def lib() -> C.CDLL:
         L.lf_enable_trace.restype = C.c_int
         L.lf_read_trace.argtypes = [vp, vp, C.c_int64, C.POINTER(C.c_int64)]
         L.lf_read_trace.restype = C.c_int
+        L.lf_sync_latency.argtypes = [C.c_int32, C.c_int32, C.c_int32, C.POINTER(C.c_double)]
+        L.lf_sync_latency.restype = C.c_int
         for name in ("lf_create", "lf_prefill", "lf_decode", "lf_generate", "lf_sync", "lf_reset",
                      "lf_set_schedule", "lf_get_info"):
             getattr(L, name).restype = C.c_int
@@ -215,6 +217,13 @@ class Decoder:
         i = lf_info()
         _check(lib().lf_get_info(self._h, C.byref(i)), "lf_get_info")
         return {f: getattr(i, f) for f, _ in lf_info._fields_}
+
+
+def sync_latency_ns(mode: int, n_ctas: int, iters: int) -> float:
+    """lf_sync_latency: ns per flag hop (mode 0) or per grid barrier (mode 1)."""
+    v = C.c_double()
+    _check(lib().lf_sync_latency(int(mode), int(n_ctas), int(iters), C.byref(v)), "lf_sync_latency")
+    return v.value
 
 
 def error_string(status: int) -> str:

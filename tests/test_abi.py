@@ -58,6 +58,12 @@ def test_create_rejects_bad_arguments_before_touching_the_gpu(pm):
     wnull = pm.lf_weights(*([0x1000] * 11 + [0]))
     cfg = pm.lf_config(**good)
     assert L.lf_create(C.byref(cfg), C.byref(wnull), C.byref(h)) == 1
+    # bulk copies read the weights: every pointer must be 16-byte aligned
+    wodd = pm.lf_weights(*([0x1000] * 3 + [0x1008] + [0x1000] * 8))
+    assert L.lf_create(C.byref(cfg), C.byref(wodd), C.byref(h)) == 1
+    # more than 64 column groups of 256 in one vector
+    cfg = pm.lf_config(**{**good, "ffn_dim": 256 * 65})
+    assert L.lf_create(C.byref(cfg), C.byref(w), C.byref(h)) == 7
 
 
 def test_calls_on_a_null_handle_are_rejected(pm):
@@ -69,3 +75,12 @@ def test_calls_on_a_null_handle_are_rejected(pm):
     assert L.lf_reset(None) == 1
     assert L.lf_set_schedule(None, 0) == 1
     L.lf_destroy(None)
+
+
+def test_sync_latency_rejects_bad_arguments_before_touching_the_gpu(pm):
+    L = pm.lib()
+    v = C.c_double()
+    assert L.lf_sync_latency(2, 8, 10, C.byref(v)) == 1
+    assert L.lf_sync_latency(0, 1, 10, C.byref(v)) == 1
+    assert L.lf_sync_latency(1, 8, 0, C.byref(v)) == 1
+    assert L.lf_sync_latency(0, 8, 10, None) == 1
