@@ -31,7 +31,7 @@ constexpr int SIG_STRIDE = 8;         // uint32 words between slice readiness co
 constexpr int PART_BUFS = 8;          // rotating per-tile partial-sum buffers of a GEMV stage
 constexpr int PART_STRIDE = TILE_ROWS + 1;  // per warp: 32 row sums + the sum of squares of x
 constexpr int MAX_SLICES = 64;        // 256-element slices of one activation vector (length <= 16384)
-constexpr int B_RING_SLOTS = 16;      // slots of the O / down-projection input ring
+constexpr int B_RING_SLOTS = 32;      // slots of the O / down-projection input ring
 
 enum Stage { ST_QKV = 0, ST_O = 1, ST_GU = 2, ST_D = 3, ST_LM = 4, N_GEMV = 5 };
 enum Mode { MODE_PREFILL = 0, MODE_DECODE = 1 };
