@@ -77,6 +77,7 @@ def lib():
             L.orc_create.restype = C.c_void_p
             L.orc_destroy.argtypes = [C.c_void_p]
             L.orc_reset.argtypes = [C.c_void_p]
+            L.orc_set_windows.argtypes = [C.c_void_p, C.POINTER(C.c_int32)]
             L.orc_pos.argtypes = [C.c_void_p]
             L.orc_pending.argtypes = [C.c_void_p]
             L.orc_kcache.argtypes = [C.c_void_p]
@@ -187,9 +188,11 @@ def num_threads() -> int:
 
 class OracleDecoder:
     """The whole decoder on the CPU.  `weights` maps the synthetic tensor
-    names to FP16 arrays (numpy float16 or CPU torch.float16)."""
+    names to FP16 arrays (numpy float16 or CPU torch.float16).
+    `layer_window`: None (every layer attends to the whole cache) or one
+    window per layer in positions, 0 = the whole cache."""
 
-    def __init__(self, cfg, weights: dict, max_seq: int):
+    def __init__(self, cfg, weights: dict, max_seq: int, layer_window=None):
         self.cfg = cfg
         self.max_seq = max_seq
         self._keep = {n: _as_u16(weights[n]) for n in _WNAMES}
@@ -199,6 +202,11 @@ class OracleDecoder:
         self._h = lib().orc_create(C.byref(c), C.byref(w))
         if not self._h:
             raise ValueError("orc_create rejected the configuration")
+        if layer_window is not None:
+            win = np.ascontiguousarray(np.asarray(layer_window, dtype=np.int32))
+            if win.shape != (cfg.n_layers,):
+                raise ValueError("layer_window needs one entry per layer")
+            lib().orc_set_windows(self._h, _i32(win))
 
     def close(self):
         if getattr(self, "_h", None):

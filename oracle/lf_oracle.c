@@ -265,6 +265,7 @@ typedef struct {
     uint16_t *vcache;
     int pos;            /* position of the pending token */
     int pending;        /* token fed to the next forward pass, -1 if none */
+    int *window;        /* [L] attention window of each layer in positions, 0 = the whole cache */
     /* activations */
     float *x, *xn, *q, *k, *v, *attn, *tmp, *gate, *up, *hbuf, *scores;
 } orc_model;
@@ -290,7 +291,8 @@ ORC_API orc_model *orc_create(const orc_config *c, const orc_weights *w)
     m->up = (float *)calloc((size_t)F, 4);
     m->hbuf = (float *)calloc((size_t)F, 4);
     m->scores = (float *)calloc((size_t)c->n_heads * (size_t)c->max_seq, 4);
-    if (!m->kcache || !m->vcache || !m->scores) { free(m); return NULL; }
+    m->window = (int *)calloc((size_t)c->n_layers, sizeof(int));
+    if (!m->kcache || !m->vcache || !m->scores || !m->window) { free(m); return NULL; }
     m->pos = 0;
     m->pending = -1;
     return m;
@@ -301,11 +303,21 @@ ORC_API void orc_destroy(orc_model *m)
     if (!m) return;
     free(m->kcache); free(m->vcache);
     free(m->x); free(m->xn); free(m->q); free(m->k); free(m->v); free(m->attn);
-    free(m->tmp); free(m->gate); free(m->up); free(m->hbuf); free(m->scores);
+    free(m->tmp); free(m->gate); free(m->up); free(m->hbuf); free(m->scores); free(m->window);
     free(m);
 }
 
 ORC_API void orc_reset(orc_model *m) { m->pos = 0; m->pending = -1; }
+
+/* Sliding-window attention (shivam2003.com, model table and "Why GQA and
+ * sliding windows": some layers attend only to a window of recent positions,
+ * so that the KV cache they read stops growing with the context).  window[l]
+ * = W > 0: the query at position p of layer l attends to the W positions
+ * max(0, p-W+1) .. p; W = 0: to every cached position.  NULL clears them. */
+ORC_API void orc_set_windows(orc_model *m, const int *window)
+{
+    for (int l = 0; l < m->c.n_layers; ++l) m->window[l] = window ? (window[l] > 0 ? window[l] : 0) : 0;
+}
 ORC_API int orc_pos(const orc_model *m) { return m->pos; }
 ORC_API int orc_pending(const orc_model *m) { return m->pending; }
 ORC_API const uint16_t *orc_kcache(const orc_model *m) { return m->kcache; }
@@ -350,11 +362,14 @@ ORC_API int orc_forward(orc_model *m, int token, float *logits)
                 m->vcache[base + i] = orc_float_to_half(m->v[g * hd + i]);
             }
         }
+        /* positions j0 .. p: the whole cache, or the layer's window */
+        int j0 = 0;
+        if (m->window[l] > 0 && p + 1 > m->window[l]) j0 = p + 1 - m->window[l];
         #pragma omp parallel for schedule(static)
         for (int h = 0; h < Hq; ++h) {
             int g = h / group;
-            size_t base = ((size_t)l * Hkv + g) * (size_t)c->max_seq * hd;
-            orc_attend_head(m->q + h * hd, m->kcache + base, m->vcache + base, p + 1, hd, scale,
+            size_t base = (((size_t)l * Hkv + g) * (size_t)c->max_seq + (size_t)j0) * hd;
+            orc_attend_head(m->q + h * hd, m->kcache + base, m->vcache + base, p + 1 - j0, hd, scale,
                             m->scores + (size_t)h * c->max_seq, m->attn + h * hd);
         }
         orc_matvec(w->wo + (size_t)l * d * Q, m->attn, d, Q, m->tmp);

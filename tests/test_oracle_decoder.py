@@ -16,9 +16,10 @@ def _w(cfg, seed, gains="random"):
     return {k: v.numpy() for k, v in make_weights(cfg, seed, gains=gains).items()}
 
 
-def _brute_force_logits(cfg, w, tokens):
+def _brute_force_logits(cfg, w, tokens, window=None):
     """The decoder written out literally in float64 (K and V rounded to FP16
-    on store), one position at a time; returns logits for every position."""
+    on store), one position at a time; returns logits for every position.
+    window[l] = W > 0: layer l attends to positions max(0, p-W+1) .. p only."""
     L, d, Hq, Hkv, hd, F = cfg.n_layers, cfg.d_model, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim, cfg.ffn_dim
     f = {k: v.astype(np.float64) for k, v in w.items()}
     Kc = np.zeros((L, Hkv, len(tokens), hd))
@@ -50,9 +51,10 @@ def _brute_force_logits(cfg, w, tokens):
             for h in range(Hq):
                 g = h // (Hq // Hkv)
                 qh = rope(q[h * hd:(h + 1) * hd], p)
-                s = np.array([qh @ Kc[l, g, j] / math.sqrt(hd) for j in range(p + 1)])
+                j0 = max(0, p + 1 - window[l]) if window is not None and window[l] > 0 else 0
+                s = np.array([qh @ Kc[l, g, j] / math.sqrt(hd) for j in range(j0, p + 1)])
                 e = np.exp(s - s.max())
-                att[h * hd:(h + 1) * hd] = (e / e.sum()) @ Vc[l, g, :p + 1]
+                att[h * hd:(h + 1) * hd] = (e / e.sum()) @ Vc[l, g, j0:p + 1]
             x = x + f["wo"][l] @ att
             xn = norm(x, f["ffn_norm"][l])
             gt = f["w_gate"][l] @ xn
@@ -61,8 +63,8 @@ def _brute_force_logits(cfg, w, tokens):
     return np.array(all_logits)
 
 
-def _oracle_logits(cfg, w, tokens, max_seq=None):
-    o = oracle.OracleDecoder(cfg, w, max_seq or len(tokens))
+def _oracle_logits(cfg, w, tokens, max_seq=None, window=None):
+    o = oracle.OracleDecoder(cfg, w, max_seq or len(tokens), layer_window=window)
     return np.array([o.forward(int(t)) for t in tokens])
 
 
@@ -196,3 +198,41 @@ def test_synthetic_weights_are_device_independent_and_normal():
     assert abs(x.std() - 0.02) < 2e-4 and abs(x.mean()) < 2e-4
     from scipy import stats
     assert stats.kstest(x[::37] / 0.02, "norm").pvalue > 1e-3
+
+
+# ---- sliding-window attention (shivam2003.com, "Why GQA and sliding windows")
+
+@pytest.mark.parametrize("window", [[3, 0], [1, 4], [2, 2]])
+def test_sliding_window_matches_float64_brute_force(window):
+    cfg = TINYCFG
+    w = _w(cfg, 12)
+    for k in ("wq", "wk"):
+        w[k] = (w[k].astype(np.float32) * 40).astype(np.float16)
+    tokens = make_prompt(cfg.vocab, 10, 6).numpy()
+    got = _oracle_logits(cfg, w, tokens, window=window)
+    ref = _brute_force_logits(cfg, w, tokens, window=window)
+    np.testing.assert_allclose(got, ref, atol=2e-4, rtol=0)
+    # and the window does change the result once the context outgrows it
+    full = _brute_force_logits(cfg, w, tokens)
+    assert np.abs(full[-1] - ref[-1]).max() > 1e-3
+
+
+def test_window_covering_the_context_changes_nothing():
+    cfg = TINYCFG
+    w = _w(cfg, 13)
+    tokens = make_prompt(cfg.vocab, 8, 7).numpy()
+    np.testing.assert_array_equal(_oracle_logits(cfg, w, tokens, window=[8, 100]), _oracle_logits(cfg, w, tokens))
+
+
+def test_window_of_one_makes_every_position_see_only_itself():
+    """With W = 1 everywhere, attention returns the current position's V row
+    (one softmax weight of exactly 1), and the query-key rotations cancel, so
+    a token's logits no longer depend on its position or on earlier tokens."""
+    cfg = TINYCFG
+    w = _w(cfg, 14)
+    o = oracle.OracleDecoder(cfg, w, 16, layer_window=[1, 1])
+    first = o.forward(7)
+    for t in (3, 9, 1):
+        o.forward(t)
+    again = o.forward(7)
+    np.testing.assert_array_equal(first, again)
