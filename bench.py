@@ -151,19 +151,24 @@ def dist_setup():
 def workload_desc(wl, K):
     m = wl.model
     samp = "greedy" if not wl.temperature > 0 else f"T={wl.temperature}, top-k {wl.top_k}, Philox seed {wl.sample_seed}"
+    win = ""
+    if wl.layer_window is not None:
+        ws = sorted({w for w in wl.layer_window if w > 0})
+        nwin = sum(1 for w in wl.layer_window if w > 0)
+        win = f"; sliding-window attention (window {'/'.join(map(str, ws))}) in {nwin} of {m.n_layers} layers"
     return (f"{wl.name}: {m.n_layers} layers, d_model {m.d_model}, {m.n_heads}/{m.n_kv_heads} heads x {m.head_dim}, "
-            f"SwiGLU FFN {m.ffn_dim}, vocab {m.vocab}, FP16 weights ~N(0,0.02); prompt {wl.prompt_len}, "
+            f"SwiGLU FFN {m.ffn_dim}, vocab {m.vocab}, FP16 weights ~N(0,0.02){win}; prompt {wl.prompt_len}, "
             f"{K} decode steps ({samp})")
 
 
 # ------------------------------------------------------------------ CPU oracle timing
 
-def time_oracle(cfg, weights_cpu, prompt, budget_s: float, max_steps: int, warmup: int = 1):
+def time_oracle(cfg, weights_cpu, prompt, budget_s: float, max_steps: int, warmup: int = 1, layer_window=None):
     """Decode steps of the CPU oracle after a short prompt; returns (tok/s, steps, seconds, threads)."""
     import oracle
     n_prompt = len(prompt)
     cap = n_prompt + warmup + max_steps + 1
-    orc = oracle.OracleDecoder(cfg, weights_cpu, cap)
+    orc = oracle.OracleDecoder(cfg, weights_cpu, cap, layer_window=layer_window)
     orc.prefill(prompt)
     if warmup:
         orc.decode(warmup, want_logits=False)
@@ -208,7 +213,7 @@ def run_ours(args):
     max_seq = wl.prompt_len + max(K, W, 128)
     weights = make_weights(cfg, wl.weight_seed, device="cuda")
     prompt = make_prompt(cfg.vocab, wl.prompt_len, wl.prompt_seed).cuda()
-    dec = pm.Decoder(cfg, weights, max_seq)
+    dec = pm.Decoder(cfg, weights, max_seq, layer_window=wl.layer_window)
     info = dec.info()
     stream = torch.cuda.current_stream()
     samp = dict(temperature=wl.temperature, top_k=wl.top_k, seed=wl.sample_seed)
@@ -369,7 +374,7 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         wc = {k: v.cpu() for k, v in weights.items()}
         pr = make_prompt(cfg.vocab, 8, wl.prompt_seed).numpy()
-        tok_s, n, dt, threads = time_oracle(cfg, wc, pr, budget_s=15.0, max_steps=256)
+        tok_s, n, dt, threads = time_oracle(cfg, wc, pr, budget_s=15.0, max_steps=256, layer_window=wl.layer_window)
         result["cpu_baseline"] = {
             "value": round(tok_s, 4),
             "unit": "tok/s",
@@ -407,7 +412,8 @@ def run_reference(args):
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     wc = {k: v.cpu() for k, v in make_weights(cfg, wl.weight_seed, device=dev).items()}
     pr = make_prompt(cfg.vocab, 8, wl.prompt_seed).numpy()
-    tok_s, n, dt, threads = time_oracle(cfg, wc, pr, budget_s=60.0, max_steps=K, warmup=min(W, 3))
+    tok_s, n, dt, threads = time_oracle(cfg, wc, pr, budget_s=60.0, max_steps=K, warmup=min(W, 3),
+                                        layer_window=wl.layer_window)
     sample = (f"{n} of the {K} requested decode steps of the same decoder after an 8-token prompt "
               f"(context 8..{8 + n}), {dt:.1f} s on {threads} OpenMP threads; warm-up {min(W, 3)} steps")
     print(json.dumps({

@@ -44,7 +44,7 @@ extern "C" {
 #define LF_API
 #endif
 
-#define LF_ABI_VERSION 1
+#define LF_ABI_VERSION 2
 #define LF_MAX_TOP_K 64          /* largest top_k that lf_decode accepts (besides 0) */
 
 typedef enum {
@@ -96,6 +96,14 @@ typedef struct {
     int32_t fault_step;      /* test hook: -1 (off), or the decode step (within one lf_decode call)
                                 at which layer 0's QKV stage withholds its readiness signal, so
                                 that the consumers' bounded waits run out */
+    /* Sliding-window attention (shivam2003.com, model table and "Why GQA and
+     * sliding windows": windowed layers bound the KV cache each token reads).
+     * NULL: every layer attends to the whole cache.  Otherwise a HOST array
+     * of n_layers windows, copied by lf_create: layer_window[l] = W > 0 makes
+     * the query at position p of layer l attend to positions
+     * max(0, p-W+1) .. p only; 0 keeps the whole cache.  The KV cache still
+     * holds every position (max_seq). */
+    const int32_t *layer_window;
 } lf_config;
 
 /* Device pointers to the caller's FP16 weights (row-major, stacked over

@@ -37,7 +37,8 @@ class lf_config(C.Structure):
     _fields_ = [("n_layers", C.c_int32), ("d_model", C.c_int32), ("n_heads", C.c_int32),
                 ("n_kv_heads", C.c_int32), ("head_dim", C.c_int32), ("ffn_dim", C.c_int32), ("vocab", C.c_int32),
                 ("max_seq", C.c_int32), ("rope_theta", C.c_float), ("rms_eps", C.c_float),
-                ("wait_timeout_ns", C.c_int64), ("n_ctas", C.c_int32), ("fault_step", C.c_int32)]
+                ("wait_timeout_ns", C.c_int64), ("n_ctas", C.c_int32), ("fault_step", C.c_int32),
+                ("layer_window", C.POINTER(C.c_int32))]
 
 
 WEIGHT_FIELDS = ("embed", "attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down",
@@ -117,6 +118,16 @@ def _dptr(t) -> int:
     return 0 if t is None else int(t.data_ptr())
 
 
+def _windows(model, layer_window):
+    """lf_config.layer_window: NULL, or a host int32 array of one window per layer."""
+    if layer_window is None:
+        return None
+    vals = [int(v) for v in layer_window]
+    if len(vals) != model.n_layers:
+        raise ValueError("layer_window needs one entry per layer")
+    return (C.c_int32 * len(vals))(*vals)
+
+
 class Decoder:
     """One decoder on the current CUDA device.
 
@@ -126,7 +137,7 @@ class Decoder:
     """
 
     def __init__(self, model, weights: dict, max_seq: int, n_ctas: int = 0, wait_timeout_ns: int = 0,
-                 fault_step: int = -1):
+                 fault_step: int = -1, layer_window=None):
         import torch
         self.model = model
         self.max_seq = int(max_seq)
@@ -138,7 +149,7 @@ class Decoder:
         self._keep = {n: weights[n] for n in ("embed", "attn_norm", "ffn_norm", "final_norm")}
         cfg = lf_config(model.n_layers, model.d_model, model.n_heads, model.n_kv_heads, model.head_dim,
                         model.ffn_dim, model.vocab, self.max_seq, model.rope_theta, model.rms_eps,
-                        int(wait_timeout_ns), int(n_ctas), int(fault_step))
+                        int(wait_timeout_ns), int(n_ctas), int(fault_step), _windows(model, layer_window))
         w = lf_weights(*[_dptr(weights[n]) for n in WEIGHT_FIELDS])
         h = C.c_void_p()
         _check(lib().lf_create(C.byref(cfg), C.byref(w), C.byref(h)), "lf_create")

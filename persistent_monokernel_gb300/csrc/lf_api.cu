@@ -17,7 +17,7 @@ extern "C" cudaError_t lfk_set_smem(int smem_bytes);
 extern "C" cudaError_t lfk_launch_monokernel(const lfk::Params *p, int smem_bytes, cudaStream_t stream,
                                              int cooperative);
 extern "C" cudaError_t lfk_occupancy(int smem_bytes, int *blocks_per_sm);
-extern "C" unsigned lfk_smem_bytes(int ring_bytes, int a_floats, int b_slots, int d, int lm_rows_max);
+extern "C" unsigned lfk_smem_bytes(int ring_bytes, int a_floats, int b_slots, int d, int lm_rows_max, int L);
 extern "C" cudaError_t lfk_launch_repack(lfk::Geo g, int P, const lfk::CtaPlan *plans, const void *wq,
                                          const void *wk, const void *wv, const void *wo, const void *wg,
                                          const void *wu, const void *wd, const void *head, void *dst,
@@ -53,6 +53,7 @@ struct lf_handle {
     __half *kc = nullptr, *vc = nullptr;
     float2 *rope = nullptr;
     float *qbuf = nullptr, *attn = nullptr, *xattn = nullptr, *hbuf = nullptr, *xout = nullptr, *apart = nullptr;
+    int *win = nullptr;            // [L] attention window per layer, or null (every layer: the whole cache)
     int max_split = 1;
     unsigned *counters = nullptr;  // one allocation: slice counters, attn_done, lm_done, tok_cnt, gbar
     size_t counters_bytes = 0;
@@ -89,7 +90,7 @@ cudaError_t dalloc(T **p, size_t count)
 void free_all(lf_handle *h)
 {
     void *ptrs[] = {h->d_plans, h->wstream, h->kc, h->vc, h->rope, h->qbuf, h->attn, h->xattn, h->hbuf,
-                    h->xout, h->apart, h->counters, h->lm_part, h->tok_buf, h->tok_seq, h->status,
+                    h->xout, h->apart, h->win, h->counters, h->lm_part, h->tok_buf, h->tok_seq, h->status,
                     h->stage_in, h->stage_out, h->trace};
     for (void *p : ptrs)
         if (p) cudaFree(p);
@@ -115,6 +116,9 @@ lf_status validate_config(const lf_config &c)
     if (c.d_model % lfk::KC || Q % lfk::KC || c.ffn_dim % lfk::KC) return LF_ERR_NOT_SUPPORTED;
     const long long most = (long long)lfk::MAX_SLICES * lfk::KC;
     if (c.d_model > most || Q > most || c.ffn_dim > most) return LF_ERR_NOT_SUPPORTED;
+    if (c.layer_window)
+        for (int l = 0; l < c.n_layers; ++l)
+            if (c.layer_window[l] < 0) return LF_ERR_INVALID_ARG;
     return LF_OK;
 }
 
@@ -151,6 +155,7 @@ lfk::Params base_params(lf_handle *h)
     p.hbuf = h->hbuf;
     p.xout = h->xout;
     p.apart = h->apart;
+    p.win = h->win;
     p.max_split = h->max_split;
     p.sig = h->sig;
     p.attn_done = h->attn_done;
@@ -257,6 +262,7 @@ lf_status lf_create(const lf_config *cfg, const lf_weights *w, lf_handle **out)
     lf_handle *h = new (std::nothrow) lf_handle();
     if (!h) return LF_ERR_OUT_OF_MEMORY;
     h->cfg = *cfg;
+    h->cfg.layer_window = nullptr;   // the caller's array is copied to the device below
     h->l2_prefetch_bytes = l2_prefetch_bytes_from_env();
     h->l2_prefetch_last = std::getenv("LF_L2_PREFETCH_LAST") ? 1 : 0;
     lfk::Geo &g = h->g;
@@ -317,15 +323,15 @@ lf_status lf_create(const lf_config *cfg, const lf_weights *w, lf_handle **out)
     // ---- shared memory: everything but the ring, then the largest ring that fits
     h->max_split = std::max(1, P / g.Hkv);
     lfk::act_sizes(g, h->plans.data(), P, h->max_split, h->a_floats, h->b_slots);
-    const unsigned rest = lfk_smem_bytes(0, h->a_floats, h->b_slots, g.d, lm_rows_max);
+    const unsigned rest = lfk_smem_bytes(0, h->a_floats, h->b_slots, g.d, lm_rows_max, g.L);
     if ((int)rest + 2 * lfk::ATT_CHUNK_BYTES > optin) {
         delete h;
         return LF_ERR_NOT_SUPPORTED;
     }
     h->ring_bytes = (int)(((unsigned)optin - rest) / 1024u * 1024u);
-    while ((int)lfk_smem_bytes(h->ring_bytes, h->a_floats, h->b_slots, g.d, lm_rows_max) > optin)
+    while ((int)lfk_smem_bytes(h->ring_bytes, h->a_floats, h->b_slots, g.d, lm_rows_max, g.L) > optin)
         h->ring_bytes -= 1024;
-    h->smem_bytes = (int)lfk_smem_bytes(h->ring_bytes, h->a_floats, h->b_slots, g.d, lm_rows_max);
+    h->smem_bytes = (int)lfk_smem_bytes(h->ring_bytes, h->a_floats, h->b_slots, g.d, lm_rows_max, g.L);
     if (h->ring_bytes < 2 * lfk::ATT_CHUNK_BYTES) {
         delete h;
         return LF_ERR_NOT_SUPPORTED;
@@ -363,6 +369,18 @@ lf_status lf_create(const lf_config *cfg, const lf_weights *w, lf_handle **out)
         free_all(h);
         delete h;
         return from_cuda(e);
+    }
+    bool windowed = false;
+    if (cfg->layer_window)
+        for (int l = 0; l < g.L; ++l) windowed = windowed || cfg->layer_window[l] > 0;
+    if (windowed) {
+        e = dalloc(&h->win, (size_t)g.L);
+        if (e == cudaSuccess) e = cudaMemcpy(h->win, cfg->layer_window, sizeof(int) * g.L, cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) {
+            free_all(h);
+            delete h;
+            return from_cuda(e);
+        }
     }
     h->sig = h->counters;
     h->attn_done = h->counters + sig_words;

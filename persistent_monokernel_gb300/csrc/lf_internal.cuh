@@ -101,6 +101,9 @@ __host__ __device__ inline int attn_unit_first(int b, int l, int U, int P)
     return (int)r;
 }
 __host__ __device__ inline int attn_sub_positions(int hd) { return ATT_CHUNK_BYTES / (4 * hd); }
+// First position the query at `pos` attends to in a layer of window W
+// (W > 0: the W most recent positions, itself included; 0: the whole cache).
+__host__ __device__ inline int attn_first_pos(int pos, int W) { return (W > 0 && pos + 1 > W) ? pos + 1 - W : 0; }
 
 // Per-CTA plan: unit ranges of the five GEMV stages and the byte offsets of
 // this CTA's weight stream.  The stream of CTA b is laid out as
@@ -183,6 +186,7 @@ struct Params {
     float *hbuf;                 // [L][F]   SiLU(gate) * up
     float *xout;                 // [L][d]   residual after FFN
     float *apart;                // [L][Hq][max_split][hd + 2]  (o[hd], m, l) per piece
+    const int *win;              // [L] attention window per layer in positions (0: whole cache), or null
     int max_split;
     unsigned *sig;               // [L][sig_layout().per_layer] readiness counters
     unsigned *attn_done;         // [L][Hkv] pieces of each KV head that have published

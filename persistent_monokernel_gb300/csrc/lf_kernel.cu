@@ -43,12 +43,12 @@ namespace lfk {
 
 struct SmemLayout {
     unsigned res, full, empty, chunk_end, afull, bfull, gfull, brel, red, hist, misc, plan;
-    unsigned ring, acta, actb, gain, lmkeys, total;
+    unsigned ring, acta, actb, gain, lmkeys, win, total;
 };
 
 __host__ __device__ inline unsigned align_up(unsigned x, unsigned a) { return (x + a - 1) / a * a; }
 
-__host__ __device__ inline SmemLayout smem_layout(int ring_bytes, int a_floats, int b_slots, int d, int lm_rows_max)
+__host__ __device__ inline SmemLayout smem_layout(int ring_bytes, int a_floats, int b_slots, int d, int lm_rows_max, int L)
 {
     // Fixed-size parts first: their offsets are compile-time constants, so
     // their addresses cost no registers; the ring, the two activation buffers,
@@ -73,6 +73,7 @@ __host__ __device__ inline SmemLayout smem_layout(int ring_bytes, int a_floats, 
     s.actb = o;      o = align_up(o + 4u * KC * (unsigned)b_slots, 128);
     s.gain = o;      o = align_up(o + 2u * (unsigned)d, 128);
     s.lmkeys = o;    o = align_up(o + 8u * (unsigned)lm_rows_max, 128);
+    s.win = o;       o = align_up(o + 4u * (unsigned)L, 128);   // attention window of each layer
     // the GEMV reads whole 8-row blocks: keep 7 rows of readable bytes after the ring
     const unsigned slack_end = s.ring + (unsigned)ring_bytes + 7u * KC_BYTES;
     s.total = o > slack_end ? o : align_up(slack_end, 128);
@@ -102,6 +103,7 @@ struct Ctx {
     float *red;
     unsigned *hist;
     unsigned *misc;
+    const int *win;   // [L] attention window of each layer (0: whole cache), in shared memory
     int b;            // CTA index
     int tid, warp, lane;
 };
@@ -1020,7 +1022,8 @@ __device__ void reducer(const Ctx &c)
 // ---------------------------------------------------------------- attention
 
 // One split-KV piece: positions [j0, j1) of KV head gkv for the G query heads
-// that share it.  Warp w owns query head w mod G and every (8/G)-th slab of 32
+// that share it (j0 = w0 + cpiece * per, where w0 is the first position the
+// layer attends to: 0, or pos + 1 - W in a layer with a sliding window of W).  Warp w owns query head w mod G and every (8/G)-th slab of 32
 // positions, and keeps an online-softmax state (running max m, sum l, output
 // o) for it.  Per slab, lanes first take one position each and compute its full
 // score q . k over the head dimension (element index rotated by the lane, so
@@ -1029,7 +1032,7 @@ __device__ void reducer(const Ctx &c)
 // Positions < pos come from the ring; position pos (written by this step's QKV
 // stage) is staged from the cache.  The warps of a head are merged at the end.
 template <int HD>
-__device__ __forceinline__ bool attn_piece(const Ctx &c, ConsRing &rc, int l, int step, int gkv, int cpiece,
+__device__ __forceinline__ bool attn_piece(const Ctx &c, ConsRing &rc, int l, int step, int gkv, int cpiece, int w0,
                                         const AttnSplit &sp, bool ab)
 {
     constexpr int E = HD / 32;
@@ -1041,9 +1044,8 @@ __device__ __forceinline__ bool attn_piece(const Ctx &c, ConsRing &rc, int l, in
     const int G = g.group;                              // divides NCW
     const int WPH = NCW / G;                            // warps per head
     const int pos = p.pos0 + step;
-    const int ctx = pos + 1;
-    const int j0 = cpiece * sp.per;
-    const int j1 = min(j0 + sp.per, ctx);
+    const int j0 = w0 + cpiece * sp.per;
+    const int j1 = min(j0 + sp.per, pos + 1);
     const int jr = min(j1, pos);
     const float scale = 1.0f / sqrtf((float)HD);
     const int hq0 = gkv * G;
@@ -1436,13 +1438,14 @@ __device__ void consumer(const Ctx &c)
                     if (cons_wait(c, p.gbar, (idx + 1u) * (unsigned)p.P, 2, l, step, ab)) return;
                 }
                 trace_mark(c, step, k, TR_READY);
-                const int ctx = p.pos0 + step + 1;
-                const AttnSplit sp = attn_split(ctx, p.P, g.Hkv, p.attn_min_len);
+                const int pos = p.pos0 + step;
+                const int w0 = attn_first_pos(pos, c.win[l]);    // first attended position
+                const AttnSplit sp = attn_split(pos + 1 - w0, p.P, g.Hkv, p.attn_min_len);
                 const int U = g.Hkv * sp.n_split;
                 for (int u = attn_unit_first(c.b, l, U, p.P); u < U; u += p.P) {
                     const int gkv = u / sp.n_split, cp = u % sp.n_split;
-                    const bool stop = (g.hd == 128) ? attn_piece<128>(c, rc, l, step, gkv, cp, sp, ab)
-                                                    : attn_piece<64>(c, rc, l, step, gkv, cp, sp, ab);
+                    const bool stop = (g.hd == 128) ? attn_piece<128>(c, rc, l, step, gkv, cp, w0, sp, ab)
+                                                    : attn_piece<64>(c, rc, l, step, gkv, cp, w0, sp, ab);
                     if (stop) return;
                 }
                 // hand the scratch in buffer A back to the loader
@@ -1595,12 +1598,13 @@ __device__ void producer(const Ctx &c, const RepackSrc *w)
                 trace_mark_producer(c, step, k, TR_P1);
                 continue;
             }
-            const AttnSplit sp = attn_split(pos + 1, p.P, g.Hkv, p.attn_min_len);
+            const int w0 = attn_first_pos(pos, c.win[l]);
+            const AttnSplit sp = attn_split(pos + 1 - w0, p.P, g.Hkv, p.attn_min_len);
             const int U = g.Hkv * sp.n_split;
             const int S = attn_sub_positions(g.hd);
             for (int u = attn_unit_first(c.b, l, U, p.P); u < U && ok; u += p.P) {
                 const int gkv = u / sp.n_split, cp = u % sp.n_split;
-                const int j0 = cp * sp.per;
+                const int j0 = w0 + cp * sp.per;
                 const int jr = min(min(j0 + sp.per, pos + 1), pos);
                 if (jr > j0 && step > 0) {
                     // position pos - 1 of step > 0 was written by the previous
@@ -1630,7 +1634,7 @@ template <bool kDirect>
 __device__ __forceinline__ void monokernel_body(const Params &p, const RepackSrc *w)
 {
     extern __shared__ __align__(128) uint8_t smem[];
-    const SmemLayout L = smem_layout(p.ring_bytes, p.a_floats, p.b_slots, p.g.d, p.lm_rows_max);
+    const SmemLayout L = smem_layout(p.ring_bytes, p.a_floats, p.b_slots, p.g.d, p.lm_rows_max, p.g.L);
     Ctx c;
     c.p = &p;
     c.ring = smem + L.ring;
@@ -1649,6 +1653,11 @@ __device__ __forceinline__ void monokernel_body(const Params &p, const RepackSrc
     c.red = reinterpret_cast<float *>(smem + L.red);
     c.hist = reinterpret_cast<unsigned *>(smem + L.hist);
     c.misc = reinterpret_cast<unsigned *>(smem + L.misc);
+    {
+        int *win = reinterpret_cast<int *>(smem + L.win);
+        for (int i = threadIdx.x; i < p.g.L; i += blockDim.x) win[i] = p.win ? p.win[i] : 0;
+        c.win = win;
+    }
     CtaPlan *plan_s = reinterpret_cast<CtaPlan *>(smem + L.plan);
     c.plan = plan_s;
     c.b = blockIdx.x;
@@ -1764,9 +1773,9 @@ extern "C" cudaError_t lfk_occupancy(int smem_bytes, int *blocks_per_sm)
                                                         (size_t)smem_bytes);
 }
 
-extern "C" unsigned lfk_smem_bytes(int ring_bytes, int a_floats, int b_slots, int d, int lm_rows_max)
+extern "C" unsigned lfk_smem_bytes(int ring_bytes, int a_floats, int b_slots, int d, int lm_rows_max, int L)
 {
-    return lfk::smem_layout(ring_bytes, a_floats, b_slots, d, lm_rows_max).total;
+    return lfk::smem_layout(ring_bytes, a_floats, b_slots, d, lm_rows_max, L).total;
 }
 
 extern "C" cudaError_t lfk_launch_repack(lfk::Geo g, int P, const lfk::CtaPlan *plans, const void *wq, const void *wk,

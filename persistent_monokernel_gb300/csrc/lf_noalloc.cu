@@ -26,7 +26,7 @@
 #include "../../include/lf.h"
 #include "lf_internal.cuh"
 
-extern "C" unsigned lfk_smem_bytes(int ring_bytes, int a_floats, int b_slots, int d, int lm_rows_max);
+extern "C" unsigned lfk_smem_bytes(int ring_bytes, int a_floats, int b_slots, int d, int lm_rows_max, int L);
 extern "C" cudaError_t lfk_set_smem_direct(int smem_bytes);
 extern "C" cudaError_t lfk_launch_monokernel_direct(const lfk::Params *p, const void *wq, const void *wk,
                                                     const void *wv, const void *wo, const void *wg, const void *wu,
@@ -81,6 +81,9 @@ extern "C" LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_w
     if (cfg->d_model > most || (long long)cfg->n_heads * cfg->head_dim > most || cfg->ffn_dim > most)
         return LF_ERR_NOT_SUPPORTED;
     if (sp->top_k < 0 || sp->top_k > LF_MAX_TOP_K) return LF_ERR_NOT_SUPPORTED;
+    if (cfg->layer_window)
+        for (int l = 0; l < cfg->n_layers; ++l)
+            if (cfg->layer_window[l] < 0) return LF_ERR_INVALID_ARG;
     if ((long long)n_prompt + n_steps > cfg->max_seq) return LF_ERR_CAPACITY;
 
     lfk::Geo g;
@@ -121,11 +124,11 @@ extern "C" LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_w
     const int max_split = P / g.Hkv > 1 ? P / g.Hkv : 1;
     int a_floats = 0, b_slots = 0;
     lfk::act_sizes(g, h_plans, P, max_split, a_floats, b_slots);
-    const unsigned rest = lfk_smem_bytes(0, a_floats, b_slots, g.d, lm_rows_max);
+    const unsigned rest = lfk_smem_bytes(0, a_floats, b_slots, g.d, lm_rows_max, g.L);
     if ((int)rest + 2 * lfk::ATT_CHUNK_BYTES > optin) return LF_ERR_NOT_SUPPORTED;
     int ring = (int)(((unsigned)optin - rest) / 1024u * 1024u);
-    while ((int)lfk_smem_bytes(ring, a_floats, b_slots, g.d, lm_rows_max) > optin) ring -= 1024;
-    const int smem = (int)lfk_smem_bytes(ring, a_floats, b_slots, g.d, lm_rows_max);
+    while ((int)lfk_smem_bytes(ring, a_floats, b_slots, g.d, lm_rows_max, g.L) > optin) ring -= 1024;
+    const int smem = (int)lfk_smem_bytes(ring, a_floats, b_slots, g.d, lm_rows_max, g.L);
 
     // ---- scratch layout inside the static array
     const size_t kv_elems = (size_t)g.L * g.Hkv * (size_t)g.max_seq * g.hd;
@@ -145,6 +148,10 @@ extern "C" LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_w
     const size_t o_lm = carve(off, 8ull * P * lfk::MAX_TOPK);
     const size_t o_tok = carve(off, 4ull * (1 + g.max_seq));
     const size_t o_status = carve(off, 4 * 8);
+    bool windowed = false;
+    if (cfg->layer_window)
+        for (int l = 0; l < g.L; ++l) windowed = windowed || cfg->layer_window[l] > 0;
+    const size_t o_win = windowed ? carve(off, sizeof(int) * g.L) : 0;
     if (off > (size_t)LF_NOALLOC_SCRATCH_BYTES) return LF_ERR_CAPACITY;
 
     // ---- per-device set-up: device address of the scratch array, kernel smem limit
@@ -171,6 +178,8 @@ extern "C" LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_w
     if (e == cudaSuccess) e = cudaMemcpyAsync(base + o_rope, h_rope, sizeof(float2) * rope_elems, cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(base + o_cnt, 0, 4 * cnt_words, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(base + o_status, 0, 4 * 8, st);
+    if (e == cudaSuccess && windowed)
+        e = cudaMemcpyAsync(base + o_win, cfg->layer_window, sizeof(int) * g.L, cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) return LF_ERR_CUDA;
 
     lfk::Params p;
@@ -192,6 +201,7 @@ extern "C" LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_w
     p.hbuf = reinterpret_cast<float *>(base + o_h);
     p.xout = reinterpret_cast<float *>(base + o_xout);
     p.apart = reinterpret_cast<float *>(base + o_apart);
+    p.win = windowed ? reinterpret_cast<const int *>(base + o_win) : nullptr;
     p.max_split = max_split;
     unsigned *cnt = reinterpret_cast<unsigned *>(base + o_cnt);
     p.sig = cnt;

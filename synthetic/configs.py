@@ -64,6 +64,8 @@ class Workload:
     temperature: float = 0.0
     top_k: int = 0
     sample_seed: int = 0
+    # None, or one attention window per layer in positions (0 = the whole cache)
+    layer_window: tuple | None = None
 
     @property
     def max_seq(self) -> int:
@@ -71,10 +73,17 @@ class Workload:
 
     def bytes_per_step(self, pos: int) -> int:
         """Algorithmic HBM bytes of the decode step whose input token sits at
-        position `pos`: weights, the KV read over ctx = pos + 1 positions and
-        the KV write of one position."""
+        position `pos`: weights, the KV read of every layer (ctx = pos + 1
+        positions, or the layer's window if shorter) and the KV write of one
+        position."""
         m = self.model
-        return m.weight_bytes_per_token() + (pos + 1) * m.kv_bytes_per_position() + m.kv_bytes_per_position()
+        per_layer = m.kv_bytes_per_position() // m.n_layers
+        ctx = pos + 1
+        if self.layer_window is None:
+            kv_read = ctx * m.kv_bytes_per_position()
+        else:
+            kv_read = sum(min(ctx, w) if w > 0 else ctx for w in self.layer_window) * per_layer
+        return m.weight_bytes_per_token() + kv_read + m.kv_bytes_per_position()
 
     def decode_bytes(self, first_pos: int, n_steps: int) -> int:
         return sum(self.bytes_per_step(first_pos + i) for i in range(n_steps))
@@ -92,6 +101,11 @@ WORKLOADS = {
     "small": Workload("small", MODELS["small"], 1, 1001, 128, 256),
     "2.3b": Workload("2.3b", MODELS["2.3b"], 2, 1002, 512, 1024),
     "2.3b-32k": Workload("2.3b-32k", MODELS["2.3b"], 2, 1003, 32768, 256),
+    # the same at 32k context with sliding-window attention in two of every
+    # three layers (the pages' LaneFormer: 10 of 15 layers), window 4,096
+    # positions (its stated context length; the pages give no window size)
+    "2.3b-32k-swa": Workload("2.3b-32k-swa", MODELS["2.3b"], 2, 1003, 32768, 256,
+                             layer_window=tuple(4096 if l % 3 != 2 else 0 for l in range(25))),
     "8b": Workload("8b", MODELS["8b"], 3, 1004, 2048, 512, temperature=0.8, top_k=50, sample_seed=1234),
 }
 

@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(pm):
 
 
 def test_abi_version_and_error_strings(pm):
-    assert pm.lib().lf_abi_version() == 1
+    assert pm.lib().lf_abi_version() == 2
     for code, name in pm.STATUS_NAMES.items():
         assert pm.error_string(code).startswith(name)
 
@@ -64,6 +64,10 @@ def test_create_rejects_bad_arguments_before_touching_the_gpu(pm):
     # more than 64 column groups of 256 in one vector
     cfg = pm.lf_config(**{**good, "ffn_dim": 256 * 65})
     assert L.lf_create(C.byref(cfg), C.byref(w), C.byref(h)) == 7
+    # a negative sliding window
+    win = (C.c_int32 * 2)(16, -1)
+    cfg = pm.lf_config(**{**good, "layer_window": win})
+    assert L.lf_create(C.byref(cfg), C.byref(w), C.byref(h)) == 1
 
 
 def test_calls_on_a_null_handle_are_rejected(pm):

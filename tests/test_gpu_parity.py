@@ -23,7 +23,7 @@ def _setup(pm, cfg, wseed, max_seq, gains="ones", **kw):
     wg = make_weights(cfg, wseed, device="cuda", gains=gains)
     wc = {k: v.cpu() for k, v in wg.items()}
     dec = pm.Decoder(cfg, wg, max_seq, **kw)
-    orc = oracle.OracleDecoder(cfg, wc, max_seq)
+    orc = oracle.OracleDecoder(cfg, wc, max_seq, layer_window=kw.get("layer_window"))
     return dec, orc, wg
 
 
@@ -265,3 +265,38 @@ def test_full_size_8b_sampled_parity(pm):
                                 seed=wl.sample_seed)
     compare_logits(lg, ref)
     check_tokens(toks, ref, wl.temperature, wl.top_k, wl.sample_seed, 7)
+
+
+# ---- sliding-window attention (shivam2003.com, "Why GQA and sliding windows")
+
+@pytest.mark.parametrize("cfg,window,prompt_len,steps", [
+    # MHA, windows below, at and above the context, one window not a multiple of the 32-position sub-block
+    (MODELS["tiny"], [37, 0], 64, 24),
+    # GQA 16/4 x 64, windowed and full layers interleaved (the pages: 10 of 15 layers windowed)
+    (MODELS["small"].with_(n_layers=6), [100, 100, 0, 100, 100, 0], 160, 24),
+    # hd 128, the window spans several split-KV pieces and moves across them step by step
+    (ModelConfig("gqa128w", 2, 512, 8, 2, 128, 1024, 3000), [700, 1], 900, 40),
+])
+def test_sliding_window_parity(pm, cfg, window, prompt_len, steps):
+    dec, orc, _ = _setup(pm, cfg, 31, prompt_len + steps + 1, gains="random", layer_window=window)
+    prompt = make_prompt(cfg.vocab, prompt_len, 32)
+    toks, lg, ref = _forced_run(pm, dec, orc, cfg, prompt, steps, 33)
+    compare_logits(lg, ref)
+    check_tokens(toks, ref, 0.0, 0, 0, prompt_len - 1)
+
+
+def test_window_covering_the_context_is_bitwise_full_attention(pm):
+    wl = WORKLOADS["tiny"]
+    cfg = wl.model
+    wg = make_weights(cfg, wl.weight_seed, device="cuda")
+    prompt = make_prompt(cfg.vocab, wl.prompt_len, wl.prompt_seed).cuda()
+    out = []
+    for win in (None, [wl.max_seq, wl.max_seq + 7]):
+        dec = pm.Decoder(cfg, wg, wl.max_seq, layer_window=win)
+        dec.prefill(prompt)
+        lg = torch.empty((16, cfg.vocab), dtype=torch.float32, device="cuda")
+        toks = dec.decode(16, debug_logits=lg)
+        assert dec.sync() == 0
+        out.append((toks.cpu(), lg.cpu()))
+        dec.close()
+    assert torch.equal(out[0][0], out[1][0]) and torch.equal(out[0][1], out[1][1])

@@ -29,9 +29,10 @@ def pm():
     return pm
 
 
-def _cfg(pm, m, max_seq):
+def _cfg(pm, m, max_seq, window=None):
+    win = (C.c_int32 * m.n_layers)(*window) if window is not None else None
     return pm.lf_config(m.n_layers, m.d_model, m.n_heads, m.n_kv_heads, m.head_dim, m.ffn_dim, m.vocab, max_seq,
-                        m.rope_theta, m.rms_eps, 0, 0, -1)
+                        m.rope_theta, m.rms_eps, 0, 0, -1, win)
 
 
 def _noalloc(pm, cfg, weights, prompt, n_steps, T, k, seed):
@@ -46,8 +47,8 @@ def _noalloc(pm, cfg, weights, prompt, n_steps, T, k, seed):
     return out.cpu().numpy(), lg.cpu().numpy()
 
 
-def _handle_path(pm, model, weights, max_seq, prompt, n_steps, T, k, seed):
-    dec = pm.Decoder(model, weights, max_seq)
+def _handle_path(pm, model, weights, max_seq, prompt, n_steps, T, k, seed, window=None):
+    dec = pm.Decoder(model, weights, max_seq, layer_window=window)
     dec.prefill(prompt)
     lg = torch.empty((n_steps, model.vocab), dtype=torch.float32, device="cuda")
     toks = dec.decode(n_steps, temperature=T, top_k=k, seed=seed, debug_logits=lg)
@@ -69,6 +70,19 @@ def test_noalloc_matches_the_handle_path_on_two_calls_in_a_row(pm):
         compare_logits(lg, ref_lg)
         check_tokens(toks, ref_lg, T, k, seed, prompt.numel() - 1)
         assert np.all((toks >= 0) & (toks < m.vocab))
+
+
+def test_noalloc_with_sliding_windows_matches_the_handle_path(pm):
+    wl = WORKLOADS["tiny"]
+    m = wl.model
+    weights = make_weights(m, wl.weight_seed, device="cuda")
+    window = [29, 0]
+    cfg = _cfg(pm, m, wl.max_seq, window)
+    prompt = make_prompt(m.vocab, wl.prompt_len, wl.prompt_seed).cuda()
+    toks, lg = _noalloc(pm, cfg, weights, prompt, 24, 0.0, 0, 0)
+    ref_toks, ref_lg = _handle_path(pm, m, weights, wl.max_seq, prompt, 24, 0.0, 0, 0, window)
+    compare_logits(lg, ref_lg)
+    check_tokens(toks, ref_lg, 0.0, 0, 0, prompt.numel() - 1)
 
 
 def test_noalloc_rejects_requests_beyond_its_scratch(pm):
