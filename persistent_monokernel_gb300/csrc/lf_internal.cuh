@@ -101,6 +101,12 @@ __host__ __device__ inline int attn_unit_first(int b, int l, int U, int P)
     return (int)r;
 }
 __host__ __device__ inline int attn_sub_positions(int hd) { return ATT_CHUNK_BYTES / (4 * hd); }
+// KV-cache row layout: element j of the row of position p sits at
+// kv_swz(p, j): its 16-byte group (8 FP16 values) j/8 is XOR-ed with p mod 8,
+// so that 8 consecutive positions' groups j/8 fall in 8 different shared-
+// memory bank quads once a block of rows is copied into the ring, and the
+// tensor-core fragment loads (ldmatrix, 8 rows x 16 bytes) are conflict-free.
+__host__ __device__ inline int kv_swz(int p, int j) { return ((((j >> 3) ^ (p & 7)) << 3) | (j & 7)); }
 // First position the query at `pos` attends to in a layer of window W
 // (W > 0: the W most recent positions, itself included; 0: the whole cache).
 __host__ __device__ inline int attn_first_pos(int pos, int W) { return (W > 0 && pos + 1 > W) ? pos + 1 - W : 0; }
@@ -135,11 +141,15 @@ __host__ __device__ inline SigLayout sig_layout(const Geo &g)
 }
 
 // Attention scratch (floats) in activation buffer A: q of the group [G][hd],
-// the staged fresh K and V rows (hd floats' worth of FP16) and the eight warp
-// states [NCW][hd + 2]; or, in the combine, the (m, l) table [G][max_split].
+// the staged fresh K and V rows (hd floats' worth of FP16), the states that
+// half of the warps hand to the other half in one round of the merge (4 warps
+// x 8 x ceil(G/2) lanes x hd/4 output values, then [4][8] running maxima and
+// sums) and the table of q's tensor-core fragments (hd/16 x 32 lanes x 4
+// words); or, in the combine, the (m, l) table [G][max_split].
 __host__ __device__ inline int attn_scratch_floats(const Geo &g, int max_split)
 {
-    const int piece = MAX_GROUP * g.hd + g.hd + NCW * (g.hd + 2);
+    const int piece = g.group * g.hd + g.hd + (NCW / 2) * 8 * ((g.group + 1) / 2) * (g.hd / 4) + 2 * (NCW / 2) * 8 +
+                      (g.hd / 16) * 32 * 4;
     const int combine = 2 * g.group * max_split;
     return piece > combine ? piece : combine;
 }

@@ -953,14 +953,14 @@ __device__ __forceinline__ bool reduce_stage(const Ctx &c, PipeState &ps, int s,
                     } else {
                         const int kvh = hh - g.Hq;
                         __half *kr = p.kc + (((size_t)l * g.Hkv + kvh) * g.max_seq + pos) * g.hd;
-                        kr[j] = __float2half_rn(r0);
-                        kr[j + half] = __float2half_rn(r1);
+                        kr[kv_swz(pos, j)] = __float2half_rn(r0);
+                        kr[kv_swz(pos, j + half)] = __float2half_rn(r1);
                     }
                 } else {
                     const int kvh = hh - g.Hq - g.Hkv;
                     __half *vr = p.vc + (((size_t)l * g.Hkv + kvh) * g.max_seq + pos) * g.hd;
-                    vr[j] = __float2half_rn(v0);
-                    vr[j + half] = __float2half_rn(v1);
+                    vr[kv_swz(pos, j)] = __float2half_rn(v0);
+                    vr[kv_swz(pos, j + half)] = __float2half_rn(v1);
                 }
                 if (hh >= g.Hq) fence_proxy_async_global();   // K/V rows are read by TMA in later steps
             } else if (s == ST_O) {
@@ -1023,38 +1023,81 @@ __device__ void reducer(const Ctx &c)
 
 // One split-KV piece: positions [j0, j1) of KV head gkv for the G query heads
 // that share it (j0 = w0 + cpiece * per, where w0 is the first position the
-// layer attends to: 0, or pos + 1 - W in a layer with a sliding window of W).  Warp w owns query head w mod G and every (8/G)-th slab of 32
-// positions, and keeps an online-softmax state (running max m, sum l, output
-// o) for it.  Per slab, lanes first take one position each and compute its full
-// score q . k over the head dimension (element index rotated by the lane, so
-// the 32 rows are read from distinct shared-memory banks), then take E = hd/32
-// output elements each and accumulate p_j * v_j with p_j broadcast by shuffle.
-// Positions < pos come from the ring; position pos (written by this step's QKV
-// stage) is staged from the cache.  The warps of a head are merged at the end.
+// layer attends to: 0, or pos + 1 - W in a layer with a sliding window of W).
+//
+// The piece is a small dense contraction on the tensor cores (warp-level
+// mma.sync m16n8k16, FP16 operands, FP32 accumulators).  The K/V rows sit in
+// the ring as [position][hd] FP16 rows (group-swizzled, kv_swz); the ring's
+// 16-position slabs go round-robin to the eight consumer warps.  Per slab a
+// warp forms the scores S[h][j] = q_h . k_j for all G heads at once (the G
+// query rows padded to 16, K^T as the B operand loaded with ldmatrix), runs an
+// online softmax per head in FP32 (running max m, running sum l), and adds
+// P V into its output, computed transposed, O^T[dim][h] = V^T P^T, so that
+// the score accumulators are the B operand of the second product without
+// leaving registers.  q and the probabilities p are each split into an FP16
+// head and an FP16 remainder (two products each), which keeps them accurate to
+// about 2^-22: the sums are FP32 like the rest of the path.  Position pos
+// (written by this step's QKV stage) is staged from the cache and added by one
+// warp with plain FP32 arithmetic.  The warps' states are merged pairwise
+// through shared memory.
+__device__ __forceinline__ void mma16816(float (&d)[4], unsigned a0, unsigned a1, unsigned a2, unsigned a3, unsigned b0,
+                                         unsigned b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+                 "{%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm_x4(unsigned (&r)[4], uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(unsigned (&r)[4], uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ unsigned pack_h2(__half lo, __half hi)
+{
+    return (unsigned)__half_as_ushort(lo) | ((unsigned)__half_as_ushort(hi) << 16);
+}
+// x = head + remainder, both FP16 (head = x rounded, remainder = the rest rounded)
+__device__ __forceinline__ void split_h(float x, __half &hd, __half &rm)
+{
+    hd = __float2half_rn(x);
+    rm = __float2half_rn(x - __half2float(hd));
+}
+
 template <int HD>
 __device__ __forceinline__ bool attn_piece(const Ctx &c, ConsRing &rc, int l, int step, int gkv, int cpiece, int w0,
                                         const AttnSplit &sp, bool ab)
 {
-    constexpr int E = HD / 32;
     constexpr int S = ATT_CHUNK_BYTES / (4 * HD);     // positions per ring sub-block
-    constexpr int SLABS = S / 32;                       // 32-position slabs per sub-block
+    constexpr int SPB = S / 16;                         // 16-position slabs per sub-block
+    constexpr int KS = HD / 16;                         // 16-wide k-steps over the head dimension
+    constexpr int ROW = HD * 2;                         // bytes of one K or V row
     constexpr int H2 = HD / 2;
     const Params &p = *c.p;
     const Geo &g = p.g;
-    const int G = g.group;                              // divides NCW
-    const int WPH = NCW / G;                            // warps per head
+    const int G = g.group;                              // query heads of the group (<= 8)
+    const int TT = (G + 1) / 2;                         // lanes t < TT hold output columns of real heads
     const int pos = p.pos0 + step;
     const int j0 = w0 + cpiece * sp.per;
     const int j1 = min(j0 + sp.per, pos + 1);
     const int jr = min(j1, pos);
     const float scale = 1.0f / sqrtf((float)HD);
     const int hq0 = gkv * G;
-    const int myh = c.warp % G, mys = c.warp / G;       // head, slab residue of this warp
+    const int gq = c.lane >> 2, tq = c.lane & 3;        // mma fragment coordinates of this lane
 
-    // ---- shared scratch: q [G][HD] FP32, fresh K and V rows [2][HD] FP16, warp states [NCW][HD + 2]
+    // ---- shared scratch: q [G][HD] FP32, fresh K and V rows [2][HD] FP16, merge states
     float *qs = c.acta;
     __half *fresh = reinterpret_cast<__half *>(qs + G * HD);
-    float *ws = qs + G * HD + HD;
+    float *ws = qs + G * HD + HD;                       // [4][8 * TT][HD / 4] outputs, then [4][8] m and l
+    float *wml = ws + (NCW / 2) * 8 * TT * (HD / 4);
+    uint4 *qfr = reinterpret_cast<uint4 *>(wml + 2 * (NCW / 2) * 8);   // [KS][32 lanes] q fragments
     const size_t kvbase = ((size_t)l * g.Hkv + gkv) * g.max_seq;
     const bool has_fresh = pos >= j0 && pos < j1;
     // ---- flag schedule: wait for the query heads of the group and the key and
@@ -1073,108 +1116,233 @@ __device__ __forceinline__ bool attn_piece(const Ctx &c, ConsRing &rc, int l, in
         for (int i = c.tid; i < G * HD / 4; i += NCT)
             reinterpret_cast<float4 *>(qs)[i] = __ldcg(reinterpret_cast<const float4 *>(qsrc) + i);
         if (has_fresh) {
+            // the cache row is group-swizzled: stage it in plain order
             const unsigned *ksrc = reinterpret_cast<const unsigned *>(p.kc + (kvbase + pos) * HD);
             const unsigned *vsrc = reinterpret_cast<const unsigned *>(p.vc + (kvbase + pos) * HD);
             for (int i = c.tid; i < H2; i += NCT) {
-                reinterpret_cast<unsigned *>(fresh)[i] = __ldcg(ksrc + i);
-                reinterpret_cast<unsigned *>(fresh)[H2 + i] = __ldcg(vsrc + i);
+                const int ph = kv_swz(pos, 2 * i) >> 1;
+                reinterpret_cast<unsigned *>(fresh)[i] = __ldcg(ksrc + ph);
+                reinterpret_cast<unsigned *>(fresh)[H2 + i] = __ldcg(vsrc + ph);
             }
         }
     }
     if (cons_sync_or(ab)) return true;
 
-    float m = -INFINITY, lsum = 0.f, o[E];
+    // ---- q fragments (A operand, rows = heads, padded to 16), one table for
+    // all warps: entry [k][lane] = (a0 head, a2 head, a0 remainder, a2
+    // remainder) of row lane/4, columns 16k + 2(lane%4) (+1) and 16k + 8 +
+    // 2(lane%4) (+1); rows >= G and rows 8..15 are zero
+    for (int i = c.tid; i < KS * 32; i += NCT) {
+        const int k = i / 32, gi = (i % 32) >> 2, ti = i & 3;
+        uint4 fr = make_uint4(0u, 0u, 0u, 0u);
+        if (gi < G) {
+            const float *qr = qs + gi * HD + 16 * k + 2 * ti;
+            __half h0, r0, h1, r1;
+            split_h(qr[0], h0, r0);
+            split_h(qr[1], h1, r1);
+            fr.x = pack_h2(h0, h1);
+            fr.z = pack_h2(r0, r1);
+            split_h(qr[8], h0, r0);
+            split_h(qr[9], h1, r1);
+            fr.y = pack_h2(h0, h1);
+            fr.w = pack_h2(r0, r1);
+        }
+        qfr[i] = fr;
+    }
+    if (cons_sync_or(ab)) return true;
+    const uint32_t qfa = smem_u32(qfr) + (uint32_t)c.lane * 16u;
+    // ---- per-warp state: m, l of head gq (lanes of row gq; l partial per lane)
+    // and O^T tiles: o[d][0..3] = O[2tq][16d+gq], O[2tq+1][16d+gq],
+    // O[2tq][16d+gq+8], O[2tq+1][16d+gq+8]
+    float m = -INFINITY, lsum = 0.f;
+    float o[KS][4];
 #pragma unroll
-    for (int e = 0; e < E; ++e) o[e] = 0.f;
-    const float2 *q2 = reinterpret_cast<const float2 *>(qs + myh * HD);
+    for (int d = 0; d < KS; ++d) o[d][0] = o[d][1] = o[d][2] = o[d][3] = 0.f;
+    // ldmatrix row addresses: lanes 8i..8i+7 address matrix i; row r = lane & 7
+    // of 8 positions (matrices 2, 3: positions 8..15) and 16-byte group
+    // 2k (+1 for matrices 1, 3)
+    const int lrow = (c.lane & 7) + ((c.lane >> 4) << 3);
+    const int lgrp = (c.lane >> 3) & 1;
 
-    // one slab of n (1..32) positions: K rows at Kb, V rows at Vb (row stride HD)
-    auto slab = [&](const __half *Kb, const __half *Vb, int n) {
-        float sc = -INFINITY;
-        if (c.lane < n) {
-            const __half2 *kr = reinterpret_cast<const __half2 *>(Kb + (size_t)c.lane * HD);
-            float d0 = 0.f, d1 = 0.f;
-#pragma unroll 8
-            for (int it = 0; it < H2; ++it) {
-                const int e2 = (it + c.lane) & (H2 - 1);
-                const float2 kv = __half22float2(kr[e2]);
-                const float2 qv = q2[e2];
-                d0 = fmaf(qv.x, kv.x, d0);
-                d1 = fmaf(qv.y, kv.y, d1);
-            }
-            sc = (d0 + d1) * scale;
-        }
-        const float mn = fmaxf(m, warp_max(sc));
-        const float corr = __expf(m - mn);           // 0 while m is -inf
-        const float pe = c.lane < n ? __expf(sc - mn) : 0.f;
-        lsum = fmaf(lsum, corr, warp_sum(pe));
+    // one 16-position slab: positions q0 .. q0+nv-1 (nv in 1..16), rows at Kb/Vb
+    auto slab = [&](uint32_t kb, uint32_t vb, int q0, int nv) {
+        const int prow = q0 + lrow;                     // position of the row this lane addresses
+        const uint32_t krow = kb + (uint32_t)lrow * ROW, vrow = vb + (uint32_t)lrow * ROW;
+        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};   // positions 0-7, 8-15
 #pragma unroll
-        for (int e = 0; e < E; ++e) o[e] *= corr;
-        for (int jj = 0; jj < n; ++jj) {
-            const float pj = __shfl_sync(0xffffffffu, pe, jj);
-            const __half *vr = Vb + (size_t)jj * HD + c.lane * E;
-            if constexpr (E == 4) {
-                const uint2 w = *reinterpret_cast<const uint2 *>(vr);
-                const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(&w.x));
-                const float2 b = __half22float2(*reinterpret_cast<const __half2 *>(&w.y));
-                o[0] = fmaf(pj, a.x, o[0]);
-                o[1] = fmaf(pj, a.y, o[1]);
-                o[2] = fmaf(pj, b.x, o[2]);
-                o[3] = fmaf(pj, b.y, o[3]);
-            } else {
-                const float2 a = __half22float2(*reinterpret_cast<const __half2 *>(vr));
-                o[0] = fmaf(pj, a.x, o[0]);
-                o[1] = fmaf(pj, a.y, o[1]);
-            }
+        for (int k = 0; k < KS; ++k) {
+            unsigned b[4];
+            ldsm_x4(b, krow + (uint32_t)((((2 * k + lgrp) ^ (prow & 7))) << 4));
+            const uint4 qa = lds_u4(qfa + (uint32_t)k * 512u);
+            mma16816(s0, qa.x, 0u, qa.y, 0u, b[0], b[1]);
+            mma16816(s0, qa.z, 0u, qa.w, 0u, b[0], b[1]);
+            mma16816(s1, qa.x, 0u, qa.y, 0u, b[2], b[3]);
+            mma16816(s1, qa.z, 0u, qa.w, 0u, b[2], b[3]);
         }
+        // scores of row gq at positions 2tq, 2tq+1, 8+2tq, 9+2tq; masked past nv
+        float sc[4] = {s0[0] * scale, s0[1] * scale, s1[0] * scale, s1[1] * scale};
+        const int cp[4] = {2 * tq, 2 * tq + 1, 8 + 2 * tq, 9 + 2 * tq};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if (cp[i] >= nv) sc[i] = -INFINITY;
+        float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float mn = fmaxf(m, mx);                  // finite: nv >= 1
+        const float corr = __expf(m - mn);              // 0 while m is -inf
+        float pr[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) pr[i] = __expf(sc[i] - mn);
+        lsum = fmaf(lsum, corr, (pr[0] + pr[1]) + (pr[2] + pr[3]));
         m = mn;
+        // the output columns of this lane are heads 2tq and 2tq+1
+        const float ca = __shfl_sync(0xffffffffu, corr, 8 * tq), cb = __shfl_sync(0xffffffffu, corr, 8 * tq + 4);
+        // P^T as the B operand: b0 = P[gq][2tq, 2tq+1], b1 = P[gq][8+2tq, 9+2tq]
+        __half ph[4], pr2[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) split_h(pr[i], ph[i], pr2[i]);
+        const unsigned pb0h = pack_h2(ph[0], ph[1]), pb1h = pack_h2(ph[2], ph[3]);
+        const unsigned pb0r = pack_h2(pr2[0], pr2[1]), pb1r = pack_h2(pr2[2], pr2[3]);
+        // V^T as the A operand (rows = dims, columns = positions), rows past nv zeroed
+        const unsigned keep0 = (2 * tq < nv ? 0x0000FFFFu : 0u) | (2 * tq + 1 < nv ? 0xFFFF0000u : 0u);
+        const unsigned keep1 = (8 + 2 * tq < nv ? 0x0000FFFFu : 0u) | (9 + 2 * tq < nv ? 0xFFFF0000u : 0u);
+#pragma unroll
+        for (int d = 0; d < KS; ++d) {
+            o[d][0] *= ca;
+            o[d][1] *= cb;
+            o[d][2] *= ca;
+            o[d][3] *= cb;
+            unsigned a[4];
+            ldsm_x4_t(a, vrow + (uint32_t)((((2 * d + lgrp) ^ (prow & 7))) << 4));
+            // matrices (transposed): 0 = positions 0-7 x dims 16d..16d+7, 1 = positions 0-7 x dims
+            // 16d+8.., 2 = positions 8-15 x dims 16d.., 3 = positions 8-15 x dims 16d+8.. --
+            // exactly the A fragments a0..a3 of V^T (rows gq / gq+8, columns 2tq / 8+2tq)
+            const unsigned va0 = a[0] & keep0, va1 = a[1] & keep0, va2 = a[2] & keep1, va3 = a[3] & keep1;
+            mma16816(o[d], va0, va1, va2, va3, pb0h, pb1h);
+            mma16816(o[d], va0, va1, va2, va3, pb0r, pb1r);
+        }
     };
 
     const int nring = jr > j0 ? ceil_div(jr - j0, S) : 0;
+    int nslab = 0;
     for (int blk = 0; blk < nring; ++blk) {
         const int nb = min(S, jr - (j0 + blk * S));
         const uint8_t *ch = rc.acquire(c, 4u * (unsigned)nb * HD, ab);
         if (ab) break;
-        const __half *Kb = reinterpret_cast<const __half *>(ch);
-        const __half *Vb = Kb + (size_t)nb * HD;
-#pragma unroll
-        for (int sl = 0; sl < SLABS; ++sl) {
-            const int gslab = blk * SLABS + sl;
-            const int n = min(32, nb - sl * 32);
-            if (n > 0 && gslab % WPH == mys) slab(Kb + (size_t)sl * 32 * HD, Vb + (size_t)sl * 32 * HD, n);
+        const uint32_t kb = smem_u32(ch), vb = kb + (uint32_t)nb * ROW;
+        const int q0 = j0 + blk * S;
+#pragma unroll 1
+        for (int sl = 0; sl < SPB; ++sl) {
+            const int nv = min(16, nb - 16 * sl);
+            if (nv > 0) {
+                if ((nslab + sl) % NCW == c.warp)
+                    slab(kb + (uint32_t)(16 * sl) * ROW, vb + (uint32_t)(16 * sl) * ROW, q0 + 16 * sl, nv);
+            }
         }
+        nslab += ceil_div(nb, 16);
         rc.release(c);
     }
-    if (!ab && has_fresh && (nring * SLABS) % WPH == mys) slab(fresh, fresh + HD, 1);
-    trace_mark(c, step, 5 * l + 1, TR_X1);
-
-    // ---- merge the warps of each head: ws[warp][HD + 2] = (o, m, l)
-    {
-        float *dst = ws + (size_t)c.warp * (HD + 2);
+    if (!ab && has_fresh && nslab % NCW == c.warp) {
+        // position pos: scores q_h . k for all heads (lane: HD/32 elements), then one online-softmax step
+        constexpr int EL = HD / 32;
+        float kf[EL], vlo[KS], vhi[KS];
 #pragma unroll
-        for (int e = 0; e < E; ++e) dst[c.lane * E + e] = o[e];
-        if (c.lane == 0) {
-            dst[HD] = m;
-            dst[HD + 1] = lsum;
+        for (int e = 0; e < EL; ++e) kf[e] = __half2float(fresh[c.lane * EL + e]);
+#pragma unroll
+        for (int d = 0; d < KS; ++d) {
+            vlo[d] = __half2float(fresh[HD + 16 * d + gq]);
+            vhi[d] = __half2float(fresh[HD + 16 * d + gq + 8]);
+        }
+        float sf = -INFINITY;                            // score of head gq
+        for (int h = 0; h < G; ++h) {
+            float dot = 0.f;
+#pragma unroll
+            for (int e = 0; e < EL; ++e) dot = fmaf(qs[h * HD + c.lane * EL + e], kf[e], dot);
+            dot = warp_sum(dot) * scale;
+            if (h == gq) sf = dot;
+        }
+        if (gq >= G) sf = 0.f;                           // padding rows (never written out)
+        const float mn = fmaxf(m, sf);
+        const float corr = __expf(m - mn), pf = __expf(sf - mn);
+        lsum = fmaf(lsum, corr, tq == 0 ? pf : 0.f);
+        m = mn;
+        const float ca = __shfl_sync(0xffffffffu, corr, 8 * tq), cb = __shfl_sync(0xffffffffu, corr, 8 * tq + 4);
+        const float pa = __shfl_sync(0xffffffffu, pf, 8 * tq), pb = __shfl_sync(0xffffffffu, pf, 8 * tq + 4);
+#pragma unroll
+        for (int d = 0; d < KS; ++d) {
+            o[d][0] = fmaf(o[d][0], ca, pa * vlo[d]);
+            o[d][1] = fmaf(o[d][1], cb, pb * vlo[d]);
+            o[d][2] = fmaf(o[d][2], ca, pa * vhi[d]);
+            o[d][3] = fmaf(o[d][3], cb, pb * vhi[d]);
         }
     }
-    if (cons_sync_or(ab)) return true;
-    for (int eidx = c.tid; eidx < G * HD; eidx += NCT) {
-        const int h = eidx / HD, i = eidx % HD;
-        float M = -INFINITY;
-        for (int k = 0; k < WPH; ++k) M = fmaxf(M, ws[(size_t)(h + k * G) * (HD + 2) + HD]);
-        float num = 0.f, den = 0.f;
-        for (int k = 0; k < WPH; ++k) {
-            const float *src = ws + (size_t)(h + k * G) * (HD + 2);
-            const float wgt = (src[HD] == -INFINITY) ? 0.f : __expf(src[HD] - M);
-            num = fmaf(wgt, src[i], num);
-            den = fmaf(wgt, src[HD + 1], den);
+    trace_mark(c, step, 5 * l + 1, TR_X1);
+    lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
+    lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
+
+    // ---- merge the warps pairwise (warp w + st into warp w, st = 4, 2, 1):
+    // state = (m, l) per head and the O^T tiles of the lanes t < TT
+    for (int st = NCW / 2; st >= 1; st >>= 1) {
+        const bool sender = c.warp >= st && c.warp < 2 * st, taker = c.warp < st;
+        const int slot = sender ? c.warp - st : c.warp;
+        if (sender) {
+            if (tq < TT) {
+                float *dst = ws + ((size_t)slot * 8 * TT + gq * TT + tq) * (HD / 4);
+#pragma unroll
+                for (int d = 0; d < KS; ++d)
+                    reinterpret_cast<float4 *>(dst)[d] = make_float4(o[d][0], o[d][1], o[d][2], o[d][3]);
+            }
+            if (tq == 0) {
+                wml[slot * 16 + gq] = m;
+                wml[slot * 16 + 8 + gq] = lsum;
+            }
         }
-        float *dst = p.apart + (((size_t)l * g.Hq + hq0 + h) * p.max_split + cpiece) * (HD + 2);
-        dst[i] = num;
-        if (i == 0) {
-            dst[HD] = M;
-            dst[HD + 1] = den;
+        if (cons_sync_or(ab)) return true;
+        if (taker) {
+            const float mo = wml[slot * 16 + gq], lo = wml[slot * 16 + 8 + gq];
+            const float M = fmaxf(m, mo);
+            const float fa = (m == -INFINITY) ? 0.f : __expf(m - M);
+            const float fb = (mo == -INFINITY) ? 0.f : __expf(mo - M);
+            // output columns 2tq, 2tq+1: factors of those heads
+            const float fa0 = __shfl_sync(0xffffffffu, fa, 8 * tq), fa1 = __shfl_sync(0xffffffffu, fa, 8 * tq + 4);
+            const float fb0 = __shfl_sync(0xffffffffu, fb, 8 * tq), fb1 = __shfl_sync(0xffffffffu, fb, 8 * tq + 4);
+            if (tq < TT) {
+                const float *src = ws + ((size_t)slot * 8 * TT + gq * TT + tq) * (HD / 4);
+#pragma unroll
+                for (int d = 0; d < KS; ++d) {
+                    const float4 v = reinterpret_cast<const float4 *>(src)[d];
+                    o[d][0] = fmaf(o[d][0], fa0, v.x * fb0);
+                    o[d][1] = fmaf(o[d][1], fa1, v.y * fb1);
+                    o[d][2] = fmaf(o[d][2], fa0, v.z * fb0);
+                    o[d][3] = fmaf(o[d][3], fa1, v.w * fb1);
+                }
+            }
+            lsum = fmaf(lsum, fa, lo * fb);
+            m = M;
+        }
+        if (cons_sync_or(ab)) return true;
+    }
+    // ---- warp 0 holds the piece: (o, m, l) per head into the partials
+    if (c.warp == 0) {
+        float *base = p.apart + (((size_t)l * g.Hq + hq0) * p.max_split + cpiece) * (HD + 2);
+        const size_t hstride = (size_t)p.max_split * (HD + 2);
+        if (2 * tq < G) {
+#pragma unroll
+            for (int d = 0; d < KS; ++d) {
+                base[(size_t)(2 * tq) * hstride + 16 * d + gq] = o[d][0];
+                base[(size_t)(2 * tq) * hstride + 16 * d + gq + 8] = o[d][2];
+            }
+        }
+        if (2 * tq + 1 < G) {
+#pragma unroll
+            for (int d = 0; d < KS; ++d) {
+                base[(size_t)(2 * tq + 1) * hstride + 16 * d + gq] = o[d][1];
+                base[(size_t)(2 * tq + 1) * hstride + 16 * d + gq + 8] = o[d][3];
+            }
+        }
+        if (tq == 0 && gq < G) {
+            base[(size_t)gq * hstride + HD] = m;
+            base[(size_t)gq * hstride + HD + 1] = lsum;
         }
     }
     if (cons_sync_or(ab)) return true;
