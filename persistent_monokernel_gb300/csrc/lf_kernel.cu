@@ -1060,6 +1060,13 @@ __device__ __forceinline__ void ldsm_x4_t(unsigned (&r)[4], uint32_t addr)
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(addr));
 }
+// Transpose of an 8x8 FP16 matrix held as one m8n8 fragment per warp.
+__device__ __forceinline__ unsigned movm_t(unsigned a)
+{
+    unsigned d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
 __device__ __forceinline__ unsigned pack_h2(__half lo, __half hi)
 {
     return (unsigned)__half_as_ushort(lo) | ((unsigned)__half_as_ushort(hi) << 16);
@@ -1151,59 +1158,63 @@ __device__ __forceinline__ bool attn_piece(const Ctx &c, ConsRing &rc, int l, in
     }
     if (cons_sync_or(ab)) return true;
     const uint32_t qfa = smem_u32(qfr) + (uint32_t)c.lane * 16u;
-    // ---- per-warp state: m, l of head gq (lanes of row gq; l partial per lane)
-    // and O^T tiles: o[d][0..3] = O[2tq][16d+gq], O[2tq+1][16d+gq],
-    // O[2tq][16d+gq+8], O[2tq+1][16d+gq+8]
-    float m = -INFINITY, lsum = 0.f;
+    // ---- per-warp state, per lane: running max and (partial) sum of heads
+    // 2tq and 2tq+1, and O^T tiles o[d][0..3] = O[2tq][16d+gq],
+    // O[2tq+1][16d+gq], O[2tq][16d+gq+8], O[2tq+1][16d+gq+8]
+    float ma = -INFINITY, mb = -INFINITY, la = 0.f, lb = 0.f;
     float o[KS][4];
 #pragma unroll
     for (int d = 0; d < KS; ++d) o[d][0] = o[d][1] = o[d][2] = o[d][3] = 0.f;
-    // ldmatrix row addresses: lanes 8i..8i+7 address matrix i; row r = lane & 7
-    // of 8 positions (matrices 2, 3: positions 8..15) and 16-byte group
-    // 2k (+1 for matrices 1, 3)
-    const int lrow = (c.lane & 7) + ((c.lane >> 4) << 3);
-    const int lgrp = (c.lane >> 3) & 1;
+    // ldmatrix row addresses (lanes 8i..8i+7 address matrix i, row = lane & 7):
+    // K as the A operand of S^T = K Q^T: matrices (positions 0-7 | 8-15) x
+    // (group 2k | 2k+1) in the order a0..a3; V for V^T: (positions 0-7 | 8-15)
+    // outer, (group 2d | 2d+1) inner, transposed
+    const int krw = (c.lane & 7) + (((c.lane >> 3) & 1) << 3), kgp = c.lane >> 4;
+    const int vrw = (c.lane & 7) + ((c.lane >> 4) << 3), vgp = (c.lane >> 3) & 1;
 
-    // one 16-position slab: positions q0 .. q0+nv-1 (nv in 1..16), rows at Kb/Vb
+    // one 16-position slab: positions q0 .. q0+nv-1 (nv in 1..16), rows at kb/vb
     auto slab = [&](uint32_t kb, uint32_t vb, int q0, int nv) {
-        const int prow = q0 + lrow;                     // position of the row this lane addresses
-        const uint32_t krow = kb + (uint32_t)lrow * ROW, vrow = vb + (uint32_t)lrow * ROW;
-        float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};   // positions 0-7, 8-15
+        const int kpos = q0 + krw, vpos = q0 + vrw;     // positions of the rows this lane addresses
+        const uint32_t krow = kb + (uint32_t)krw * ROW, vrow = vb + (uint32_t)vrw * ROW;
+        // S^T[pos][head]: sc0 = (gq, 2tq), sc1 = (gq, 2tq+1), sc2 = (gq+8, 2tq), sc3 = (gq+8, 2tq+1)
+        float st[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int k = 0; k < KS; ++k) {
-            unsigned b[4];
-            ldsm_x4(b, krow + (uint32_t)((((2 * k + lgrp) ^ (prow & 7))) << 4));
-            const uint4 qa = lds_u4(qfa + (uint32_t)k * 512u);
-            mma16816(s0, qa.x, 0u, qa.y, 0u, b[0], b[1]);
-            mma16816(s0, qa.z, 0u, qa.w, 0u, b[0], b[1]);
-            mma16816(s1, qa.x, 0u, qa.y, 0u, b[2], b[3]);
-            mma16816(s1, qa.z, 0u, qa.w, 0u, b[2], b[3]);
+            unsigned a[4];
+            ldsm_x4(a, krow + (uint32_t)((((2 * k + kgp) ^ (kpos & 7))) << 4));
+            const uint4 qb = lds_u4(qfa + (uint32_t)k * 512u);
+            mma16816(st, a[0], a[1], a[2], a[3], qb.x, qb.y);
+            mma16816(st, a[0], a[1], a[2], a[3], qb.z, qb.w);
         }
-        // scores of row gq at positions 2tq, 2tq+1, 8+2tq, 9+2tq; masked past nv
-        float sc[4] = {s0[0] * scale, s0[1] * scale, s1[0] * scale, s1[1] * scale};
-        const int cp[4] = {2 * tq, 2 * tq + 1, 8 + 2 * tq, 9 + 2 * tq};
+        float sc[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            if (cp[i] >= nv) sc[i] = -INFINITY;
-        float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float mn = fmaxf(m, mx);                  // finite: nv >= 1
-        const float corr = __expf(m - mn);              // 0 while m is -inf
-        float pr[4];
+        for (int i = 0; i < 4; ++i) sc[i] = st[i] * scale;
+        if (gq >= nv) sc[0] = sc[1] = -INFINITY;
+        if (gq + 8 >= nv) sc[2] = sc[3] = -INFINITY;
+        // maxima of heads 2tq, 2tq+1 over the slab (lanes of equal tq)
+        float xa = fmaxf(sc[0], sc[2]), xb = fmaxf(sc[1], sc[3]);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) pr[i] = __expf(sc[i] - mn);
-        lsum = fmaf(lsum, corr, (pr[0] + pr[1]) + (pr[2] + pr[3]));
-        m = mn;
-        // the output columns of this lane are heads 2tq and 2tq+1
-        const float ca = __shfl_sync(0xffffffffu, corr, 8 * tq), cb = __shfl_sync(0xffffffffu, corr, 8 * tq + 4);
-        // P^T as the B operand: b0 = P[gq][2tq, 2tq+1], b1 = P[gq][8+2tq, 9+2tq]
-        __half ph[4], pr2[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) split_h(pr[i], ph[i], pr2[i]);
-        const unsigned pb0h = pack_h2(ph[0], ph[1]), pb1h = pack_h2(ph[2], ph[3]);
-        const unsigned pb0r = pack_h2(pr2[0], pr2[1]), pb1r = pack_h2(pr2[2], pr2[3]);
-        // V^T as the A operand (rows = dims, columns = positions), rows past nv zeroed
+        for (int sh = 4; sh <= 16; sh <<= 1) {
+            xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, sh));
+            xb = fmaxf(xb, __shfl_xor_sync(0xffffffffu, xb, sh));
+        }
+        const float na = fmaxf(ma, xa), nb2 = fmaxf(mb, xb);   // finite: nv >= 1
+        const float ca = __expf(ma - na), cb = __expf(mb - nb2);   // 0 while the max is -inf
+        ma = na;
+        mb = nb2;
+        const float p0 = __expf(sc[0] - na), p1 = __expf(sc[1] - nb2), p2 = __expf(sc[2] - na), p3 = __expf(sc[3] - nb2);
+        la = fmaf(la, ca, p0 + p2);
+        lb = fmaf(lb, cb, p1 + p3);
+        // P^T as the B operand of O^T = V^T P^T: the 8x8 blocks (positions 0-7 |
+        // 8-15) x heads, transposed in registers
+        __half h0, r0, h1, r1, h2, r2, h3, r3;
+        split_h(p0, h0, r0);
+        split_h(p1, h1, r1);
+        split_h(p2, h2, r2);
+        split_h(p3, h3, r3);
+        const unsigned pb0h = movm_t(pack_h2(h0, h1)), pb1h = movm_t(pack_h2(h2, h3));
+        const unsigned pb0r = movm_t(pack_h2(r0, r1)), pb1r = movm_t(pack_h2(r2, r3));
+        // V^T as the A operand (rows = dims, columns = positions), positions past nv zeroed
         const unsigned keep0 = (2 * tq < nv ? 0x0000FFFFu : 0u) | (2 * tq + 1 < nv ? 0xFFFF0000u : 0u);
         const unsigned keep1 = (8 + 2 * tq < nv ? 0x0000FFFFu : 0u) | (9 + 2 * tq < nv ? 0xFFFF0000u : 0u);
 #pragma unroll
@@ -1213,7 +1224,7 @@ __device__ __forceinline__ bool attn_piece(const Ctx &c, ConsRing &rc, int l, in
             o[d][2] *= ca;
             o[d][3] *= cb;
             unsigned a[4];
-            ldsm_x4_t(a, vrow + (uint32_t)((((2 * d + lgrp) ^ (prow & 7))) << 4));
+            ldsm_x4_t(a, vrow + (uint32_t)((((2 * d + vgp) ^ (vpos & 7))) << 4));
             // matrices (transposed): 0 = positions 0-7 x dims 16d..16d+7, 1 = positions 0-7 x dims
             // 16d+8.., 2 = positions 8-15 x dims 16d.., 3 = positions 8-15 x dims 16d+8.. --
             // exactly the A fragments a0..a3 of V^T (rows gq / gq+8, columns 2tq / 8+2tq)
@@ -1253,21 +1264,22 @@ __device__ __forceinline__ bool attn_piece(const Ctx &c, ConsRing &rc, int l, in
             vlo[d] = __half2float(fresh[HD + 16 * d + gq]);
             vhi[d] = __half2float(fresh[HD + 16 * d + gq + 8]);
         }
-        float sf = -INFINITY;                            // score of head gq
+        float sa = 0.f, sb = 0.f;                        // scores of heads 2tq, 2tq+1 (0 for padding heads)
         for (int h = 0; h < G; ++h) {
             float dot = 0.f;
 #pragma unroll
             for (int e = 0; e < EL; ++e) dot = fmaf(qs[h * HD + c.lane * EL + e], kf[e], dot);
             dot = warp_sum(dot) * scale;
-            if (h == gq) sf = dot;
+            if (h == 2 * tq) sa = dot;
+            if (h == 2 * tq + 1) sb = dot;
         }
-        if (gq >= G) sf = 0.f;                           // padding rows (never written out)
-        const float mn = fmaxf(m, sf);
-        const float corr = __expf(m - mn), pf = __expf(sf - mn);
-        lsum = fmaf(lsum, corr, tq == 0 ? pf : 0.f);
-        m = mn;
-        const float ca = __shfl_sync(0xffffffffu, corr, 8 * tq), cb = __shfl_sync(0xffffffffu, corr, 8 * tq + 4);
-        const float pa = __shfl_sync(0xffffffffu, pf, 8 * tq), pb = __shfl_sync(0xffffffffu, pf, 8 * tq + 4);
+        const float na = fmaxf(ma, sa), nb2 = fmaxf(mb, sb);
+        const float ca = __expf(ma - na), cb = __expf(mb - nb2);
+        const float pa = __expf(sa - na), pb = __expf(sb - nb2);
+        la = fmaf(la, ca, gq == 0 ? pa : 0.f);
+        lb = fmaf(lb, cb, gq == 0 ? pb : 0.f);
+        ma = na;
+        mb = nb2;
 #pragma unroll
         for (int d = 0; d < KS; ++d) {
             o[d][0] = fmaf(o[d][0], ca, pa * vlo[d]);
@@ -1277,11 +1289,14 @@ __device__ __forceinline__ bool attn_piece(const Ctx &c, ConsRing &rc, int l, in
         }
     }
     trace_mark(c, step, 5 * l + 1, TR_X1);
-    lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
-    lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
+#pragma unroll
+    for (int sh = 4; sh <= 16; sh <<= 1) {
+        la += __shfl_xor_sync(0xffffffffu, la, sh);
+        lb += __shfl_xor_sync(0xffffffffu, lb, sh);
+    }
 
     // ---- merge the warps pairwise (warp w + st into warp w, st = 4, 2, 1):
-    // state = (m, l) per head and the O^T tiles of the lanes t < TT
+    // state = (m, l) of heads 2tq, 2tq+1 and the O^T tiles of the lanes t < TT
     for (int st = NCW / 2; st >= 1; st >>= 1) {
         const bool sender = c.warp >= st && c.warp < 2 * st, taker = c.warp < st;
         const int slot = sender ? c.warp - st : c.warp;
@@ -1292,20 +1307,20 @@ __device__ __forceinline__ bool attn_piece(const Ctx &c, ConsRing &rc, int l, in
                 for (int d = 0; d < KS; ++d)
                     reinterpret_cast<float4 *>(dst)[d] = make_float4(o[d][0], o[d][1], o[d][2], o[d][3]);
             }
-            if (tq == 0) {
-                wml[slot * 16 + gq] = m;
-                wml[slot * 16 + 8 + gq] = lsum;
+            if (gq == 0) {
+                wml[slot * 16 + 2 * tq] = ma;
+                wml[slot * 16 + 2 * tq + 1] = mb;
+                wml[slot * 16 + 8 + 2 * tq] = la;
+                wml[slot * 16 + 9 + 2 * tq] = lb;
             }
         }
         if (cons_sync_or(ab)) return true;
         if (taker) {
-            const float mo = wml[slot * 16 + gq], lo = wml[slot * 16 + 8 + gq];
-            const float M = fmaxf(m, mo);
-            const float fa = (m == -INFINITY) ? 0.f : __expf(m - M);
-            const float fb = (mo == -INFINITY) ? 0.f : __expf(mo - M);
-            // output columns 2tq, 2tq+1: factors of those heads
-            const float fa0 = __shfl_sync(0xffffffffu, fa, 8 * tq), fa1 = __shfl_sync(0xffffffffu, fa, 8 * tq + 4);
-            const float fb0 = __shfl_sync(0xffffffffu, fb, 8 * tq), fb1 = __shfl_sync(0xffffffffu, fb, 8 * tq + 4);
+            const float moa = wml[slot * 16 + 2 * tq], mob = wml[slot * 16 + 2 * tq + 1];
+            const float loa = wml[slot * 16 + 8 + 2 * tq], lob = wml[slot * 16 + 9 + 2 * tq];
+            const float Ma = fmaxf(ma, moa), Mb = fmaxf(mb, mob);
+            const float fa0 = (ma == -INFINITY) ? 0.f : __expf(ma - Ma), fb0 = (moa == -INFINITY) ? 0.f : __expf(moa - Ma);
+            const float fa1 = (mb == -INFINITY) ? 0.f : __expf(mb - Mb), fb1 = (mob == -INFINITY) ? 0.f : __expf(mob - Mb);
             if (tq < TT) {
                 const float *src = ws + ((size_t)slot * 8 * TT + gq * TT + tq) * (HD / 4);
 #pragma unroll
@@ -1317,8 +1332,10 @@ __device__ __forceinline__ bool attn_piece(const Ctx &c, ConsRing &rc, int l, in
                     o[d][3] = fmaf(o[d][3], fa1, v.w * fb1);
                 }
             }
-            lsum = fmaf(lsum, fa, lo * fb);
-            m = M;
+            la = fmaf(la, fa0, loa * fb0);
+            lb = fmaf(lb, fa1, lob * fb1);
+            ma = Ma;
+            mb = Mb;
         }
         if (cons_sync_or(ab)) return true;
     }
@@ -1327,22 +1344,28 @@ __device__ __forceinline__ bool attn_piece(const Ctx &c, ConsRing &rc, int l, in
         float *base = p.apart + (((size_t)l * g.Hq + hq0) * p.max_split + cpiece) * (HD + 2);
         const size_t hstride = (size_t)p.max_split * (HD + 2);
         if (2 * tq < G) {
+            float *ha = base + (size_t)(2 * tq) * hstride;
 #pragma unroll
             for (int d = 0; d < KS; ++d) {
-                base[(size_t)(2 * tq) * hstride + 16 * d + gq] = o[d][0];
-                base[(size_t)(2 * tq) * hstride + 16 * d + gq + 8] = o[d][2];
+                ha[16 * d + gq] = o[d][0];
+                ha[16 * d + gq + 8] = o[d][2];
+            }
+            if (gq == 0) {
+                ha[HD] = ma;
+                ha[HD + 1] = la;
             }
         }
         if (2 * tq + 1 < G) {
+            float *hb = base + (size_t)(2 * tq + 1) * hstride;
 #pragma unroll
             for (int d = 0; d < KS; ++d) {
-                base[(size_t)(2 * tq + 1) * hstride + 16 * d + gq] = o[d][1];
-                base[(size_t)(2 * tq + 1) * hstride + 16 * d + gq + 8] = o[d][3];
+                hb[16 * d + gq] = o[d][1];
+                hb[16 * d + gq + 8] = o[d][3];
             }
-        }
-        if (tq == 0 && gq < G) {
-            base[(size_t)gq * hstride + HD] = m;
-            base[(size_t)gq * hstride + HD + 1] = lsum;
+            if (gq == 0) {
+                hb[HD] = mb;
+                hb[HD + 1] = lb;
+            }
         }
     }
     if (cons_sync_or(ab)) return true;
