@@ -23,7 +23,7 @@ constexpr int NCT = NCW * 32;         // consumer threads
 constexpr int W_PROD = NCW, W_LOAD = NCW + 1, W_RED = NCW + 2;
 constexpr int NTHREADS = NCT + 96;
 constexpr int TICKETS = 32;           // ring slots in flight (mbarrier pairs)
-constexpr int ATT_CHUNK_BYTES = 16384;// K + V bytes of one attention sub-block
+constexpr int ATT_CHUNK_BYTES = 32768;// K + V bytes of one attention sub-block
 constexpr int MAX_TOPK = 64;
 constexpr int MAX_GROUP = 8;          // query heads per KV head
 constexpr int CNT_STRIDE = 32;        // uint32 words between counters (one 128-byte line each)

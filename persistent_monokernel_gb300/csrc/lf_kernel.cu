@@ -288,8 +288,7 @@ struct ProdRing {
         ++n;
         return true;
     }
-    // K and V rows of one attention sub-block: re-read every step, so they
-    // keep the normal L2 priority.
+    // K and V rows of one attention sub-block (L2 policy pol_kv).
     __device__ bool emit2(const Ctx &c, const void *src0, const void *src1, unsigned half_bytes)
     {
         int o = reserve(c, 2 * half_bytes);
@@ -1759,7 +1758,14 @@ __device__ void producer(const Ctx &c, const RepackSrc *w)
         else return produce_tiles(cc, r, s, l, step_now);
     };
     pr.pol = policy_evict_first();
-    pr.pol_kv = policy_evict_normal();
+    // K/V rows are read again by the next step: they keep the normal L2
+    // priority while the cache the call reads fits in L2, and are streamed
+    // evict-first like the weights once it cannot stay resident anyway
+    {
+        const long long ctx_end = (long long)p.pos0 + p.n_steps;
+        const long long kv_read = ctx_end * (long long)p.g.L * p.g.KV * 4;   // K + V, FP16, every layer
+        pr.pol_kv = kv_read > (128ll << 20) ? policy_evict_first() : policy_evict_normal();
+    }
     pr.pol_pf = p.l2_prefetch_last ? policy_evict_last() : policy_evict_normal();
     if (!kDirect && p.only_stage < 0 && p.l2_prefetch_bytes > 0) {
         const CtaPlan &pl = *c.plan;
