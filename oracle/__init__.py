@@ -78,6 +78,10 @@ def lib():
             L.orc_destroy.argtypes = [C.c_void_p]
             L.orc_reset.argtypes = [C.c_void_p]
             L.orc_set_windows.argtypes = [C.c_void_p, C.POINTER(C.c_int32)]
+            L.orc_set_fp8.argtypes = [C.c_void_p, C.POINTER(C.c_void_p)]
+            L.orc_e4m3_to_float.argtypes = [C.c_uint8]
+            L.orc_e4m3_to_float.restype = C.c_float
+            L.orc_matvec_fp8.argtypes = [C.POINTER(C.c_uint8), f32p, f32p, C.c_int, C.c_int, f32p]
             L.orc_pos.argtypes = [C.c_void_p]
             L.orc_pending.argtypes = [C.c_void_p]
             L.orc_kcache.argtypes = [C.c_void_p]
@@ -102,6 +106,15 @@ def _u16(a):
 
 def _i32(a):
     return a.ctypes.data_as(C.POINTER(C.c_int32))
+
+
+def _as_np(a) -> np.ndarray:
+    if hasattr(a, "numpy"):
+        a = a.detach().cpu().contiguous().numpy()
+    return np.ascontiguousarray(a)
+
+
+FP8_MATRICES = ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down", "lm_head")
 
 
 def _as_u16(a) -> np.ndarray:
@@ -139,6 +152,20 @@ def matvec(W, x):
     x = np.ascontiguousarray(x, dtype=np.float32)
     y = np.empty(W.shape[0], dtype=np.float32)
     lib().orc_matvec(_u16(W), _f32(x), W.shape[0], W.shape[1], _f32(y))
+    return y
+
+
+def e4m3_to_float(code: int) -> float:
+    return lib().orc_e4m3_to_float(code)
+
+
+def matvec_fp8(codes, scale, x):
+    """y = diag(scale) . decode_e4m3(codes) . x (codes uint8 [rows, cols])."""
+    Cc = np.ascontiguousarray(_as_np(codes), dtype=np.uint8)
+    sc = np.ascontiguousarray(_as_np(scale), dtype=np.float32)
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    y = np.empty(Cc.shape[0], dtype=np.float32)
+    lib().orc_matvec_fp8(Cc.ctypes.data_as(C.POINTER(C.c_uint8)), _f32(sc), _f32(x), Cc.shape[0], Cc.shape[1], _f32(y))
     return y
 
 
@@ -195,13 +222,25 @@ class OracleDecoder:
     def __init__(self, cfg, weights: dict, max_seq: int, layer_window=None):
         self.cfg = cfg
         self.max_seq = max_seq
-        self._keep = {n: _as_u16(weights[n]) for n in _WNAMES}
+        # FP8 weights: the eight projections are uint8 E4M3 codes with FP32
+        # per-row scales in weights["<name>_scale"]
+        self.fp8 = _as_np(weights["wq"]).dtype == np.uint8
+        self._keep = {}
+        for n in _WNAMES:
+            if self.fp8 and n in FP8_MATRICES:
+                self._keep[n] = np.ascontiguousarray(_as_np(weights[n]), dtype=np.uint8)
+                self._keep[n + "_scale"] = np.ascontiguousarray(_as_np(weights[n + "_scale"]), dtype=np.float32)
+            else:
+                self._keep[n] = _as_u16(weights[n])
         c = _Config(cfg.n_layers, cfg.d_model, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim, cfg.ffn_dim,
                     cfg.vocab, max_seq, cfg.rope_theta, cfg.rms_eps)
         w = _Weights(*[self._keep[n].ctypes.data for n in _WNAMES])
         self._h = lib().orc_create(C.byref(c), C.byref(w))
         if not self._h:
             raise ValueError("orc_create rejected the configuration")
+        if self.fp8:
+            ptrs = (C.c_void_p * 8)(*[self._keep[n + "_scale"].ctypes.data for n in FP8_MATRICES])
+            lib().orc_set_fp8(self._h, ptrs)
         if layer_window is not None:
             win = np.ascontiguousarray(np.asarray(layer_window, dtype=np.int32))
             if win.shape != (cfg.n_layers,):

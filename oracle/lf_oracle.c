@@ -107,6 +107,33 @@ ORC_API void orc_matvec(const uint16_t *W, const float *x, int n_rows, int k_dim
     }
 }
 
+/* FP8 E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; no
+ * infinities; S.1111.111 is NaN; largest finite value 448), decoded from the
+ * format definition: exponent field 0 gives the subnormals m/8 * 2^-6. */
+ORC_API float orc_e4m3_to_float(uint8_t c)
+{
+    const int s = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    if (e == 15 && m == 7) return NAN;
+    const float mag = e == 0 ? ldexpf((float)m / 8.0f, -6) : ldexpf(1.0f + (float)m / 8.0f, e - 7);
+    return s ? -mag : mag;
+}
+
+/* y = diag(scale) . decode(C) . x for an [n_rows, k_dim] matrix of E4M3 codes
+ * with one FP32 scale per row (weight-only FP8; the pages' FP8 streaming,
+ * shivam2003.com, "Scaling the idea to frontier models"): each row's dot
+ * product of the decoded codes with x in FP32, index order, then times the
+ * row's scale. */
+ORC_API void orc_matvec_fp8(const uint8_t *C, const float *scale, const float *x, int n_rows, int k_dim, float *y)
+{
+    #pragma omp parallel for schedule(static)
+    for (int r = 0; r < n_rows; ++r) {
+        const uint8_t *row = C + (size_t)r * (size_t)k_dim;
+        float acc = 0.0f;
+        for (int k = 0; k < k_dim; ++k) acc += orc_e4m3_to_float(row[k]) * x[k];
+        y[r] = acc * scale[r];
+    }
+}
+
 /* Rotate-half RoPE of one head vector v[hd] at position pos:
  * for i < hd/2, theta_i = pos * base^(-2i/hd) (in double), and
  *   v[i]        <- v[i] cos - v[i+hd/2] sin
@@ -266,6 +293,11 @@ typedef struct {
     int pos;            /* position of the pending token */
     int pending;        /* token fed to the next forward pass, -1 if none */
     int *window;        /* [L] attention window of each layer in positions, 0 = the whole cache */
+    /* FP8 weights: the eight projection pointers of w hold E4M3 codes, and
+     * scale[i] the per-row FP32 scales of matrix i (wq, wk, wv, wo, w_gate,
+     * w_up, w_down, lm_head); fp8 = 0: FP16 weights */
+    int fp8;
+    const float *scale[8];
     /* activations */
     float *x, *xn, *q, *k, *v, *attn, *tmp, *gate, *up, *hbuf, *scores;
 } orc_model;
@@ -314,6 +346,25 @@ ORC_API void orc_reset(orc_model *m) { m->pos = 0; m->pending = -1; }
  * so that the KV cache they read stops growing with the context).  window[l]
  * = W > 0: the query at position p of layer l attends to the W positions
  * max(0, p-W+1) .. p; W = 0: to every cached position.  NULL clears them. */
+/* Switch the model to FP8 weights (see orc_model); NULL scales switch back. */
+ORC_API void orc_set_fp8(orc_model *m, const float *const *scales)
+{
+    m->fp8 = scales != NULL;
+    for (int i = 0; i < 8; ++i) m->scale[i] = scales ? scales[i] : NULL;
+}
+
+/* Projection `which` (0 wq .. 7 lm_head) of layer l: y = W x. */
+static void orc_project(const orc_model *m, int which, int l, int n_rows, int k_dim, const float *x, float *y)
+{
+    const orc_weights *w = &m->w;
+    const uint16_t *base[8] = {w->wq, w->wk, w->wv, w->wo, w->w_gate, w->w_up, w->w_down, w->lm_head};
+    const size_t off = (size_t)l * (size_t)n_rows * (size_t)k_dim;
+    if (m->fp8)
+        orc_matvec_fp8((const uint8_t *)base[which] + off, m->scale[which] + (size_t)l * n_rows, x, n_rows, k_dim, y);
+    else
+        orc_matvec(base[which] + off, x, n_rows, k_dim, y);
+}
+
 ORC_API void orc_set_windows(orc_model *m, const int *window)
 {
     for (int l = 0; l < m->c.n_layers; ++l) m->window[l] = window ? (window[l] > 0 ? window[l] : 0) : 0;
@@ -350,9 +401,9 @@ ORC_API int orc_forward(orc_model *m, int token, float *logits)
     for (int l = 0; l < L; ++l) {
         /* attention block */
         orc_rmsnorm(m->x, w->attn_norm + (size_t)l * d, d, c->rms_eps, m->xn);
-        orc_matvec(w->wq + (size_t)l * Q * d, m->xn, Q, d, m->q);
-        orc_matvec(w->wk + (size_t)l * KV * d, m->xn, KV, d, m->k);
-        orc_matvec(w->wv + (size_t)l * KV * d, m->xn, KV, d, m->v);
+        orc_project(m, 0, l, Q, d, m->xn, m->q);
+        orc_project(m, 1, l, KV, d, m->xn, m->k);
+        orc_project(m, 2, l, KV, d, m->xn, m->v);
         for (int h = 0; h < Hq; ++h) orc_rope(m->q + h * hd, hd, p, c->rope_theta);
         for (int g = 0; g < Hkv; ++g) orc_rope(m->k + g * hd, hd, p, c->rope_theta);
         for (int g = 0; g < Hkv; ++g) {
@@ -372,20 +423,20 @@ ORC_API int orc_forward(orc_model *m, int token, float *logits)
             orc_attend_head(m->q + h * hd, m->kcache + base, m->vcache + base, p + 1 - j0, hd, scale,
                             m->scores + (size_t)h * c->max_seq, m->attn + h * hd);
         }
-        orc_matvec(w->wo + (size_t)l * d * Q, m->attn, d, Q, m->tmp);
+        orc_project(m, 3, l, d, Q, m->attn, m->tmp);
         for (int i = 0; i < d; ++i) m->x[i] = m->x[i] + m->tmp[i];
 
         /* FFN block */
         orc_rmsnorm(m->x, w->ffn_norm + (size_t)l * d, d, c->rms_eps, m->xn);
-        orc_matvec(w->w_gate + (size_t)l * F * d, m->xn, F, d, m->gate);
-        orc_matvec(w->w_up + (size_t)l * F * d, m->xn, F, d, m->up);
+        orc_project(m, 4, l, F, d, m->xn, m->gate);
+        orc_project(m, 5, l, F, d, m->xn, m->up);
         for (int i = 0; i < F; ++i) m->hbuf[i] = orc_silu(m->gate[i]) * m->up[i];
-        orc_matvec(w->w_down + (size_t)l * d * F, m->hbuf, d, F, m->tmp);
+        orc_project(m, 6, l, d, F, m->hbuf, m->tmp);
         for (int i = 0; i < d; ++i) m->x[i] = m->x[i] + m->tmp[i];
     }
     if (logits) {
         orc_rmsnorm(m->x, w->final_norm, d, c->rms_eps, m->xn);
-        orc_matvec(w->lm_head, m->xn, c->vocab, d, logits);
+        orc_project(m, 7, 0, c->vocab, d, m->xn, logits);
     }
     m->pos = p + 1;
     return 0;

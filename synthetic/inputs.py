@@ -94,12 +94,13 @@ def _fill(out: torch.Tensor, table: torch.Tensor, seed: int, tensor_id: int, lay
         flat[s:s + m] = table[idx]
 
 
-def make_weights(cfg: ModelConfig, seed: int, device="cpu", gains: str = "ones") -> dict:
+def make_weights(cfg: ModelConfig, seed: int, device="cpu", gains: str = "ones", projections: bool = True) -> dict:
     """All FP16 tensors of one decoder.
 
     gains="ones" gives RMSNorm gains of exactly 1.0 (the configured
     workloads); gains="random" gives 1 + N(0, 0.1)-distributed gains, used by
-    tests to exercise the gain multiply.
+    tests to exercise the gain multiply.  projections=False leaves out the
+    eight projection matrices (embedding and gains only).
     """
     device = torch.device(device)
     table = normal_table(0.02).to(device)
@@ -111,6 +112,8 @@ def make_weights(cfg: ModelConfig, seed: int, device="cpu", gains: str = "ones")
     }
     w = {}
     for name in WEIGHT_ORDER[:9]:
+        if not projections and name != "embed":
+            continue
         shp = shapes[name]
         t = torch.empty(shp, dtype=torch.float16, device=device)
         if len(shp) == 3:
@@ -130,6 +133,59 @@ def make_weights(cfg: ModelConfig, seed: int, device="cpu", gains: str = "ones")
             w[name] = (1.0 + 5.0 * t.to(torch.float32)).to(torch.float16)
         else:
             raise ValueError(f"gains must be 'ones' or 'random', not {gains!r}")
+    return w
+
+
+# ---- FP8 (E4M3) weights with one FP32 scale per output row
+
+FP8_MATRICES = ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down", "lm_head")
+_FP8_CODE_STD = 64.0    # the codes' N(0, 64): +-448 (E4M3's largest finite value) is 7 sigma
+_FP8_TABLE_CACHE: dict = {}
+
+
+def fp8_code_table() -> torch.Tensor:
+    """uint8 table of 65,536 E4M3 codes: the mid-quantiles of N(0, 64), each
+    clipped to +-448 and converted to E4M3 by torch's float8_e4m3fn cast."""
+    if "t" not in _FP8_TABLE_CACHE:
+        nd = NormalDist(0.0, _FP8_CODE_STD)
+        vals = torch.tensor([nd.inv_cdf((k + 0.5) / 65536.0) for k in range(65536)], dtype=torch.float32)
+        vals = vals.clamp(-448.0, 448.0)
+        _FP8_TABLE_CACHE["t"] = vals.to(torch.float8_e4m3fn).view(torch.uint8)
+    return _FP8_TABLE_CACHE["t"]
+
+
+def _fill_scales(out: torch.Tensor, seed: int, tensor_id: int, layer: int) -> None:
+    """Per-row FP32 scales 0.02/64 * u, u uniform on [0.75, 1.25) in 2**-16 steps,
+    so that code * scale follows N(0, 0.02) with a row-dependent spread."""
+    idx = hashed_indices(seed, 0x100 + tensor_id, layer, 0, out.numel(), out.device)
+    u = 0.75 + idx.to(torch.float64) * (0.5 / 65536.0)
+    out.copy_((u * (0.02 / _FP8_CODE_STD)).to(torch.float32).view(out.shape))
+
+
+def make_weights_fp8(cfg: ModelConfig, seed: int, device="cpu", gains: str = "ones") -> dict:
+    """A decoder whose eight projection matrices are E4M3 codes (uint8, same
+    shapes as the FP16 weights) with FP32 scales per output row (`<name>_scale`,
+    [L, rows] or [V]); the embedding and the norm gains stay FP16 (make_weights).
+    The matrix a layer applies is diag(scale) . decode(codes)."""
+    w = make_weights(cfg, seed, device=device, gains=gains, projections=False)
+    device = torch.device(device)
+    table = fp8_code_table().to(device)
+    L, d, F, V, Q, KV = cfg.n_layers, cfg.d_model, cfg.ffn_dim, cfg.vocab, cfg.q_dim, cfg.kv_dim
+    shapes = {"wq": (L, Q, d), "wk": (L, KV, d), "wv": (L, KV, d), "wo": (L, d, Q), "w_gate": (L, F, d),
+              "w_up": (L, F, d), "w_down": (L, d, F), "lm_head": (V, d)}
+    for name in FP8_MATRICES:
+        shp = shapes[name]
+        codes = torch.empty(shp, dtype=torch.uint8, device=device)
+        scales = torch.empty(shp[:-1], dtype=torch.float32, device=device)
+        if len(shp) == 3:
+            for layer in range(shp[0]):
+                _fill(codes[layer], table, seed, _TENSOR_ID[name], layer)
+                _fill_scales(scales[layer], seed, _TENSOR_ID[name], layer)
+        else:
+            _fill(codes, table, seed, _TENSOR_ID[name], 0)
+            _fill_scales(scales, seed, _TENSOR_ID[name], 0)
+        w[name] = codes
+        w[name + "_scale"] = scales
     return w
 
 
