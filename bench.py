@@ -156,8 +156,10 @@ def workload_desc(wl, K):
         ws = sorted({w for w in wl.layer_window if w > 0})
         nwin = sum(1 for w in wl.layer_window if w > 0)
         win = f"; sliding-window attention (window {'/'.join(map(str, ws))}) in {nwin} of {m.n_layers} layers"
+    wdesc = ("FP8 E4M3 projection weights with FP32 per-row scales (~N(0,0.02) after scaling)"
+             if wl.weights == "fp8" else "FP16 weights ~N(0,0.02)")
     return (f"{wl.name}: {m.n_layers} layers, d_model {m.d_model}, {m.n_heads}/{m.n_kv_heads} heads x {m.head_dim}, "
-            f"SwiGLU FFN {m.ffn_dim}, vocab {m.vocab}, FP16 weights ~N(0,0.02){win}; prompt {wl.prompt_len}, "
+            f"SwiGLU FFN {m.ffn_dim}, vocab {m.vocab}, {wdesc}{win}; prompt {wl.prompt_len}, "
             f"{K} decode steps ({samp})")
 
 
@@ -191,7 +193,7 @@ def run_ours(args):
 
     import persistent_monokernel_gb300 as pm
     from persistent_monokernel_gb300 import build as pm_build
-    from synthetic import WORKLOADS, make_prompt, make_weights
+    from synthetic import WORKLOADS, make_prompt, make_weights, make_weights_fp8
 
     world, rank, local = dist_setup()
     if world != args.gpus:
@@ -211,7 +213,7 @@ def run_ours(args):
     K = args.steps or wl.decode_steps
     W = max(3, args.warmup)
     max_seq = wl.prompt_len + max(K, W, 128)
-    weights = make_weights(cfg, wl.weight_seed, device="cuda")
+    weights = (make_weights_fp8 if wl.weights == "fp8" else make_weights)(cfg, wl.weight_seed, device="cuda")
     prompt = make_prompt(cfg.vocab, wl.prompt_len, wl.prompt_seed).cuda()
     dec = pm.Decoder(cfg, weights, max_seq, layer_window=wl.layer_window)
     info = dec.info()
@@ -275,14 +277,14 @@ def run_ours(args):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f32",
-        "weights_dtype": "fp16",
+        "weights_dtype": "fp8_e4m3 (FP32 per-row scales)" if wl.weights == "fp8" else "fp16",
         "data": "synthetic: seeded FP16 weights ~N(0,0.02), seeded uniform prompt ids",
         "config": {
             "workload": workload_desc(wl, K),
             "prompt_len": wl.prompt_len,
             "decode_positions": [first_pos, first_pos + K - 1],
             "parallelism": f"replicas x{world} (no sharding)",
-            "l2": f"inputs larger than L2: {cfg.weight_bytes_per_token() / 1e9:.2f} GB of weights streamed per step",
+            "l2": f"inputs larger than L2: {cfg.weight_bytes_per_token(wl.weights) / 1e9:.2f} GB of weights streamed per step",
             "schedule": "monokernel, per-dependency flags",
             "grid": f"{info['n_ctas']} CTAs x {info['threads_per_cta']} threads, {info['smem_bytes']} B smem "
                     f"({info['ring_bytes']} B weight ring)",
@@ -401,7 +403,7 @@ def run_reference(args):
         return
     import torch
 
-    from synthetic import WORKLOADS, make_prompt, make_weights
+    from synthetic import WORKLOADS, make_prompt, make_weights, make_weights_fp8
     import oracle
 
     oracle.build()
@@ -410,7 +412,8 @@ def run_reference(args):
     K = args.steps or wl.decode_steps
     W = max(3, args.warmup)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    wc = {k: v.cpu() for k, v in make_weights(cfg, wl.weight_seed, device=dev).items()}
+    mk = make_weights_fp8 if wl.weights == "fp8" else make_weights
+    wc = {k: v.cpu() for k, v in mk(cfg, wl.weight_seed, device=dev).items()}
     pr = make_prompt(cfg.vocab, 8, wl.prompt_seed).numpy()
     tok_s, n, dt, threads = time_oracle(cfg, wc, pr, budget_s=60.0, max_steps=K, warmup=min(W, 3),
                                         layer_window=wl.layer_window)

@@ -44,7 +44,7 @@ extern "C" {
 #define LF_API
 #endif
 
-#define LF_ABI_VERSION 2
+#define LF_ABI_VERSION 3
 #define LF_MAX_TOP_K 64          /* largest top_k that lf_decode accepts (besides 0) */
 
 typedef enum {
@@ -104,16 +104,31 @@ typedef struct {
      * max(0, p-W+1) .. p only; 0 keeps the whole cache.  The KV cache still
      * holds every position (max_seq). */
     const int32_t *layer_window;
+    /* Format of the eight projection matrices (wq .. w_down, lm_head):
+     * LF_WEIGHTS_FP16 (0), or LF_WEIGHTS_FP8_E4M3 (1): weight-only FP8 (the
+     * pages' FP8 streaming, shivam2003.com, "Scaling the idea to frontier
+     * models"), one byte per weight in OCP E4M3 (no infinities, 448 largest)
+     * and one FP32 scale per output row in the lf_weights *_scale arrays; the
+     * matrix applied is diag(scale) . decode(codes), dot products in FP32 with
+     * the scale applied to each finished row sum.  The embedding and the norm
+     * gains stay FP16.  lf_generate_noalloc takes FP16 weights only. */
+    int32_t weight_format;
 } lf_config;
 
-/* Device pointers to the caller's FP16 weights (row-major, stacked over
- * layers).  L = n_layers, d = d_model, Q = n_heads*head_dim,
- * KV = n_kv_heads*head_dim, F = ffn_dim, V = vocab.
- * lf_create copies the projection matrices and the LM head into a
- * library-owned, per-CTA streaming layout; the caller may free those after
- * lf_create returns.  embed and the three norm-gain tensors are read in
- * place by every decode step and must outlive the handle.  Every pointer
- * must be 16-byte aligned (the kernels read them with bulk copies). */
+#define LF_WEIGHTS_FP16 0
+#define LF_WEIGHTS_FP8_E4M3 1
+
+/* Device pointers to the caller's weights (row-major, stacked over layers):
+ * FP16, or for lf_config.weight_format = LF_WEIGHTS_FP8_E4M3 the eight
+ * projections as E4M3 bytes with FP32 per-row scales.  L = n_layers,
+ * d = d_model, Q = n_heads*head_dim, KV = n_kv_heads*head_dim, F = ffn_dim,
+ * V = vocab.  lf_create copies the projection matrices, the LM head and the
+ * scales into library-owned memory (a per-CTA streaming layout for the
+ * matrices); the caller may free those after lf_create returns.  embed and
+ * the three norm-gain tensors are read in place by every decode step and must
+ * outlive the handle.  Every matrix pointer must be 16-byte aligned (the
+ * kernels read them with bulk copies); the scale pointers are NULL for FP16
+ * weights and 4-byte aligned otherwise. */
 typedef struct {
     const void *embed;       /* [V, d]      read in place */
     const void *attn_norm;   /* [L, d]      read in place */
@@ -127,6 +142,15 @@ typedef struct {
     const void *w_down;      /* [L, d, F]   copied */
     const void *final_norm;  /* [d]         read in place */
     const void *lm_head;     /* [V, d]      copied (untied from embed) */
+    /* FP8 weights only: FP32 scale of every row of the matrix of the same name */
+    const float *wq_scale;      /* [L, Q]  */
+    const float *wk_scale;      /* [L, KV] */
+    const float *wv_scale;      /* [L, KV] */
+    const float *wo_scale;      /* [L, d]  */
+    const float *w_gate_scale;  /* [L, F]  */
+    const float *w_up_scale;    /* [L, F]  */
+    const float *w_down_scale;  /* [L, d]  */
+    const float *lm_head_scale; /* [V]     */
 } lf_weights;
 
 /* Token choice, after the Gumbel-max trick of shivam2003.com ("The fused

@@ -38,15 +38,18 @@ class lf_config(C.Structure):
                 ("n_kv_heads", C.c_int32), ("head_dim", C.c_int32), ("ffn_dim", C.c_int32), ("vocab", C.c_int32),
                 ("max_seq", C.c_int32), ("rope_theta", C.c_float), ("rms_eps", C.c_float),
                 ("wait_timeout_ns", C.c_int64), ("n_ctas", C.c_int32), ("fault_step", C.c_int32),
-                ("layer_window", C.POINTER(C.c_int32))]
+                ("layer_window", C.POINTER(C.c_int32)), ("weight_format", C.c_int32)]
 
 
+WEIGHTS_FP16, WEIGHTS_FP8_E4M3 = 0, 1
 WEIGHT_FIELDS = ("embed", "attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down",
                  "final_norm", "lm_head")
+FP8_MATRICES = ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down", "lm_head")
+SCALE_FIELDS = tuple(n + "_scale" for n in FP8_MATRICES)
 
 
 class lf_weights(C.Structure):
-    _fields_ = [(n, C.c_void_p) for n in WEIGHT_FIELDS]
+    _fields_ = [(n, C.c_void_p) for n in WEIGHT_FIELDS + SCALE_FIELDS]
 
 
 class lf_sampling(C.Structure):
@@ -141,16 +144,22 @@ class Decoder:
         import torch
         self.model = model
         self.max_seq = int(max_seq)
-        for n in WEIGHT_FIELDS:
+        # FP8 weights: the eight projections as uint8 E4M3 codes plus FP32 per-row scales
+        self.fp8 = weights["wq"].dtype == torch.uint8
+        for n in WEIGHT_FIELDS + (SCALE_FIELDS if self.fp8 else ()):
             t = weights[n]
-            if not (t.is_cuda and t.dtype == torch.float16 and t.is_contiguous()):
-                raise ValueError(f"weight {n} must be a contiguous CUDA float16 tensor")
+            want = (torch.uint8 if n in FP8_MATRICES else torch.float32 if n in SCALE_FIELDS else torch.float16) \
+                if self.fp8 else torch.float16
+            if not (t.is_cuda and t.dtype == want and t.is_contiguous()):
+                raise ValueError(f"weight {n} must be a contiguous CUDA {want} tensor")
         # embed and the norm gains are read in place by every step: keep them alive
         self._keep = {n: weights[n] for n in ("embed", "attn_norm", "ffn_norm", "final_norm")}
         cfg = lf_config(model.n_layers, model.d_model, model.n_heads, model.n_kv_heads, model.head_dim,
                         model.ffn_dim, model.vocab, self.max_seq, model.rope_theta, model.rms_eps,
-                        int(wait_timeout_ns), int(n_ctas), int(fault_step), _windows(model, layer_window))
-        w = lf_weights(*[_dptr(weights[n]) for n in WEIGHT_FIELDS])
+                        int(wait_timeout_ns), int(n_ctas), int(fault_step), _windows(model, layer_window),
+                        WEIGHTS_FP8_E4M3 if self.fp8 else WEIGHTS_FP16)
+        w = lf_weights(*[_dptr(weights[n]) for n in WEIGHT_FIELDS],
+                       *[_dptr(weights[n]) if self.fp8 else None for n in SCALE_FIELDS])
         h = C.c_void_p()
         _check(lib().lf_create(C.byref(cfg), C.byref(w), C.byref(h)), "lf_create")
         self._h = h

@@ -54,6 +54,8 @@ struct lf_handle {
     float2 *rope = nullptr;
     float *qbuf = nullptr, *attn = nullptr, *xattn = nullptr, *hbuf = nullptr, *xout = nullptr, *apart = nullptr;
     int *win = nullptr;            // [L] attention window per layer, or null (every layer: the whole cache)
+    float *wsc = nullptr;          // FP8 weights: copies of the eight per-row scale arrays, back to back
+    size_t wsc_off[8] = {};
     int max_split = 1;
     unsigned *counters = nullptr;  // one allocation: slice counters, attn_done, lm_done, tok_cnt, gbar
     size_t counters_bytes = 0;
@@ -90,7 +92,7 @@ cudaError_t dalloc(T **p, size_t count)
 void free_all(lf_handle *h)
 {
     void *ptrs[] = {h->d_plans, h->wstream, h->kc, h->vc, h->rope, h->qbuf, h->attn, h->xattn, h->hbuf,
-                    h->xout, h->apart, h->win, h->counters, h->lm_part, h->tok_buf, h->tok_seq, h->status,
+                    h->xout, h->apart, h->win, h->wsc, h->counters, h->lm_part, h->tok_buf, h->tok_seq, h->status,
                     h->stage_in, h->stage_out, h->trace};
     for (void *p : ptrs)
         if (p) cudaFree(p);
@@ -119,6 +121,7 @@ lf_status validate_config(const lf_config &c)
     if (c.layer_window)
         for (int l = 0; l < c.n_layers; ++l)
             if (c.layer_window[l] < 0) return LF_ERR_INVALID_ARG;
+    if (c.weight_format != LF_WEIGHTS_FP16 && c.weight_format != LF_WEIGHTS_FP8_E4M3) return LF_ERR_NOT_SUPPORTED;
     return LF_OK;
 }
 
@@ -156,6 +159,7 @@ lfk::Params base_params(lf_handle *h)
     p.xout = h->xout;
     p.apart = h->apart;
     p.win = h->win;
+    for (int i = 0; i < 8; ++i) p.wsc[i] = h->wsc ? h->wsc + h->wsc_off[i] : nullptr;
     p.max_split = h->max_split;
     p.sig = h->sig;
     p.attn_done = h->attn_done;
@@ -258,6 +262,11 @@ lf_status lf_create(const lf_config *cfg, const lf_weights *w, lf_handle **out)
                           w->w_gate, w->w_up, w->w_down, w->final_norm, w->lm_head};
     for (const void *p : need)
         if (!p || (reinterpret_cast<uintptr_t>(p) & 15u)) return LF_ERR_INVALID_ARG;   // bulk copies need 16 B
+    const bool fp8 = cfg->weight_format == LF_WEIGHTS_FP8_E4M3;
+    const float *scales[8] = {w->wq_scale, w->wk_scale, w->wv_scale, w->wo_scale,
+                              w->w_gate_scale, w->w_up_scale, w->w_down_scale, w->lm_head_scale};
+    for (const float *p : scales)
+        if (fp8 ? (!p || (reinterpret_cast<uintptr_t>(p) & 3u)) : p != nullptr) return LF_ERR_INVALID_ARG;
 
     lf_handle *h = new (std::nothrow) lf_handle();
     if (!h) return LF_ERR_OUT_OF_MEMORY;
@@ -277,6 +286,7 @@ lf_status lf_create(const lf_config *cfg, const lf_weights *w, lf_handle **out)
     g.KV = g.Hkv * g.hd;
     g.group = g.Hq / g.Hkv;
     g.max_seq = cfg->max_seq;
+    g.esz = fp8 ? 1 : 2;
 
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -308,11 +318,11 @@ lf_status lf_create(const lf_config *cfg, const lf_weights *w, lf_handle **out)
         for (int s = 0; s < 4; ++s) {
             const lfk::StageGeom sg = lfk::stage_geom(g, s);
             pl.stage_off[s] = off;
-            off += (unsigned long long)(pl.u1[s] - pl.u0[s]) * sg.rows_per_unit * sg.K * 2ull;
+            off += (unsigned long long)(pl.u1[s] - pl.u0[s]) * sg.rows_per_unit * sg.K * (unsigned long long)g.esz;
         }
         pl.layer_bytes = off;
         pl.lm_off = off * (unsigned long long)g.L;
-        const unsigned long long lm_bytes = (unsigned long long)(pl.u1[lfk::ST_LM] - pl.u0[lfk::ST_LM]) * g.d * 2ull;
+        const unsigned long long lm_bytes = (unsigned long long)(pl.u1[lfk::ST_LM] - pl.u0[lfk::ST_LM]) * g.d * (unsigned long long)g.esz;
         pl.base = base;
         base += pl.lm_off + lm_bytes;
         lm_rows_max = std::max(lm_rows_max, pl.u1[lfk::ST_LM] - pl.u0[lfk::ST_LM]);
@@ -369,6 +379,23 @@ lf_status lf_create(const lf_config *cfg, const lf_weights *w, lf_handle **out)
         free_all(h);
         delete h;
         return from_cuda(e);
+    }
+    if (fp8) {
+        const size_t rows[8] = {(size_t)g.L * g.Q, (size_t)g.L * g.KV, (size_t)g.L * g.KV, (size_t)g.L * g.d,
+                                (size_t)g.L * g.F, (size_t)g.L * g.F, (size_t)g.L * g.d, (size_t)g.V};
+        size_t total = 0;
+        for (int i = 0; i < 8; ++i) {
+            h->wsc_off[i] = total;
+            total += rows[i];
+        }
+        e = dalloc(&h->wsc, total);
+        for (int i = 0; i < 8 && e == cudaSuccess; ++i)
+            e = cudaMemcpy(h->wsc + h->wsc_off[i], scales[i], rows[i] * sizeof(float), cudaMemcpyDeviceToDevice);
+        if (e != cudaSuccess) {
+            free_all(h);
+            delete h;
+            return from_cuda(e);
+        }
     }
     bool windowed = false;
     if (cfg->layer_window)

@@ -40,7 +40,10 @@ enum StatusCode { STATUS_OK = 0, STATUS_BAD_TOKEN = 1, STATUS_TIMEOUT = 6 };
 
 struct Geo {
     int L, d, Hq, Hkv, hd, F, V, Q, KV, group, max_seq;
+    int esz;            // bytes of one projection weight: 2 (FP16) or 1 (FP8 E4M3 with per-row FP32 scales)
 };
+// Bytes of one row of one column group (256 weights) of a projection.
+__host__ __device__ inline int chunk_row_bytes(const Geo &g) { return KC * g.esz; }
 
 struct StageGeom {
     int units;          // work units of the stage
@@ -197,6 +200,9 @@ struct Params {
     float *xout;                 // [L][d]   residual after FFN
     float *apart;                // [L][Hq][max_split][hd + 2]  (o[hd], m, l) per piece
     const int *win;              // [L] attention window per layer in positions (0: whole cache), or null
+    // FP8 weights (g.esz == 1): per-row FP32 scales of wq, wk, wv, wo, w_gate,
+    // w_up, w_down, lm_head in the caller's row order ([L][rows], [V])
+    const float *wsc[8];
     int max_split;
     unsigned *sig;               // [L][sig_layout().per_layer] readiness counters
     unsigned *attn_done;         // [L][Hkv] pieces of each KV head that have published

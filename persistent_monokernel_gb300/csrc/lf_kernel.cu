@@ -543,6 +543,27 @@ __device__ __forceinline__ int step_token(const Params &p, int step)
     return t;
 }
 
+// FP32 scale of row `part` of unit `unit` of stage s, layer l (FP8 weights),
+// from the caller's per-row scales.
+__device__ __forceinline__ float row_scale(const Params &p, int s, int l, int unit, int part)
+{
+    const Geo &g = p.g;
+    switch (s) {
+    case ST_QKV: {
+        const int half = g.hd / 2;
+        const int hh = unit / half, j = unit % half;
+        const int r = hh * g.hd + j + part * half;
+        if (r < g.Q) return __ldg(p.wsc[0] + (size_t)l * g.Q + r);
+        if (r < g.Q + g.KV) return __ldg(p.wsc[1] + (size_t)l * g.KV + (r - g.Q));
+        return __ldg(p.wsc[2] + (size_t)l * g.KV + (r - g.Q - g.KV));
+    }
+    case ST_O: return __ldg(p.wsc[3] + (size_t)l * g.d + unit);
+    case ST_GU: return __ldg(p.wsc[part ? 5 : 4] + (size_t)l * g.F + unit);
+    case ST_D: return __ldg(p.wsc[6] + (size_t)l * g.d + unit);
+    default: return __ldg(p.wsc[7] + unit);
+    }
+}
+
 // ---------------------------------------------------------------- loader warp
 
 // Brings each GEMV stage's input into shared memory, one 256-element slice at
@@ -717,6 +738,52 @@ __device__ __forceinline__ void gemv_chunk(const Ctx &c, const uint8_t *ch, int 
     }
 }
 
+// The same for an FP8 chunk (R rows x 256 E4M3 codes, 256 bytes per row): lane
+// l's 8 bytes of row r are decoded pairwise to FP16 (cvt.rn.f16x2.e4m3x2) and
+// then to FP32 before the FMAs; the row's scale is applied to the finished sum.
+__device__ __forceinline__ float2 e4m3x2_f2(unsigned short v)
+{
+    unsigned h;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(v));
+    return __half22float2(*reinterpret_cast<const __half2 *>(&h));
+}
+__device__ __forceinline__ float dot8_fp8(uint2 w, const float4 &xa, const float4 &xb, float acc)
+{
+    const float2 f0 = e4m3x2_f2((unsigned short)(w.x & 0xFFFFu)), f1 = e4m3x2_f2((unsigned short)(w.x >> 16));
+    const float2 f2 = e4m3x2_f2((unsigned short)(w.y & 0xFFFFu)), f3 = e4m3x2_f2((unsigned short)(w.y >> 16));
+    acc = fmaf(f0.x, xa.x, acc);
+    acc = fmaf(f0.y, xa.y, acc);
+    acc = fmaf(f1.x, xa.z, acc);
+    acc = fmaf(f1.y, xa.w, acc);
+    acc = fmaf(f2.x, xb.x, acc);
+    acc = fmaf(f2.y, xb.y, acc);
+    acc = fmaf(f3.x, xb.z, acc);
+    acc = fmaf(f3.y, xb.w, acc);
+    return acc;
+}
+__device__ __forceinline__ uint2 lds_u2(uint32_t a)
+{
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ void gemv_chunk_fp8(const Ctx &c, const uint8_t *ch, int R, const float4 &xa, const float4 &xb,
+                                               float (&acc)[TILE_ROWS])
+{
+    constexpr uint32_t RB = KC;                        // bytes of one row
+    const uint32_t a0 = smem_u32(ch) + (uint32_t)c.lane * 8u;
+#pragma unroll
+    for (int rb = 0; rb < TILE_ROWS; rb += 8) {
+        if (rb < R) {
+            uint2 wv[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) wv[r] = lds_u2(a0 + (uint32_t)(rb + r) * RB);
+#pragma unroll
+            for (int r = 0; r < 8; ++r) acc[rb + r] = dot8_fp8(wv[r], xa, xb, acc[rb + r]);
+        }
+    }
+}
+
 // Sum each of 32 per-lane values over the warp; afterwards lane r holds the
 // sum of value r (31 shuffles: each level hands half of the values to the
 // partner lane).
@@ -744,6 +811,7 @@ __device__ __forceinline__ float2 h2f(unsigned w) { return __half22float2(*reint
 // RMSNorm sum (tile 0 covers every slice once) and applies the gain.  After
 // each tile the warp reduces its 32 row sums over the lanes and hands them to
 // the reducer through a rotating partial-sum buffer.
+template <int ESZ>
 __device__ __forceinline__ bool stage_gemv(const Ctx &c, ConsRing &rc, PipeState &ps, int s, int l, int step, bool ab)
 {
     const Params &p = *c.p;
@@ -773,7 +841,7 @@ __device__ __forceinline__ bool stage_gemv(const Ctx &c, ConsRing &rc, PipeState
         int a, bnd;
         tile_range(u0, n, nt, t, a, bnd);
         const int R = (bnd - a) * sg.rows_per_unit;
-        const unsigned bytes = (unsigned)R * KC_BYTES;
+        const unsigned bytes = (unsigned)R * (unsigned)(KC * ESZ);
         float acc[TILE_ROWS];
 #pragma unroll
         for (int r = 0; r < TILE_ROWS; ++r) acc[r] = 0.f;
@@ -832,7 +900,8 @@ __device__ __forceinline__ bool stage_gemv(const Ctx &c, ConsRing &rc, PipeState
             }
             const uint8_t *ch = rc.acquire(c, bytes, ab);
             if (ab) break;
-            gemv_chunk(c, ch, R, xa, xb, acc);
+            if constexpr (ESZ == 1) gemv_chunk_fp8(c, ch, R, xa, xb, acc);
+            else gemv_chunk(c, ch, R, xa, xb, acc);
             mine = true;
             rc.release_own(c);
             if (in.bufb) {
@@ -905,6 +974,12 @@ __device__ __forceinline__ bool reduce_stage(const Ctx &c, PipeState &ps, int s,
         // the epilogue's other inputs (RoPE row, residual) do not depend on
         // the partials: load them while the consumers finish the tile
         const int u = a + min(c.lane, nu - 1);
+        // FP8 weights: the scales of the lane's rows (pair stages: both rows)
+        float sc0 = 1.f, sc1 = 1.f;
+        if (g.esz == 1) {
+            sc0 = row_scale(p, s, l, u, 0);
+            if (sg.rows_per_unit == 2) sc1 = row_scale(p, s, l, u, 1);
+        }
         float2 pre = make_float2(0.f, 0.f);
         if (s == ST_QKV) {
             const int half = g.hd / 2;
@@ -935,7 +1010,11 @@ __device__ __forceinline__ bool reduce_stage(const Ctx &c, PipeState &ps, int s,
             *reinterpret_cast<volatile unsigned *>(&c.misc[M_TRED + buf]) = use + 1u;
         }
         // ---- epilogue: lane i handles unit a + i (pair stages: rows i and i + nu)
-        const float partner = __shfl_sync(0xffffffffu, sum, (c.lane + nu) & 31);
+        float partner = __shfl_sync(0xffffffffu, sum, (c.lane + nu) & 31);
+        if (g.esz == 1) {
+            sum *= sc0;
+            partner *= sc1;
+        }
         if (c.lane < nu) {
             if (s == ST_QKV) {
                 const int half = g.hd / 2;
@@ -1604,6 +1683,7 @@ __device__ __forceinline__ bool stage_lm_sample(const Ctx &c, int step, bool ab)
 // attention, O, gate/up, down, then the LM head -- through ONE loop body, so
 // that each stage's code exists once in the kernel and stays warm in the
 // instruction cache from one layer to the next.
+template <int ESZ>
 __device__ void consumer(const Ctx &c)
 {
     const Params &p = *c.p;
@@ -1647,7 +1727,7 @@ __device__ void consumer(const Ctx &c)
                 if (p.sched == SCHED_GRID && cons_grid_arrive(c, ab)) return;
                 trace_mark(c, step, k, TR_DONE);
             } else {
-                if (stage_gemv(c, rc, ps, stage_of(sid), l, step, ab)) return;
+                if (stage_gemv<ESZ>(c, rc, ps, stage_of(sid), l, step, ab)) return;
                 if (lm) {
                     // the reducer's keys of every LM-head tile of this CTA
                     bool fail = false;
@@ -1663,24 +1743,27 @@ __device__ void consumer(const Ctx &c)
 // ---------------------------------------------------------------- caller-layout weight rows
 
 struct RepackSrc {
-    const __half *wq, *wk, *wv, *wo, *wg, *wu, *wd, *head;
+    const uint8_t *wq, *wk, *wv, *wo, *wg, *wu, *wd, *head;
 };
 
-__device__ const __half *src_row(const Geo &g, const RepackSrc &w, int s, int l, int unit, int part)
+// Row `part` of unit `unit` of stage s, layer l, in the caller's row-major
+// weights (element size g.esz).
+__device__ const uint8_t *src_row(const Geo &g, const RepackSrc &w, int s, int l, int unit, int part)
 {
+    const size_t e = (size_t)g.esz;
     switch (s) {
     case ST_QKV: {
         const int half = g.hd / 2;
         const int hh = unit / half, j = unit % half;
         const int r = hh * g.hd + j + part * half;  // row of the fused [q; k; v] space
-        if (r < g.Q) return w.wq + ((size_t)l * g.Q + r) * g.d;
-        if (r < g.Q + g.KV) return w.wk + ((size_t)l * g.KV + (r - g.Q)) * g.d;
-        return w.wv + ((size_t)l * g.KV + (r - g.Q - g.KV)) * g.d;
+        if (r < g.Q) return w.wq + ((size_t)l * g.Q + r) * g.d * e;
+        if (r < g.Q + g.KV) return w.wk + ((size_t)l * g.KV + (r - g.Q)) * g.d * e;
+        return w.wv + ((size_t)l * g.KV + (r - g.Q - g.KV)) * g.d * e;
     }
-    case ST_O: return w.wo + ((size_t)l * g.d + unit) * g.Q;
-    case ST_GU: return (part ? w.wu : w.wg) + ((size_t)l * g.F + unit) * g.d;
-    case ST_D: return w.wd + ((size_t)l * g.d + unit) * g.F;
-    default: return w.head + (size_t)unit * g.d;
+    case ST_O: return w.wo + ((size_t)l * g.d + unit) * g.Q * e;
+    case ST_GU: return (part ? w.wu : w.wg) + ((size_t)l * g.F + unit) * g.d * e;
+    case ST_D: return w.wd + ((size_t)l * g.d + unit) * g.F * e;
+    default: return w.head + (size_t)unit * g.d * e;
     }
 }
 
@@ -1699,7 +1782,7 @@ __device__ __forceinline__ bool produce_tiles(const Ctx &c, ProdRing &pr, int s,
         int a, bnd;
         tile_range(u0, n, nt, t, a, bnd);
         const int R = (bnd - a) * sg.rows_per_unit;
-        const unsigned bytes = (unsigned)R * KC_BYTES;
+        const unsigned bytes = (unsigned)R * (unsigned)chunk_row_bytes(p.g);
         const int nch = sg.K / KC;
         for (int k = 0; k < nch; ++k) {
             if (pr.pf_dist)
@@ -1727,7 +1810,7 @@ __device__ __forceinline__ bool produce_tiles_direct(const Ctx &c, ProdRing &pr,
         tile_range(u0, n, nt, t, a, bnd);
         const int nu = bnd - a;
         const int R = nu * sg.rows_per_unit;
-        const unsigned row_bytes = KC_BYTES;
+        const unsigned row_bytes = (unsigned)chunk_row_bytes(p.g);
         const int nch = sg.K / KC;
         for (int k = 0; k < nch; ++k) {
             const int o = pr.reserve(c, (unsigned)R * row_bytes);
@@ -1737,7 +1820,7 @@ __device__ __forceinline__ bool produce_tiles_direct(const Ctx &c, ProdRing &pr,
             for (int r = 0; r < R; ++r) {
                 const int unit = a + (sg.rows_per_unit == 2 ? r % nu : r);
                 const int part = sg.rows_per_unit == 2 ? r / nu : 0;
-                const __half *src = src_row(p.g, w, s, l, unit, part) + (size_t)k * KC;
+                const uint8_t *src = src_row(p.g, w, s, l, unit, part) + (size_t)k * row_bytes;
                 bulk_g2s(c.ring + o + r * row_bytes, src, row_bytes, bar, pr.pol);
             }
             ++pr.n;
@@ -1772,7 +1855,7 @@ __device__ void producer(const Ctx &c, const RepackSrc *w)
         pr.stream_base = p.wstream + pl.base;
         pr.token_bytes = pl.lm_off;
         if (p.mode == MODE_DECODE)
-            pr.token_bytes += (unsigned long long)(pl.u1[ST_LM] - pl.u0[ST_LM]) * g.d * 2ull;
+            pr.token_bytes += (unsigned long long)(pl.u1[ST_LM] - pl.u0[ST_LM]) * g.d * (unsigned long long)g.esz;
         pr.pf_limit = pr.token_bytes * (unsigned long long)p.n_steps;
         pr.pf_dist = (unsigned long long)p.l2_prefetch_bytes;
     }
@@ -1827,7 +1910,7 @@ __device__ void producer(const Ctx &c, const RepackSrc *w)
 
 // ---------------------------------------------------------------- kernel
 
-template <bool kDirect>
+template <bool kDirect, int ESZ>
 __device__ __forceinline__ void monokernel_body(const Params &p, const RepackSrc *w)
 {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -1889,19 +1972,25 @@ __device__ __forceinline__ void monokernel_body(const Params &p, const RepackSrc
         reducer(c);
         return;
     }
-    consumer(c);
+    consumer<ESZ>(c);
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1) lf_monokernel(const __grid_constant__ Params p)
 {
-    monokernel_body<false>(p, nullptr);
+    monokernel_body<false, 2>(p, nullptr);
+}
+
+// The same kernel for FP8 (E4M3) projection weights.
+__global__ void __launch_bounds__(NTHREADS, 1) lf_monokernel_fp8(const __grid_constant__ Params p)
+{
+    monokernel_body<false, 1>(p, nullptr);
 }
 
 // Same kernel, streaming weights from the caller's layout (lf_generate_noalloc).
 __global__ void __launch_bounds__(NTHREADS, 1) lf_monokernel_direct(const __grid_constant__ Params p,
                                                                    const __grid_constant__ RepackSrc w)
 {
-    monokernel_body<true>(p, &w);
+    monokernel_body<true, 2>(p, &w);
 }
 
 // ---------------------------------------------------------------- repack
@@ -1925,17 +2014,18 @@ __global__ void lf_repack_kernel(Geo g, const CtaPlan *plans, RepackSrc w, uint8
                 const int nu = bnd - a;
                 const int R = nu * sg.rows_per_unit;
                 const int nch = sg.K / KC;
+                const int v16 = chunk_row_bytes(g) / 16;   // 16-byte words of one row of a chunk
                 for (int k = 0; k < nch; ++k) {
                     // chunk: R rows x 256 columns, stored row r -> (unit a + r % nu, part r / nu)
-                    for (int q = threadIdx.x; q < R * 32; q += blockDim.x) {
-                        const int r = q / 32, rem = q % 32;
+                    for (int q = threadIdx.x; q < R * v16; q += blockDim.x) {
+                        const int r = q / v16, rem = q % v16;
                         const int unit = a + (sg.rows_per_unit == 2 ? r % nu : r);
                         const int part = sg.rows_per_unit == 2 ? r / nu : 0;
                         const uint4 *srow =
                             reinterpret_cast<const uint4 *>(src_row(g, w, s, l < g.L ? l : 0, unit, part));
-                        reinterpret_cast<uint4 *>(out)[q] = srow[(size_t)k * 32 + rem];
+                        reinterpret_cast<uint4 *>(out)[q] = srow[(size_t)k * v16 + rem];
                     }
-                    out += (size_t)R * KC_BYTES;
+                    out += (size_t)R * chunk_row_bytes(g);
                 }
             }
         }
@@ -1948,18 +2038,20 @@ __global__ void lf_repack_kernel(Geo g, const CtaPlan *plans, RepackSrc w, uint8
 
 extern "C" cudaError_t lfk_set_smem(int smem_bytes)
 {
-    return cudaFuncSetAttribute(lfk::lf_monokernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    cudaError_t e = cudaFuncSetAttribute(lfk::lf_monokernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(lfk::lf_monokernel_fp8, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    return e;
 }
 
 extern "C" cudaError_t lfk_launch_monokernel(const lfk::Params *p, int smem_bytes, cudaStream_t stream,
                                              int cooperative)
 {
     void *args[] = {const_cast<lfk::Params *>(p)};
+    const void *fn = p->g.esz == 1 ? (const void *)lfk::lf_monokernel_fp8 : (const void *)lfk::lf_monokernel;
     if (cooperative)
-        return cudaLaunchCooperativeKernel((const void *)lfk::lf_monokernel, dim3(p->P), dim3(lfk::NTHREADS), args,
-                                           (size_t)smem_bytes, stream);
-    return cudaLaunchKernel((const void *)lfk::lf_monokernel, dim3(p->P), dim3(lfk::NTHREADS), args,
-                            (size_t)smem_bytes, stream);
+        return cudaLaunchCooperativeKernel(fn, dim3(p->P), dim3(lfk::NTHREADS), args, (size_t)smem_bytes, stream);
+    return cudaLaunchKernel(fn, dim3(p->P), dim3(lfk::NTHREADS), args, (size_t)smem_bytes, stream);
 }
 
 extern "C" cudaError_t lfk_occupancy(int smem_bytes, int *blocks_per_sm)
@@ -1979,8 +2071,8 @@ extern "C" cudaError_t lfk_launch_repack(lfk::Geo g, int P, const lfk::CtaPlan *
                                          const void *wv, const void *wo, const void *wg, const void *wu,
                                          const void *wd, const void *head, void *dst, cudaStream_t stream)
 {
-    lfk::RepackSrc w{(const __half *)wq, (const __half *)wk, (const __half *)wv, (const __half *)wo,
-                     (const __half *)wg, (const __half *)wu, (const __half *)wd, (const __half *)head};
+    lfk::RepackSrc w{(const uint8_t *)wq, (const uint8_t *)wk, (const uint8_t *)wv, (const uint8_t *)wo,
+                     (const uint8_t *)wg, (const uint8_t *)wu, (const uint8_t *)wd, (const uint8_t *)head};
     lfk::lf_repack_kernel<<<P, 256, 0, stream>>>(g, plans, w, (uint8_t *)dst);
     return cudaGetLastError();
 }
@@ -1995,8 +2087,8 @@ extern "C" cudaError_t lfk_launch_monokernel_direct(const lfk::Params *p, const 
                                                     const void *wd, const void *head, int smem_bytes,
                                                     cudaStream_t stream)
 {
-    lfk::RepackSrc w{(const __half *)wq, (const __half *)wk, (const __half *)wv, (const __half *)wo,
-                     (const __half *)wg, (const __half *)wu, (const __half *)wd, (const __half *)head};
+    lfk::RepackSrc w{(const uint8_t *)wq, (const uint8_t *)wk, (const uint8_t *)wv, (const uint8_t *)wo,
+                     (const uint8_t *)wg, (const uint8_t *)wu, (const uint8_t *)wd, (const uint8_t *)head};
     void *args[] = {const_cast<lfk::Params *>(p), &w};
     return cudaLaunchCooperativeKernel((const void *)lfk::lf_monokernel_direct, dim3(p->P), dim3(lfk::NTHREADS),
                                        args, (size_t)smem_bytes, stream);

@@ -38,12 +38,21 @@ class ModelConfig:
         per_layer = (self.q_dim + 2 * self.kv_dim) * d + d * self.q_dim + 3 * d * F + 2 * d
         return V * d * 2 + L * per_layer + d
 
-    def weight_bytes_per_token(self) -> int:
-        """FP16 bytes every decode step must stream: all layer matrices and
-        norm gains, the final norm, the LM head and one embedding row."""
+    def weight_bytes_per_token(self, weights: str = "fp16") -> int:
+        """Bytes every decode step must stream: all layer matrices and norm
+        gains, the final norm, the LM head and one embedding row.  FP16
+        throughout, or ("fp8") the eight projection matrices as one byte per
+        weight plus one FP32 scale per row (embedding and gains stay FP16)."""
         L, d, F, V = self.n_layers, self.d_model, self.ffn_dim, self.vocab
-        per_layer = (self.q_dim + 2 * self.kv_dim) * d + d * self.q_dim + 3 * d * F + 2 * d
-        return 2 * (L * per_layer + d + V * d + d)
+        Q, KV = self.q_dim, self.kv_dim
+        if weights == "fp16":
+            per_layer = (Q + 2 * KV) * d + d * Q + 3 * d * F + 2 * d
+            return 2 * (L * per_layer + d + V * d + d)
+        if weights != "fp8":
+            raise ValueError(weights)
+        rows = L * ((Q + 2 * KV) + d + 2 * F + d) + V
+        elems = L * ((Q + 2 * KV) * d + d * Q + 3 * d * F) + V * d
+        return elems + 4 * rows + 2 * (L * 2 * d + d + d)
 
     def kv_bytes_per_position(self) -> int:
         """FP16 K and V bytes of one cached position over all layers."""
@@ -66,6 +75,8 @@ class Workload:
     sample_seed: int = 0
     # None, or one attention window per layer in positions (0 = the whole cache)
     layer_window: tuple | None = None
+    # projection weights: "fp16", or "fp8" (E4M3 codes + FP32 per-row scales)
+    weights: str = "fp16"
 
     @property
     def max_seq(self) -> int:
@@ -83,7 +94,7 @@ class Workload:
             kv_read = ctx * m.kv_bytes_per_position()
         else:
             kv_read = sum(min(ctx, w) if w > 0 else ctx for w in self.layer_window) * per_layer
-        return m.weight_bytes_per_token() + kv_read + m.kv_bytes_per_position()
+        return m.weight_bytes_per_token(self.weights) + kv_read + m.kv_bytes_per_position()
 
     def decode_bytes(self, first_pos: int, n_steps: int) -> int:
         return sum(self.bytes_per_step(first_pos + i) for i in range(n_steps))
@@ -107,6 +118,9 @@ WORKLOADS = {
     "2.3b-32k-swa": Workload("2.3b-32k-swa", MODELS["2.3b"], 2, 1003, 32768, 256,
                              layer_window=tuple(4096 if l % 3 != 2 else 0 for l in range(25))),
     "8b": Workload("8b", MODELS["8b"], 3, 1004, 2048, 512, temperature=0.8, top_k=50, sample_seed=1234),
+    # the ~2.3B decoder with weight-only FP8 projections (the pages: FP8 streaming
+    # halves the bytes that bound batch-1 decode)
+    "2.3b-fp8": Workload("2.3b-fp8", MODELS["2.3b"], 2, 1002, 512, 1024, weights="fp8"),
 }
 
 

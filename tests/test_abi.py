@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(pm):
 
 
 def test_abi_version_and_error_strings(pm):
-    assert pm.lib().lf_abi_version() == 2
+    assert pm.lib().lf_abi_version() == 3
     for code, name in pm.STATUS_NAMES.items():
         assert pm.error_string(code).startswith(name)
 
@@ -68,6 +68,15 @@ def test_create_rejects_bad_arguments_before_touching_the_gpu(pm):
     win = (C.c_int32 * 2)(16, -1)
     cfg = pm.lf_config(**{**good, "layer_window": win})
     assert L.lf_create(C.byref(cfg), C.byref(w), C.byref(h)) == 1
+    # weight formats: unknown -> NOT_SUPPORTED; FP8 needs every scale array, FP16 takes none
+    cfg = pm.lf_config(**{**good, "weight_format": 7})
+    assert L.lf_create(C.byref(cfg), C.byref(w), C.byref(h)) == 7
+    cfg = pm.lf_config(**{**good, "weight_format": pm.WEIGHTS_FP8_E4M3})
+    assert L.lf_create(C.byref(cfg), C.byref(w), C.byref(h)) == 1
+    w8 = pm.lf_weights(*([0x1000] * 12 + [0x2000] * 7 + [0]))
+    assert L.lf_create(C.byref(cfg), C.byref(w8), C.byref(h)) == 1
+    cfg = pm.lf_config(**good)
+    assert L.lf_create(C.byref(cfg), C.byref(w8), C.byref(h)) == 1
 
 
 def test_calls_on_a_null_handle_are_rejected(pm):
