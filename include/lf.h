@@ -44,7 +44,7 @@ extern "C" {
 #define LF_API
 #endif
 
-#define LF_ABI_VERSION 3
+#define LF_ABI_VERSION 4
 #define LF_MAX_TOP_K 64          /* largest top_k that lf_decode accepts (besides 0) */
 
 typedef enum {
@@ -113,6 +113,18 @@ typedef struct {
      * the scale applied to each finished row sum.  The embedding and the norm
      * gains stay FP16.  lf_generate_noalloc takes FP16 weights only. */
     int32_t weight_format;
+    /* Prefill implementation.  0: lf_prefill runs the prompt as repeated
+     * decode steps inside the monokernel (one position per step, the
+     * weights streamed once per position).  B > 0: batched prefill over
+     * blocks of up to B positions (min(B, max_seq)): per layer, the
+     * projections of the whole block as tensor-core GEMMs and a causal
+     * flash-style attention over the cache, the same arithmetic per
+     * position (FP32 activations, FP16 weights and cache).  lf_create then
+     * keeps a row-major FP16 copy of the seven layer projections (FP8
+     * models: the decoded codes; the scales are applied to the sums), a
+     * cuBLAS handle and a workspace that grows with B; lf_info.prefill_bytes
+     * reports them.  lf_generate_noalloc takes 0 only. */
+    int32_t prefill_block;
 } lf_config;
 
 #define LF_WEIGHTS_FP16 0
@@ -186,6 +198,8 @@ typedef struct {
     int32_t schedule;            /* current lf_schedule */
     int64_t weight_stream_bytes; /* bytes of the library's repacked weight copy */
     int64_t kv_cache_bytes;      /* bytes of the FP16 K and V caches */
+    int32_t prefill_block;       /* lf_config.prefill_block as used (0: prefill in the monokernel) */
+    int64_t prefill_bytes;       /* bytes of the batched prefill's weight copy and workspace (0 if off) */
 } lf_info;
 
 /* Validate cfg, allocate the KV cache, activations, counters and the
@@ -194,20 +208,23 @@ typedef struct {
  * repack kernel on the legacy default stream and synchronizes.  On success
  * *out receives a handle with no pending token at position 0.
  * Errors: INVALID_ARG (NULL or not 16-byte aligned weight pointers,
- * non-positive sizes), NOT_SUPPORTED (shape: head_dim other than 64 or 128,
- * d_model, n_heads*head_dim or ffn_dim not a multiple of 256 or above 16384),
- * OUT_OF_MEMORY, NOT_RESIDENT, CUDA. */
+ * non-positive sizes, a negative window or prefill_block), NOT_SUPPORTED
+ * (shape: head_dim other than 64 or 128, d_model, n_heads*head_dim or
+ * ffn_dim not a multiple of 256 or above 16384), OUT_OF_MEMORY,
+ * NOT_RESIDENT, CUDA (also: the cuBLAS handle of the batched prefill could
+ * not be created). */
 LF_API lf_status lf_create(const lf_config *cfg, const lf_weights *weights, lf_handle **out);
 
 /* Release every library-owned allocation.  Synchronizes the device first.
  * Accepts NULL. */
 LF_API void lf_destroy(lf_handle *h);
 
-/* Prefill, implemented as repeated decode steps in one persistent launch:
- * runs the forward pass of the pending token (if any) and of
+/* Prefill: runs the forward pass of the pending token (if any) and of
  * tokens_dev[0 .. n-2] at consecutive positions, appending their K and V to
  * the cache, and makes tokens_dev[n-1] the pending token.  No logits are
- * computed.  tokens_dev: device int32 [n], each in [0, vocab).
+ * computed.  With lf_config.prefill_block = 0 the passes are repeated decode
+ * steps in one persistent launch; with B > 0 they run batched, B positions
+ * per pass (see lf_config.prefill_block), on the same stream.  tokens_dev: device int32 [n], each in [0, vocab).
  * Errors: INVALID_ARG (n < 1, NULL), CAPACITY (not enough positions left for
  * these tokens plus the pending one), STATE (latched device error). */
 LF_API lf_status lf_prefill(lf_handle *h, const int32_t *tokens_dev, int32_t n, void *stream);
@@ -292,7 +309,8 @@ LF_API lf_status lf_read_trace(lf_handle *h, uint64_t *host_out, int64_t capacit
  * calls from two host threads at once, race on the array: serialise them.
  * The call synchronizes `stream` and returns the device status (LF_OK,
  * LF_ERR_TIMEOUT, or LF_ERR_INVALID_ARG for a token id outside [0, vocab)).
- * Other errors: INVALID_ARG, NOT_SUPPORTED, CAPACITY, NOT_RESIDENT, CUDA. */
+ * Other errors: INVALID_ARG, NOT_SUPPORTED (also: FP8 weights, or
+ * prefill_block other than 0), CAPACITY, NOT_RESIDENT, CUDA. */
 LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_weights *w, const int32_t *prompt_dev,
                                      int32_t n_prompt, int32_t n_steps, const lf_sampling *sp, uint64_t seed,
                                      int32_t *out_tokens_dev, void *stream);

@@ -38,7 +38,8 @@ class lf_config(C.Structure):
                 ("n_kv_heads", C.c_int32), ("head_dim", C.c_int32), ("ffn_dim", C.c_int32), ("vocab", C.c_int32),
                 ("max_seq", C.c_int32), ("rope_theta", C.c_float), ("rms_eps", C.c_float),
                 ("wait_timeout_ns", C.c_int64), ("n_ctas", C.c_int32), ("fault_step", C.c_int32),
-                ("layer_window", C.POINTER(C.c_int32)), ("weight_format", C.c_int32)]
+                ("layer_window", C.POINTER(C.c_int32)), ("weight_format", C.c_int32),
+                ("prefill_block", C.c_int32)]
 
 
 WEIGHTS_FP16, WEIGHTS_FP8_E4M3 = 0, 1
@@ -61,7 +62,7 @@ class lf_info(C.Structure):
     _fields_ = [("n_ctas", C.c_int32), ("threads_per_cta", C.c_int32), ("smem_bytes", C.c_int32),
                 ("ring_bytes", C.c_int32), ("sm_count", C.c_int32), ("position", C.c_int32),
                 ("has_pending", C.c_int32), ("schedule", C.c_int32), ("weight_stream_bytes", C.c_int64),
-                ("kv_cache_bytes", C.c_int64)]
+                ("kv_cache_bytes", C.c_int64), ("prefill_block", C.c_int32), ("prefill_bytes", C.c_int64)]
 
 
 _lib = None
@@ -140,7 +141,7 @@ class Decoder:
     """
 
     def __init__(self, model, weights: dict, max_seq: int, n_ctas: int = 0, wait_timeout_ns: int = 0,
-                 fault_step: int = -1, layer_window=None):
+                 fault_step: int = -1, layer_window=None, prefill_block: int = 0):
         import torch
         self.model = model
         self.max_seq = int(max_seq)
@@ -157,7 +158,7 @@ class Decoder:
         cfg = lf_config(model.n_layers, model.d_model, model.n_heads, model.n_kv_heads, model.head_dim,
                         model.ffn_dim, model.vocab, self.max_seq, model.rope_theta, model.rms_eps,
                         int(wait_timeout_ns), int(n_ctas), int(fault_step), _windows(model, layer_window),
-                        WEIGHTS_FP8_E4M3 if self.fp8 else WEIGHTS_FP16)
+                        WEIGHTS_FP8_E4M3 if self.fp8 else WEIGHTS_FP16, int(prefill_block))
         w = lf_weights(*[_dptr(weights[n]) for n in WEIGHT_FIELDS],
                        *[_dptr(weights[n]) if self.fp8 else None for n in SCALE_FIELDS])
         h = C.c_void_p()

@@ -12,6 +12,7 @@
 
 #include "../../include/lf.h"
 #include "lf_internal.cuh"
+#include "lf_prefill.h"
 
 extern "C" cudaError_t lfk_set_smem(int smem_bytes);
 extern "C" cudaError_t lfk_launch_monokernel(const lfk::Params *p, int smem_bytes, cudaStream_t stream,
@@ -79,6 +80,16 @@ struct lf_handle {
     int trace_steps = 0;
     int l2_prefetch_bytes = 0;
     int l2_prefetch_last = 0;
+    // batched prefill (cfg.prefill_block > 0): row-major projection copy,
+    // FP8 row scales in the same layout, workspace, token staging, cuBLAS
+    int pf_block = 0;
+    __half *pf_w = nullptr;
+    float *pf_s = nullptr;
+    uint8_t *pf_ws = nullptr;
+    int *pf_tok = nullptr;
+    void *cublas = nullptr;
+    size_t pf_bytes = 0;
+    size_t pf_woff[4] = {}, pf_soff[4] = {};   // [qkv, o, gu, d] element offsets
 };
 
 namespace {
@@ -93,9 +104,10 @@ void free_all(lf_handle *h)
 {
     void *ptrs[] = {h->d_plans, h->wstream, h->kc, h->vc, h->rope, h->qbuf, h->attn, h->xattn, h->hbuf,
                     h->xout, h->apart, h->win, h->wsc, h->counters, h->lm_part, h->tok_buf, h->tok_seq, h->status,
-                    h->stage_in, h->stage_out, h->trace};
+                    h->stage_in, h->stage_out, h->trace, h->pf_w, h->pf_s, h->pf_ws, h->pf_tok};
     for (void *p : ptrs)
         if (p) cudaFree(p);
+    lfp_cublas_destroy(h->cublas);
 }
 
 lf_status from_cuda(cudaError_t e)
@@ -122,7 +134,71 @@ lf_status validate_config(const lf_config &c)
         for (int l = 0; l < c.n_layers; ++l)
             if (c.layer_window[l] < 0) return LF_ERR_INVALID_ARG;
     if (c.weight_format != LF_WEIGHTS_FP16 && c.weight_format != LF_WEIGHTS_FP8_E4M3) return LF_ERR_NOT_SUPPORTED;
+    if (c.prefill_block < 0) return LF_ERR_INVALID_ARG;
     return LF_OK;
+}
+
+// Batched prefill state: the eight layer projections copied row-major as FP16
+// into four stacked arrays [L, Q+2KV, d] (q, k, v rows), [L, d, Q],
+// [L, 2F, d] (gate rows, then up rows) and [L, d, F] -- FP8 models: the
+// decoded codes, with the row scales gathered into the same row layout --
+// plus the block workspace, a token staging buffer and a cuBLAS handle.
+lf_status setup_prefill(lf_handle *h, const lf_weights *w)
+{
+    const lfk::Geo &g = h->g;
+    h->pf_block = std::min(h->cfg.prefill_block, g.max_seq);
+    const size_t L = g.L, d = g.d, Q = g.Q, KV = g.KV, F = g.F, NQKV = Q + 2 * KV;
+    const size_t wlen[4] = {L * NQKV * d, L * d * Q, L * 2 * F * d, L * d * F};
+    const size_t slen[4] = {L * NQKV, L * d, L * 2 * F, L * d};
+    size_t wt = 0, st = 0;
+    for (int i = 0; i < 4; ++i) {
+        h->pf_woff[i] = wt;
+        h->pf_soff[i] = st;
+        wt += wlen[i];
+        st += slen[i];
+    }
+    const bool fp8 = g.esz == 1;
+    const size_t ws_bytes = lfp_workspace_bytes(g, h->pf_block);
+    cudaError_t e = dalloc(&h->pf_w, wt);
+    if (e == cudaSuccess && fp8) e = dalloc(&h->pf_s, st);
+    if (e == cudaSuccess) e = dalloc(&h->pf_ws, ws_bytes);
+    if (e == cudaSuccess) e = dalloc(&h->pf_tok, (size_t)g.max_seq);
+    if (e != cudaSuccess) return from_cuda(e);
+    h->pf_bytes = wt * sizeof(__half) + (fp8 ? st * sizeof(float) : 0) + ws_bytes + (size_t)g.max_seq * sizeof(int);
+    if (lfp_cublas_create(&h->cublas) != 0) {
+        h->cublas = nullptr;
+        return LF_ERR_CUDA;
+    }
+    // per matrix: source, rows, cols, destination array, row offset inside a layer
+    struct Part {
+        const void *src;
+        size_t rows, cols;
+        int arr;
+        size_t row0;
+    };
+    const Part parts[7] = {{w->wq, Q, d, 0, 0},      {w->wk, KV, d, 0, Q},     {w->wv, KV, d, 0, Q + KV},
+                           {w->wo, d, Q, 1, 0},      {w->w_gate, F, d, 2, 0},  {w->w_up, F, d, 2, F},
+                           {w->w_down, d, F, 3, 0}};
+    const size_t arr_rows[4] = {NQKV, d, 2 * F, d};
+    for (int i = 0; i < 7 && e == cudaSuccess; ++i) {
+        const Part &pt = parts[i];
+        const size_t n = pt.rows * pt.cols;
+        for (size_t l = 0; l < L && e == cudaSuccess; ++l) {
+            __half *dst = h->pf_w + h->pf_woff[pt.arr] + (l * arr_rows[pt.arr] + pt.row0) * pt.cols;
+            if (fp8) {
+                e = lfp_decode_e4m3(static_cast<const uint8_t *>(pt.src) + l * n, dst, n, nullptr);
+                if (e == cudaSuccess)
+                    e = cudaMemcpy(h->pf_s + h->pf_soff[pt.arr] + l * arr_rows[pt.arr] + pt.row0,
+                                   h->wsc + h->wsc_off[i] + l * pt.rows, pt.rows * sizeof(float),
+                                   cudaMemcpyDeviceToDevice);
+            } else {
+                e = cudaMemcpy(dst, static_cast<const __half *>(pt.src) + l * n, n * sizeof(__half),
+                               cudaMemcpyDeviceToDevice);
+            }
+        }
+    }
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    return from_cuda(e);
 }
 
 lf_status launch(lf_handle *h, const lfk::Params &p, cudaStream_t stream)
@@ -443,6 +519,14 @@ lf_status lf_create(const lf_config *cfg, const lf_weights *w, lf_handle **out)
         delete h;
         return from_cuda(e);
     }
+    if (cfg->prefill_block > 0) {
+        st = setup_prefill(h, w);
+        if (st != LF_OK) {
+            free_all(h);
+            delete h;
+            return st;
+        }
+    }
     *out = h;
     return LF_OK;
 }
@@ -462,7 +546,45 @@ lf_status lf_prefill(lf_handle *h, const int32_t *tokens_dev, int32_t n, void *s
     const int steps = (h->has_pending ? 1 : 0) + n - 1;
     if ((long long)h->pos + steps + 1 > h->g.max_seq) return LF_ERR_CAPACITY;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (steps > 0) {
+    if (steps > 0 && h->pf_block > 0) {
+        // batched: the pending token, then tokens_dev[0 .. n-2]
+        const int hp = h->has_pending ? 1 : 0;
+        cudaError_t e = cudaSuccess;
+        if (hp) e = cudaMemcpyAsync(h->pf_tok, h->tok_buf, sizeof(int32_t), cudaMemcpyDeviceToDevice, s);
+        if (e == cudaSuccess && n > 1)
+            e = cudaMemcpyAsync(h->pf_tok + hp, tokens_dev, sizeof(int32_t) * (size_t)(n - 1),
+                                cudaMemcpyDeviceToDevice, s);
+        if (e != cudaSuccess) return from_cuda(e);
+        const lfk::Geo &g = h->g;
+        lfp_args a;
+        a.g = g;
+        a.block = h->pf_block;
+        a.n = steps;
+        a.pos0 = h->pos;
+        a.eps = h->cfg.rms_eps;
+        a.tokens = h->pf_tok;
+        a.embed = h->embed;
+        a.attn_norm = h->attn_norm;
+        a.ffn_norm = h->ffn_norm;
+        a.wqkv = h->pf_w + h->pf_woff[0];
+        a.wo = h->pf_w + h->pf_woff[1];
+        a.wgu = h->pf_w + h->pf_woff[2];
+        a.wd = h->pf_w + h->pf_woff[3];
+        const bool fp8 = h->pf_s != nullptr;
+        a.sqkv = fp8 ? h->pf_s + h->pf_soff[0] : nullptr;
+        a.so = fp8 ? h->pf_s + h->pf_soff[1] : nullptr;
+        a.sgu = fp8 ? h->pf_s + h->pf_soff[2] : nullptr;
+        a.sd = fp8 ? h->pf_s + h->pf_soff[3] : nullptr;
+        a.rope = h->rope;
+        a.win = h->win;
+        a.kc = h->kc;
+        a.vc = h->vc;
+        a.status = h->status;
+        a.cublas = h->cublas;
+        a.ws = lfp_carve(h->pf_ws, g, h->pf_block);
+        if (lfp_run(&a, s) != 0) return LF_ERR_CUDA;
+        h->pos += steps;   // the monokernel's counters and epoch are untouched
+    } else if (steps > 0) {
         lfk::Params p = base_params(h);
         p.mode = lfk::MODE_PREFILL;
         p.n_steps = steps;
@@ -567,6 +689,8 @@ lf_status lf_get_info(const lf_handle *h, lf_info *out)
     out->schedule = h->sched;
     out->weight_stream_bytes = (int64_t)h->wstream_bytes;
     out->kv_cache_bytes = (int64_t)(2ull * h->g.L * h->g.Hkv * (size_t)h->g.max_seq * h->g.hd * 2ull);
+    out->prefill_block = h->pf_block;
+    out->prefill_bytes = (int64_t)h->pf_bytes;
     return LF_OK;
 }
 

@@ -81,7 +81,7 @@ extern "C" LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_w
     if (cfg->d_model > most || (long long)cfg->n_heads * cfg->head_dim > most || cfg->ffn_dim > most)
         return LF_ERR_NOT_SUPPORTED;
     if (sp->top_k < 0 || sp->top_k > LF_MAX_TOP_K) return LF_ERR_NOT_SUPPORTED;
-    if (cfg->weight_format != LF_WEIGHTS_FP16) return LF_ERR_NOT_SUPPORTED;
+    if (cfg->weight_format != LF_WEIGHTS_FP16 || cfg->prefill_block != 0) return LF_ERR_NOT_SUPPORTED;
     if (cfg->layer_window)
         for (int l = 0; l < cfg->n_layers; ++l)
             if (cfg->layer_window[l] < 0) return LF_ERR_INVALID_ARG;

@@ -1,6 +1,6 @@
 // lf_ptx.cuh -- inline-PTX primitives for sm_103a: gpu-scope release/acquire
 // counters, mbarriers, 1-D TMA bulk copies with an L2 eviction hint, the
-// global nanosecond timer, and Philox4x32-10.
+// global nanosecond timer, Philox4x32-10, and warp-level tensor-core fragments.
 #pragma once
 #include <cuda_fp16.h>
 #include <stdint.h>
@@ -228,5 +228,45 @@ __device__ __forceinline__ int sel_key_index(unsigned long long k)
     return (int)(0xFFFFFFFFu - (unsigned)(k & 0xFFFFFFFFull));
 }
 __device__ __forceinline__ float sel_key_value(unsigned long long k) { return order_key_float((unsigned)(k >> 32)); }
+
+// Warp-level tensor-core pieces (mma.sync m16n8k16 FP16 -> FP32, ldmatrix,
+// movmatrix) used by the attention contractions.
+__device__ __forceinline__ void mma16816(float (&d)[4], unsigned a0, unsigned a1, unsigned a2, unsigned a3, unsigned b0,
+                                         unsigned b1)
+{
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+                 "{%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm_x4(unsigned (&r)[4], uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(unsigned (&r)[4], uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+// Transpose of an 8x8 FP16 matrix held as one m8n8 fragment per warp.
+__device__ __forceinline__ unsigned movm_t(unsigned a)
+{
+    unsigned d;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+__device__ __forceinline__ unsigned pack_h2(__half lo, __half hi)
+{
+    return (unsigned)__half_as_ushort(lo) | ((unsigned)__half_as_ushort(hi) << 16);
+}
+// x = head + remainder, both FP16 (head = x rounded, remainder = the rest rounded)
+__device__ __forceinline__ void split_h(float x, __half &hd, __half &rm)
+{
+    hd = __float2half_rn(x);
+    rm = __float2half_rn(x - __half2float(hd));
+}
 
 }  // namespace lfk

@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(pm):
 
 
 def test_abi_version_and_error_strings(pm):
-    assert pm.lib().lf_abi_version() == 3
+    assert pm.lib().lf_abi_version() == 4
     for code, name in pm.STATUS_NAMES.items():
         assert pm.error_string(code).startswith(name)
 
@@ -77,6 +77,20 @@ def test_create_rejects_bad_arguments_before_touching_the_gpu(pm):
     assert L.lf_create(C.byref(cfg), C.byref(w8), C.byref(h)) == 1
     cfg = pm.lf_config(**good)
     assert L.lf_create(C.byref(cfg), C.byref(w8), C.byref(h)) == 1
+    # a negative prefill block
+    cfg = pm.lf_config(**{**good, "prefill_block": -1})
+    assert L.lf_create(C.byref(cfg), C.byref(w), C.byref(h)) == 1
+
+
+def test_noalloc_rejects_batched_prefill_before_touching_the_gpu(pm):
+    L = pm.lib()
+    good = dict(n_layers=2, d_model=256, n_heads=4, n_kv_heads=4, head_dim=64, ffn_dim=1024, vocab=4096,
+                max_seq=64, rope_theta=10000.0, rms_eps=1e-5, wait_timeout_ns=0, n_ctas=0, fault_step=-1,
+                prefill_block=32)
+    cfg = pm.lf_config(**good)
+    w = pm.lf_weights(*([0x1000] * 12))
+    sp = pm.lf_sampling(0.0, 0, None, None)
+    assert L.lf_generate_noalloc(C.byref(cfg), C.byref(w), 0x1000, 8, 4, C.byref(sp), 0, 0x1000, None) == 7
 
 
 def test_calls_on_a_null_handle_are_rejected(pm):
