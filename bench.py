@@ -49,6 +49,8 @@ def parse_args():
     ap.add_argument("--no-ablations", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--prefill-block", type=int, default=1024,
+                    help="positions per batched-prefill pass (0: prefill as repeated decode steps)")
     return ap.parse_args()
 
 
@@ -58,6 +60,30 @@ def kernel_source_hash() -> str:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def bf16_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def prefill_flops(wl, n: int) -> int:
+    """Algorithmic FLOPs of the forward passes at positions 0 .. n-1 without
+    the LM head: 2 per weight of the seven layer projections per position, and
+    4 * head_dim per query head per (query, key) pair attended (Q K^T and P V)."""
+    m = wl.model
+    proj = (m.q_dim + 2 * m.kv_dim) * m.d_model + m.d_model * m.q_dim + 3 * m.d_model * m.ffn_dim
+    pairs = 0
+    for l in range(m.n_layers):
+        w = wl.layer_window[l] if wl.layer_window is not None else 0
+        if w <= 0 or n <= w:
+            pairs += n * (n + 1) // 2
+        else:
+            pairs += w * (w + 1) // 2 + (n - w) * w
+    return 2 * m.n_layers * proj * n + 4 * m.n_heads * m.head_dim * pairs
 
 
 def hbm_peak():
@@ -215,7 +241,7 @@ def run_ours(args):
     max_seq = wl.prompt_len + max(K, W, 128)
     weights = (make_weights_fp8 if wl.weights == "fp8" else make_weights)(cfg, wl.weight_seed, device="cuda")
     prompt = make_prompt(cfg.vocab, wl.prompt_len, wl.prompt_seed).cuda()
-    dec = pm.Decoder(cfg, weights, max_seq, layer_window=wl.layer_window)
+    dec = pm.Decoder(cfg, weights, max_seq, layer_window=wl.layer_window, prefill_block=args.prefill_block)
     info = dec.info()
     stream = torch.cuda.current_stream()
     samp = dict(temperature=wl.temperature, top_k=wl.top_k, seed=wl.sample_seed)
@@ -286,6 +312,8 @@ def run_ours(args):
             "parallelism": f"replicas x{world} (no sharding)",
             "l2": f"inputs larger than L2: {cfg.weight_bytes_per_token(wl.weights) / 1e9:.2f} GB of weights streamed per step",
             "schedule": "monokernel, per-dependency flags",
+            "prefill": f"batched, blocks of {info['prefill_block']} positions" if info["prefill_block"]
+            else "repeated decode steps",
             "grid": f"{info['n_ctas']} CTAs x {info['threads_per_cta']} threads, {info['smem_bytes']} B smem "
                     f"({info['ring_bytes']} B weight ring)",
         },
@@ -307,6 +335,40 @@ def run_ours(args):
         "kernel": "lfk::lf_monokernel (one launch = all K steps)",
     }
     result["clocks"] = clk
+
+    def timed_prefill(d):
+        d.reset()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        d.prefill(prompt)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if d.sync() != 0:
+            raise RuntimeError("prefill failed")
+        return e0.elapsed_time(e1) / 1e3
+
+    # ---- the prompt's prefill (the step before the timed path), timed alone
+    n_pos = wl.prompt_len - 1
+    if rank == 0 and n_pos > 0:
+        reps = 3 if info["prefill_block"] or n_pos <= 4096 else 1
+        t_pf = statistics.median(timed_prefill(dec) for _ in range(reps))
+        tf_peak, tf_kind = bf16_peak()
+        tflops = prefill_flops(wl, n_pos) / t_pf / 1e12
+        result["prefill"] = {
+            "positions": n_pos,
+            "mode": f"batched, blocks of {info['prefill_block']} positions" if info["prefill_block"]
+            else "repeated decode steps in the monokernel",
+            "ms": round(t_pf * 1e3, 3),
+            "positions_per_s": round(n_pos / t_pf, 1),
+            "tflops_algorithmic": round(tflops, 1),
+            "bf16_peak_tflops": tf_peak,
+            "frac": round(tflops / tf_peak, 4),
+            "peak_source": f"{tf_kind} cuBLAS bf16 GEMM (MEASURED_PEAKS.json bf16_tflops)" if tf_kind == "measured"
+            else "fallback 1.9 PFLOP/s",
+            "note": "FP16 tensor-core products with the activations split into an FP16 head and remainder: "
+                    "the tensor work is twice the algorithmic FLOPs",
+        }
 
     if rank == 0 and world == 1 and not args.no_ablations:
         n_ab = min(K, 64)
@@ -341,6 +403,12 @@ def run_ours(args):
             raise RuntimeError("multi-kernel graph ablation failed")
         dec.set_schedule(pm.SCHED_FLAGS)
         ab["launches_per_step_multi_kernel"] = 5 * cfg.n_layers + 1
+        # prefill of the same prompt as repeated decode steps (the monokernel's own path)
+        if info["prefill_block"] and "prefill" in result and n_pos <= 4096:
+            dec0 = pm.Decoder(cfg, weights, max_seq, layer_window=wl.layer_window, prefill_block=0)
+            ab["stepwise_prefill_ms"] = round(timed_prefill(dec0) * 1e3, 3)
+            ab["batched_prefill_speedup"] = round(ab["stepwise_prefill_ms"] / result["prefill"]["ms"], 1)
+            dec0.close()
         result["ablations"] = ab
         # one-hop readiness flag vs grid barrier over the same number of CTAs
         n_ctas = info["n_ctas"]
@@ -369,7 +437,7 @@ def run_ours(args):
             "h2d_bytes_per_step": round(4 * wl.prompt_len / K, 3),
             "d2h_bytes_per_step": 4,
             "what": f"lf_generate with host buffers: prompt upload ({wl.prompt_len} ids), prefill of the prompt "
-                    f"(repeated decode steps), {K} decode steps, token download, synchronize",
+                    f"({result['config']['prefill']}), {K} decode steps, token download, synchronize",
             "request_ms": round(t_e2e * 1e3, 3),
         }
 
