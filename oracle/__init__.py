@@ -82,6 +82,12 @@ def lib():
             L.orc_e4m3_to_float.argtypes = [C.c_uint8]
             L.orc_e4m3_to_float.restype = C.c_float
             L.orc_matvec_fp8.argtypes = [C.POINTER(C.c_uint8), f32p, f32p, C.c_int, C.c_int, f32p]
+            L.orc_set_mxfp4.argtypes = [C.c_void_p, C.POINTER(C.c_void_p)]
+            L.orc_e2m1_to_float.argtypes = [C.c_uint8]
+            L.orc_e2m1_to_float.restype = C.c_float
+            L.orc_e8m0_to_float.argtypes = [C.c_uint8]
+            L.orc_e8m0_to_float.restype = C.c_float
+            L.orc_matvec_mxfp4.argtypes = [C.POINTER(C.c_uint8), C.POINTER(C.c_uint8), f32p, C.c_int, C.c_int, f32p]
             L.orc_pos.argtypes = [C.c_void_p]
             L.orc_pending.argtypes = [C.c_void_p]
             L.orc_kcache.argtypes = [C.c_void_p]
@@ -169,6 +175,26 @@ def matvec_fp8(codes, scale, x):
     return y
 
 
+def e2m1_to_float(nibble: int) -> float:
+    return lib().orc_e2m1_to_float(nibble)
+
+
+def e8m0_to_float(code: int) -> float:
+    return lib().orc_e8m0_to_float(code)
+
+
+def matvec_mxfp4(codes, bscale, x):
+    """y = decode_mxfp4(codes, bscale) . x (codes uint8 [rows, cols/2], two
+    E2M1 elements per byte, low nibble first; bscale uint8 [rows, cols/32])."""
+    Cc = np.ascontiguousarray(_as_np(codes), dtype=np.uint8)
+    Sc = np.ascontiguousarray(_as_np(bscale), dtype=np.uint8)
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    y = np.empty(Cc.shape[0], dtype=np.float32)
+    u8p = C.POINTER(C.c_uint8)
+    lib().orc_matvec_mxfp4(Cc.ctypes.data_as(u8p), Sc.ctypes.data_as(u8p), _f32(x), Cc.shape[0], x.size, _f32(y))
+    return y
+
+
 def rope(v, pos, base):
     v = np.array(v, dtype=np.float32, copy=True)
     lib().orc_rope(_f32(v), v.size, pos, base)
@@ -223,13 +249,17 @@ class OracleDecoder:
         self.cfg = cfg
         self.max_seq = max_seq
         # FP8 weights: the eight projections are uint8 E4M3 codes with FP32
-        # per-row scales in weights["<name>_scale"]
-        self.fp8 = _as_np(weights["wq"]).dtype == np.uint8
+        # per-row scales in weights["<name>_scale"]; MXFP4 weights: packed
+        # E2M1 codes [rows, cols/2] with uint8 E8M0 block scales [rows, cols/32]
+        quant = _as_np(weights["wq"]).dtype == np.uint8
+        self.mxfp4 = quant and _as_np(weights["wq_scale"]).dtype == np.uint8
+        self.fp8 = quant and not self.mxfp4
         self._keep = {}
         for n in _WNAMES:
-            if self.fp8 and n in FP8_MATRICES:
+            if quant and n in FP8_MATRICES:
                 self._keep[n] = np.ascontiguousarray(_as_np(weights[n]), dtype=np.uint8)
-                self._keep[n + "_scale"] = np.ascontiguousarray(_as_np(weights[n + "_scale"]), dtype=np.float32)
+                self._keep[n + "_scale"] = np.ascontiguousarray(_as_np(weights[n + "_scale"]),
+                                                                dtype=np.uint8 if self.mxfp4 else np.float32)
             else:
                 self._keep[n] = _as_u16(weights[n])
         c = _Config(cfg.n_layers, cfg.d_model, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim, cfg.ffn_dim,
@@ -238,9 +268,9 @@ class OracleDecoder:
         self._h = lib().orc_create(C.byref(c), C.byref(w))
         if not self._h:
             raise ValueError("orc_create rejected the configuration")
-        if self.fp8:
+        if quant:
             ptrs = (C.c_void_p * 8)(*[self._keep[n + "_scale"].ctypes.data for n in FP8_MATRICES])
-            lib().orc_set_fp8(self._h, ptrs)
+            (lib().orc_set_mxfp4 if self.mxfp4 else lib().orc_set_fp8)(self._h, ptrs)
         if layer_window is not None:
             win = np.ascontiguousarray(np.asarray(layer_window, dtype=np.int32))
             if win.shape != (cfg.n_layers,):

@@ -134,6 +134,45 @@ ORC_API void orc_matvec_fp8(const uint8_t *C, const float *scale, const float *x
     }
 }
 
+/* MXFP4 (OCP Microscaling FP4; the pages' "FP8/MXFP4" streaming,
+ * shivam2003.com, "Scaling the idea to frontier models").  Elements are E2M1
+ * (1 sign, 2 exponent bits with bias 1, 1 mantissa bit; no infinities or NaN):
+ * exponent field 0 gives the subnormals m * 0.5, so the magnitudes are 0,
+ * 0.5, 1, 1.5, 2, 3, 4 and 6.  Blocks of 32 consecutive elements of a row
+ * share one E8M0 scale, 2^(E - 127), with E = 255 meaning NaN. */
+ORC_API float orc_e2m1_to_float(uint8_t nib)
+{
+    const int s = (nib >> 3) & 1, e = (nib >> 1) & 3, m = nib & 1;
+    const float mag = e == 0 ? 0.5f * (float)m : ldexpf(1.0f + 0.5f * (float)m, e - 1);
+    return s ? -mag : mag;
+}
+ORC_API float orc_e8m0_to_float(uint8_t e)
+{
+    if (e == 255) return NAN;
+    return ldexpf(1.0f, (int)e - 127);
+}
+
+/* y = decode(C, S) . x for an [n_rows, k_dim] MXFP4 matrix: C holds two
+ * elements per byte (element k of a row in the low nibble of byte k/2 for
+ * even k, in the high nibble for odd k), S one E8M0 scale per 32 elements
+ * ([n_rows, k_dim/32]).  Weight (r, k) = e2m1(C) * e8m0(S[r][k/32]), exact in
+ * FP32; each row's dot product with x in FP32, index order. */
+ORC_API void orc_matvec_mxfp4(const uint8_t *C, const uint8_t *S, const float *x, int n_rows, int k_dim, float *y)
+{
+    #pragma omp parallel for schedule(static)
+    for (int r = 0; r < n_rows; ++r) {
+        const uint8_t *row = C + (size_t)r * (size_t)(k_dim / 2);
+        const uint8_t *sc = S + (size_t)r * (size_t)(k_dim / 32);
+        float acc = 0.0f;
+        for (int k = 0; k < k_dim; ++k) {
+            const uint8_t nib = (k & 1) ? (uint8_t)(row[k / 2] >> 4) : (uint8_t)(row[k / 2] & 15);
+            const float w = orc_e2m1_to_float(nib) * orc_e8m0_to_float(sc[k / 32]);
+            acc += w * x[k];
+        }
+        y[r] = acc;
+    }
+}
+
 /* Rotate-half RoPE of one head vector v[hd] at position pos:
  * for i < hd/2, theta_i = pos * base^(-2i/hd) (in double), and
  *   v[i]        <- v[i] cos - v[i+hd/2] sin
@@ -298,6 +337,10 @@ typedef struct {
      * w_up, w_down, lm_head); fp8 = 0: FP16 weights */
     int fp8;
     const float *scale[8];
+    /* MXFP4 weights: the eight projection pointers hold packed E2M1 codes and
+     * bscale[i] the E8M0 block scales of matrix i ([rows, cols/32]) */
+    int mxfp4;
+    const uint8_t *bscale[8];
     /* activations */
     float *x, *xn, *q, *k, *v, *attn, *tmp, *gate, *up, *hbuf, *scores;
 } orc_model;
@@ -353,13 +396,22 @@ ORC_API void orc_set_fp8(orc_model *m, const float *const *scales)
     for (int i = 0; i < 8; ++i) m->scale[i] = scales ? scales[i] : NULL;
 }
 
+/* Switch the model to MXFP4 weights (see orc_model); NULL switches back. */
+ORC_API void orc_set_mxfp4(orc_model *m, const uint8_t *const *bscales)
+{
+    m->mxfp4 = bscales != NULL;
+    for (int i = 0; i < 8; ++i) m->bscale[i] = bscales ? bscales[i] : NULL;
+}
+
 /* Projection `which` (0 wq .. 7 lm_head) of layer l: y = W x. */
 static void orc_project(const orc_model *m, int which, int l, int n_rows, int k_dim, const float *x, float *y)
 {
     const orc_weights *w = &m->w;
     const uint16_t *base[8] = {w->wq, w->wk, w->wv, w->wo, w->w_gate, w->w_up, w->w_down, w->lm_head};
     const size_t off = (size_t)l * (size_t)n_rows * (size_t)k_dim;
-    if (m->fp8)
+    if (m->mxfp4)
+        orc_matvec_mxfp4((const uint8_t *)base[which] + off / 2, m->bscale[which] + off / 32, x, n_rows, k_dim, y);
+    else if (m->fp8)
         orc_matvec_fp8((const uint8_t *)base[which] + off, m->scale[which] + (size_t)l * n_rows, x, n_rows, k_dim, y);
     else
         orc_matvec(base[which] + off, x, n_rows, k_dim, y);

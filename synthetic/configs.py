@@ -41,18 +41,23 @@ class ModelConfig:
     def weight_bytes_per_token(self, weights: str = "fp16") -> int:
         """Bytes every decode step must stream: all layer matrices and norm
         gains, the final norm, the LM head and one embedding row.  FP16
-        throughout, or ("fp8") the eight projection matrices as one byte per
-        weight plus one FP32 scale per row (embedding and gains stay FP16)."""
+        throughout, or the eight projection matrices as ("fp8") one byte per
+        weight plus one FP32 scale per row, or ("mxfp4") half a byte per
+        weight plus one scale byte per 32 weights (embedding and gains stay
+        FP16)."""
         L, d, F, V = self.n_layers, self.d_model, self.ffn_dim, self.vocab
         Q, KV = self.q_dim, self.kv_dim
         if weights == "fp16":
             per_layer = (Q + 2 * KV) * d + d * Q + 3 * d * F + 2 * d
             return 2 * (L * per_layer + d + V * d + d)
-        if weights != "fp8":
-            raise ValueError(weights)
         rows = L * ((Q + 2 * KV) + d + 2 * F + d) + V
         elems = L * ((Q + 2 * KV) * d + d * Q + 3 * d * F) + V * d
-        return elems + 4 * rows + 2 * (L * 2 * d + d + d)
+        if weights == "fp8":
+            return elems + 4 * rows + 2 * (L * 2 * d + d + d)
+        if weights == "mxfp4":
+            # half a byte per element plus one E8M0 scale byte per 32 elements
+            return elems // 2 + elems // 32 + 2 * (L * 2 * d + d + d)
+        raise ValueError(weights)
 
     def kv_bytes_per_position(self) -> int:
         """FP16 K and V bytes of one cached position over all layers."""
@@ -75,7 +80,8 @@ class Workload:
     sample_seed: int = 0
     # None, or one attention window per layer in positions (0 = the whole cache)
     layer_window: tuple | None = None
-    # projection weights: "fp16", or "fp8" (E4M3 codes + FP32 per-row scales)
+    # projection weights: "fp16", "fp8" (E4M3 codes + FP32 per-row scales) or
+    # "mxfp4" (E2M1 codes + E8M0 scales per 32 elements)
     weights: str = "fp16"
 
     @property
@@ -121,6 +127,8 @@ WORKLOADS = {
     # the ~2.3B decoder with weight-only FP8 projections (the pages: FP8 streaming
     # halves the bytes that bound batch-1 decode)
     "2.3b-fp8": Workload("2.3b-fp8", MODELS["2.3b"], 2, 1002, 512, 1024, weights="fp8"),
+    # the same with MXFP4 projections (the pages: "FP8/MXFP4" for frontier models)
+    "2.3b-mxfp4": Workload("2.3b-mxfp4", MODELS["2.3b"], 2, 1002, 512, 1024, weights="mxfp4"),
 }
 
 

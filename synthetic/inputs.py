@@ -189,6 +189,63 @@ def make_weights_fp8(cfg: ModelConfig, seed: int, device="cpu", gains: str = "on
     return w
 
 
+# MXFP4 codes: each byte holds two 4-bit codes (sign bit 3, magnitude code
+# 0..7 in bits 0-2).  Magnitude codes are drawn with these frequencies (in
+# 128ths), a bell-shaped spread over the code range; signs are even.
+_MXFP4_MAG_FREQ = (24, 32, 26, 18, 14, 9, 4, 1)
+_MXFP4_TABLE_CACHE: dict = {}
+
+
+def mxfp4_byte_table() -> torch.Tensor:
+    """uint8 table of 65,536 bytes: index bits 0-6 pick the low code's
+    magnitude bucket, bit 7 its sign, bits 8-14 / 15 the same for the high code."""
+    if "t" not in _MXFP4_TABLE_CACHE:
+        bucket = []
+        for code, f in enumerate(_MXFP4_MAG_FREQ):
+            bucket += [code] * f
+        assert len(bucket) == 128
+        t = torch.empty(65536, dtype=torch.uint8)
+        for k in range(65536):
+            lo = bucket[k & 127] | (8 if k & 128 else 0)
+            hi = bucket[(k >> 8) & 127] | (8 if k & 32768 else 0)
+            t[k] = lo | (hi << 4)
+        _MXFP4_TABLE_CACHE["t"] = t
+    return _MXFP4_TABLE_CACHE["t"]
+
+
+def _fill_block_scales(out: torch.Tensor, seed: int, tensor_id: int, layer: int) -> None:
+    """E8M0 block scales 121 + {-1, 0, +1} (2^-7 .. 2^-5), seeded per element."""
+    idx = hashed_indices(seed, 0x200 + tensor_id, layer, 0, out.numel(), out.device)
+    out.copy_((120 + idx % 3).to(torch.uint8).view(out.shape))
+
+
+def make_weights_mxfp4(cfg: ModelConfig, seed: int, device="cpu", gains: str = "ones") -> dict:
+    """A decoder whose eight projection matrices are MXFP4: packed 4-bit E2M1
+    codes (uint8 [.., rows, cols/2], element 2i in the low nibble of byte i)
+    with one E8M0 scale byte per 32 elements of a row (`<name>_scale`, uint8
+    [.., rows, cols/32]); the embedding and the norm gains stay FP16."""
+    w = make_weights(cfg, seed, device=device, gains=gains, projections=False)
+    device = torch.device(device)
+    table = mxfp4_byte_table().to(device)
+    L, d, F, V, Q, KV = cfg.n_layers, cfg.d_model, cfg.ffn_dim, cfg.vocab, cfg.q_dim, cfg.kv_dim
+    shapes = {"wq": (L, Q, d), "wk": (L, KV, d), "wv": (L, KV, d), "wo": (L, d, Q), "w_gate": (L, F, d),
+              "w_up": (L, F, d), "w_down": (L, d, F), "lm_head": (V, d)}
+    for name in FP8_MATRICES:
+        shp = shapes[name]
+        codes = torch.empty(shp[:-1] + (shp[-1] // 2,), dtype=torch.uint8, device=device)
+        scales = torch.empty(shp[:-1] + (shp[-1] // 32,), dtype=torch.uint8, device=device)
+        if len(shp) == 3:
+            for layer in range(shp[0]):
+                _fill(codes[layer], table, seed, _TENSOR_ID[name], layer)
+                _fill_block_scales(scales[layer], seed, _TENSOR_ID[name], layer)
+        else:
+            _fill(codes, table, seed, _TENSOR_ID[name], 0)
+            _fill_block_scales(scales, seed, _TENSOR_ID[name], 0)
+        w[name] = codes
+        w[name + "_scale"] = scales
+    return w
+
+
 def make_prompt(vocab: int, n: int, seed: int, device="cpu") -> torch.Tensor:
     """n token ids, uniform on [0, vocab) (up to a 2**-32 modulo bias), int32."""
     k1, k2 = _stream_key(seed, 0x50524F4D, 0)  # tensor id "PROM"
