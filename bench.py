@@ -182,8 +182,9 @@ def workload_desc(wl, K):
         ws = sorted({w for w in wl.layer_window if w > 0})
         nwin = sum(1 for w in wl.layer_window if w > 0)
         win = f"; sliding-window attention (window {'/'.join(map(str, ws))}) in {nwin} of {m.n_layers} layers"
-    wdesc = ("FP8 E4M3 projection weights with FP32 per-row scales (~N(0,0.02) after scaling)"
-             if wl.weights == "fp8" else "FP16 weights ~N(0,0.02)")
+    wdesc = {"fp8": "FP8 E4M3 projection weights with FP32 per-row scales (~N(0,0.02) after scaling)",
+             "mxfp4": "MXFP4 projection weights (E2M1 codes, E8M0 scale per 32 weights, 2^-7..2^-5)"
+             }.get(wl.weights, "FP16 weights ~N(0,0.02)")
     return (f"{wl.name}: {m.n_layers} layers, d_model {m.d_model}, {m.n_heads}/{m.n_kv_heads} heads x {m.head_dim}, "
             f"SwiGLU FFN {m.ffn_dim}, vocab {m.vocab}, {wdesc}{win}; prompt {wl.prompt_len}, "
             f"{K} decode steps ({samp})")
@@ -219,7 +220,7 @@ def run_ours(args):
 
     import persistent_monokernel_gb300 as pm
     from persistent_monokernel_gb300 import build as pm_build
-    from synthetic import WORKLOADS, make_prompt, make_weights, make_weights_fp8
+    from synthetic import WORKLOADS, make_prompt, make_weights, make_weights_fp8, make_weights_mxfp4
 
     world, rank, local = dist_setup()
     if world != args.gpus:
@@ -239,9 +240,12 @@ def run_ours(args):
     K = args.steps or wl.decode_steps
     W = max(3, args.warmup)
     max_seq = wl.prompt_len + max(K, W, 128)
-    weights = (make_weights_fp8 if wl.weights == "fp8" else make_weights)(cfg, wl.weight_seed, device="cuda")
+    mk = {"fp8": make_weights_fp8, "mxfp4": make_weights_mxfp4}.get(wl.weights, make_weights)
+    weights = mk(cfg, wl.weight_seed, device="cuda")
     prompt = make_prompt(cfg.vocab, wl.prompt_len, wl.prompt_seed).cuda()
-    dec = pm.Decoder(cfg, weights, max_seq, layer_window=wl.layer_window, prefill_block=args.prefill_block)
+    # MXFP4 handles prefill as monokernel steps only
+    pf_block = 0 if wl.weights == "mxfp4" else args.prefill_block
+    dec = pm.Decoder(cfg, weights, max_seq, layer_window=wl.layer_window, prefill_block=pf_block)
     info = dec.info()
     stream = torch.cuda.current_stream()
     samp = dict(temperature=wl.temperature, top_k=wl.top_k, seed=wl.sample_seed)
@@ -303,7 +307,8 @@ def run_ours(args):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "f32",
-        "weights_dtype": "fp8_e4m3 (FP32 per-row scales)" if wl.weights == "fp8" else "fp16",
+        "weights_dtype": {"fp8": "fp8_e4m3 (FP32 per-row scales)", "mxfp4": "mxfp4 (e2m1, e8m0 per 32)"
+                          }.get(wl.weights, "fp16"),
         "data": "synthetic: seeded FP16 weights ~N(0,0.02), seeded uniform prompt ids",
         "config": {
             "workload": workload_desc(wl, K),
@@ -471,7 +476,7 @@ def run_reference(args):
         return
     import torch
 
-    from synthetic import WORKLOADS, make_prompt, make_weights, make_weights_fp8
+    from synthetic import WORKLOADS, make_prompt, make_weights, make_weights_fp8, make_weights_mxfp4
     import oracle
 
     oracle.build()
@@ -480,7 +485,7 @@ def run_reference(args):
     K = args.steps or wl.decode_steps
     W = max(3, args.warmup)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    mk = make_weights_fp8 if wl.weights == "fp8" else make_weights
+    mk = {"fp8": make_weights_fp8, "mxfp4": make_weights_mxfp4}.get(wl.weights, make_weights)
     wc = {k: v.cpu() for k, v in mk(cfg, wl.weight_seed, device=dev).items()}
     pr = make_prompt(cfg.vocab, 8, wl.prompt_seed).numpy()
     tok_s, n, dt, threads = time_oracle(cfg, wc, pr, budget_s=60.0, max_steps=K, warmup=min(W, 3),

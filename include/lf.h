@@ -44,7 +44,7 @@ extern "C" {
 #define LF_API
 #endif
 
-#define LF_ABI_VERSION 4
+#define LF_ABI_VERSION 5
 #define LF_MAX_TOP_K 64          /* largest top_k that lf_decode accepts (besides 0) */
 
 typedef enum {
@@ -110,8 +110,14 @@ typedef struct {
      * models"), one byte per weight in OCP E4M3 (no infinities, 448 largest)
      * and one FP32 scale per output row in the lf_weights *_scale arrays; the
      * matrix applied is diag(scale) . decode(codes), dot products in FP32 with
-     * the scale applied to each finished row sum.  The embedding and the norm
-     * gains stay FP16.  lf_generate_noalloc takes FP16 weights only. */
+     * the scale applied to each finished row sum.  Or LF_WEIGHTS_MXFP4 (2):
+     * OCP Microscaling FP4 (the pages' "FP8/MXFP4", same section), two E2M1
+     * elements per byte (element 2i in the low nibble of byte i; magnitudes
+     * 0, 0.5, 1, 1.5, 2, 3, 4, 6) and one E8M0 scale byte, 2^(E-127), per 32
+     * consecutive elements of a row in the *_scale arrays; weight (r, k) =
+     * e2m1 * 2^(E-127), dot products in FP32.  The embedding and the norm
+     * gains stay FP16.  lf_generate_noalloc takes FP16 weights only; MXFP4
+     * handles take prefill_block = 0 only. */
     int32_t weight_format;
     /* Prefill implementation.  0: lf_prefill runs the prompt as repeated
      * decode steps inside the monokernel (one position per step, the
@@ -129,10 +135,13 @@ typedef struct {
 
 #define LF_WEIGHTS_FP16 0
 #define LF_WEIGHTS_FP8_E4M3 1
+#define LF_WEIGHTS_MXFP4 2
 
 /* Device pointers to the caller's weights (row-major, stacked over layers):
  * FP16, or for lf_config.weight_format = LF_WEIGHTS_FP8_E4M3 the eight
- * projections as E4M3 bytes with FP32 per-row scales.  L = n_layers,
+ * projections as E4M3 bytes with FP32 per-row scales, or for
+ * LF_WEIGHTS_MXFP4 as packed E2M1 codes ([.., rows, cols/2] bytes) with E8M0
+ * block scales ([.., rows, cols/32] bytes).  L = n_layers,
  * d = d_model, Q = n_heads*head_dim, KV = n_kv_heads*head_dim, F = ffn_dim,
  * V = vocab.  lf_create copies the projection matrices, the LM head and the
  * scales into library-owned memory (a per-CTA streaming layout for the
@@ -140,7 +149,7 @@ typedef struct {
  * the three norm-gain tensors are read in place by every decode step and must
  * outlive the handle.  Every matrix pointer must be 16-byte aligned (the
  * kernels read them with bulk copies); the scale pointers are NULL for FP16
- * weights and 4-byte aligned otherwise. */
+ * weights, 4-byte aligned for FP8 and any byte address for MXFP4. */
 typedef struct {
     const void *embed;       /* [V, d]      read in place */
     const void *attn_norm;   /* [L, d]      read in place */
@@ -154,15 +163,17 @@ typedef struct {
     const void *w_down;      /* [L, d, F]   copied */
     const void *final_norm;  /* [d]         read in place */
     const void *lm_head;     /* [V, d]      copied (untied from embed) */
-    /* FP8 weights only: FP32 scale of every row of the matrix of the same name */
-    const float *wq_scale;      /* [L, Q]  */
-    const float *wk_scale;      /* [L, KV] */
-    const float *wv_scale;      /* [L, KV] */
-    const float *wo_scale;      /* [L, d]  */
-    const float *w_gate_scale;  /* [L, F]  */
-    const float *w_up_scale;    /* [L, F]  */
-    const float *w_down_scale;  /* [L, d]  */
-    const float *lm_head_scale; /* [V]     */
+    /* FP8: FP32 scale of every row of the matrix of the same name (shapes
+     * below); MXFP4: uint8 E8M0 scale of every 32 elements of a row (the
+     * shapes below with a last dimension of cols/32); FP16: NULL */
+    const void *wq_scale;      /* [L, Q]  */
+    const void *wk_scale;      /* [L, KV] */
+    const void *wv_scale;      /* [L, KV] */
+    const void *wo_scale;      /* [L, d]  */
+    const void *w_gate_scale;  /* [L, F]  */
+    const void *w_up_scale;    /* [L, F]  */
+    const void *w_down_scale;  /* [L, d]  */
+    const void *lm_head_scale; /* [V]     */
 } lf_weights;
 
 /* Token choice, after the Gumbel-max trick of shivam2003.com ("The fused
@@ -210,7 +221,8 @@ typedef struct {
  * Errors: INVALID_ARG (NULL or not 16-byte aligned weight pointers,
  * non-positive sizes, a negative window or prefill_block), NOT_SUPPORTED
  * (shape: head_dim other than 64 or 128, d_model, n_heads*head_dim or
- * ffn_dim not a multiple of 256 or above 16384), OUT_OF_MEMORY,
+ * ffn_dim not a multiple of 256 or above 16384; an unknown weight_format;
+ * MXFP4 with prefill_block > 0), OUT_OF_MEMORY,
  * NOT_RESIDENT, CUDA (also: the cuBLAS handle of the batched prefill could
  * not be created). */
 LF_API lf_status lf_create(const lf_config *cfg, const lf_weights *weights, lf_handle **out);
@@ -309,7 +321,7 @@ LF_API lf_status lf_read_trace(lf_handle *h, uint64_t *host_out, int64_t capacit
  * calls from two host threads at once, race on the array: serialise them.
  * The call synchronizes `stream` and returns the device status (LF_OK,
  * LF_ERR_TIMEOUT, or LF_ERR_INVALID_ARG for a token id outside [0, vocab)).
- * Other errors: INVALID_ARG, NOT_SUPPORTED (also: FP8 weights, or
+ * Other errors: INVALID_ARG, NOT_SUPPORTED (also: FP8 or MXFP4 weights, or
  * prefill_block other than 0), CAPACITY, NOT_RESIDENT, CUDA. */
 LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_weights *w, const int32_t *prompt_dev,
                                      int32_t n_prompt, int32_t n_steps, const lf_sampling *sp, uint64_t seed,

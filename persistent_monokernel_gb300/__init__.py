@@ -42,7 +42,7 @@ class lf_config(C.Structure):
                 ("prefill_block", C.c_int32)]
 
 
-WEIGHTS_FP16, WEIGHTS_FP8_E4M3 = 0, 1
+WEIGHTS_FP16, WEIGHTS_FP8_E4M3, WEIGHTS_MXFP4 = 0, 1, 2
 WEIGHT_FIELDS = ("embed", "attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down",
                  "final_norm", "lm_head")
 FP8_MATRICES = ("wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down", "lm_head")
@@ -145,22 +145,30 @@ class Decoder:
         import torch
         self.model = model
         self.max_seq = int(max_seq)
-        # FP8 weights: the eight projections as uint8 E4M3 codes plus FP32 per-row scales
-        self.fp8 = weights["wq"].dtype == torch.uint8
-        for n in WEIGHT_FIELDS + (SCALE_FIELDS if self.fp8 else ()):
+        # FP8 weights: the eight projections as uint8 E4M3 codes plus FP32 per-row scales;
+        # MXFP4 weights: packed uint8 E2M1 codes plus uint8 E8M0 scales per 32 elements
+        quant = weights["wq"].dtype == torch.uint8
+        self.mxfp4 = quant and weights["wq_scale"].dtype == torch.uint8
+        self.fp8 = quant and not self.mxfp4
+        for n in WEIGHT_FIELDS + (SCALE_FIELDS if quant else ()):
             t = weights[n]
-            want = (torch.uint8 if n in FP8_MATRICES else torch.float32 if n in SCALE_FIELDS else torch.float16) \
-                if self.fp8 else torch.float16
+            if not quant or n not in FP8_MATRICES + SCALE_FIELDS:
+                want = torch.float16
+            elif n in FP8_MATRICES or self.mxfp4:
+                want = torch.uint8
+            else:
+                want = torch.float32
             if not (t.is_cuda and t.dtype == want and t.is_contiguous()):
                 raise ValueError(f"weight {n} must be a contiguous CUDA {want} tensor")
+        fmt = WEIGHTS_MXFP4 if self.mxfp4 else WEIGHTS_FP8_E4M3 if self.fp8 else WEIGHTS_FP16
         # embed and the norm gains are read in place by every step: keep them alive
         self._keep = {n: weights[n] for n in ("embed", "attn_norm", "ffn_norm", "final_norm")}
         cfg = lf_config(model.n_layers, model.d_model, model.n_heads, model.n_kv_heads, model.head_dim,
                         model.ffn_dim, model.vocab, self.max_seq, model.rope_theta, model.rms_eps,
                         int(wait_timeout_ns), int(n_ctas), int(fault_step), _windows(model, layer_window),
-                        WEIGHTS_FP8_E4M3 if self.fp8 else WEIGHTS_FP16, int(prefill_block))
+                        fmt, int(prefill_block))
         w = lf_weights(*[_dptr(weights[n]) for n in WEIGHT_FIELDS],
-                       *[_dptr(weights[n]) if self.fp8 else None for n in SCALE_FIELDS])
+                       *[_dptr(weights[n]) if quant else None for n in SCALE_FIELDS])
         h = C.c_void_p()
         _check(lib().lf_create(C.byref(cfg), C.byref(w), C.byref(h)), "lf_create")
         self._h = h

@@ -19,6 +19,8 @@ extern "C" cudaError_t lfk_launch_monokernel(const lfk::Params *p, int smem_byte
                                              int cooperative);
 extern "C" cudaError_t lfk_occupancy(int smem_bytes, int *blocks_per_sm);
 extern "C" unsigned lfk_smem_bytes(int ring_bytes, int a_floats, int b_slots, int d, int lm_rows_max, int L);
+extern "C" cudaError_t lfk_launch_mxfp4_interleave(const void *codes, const void *scales, size_t rows, int cols,
+                                                   void *out, cudaStream_t stream);
 extern "C" cudaError_t lfk_launch_repack(lfk::Geo g, int P, const lfk::CtaPlan *plans, const void *wq,
                                          const void *wk, const void *wv, const void *wo, const void *wg,
                                          const void *wu, const void *wd, const void *head, void *dst,
@@ -133,8 +135,11 @@ lf_status validate_config(const lf_config &c)
     if (c.layer_window)
         for (int l = 0; l < c.n_layers; ++l)
             if (c.layer_window[l] < 0) return LF_ERR_INVALID_ARG;
-    if (c.weight_format != LF_WEIGHTS_FP16 && c.weight_format != LF_WEIGHTS_FP8_E4M3) return LF_ERR_NOT_SUPPORTED;
+    if (c.weight_format != LF_WEIGHTS_FP16 && c.weight_format != LF_WEIGHTS_FP8_E4M3 &&
+        c.weight_format != LF_WEIGHTS_MXFP4)
+        return LF_ERR_NOT_SUPPORTED;
     if (c.prefill_block < 0) return LF_ERR_INVALID_ARG;
+    if (c.weight_format == LF_WEIGHTS_MXFP4 && c.prefill_block > 0) return LF_ERR_NOT_SUPPORTED;
     return LF_OK;
 }
 
@@ -157,7 +162,7 @@ lf_status setup_prefill(lf_handle *h, const lf_weights *w)
         wt += wlen[i];
         st += slen[i];
     }
-    const bool fp8 = g.esz == 1;
+    const bool fp8 = g.fmt == lfk::FMT_FP8;
     const size_t ws_bytes = lfp_workspace_bytes(g, h->pf_block);
     cudaError_t e = dalloc(&h->pf_w, wt);
     if (e == cudaSuccess && fp8) e = dalloc(&h->pf_s, st);
@@ -339,10 +344,17 @@ lf_status lf_create(const lf_config *cfg, const lf_weights *w, lf_handle **out)
     for (const void *p : need)
         if (!p || (reinterpret_cast<uintptr_t>(p) & 15u)) return LF_ERR_INVALID_ARG;   // bulk copies need 16 B
     const bool fp8 = cfg->weight_format == LF_WEIGHTS_FP8_E4M3;
-    const float *scales[8] = {w->wq_scale, w->wk_scale, w->wv_scale, w->wo_scale,
-                              w->w_gate_scale, w->w_up_scale, w->w_down_scale, w->lm_head_scale};
-    for (const float *p : scales)
-        if (fp8 ? (!p || (reinterpret_cast<uintptr_t>(p) & 3u)) : p != nullptr) return LF_ERR_INVALID_ARG;
+    const bool mxfp4 = cfg->weight_format == LF_WEIGHTS_MXFP4;
+    const void *scales_v[8] = {w->wq_scale, w->wk_scale, w->wv_scale, w->wo_scale,
+                               w->w_gate_scale, w->w_up_scale, w->w_down_scale, w->lm_head_scale};
+    const float *scales[8];
+    for (int i = 0; i < 8; ++i) {
+        const void *p = scales_v[i];
+        scales[i] = static_cast<const float *>(p);
+        // FP8: FP32 row scales (4-byte aligned); MXFP4: E8M0 block scales (bytes); FP16: none
+        if (fp8 ? (!p || (reinterpret_cast<uintptr_t>(p) & 3u)) : mxfp4 ? !p : p != nullptr)
+            return LF_ERR_INVALID_ARG;
+    }
 
     lf_handle *h = new (std::nothrow) lf_handle();
     if (!h) return LF_ERR_OUT_OF_MEMORY;
@@ -362,7 +374,8 @@ lf_status lf_create(const lf_config *cfg, const lf_weights *w, lf_handle **out)
     g.KV = g.Hkv * g.hd;
     g.group = g.Hq / g.Hkv;
     g.max_seq = cfg->max_seq;
-    g.esz = fp8 ? 1 : 2;
+    g.fmt = fp8 ? lfk::FMT_FP8 : mxfp4 ? lfk::FMT_MXFP4 : lfk::FMT_FP16;
+    g.crb = lfk::fmt_crb(g.fmt);
 
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -394,11 +407,13 @@ lf_status lf_create(const lf_config *cfg, const lf_weights *w, lf_handle **out)
         for (int s = 0; s < 4; ++s) {
             const lfk::StageGeom sg = lfk::stage_geom(g, s);
             pl.stage_off[s] = off;
-            off += (unsigned long long)(pl.u1[s] - pl.u0[s]) * sg.rows_per_unit * sg.K * (unsigned long long)g.esz;
+            off += (unsigned long long)(pl.u1[s] - pl.u0[s]) * sg.rows_per_unit * (sg.K / lfk::KC) *
+                   (unsigned long long)g.crb;
         }
         pl.layer_bytes = off;
         pl.lm_off = off * (unsigned long long)g.L;
-        const unsigned long long lm_bytes = (unsigned long long)(pl.u1[lfk::ST_LM] - pl.u0[lfk::ST_LM]) * g.d * (unsigned long long)g.esz;
+        const unsigned long long lm_bytes =
+            (unsigned long long)(pl.u1[lfk::ST_LM] - pl.u0[lfk::ST_LM]) * (g.d / lfk::KC) * (unsigned long long)g.crb;
         pl.base = base;
         base += pl.lm_off + lm_bytes;
         lm_rows_max = std::max(lm_rows_max, pl.u1[lfk::ST_LM] - pl.u0[lfk::ST_LM]);
@@ -509,9 +524,27 @@ lf_status lf_create(const lf_config *cfg, const lf_weights *w, lf_handle **out)
     if (e == cudaSuccess) e = cudaMemset(h->counters, 0, h->counters_bytes);
     if (e == cudaSuccess) e = cudaMemset(h->status, 0, 8 * sizeof(unsigned));
     if (e == cudaSuccess) e = cudaMemset(h->tok_buf, 0, sizeof(int));
-    if (e == cudaSuccess)
+    if (e == cudaSuccess && !mxfp4)
         e = lfk_launch_repack(g, P, h->d_plans, w->wq, w->wk, w->wv, w->wo, w->w_gate, w->w_up, w->w_down,
                               w->lm_head, h->wstream, nullptr);
+    if (e == cudaSuccess && mxfp4) {
+        // codes and block scales -> rows of 144-byte column groups (temporary), then the usual repack
+        const void *codes[8] = {w->wq, w->wk, w->wv, w->wo, w->w_gate, w->w_up, w->w_down, w->lm_head};
+        const size_t rows[8] = {(size_t)g.L * g.Q, (size_t)g.L * g.KV, (size_t)g.L * g.KV, (size_t)g.L * g.d,
+                                (size_t)g.L * g.F, (size_t)g.L * g.F, (size_t)g.L * g.d, (size_t)g.V};
+        const int cols[8] = {g.d, g.d, g.d, g.Q, g.d, g.d, g.F, g.d};
+        uint8_t *tmp[8] = {};
+        for (int i = 0; i < 8 && e == cudaSuccess; ++i) {
+            e = dalloc(&tmp[i], rows[i] * (size_t)(cols[i] / lfk::KC) * (size_t)g.crb);
+            if (e == cudaSuccess) e = lfk_launch_mxfp4_interleave(codes[i], scales_v[i], rows[i], cols[i], tmp[i], nullptr);
+        }
+        if (e == cudaSuccess)
+            e = lfk_launch_repack(g, P, h->d_plans, tmp[0], tmp[1], tmp[2], tmp[3], tmp[4], tmp[5], tmp[6], tmp[7],
+                                  h->wstream, nullptr);
+        if (e == cudaSuccess) e = cudaDeviceSynchronize();
+        for (uint8_t *t : tmp)
+            if (t) cudaFree(t);
+    }
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e == cudaSuccess) e = lfk_set_smem(h->smem_bytes);
     if (e != cudaSuccess) {

@@ -38,12 +38,22 @@ enum Mode { MODE_PREFILL = 0, MODE_DECODE = 1 };
 enum Sched { SCHED_FLAGS = 0, SCHED_GRID = 1, SCHED_MULTI = 2 };
 enum StatusCode { STATUS_OK = 0, STATUS_BAD_TOKEN = 1, STATUS_TIMEOUT = 6 };
 
+// Formats of the projection weights in the per-CTA streams.  One row of one
+// column group (256 weights) of a chunk takes fmt_crb(fmt) bytes: FP16 512; FP8
+// E4M3 256 (per-row FP32 scales applied in the epilogue); MXFP4 144 = 128 bytes
+// of packed E2M1 codes (element 2i in the low nibble of byte i), the E8M0
+// scales of the group's eight 32-element blocks, and 8 bytes of padding that
+// keep every chunk a multiple of 16 bytes for the bulk copies.
+enum WeightFmt { FMT_FP16 = 0, FMT_FP8 = 1, FMT_MXFP4 = 2 };
+__host__ __device__ constexpr int fmt_crb(int fmt) { return fmt == FMT_FP16 ? 512 : fmt == FMT_FP8 ? 256 : 144; }
+
 struct Geo {
     int L, d, Hq, Hkv, hd, F, V, Q, KV, group, max_seq;
-    int esz;            // bytes of one projection weight: 2 (FP16) or 1 (FP8 E4M3 with per-row FP32 scales)
+    int fmt;            // WeightFmt of the eight projections
+    int crb;            // fmt_crb(fmt)
 };
-// Bytes of one row of one column group (256 weights) of a projection.
-__host__ __device__ inline int chunk_row_bytes(const Geo &g) { return KC * g.esz; }
+// Bytes of one row of one column group (256 weights) of a projection in the stream.
+__host__ __device__ inline int chunk_row_bytes(const Geo &g) { return g.crb; }
 
 struct StageGeom {
     int units;          // work units of the stage
@@ -200,7 +210,7 @@ struct Params {
     float *xout;                 // [L][d]   residual after FFN
     float *apart;                // [L][Hq][max_split][hd + 2]  (o[hd], m, l) per piece
     const int *win;              // [L] attention window per layer in positions (0: whole cache), or null
-    // FP8 weights (g.esz == 1): per-row FP32 scales of wq, wk, wv, wo, w_gate,
+    // FP8 weights (g.fmt == FMT_FP8): per-row FP32 scales of wq, wk, wv, wo, w_gate,
     // w_up, w_down, lm_head in the caller's row order ([L][rows], [V])
     const float *wsc[8];
     int max_split;

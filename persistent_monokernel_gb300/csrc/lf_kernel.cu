@@ -34,6 +34,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "lf_internal.cuh"
 #include "lf_ptx.cuh"
 
@@ -784,6 +786,80 @@ __device__ __forceinline__ void gemv_chunk_fp8(const Ctx &c, const uint8_t *ch, 
     }
 }
 
+// The same for an MXFP4 chunk (R rows x 144 bytes: 128 bytes of packed E2M1
+// codes, then the E8M0 scales of the row's eight 32-column blocks): lane l's
+// 4 code bytes (columns 8l..8l+7, one quarter of block l/4) are decoded
+// pairwise to FP16 (cvt.rn.f16x2.e2m1x2, exact), multiplied with x in FP32,
+// and the lane's partial sum is scaled by its block's 2^(E-127) (exact) before
+// it joins the row's accumulator.
+__device__ __forceinline__ void e2m1x8_h2(unsigned w, unsigned &h0, unsigned &h1, unsigned &h2, unsigned &h3)
+{
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(h0), "=r"(h1), "=r"(h2), "=r"(h3)
+        : "r"(w));
+}
+// 2^(e - 127) for an E8M0 byte: the FP32 with that exponent field (e = 0:
+// the subnormal 2^-127; e = 255: NaN).
+__device__ __forceinline__ float e8m0_f(unsigned e)
+{
+    return e == 0u ? __uint_as_float(0x00400000u) : e == 255u ? __uint_as_float(0x7FC00000u) : __uint_as_float(e << 23);
+}
+__device__ __forceinline__ float dot8_mxfp4(unsigned w, unsigned sc, const float4 &xa, const float4 &xb, float acc)
+{
+    unsigned h0, h1, h2, h3;
+    e2m1x8_h2(w, h0, h1, h2, h3);
+    const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&h0));
+    const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&h1));
+    const float2 f2 = __half22float2(*reinterpret_cast<const __half2 *>(&h2));
+    const float2 f3 = __half22float2(*reinterpret_cast<const __half2 *>(&h3));
+    float part = f0.x * xa.x;
+    part = fmaf(f0.y, xa.y, part);
+    part = fmaf(f1.x, xa.z, part);
+    part = fmaf(f1.y, xa.w, part);
+    part = fmaf(f2.x, xb.x, part);
+    part = fmaf(f2.y, xb.y, part);
+    part = fmaf(f3.x, xb.z, part);
+    part = fmaf(f3.y, xb.w, part);
+    return fmaf(part, e8m0_f(sc), acc);
+}
+__device__ __forceinline__ unsigned lds_u32(uint32_t a)
+{
+    unsigned v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ unsigned lds_u8(uint32_t a)
+{
+    unsigned short v;
+    asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ void gemv_chunk_mxfp4(const Ctx &c, const uint8_t *ch, int R, const float4 &xa,
+                                                 const float4 &xb, float (&acc)[TILE_ROWS])
+{
+    constexpr uint32_t RB = fmt_crb(FMT_MXFP4);        // bytes of one row
+    const uint32_t a0 = smem_u32(ch) + (uint32_t)c.lane * 4u;
+    const uint32_t s0 = smem_u32(ch) + 128u + (uint32_t)(c.lane >> 2);
+#pragma unroll
+    for (int rb = 0; rb < TILE_ROWS; rb += 8) {
+        if (rb < R) {
+            unsigned wv[8], sv[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                wv[r] = lds_u32(a0 + (uint32_t)(rb + r) * RB);
+                sv[r] = lds_u8(s0 + (uint32_t)(rb + r) * RB);
+            }
+#pragma unroll
+            for (int r = 0; r < 8; ++r) acc[rb + r] = dot8_mxfp4(wv[r], sv[r], xa, xb, acc[rb + r]);
+        }
+    }
+}
+
 // Sum each of 32 per-lane values over the warp; afterwards lane r holds the
 // sum of value r (31 shuffles: each level hands half of the values to the
 // partner lane).
@@ -811,7 +887,7 @@ __device__ __forceinline__ float2 h2f(unsigned w) { return __half22float2(*reint
 // RMSNorm sum (tile 0 covers every slice once) and applies the gain.  After
 // each tile the warp reduces its 32 row sums over the lanes and hands them to
 // the reducer through a rotating partial-sum buffer.
-template <int ESZ>
+template <int FMT>
 __device__ __forceinline__ bool stage_gemv(const Ctx &c, ConsRing &rc, PipeState &ps, int s, int l, int step, bool ab)
 {
     const Params &p = *c.p;
@@ -841,7 +917,7 @@ __device__ __forceinline__ bool stage_gemv(const Ctx &c, ConsRing &rc, PipeState
         int a, bnd;
         tile_range(u0, n, nt, t, a, bnd);
         const int R = (bnd - a) * sg.rows_per_unit;
-        const unsigned bytes = (unsigned)R * (unsigned)(KC * ESZ);
+        const unsigned bytes = (unsigned)R * (unsigned)fmt_crb(FMT);
         float acc[TILE_ROWS];
 #pragma unroll
         for (int r = 0; r < TILE_ROWS; ++r) acc[r] = 0.f;
@@ -900,7 +976,8 @@ __device__ __forceinline__ bool stage_gemv(const Ctx &c, ConsRing &rc, PipeState
             }
             const uint8_t *ch = rc.acquire(c, bytes, ab);
             if (ab) break;
-            if constexpr (ESZ == 1) gemv_chunk_fp8(c, ch, R, xa, xb, acc);
+            if constexpr (FMT == FMT_FP8) gemv_chunk_fp8(c, ch, R, xa, xb, acc);
+            else if constexpr (FMT == FMT_MXFP4) gemv_chunk_mxfp4(c, ch, R, xa, xb, acc);
             else gemv_chunk(c, ch, R, xa, xb, acc);
             mine = true;
             rc.release_own(c);
@@ -976,7 +1053,7 @@ __device__ __forceinline__ bool reduce_stage(const Ctx &c, PipeState &ps, int s,
         const int u = a + min(c.lane, nu - 1);
         // FP8 weights: the scales of the lane's rows (pair stages: both rows)
         float sc0 = 1.f, sc1 = 1.f;
-        if (g.esz == 1) {
+        if (g.fmt == FMT_FP8) {
             sc0 = row_scale(p, s, l, u, 0);
             if (sg.rows_per_unit == 2) sc1 = row_scale(p, s, l, u, 1);
         }
@@ -1011,7 +1088,7 @@ __device__ __forceinline__ bool reduce_stage(const Ctx &c, PipeState &ps, int s,
         }
         // ---- epilogue: lane i handles unit a + i (pair stages: rows i and i + nu)
         float partner = __shfl_sync(0xffffffffu, sum, (c.lane + nu) & 31);
-        if (g.esz == 1) {
+        if (g.fmt == FMT_FP8) {
             sum *= sc0;
             partner *= sc1;
         }
@@ -1645,7 +1722,7 @@ __device__ __forceinline__ bool stage_lm_sample(const Ctx &c, int step, bool ab)
 // attention, O, gate/up, down, then the LM head -- through ONE loop body, so
 // that each stage's code exists once in the kernel and stays warm in the
 // instruction cache from one layer to the next.
-template <int ESZ>
+template <int FMT>
 __device__ void consumer(const Ctx &c)
 {
     const Params &p = *c.p;
@@ -1689,7 +1766,7 @@ __device__ void consumer(const Ctx &c)
                 if (p.sched == SCHED_GRID && cons_grid_arrive(c, ab)) return;
                 trace_mark(c, step, k, TR_DONE);
             } else {
-                if (stage_gemv<ESZ>(c, rc, ps, stage_of(sid), l, step, ab)) return;
+                if (stage_gemv<FMT>(c, rc, ps, stage_of(sid), l, step, ab)) return;
                 if (lm) {
                     // the reducer's keys of every LM-head tile of this CTA
                     bool fail = false;
@@ -1709,23 +1786,24 @@ struct RepackSrc {
 };
 
 // Row `part` of unit `unit` of stage s, layer l, in the caller's row-major
-// weights (element size g.esz).
+// weights, or for MXFP4 in the chunk-interleaved copy lf_create builds: a row
+// of `cols` columns takes cols / 256 * g.crb bytes either way.
 __device__ const uint8_t *src_row(const Geo &g, const RepackSrc &w, int s, int l, int unit, int part)
 {
-    const size_t e = (size_t)g.esz;
+    const size_t rd = (size_t)(g.d / KC) * g.crb, rq = (size_t)(g.Q / KC) * g.crb, rf = (size_t)(g.F / KC) * g.crb;
     switch (s) {
     case ST_QKV: {
         const int half = g.hd / 2;
         const int hh = unit / half, j = unit % half;
         const int r = hh * g.hd + j + part * half;  // row of the fused [q; k; v] space
-        if (r < g.Q) return w.wq + ((size_t)l * g.Q + r) * g.d * e;
-        if (r < g.Q + g.KV) return w.wk + ((size_t)l * g.KV + (r - g.Q)) * g.d * e;
-        return w.wv + ((size_t)l * g.KV + (r - g.Q - g.KV)) * g.d * e;
+        if (r < g.Q) return w.wq + ((size_t)l * g.Q + r) * rd;
+        if (r < g.Q + g.KV) return w.wk + ((size_t)l * g.KV + (r - g.Q)) * rd;
+        return w.wv + ((size_t)l * g.KV + (r - g.Q - g.KV)) * rd;
     }
-    case ST_O: return w.wo + ((size_t)l * g.d + unit) * g.Q * e;
-    case ST_GU: return (part ? w.wu : w.wg) + ((size_t)l * g.F + unit) * g.d * e;
-    case ST_D: return w.wd + ((size_t)l * g.d + unit) * g.F * e;
-    default: return w.head + (size_t)unit * g.d * e;
+    case ST_O: return w.wo + ((size_t)l * g.d + unit) * rq;
+    case ST_GU: return (part ? w.wu : w.wg) + ((size_t)l * g.F + unit) * rd;
+    case ST_D: return w.wd + ((size_t)l * g.d + unit) * rf;
+    default: return w.head + (size_t)unit * rd;
     }
 }
 
@@ -1817,7 +1895,7 @@ __device__ void producer(const Ctx &c, const RepackSrc *w)
         pr.stream_base = p.wstream + pl.base;
         pr.token_bytes = pl.lm_off;
         if (p.mode == MODE_DECODE)
-            pr.token_bytes += (unsigned long long)(pl.u1[ST_LM] - pl.u0[ST_LM]) * g.d * (unsigned long long)g.esz;
+            pr.token_bytes += (unsigned long long)(pl.u1[ST_LM] - pl.u0[ST_LM]) * (g.d / KC) * (unsigned long long)g.crb;
         pr.pf_limit = pr.token_bytes * (unsigned long long)p.n_steps;
         pr.pf_dist = (unsigned long long)p.l2_prefetch_bytes;
     }
@@ -1872,7 +1950,7 @@ __device__ void producer(const Ctx &c, const RepackSrc *w)
 
 // ---------------------------------------------------------------- kernel
 
-template <bool kDirect, int ESZ>
+template <bool kDirect, int FMT>
 __device__ __forceinline__ void monokernel_body(const Params &p, const RepackSrc *w)
 {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -1934,25 +2012,31 @@ __device__ __forceinline__ void monokernel_body(const Params &p, const RepackSrc
         reducer(c);
         return;
     }
-    consumer<ESZ>(c);
+    consumer<FMT>(c);
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1) lf_monokernel(const __grid_constant__ Params p)
 {
-    monokernel_body<false, 2>(p, nullptr);
+    monokernel_body<false, FMT_FP16>(p, nullptr);
 }
 
 // The same kernel for FP8 (E4M3) projection weights.
 __global__ void __launch_bounds__(NTHREADS, 1) lf_monokernel_fp8(const __grid_constant__ Params p)
 {
-    monokernel_body<false, 1>(p, nullptr);
+    monokernel_body<false, FMT_FP8>(p, nullptr);
+}
+
+// The same kernel for MXFP4 projection weights.
+__global__ void __launch_bounds__(NTHREADS, 1) lf_monokernel_mxfp4(const __grid_constant__ Params p)
+{
+    monokernel_body<false, FMT_MXFP4>(p, nullptr);
 }
 
 // Same kernel, streaming weights from the caller's layout (lf_generate_noalloc).
 __global__ void __launch_bounds__(NTHREADS, 1) lf_monokernel_direct(const __grid_constant__ Params p,
                                                                    const __grid_constant__ RepackSrc w)
 {
-    monokernel_body<true, 2>(p, &w);
+    monokernel_body<true, FMT_FP16>(p, &w);
 }
 
 // ---------------------------------------------------------------- repack
@@ -1994,6 +2078,33 @@ __global__ void lf_repack_kernel(Geo g, const CtaPlan *plans, RepackSrc w, uint8
     }
 }
 
+// MXFP4: one matrix ([rows, cols] elements: codes [rows, cols/2], E8M0 scales
+// [rows, cols/32]) rewritten as rows of cols/256 groups of 144 bytes (128
+// code bytes, 8 scale bytes, 8 zero bytes), the row layout the repack copies
+// into the streams.  One thread per 16 output bytes.
+__global__ void lf_mxfp4_interleave_kernel(const uint8_t *codes, const uint8_t *scales, size_t rows, int cols,
+                                           uint8_t *out)
+{
+    const int ng = cols / KC;
+    const size_t n16 = rows * (size_t)ng * 9;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (size_t)gridDim.x * blockDim.x) {
+        const size_t rg = i / 9;
+        const int q = (int)(i % 9);
+        const size_t r = rg / ng;
+        const int gidx = (int)(rg % ng);
+        uint4 v;
+        if (q < 8) {
+            v = *reinterpret_cast<const uint4 *>(codes + r * (size_t)(cols / 2) + (size_t)gidx * 128 + q * 16);
+        } else {
+            const uint8_t *sp = scales + r * (size_t)(cols / 32) + (size_t)gidx * 8;
+            uint8_t b[16] = {};
+            for (int k = 0; k < 8; ++k) b[k] = sp[k];
+            v = *reinterpret_cast<const uint4 *>(b);
+        }
+        *reinterpret_cast<uint4 *>(out + i * 16) = v;
+    }
+}
+
 }  // namespace lfk
 
 // ---------------------------------------------------------------- launch hooks used by lf_api.cu
@@ -2003,6 +2114,8 @@ extern "C" cudaError_t lfk_set_smem(int smem_bytes)
     cudaError_t e = cudaFuncSetAttribute(lfk::lf_monokernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(lfk::lf_monokernel_fp8, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(lfk::lf_monokernel_mxfp4, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     return e;
 }
 
@@ -2010,7 +2123,9 @@ extern "C" cudaError_t lfk_launch_monokernel(const lfk::Params *p, int smem_byte
                                              int cooperative)
 {
     void *args[] = {const_cast<lfk::Params *>(p)};
-    const void *fn = p->g.esz == 1 ? (const void *)lfk::lf_monokernel_fp8 : (const void *)lfk::lf_monokernel;
+    const void *fn = p->g.fmt == lfk::FMT_FP8     ? (const void *)lfk::lf_monokernel_fp8
+                     : p->g.fmt == lfk::FMT_MXFP4 ? (const void *)lfk::lf_monokernel_mxfp4
+                                                  : (const void *)lfk::lf_monokernel;
     if (cooperative)
         return cudaLaunchCooperativeKernel(fn, dim3(p->P), dim3(lfk::NTHREADS), args, (size_t)smem_bytes, stream);
     return cudaLaunchKernel(fn, dim3(p->P), dim3(lfk::NTHREADS), args, (size_t)smem_bytes, stream);
@@ -2054,4 +2169,15 @@ extern "C" cudaError_t lfk_launch_monokernel_direct(const lfk::Params *p, const 
     void *args[] = {const_cast<lfk::Params *>(p), &w};
     return cudaLaunchCooperativeKernel((const void *)lfk::lf_monokernel_direct, dim3(p->P), dim3(lfk::NTHREADS),
                                        args, (size_t)smem_bytes, stream);
+}
+
+extern "C" cudaError_t lfk_launch_mxfp4_interleave(const void *codes, const void *scales, size_t rows, int cols,
+                                                   void *out, cudaStream_t stream)
+{
+    const size_t n16 = rows * (size_t)(cols / lfk::KC) * 9;
+    const int grid = (int)std::min<size_t>((n16 + 255) / 256, 8192);
+    lfk::lf_mxfp4_interleave_kernel<<<grid, 256, 0, stream>>>(static_cast<const uint8_t *>(codes),
+                                                              static_cast<const uint8_t *>(scales), rows, cols,
+                                                              static_cast<uint8_t *>(out));
+    return cudaGetLastError();
 }

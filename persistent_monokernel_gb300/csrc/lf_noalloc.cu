@@ -99,7 +99,8 @@ extern "C" LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_w
     g.KV = g.Hkv * g.hd;
     g.group = g.Hq / g.Hkv;
     g.max_seq = cfg->max_seq;
-    g.esz = 2;
+    g.fmt = lfk::FMT_FP16;
+    g.crb = lfk::fmt_crb(lfk::FMT_FP16);
 
     // ---- device, grid and the static partition (as lf_create)
     int dev = 0, sm = 0, optin = 0;

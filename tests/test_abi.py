@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(pm):
 
 
 def test_abi_version_and_error_strings(pm):
-    assert pm.lib().lf_abi_version() == 4
+    assert pm.lib().lf_abi_version() == 5
     for code, name in pm.STATUS_NAMES.items():
         assert pm.error_string(code).startswith(name)
 
@@ -80,6 +80,13 @@ def test_create_rejects_bad_arguments_before_touching_the_gpu(pm):
     # a negative prefill block
     cfg = pm.lf_config(**{**good, "prefill_block": -1})
     assert L.lf_create(C.byref(cfg), C.byref(w), C.byref(h)) == 1
+    # MXFP4: every block-scale pointer is needed (any byte address); no batched prefill
+    cfg = pm.lf_config(**{**good, "weight_format": pm.WEIGHTS_MXFP4})
+    assert L.lf_create(C.byref(cfg), C.byref(w), C.byref(h)) == 1
+    w4 = pm.lf_weights(*([0x1000] * 12 + [0x2001] * 7 + [0]))
+    assert L.lf_create(C.byref(cfg), C.byref(w4), C.byref(h)) == 1
+    cfg = pm.lf_config(**{**good, "weight_format": pm.WEIGHTS_MXFP4, "prefill_block": 16})
+    assert L.lf_create(C.byref(cfg), C.byref(w), C.byref(h)) == 7
 
 
 def test_noalloc_rejects_batched_prefill_before_touching_the_gpu(pm):
