@@ -83,6 +83,8 @@ def lib():
             L.orc_e4m3_to_float.restype = C.c_float
             L.orc_matvec_fp8.argtypes = [C.POINTER(C.c_uint8), f32p, f32p, C.c_int, C.c_int, f32p]
             L.orc_set_mxfp4.argtypes = [C.c_void_p, C.POINTER(C.c_void_p)]
+            L.orc_set_moe.argtypes = [C.c_void_p, C.c_int, C.c_int, u16p]
+            L.orc_route.argtypes = [f32p, C.c_int, C.c_int, C.POINTER(C.c_int32), f32p]
             L.orc_e2m1_to_float.argtypes = [C.c_uint8]
             L.orc_e2m1_to_float.restype = C.c_float
             L.orc_e8m0_to_float.argtypes = [C.c_uint8]
@@ -195,6 +197,15 @@ def matvec_mxfp4(codes, bscale, x):
     return y
 
 
+def route(logits, top_k: int):
+    """Top-k expert choice of one token: (experts in decreasing logit order, gates)."""
+    lg = np.ascontiguousarray(logits, dtype=np.float32)
+    sel = np.empty(top_k, dtype=np.int32)
+    gate = np.empty(top_k, dtype=np.float32)
+    lib().orc_route(_f32(lg), lg.size, top_k, _i32(sel), _f32(gate))
+    return sel, gate
+
+
 def rope(v, pos, base):
     v = np.array(v, dtype=np.float32, copy=True)
     lib().orc_rope(_f32(v), v.size, pos, base)
@@ -271,6 +282,13 @@ class OracleDecoder:
         if quant:
             ptrs = (C.c_void_p * 8)(*[self._keep[n + "_scale"].ctypes.data for n in FP8_MATRICES])
             (lib().orc_set_mxfp4 if self.mxfp4 else lib().orc_set_fp8)(self._h, ptrs)
+        # mixture-of-experts FFN: w_gate / w_up [L, E, F, d], w_down [L, E, d, F], w_router [L, E, d]
+        self.n_experts = int(getattr(cfg, "n_experts", 0) or 0)
+        if self.n_experts:
+            self._keep["w_router"] = _as_u16(weights["w_router"])
+            if lib().orc_set_moe(self._h, self.n_experts, int(cfg.top_k_experts),
+                                 _u16(self._keep["w_router"])):
+                raise ValueError("orc_set_moe rejected the expert configuration")
         if layer_window is not None:
             win = np.ascontiguousarray(np.asarray(layer_window, dtype=np.int32))
             if win.shape != (cfg.n_layers,):

@@ -341,6 +341,13 @@ typedef struct {
      * bscale[i] the E8M0 block scales of matrix i ([rows, cols/32]) */
     int mxfp4;
     const uint8_t *bscale[8];
+    /* Mixture-of-experts FFN: n_experts = E > 0 experts per layer, top_k of
+     * them active per token; w_gate / w_up are then [L, E, F, d], w_down
+     * [L, E, d, F] (F = ffn_dim per expert) and router [L, E, d] */
+    int n_experts, top_k;
+    const uint16_t *router;
+    float *ffn_acc;     /* [d] */
+    float *rlogit;      /* [E] */
     /* activations */
     float *x, *xn, *q, *k, *v, *attn, *tmp, *gate, *up, *hbuf, *scores;
 } orc_model;
@@ -376,6 +383,7 @@ ORC_API orc_model *orc_create(const orc_config *c, const orc_weights *w)
 ORC_API void orc_destroy(orc_model *m)
 {
     if (!m) return;
+    free(m->ffn_acc); free(m->rlogit);
     free(m->kcache); free(m->vcache);
     free(m->x); free(m->xn); free(m->q); free(m->k); free(m->v); free(m->attn);
     free(m->tmp); free(m->gate); free(m->up); free(m->hbuf); free(m->scores); free(m->window);
@@ -401,6 +409,48 @@ ORC_API void orc_set_mxfp4(orc_model *m, const uint8_t *const *bscales)
 {
     m->mxfp4 = bscales != NULL;
     for (int i = 0; i < 8; ++i) m->bscale[i] = bscales ? bscales[i] : NULL;
+}
+
+/* Switch the model to a mixture-of-experts FFN (see orc_model; FP16
+ * weights).  n_experts = 0 switches back to the dense FFN.  Returns 0, or -1
+ * for top_k outside [1, min(n_experts, 8)] or n_experts above 64. */
+ORC_API int orc_set_moe(orc_model *m, int n_experts, int top_k, const uint16_t *router)
+{
+    if (n_experts == 0) {
+        m->n_experts = 0;
+        return 0;
+    }
+    if (n_experts < 1 || n_experts > 64 || top_k < 1 || top_k > 8 || top_k > n_experts || !router) return -1;
+    if (!m->ffn_acc) m->ffn_acc = (float *)calloc((size_t)m->c.d_model, 4);
+    if (!m->rlogit) m->rlogit = (float *)calloc(64, 4);
+    if (!m->ffn_acc || !m->rlogit) return -1;
+    m->n_experts = n_experts;
+    m->top_k = top_k;
+    m->router = router;
+    return 0;
+}
+
+/* Top-k routing of one token (the plain mixture-of-experts reading of the
+ * pages' "only the active experts' weights stream per token", shivam2003.com,
+ * "Scaling the idea to frontier models"): the k largest router logits, ties
+ * to the lower expert index, in decreasing order; gate_j = softmax over the
+ * k selected logits (FP32, the largest subtracted). */
+ORC_API void orc_route(const float *logits, int n_experts, int top_k, int *sel, float *gate)
+{
+    unsigned long long used = 0ull;
+    for (int j = 0; j < top_k; ++j) {
+        int best = -1;
+        for (int e = 0; e < n_experts; ++e)
+            if (!(used >> e & 1ull) && (best < 0 || logits[e] > logits[best])) best = e;
+        used |= 1ull << best;
+        sel[j] = best;
+    }
+    float sum = 0.0f;
+    for (int j = 0; j < top_k; ++j) {
+        gate[j] = expf(logits[sel[j]] - logits[sel[0]]);
+        sum += gate[j];
+    }
+    for (int j = 0; j < top_k; ++j) gate[j] = gate[j] / sum;
 }
 
 /* Projection `which` (0 wq .. 7 lm_head) of layer l: y = W x. */
@@ -480,11 +530,30 @@ ORC_API int orc_forward(orc_model *m, int token, float *logits)
 
         /* FFN block */
         orc_rmsnorm(m->x, w->ffn_norm + (size_t)l * d, d, c->rms_eps, m->xn);
-        orc_project(m, 4, l, F, d, m->xn, m->gate);
-        orc_project(m, 5, l, F, d, m->xn, m->up);
-        for (int i = 0; i < F; ++i) m->hbuf[i] = orc_silu(m->gate[i]) * m->up[i];
-        orc_project(m, 6, l, d, F, m->hbuf, m->tmp);
-        for (int i = 0; i < d; ++i) m->x[i] = m->x[i] + m->tmp[i];
+        if (m->n_experts > 0) {
+            /* mixture of experts: y = sum_j gate_j * expert_{e_j}(xn) */
+            const int E = m->n_experts;
+            int sel[8];
+            float gate[8];
+            orc_matvec(m->router + (size_t)l * E * d, m->xn, E, d, m->rlogit);
+            orc_route(m->rlogit, E, m->top_k, sel, gate);
+            for (int i = 0; i < d; ++i) m->ffn_acc[i] = 0.0f;
+            for (int j = 0; j < m->top_k; ++j) {
+                const size_t ex = (size_t)l * E + (size_t)sel[j];
+                orc_matvec(w->w_gate + ex * F * d, m->xn, F, d, m->gate);
+                orc_matvec(w->w_up + ex * F * d, m->xn, F, d, m->up);
+                for (int i = 0; i < F; ++i) m->hbuf[i] = orc_silu(m->gate[i]) * m->up[i];
+                orc_matvec(w->w_down + ex * d * F, m->hbuf, d, F, m->tmp);
+                for (int i = 0; i < d; ++i) m->ffn_acc[i] = m->ffn_acc[i] + gate[j] * m->tmp[i];
+            }
+            for (int i = 0; i < d; ++i) m->x[i] = m->x[i] + m->ffn_acc[i];
+        } else {
+            orc_project(m, 4, l, F, d, m->xn, m->gate);
+            orc_project(m, 5, l, F, d, m->xn, m->up);
+            for (int i = 0; i < F; ++i) m->hbuf[i] = orc_silu(m->gate[i]) * m->up[i];
+            orc_project(m, 6, l, d, F, m->hbuf, m->tmp);
+            for (int i = 0; i < d; ++i) m->x[i] = m->x[i] + m->tmp[i];
+        }
     }
     if (logits) {
         orc_rmsnorm(m->x, w->final_norm, d, c->rms_eps, m->xn);

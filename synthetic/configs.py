@@ -24,6 +24,10 @@ class ModelConfig:
     vocab: int
     rope_theta: float = 10000.0
     rms_eps: float = 1e-5
+    # mixture of experts: n_experts FFNs of ffn_dim per layer, top_k_experts of
+    # them active per token (0: the dense FFN)
+    n_experts: int = 0
+    top_k_experts: int = 0
 
     @property
     def q_dim(self) -> int:
@@ -35,8 +39,17 @@ class ModelConfig:
 
     def n_params(self) -> int:
         L, d, F, V = self.n_layers, self.d_model, self.ffn_dim, self.vocab
-        per_layer = (self.q_dim + 2 * self.kv_dim) * d + d * self.q_dim + 3 * d * F + 2 * d
+        ffn = 3 * d * F if not self.n_experts else self.n_experts * (3 * d * F + d)
+        per_layer = (self.q_dim + 2 * self.kv_dim) * d + d * self.q_dim + ffn + 2 * d
         return V * d * 2 + L * per_layer + d
+
+    def active_ffn_weights(self) -> int:
+        """FFN weights one token uses in one layer: the dense FFN, or the
+        router and the top_k_experts active experts."""
+        d, F = self.d_model, self.ffn_dim
+        if not self.n_experts:
+            return 3 * d * F
+        return self.n_experts * d + self.top_k_experts * 3 * d * F
 
     def weight_bytes_per_token(self, weights: str = "fp16") -> int:
         """Bytes every decode step must stream: all layer matrices and norm
@@ -48,8 +61,10 @@ class ModelConfig:
         L, d, F, V = self.n_layers, self.d_model, self.ffn_dim, self.vocab
         Q, KV = self.q_dim, self.kv_dim
         if weights == "fp16":
-            per_layer = (Q + 2 * KV) * d + d * Q + 3 * d * F + 2 * d
+            per_layer = (Q + 2 * KV) * d + d * Q + self.active_ffn_weights() + 2 * d
             return 2 * (L * per_layer + d + V * d + d)
+        if self.n_experts:
+            raise ValueError("mixture-of-experts models take FP16 weights")
         rows = L * ((Q + 2 * KV) + d + 2 * F + d) + V
         elems = L * ((Q + 2 * KV) * d + d * Q + 3 * d * F) + V * d
         if weights == "fp8":
@@ -111,6 +126,9 @@ MODELS = {
     "small": ModelConfig("small", 16, 1024, 16, 4, 64, 4096, 32000),
     "2.3b": ModelConfig("2.3b", 25, 2560, 20, 5, 128, 8192, 64000),
     "8b": ModelConfig("8b", 32, 4096, 32, 8, 128, 14336, 128256),
+    # the ~2.3B decoder's attention with 8 experts of half its FFN width per
+    # layer, 2 active: 6.3B parameters, the 2.3B's bytes per token
+    "moe-8x": ModelConfig("moe-8x", 25, 2560, 20, 5, 128, 4096, 64000, n_experts=8, top_k_experts=2),
 }
 
 WORKLOADS = {
@@ -127,6 +145,8 @@ WORKLOADS = {
     # the ~2.3B decoder with weight-only FP8 projections (the pages: FP8 streaming
     # halves the bytes that bound batch-1 decode)
     "2.3b-fp8": Workload("2.3b-fp8", MODELS["2.3b"], 2, 1002, 512, 1024, weights="fp8"),
+    # mixture of experts (the pages: only the active experts' weights stream per token)
+    "moe-8x": Workload("moe-8x", MODELS["moe-8x"], 4, 1002, 512, 1024),
     # the same with MXFP4 projections (the pages: "FP8/MXFP4" for frontier models)
     "2.3b-mxfp4": Workload("2.3b-mxfp4", MODELS["2.3b"], 2, 1002, 512, 1024, weights="mxfp4"),
 }

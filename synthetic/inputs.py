@@ -30,6 +30,7 @@ _C4 = 0x5BD1E995 & 0x7FFFFFFF
 WEIGHT_ORDER = ("embed", "wq", "wk", "wv", "wo", "w_gate", "w_up", "w_down", "lm_head",
                 "attn_norm", "ffn_norm", "final_norm")
 _TENSOR_ID = {name: i + 1 for i, name in enumerate(WEIGHT_ORDER)}
+_TENSOR_ID["w_router"] = 0x30
 
 _TABLE_CACHE: dict = {}
 
@@ -110,13 +111,19 @@ def make_weights(cfg: ModelConfig, seed: int, device="cpu", gains: str = "ones",
         "embed": (V, d), "wq": (L, Q, d), "wk": (L, KV, d), "wv": (L, KV, d), "wo": (L, d, Q),
         "w_gate": (L, F, d), "w_up": (L, F, d), "w_down": (L, d, F), "lm_head": (V, d),
     }
+    names = WEIGHT_ORDER[:9]
+    E = getattr(cfg, "n_experts", 0)
+    if E:
+        # mixture of experts: E FFNs per layer and the router
+        shapes.update({"w_gate": (L, E, F, d), "w_up": (L, E, F, d), "w_down": (L, E, d, F), "w_router": (L, E, d)})
+        names = names + ("w_router",)
     w = {}
-    for name in WEIGHT_ORDER[:9]:
+    for name in names:
         if not projections and name != "embed":
             continue
         shp = shapes[name]
         t = torch.empty(shp, dtype=torch.float16, device=device)
-        if len(shp) == 3:
+        if len(shp) >= 3:
             for layer in range(shp[0]):
                 _fill(t[layer], table, seed, _TENSOR_ID[name], layer)
         else:

@@ -57,8 +57,18 @@ def _brute_force_logits(cfg, w, tokens, window=None):
                 att[h * hd:(h + 1) * hd] = (e / e.sum()) @ Vc[l, g, j0:p + 1]
             x = x + f["wo"][l] @ att
             xn = norm(x, f["ffn_norm"][l])
-            gt = f["w_gate"][l] @ xn
-            x = x + f["w_down"][l] @ ((gt / (1 + np.exp(-gt))) * (f["w_up"][l] @ xn))
+            if getattr(cfg, "n_experts", 0):
+                # mixture of experts: the top-k router logits (ties: lower index), softmax over them
+                r = f["w_router"][l] @ xn
+                sel = np.argsort(-r, kind="stable")[:cfg.top_k_experts]
+                gw = np.exp(r[sel] - r[sel].max())
+                gw = gw / gw.sum()
+                for j, e in enumerate(sel):
+                    gt = f["w_gate"][l, e] @ xn
+                    x = x + gw[j] * (f["w_down"][l, e] @ ((gt / (1 + np.exp(-gt))) * (f["w_up"][l, e] @ xn)))
+            else:
+                gt = f["w_gate"][l] @ xn
+                x = x + f["w_down"][l] @ ((gt / (1 + np.exp(-gt))) * (f["w_up"][l] @ xn))
         all_logits.append(f["lm_head"] @ norm(x, f["final_norm"]))
     return np.array(all_logits)
 
