@@ -185,8 +185,11 @@ def workload_desc(wl, K):
     wdesc = {"fp8": "FP8 E4M3 projection weights with FP32 per-row scales (~N(0,0.02) after scaling)",
              "mxfp4": "MXFP4 projection weights (E2M1 codes, E8M0 scale per 32 weights, 2^-7..2^-5)"
              }.get(wl.weights, "FP16 weights ~N(0,0.02)")
+    ffn = (f"SwiGLU FFN {m.ffn_dim}" if not m.n_experts else
+           f"{m.n_experts} SwiGLU experts of {m.ffn_dim} per layer, {m.top_k_experts} active per token "
+           f"(top-k router, softmax gates)")
     return (f"{wl.name}: {m.n_layers} layers, d_model {m.d_model}, {m.n_heads}/{m.n_kv_heads} heads x {m.head_dim}, "
-            f"SwiGLU FFN {m.ffn_dim}, vocab {m.vocab}, {wdesc}{win}; prompt {wl.prompt_len}, "
+            f"{ffn}, vocab {m.vocab}, {wdesc}{win}; prompt {wl.prompt_len}, "
             f"{K} decode steps ({samp})")
 
 
@@ -243,8 +246,8 @@ def run_ours(args):
     mk = {"fp8": make_weights_fp8, "mxfp4": make_weights_mxfp4}.get(wl.weights, make_weights)
     weights = mk(cfg, wl.weight_seed, device="cuda")
     prompt = make_prompt(cfg.vocab, wl.prompt_len, wl.prompt_seed).cuda()
-    # MXFP4 handles prefill as monokernel steps only
-    pf_block = 0 if wl.weights == "mxfp4" else args.prefill_block
+    # MXFP4 and mixture-of-experts handles prefill as monokernel steps only
+    pf_block = 0 if (wl.weights == "mxfp4" or cfg.n_experts) else args.prefill_block
     dec = pm.Decoder(cfg, weights, max_seq, layer_window=wl.layer_window, prefill_block=pf_block)
     info = dec.info()
     stream = torch.cuda.current_stream()
@@ -378,10 +381,14 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_ablations:
         n_ab = min(K, 64)
         ab = {"steps": n_ab}
-        for name, sched in (("monokernel_flags", pm.SCHED_FLAGS), ("grid_barrier", pm.SCHED_GRID_BARRIER),
-                            ("multi_kernel", pm.SCHED_MULTI_KERNEL)):
+        # (a mixture of experts keeps its expert choice inside one launch: no multi-kernel schedule)
+        scheds = (("monokernel_flags", pm.SCHED_FLAGS), ("grid_barrier", pm.SCHED_GRID_BARRIER)) + \
+            ((("multi_kernel", pm.SCHED_MULTI_KERNEL),) if not cfg.n_experts else ())
+        for name, sched in scheds:
             dec.set_schedule(sched)
             ab[name + "_tok_s"] = round(n_ab / timed_decode(n_ab), 2)
+        dec.set_schedule(pm.SCHED_FLAGS)
+    if rank == 0 and world == 1 and not args.no_ablations and not cfg.n_experts:
         # the multi-kernel launches captured once into a CUDA graph and replayed:
         # the graph removes the host launch overhead, not the kernel boundaries
         # (replays recompute the same positions, so the work per replay is fixed)
@@ -408,6 +415,7 @@ def run_ours(args):
             raise RuntimeError("multi-kernel graph ablation failed")
         dec.set_schedule(pm.SCHED_FLAGS)
         ab["launches_per_step_multi_kernel"] = 5 * cfg.n_layers + 1
+    if rank == 0 and world == 1 and not args.no_ablations:
         # prefill of the same prompt as repeated decode steps (the monokernel's own path)
         if info["prefill_block"] and "prefill" in result and n_pos <= 4096:
             dec0 = pm.Decoder(cfg, weights, max_seq, layer_window=wl.layer_window, prefill_block=0)

@@ -44,7 +44,7 @@ extern "C" {
 #define LF_API
 #endif
 
-#define LF_ABI_VERSION 5
+#define LF_ABI_VERSION 6
 #define LF_MAX_TOP_K 64          /* largest top_k that lf_decode accepts (besides 0) */
 
 typedef enum {
@@ -131,6 +131,20 @@ typedef struct {
      * cuBLAS handle and a workspace that grows with B; lf_info.prefill_bytes
      * reports them.  lf_generate_noalloc takes 0 only. */
     int32_t prefill_block;
+    /* Mixture-of-experts FFN (the pages: only the active experts' weights
+     * stream per token, shivam2003.com, "Scaling the idea to frontier
+     * models").  n_experts = 0: the dense SwiGLU FFN.  n_experts = E in
+     * [1, 64]: every layer holds E SwiGLU experts of ffn_dim hidden units
+     * (lf_weights.w_gate / w_up [L, E, ffn_dim, d], w_down [L, E, d,
+     * ffn_dim]) and a router lf_weights.w_router [L, E, d]; per token and
+     * layer the kernel forms the router logits W_router . xn (xn the FFN's
+     * RMSNorm output), takes the top_k_experts in [1, min(8, E)] largest
+     * (ties to the lower index), weights expert j by the softmax of the
+     * chosen logits, and streams only the chosen experts' rows.  Needs FP16
+     * weights, prefill_block = 0, top_k_experts * ffn_dim <= 16384 and a
+     * schedule other than LF_SCHED_MULTI_KERNEL. */
+    int32_t n_experts;
+    int32_t top_k_experts;
 } lf_config;
 
 #define LF_WEIGHTS_FP16 0
@@ -174,6 +188,10 @@ typedef struct {
     const void *w_up_scale;    /* [L, F]  */
     const void *w_down_scale;  /* [L, d]  */
     const void *lm_head_scale; /* [V]     */
+    /* Mixture of experts only (lf_config.n_experts > 0), else NULL: the
+     * router rows [L, E, d] FP16, read in place (must outlive the handle),
+     * 16-byte aligned */
+    const void *w_router;
 } lf_weights;
 
 /* Token choice, after the Gumbel-max trick of shivam2003.com ("The fused
@@ -222,7 +240,8 @@ typedef struct {
  * non-positive sizes, a negative window or prefill_block), NOT_SUPPORTED
  * (shape: head_dim other than 64 or 128, d_model, n_heads*head_dim or
  * ffn_dim not a multiple of 256 or above 16384; an unknown weight_format;
- * MXFP4 with prefill_block > 0), OUT_OF_MEMORY,
+ * MXFP4 with prefill_block > 0; an expert configuration outside the limits
+ * of lf_config.n_experts), OUT_OF_MEMORY,
  * NOT_RESIDENT, CUDA (also: the cuBLAS handle of the batched prefill could
  * not be created). */
 LF_API lf_status lf_create(const lf_config *cfg, const lf_weights *weights, lf_handle **out);
@@ -267,7 +286,10 @@ LF_API lf_status lf_sync(lf_handle *h);
  * latched device error cleared.  Synchronizes the device. */
 LF_API lf_status lf_reset(lf_handle *h);
 
-/* Select the schedule used by later lf_prefill / lf_decode calls. */
+/* Select the schedule used by later lf_prefill / lf_decode calls.  Errors:
+ * INVALID_ARG (unknown schedule), NOT_SUPPORTED (LF_SCHED_MULTI_KERNEL on a
+ * mixture-of-experts handle: the expert choice is kept in shared memory
+ * within one launch). */
 LF_API lf_status lf_set_schedule(lf_handle *h, int32_t schedule);
 
 /* Fill *out with the handle's launch geometry and state. */
@@ -321,8 +343,9 @@ LF_API lf_status lf_read_trace(lf_handle *h, uint64_t *host_out, int64_t capacit
  * calls from two host threads at once, race on the array: serialise them.
  * The call synchronizes `stream` and returns the device status (LF_OK,
  * LF_ERR_TIMEOUT, or LF_ERR_INVALID_ARG for a token id outside [0, vocab)).
- * Other errors: INVALID_ARG, NOT_SUPPORTED (also: FP8 or MXFP4 weights, or
- * prefill_block other than 0), CAPACITY, NOT_RESIDENT, CUDA. */
+ * Other errors: INVALID_ARG, NOT_SUPPORTED (also: FP8 or MXFP4 weights,
+ * prefill_block other than 0, or a mixture of experts), CAPACITY,
+ * NOT_RESIDENT, CUDA. */
 LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_weights *w, const int32_t *prompt_dev,
                                      int32_t n_prompt, int32_t n_steps, const lf_sampling *sp, uint64_t seed,
                                      int32_t *out_tokens_dev, void *stream);

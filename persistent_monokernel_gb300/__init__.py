@@ -39,7 +39,7 @@ class lf_config(C.Structure):
                 ("max_seq", C.c_int32), ("rope_theta", C.c_float), ("rms_eps", C.c_float),
                 ("wait_timeout_ns", C.c_int64), ("n_ctas", C.c_int32), ("fault_step", C.c_int32),
                 ("layer_window", C.POINTER(C.c_int32)), ("weight_format", C.c_int32),
-                ("prefill_block", C.c_int32)]
+                ("prefill_block", C.c_int32), ("n_experts", C.c_int32), ("top_k_experts", C.c_int32)]
 
 
 WEIGHTS_FP16, WEIGHTS_FP8_E4M3, WEIGHTS_MXFP4 = 0, 1, 2
@@ -50,7 +50,7 @@ SCALE_FIELDS = tuple(n + "_scale" for n in FP8_MATRICES)
 
 
 class lf_weights(C.Structure):
-    _fields_ = [(n, C.c_void_p) for n in WEIGHT_FIELDS + SCALE_FIELDS]
+    _fields_ = [(n, C.c_void_p) for n in WEIGHT_FIELDS + SCALE_FIELDS + ("w_router",)]
 
 
 class lf_sampling(C.Structure):
@@ -161,14 +161,22 @@ class Decoder:
             if not (t.is_cuda and t.dtype == want and t.is_contiguous()):
                 raise ValueError(f"weight {n} must be a contiguous CUDA {want} tensor")
         fmt = WEIGHTS_MXFP4 if self.mxfp4 else WEIGHTS_FP8_E4M3 if self.fp8 else WEIGHTS_FP16
-        # embed and the norm gains are read in place by every step: keep them alive
-        self._keep = {n: weights[n] for n in ("embed", "attn_norm", "ffn_norm", "final_norm")}
+        # mixture of experts: w_gate / w_up [L, E, F, d], w_down [L, E, d, F] and the router [L, E, d]
+        n_exp = int(getattr(model, "n_experts", 0) or 0)
+        if n_exp:
+            t = weights["w_router"]
+            if not (t.is_cuda and t.dtype == torch.float16 and t.is_contiguous()):
+                raise ValueError("weight w_router must be a contiguous CUDA torch.float16 tensor")
+        # embed, the norm gains and the router are read in place by every step: keep them alive
+        self._keep = {n: weights[n] for n in ("embed", "attn_norm", "ffn_norm", "final_norm")
+                      + (("w_router",) if n_exp else ())}
         cfg = lf_config(model.n_layers, model.d_model, model.n_heads, model.n_kv_heads, model.head_dim,
                         model.ffn_dim, model.vocab, self.max_seq, model.rope_theta, model.rms_eps,
                         int(wait_timeout_ns), int(n_ctas), int(fault_step), _windows(model, layer_window),
-                        fmt, int(prefill_block))
+                        fmt, int(prefill_block), n_exp, int(getattr(model, "top_k_experts", 0) or 0) if n_exp else 0)
         w = lf_weights(*[_dptr(weights[n]) for n in WEIGHT_FIELDS],
-                       *[_dptr(weights[n]) if quant else None for n in SCALE_FIELDS])
+                       *[_dptr(weights[n]) if quant else None for n in SCALE_FIELDS],
+                       _dptr(weights["w_router"]) if n_exp else None)
         h = C.c_void_p()
         _check(lib().lf_create(C.byref(cfg), C.byref(w), C.byref(h)), "lf_create")
         self._h = h

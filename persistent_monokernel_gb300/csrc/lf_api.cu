@@ -57,6 +57,7 @@ struct lf_handle {
     float2 *rope = nullptr;
     float *qbuf = nullptr, *attn = nullptr, *xattn = nullptr, *hbuf = nullptr, *xout = nullptr, *apart = nullptr;
     int *win = nullptr;            // [L] attention window per layer, or null (every layer: the whole cache)
+    const __half *router = nullptr;  // mixture of experts: the caller's [L][E][d] router rows (read in place)
     float *wsc = nullptr;          // FP8 weights: copies of the eight per-row scale arrays, back to back
     size_t wsc_off[8] = {};
     int max_split = 1;
@@ -140,6 +141,15 @@ lf_status validate_config(const lf_config &c)
         return LF_ERR_NOT_SUPPORTED;
     if (c.prefill_block < 0) return LF_ERR_INVALID_ARG;
     if (c.weight_format == LF_WEIGHTS_MXFP4 && c.prefill_block > 0) return LF_ERR_NOT_SUPPORTED;
+    if (c.n_experts < 0 || c.top_k_experts < 0) return LF_ERR_INVALID_ARG;
+    if (c.n_experts > 0) {
+        // mixture of experts: up to 64 experts, 1..8 active, FP16 weights, prefill in the monokernel
+        if (c.n_experts > lfk::MAX_EXPERTS || c.top_k_experts < 1 || c.top_k_experts > lfk::MAX_ACTIVE_EXPERTS ||
+            c.top_k_experts > c.n_experts)
+            return LF_ERR_NOT_SUPPORTED;
+        if (c.weight_format != LF_WEIGHTS_FP16 || c.prefill_block > 0) return LF_ERR_NOT_SUPPORTED;
+        if ((long long)c.top_k_experts * c.ffn_dim > (long long)lfk::MAX_SLICES * lfk::KC) return LF_ERR_NOT_SUPPORTED;
+    }
     return LF_OK;
 }
 
@@ -240,6 +250,7 @@ lfk::Params base_params(lf_handle *h)
     p.xout = h->xout;
     p.apart = h->apart;
     p.win = h->win;
+    p.router = h->router;
     for (int i = 0; i < 8; ++i) p.wsc[i] = h->wsc ? h->wsc + h->wsc_off[i] : nullptr;
     p.max_split = h->max_split;
     p.sig = h->sig;
@@ -343,6 +354,8 @@ lf_status lf_create(const lf_config *cfg, const lf_weights *w, lf_handle **out)
                           w->w_gate, w->w_up, w->w_down, w->final_norm, w->lm_head};
     for (const void *p : need)
         if (!p || (reinterpret_cast<uintptr_t>(p) & 15u)) return LF_ERR_INVALID_ARG;   // bulk copies need 16 B
+    if (cfg->n_experts > 0 ? (!w->w_router || (reinterpret_cast<uintptr_t>(w->w_router) & 15u)) : w->w_router != nullptr)
+        return LF_ERR_INVALID_ARG;
     const bool fp8 = cfg->weight_format == LF_WEIGHTS_FP8_E4M3;
     const bool mxfp4 = cfg->weight_format == LF_WEIGHTS_MXFP4;
     const void *scales_v[8] = {w->wq_scale, w->wk_scale, w->wv_scale, w->wo_scale,
@@ -368,7 +381,10 @@ lf_status lf_create(const lf_config *cfg, const lf_weights *w, lf_handle **out)
     g.Hq = cfg->n_heads;
     g.Hkv = cfg->n_kv_heads;
     g.hd = cfg->head_dim;
-    g.F = cfg->ffn_dim;
+    g.E = cfg->n_experts;
+    g.topk = g.E > 0 ? cfg->top_k_experts : 1;
+    g.Fe = cfg->ffn_dim;
+    g.F = g.topk * g.Fe;
     g.V = cfg->vocab;
     g.Q = g.Hq * g.hd;
     g.KV = g.Hkv * g.hd;
@@ -407,7 +423,10 @@ lf_status lf_create(const lf_config *cfg, const lf_weights *w, lf_handle **out)
         for (int s = 0; s < 4; ++s) {
             const lfk::StageGeom sg = lfk::stage_geom(g, s);
             pl.stage_off[s] = off;
-            off += (unsigned long long)(pl.u1[s] - pl.u0[s]) * sg.rows_per_unit * (sg.K / lfk::KC) *
+            // gate/up and down hold every expert's rows (down: Fe columns each)
+            const int nexp = (s == lfk::ST_GU || s == lfk::ST_D) ? lfk::n_expert_parts(g) : 1;
+            const int kcols = s == lfk::ST_D ? g.Fe : sg.K;
+            off += (unsigned long long)nexp * (pl.u1[s] - pl.u0[s]) * sg.rows_per_unit * (kcols / lfk::KC) *
                    (unsigned long long)g.crb;
         }
         pl.layer_bytes = off;
@@ -507,6 +526,7 @@ lf_status lf_create(const lf_config *cfg, const lf_weights *w, lf_handle **out)
     h->gbar = h->tok_cnt + lfk::CNT_STRIDE;
     h->abort_flag = h->status + 4;
     h->embed = static_cast<const __half *>(w->embed);
+    h->router = static_cast<const __half *>(w->w_router);
     h->attn_norm = static_cast<const __half *>(w->attn_norm);
     h->ffn_norm = static_cast<const __half *>(w->ffn_norm);
     h->final_norm = static_cast<const __half *>(w->final_norm);
@@ -705,6 +725,8 @@ lf_status lf_set_schedule(lf_handle *h, int32_t schedule)
     if (!h) return LF_ERR_INVALID_ARG;
     if (schedule != LF_SCHED_FLAGS && schedule != LF_SCHED_GRID_BARRIER && schedule != LF_SCHED_MULTI_KERNEL)
         return LF_ERR_INVALID_ARG;
+    // the expert choice lives in shared memory for the rest of the launch
+    if (schedule == LF_SCHED_MULTI_KERNEL && h->g.E > 0) return LF_ERR_NOT_SUPPORTED;
     h->sched = schedule;
     return LF_OK;
 }

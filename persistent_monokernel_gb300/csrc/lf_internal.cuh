@@ -51,7 +51,15 @@ struct Geo {
     int L, d, Hq, Hkv, hd, F, V, Q, KV, group, max_seq;
     int fmt;            // WeightFmt of the eight projections
     int crb;            // fmt_crb(fmt)
+    // FFN: E = 0 dense (topk = 1, Fe = F); E > 0: mixture of E experts of
+    // Fe hidden units each, topk active per token, and F = topk * Fe, the
+    // length of the hidden vector h (the active experts' units, slot by slot)
+    int E, topk, Fe;
 };
+constexpr int MAX_EXPERTS = 64;          // router logits: two per lane of one warp
+constexpr int MAX_ACTIVE_EXPERTS = 8;    // expert slots in shared memory per layer
+// Experts whose weights a stage's stream holds per layer (1 for a dense FFN).
+__host__ __device__ inline int n_expert_parts(const Geo &g) { return g.E > 0 ? g.E : 1; }
 // Bytes of one row of one column group (256 weights) of a projection in the stream.
 __host__ __device__ inline int chunk_row_bytes(const Geo &g) { return g.crb; }
 
@@ -72,7 +80,7 @@ __host__ __device__ inline StageGeom stage_geom(const Geo &g, int s)
     switch (s) {
     case ST_QKV: return {(g.Q + 2 * g.KV) / 2, 2, g.d};
     case ST_O: return {g.d, 1, g.Q};
-    case ST_GU: return {g.F, 2, g.d};
+    case ST_GU: return {g.Fe, 2, g.d};     // per slot (active expert)
     case ST_D: return {g.d, 1, g.F};
     default: return {g.V, 1, g.d};
     }
@@ -213,6 +221,7 @@ struct Params {
     // FP8 weights (g.fmt == FMT_FP8): per-row FP32 scales of wq, wk, wv, wo, w_gate,
     // w_up, w_down, lm_head in the caller's row order ([L][rows], [V])
     const float *wsc[8];
+    const __half *router;        // [L][E][d] FP16 router rows (mixture of experts), or null
     int max_split;
     unsigned *sig;               // [L][sig_layout().per_layer] readiness counters
     unsigned *attn_done;         // [L][Hkv] pieces of each KV head that have published

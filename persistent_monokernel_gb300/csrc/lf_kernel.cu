@@ -86,8 +86,11 @@ __host__ __device__ inline SmemLayout smem_layout(int ring_bytes, int a_floats, 
 // passes over partial-sum buffer b (cumulative).  M_AREL: consumer warps done
 // with an input in buffer A; M_ASCR: attention stages done with their scratch
 // in buffer A; M_LMDONE: decode steps whose LM-head keys are complete.
-enum { M_FLAG = 0, M_TOKEN = 1, M_DIGIT = 2, M_REMAIN = 3, M_AREL = 4, M_ASCR = 5, M_LMDONE = 6, M_TCNT = 16,
-       M_TRED = 24 };
+// Mixture of experts: M_ROUTE counts the expert choices made in this launch;
+// M_SEL + 8 * (l & 1) + j and M_GATE + 8 * (l & 1) + j hold slot j's expert
+// and gate (FP32 bits) of layer l.
+enum { M_FLAG = 0, M_TOKEN = 1, M_DIGIT = 2, M_REMAIN = 3, M_AREL = 4, M_ASCR = 5, M_LMDONE = 6, M_ROUTE = 7,
+       M_TCNT = 16, M_TRED = 24, M_SEL = 32, M_GATE = 48 };
 
 struct Ctx {
     const Params *p;
@@ -523,7 +526,7 @@ __device__ __forceinline__ StageIn stage_input(const Params &p, int s, int l)
 // partial-sum buffer sequence), fills of buffer A, phases of buffer B's slots,
 // inputs of buffer A handed back by the consumers, attention stages passed.
 struct PipeState {
-    unsigned seq = 0, afill = 0, bphase = 0, a_uses = 0, attn_uses = 0;
+    unsigned seq = 0, afill = 0, bphase = 0, a_uses = 0, attn_uses = 0, routes = 0;
 };
 
 // Token fed to forward pass `step` (decode: after its counter was acquired).
@@ -887,6 +890,94 @@ __device__ __forceinline__ float2 h2f(unsigned w) { return __half22float2(*reint
 // RMSNorm sum (tile 0 covers every slice once) and applies the gain.  After
 // each tile the warp reduces its 32 row sums over the lanes and hands them to
 // the reducer through a rotating partial-sum buffer.
+// Mixture of experts: every CTA chooses the layer's active experts itself,
+// from the gate/up stage's input it has just loaded (the pages: only the
+// active experts' weights stream per token), so the choice costs no grid-wide
+// hop.  Warp w forms the router logits of experts w, w + 8, ... as FP32 dot
+// products of the FP16 router rows with x * gain (the RMSNorm factor is a
+// positive scale, applied afterwards); warp 0 scales them, takes the top k
+// (ties to the lower index) and the softmax of the chosen logits, and
+// publishes experts and gates in shared memory for the producer, which then
+// streams only those experts' rows, and for the reducer.  Returns true if the
+// CTA must stop.
+__device__ __forceinline__ bool route_experts(const Ctx &c, PipeState &ps, int l, int step, bool ab)
+{
+    const Params &p = *c.p;
+    const Geo &g = p.g;
+    const unsigned apar = ps.afill & 1u;
+    bool fail = ab;
+    if (!fail && !mbar_try_wait(c.gfull, apar)) fail = !wait_mbar(p, c.gfull, apar, 140);
+    for (int k = 0; k < g.d / KC && !fail; ++k)
+        if (!mbar_try_wait(c.afull + k, apar)) fail = !wait_mbar(p, c.afull + k, apar, 141);
+    fail = __any_sync(0xffffffffu, fail);
+    float *logit = reinterpret_cast<float *>(c.hist);
+    float ss = 0.f;
+    if (!fail) {
+        const __half *wr = p.router + (size_t)l * g.E * g.d;
+        for (int e = c.warp; e < g.E; e += NCW) {
+            const __half *row = wr + (size_t)e * g.d;
+            float acc = 0.f;
+            for (int i = c.lane * 8; i < g.d; i += 256) {
+                float4 xa = lds_f4(smem_u32(c.acta + i)), xb = lds_f4(smem_u32(c.acta + i + 4));
+                if (e == 0) {
+                    ss = fmaf(xa.x, xa.x, ss); ss = fmaf(xa.y, xa.y, ss);
+                    ss = fmaf(xa.z, xa.z, ss); ss = fmaf(xa.w, xa.w, ss);
+                    ss = fmaf(xb.x, xb.x, ss); ss = fmaf(xb.y, xb.y, ss);
+                    ss = fmaf(xb.z, xb.z, ss); ss = fmaf(xb.w, xb.w, ss);
+                }
+                const uint4 gv = lds_u4(smem_u32(c.gain + i));
+                const float2 g0 = h2f(gv.x), g1 = h2f(gv.y), g2 = h2f(gv.z), g3 = h2f(gv.w);
+                xa.x *= g0.x; xa.y *= g0.y; xa.z *= g1.x; xa.w *= g1.y;
+                xb.x *= g2.x; xb.y *= g2.y; xb.z *= g3.x; xb.w *= g3.y;
+                acc = dot8(__ldg(reinterpret_cast<const uint4 *>(row + i)), xa, xb, acc);
+            }
+            acc = warp_sum(acc);
+            if (c.lane == 0) logit[e] = acc;
+        }
+    }
+    if (cons_sync_or(fail)) return true;
+    if (c.warp == 0) {
+        const float inv = 1.0f / sqrtf(warp_sum(ss) / (float)g.d + p.eps);
+        float v0 = c.lane < g.E ? logit[c.lane] * inv : -INFINITY;
+        float v1 = c.lane + 32 < g.E ? logit[c.lane + 32] * inv : -INFINITY;
+        __syncwarp();
+        const int b = 8 * (l & 1);
+        float *top = logit + MAX_EXPERTS;   // the chosen logits, in order
+        for (int j = 0; j < g.topk; ++j) {
+            float bv = v0;
+            int bi = c.lane;
+            if (v1 > bv) {
+                bv = v1;
+                bi = c.lane + 32;
+            }
+#pragma unroll
+            for (int o = 16; o; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+                if (ov > bv || (ov == bv && oi < bi)) {
+                    bv = ov;
+                    bi = oi;
+                }
+            }
+            if (bi == c.lane) v0 = -INFINITY;
+            else if (bi == c.lane + 32) v1 = -INFINITY;
+            if (c.lane == 0) {
+                top[j] = bv;
+                c.misc[M_SEL + b + j] = (unsigned)bi;
+            }
+        }
+        if (c.lane == 0) {
+            float sum = 0.f;
+            for (int j = 0; j < g.topk; ++j) sum += expf(top[j] - top[0]);
+            for (int j = 0; j < g.topk; ++j) c.misc[M_GATE + b + j] = __float_as_uint(expf(top[j] - top[0]) / sum);
+            __threadfence_block();
+            *reinterpret_cast<volatile unsigned *>(&c.misc[M_ROUTE]) = ps.routes + 1u;
+        }
+    }
+    ps.routes++;
+    return false;
+}
+
 template <int FMT>
 __device__ __forceinline__ bool stage_gemv(const Ctx &c, ConsRing &rc, PipeState &ps, int s, int l, int step, bool ab)
 {
@@ -911,9 +1002,13 @@ __device__ __forceinline__ bool stage_gemv(const Ctx &c, ConsRing &rc, PipeState
     }
     const int u0 = pl.u0[s], n = pl.u1[s] - u0;
     const int nt = tiles_of(n, sg.rows_per_unit);
+    // gate/up: the CTA's tiles once per active expert (slot); the weights of
+    // slot j's expert arrive through the ring like any other tile
+    const int nslot = s == ST_GU ? g.topk : 1;
     int jc = 0;
     bool first = true;
-    for (int t = 0; t < nt && !ab; ++t) {
+    for (int jt = 0; jt < nslot * nt && !ab; ++jt) {
+        const int t = jt % nt;
         int a, bnd;
         tile_range(u0, n, nt, t, a, bnd);
         const int R = (bnd - a) * sg.rows_per_unit;
@@ -963,7 +1058,7 @@ __device__ __forceinline__ bool stage_gemv(const Ctx &c, ConsRing &rc, PipeState
                 xb = lds_f4(xaddr + 16u);
             }
             if (norm) {
-                if (t == 0) {
+                if (jt == 0) {
                     ss = fmaf(xa.x, xa.x, ss); ss = fmaf(xa.y, xa.y, ss);
                     ss = fmaf(xa.z, xa.z, ss); ss = fmaf(xa.w, xa.w, ss);
                     ss = fmaf(xb.x, xb.x, ss); ss = fmaf(xb.y, xb.y, ss);
@@ -989,7 +1084,7 @@ __device__ __forceinline__ bool stage_gemv(const Ctx &c, ConsRing &rc, PipeState
         if (ab) break;
         // ---- per-warp row sums -> partial buffer of this tile
         const float v = mine ? reduce_rows32(acc, c.lane) : 0.f;
-        const float ssw = (norm && t == 0) ? warp_sum(ss) : 0.f;
+        const float ssw = (norm && jt == 0) ? warp_sum(ss) : 0.f;
         const unsigned seq = ps.seq++;
         const int buf = (int)(seq % PART_BUFS);
         const unsigned use = seq / PART_BUFS;
@@ -1040,8 +1135,19 @@ __device__ __forceinline__ bool reduce_stage(const Ctx &c, PipeState &ps, int s,
     const bool withhold = p.mode == MODE_DECODE && step == p.fault_step && l == 0 && s == ST_QKV;
     const int u0 = pl.u0[s], n = pl.u1[s] - u0;
     const int nt = tiles_of(n, sg.rows_per_unit);
+    const int nslot = s == ST_GU ? g.topk : 1;
+    const bool moe = s == ST_GU && g.E > 0;
+    if (moe) {
+        // the layer's expert choice (made by the consumers before any gate/up tile)
+        bool ok = true;
+        if (c.lane == 0) ok = wait_smem_ge(p, &c.misc[M_ROUTE], ps.routes + 1u, 113, l, step);
+        if (!__shfl_sync(0xffffffffu, (int)ok, 0)) return true;
+        __threadfence_block();
+        ps.routes++;
+    }
     float inv = 1.f;
-    for (int t = 0; t < nt; ++t) {
+    for (int jt = 0; jt < nslot * nt; ++jt) {
+        const int t = jt % nt, slot = jt / nt;
         int a, bnd;
         tile_range(u0, n, nt, t, a, bnd);
         const int nu = bnd - a;
@@ -1069,13 +1175,13 @@ __device__ __forceinline__ bool reduce_stage(const Ctx &c, PipeState &ps, int s,
         bool ok = true;
         if (c.lane == 0) ok = wait_smem_ge(p, &c.misc[M_TCNT + buf], (use + 1u) * NCW, 111, l, step);
         if (!__shfl_sync(0xffffffffu, (int)ok, 0)) return true;
-        if (t == nt - 1 && c.lane == 0) trace_mark_producer(c, step, tslot, TR_X2);
+        if (jt == nslot * nt - 1 && c.lane == 0) trace_mark_producer(c, step, tslot, TR_X2);
         __threadfence_block();
         const volatile float *part = c.res + (size_t)buf * NCW * PART_STRIDE;
         float sum = 0.f;
 #pragma unroll
         for (int w = 0; w < NCW; ++w) sum += part[w * PART_STRIDE + c.lane];
-        if (norm && t == 0) {
+        if (norm && jt == 0) {
             float tot = 0.f;
 #pragma unroll
             for (int w = 0; w < NCW; ++w) tot += part[w * PART_STRIDE + TILE_ROWS];
@@ -1122,7 +1228,11 @@ __device__ __forceinline__ bool reduce_stage(const Ctx &c, PipeState &ps, int s,
                 p.xattn[(size_t)l * g.d + u] = pre.x + sum;
             } else if (s == ST_GU) {
                 const float gt = sum * inv, up = partner * inv;
-                p.hbuf[(size_t)l * g.F + u] = gt / (1.0f + expf(-gt)) * up;
+                float hv = gt / (1.0f + expf(-gt)) * up;
+                if (moe)   // slot j's gate weights its expert's hidden units
+                    hv *= __uint_as_float(*reinterpret_cast<const volatile unsigned *>(
+                        &c.misc[M_GATE + 8 * (l & 1) + slot]));
+                p.hbuf[(size_t)l * g.F + (size_t)slot * g.Fe + u] = hv;
             } else if (s == ST_D) {
                 p.xout[(size_t)l * g.d + u] = pre.x + sum;
             } else {
@@ -1138,7 +1248,7 @@ __device__ __forceinline__ bool reduce_stage(const Ctx &c, PipeState &ps, int s,
         if (c.lane == 0 && s != ST_LM && !withhold) {
             if (s == ST_QKV) publish_range(sig_ptr(p, l, sl.qkvh), a, nu, g.hd / 2);
             else if (s == ST_O) publish_range(sig_ptr(p, l, sl.xattn), a, nu, KC);
-            else if (s == ST_GU) publish_range(sig_ptr(p, l, sl.h), a, nu, KC);
+            else if (s == ST_GU) publish_range(sig_ptr(p, l, sl.h), slot * g.Fe + a, nu, KC);
             else publish_range(sig_ptr(p, l, sl.xout), a, nu, KC);
         }
     }
@@ -1766,6 +1876,7 @@ __device__ void consumer(const Ctx &c)
                 if (p.sched == SCHED_GRID && cons_grid_arrive(c, ab)) return;
                 trace_mark(c, step, k, TR_DONE);
             } else {
+                if (sid == SID_GU && g.E > 0 && route_experts(c, ps, l, step, ab)) return;
                 if (stage_gemv<FMT>(c, rc, ps, stage_of(sid), l, step, ab)) return;
                 if (lm) {
                     // the reducer's keys of every LM-head tile of this CTA
@@ -1788,9 +1899,11 @@ struct RepackSrc {
 // Row `part` of unit `unit` of stage s, layer l, in the caller's row-major
 // weights, or for MXFP4 in the chunk-interleaved copy lf_create builds: a row
 // of `cols` columns takes cols / 256 * g.crb bytes either way.
-__device__ const uint8_t *src_row(const Geo &g, const RepackSrc &w, int s, int l, int unit, int part)
+__device__ const uint8_t *src_row(const Geo &g, const RepackSrc &w, int s, int l, int unit, int part, int e = 0)
 {
-    const size_t rd = (size_t)(g.d / KC) * g.crb, rq = (size_t)(g.Q / KC) * g.crb, rf = (size_t)(g.F / KC) * g.crb;
+    // gate/up/down of a mixture of experts: [L][E][rows][cols]; dense: E = 1, Fe = F
+    const size_t rd = (size_t)(g.d / KC) * g.crb, rq = (size_t)(g.Q / KC) * g.crb, rf = (size_t)(g.Fe / KC) * g.crb;
+    const size_t le = (size_t)l * n_expert_parts(g) + e;
     switch (s) {
     case ST_QKV: {
         const int half = g.hd / 2;
@@ -1801,13 +1914,65 @@ __device__ const uint8_t *src_row(const Geo &g, const RepackSrc &w, int s, int l
         return w.wv + ((size_t)l * g.KV + (r - g.Q - g.KV)) * rd;
     }
     case ST_O: return w.wo + ((size_t)l * g.d + unit) * rq;
-    case ST_GU: return (part ? w.wu : w.wg) + ((size_t)l * g.F + unit) * rd;
-    case ST_D: return w.wd + ((size_t)l * g.d + unit) * rf;
+    case ST_GU: return (part ? w.wu : w.wg) + (le * g.Fe + unit) * rd;
+    case ST_D: return w.wd + (le * g.d + unit) * rf;
     default: return w.head + (size_t)unit * rd;
     }
 }
 
 // ---------------------------------------------------------------- producer
+
+// Mixture of experts: the stream holds the gate/up and down rows of every
+// expert of the layer, expert after expert (gate/up: the CTA's tiles with
+// d/256 chunks each; down: the CTA's tiles with Fe/256 chunks each), and only
+// the active experts' parts are sent, in the consumers' order: gate/up slot by
+// slot; down tile by tile, each tile's chunks slot by slot.
+__device__ __forceinline__ bool produce_moe(const Ctx &c, ProdRing &pr, int s, int l)
+{
+    // slot j's expert, chosen by the consumers for this layer
+    auto sel = [&c, l](int j) {
+        return (int)*reinterpret_cast<const volatile unsigned *>(&c.misc[M_SEL + 8 * (l & 1) + j]);
+    };
+    const Params &p = *c.p;
+    const Geo &g = p.g;
+    const CtaPlan &pl = *c.plan;
+    const StageGeom sg = stage_geom(g, s);
+    const int u0 = pl.u0[s], n = pl.u1[s] - u0;
+    const int nt = tiles_of(n, sg.rows_per_unit);
+    const uint8_t *base = p.wstream + pl.base + (unsigned long long)l * pl.layer_bytes + pl.stage_off[s];
+    const int nch = (s == ST_GU ? g.d : g.Fe) / KC;
+    const unsigned long long part = (unsigned long long)n * sg.rows_per_unit * nch * (unsigned long long)g.crb;
+    if (s == ST_GU) {
+        for (int j = 0; j < g.topk; ++j) {
+            const uint8_t *src = base + (unsigned long long)sel(j) * part;
+            for (int t = 0; t < nt; ++t) {
+                int a, bnd;
+                tile_range(u0, n, nt, t, a, bnd);
+                const unsigned bytes = (unsigned)((bnd - a) * sg.rows_per_unit) * (unsigned)g.crb;
+                for (int k = 0; k < nch; ++k) {
+                    if (!pr.emit(c, src, bytes)) return false;
+                    src += bytes;
+                }
+            }
+        }
+        return true;
+    }
+    unsigned long long toff = 0;   // offset of tile t inside an expert's part
+    for (int t = 0; t < nt; ++t) {
+        int a, bnd;
+        tile_range(u0, n, nt, t, a, bnd);
+        const unsigned bytes = (unsigned)((bnd - a) * sg.rows_per_unit) * (unsigned)g.crb;
+        for (int j = 0; j < g.topk; ++j) {
+            const uint8_t *src = base + (unsigned long long)sel(j) * part + toff;
+            for (int k = 0; k < nch; ++k) {
+                if (!pr.emit(c, src, bytes)) return false;
+                src += bytes;
+            }
+        }
+        toff += (unsigned long long)bytes * nch;
+    }
+    return true;
+}
 
 __device__ __forceinline__ bool produce_tiles(const Ctx &c, ProdRing &pr, int s, int l, int step)
 {
@@ -1890,7 +2055,7 @@ __device__ void producer(const Ctx &c, const RepackSrc *w)
         pr.pol_kv = kv_read > (128ll << 20) ? policy_evict_first() : policy_evict_normal();
     }
     pr.pol_pf = p.l2_prefetch_last ? policy_evict_last() : policy_evict_normal();
-    if (!kDirect && p.only_stage < 0 && p.l2_prefetch_bytes > 0) {
+    if (!kDirect && p.only_stage < 0 && p.l2_prefetch_bytes > 0 && g.E == 0) {
         const CtaPlan &pl = *c.plan;
         pr.stream_base = p.wstream + pl.base;
         pr.token_bytes = pl.lm_off;
@@ -1901,6 +2066,7 @@ __device__ void producer(const Ctx &c, const RepackSrc *w)
     }
     bool ok = true;
     const int n_sub = 5 * g.L + (p.mode == MODE_DECODE ? 1 : 0);
+    unsigned routes = 0;   // expert choices consumed (mixture of experts)
     for (int step = 0; step < p.n_steps && ok; ++step) {
         step_now = step;
         const unsigned e = p.epoch0 + (unsigned)step;
@@ -1914,6 +2080,16 @@ __device__ void producer(const Ctx &c, const RepackSrc *w)
             if (sid != SID_ATTN) {
                 const int st = sid == SID_QKV ? ST_QKV : sid == SID_O ? ST_O : sid == SID_GU ? ST_GU
                                                        : sid == SID_D ? ST_D : ST_LM;
+                if (g.E > 0 && (st == ST_GU || st == ST_D)) {
+                    if (st == ST_GU) {
+                        // the consumers' expert choice for this layer
+                        ok = wait_smem_ge(p, &c.misc[M_ROUTE], routes + 1u, 104, l, step);
+                        ++routes;
+                    }
+                    if (ok) ok = produce_moe(c, pr, st, l);
+                    trace_mark_producer(c, step, k, TR_P1);
+                    continue;
+                }
                 ok = tiles(c, pr, w, st, l);
                 trace_mark_producer(c, step, k, TR_P1);
                 continue;
@@ -2054,24 +2230,28 @@ __global__ void lf_repack_kernel(Geo g, const CtaPlan *plans, RepackSrc w, uint8
             const int u0 = pl.u0[s], n = pl.u1[s] - u0;
             const int nt = tiles_of(n, sg.rows_per_unit);
             uint8_t *out = dst + pl.base + (s == ST_LM ? pl.lm_off : (unsigned long long)l * pl.layer_bytes + pl.stage_off[s]);
-            for (int t = 0; t < nt; ++t) {
-                int a, bnd;
-                tile_range(u0, n, nt, t, a, bnd);
-                const int nu = bnd - a;
-                const int R = nu * sg.rows_per_unit;
-                const int nch = sg.K / KC;
-                const int v16 = chunk_row_bytes(g) / 16;   // 16-byte words of one row of a chunk
-                for (int k = 0; k < nch; ++k) {
-                    // chunk: R rows x 256 columns, stored row r -> (unit a + r % nu, part r / nu)
-                    for (int q = threadIdx.x; q < R * v16; q += blockDim.x) {
-                        const int r = q / v16, rem = q % v16;
-                        const int unit = a + (sg.rows_per_unit == 2 ? r % nu : r);
-                        const int part = sg.rows_per_unit == 2 ? r / nu : 0;
-                        const uint4 *srow =
-                            reinterpret_cast<const uint4 *>(src_row(g, w, s, l < g.L ? l : 0, unit, part));
-                        reinterpret_cast<uint4 *>(out)[q] = srow[(size_t)k * v16 + rem];
+            // gate/up and down: every expert's rows, expert after expert
+            const int nexp = (s == ST_GU || s == ST_D) ? n_expert_parts(g) : 1;
+            const int nch = (s == ST_D ? g.Fe : sg.K) / KC;
+            for (int e = 0; e < nexp; ++e) {
+                for (int t = 0; t < nt; ++t) {
+                    int a, bnd;
+                    tile_range(u0, n, nt, t, a, bnd);
+                    const int nu = bnd - a;
+                    const int R = nu * sg.rows_per_unit;
+                    const int v16 = chunk_row_bytes(g) / 16;   // 16-byte words of one row of a chunk
+                    for (int k = 0; k < nch; ++k) {
+                        // chunk: R rows x 256 columns, stored row r -> (unit a + r % nu, part r / nu)
+                        for (int q = threadIdx.x; q < R * v16; q += blockDim.x) {
+                            const int r = q / v16, rem = q % v16;
+                            const int unit = a + (sg.rows_per_unit == 2 ? r % nu : r);
+                            const int part = sg.rows_per_unit == 2 ? r / nu : 0;
+                            const uint4 *srow =
+                                reinterpret_cast<const uint4 *>(src_row(g, w, s, l < g.L ? l : 0, unit, part, e));
+                            reinterpret_cast<uint4 *>(out)[q] = srow[(size_t)k * v16 + rem];
+                        }
+                        out += (size_t)R * chunk_row_bytes(g);
                     }
-                    out += (size_t)R * chunk_row_bytes(g);
                 }
             }
         }

@@ -81,7 +81,8 @@ extern "C" LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_w
     if (cfg->d_model > most || (long long)cfg->n_heads * cfg->head_dim > most || cfg->ffn_dim > most)
         return LF_ERR_NOT_SUPPORTED;
     if (sp->top_k < 0 || sp->top_k > LF_MAX_TOP_K) return LF_ERR_NOT_SUPPORTED;
-    if (cfg->weight_format != LF_WEIGHTS_FP16 || cfg->prefill_block != 0) return LF_ERR_NOT_SUPPORTED;
+    if (cfg->weight_format != LF_WEIGHTS_FP16 || cfg->prefill_block != 0 || cfg->n_experts != 0)
+        return LF_ERR_NOT_SUPPORTED;
     if (cfg->layer_window)
         for (int l = 0; l < cfg->n_layers; ++l)
             if (cfg->layer_window[l] < 0) return LF_ERR_INVALID_ARG;
@@ -100,6 +101,9 @@ extern "C" LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_w
     g.group = g.Hq / g.Hkv;
     g.max_seq = cfg->max_seq;
     g.fmt = lfk::FMT_FP16;
+    g.E = 0;
+    g.topk = 1;
+    g.Fe = g.F;
     g.crb = lfk::fmt_crb(lfk::FMT_FP16);
 
     // ---- device, grid and the static partition (as lf_create)

@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(pm):
 
 
 def test_abi_version_and_error_strings(pm):
-    assert pm.lib().lf_abi_version() == 5
+    assert pm.lib().lf_abi_version() == 6
     for code, name in pm.STATUS_NAMES.items():
         assert pm.error_string(code).startswith(name)
 
@@ -87,6 +87,20 @@ def test_create_rejects_bad_arguments_before_touching_the_gpu(pm):
     assert L.lf_create(C.byref(cfg), C.byref(w4), C.byref(h)) == 1
     cfg = pm.lf_config(**{**good, "weight_format": pm.WEIGHTS_MXFP4, "prefill_block": 16})
     assert L.lf_create(C.byref(cfg), C.byref(w), C.byref(h)) == 7
+    # mixture of experts: limits on the expert counts, FP16 only, the router pointer required
+    for change, expect in [(dict(n_experts=-1), 1), (dict(n_experts=65, top_k_experts=2), 7),
+                           (dict(n_experts=8, top_k_experts=0), 7), (dict(n_experts=8, top_k_experts=9), 7),
+                           (dict(n_experts=2, top_k_experts=3), 7), (dict(n_experts=8, top_k_experts=2, prefill_block=8), 7),
+                           (dict(n_experts=8, top_k_experts=2, weight_format=pm.WEIGHTS_FP8_E4M3), 7),
+                           (dict(n_experts=8, top_k_experts=8, ffn_dim=4096), 7),
+                           (dict(n_experts=8, top_k_experts=2), 1)]:      # no w_router
+        cfg = pm.lf_config(**{**good, **change})
+        assert L.lf_create(C.byref(cfg), C.byref(w), C.byref(h)) == expect, change
+    wr = pm.lf_weights(*([0x1000] * 12 + [0] * 8 + [0x1008]))           # router not 16-byte aligned
+    cfg = pm.lf_config(**{**good, "n_experts": 8, "top_k_experts": 2})
+    assert L.lf_create(C.byref(cfg), C.byref(wr), C.byref(h)) == 1
+    wr = pm.lf_weights(*([0x1000] * 12 + [0] * 8 + [0x1000]))           # a router on a dense model
+    assert L.lf_create(C.byref(pm.lf_config(**good)), C.byref(wr), C.byref(h)) == 1
 
 
 def test_noalloc_rejects_batched_prefill_before_touching_the_gpu(pm):
