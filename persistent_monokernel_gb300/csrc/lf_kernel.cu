@@ -963,7 +963,9 @@ __device__ __forceinline__ bool route_experts(const Ctx &c, PipeState &ps, int l
             else if (bi == c.lane + 32) v1 = -INFINITY;
             if (c.lane == 0) {
                 top[j] = bv;
-                c.misc[M_SEL + b + j] = (unsigned)bi;
+                // (bi < E for any finite logits; the clamp keeps a NaN logit's
+                // choice inside the stream)
+                c.misc[M_SEL + b + j] = (unsigned)min(bi, g.E - 1);
             }
         }
         if (c.lane == 0) {
