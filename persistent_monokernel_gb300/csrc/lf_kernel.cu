@@ -980,7 +980,7 @@ __device__ __forceinline__ bool route_experts(const Ctx &c, PipeState &ps, int l
     return false;
 }
 
-template <int FMT>
+template <int FMT, bool MOE>
 __device__ __forceinline__ bool stage_gemv(const Ctx &c, ConsRing &rc, PipeState &ps, int s, int l, int step, bool ab)
 {
     const Params &p = *c.p;
@@ -1006,11 +1006,11 @@ __device__ __forceinline__ bool stage_gemv(const Ctx &c, ConsRing &rc, PipeState
     const int nt = tiles_of(n, sg.rows_per_unit);
     // gate/up: the CTA's tiles once per active expert (slot); the weights of
     // slot j's expert arrive through the ring like any other tile
-    const int nslot = s == ST_GU ? g.topk : 1;
+    const int nslot = (MOE && s == ST_GU) ? g.topk : 1;
     int jc = 0;
     bool first = true;
     for (int jt = 0; jt < nslot * nt && !ab; ++jt) {
-        const int t = jt % nt;
+        const int t = MOE ? jt % nt : jt;
         int a, bnd;
         tile_range(u0, n, nt, t, a, bnd);
         const int R = (bnd - a) * sg.rows_per_unit;
@@ -1122,6 +1122,7 @@ __device__ __forceinline__ bool stage_gemv(const Ctx &c, ConsRing &rc, PipeState
 // for the eight warps' partials, sum them in warp order, run the stage
 // epilogue (lane i: unit a + i; pair stages: rows i and i + nu) and count the
 // outputs in the readiness counters of the slices (or heads) they belong to.
+template <bool MOE>
 __device__ __forceinline__ bool reduce_stage(const Ctx &c, PipeState &ps, int s, int l, int step, bool ab)
 {
     const Params &p = *c.p;
@@ -1137,8 +1138,8 @@ __device__ __forceinline__ bool reduce_stage(const Ctx &c, PipeState &ps, int s,
     const bool withhold = p.mode == MODE_DECODE && step == p.fault_step && l == 0 && s == ST_QKV;
     const int u0 = pl.u0[s], n = pl.u1[s] - u0;
     const int nt = tiles_of(n, sg.rows_per_unit);
-    const int nslot = s == ST_GU ? g.topk : 1;
-    const bool moe = s == ST_GU && g.E > 0;
+    const int nslot = (MOE && s == ST_GU) ? g.topk : 1;
+    const bool moe = MOE && s == ST_GU;
     if (moe) {
         // the layer's expert choice (made by the consumers before any gate/up tile)
         bool ok = true;
@@ -1149,7 +1150,7 @@ __device__ __forceinline__ bool reduce_stage(const Ctx &c, PipeState &ps, int s,
     }
     float inv = 1.f;
     for (int jt = 0; jt < nslot * nt; ++jt) {
-        const int t = jt % nt, slot = jt / nt;
+        const int t = MOE ? jt % nt : jt, slot = MOE ? jt / nt : 0;
         int a, bnd;
         tile_range(u0, n, nt, t, a, bnd);
         const int nu = bnd - a;
@@ -1269,6 +1270,7 @@ __device__ __forceinline__ bool reduce_stage(const Ctx &c, PipeState &ps, int s,
 }
 
 // The reducer warp walks the same sub-stages as the consumers.
+template <bool MOE>
 __device__ void reducer(const Ctx &c)
 {
     const Params &p = *c.p;
@@ -1281,7 +1283,7 @@ __device__ void reducer(const Ctx &c)
             const int l = lm ? g.L - 1 : k / 5;
             const int sid = lm ? SID_LM : k % 5;
             if (!stage_active(p, l, sid) || sid == SID_ATTN) continue;
-            if (reduce_stage(c, ps, stage_of(sid), l, step, false)) return;
+            if (reduce_stage<MOE>(c, ps, stage_of(sid), l, step, false)) return;
         }
     }
 }
@@ -1834,7 +1836,7 @@ __device__ __forceinline__ bool stage_lm_sample(const Ctx &c, int step, bool ab)
 // attention, O, gate/up, down, then the LM head -- through ONE loop body, so
 // that each stage's code exists once in the kernel and stays warm in the
 // instruction cache from one layer to the next.
-template <int FMT>
+template <int FMT, bool MOE>
 __device__ void consumer(const Ctx &c)
 {
     const Params &p = *c.p;
@@ -1878,8 +1880,8 @@ __device__ void consumer(const Ctx &c)
                 if (p.sched == SCHED_GRID && cons_grid_arrive(c, ab)) return;
                 trace_mark(c, step, k, TR_DONE);
             } else {
-                if (sid == SID_GU && g.E > 0 && route_experts(c, ps, l, step, ab)) return;
-                if (stage_gemv<FMT>(c, rc, ps, stage_of(sid), l, step, ab)) return;
+                if (MOE && sid == SID_GU && route_experts(c, ps, l, step, ab)) return;
+                if (stage_gemv<FMT, MOE>(c, rc, ps, stage_of(sid), l, step, ab)) return;
                 if (lm) {
                     // the reducer's keys of every LM-head tile of this CTA
                     bool fail = false;
@@ -2036,7 +2038,7 @@ __device__ __forceinline__ bool produce_tiles_direct(const Ctx &c, ProdRing &pr,
     return true;
 }
 
-template <bool kDirect>
+template <bool kDirect, bool MOE>
 __device__ void producer(const Ctx &c, const RepackSrc *w)
 {
     const Params &p = *c.p;
@@ -2082,7 +2084,7 @@ __device__ void producer(const Ctx &c, const RepackSrc *w)
             if (sid != SID_ATTN) {
                 const int st = sid == SID_QKV ? ST_QKV : sid == SID_O ? ST_O : sid == SID_GU ? ST_GU
                                                        : sid == SID_D ? ST_D : ST_LM;
-                if (g.E > 0 && (st == ST_GU || st == ST_D)) {
+                if (MOE && (st == ST_GU || st == ST_D)) {
                     if (st == ST_GU) {
                         // the consumers' expert choice for this layer
                         ok = wait_smem_ge(p, &c.misc[M_ROUTE], routes + 1u, 104, l, step);
@@ -2128,7 +2130,7 @@ __device__ void producer(const Ctx &c, const RepackSrc *w)
 
 // ---------------------------------------------------------------- kernel
 
-template <bool kDirect, int FMT>
+template <bool kDirect, int FMT, bool MOE = false>
 __device__ __forceinline__ void monokernel_body(const Params &p, const RepackSrc *w)
 {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -2179,7 +2181,7 @@ __device__ __forceinline__ void monokernel_body(const Params &p, const RepackSrc
     }
     __syncthreads();
     if (c.warp == W_PROD) {
-        if (c.lane == 0) producer<kDirect>(c, w);
+        if (c.lane == 0) producer<kDirect, MOE>(c, w);
         return;
     }
     if (c.warp == W_LOAD) {
@@ -2187,10 +2189,10 @@ __device__ __forceinline__ void monokernel_body(const Params &p, const RepackSrc
         return;
     }
     if (c.warp == W_RED) {
-        reducer(c);
+        reducer<MOE>(c);
         return;
     }
-    consumer<FMT>(c);
+    consumer<FMT, MOE>(c);
 }
 
 __global__ void __launch_bounds__(NTHREADS, 1) lf_monokernel(const __grid_constant__ Params p)
@@ -2202,6 +2204,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) lf_monokernel(const __grid_consta
 __global__ void __launch_bounds__(NTHREADS, 1) lf_monokernel_fp8(const __grid_constant__ Params p)
 {
     monokernel_body<false, FMT_FP8>(p, nullptr);
+}
+
+// The same kernel for a mixture-of-experts FFN (FP16 weights).
+__global__ void __launch_bounds__(NTHREADS, 1) lf_monokernel_moe(const __grid_constant__ Params p)
+{
+    monokernel_body<false, FMT_FP16, true>(p, nullptr);
 }
 
 // The same kernel for MXFP4 projection weights.
@@ -2298,6 +2306,8 @@ extern "C" cudaError_t lfk_set_smem(int smem_bytes)
         e = cudaFuncSetAttribute(lfk::lf_monokernel_fp8, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(lfk::lf_monokernel_mxfp4, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(lfk::lf_monokernel_moe, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     return e;
 }
 
@@ -2307,6 +2317,7 @@ extern "C" cudaError_t lfk_launch_monokernel(const lfk::Params *p, int smem_byte
     void *args[] = {const_cast<lfk::Params *>(p)};
     const void *fn = p->g.fmt == lfk::FMT_FP8     ? (const void *)lfk::lf_monokernel_fp8
                      : p->g.fmt == lfk::FMT_MXFP4 ? (const void *)lfk::lf_monokernel_mxfp4
+                     : p->g.E > 0                 ? (const void *)lfk::lf_monokernel_moe
                                                   : (const void *)lfk::lf_monokernel;
     if (cooperative)
         return cudaLaunchCooperativeKernel(fn, dim3(p->P), dim3(lfk::NTHREADS), args, (size_t)smem_bytes, stream);
