@@ -18,8 +18,7 @@ extern "C" cudaError_t lfk_set_smem(int smem_bytes);
 extern "C" cudaError_t lfk_launch_monokernel(const lfk::Params *p, int smem_bytes, cudaStream_t stream,
                                              int cooperative);
 extern "C" cudaError_t lfk_occupancy(int smem_bytes, int *blocks_per_sm);
-extern "C" unsigned lfk_smem_bytes(int ring_bytes, int a_floats, int b_slots, int d, int lm_rows_max, int L,
-                                   int router_halves);
+extern "C" unsigned lfk_smem_bytes(int ring_bytes, int a_floats, int b_slots, int d, int lm_rows_max, int L);
 extern "C" cudaError_t lfk_launch_mxfp4_interleave(const void *codes, const void *scales, size_t rows, int cols,
                                                    void *out, cudaStream_t stream);
 extern "C" cudaError_t lfk_launch_repack(lfk::Geo g, int P, const lfk::CtaPlan *plans, const void *wq,
@@ -32,7 +31,6 @@ namespace {
 constexpr int kAttnMinLen = 64;         // fewest positions per split-KV piece
 constexpr long long kDefaultTimeoutNs = 2000000000LL;
 constexpr int kL2PrefetchKB = 0;        // weight-stream lookahead into L2 per CTA (measured: no gain)
-constexpr long long kRouterSmemBytes = 48 << 10;   // largest router block staged in shared memory
 
 // Tuning override of the L2 lookahead, LF_L2_PREFETCH_KB (0 disables it).
 int l2_prefetch_bytes_from_env()
@@ -60,7 +58,6 @@ struct lf_handle {
     float *qbuf = nullptr, *attn = nullptr, *xattn = nullptr, *hbuf = nullptr, *xout = nullptr, *apart = nullptr;
     int *win = nullptr;            // [L] attention window per layer, or null (every layer: the whole cache)
     const __half *router = nullptr;  // mixture of experts: the caller's [L][E][d] router rows (read in place)
-    int router_halves = 0;           // > 0: one layer's router rows (E * d) are staged in shared memory
     float *wsc = nullptr;          // FP8 weights: copies of the eight per-row scale arrays, back to back
     size_t wsc_off[8] = {};
     int max_split = 1;
@@ -254,7 +251,6 @@ lfk::Params base_params(lf_handle *h)
     p.apart = h->apart;
     p.win = h->win;
     p.router = h->router;
-    p.router_smem = h->router_halves > 0 ? 1 : 0;
     for (int i = 0; i < 8; ++i) p.wsc[i] = h->wsc ? h->wsc + h->wsc_off[i] : nullptr;
     p.max_split = h->max_split;
     p.sig = h->sig;
@@ -447,18 +443,15 @@ lf_status lf_create(const lf_config *cfg, const lf_weights *w, lf_handle **out)
     // ---- shared memory: everything but the ring, then the largest ring that fits
     h->max_split = std::max(1, P / g.Hkv);
     lfk::act_sizes(g, h->plans.data(), P, h->max_split, h->a_floats, h->b_slots);
-    // mixture of experts: a layer's router rows go to shared memory with the FFN gain row when they
-    // take at most kRouterSmemBytes (else the consumers read them from global memory)
-    if (g.E > 0 && 2ll * g.E * g.d <= kRouterSmemBytes) h->router_halves = g.E * g.d;
-    const unsigned rest = lfk_smem_bytes(0, h->a_floats, h->b_slots, g.d, lm_rows_max, g.L, h->router_halves);
+    const unsigned rest = lfk_smem_bytes(0, h->a_floats, h->b_slots, g.d, lm_rows_max, g.L);
     if ((int)rest + 2 * lfk::ATT_CHUNK_BYTES > optin) {
         delete h;
         return LF_ERR_NOT_SUPPORTED;
     }
     h->ring_bytes = (int)(((unsigned)optin - rest) / 1024u * 1024u);
-    while ((int)lfk_smem_bytes(h->ring_bytes, h->a_floats, h->b_slots, g.d, lm_rows_max, g.L, h->router_halves) > optin)
+    while ((int)lfk_smem_bytes(h->ring_bytes, h->a_floats, h->b_slots, g.d, lm_rows_max, g.L) > optin)
         h->ring_bytes -= 1024;
-    h->smem_bytes = (int)lfk_smem_bytes(h->ring_bytes, h->a_floats, h->b_slots, g.d, lm_rows_max, g.L, h->router_halves);
+    h->smem_bytes = (int)lfk_smem_bytes(h->ring_bytes, h->a_floats, h->b_slots, g.d, lm_rows_max, g.L);
     if (h->ring_bytes < 2 * lfk::ATT_CHUNK_BYTES) {
         delete h;
         return LF_ERR_NOT_SUPPORTED;

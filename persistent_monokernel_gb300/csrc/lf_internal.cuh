@@ -222,7 +222,6 @@ struct Params {
     // w_up, w_down, lm_head in the caller's row order ([L][rows], [V])
     const float *wsc[8];
     const __half *router;        // [L][E][d] FP16 router rows (mixture of experts), or null
-    int router_smem;             // 1: the loader stages each layer's router rows in shared memory
     int max_split;
     unsigned *sig;               // [L][sig_layout().per_layer] readiness counters
     unsigned *attn_done;         // [L][Hkv] pieces of each KV head that have published

@@ -45,13 +45,12 @@ namespace lfk {
 
 struct SmemLayout {
     unsigned res, full, empty, chunk_end, afull, bfull, gfull, brel, red, hist, misc, plan;
-    unsigned ring, acta, actb, gain, lmkeys, win, router, total;
+    unsigned ring, acta, actb, gain, lmkeys, win, total;
 };
 
 __host__ __device__ inline unsigned align_up(unsigned x, unsigned a) { return (x + a - 1) / a * a; }
 
-__host__ __device__ inline SmemLayout smem_layout(int ring_bytes, int a_floats, int b_slots, int d, int lm_rows_max, int L,
-                                                  int router_halves)
+__host__ __device__ inline SmemLayout smem_layout(int ring_bytes, int a_floats, int b_slots, int d, int lm_rows_max, int L)
 {
     // Fixed-size parts first: their offsets are compile-time constants, so
     // their addresses cost no registers; the ring, the two activation buffers,
@@ -77,7 +76,6 @@ __host__ __device__ inline SmemLayout smem_layout(int ring_bytes, int a_floats, 
     s.gain = o;      o = align_up(o + 2u * (unsigned)d, 128);
     s.lmkeys = o;    o = align_up(o + 8u * (unsigned)lm_rows_max, 128);
     s.win = o;       o = align_up(o + 4u * (unsigned)L, 128);   // attention window of each layer
-    s.router = o;    o = align_up(o + 2u * (unsigned)router_halves, 128);   // one layer's router rows (or none)
     // the GEMV reads whole 8-row blocks: keep 7 rows of readable bytes after the ring
     const unsigned slack_end = s.ring + (unsigned)ring_bytes + 7u * KC_BYTES;
     s.total = o > slack_end ? o : align_up(slack_end, 128);
@@ -111,7 +109,6 @@ struct Ctx {
     unsigned *hist;
     unsigned *misc;
     const int *win;   // [L] attention window of each layer (0: whole cache), in shared memory
-    const __half *router_s;   // mixture of experts: the layer's router rows [E][d] in shared memory, or null
     int b;            // CTA index
     int tid, warp, lane;
 };
@@ -637,13 +634,8 @@ __device__ void loader(const Ctx &c)
                 a_mask = 0u;
                 a_par = ps.afill & 1u;
                 if (c.lane == 0) {
-                    // mixture of experts: the layer's router rows come with the FFN gain row
-                    const unsigned rbytes = (s == ST_GU && c.router_s) ? 2u * (unsigned)(g.E * g.d) : 0u;
-                    mbar_arrive_expect_tx(c.gfull, 2u * (unsigned)g.d + rbytes);
+                    mbar_arrive_expect_tx(c.gfull, 2u * (unsigned)g.d);
                     bulk_g2s(c.gain, in.gain, 2u * (unsigned)g.d, c.gfull, pol_gain);
-                    if (rbytes)
-                        bulk_g2s(const_cast<__half *>(c.router_s), p.router + (size_t)l * g.E * g.d, rbytes, c.gfull,
-                                 pol_gain);
                     g_arm = true;
                     g_par = a_par;
                 }
@@ -937,9 +929,7 @@ __device__ __forceinline__ bool route_experts(const Ctx &c, PipeState &ps, int l
                 const float2 g0 = h2f(gv.x), g1 = h2f(gv.y), g2 = h2f(gv.z), g3 = h2f(gv.w);
                 xa.x *= g0.x; xa.y *= g0.y; xa.z *= g1.x; xa.w *= g1.y;
                 xb.x *= g2.x; xb.y *= g2.y; xb.z *= g3.x; xb.w *= g3.y;
-                const uint4 wv = c.router_s ? lds_u4(smem_u32(c.router_s + (size_t)e * g.d + i))
-                                            : __ldg(reinterpret_cast<const uint4 *>(row + i));
-                acc = dot8(wv, xa, xb, acc);
+                acc = dot8(__ldg(reinterpret_cast<const uint4 *>(row + i)), xa, xb, acc);
             }
             acc = warp_sum(acc);
             if (c.lane == 0) logit[e] = acc;
@@ -2144,8 +2134,7 @@ template <bool kDirect, int FMT, bool MOE = false>
 __device__ __forceinline__ void monokernel_body(const Params &p, const RepackSrc *w)
 {
     extern __shared__ __align__(128) uint8_t smem[];
-    const SmemLayout L = smem_layout(p.ring_bytes, p.a_floats, p.b_slots, p.g.d, p.lm_rows_max, p.g.L,
-                                     p.router_smem ? p.g.E * p.g.d : 0);
+    const SmemLayout L = smem_layout(p.ring_bytes, p.a_floats, p.b_slots, p.g.d, p.lm_rows_max, p.g.L);
     Ctx c;
     c.p = &p;
     c.ring = smem + L.ring;
@@ -2164,7 +2153,6 @@ __device__ __forceinline__ void monokernel_body(const Params &p, const RepackSrc
     c.red = reinterpret_cast<float *>(smem + L.red);
     c.hist = reinterpret_cast<unsigned *>(smem + L.hist);
     c.misc = reinterpret_cast<unsigned *>(smem + L.misc);
-    c.router_s = p.router_smem ? reinterpret_cast<const __half *>(smem + L.router) : nullptr;
     {
         int *win = reinterpret_cast<int *>(smem + L.win);
         for (int i = threadIdx.x; i < p.g.L; i += blockDim.x) win[i] = p.win ? p.win[i] : 0;
@@ -2344,10 +2332,9 @@ extern "C" cudaError_t lfk_occupancy(int smem_bytes, int *blocks_per_sm)
                                                         (size_t)smem_bytes);
 }
 
-extern "C" unsigned lfk_smem_bytes(int ring_bytes, int a_floats, int b_slots, int d, int lm_rows_max, int L,
-                                   int router_halves)
+extern "C" unsigned lfk_smem_bytes(int ring_bytes, int a_floats, int b_slots, int d, int lm_rows_max, int L)
 {
-    return lfk::smem_layout(ring_bytes, a_floats, b_slots, d, lm_rows_max, L, router_halves).total;
+    return lfk::smem_layout(ring_bytes, a_floats, b_slots, d, lm_rows_max, L).total;
 }
 
 extern "C" cudaError_t lfk_launch_repack(lfk::Geo g, int P, const lfk::CtaPlan *plans, const void *wq, const void *wk,

@@ -26,8 +26,7 @@
 #include "../../include/lf.h"
 #include "lf_internal.cuh"
 
-extern "C" unsigned lfk_smem_bytes(int ring_bytes, int a_floats, int b_slots, int d, int lm_rows_max, int L,
-                                   int router_halves);
+extern "C" unsigned lfk_smem_bytes(int ring_bytes, int a_floats, int b_slots, int d, int lm_rows_max, int L);
 extern "C" cudaError_t lfk_set_smem_direct(int smem_bytes);
 extern "C" cudaError_t lfk_launch_monokernel_direct(const lfk::Params *p, const void *wq, const void *wk,
                                                     const void *wv, const void *wo, const void *wg, const void *wu,
@@ -132,11 +131,11 @@ extern "C" LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_w
     const int max_split = P / g.Hkv > 1 ? P / g.Hkv : 1;
     int a_floats = 0, b_slots = 0;
     lfk::act_sizes(g, h_plans, P, max_split, a_floats, b_slots);
-    const unsigned rest = lfk_smem_bytes(0, a_floats, b_slots, g.d, lm_rows_max, g.L, 0);
+    const unsigned rest = lfk_smem_bytes(0, a_floats, b_slots, g.d, lm_rows_max, g.L);
     if ((int)rest + 2 * lfk::ATT_CHUNK_BYTES > optin) return LF_ERR_NOT_SUPPORTED;
     int ring = (int)(((unsigned)optin - rest) / 1024u * 1024u);
-    while ((int)lfk_smem_bytes(ring, a_floats, b_slots, g.d, lm_rows_max, g.L, 0) > optin) ring -= 1024;
-    const int smem = (int)lfk_smem_bytes(ring, a_floats, b_slots, g.d, lm_rows_max, g.L, 0);
+    while ((int)lfk_smem_bytes(ring, a_floats, b_slots, g.d, lm_rows_max, g.L) > optin) ring -= 1024;
+    const int smem = (int)lfk_smem_bytes(ring, a_floats, b_slots, g.d, lm_rows_max, g.L);
 
     // ---- scratch layout inside the static array
     const size_t kv_elems = (size_t)g.L * g.Hkv * (size_t)g.max_seq * g.hd;
