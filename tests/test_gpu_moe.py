@@ -50,6 +50,8 @@ def _forced_run(dec, orc, cfg, prompt, n_steps, force_seed, T=0.0, top_k=0, seed
     (ModelConfig("moe-c", 3, 1024, 16, 4, 64, 1024, 8000, n_experts=16, top_k_experts=4), None),
     # 64 experts (two router logits per lane), 8 active
     (ModelConfig("moe-d", 1, 256, 4, 4, 64, 256, 2000, n_experts=64, top_k_experts=8), None),
+    # d 2,048 with 16 experts (wider router rows)
+    (ModelConfig("moe-e", 1, 2048, 16, 4, 128, 512, 2000, n_experts=16, top_k_experts=2), None),
 ])
 def test_moe_forced_parity(pm, cfg, window):
     dec, orc, _ = _setup(pm, cfg, 81, 200, layer_window=window)
