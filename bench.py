@@ -174,6 +174,24 @@ def dist_setup():
     return world, rank, local
 
 
+def max_over_ranks(seconds: float, dist=None, device="cuda") -> float:
+    """The job's time: the slowest rank's (all-reduce MAX); the rank's own
+    time when there is no process group."""
+    if dist is None:
+        return seconds
+    import torch
+    t = torch.tensor([seconds], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, steps_per_rank: int, t_max: float) -> float:
+    """Whole-job throughput of `world` replicas that each decode
+    `steps_per_rank` tokens of their own request: all tokens over the slowest
+    rank's time."""
+    return world * steps_per_rank / t_max
+
+
 def workload_desc(wl, K):
     m = wl.model
     samp = "greedy" if not wl.temperature > 0 else f"T={wl.temperature}, top-k {wl.top_k}, Philox seed {wl.sample_seed}"
@@ -285,18 +303,14 @@ def run_ours(args):
     clocks.start()
     t = timed_decode(K)
     clk = clocks.stop()
-    t_max = t
-    if dist:
-        tt = torch.tensor([t], device="cuda", dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t_max = float(tt.item())
+    t_max = max_over_ranks(t, dist)
 
     peak, peak_kind = hbm_peak()
     first_pos = wl.prompt_len - 1
     bytes_launch = wl.decode_bytes(first_pos, K)
     achieved = bytes_launch / t / 1e9
     tok_s_rank = K / t
-    value = world * K / t_max
+    value = job_tokens_per_s(world, K, t_max)
 
     result = {
         "metric": METRIC,
@@ -440,12 +454,9 @@ def run_ours(args):
         out = dec.generate(host_prompt.numpy(), K, **samp)
         t_e2e = time.perf_counter() - t0
         assert out.shape == (K,) and np.all((out >= 0) & (out < cfg.vocab))
-        if dist:
-            tt = torch.tensor([t_e2e], device="cuda", dtype=torch.float64)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            t_e2e = float(tt.item())
+        t_e2e = max_over_ranks(t_e2e, dist)
         result["e2e"] = {
-            "value": round(world * K / t_e2e, 2),
+            "value": round(job_tokens_per_s(world, K, t_e2e), 2),
             "unit": "tok/s",
             "h2d_bytes_per_step": round(4 * wl.prompt_len / K, 3),
             "d2h_bytes_per_step": 4,
