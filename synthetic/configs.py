@@ -126,6 +126,8 @@ MODELS = {
     "small": ModelConfig("small", 16, 1024, 16, 4, 64, 4096, 32000),
     "2.3b": ModelConfig("2.3b", 25, 2560, 20, 5, 128, 8192, 64000),
     "8b": ModelConfig("8b", 32, 4096, 32, 8, 128, 14336, 128256),
+    # two layers with the ~2.3B's attention shape: prefill-attention profiling on a small footprint
+    "attn-2l": ModelConfig("attn-2l", 2, 2560, 20, 5, 128, 2048, 8000),
     # the ~2.3B decoder's attention with 8 experts of half its FFN width per
     # layer, 2 active: 6.3B parameters, the 2.3B's bytes per token
     "moe-8x": ModelConfig("moe-8x", 25, 2560, 20, 5, 128, 4096, 64000, n_experts=8, top_k_experts=2),
@@ -145,6 +147,8 @@ WORKLOADS = {
     # the ~2.3B decoder with weight-only FP8 projections (the pages: FP8 streaming
     # halves the bytes that bound batch-1 decode)
     "2.3b-fp8": Workload("2.3b-fp8", MODELS["2.3b"], 2, 1002, 512, 1024, weights="fp8"),
+    # a 4,096-token prompt on the two-layer model: the batched prefill's attention at length
+    "prefill-4k": Workload("prefill-4k", MODELS["attn-2l"], 3, 4, 4096, 64),
     # mixture of experts (the pages: only the active experts' weights stream per token)
     "moe-8x": Workload("moe-8x", MODELS["moe-8x"], 4, 1002, 512, 1024),
     # the same with MXFP4 projections (the pages: "FP8/MXFP4" for frontier models)
