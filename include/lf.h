@@ -116,8 +116,10 @@ typedef struct {
      * 0, 0.5, 1, 1.5, 2, 3, 4, 6) and one E8M0 scale byte, 2^(E-127), per 32
      * consecutive elements of a row in the *_scale arrays; weight (r, k) =
      * e2m1 * 2^(E-127), dot products in FP32.  The embedding and the norm
-     * gains stay FP16.  lf_generate_noalloc takes FP16 weights only; MXFP4
-     * handles take prefill_block = 0 only. */
+     * gains stay FP16.  lf_generate_noalloc takes FP16 weights only.  The
+     * batched prefill of an MXFP4 model (prefill_block > 0) uses the weights
+     * decoded to FP16, which is exact for block scales 2^-23 .. 2^13 (E 104
+     * .. 140); lf_create rejects other scales there with NOT_SUPPORTED. */
     int32_t weight_format;
     /* Prefill implementation.  0: lf_prefill runs the prompt as repeated
      * decode steps inside the monokernel (one position per step, the
@@ -240,8 +242,9 @@ typedef struct {
  * non-positive sizes, a negative window or prefill_block), NOT_SUPPORTED
  * (shape: head_dim other than 64 or 128, d_model, n_heads*head_dim or
  * ffn_dim not a multiple of 256 or above 16384; an unknown weight_format;
- * MXFP4 with prefill_block > 0; an expert configuration outside the limits
- * of lf_config.n_experts), OUT_OF_MEMORY,
+ * MXFP4 block scales outside 2^-23 .. 2^13 with prefill_block > 0; an
+ * expert configuration outside the limits of lf_config.n_experts),
+ * OUT_OF_MEMORY,
  * NOT_RESIDENT, CUDA (also: the cuBLAS handle of the batched prefill could
  * not be created). */
 LF_API lf_status lf_create(const lf_config *cfg, const lf_weights *weights, lf_handle **out);

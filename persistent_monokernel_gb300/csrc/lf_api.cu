@@ -140,7 +140,6 @@ lf_status validate_config(const lf_config &c)
         c.weight_format != LF_WEIGHTS_MXFP4)
         return LF_ERR_NOT_SUPPORTED;
     if (c.prefill_block < 0) return LF_ERR_INVALID_ARG;
-    if (c.weight_format == LF_WEIGHTS_MXFP4 && c.prefill_block > 0) return LF_ERR_NOT_SUPPORTED;
     if (c.n_experts < 0 || c.top_k_experts < 0) return LF_ERR_INVALID_ARG;
     if (c.n_experts > 0) {
         // mixture of experts: up to 64 experts, 1..8 active, FP16 weights, prefill in the monokernel
@@ -172,7 +171,20 @@ lf_status setup_prefill(lf_handle *h, const lf_weights *w)
         wt += wlen[i];
         st += slen[i];
     }
-    const bool fp8 = g.fmt == lfk::FMT_FP8;
+    const bool fp8 = g.fmt == lfk::FMT_FP8, mx = g.fmt == lfk::FMT_MXFP4;
+    const void *bsc[7] = {w->wq_scale, w->wk_scale, w->wv_scale, w->wo_scale, w->w_gate_scale, w->w_up_scale,
+                          w->w_down_scale};
+    if (mx) {
+        // the FP16 copy is exact only for block scales 2^-23 .. 2^13 (E 104 .. 140)
+        const size_t nsc[7] = {L * Q * d / 32, L * KV * d / 32, L * KV * d / 32, L * d * Q / 32,
+                               L * F * d / 32, L * F * d / 32, L * d * F / 32};
+        for (int i = 0; i < 7; ++i) {
+            unsigned lo = 0, hi = 0;
+            const cudaError_t er = lfp_byte_range(static_cast<const uint8_t *>(bsc[i]), nsc[i], &lo, &hi);
+            if (er != cudaSuccess) return from_cuda(er);
+            if (lo < 104u || hi > 140u) return LF_ERR_NOT_SUPPORTED;
+        }
+    }
     const size_t ws_bytes = lfp_workspace_bytes(g, h->pf_block);
     cudaError_t e = dalloc(&h->pf_w, wt);
     if (e == cudaSuccess && fp8) e = dalloc(&h->pf_s, st);
@@ -200,7 +212,11 @@ lf_status setup_prefill(lf_handle *h, const lf_weights *w)
         const size_t n = pt.rows * pt.cols;
         for (size_t l = 0; l < L && e == cudaSuccess; ++l) {
             __half *dst = h->pf_w + h->pf_woff[pt.arr] + (l * arr_rows[pt.arr] + pt.row0) * pt.cols;
-            if (fp8) {
+            if (mx) {
+                e = lfp_decode_mxfp4(static_cast<const uint8_t *>(pt.src) + l * n / 2,
+                                     static_cast<const uint8_t *>(bsc[i]) + l * n / 32, pt.rows, (int)pt.cols, dst,
+                                     nullptr);
+            } else if (fp8) {
                 e = lfp_decode_e4m3(static_cast<const uint8_t *>(pt.src) + l * n, dst, n, nullptr);
                 if (e == cudaSuccess)
                     e = cudaMemcpy(h->pf_s + h->pf_soff[pt.arr] + l * arr_rows[pt.arr] + pt.row0,

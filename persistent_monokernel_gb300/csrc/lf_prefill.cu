@@ -126,6 +126,36 @@ __global__ void decode_e4m3(const uint8_t *src, __half *dst, size_t n)
         dst[i] = __half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)src[i], __NV_E4M3));
 }
 
+// MXFP4 -> FP16: element k of row r is the E2M1 nibble k (low nibble first)
+// times 2^(E - 127) of its 32-element block; exact in FP16 for block scales
+// 2^-23 .. 2^13 (lfp_mxfp4_scale_range checks them before the decode).
+__global__ void decode_mxfp4(const uint8_t *codes, const uint8_t *scales, size_t rows, int cols, __half *dst)
+{
+    const size_t n = rows * (size_t)cols;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        const size_t r = i / cols;
+        const int k = (int)(i % cols);
+        const unsigned byte = codes[r * (size_t)(cols / 2) + k / 2];
+        const unsigned nib = (k & 1) ? byte >> 4 : byte & 15u;
+        const int ex = (int)((nib >> 1) & 3u), man = (int)(nib & 1u);
+        // E2M1: exponent field 0 is the subnormal m * 0.5, else 2^(e-1) * (1 + m/2)
+        float mag = ex == 0 ? 0.5f * (float)man : ldexpf(1.0f + 0.5f * (float)man, ex - 1);
+        mag = ldexpf(mag, (int)scales[r * (size_t)(cols / 32) + k / 32] - 127);
+        dst[i] = __float2half_rn((nib & 8u) ? -mag : mag);
+    }
+}
+
+__global__ void byte_min_max(const uint8_t *s, size_t n, unsigned *out)
+{
+    unsigned lo = 255u, hi = 0u;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+        lo = min(lo, (unsigned)s[i]);
+        hi = max(hi, (unsigned)s[i]);
+    }
+    atomicMin(out, lo);
+    atomicMax(out + 1, hi);
+}
+
 // RoPE on the q and k heads of row t (rotate-half pairs (j, j + hd/2), the
 // FP32 table), q to Qr, K after RoPE and V rounded to FP16 into the cache at
 // position pos0 + t of layer l.  Thread u: pair unit u of the fused [q; k; v] row.
@@ -457,6 +487,31 @@ extern "C" cudaError_t lfp_decode_e4m3(const uint8_t *src, __half *dst, size_t n
 {
     lfp::decode_e4m3<<<lfp::grid_for(n), 256, 0, stream>>>(src, dst, n);
     return cudaGetLastError();
+}
+
+extern "C" cudaError_t lfp_decode_mxfp4(const uint8_t *codes, const uint8_t *scales, size_t rows, int cols,
+                                         __half *dst, cudaStream_t stream)
+{
+    lfp::decode_mxfp4<<<lfp::grid_for(rows * (size_t)cols), 256, 0, stream>>>(codes, scales, rows, cols, dst);
+    return cudaGetLastError();
+}
+
+extern "C" cudaError_t lfp_byte_range(const uint8_t *s, size_t n, unsigned *lo, unsigned *hi)
+{
+    unsigned *d = nullptr;
+    cudaError_t e = cudaMalloc(&d, 2 * sizeof(unsigned));
+    const unsigned init[2] = {255u, 0u};
+    if (e == cudaSuccess) e = cudaMemcpy(d, init, sizeof(init), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) {
+        lfp::byte_min_max<<<lfp::grid_for(n), 256>>>(s, n, d);
+        e = cudaGetLastError();
+    }
+    unsigned res[2] = {255u, 0u};
+    if (e == cudaSuccess) e = cudaMemcpy(res, d, sizeof(res), cudaMemcpyDeviceToHost);
+    if (d) cudaFree(d);
+    *lo = res[0];
+    *hi = res[1];
+    return e;
 }
 
 extern "C" int lfp_run(const lfp_args *a, cudaStream_t s)

@@ -50,3 +50,8 @@ extern "C" int lfp_cublas_create(void **out);
 extern "C" void lfp_cublas_destroy(void *h);
 // E4M3 codes -> FP16 (exact: every finite E4M3 value is an FP16 value).
 extern "C" cudaError_t lfp_decode_e4m3(const uint8_t *src, __half *dst, size_t n, cudaStream_t stream);
+// MXFP4 matrix [rows, cols] (packed E2M1 codes, E8M0 scales per 32) -> FP16, exact for scales 2^-23 .. 2^13.
+extern "C" cudaError_t lfp_decode_mxfp4(const uint8_t *codes, const uint8_t *scales, size_t rows, int cols,
+                                         __half *dst, cudaStream_t stream);
+// Smallest and largest of n device bytes (synchronous).
+extern "C" cudaError_t lfp_byte_range(const uint8_t *s, size_t n, unsigned *lo, unsigned *hi);

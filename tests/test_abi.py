@@ -85,8 +85,6 @@ def test_create_rejects_bad_arguments_before_touching_the_gpu(pm):
     assert L.lf_create(C.byref(cfg), C.byref(w), C.byref(h)) == 1
     w4 = pm.lf_weights(*([0x1000] * 12 + [0x2001] * 7 + [0]))
     assert L.lf_create(C.byref(cfg), C.byref(w4), C.byref(h)) == 1
-    cfg = pm.lf_config(**{**good, "weight_format": pm.WEIGHTS_MXFP4, "prefill_block": 16})
-    assert L.lf_create(C.byref(cfg), C.byref(w), C.byref(h)) == 7
     # mixture of experts: limits on the expert counts, FP16 only, the router pointer required
     for change, expect in [(dict(n_experts=-1), 1), (dict(n_experts=65, top_k_experts=2), 7),
                            (dict(n_experts=8, top_k_experts=0), 7), (dict(n_experts=8, top_k_experts=9), 7),

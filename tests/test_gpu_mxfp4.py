@@ -98,3 +98,26 @@ def test_mxfp4_decoder_reports_its_format(pm):
     L, d, F, V, Q, KV = cfg.n_layers, cfg.d_model, cfg.ffn_dim, cfg.vocab, cfg.q_dim, cfg.kv_dim
     groups = L * ((Q + 2 * KV) * d + d * Q + 3 * d * F) // 256 + V * d // 256
     assert dec.info()["weight_stream_bytes"] == 144 * groups
+
+
+@pytest.mark.parametrize("cfg,window", [
+    (MODELS["tiny"], None),
+    (ModelConfig("gqa128-mxpf", 2, 512, 8, 2, 128, 1024, 3000), [100, 0]),
+])
+def test_mxfp4_batched_prefill_parity(pm, cfg, window):
+    """The batched prefill on the FP16-decoded MXFP4 weights, then the MXFP4 decode kernel."""
+    dec, orc, _ = _setup(pm, cfg, 50, 300, gains="random", layer_window=window, prefill_block=48)
+    assert dec.info()["prefill_block"] == 48
+    prompt = make_prompt(cfg.vocab, 230, 51)
+    toks, lg, ref = _forced_run(dec, orc, cfg, prompt, 16, 52)
+    compare_logits(lg, ref)
+    check_tokens(toks, ref, 0.0, 0, 0, 229)
+
+
+def test_mxfp4_batched_prefill_rejects_scales_outside_the_exact_range(pm):
+    cfg = MODELS["tiny"]
+    wg = make_weights_mxfp4(cfg, 53, device="cuda")
+    wg["w_up_scale"][1, 3, 2] = 150          # 2^23: not exact in FP16
+    with pytest.raises(pm.LFError):
+        pm.Decoder(cfg, wg, 64, prefill_block=16)
+    pm.Decoder(cfg, wg, 64).close()          # the step-wise prefill takes any scale
