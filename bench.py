@@ -264,8 +264,7 @@ def run_ours(args):
     mk = {"fp8": make_weights_fp8, "mxfp4": make_weights_mxfp4}.get(wl.weights, make_weights)
     weights = mk(cfg, wl.weight_seed, device="cuda")
     prompt = make_prompt(cfg.vocab, wl.prompt_len, wl.prompt_seed).cuda()
-    # mixture-of-experts handles prefill as monokernel steps only
-    pf_block = 0 if cfg.n_experts else args.prefill_block
+    pf_block = args.prefill_block
     dec = pm.Decoder(cfg, weights, max_seq, layer_window=wl.layer_window, prefill_block=pf_block)
     info = dec.info()
     stream = torch.cuda.current_stream()

@@ -143,8 +143,12 @@ typedef struct {
      * RMSNorm output), takes the top_k_experts in [1, min(8, E)] largest
      * (ties to the lower index), weights expert j by the softmax of the
      * chosen logits, and streams only the chosen experts' rows.  Needs FP16
-     * weights, prefill_block = 0, top_k_experts * ffn_dim <= 16384 and a
-     * schedule other than LF_SCHED_MULTI_KERNEL. */
+     * weights, top_k_experts * ffn_dim <= 16384 and a schedule other than
+     * LF_SCHED_MULTI_KERNEL.  The batched prefill (prefill_block > 0) routes
+     * the block's tokens the same way and runs one GEMM per expert over the
+     * tokens routed to it; it reads the experts' token counts back to the
+     * host once per layer and block (lf_prefill then synchronizes its
+     * stream). */
     int32_t n_experts;
     int32_t top_k_experts;
 } lf_config;

@@ -142,11 +142,11 @@ lf_status validate_config(const lf_config &c)
     if (c.prefill_block < 0) return LF_ERR_INVALID_ARG;
     if (c.n_experts < 0 || c.top_k_experts < 0) return LF_ERR_INVALID_ARG;
     if (c.n_experts > 0) {
-        // mixture of experts: up to 64 experts, 1..8 active, FP16 weights, prefill in the monokernel
+        // mixture of experts: up to 64 experts, 1..8 active, FP16 weights
         if (c.n_experts > lfk::MAX_EXPERTS || c.top_k_experts < 1 || c.top_k_experts > lfk::MAX_ACTIVE_EXPERTS ||
             c.top_k_experts > c.n_experts)
             return LF_ERR_NOT_SUPPORTED;
-        if (c.weight_format != LF_WEIGHTS_FP16 || c.prefill_block > 0) return LF_ERR_NOT_SUPPORTED;
+        if (c.weight_format != LF_WEIGHTS_FP16) return LF_ERR_NOT_SUPPORTED;
         if ((long long)c.top_k_experts * c.ffn_dim > (long long)lfk::MAX_SLICES * lfk::KC) return LF_ERR_NOT_SUPPORTED;
     }
     return LF_OK;
@@ -162,7 +162,9 @@ lf_status setup_prefill(lf_handle *h, const lf_weights *w)
     const lfk::Geo &g = h->g;
     h->pf_block = std::min(h->cfg.prefill_block, g.max_seq);
     const size_t L = g.L, d = g.d, Q = g.Q, KV = g.KV, F = g.F, NQKV = Q + 2 * KV;
-    const size_t wlen[4] = {L * NQKV * d, L * d * Q, L * 2 * F * d, L * d * F};
+    // mixture of experts: gate/up [L][E][2 Fe][d] and down [L][E][d][Fe]
+    const size_t nexp = (size_t)lfk::n_expert_parts(g), Fw = g.E > 0 ? (size_t)g.Fe : F;
+    const size_t wlen[4] = {L * NQKV * d, L * d * Q, L * nexp * 2 * Fw * d, L * nexp * d * Fw};
     const size_t slen[4] = {L * NQKV, L * d, L * 2 * F, L * d};
     size_t wt = 0, st = 0;
     for (int i = 0; i < 4; ++i) {
@@ -207,7 +209,21 @@ lf_status setup_prefill(lf_handle *h, const lf_weights *w)
                            {w->wo, d, Q, 1, 0},      {w->w_gate, F, d, 2, 0},  {w->w_up, F, d, 2, F},
                            {w->w_down, d, F, 3, 0}};
     const size_t arr_rows[4] = {NQKV, d, 2 * F, d};
-    for (int i = 0; i < 7 && e == cudaSuccess; ++i) {
+    if (g.E > 0 && e == cudaSuccess) {
+        // each expert's gate rows, then its up rows; the down projections in the caller's layout
+        const size_t ge = Fw * d;
+        for (size_t le = 0; le < L * nexp && e == cudaSuccess; ++le) {
+            __half *dst = h->pf_w + h->pf_woff[2] + le * 2 * ge;
+            e = cudaMemcpy(dst, static_cast<const __half *>(w->w_gate) + le * ge, ge * sizeof(__half),
+                           cudaMemcpyDeviceToDevice);
+            if (e == cudaSuccess)
+                e = cudaMemcpy(dst + ge, static_cast<const __half *>(w->w_up) + le * ge, ge * sizeof(__half),
+                               cudaMemcpyDeviceToDevice);
+        }
+        if (e == cudaSuccess)
+            e = cudaMemcpy(h->pf_w + h->pf_woff[3], w->w_down, wlen[3] * sizeof(__half), cudaMemcpyDeviceToDevice);
+    }
+    for (int i = 0; i < (g.E > 0 ? 4 : 7) && e == cudaSuccess; ++i) {
         const Part &pt = parts[i];
         const size_t n = pt.rows * pt.cols;
         for (size_t l = 0; l < L && e == cudaSuccess; ++l) {
@@ -644,6 +660,7 @@ lf_status lf_prefill(lf_handle *h, const int32_t *tokens_dev, int32_t n, void *s
         a.so = fp8 ? h->pf_s + h->pf_soff[1] : nullptr;
         a.sgu = fp8 ? h->pf_s + h->pf_soff[2] : nullptr;
         a.sd = fp8 ? h->pf_s + h->pf_soff[3] : nullptr;
+        a.router = h->router;
         a.rope = h->rope;
         a.win = h->win;
         a.kc = h->kc;

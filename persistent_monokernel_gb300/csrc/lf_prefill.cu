@@ -23,6 +23,7 @@
 
 #include <algorithm>
 #include <cmath>
+#include <vector>
 
 #include "lf_internal.cuh"
 #include "lf_prefill.h"
@@ -154,6 +155,113 @@ __global__ void byte_min_max(const uint8_t *s, size_t n, unsigned *out)
     }
     atomicMin(out, lo);
     atomicMax(out + 1, hi);
+}
+
+// ---- mixture of experts
+
+// Token t's top-k experts from its router logits (ties to the lower index)
+// and the softmax of the chosen logits: one warp per token, the monokernel's rule.
+__global__ void route_tokens(const float *R, int E, int k, int *sel, float *gate)
+{
+    const int t = blockIdx.x, lane = threadIdx.x;
+    float v0 = lane < E ? R[(size_t)t * E + lane] : -INFINITY;
+    float v1 = lane + 32 < E ? R[(size_t)t * E + lane + 32] : -INFINITY;
+    float top[8];
+    for (int j = 0; j < k; ++j) {
+        float bv = v0;
+        int bi = lane;
+        if (v1 > bv) {
+            bv = v1;
+            bi = lane + 32;
+        }
+        for (int o = 16; o; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            if (ov > bv || (ov == bv && oi < bi)) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if (bi == lane) v0 = -INFINITY;
+        else if (bi == lane + 32) v1 = -INFINITY;
+        top[j] = bv;
+        if (lane == 0) sel[(size_t)t * 8 + j] = min(bi, E - 1);
+    }
+    if (lane == 0) {
+        float sum = 0.f;
+        for (int j = 0; j < k; ++j) sum += expf(top[j] - top[0]);
+        for (int j = 0; j < k; ++j) gate[(size_t)t * 8 + j] = expf(top[j] - top[0]) / sum;
+    }
+}
+
+// Per expert (one block each, 256 threads): the (token, slot) pairs routed to
+// it, in token order, as t * 8 + j, and their count.
+__global__ void build_lists(const int *sel, int T, int k, int *list, int *cnt)
+{
+    __shared__ int wsum[8];
+    const int e = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int base = 0;
+    for (int c0 = 0; c0 < T; c0 += 256) {
+        const int t = c0 + threadIdx.x;
+        int j = -1;
+        if (t < T)
+            for (int jj = 0; jj < k; ++jj)
+                if (sel[(size_t)t * 8 + jj] == e) j = jj;
+        const unsigned m = __ballot_sync(0xffffffffu, j >= 0);
+        if (lane == 0) wsum[warp] = __popc(m);
+        __syncthreads();
+        int before = 0, total = 0;
+        for (int w = 0; w < 8; ++w) {
+            if (w < warp) before += wsum[w];
+            total += wsum[w];
+        }
+        if (j >= 0) list[(size_t)e * T + base + before + __popc(m & ((1u << lane) - 1u))] = t * 8 + j;
+        base += total;
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) cnt[e] = base;
+}
+
+// Row i of the gathered input: the FFN input row of token list[i] / 8.
+__global__ void gather_rows(const __half *Xh, const __half *Xl, const int *list, int d, __half *Gh, __half *Gl)
+{
+    const size_t i = blockIdx.x, t = (size_t)(list[i] >> 3);
+    for (int c = threadIdx.x; c < d; c += blockDim.x) {
+        Gh[i * d + c] = Xh[t * d + c];
+        Gl[i * d + c] = Xl[t * d + c];
+    }
+}
+
+// h = gate * SiLU(g) * u for the n gathered rows of one expert, split.
+__global__ void silu_mul_gate_split(const float *GU, int n, int Fe, const int *list, const float *gatev,
+                                    __half *Hh, __half *Hl)
+{
+    const size_t total = (size_t)n * Fe;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+        const size_t r = i / Fe, c = i % Fe;
+        const float gt = GU[r * 2 * Fe + c], up = GU[r * 2 * Fe + Fe + c];
+        split_store(gatev[list[r]] * (gt / (1.0f + expf(-gt)) * up), Hh, Hl, i);
+    }
+}
+
+// The expert's output row i goes to its (token, slot) place.
+__global__ void scatter_rows(const float *Y, const int *list, int d, int k, float *Yk)
+{
+    const size_t i = blockIdx.x;
+    const int tj = list[i];
+    float *dst = Yk + ((size_t)(tj >> 3) * k + (tj & 7)) * d;
+    for (int c = threadIdx.x; c < d; c += blockDim.x) dst[c] = Y[i * d + c];
+}
+
+// X[t] += the slots' outputs, summed in slot order.
+__global__ void combine_slots(float *X, const float *Yk, int k, int d)
+{
+    const size_t t = blockIdx.x;
+    for (int c = threadIdx.x; c < d; c += blockDim.x) {
+        float acc = 0.f;
+        for (int j = 0; j < k; ++j) acc += Yk[(t * k + j) * d + c];
+        X[t * d + c] += acc;
+    }
 }
 
 // RoPE on the q and k heads of row t (rotate-half pairs (j, j + hd/2), the
@@ -427,41 +535,86 @@ cublasStatus_t gemm2(cublasHandle_t cb, const __half *W, int N, int K, const __h
 
 int grid_for(size_t n) { return (int)std::max<size_t>(1, std::min<size_t>((n + 255) / 256, 8 * 1024)); }
 
+// The mixture-of-experts FFN of layer l for the block's T rows (input in
+// w.Xh / w.Xl): router GEMM, routing, then per expert with tokens a gather,
+// the gate/up GEMM, the gated SiLU product, the down GEMM and a scatter to
+// the (token, slot) places; the slots are summed into the residual in order.
+int moe_ffn(const lfp_args *a, cublasHandle_t cb, cudaStream_t s, int l, int T, int *cnt_host)
+{
+    const Geo &g = a->g;
+    const lfp_workspace &w = a->ws;
+    const int E = g.E, k = g.topk, Fe = g.Fe, d = g.d;
+    if (gemm2(cb, a->router + (size_t)l * E * d, E, d, w.Xh, w.Xl, T, w.R, E)) return 3;
+    route_tokens<<<T, 32, 0, s>>>(w.R, E, k, w.sel, w.gate);
+    build_lists<<<E, 256, 0, s>>>(w.sel, T, k, w.list, w.cnt);
+    if (cudaMemcpyAsync(cnt_host, w.cnt, sizeof(int) * E, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return 1;
+    for (int e = 0; e < E; ++e) {
+        const int n = cnt_host[e];
+        if (n <= 0) continue;
+        const int *lst = w.list + (size_t)e * T;
+        const size_t ex = (size_t)l * E + e;
+        gather_rows<<<n, 256, 0, s>>>(w.Xh, w.Xl, lst, d, w.Xgh, w.Xgl);
+        if (gemm2(cb, a->wgu + ex * 2 * Fe * d, 2 * Fe, d, w.Xgh, w.Xgl, n, w.GU, 2 * Fe)) return 3;
+        silu_mul_gate_split<<<grid_for((size_t)n * Fe), 256, 0, s>>>(w.GU, n, Fe, lst, w.gate, w.Hh, w.Hl);
+        if (gemm2(cb, a->wd + ex * d * Fe, d, Fe, w.Hh, w.Hl, n, w.Y, d)) return 3;
+        scatter_rows<<<n, 256, 0, s>>>(w.Y, lst, d, k, w.Yk);
+    }
+    combine_slots<<<T, 256, 0, s>>>(w.X, w.Yk, k, d);
+    return 0;
+}
+
 size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 
 }  // namespace lfp
 
-size_t lfp_workspace_bytes(const lfk::Geo &g, int block)
+// The workspace's parts, carved from `base` (or only sized when base is null).
+static size_t lfp_layout(const lfk::Geo &g, int block, uint8_t *base, lfp_workspace *w)
 {
     using lfp::align256;
     const size_t T = (size_t)block;
     const size_t kmax = (size_t)std::max(g.d, std::max(g.Q, g.F));
     const size_t ymax = (size_t)std::max(g.Q + 2 * g.KV, g.d);
-    return align256(T * g.d * 4) + 2 * align256(T * kmax * 2) + align256(T * ymax * 4) + 2 * align256(T * g.Q * 4) +
-           align256(T * 2 * g.F * 4);
+    size_t o = 0;
+    auto take = [&](size_t bytes) -> void * {
+        void *p = base ? static_cast<void *>(base + o) : nullptr;
+        o += align256(bytes);
+        return p;
+    };
+    *w = lfp_workspace{};
+    w->X = static_cast<float *>(take(T * g.d * 4));
+    w->Xh = static_cast<__half *>(take(T * kmax * 2));
+    w->Xl = static_cast<__half *>(take(T * kmax * 2));
+    w->Y = static_cast<float *>(take(T * ymax * 4));
+    w->Qr = static_cast<float *>(take(T * g.Q * 4));
+    w->A = static_cast<float *>(take(T * g.Q * 4));
+    w->GU = static_cast<float *>(take(T * 2 * g.F * 4));
+    if (g.E > 0) {
+        w->R = static_cast<float *>(take(T * g.E * 4));
+        w->sel = static_cast<int *>(take(T * 8 * 4));
+        w->gate = static_cast<float *>(take(T * 8 * 4));
+        w->list = static_cast<int *>(take((size_t)g.E * T * 4));
+        w->cnt = static_cast<int *>(take((size_t)g.E * 4));
+        w->Xgh = static_cast<__half *>(take(T * g.d * 2));
+        w->Xgl = static_cast<__half *>(take(T * g.d * 2));
+        w->Hh = static_cast<__half *>(take(T * g.Fe * 2));
+        w->Hl = static_cast<__half *>(take(T * g.Fe * 2));
+        w->Yk = static_cast<float *>(take(T * g.topk * g.d * 4));
+    }
+    return o;
+}
+
+size_t lfp_workspace_bytes(const lfk::Geo &g, int block)
+{
+    lfp_workspace w;
+    return lfp_layout(g, block, nullptr, &w);
 }
 
 lfp_workspace lfp_carve(void *base, const lfk::Geo &g, int block)
 {
-    using lfp::align256;
-    const size_t T = (size_t)block;
-    const size_t kmax = (size_t)std::max(g.d, std::max(g.Q, g.F));
-    const size_t ymax = (size_t)std::max(g.Q + 2 * g.KV, g.d);
-    uint8_t *p = static_cast<uint8_t *>(base);
     lfp_workspace w;
-    w.X = reinterpret_cast<float *>(p);
-    p += align256(T * g.d * 4);
-    w.Xh = reinterpret_cast<__half *>(p);
-    p += align256(T * kmax * 2);
-    w.Xl = reinterpret_cast<__half *>(p);
-    p += align256(T * kmax * 2);
-    w.Y = reinterpret_cast<float *>(p);
-    p += align256(T * ymax * 4);
-    w.Qr = reinterpret_cast<float *>(p);
-    p += align256(T * g.Q * 4);
-    w.A = reinterpret_cast<float *>(p);
-    p += align256(T * g.Q * 4);
-    w.GU = reinterpret_cast<float *>(p);
+    lfp_layout(g, block, static_cast<uint8_t *>(base), &w);
     return w;
 }
 
@@ -527,6 +680,7 @@ extern "C" int lfp_run(const lfp_args *a, cudaStream_t s)
                         : cudaFuncSetAttribute(attn_flash<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, fa_smem);
     if (e != cudaSuccess) return 1;
     const lfp_workspace &w = a->ws;
+    std::vector<int> cnt_host(g.E > 0 ? g.E : 1);
     for (int t0 = 0; t0 < a->n; t0 += a->block) {
         const int T = std::min(a->block, a->n - t0);
         const int pos0 = a->pos0 + t0;
@@ -547,8 +701,13 @@ extern "C" int lfp_run(const lfp_args *a, cudaStream_t s)
             if (gemm2(cb, a->wo + (size_t)l * d * Q, d, Q, w.Xh, w.Xl, T, w.Y, d)) return 3;
             if (a->so) scale_cols<<<grid_for((size_t)T * d), 256, 0, s>>>(w.Y, T, d, d, a->so + (size_t)l * d);
             resid_add<<<grid_for((size_t)T * d), 256, 0, s>>>(w.X, w.Y, (size_t)T * d);
-            // SwiGLU block
+            // SwiGLU block (or the mixture of experts)
             rmsnorm_split<<<T, 256, 0, s>>>(w.X, a->ffn_norm + (size_t)l * d, d, a->eps, w.Xh, w.Xl);
+            if (g.E > 0) {
+                const int r = moe_ffn(a, cb, s, l, T, cnt_host.data());
+                if (r) return r;
+                continue;
+            }
             if (gemm2(cb, a->wgu + (size_t)l * 2 * F * d, 2 * F, d, w.Xh, w.Xl, T, w.GU, 2 * F)) return 3;
             if (a->sgu)
                 scale_cols<<<grid_for((size_t)T * 2 * F), 256, 0, s>>>(w.GU, T, 2 * F, 2 * F,

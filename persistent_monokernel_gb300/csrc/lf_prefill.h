@@ -15,6 +15,15 @@ struct lfp_workspace {
     float *Qr;          // [T, Q]   q after RoPE
     float *A;           // [T, Q]   attention output
     float *GU;          // [T, 2F]  gate and up projections
+    // mixture of experts only (null otherwise)
+    float *R;           // [T, E]   router logits
+    int *sel;           // [T, 8]   chosen experts, slot by slot
+    float *gate;        // [T, 8]   their gates (index t * 8 + j)
+    int *list;          // [E, T]   per expert: t * 8 + j of the tokens routed to it, in token order
+    int *cnt;           // [E]      list lengths
+    __half *Xgh, *Xgl;  // [T, d]   FFN input rows gathered for one expert
+    __half *Hh, *Hl;    // [T, Fe]  gated hidden units of one expert
+    float *Yk;          // [T, k, d] expert outputs per slot
 };
 
 // Bytes of the workspace for blocks of `block` positions, and its carving.
@@ -32,9 +41,11 @@ struct lfp_args {
     // row-major FP16 projections per layer, fused where the inputs are shared:
     // [L, Q + 2 KV, d] q/k/v rows, [L, d, Q], [L, 2F, d] gate rows then up rows,
     // [L, d, F]; FP8 models: the decoded E4M3 codes, and the FP32 row scales of
-    // the same layouts (null for FP16 models)
+    // the same layouts (null for FP16 models); MXFP4 models: the decoded
+    // weights; mixture of experts: wgu [L, E, 2 Fe, d], wd [L, E, d, Fe]
     const __half *wqkv, *wo, *wgu, *wd;
     const float *sqkv, *so, *sgu, *sd;
+    const __half *router;       // mixture of experts: the caller's [L, E, d] router rows, else null
     const float2 *rope;         // [max_seq, hd/2] (cos, sin)
     const int *win;             // [L] windows, or null
     __half *kc, *vc;            // KV cache, group-swizzled rows
@@ -43,7 +54,9 @@ struct lfp_args {
     lfp_workspace ws;
 };
 
-// Runs the passes on `stream`.  0 on success; 1 a launch failed; 2/3 cuBLAS failed.
+// Runs the passes on `stream`.  0 on success; 1 a launch or copy failed; 2/3 cuBLAS failed.  With a
+// mixture of experts each layer reads its per-expert token counts back to the host (the stream is
+// synchronized once per layer and block) to size the experts' GEMMs.
 extern "C" int lfp_run(const lfp_args *a, cudaStream_t stream);
 // cuBLAS handle lifetime (kept out of lf_api.cu so that only this file includes cuBLAS).
 extern "C" int lfp_cublas_create(void **out);

@@ -88,7 +88,7 @@ def test_create_rejects_bad_arguments_before_touching_the_gpu(pm):
     # mixture of experts: limits on the expert counts, FP16 only, the router pointer required
     for change, expect in [(dict(n_experts=-1), 1), (dict(n_experts=65, top_k_experts=2), 7),
                            (dict(n_experts=8, top_k_experts=0), 7), (dict(n_experts=8, top_k_experts=9), 7),
-                           (dict(n_experts=2, top_k_experts=3), 7), (dict(n_experts=8, top_k_experts=2, prefill_block=8), 7),
+                           (dict(n_experts=2, top_k_experts=3), 7),
                            (dict(n_experts=8, top_k_experts=2, weight_format=pm.WEIGHTS_FP8_E4M3), 7),
                            (dict(n_experts=8, top_k_experts=8, ffn_dim=4096), 7),
                            (dict(n_experts=8, top_k_experts=2), 1)]:      # no w_router

@@ -122,3 +122,20 @@ def test_full_size_moe_parity(pm):
     toks, lg, ref = _forced_run(dec, orc, cfg, prompt, 8, 89)
     compare_logits(lg, ref)
     assert check_tokens(toks, ref, 0.0, 0, 0, 23) >= 6
+
+
+@pytest.mark.parametrize("cfg,window", [
+    (ModelConfig("moe-a", 2, 256, 4, 4, 64, 512, 4096, n_experts=6, top_k_experts=2), None),
+    (ModelConfig("moe-b", 2, 512, 8, 2, 128, 256, 3000, n_experts=4, top_k_experts=1), [40, 0]),
+    (ModelConfig("moe-c", 3, 1024, 16, 4, 64, 1024, 8000, n_experts=16, top_k_experts=4), None),
+    (ModelConfig("moe-d", 1, 256, 4, 4, 64, 256, 2000, n_experts=64, top_k_experts=8), None),
+])
+def test_moe_batched_prefill_parity(pm, cfg, window):
+    """The batched prefill routes the block's tokens and runs one GEMM per
+    expert; the decode that follows must match the oracle."""
+    dec, orc, _ = _setup(pm, cfg, 95, 200, layer_window=window, prefill_block=32)
+    assert dec.info()["prefill_block"] == 32
+    prompt = make_prompt(cfg.vocab, 100, 96)
+    toks, lg, ref = _forced_run(dec, orc, cfg, prompt, 16, 97)
+    compare_logits(lg, ref)
+    check_tokens(toks, ref, 0.0, 0, 0, 99)
