@@ -72,10 +72,11 @@ def bf16_peak():
 
 def prefill_flops(wl, n: int) -> int:
     """Algorithmic FLOPs of the forward passes at positions 0 .. n-1 without
-    the LM head: 2 per weight of the seven layer projections per position, and
+    the LM head: 2 per weight of the seven layer projections per position (a
+    mixture of experts: the router and the active experts' weights), and
     4 * head_dim per query head per (query, key) pair attended (Q K^T and P V)."""
     m = wl.model
-    proj = (m.q_dim + 2 * m.kv_dim) * m.d_model + m.d_model * m.q_dim + 3 * m.d_model * m.ffn_dim
+    proj = (m.q_dim + 2 * m.kv_dim) * m.d_model + m.d_model * m.q_dim + m.active_ffn_weights()
     pairs = 0
     for l in range(m.n_layers):
         w = wl.layer_window[l] if wl.layer_window is not None else 0

@@ -37,3 +37,13 @@ def test_decode_bytes_match_a_brute_force_count():
             kv += (min(pos + 1, w) if w > 0 else pos + 1) * per_layer_pos
         want = m.weight_bytes_per_token("fp16") + kv + m.n_layers * per_layer_pos
         assert wl.bytes_per_step(pos) == want
+
+
+def test_prefill_flops_of_a_mixture_of_experts_count_the_router_and_the_active_experts():
+    from synthetic import ModelConfig
+    m = ModelConfig("m", 2, 64, 4, 2, 16, 96, 50, n_experts=6, top_k_experts=2)
+    wl = Workload("m", m, 0, 0, 30, 1)
+    attn = (64 * 64 + 2 * 32 * 64) + 64 * 64          # q, k, v and o projections
+    ffn = 6 * 64 + 2 * (2 * 96 * 64 + 64 * 96)        # router rows + two experts' gate, up, down
+    n = 11
+    assert bench.prefill_flops(wl, n) == 2 * 2 * (attn + ffn) * n + 4 * 4 * 16 * _pairs_brute(n, None, 2)
