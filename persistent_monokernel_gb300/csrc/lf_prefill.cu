@@ -129,7 +129,7 @@ __global__ void decode_e4m3(const uint8_t *src, __half *dst, size_t n)
 
 // MXFP4 -> FP16: element k of row r is the E2M1 nibble k (low nibble first)
 // times 2^(E - 127) of its 32-element block; exact in FP16 for block scales
-// 2^-23 .. 2^13 (lfp_mxfp4_scale_range checks them before the decode).
+// 2^-23 .. 2^13 (lf_create checks them with lfp_byte_range before the decode).
 __global__ void decode_mxfp4(const uint8_t *codes, const uint8_t *scales, size_t rows, int cols, __half *dst)
 {
     const size_t n = rows * (size_t)cols;
