@@ -525,7 +525,9 @@ def run_reference(args):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic: seeded FP16 weights ~N(0,0.02), seeded uniform prompt ids",
-        "config": {"workload": workload_desc(wl, K)},
+        "config": {"workload": workload_desc(wl, K), "prompt_len": wl.prompt_len,
+                   "parallelism": f"the CPU oracle on rank 0's host ({threads} threads); replicas x{world} requested",
+                   "l2": "host memory: the oracle reads every weight once per step"},
         "cpu_baseline": {"value": round(tok_s, 4), "unit": "tok/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(tok_s, 4), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
