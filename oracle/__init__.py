@@ -98,6 +98,7 @@ def lib():
             L.orc_vcache.restype = C.c_void_p
             L.orc_forward.argtypes = [C.c_void_p, C.c_int, f32p]
             L.orc_prefill.argtypes = [C.c_void_p, C.POINTER(C.c_int32), C.c_int]
+            L.orc_prefill_blocked.argtypes = [C.c_void_p, C.POINTER(C.c_int32), C.c_int, C.c_int]
             L.orc_decode.argtypes = [C.c_void_p, C.c_int, C.c_float, C.c_int, C.c_uint64,
                                      C.POINTER(C.c_int32), C.POINTER(C.c_int32), f32p]
             _lib = L
@@ -333,6 +334,14 @@ class OracleDecoder:
         t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
         if lib().orc_prefill(self._h, _i32(t), t.size):
             raise ValueError("orc_prefill failed (cache full or empty prompt)")
+
+    def prefill_blocked(self, tokens, block: int = 64):
+        """The same forward passes as prefill(), visited `block` positions at a
+        time (each weight row decoded once per block); the cache and state
+        equal prefill()'s bit for bit.  Dense FP16 models only."""
+        t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
+        if lib().orc_prefill_blocked(self._h, _i32(t), t.size, int(block)):
+            raise ValueError("orc_prefill_blocked failed (cache full, empty prompt or unsupported model)")
 
     def decode(self, n_steps: int, temperature: float = 0.0, top_k: int = 0, seed: int = 0,
                force_tokens=None, want_logits: bool = True):

@@ -580,6 +580,216 @@ ORC_API int orc_prefill(orc_model *m, const int32_t *tokens, int n)
     return 0;
 }
 
+/* ------------------------------------------------------------------------ */
+/* Prefill in blocks of positions (long prompts for stored test data)       */
+/* ------------------------------------------------------------------------ */
+
+/* Y[t][r] = sum_k W[r, k] * X[t][k] for the T rows of X: the sum of
+ * orc_matvec for every t, formed the same way (FP32 products of the decoded
+ * weight and x, added left to right in index order), with each weight row
+ * decoded from FP16 once for all T inputs.  XT holds X transposed, [k_dim][Tp]
+ * with Tp = T rounded up to a multiple of 8 (zero-padded), so that eight
+ * independent sums advance together. */
+static void orc_block_matvec(const uint16_t *W, const float *XT, int T, int Tp, int n_rows, int k_dim, float *Y)
+{
+    #pragma omp parallel
+    {
+        float *wrow = (float *)malloc(sizeof(float) * (size_t)k_dim);
+        #pragma omp for schedule(static)
+        for (int r = 0; r < n_rows; ++r) {
+            const uint16_t *row = W + (size_t)r * (size_t)k_dim;
+            for (int k = 0; k < k_dim; ++k) wrow[k] = orc_half_to_float(row[k]);
+            for (int t0 = 0; t0 < Tp; t0 += 8) {
+                float acc[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+                for (int k = 0; k < k_dim; ++k) {
+                    const float w = wrow[k];
+                    const float *xk = XT + (size_t)k * (size_t)Tp + t0;
+                    #pragma omp simd
+                    for (int u = 0; u < 8; ++u) acc[u] += w * xk[u];
+                }
+                for (int u = 0; u < 8 && t0 + u < T; ++u) Y[(size_t)(t0 + u) * (size_t)n_rows + r] = acc[u];
+            }
+        }
+        free(wrow);
+    }
+}
+
+/* orc_attend_head on K and V rows already converted to FP32 (the conversion
+ * is exact, so the values are the same): the same scores, each q . K_j summed
+ * over i in index order, eight positions j at a time as independent sums; the
+ * same softmax; o_i += p_j V_j,i over j in order.  Equal to orc_attend_head
+ * bit for bit (the blocked-prefill test compares the two paths). */
+static void orc_attend_head_f32(const float *q, const float *K, const float *V, int ctx, int hd, float scale,
+                                float *scores, float *out)
+{
+    float m = -INFINITY;
+    int j = 0;
+    for (; j + 8 <= ctx; j += 8) {
+        float acc[8] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+        const float *kj = K + (size_t)j * hd;
+        for (int i = 0; i < hd; ++i) {
+            const float qi = q[i];
+            for (int u = 0; u < 8; ++u) acc[u] += qi * kj[(size_t)u * hd + i];
+        }
+        for (int u = 0; u < 8; ++u) {
+            scores[j + u] = acc[u] * scale;
+            if (scores[j + u] > m) m = scores[j + u];
+        }
+    }
+    for (; j < ctx; ++j) {
+        const float *kj = K + (size_t)j * hd;
+        float dot = 0.0f;
+        for (int i = 0; i < hd; ++i) dot += q[i] * kj[i];
+        scores[j] = dot * scale;
+        if (scores[j] > m) m = scores[j];
+    }
+    float sum = 0.0f;
+    for (j = 0; j < ctx; ++j) { scores[j] = expf(scores[j] - m); sum += scores[j]; }
+    for (j = 0; j < ctx; ++j) scores[j] = scores[j] / sum;
+    for (int i = 0; i < hd; ++i) out[i] = 0.0f;
+    for (j = 0; j < ctx; ++j) {
+        const float pj = scores[j];
+        const float *vj = V + (size_t)j * hd;
+        #pragma omp simd
+        for (int i = 0; i < hd; ++i) out[i] += pj * vj[i];
+    }
+}
+
+/* X [T][k_dim] -> XT [k_dim][Tp], zero-padded to Tp columns. */
+static void orc_transpose_pad(const float *X, int T, int Tp, int k_dim, float *XT)
+{
+    for (int k = 0; k < k_dim; ++k) {
+        float *dst = XT + (size_t)k * (size_t)Tp;
+        for (int t = 0; t < T; ++t) dst[t] = X[(size_t)t * (size_t)k_dim + k];
+        for (int t = T; t < Tp; ++t) dst[t] = 0.0f;
+    }
+}
+
+/* The forward passes of orc_prefill -- the pending token (if any), then
+ * tokens[0 .. n-2], tokens[n-1] left pending -- taken `block` positions at a
+ * time.  Nothing in the arithmetic of one position changes: every norm,
+ * product, sum (index order), rotation, rounding of K and V to FP16 and
+ * softmax is orc_forward's, and attention at position p reads cache rows
+ * j0 .. p exactly as it would after the earlier forward passes (the block's
+ * K and V rows of a layer are stored before that layer's attention runs).
+ * Only the order in which independent positions are visited changes: within
+ * a layer every position of the block goes through one projection before the
+ * next starts, so each weight row is decoded once per block instead of once
+ * per position, and attention reads FP32 copies of the cache rows
+ * (orc_attend_head_f32).  The cache and the pending state therefore equal those of
+ * orc_prefill bit for bit (checked by a test).  Dense FP16 models only (FP8,
+ * MXFP4 and mixture-of-experts models: orc_prefill).  Returns 0, or -1 on a
+ * bad argument, a full cache, an unsupported model or a failed allocation. */
+ORC_API int orc_prefill_blocked(orc_model *m, const int32_t *tokens, int n, int block)
+{
+    const orc_config *c = &m->c;
+    const orc_weights *w = &m->w;
+    const int L = c->n_layers, d = c->d_model, Hq = c->n_heads, Hkv = c->n_kv_heads, hd = c->head_dim;
+    const int F = c->ffn_dim, Q = Hq * hd, KV = Hkv * hd, group = Hq / Hkv;
+    if (n < 1 || block < 1 || m->fp8 || m->mxfp4 || m->n_experts > 0) return -1;
+    const int has_pending = m->pending >= 0;
+    const int n_pass = n - 1 + has_pending;
+    if (m->pos + n_pass + 1 > c->max_seq) return -1;
+    for (int i = 0; i < n; ++i) if (tokens[i] < 0 || tokens[i] >= c->vocab) return -1;
+    const float scale = 1.0f / sqrtf((float)hd);
+    const int Tp_max = (block + 7) / 8 * 8;
+    const int wide = Q > F ? (Q > d ? Q : d) : (F > d ? F : d);
+    float *X = (float *)malloc(sizeof(float) * (size_t)block * d);
+    float *XN = (float *)malloc(sizeof(float) * (size_t)block * wide);
+    float *XT = (float *)malloc(sizeof(float) * (size_t)Tp_max * wide);
+    float *Yq = (float *)malloc(sizeof(float) * (size_t)block * Q);
+    float *Yk = (float *)malloc(sizeof(float) * (size_t)block * KV);
+    float *Yv = (float *)malloc(sizeof(float) * (size_t)block * KV);
+    float *A = (float *)malloc(sizeof(float) * (size_t)block * Q);
+    float *G = (float *)malloc(sizeof(float) * (size_t)block * F);
+    float *U = (float *)malloc(sizeof(float) * (size_t)block * F);
+    float *Y = (float *)malloc(sizeof(float) * (size_t)block * d);
+    int nthr = 1;
+#ifdef _OPENMP
+    nthr = omp_get_max_threads();
+#endif
+    float *scr = (float *)malloc(sizeof(float) * (size_t)nthr * (size_t)c->max_seq);
+    /* FP32 copies of the cache rows (exact), converted once per row */
+    const size_t kv_elems = (size_t)L * Hkv * (size_t)c->max_seq * hd;
+    float *kf = (float *)malloc(sizeof(float) * kv_elems);
+    float *vf = (float *)malloc(sizeof(float) * kv_elems);
+    int rc = 0;
+    if (!X || !XN || !XT || !Yq || !Yk || !Yv || !A || !G || !U || !Y || !scr || !kf || !vf) rc = -1;
+    for (int l = 0; rc == 0 && l < L; ++l)
+        for (int g = 0; g < Hkv; ++g) {
+            const size_t base = ((size_t)l * Hkv + g) * (size_t)c->max_seq * hd;
+            for (size_t i = 0; i < (size_t)m->pos * hd; ++i) {
+                kf[base + i] = orc_half_to_float(m->kcache[base + i]);
+                vf[base + i] = orc_half_to_float(m->vcache[base + i]);
+            }
+        }
+    for (int b0 = 0; rc == 0 && b0 < n_pass; b0 += block) {
+        const int T = n_pass - b0 < block ? n_pass - b0 : block;
+        const int Tp = (T + 7) / 8 * 8;
+        const int p0 = m->pos;
+        for (int t = 0; t < T; ++t) {
+            const int i = b0 + t;   /* pass i: the pending token first, then the prompt */
+            const int tok = has_pending ? (i == 0 ? m->pending : tokens[i - 1]) : tokens[i];
+            for (int k = 0; k < d; ++k) X[(size_t)t * d + k] = orc_half_to_float(w->embed[(size_t)tok * d + k]);
+        }
+        for (int l = 0; l < L; ++l) {
+            /* attention block */
+            for (int t = 0; t < T; ++t)
+                orc_rmsnorm(X + (size_t)t * d, w->attn_norm + (size_t)l * d, d, c->rms_eps, XN + (size_t)t * d);
+            orc_transpose_pad(XN, T, Tp, d, XT);
+            orc_block_matvec(w->wq + (size_t)l * Q * d, XT, T, Tp, Q, d, Yq);
+            orc_block_matvec(w->wk + (size_t)l * KV * d, XT, T, Tp, KV, d, Yk);
+            orc_block_matvec(w->wv + (size_t)l * KV * d, XT, T, Tp, KV, d, Yv);
+            for (int t = 0; t < T; ++t) {
+                const int p = p0 + t;
+                for (int h = 0; h < Hq; ++h) orc_rope(Yq + (size_t)t * Q + h * hd, hd, p, c->rope_theta);
+                for (int g = 0; g < Hkv; ++g) orc_rope(Yk + (size_t)t * KV + g * hd, hd, p, c->rope_theta);
+                for (int g = 0; g < Hkv; ++g) {
+                    const size_t base = (((size_t)l * Hkv + g) * (size_t)c->max_seq + (size_t)p) * hd;
+                    for (int i = 0; i < hd; ++i) {
+                        m->kcache[base + i] = orc_float_to_half(Yk[(size_t)t * KV + g * hd + i]);
+                        m->vcache[base + i] = orc_float_to_half(Yv[(size_t)t * KV + g * hd + i]);
+                        kf[base + i] = orc_half_to_float(m->kcache[base + i]);
+                        vf[base + i] = orc_half_to_float(m->vcache[base + i]);
+                    }
+                }
+            }
+            #pragma omp parallel for schedule(dynamic, 1)
+            for (int th = 0; th < T * Hq; ++th) {
+                const int t = th / Hq, h = th % Hq, g = h / group, p = p0 + t;
+                int j0 = 0;
+                if (m->window[l] > 0 && p + 1 > m->window[l]) j0 = p + 1 - m->window[l];
+                int me = 0;
+#ifdef _OPENMP
+                me = omp_get_thread_num();
+#endif
+                const size_t base = (((size_t)l * Hkv + g) * (size_t)c->max_seq + (size_t)j0) * hd;
+                orc_attend_head_f32(Yq + (size_t)t * Q + h * hd, kf + base, vf + base, p + 1 - j0, hd, scale,
+                                    scr + (size_t)me * c->max_seq, A + (size_t)t * Q + h * hd);
+            }
+            orc_transpose_pad(A, T, Tp, Q, XT);
+            orc_block_matvec(w->wo + (size_t)l * d * Q, XT, T, Tp, d, Q, Y);
+            for (size_t i = 0; i < (size_t)T * d; ++i) X[i] = X[i] + Y[i];
+
+            /* FFN block */
+            for (int t = 0; t < T; ++t)
+                orc_rmsnorm(X + (size_t)t * d, w->ffn_norm + (size_t)l * d, d, c->rms_eps, XN + (size_t)t * d);
+            orc_transpose_pad(XN, T, Tp, d, XT);
+            orc_block_matvec(w->w_gate + (size_t)l * F * d, XT, T, Tp, F, d, G);
+            orc_block_matvec(w->w_up + (size_t)l * F * d, XT, T, Tp, F, d, U);
+            for (size_t i = 0; i < (size_t)T * F; ++i) G[i] = orc_silu(G[i]) * U[i];
+            orc_transpose_pad(G, T, Tp, F, XT);
+            orc_block_matvec(w->w_down + (size_t)l * d * F, XT, T, Tp, d, F, Y);
+            for (size_t i = 0; i < (size_t)T * d; ++i) X[i] = X[i] + Y[i];
+        }
+        m->pos = p0 + T;
+    }
+    if (rc == 0) m->pending = tokens[n - 1];
+    free(X); free(XN); free(XT); free(Yq); free(Yk); free(Yv); free(A); free(G); free(U); free(Y); free(scr);
+    free(kf); free(vf);
+    return rc;
+}
+
 /* n_steps decode steps.  Step i runs the forward pass of the pending token at
  * position pos, chooses a token from its logits (orc_sample, keyed by that
  * position), writes it to out_tokens[i] and makes it the pending token -- or,

@@ -246,3 +246,44 @@ def test_window_of_one_makes_every_position_see_only_itself():
         o.forward(t)
     again = o.forward(7)
     np.testing.assert_array_equal(first, again)
+
+
+@pytest.mark.parametrize("block", [1, 3, 8, 13, 64])
+@pytest.mark.parametrize("window", [None, (5, 0)])
+def test_blocked_prefill_equals_position_by_position_prefill(block, window):
+    """orc_prefill_blocked only reorders independent positions: its KV cache
+    and the logits of the following decode steps equal orc_prefill's bit for
+    bit, with a pending token carried over between two prefill calls, a block
+    that does not divide the prompt, and sliding windows."""
+    cfg = TINYCFG.with_(n_heads=4, n_kv_heads=2, head_dim=8, d_model=32, ffn_dim=48)
+    w = _w(cfg, 21)
+    for k in ("wq", "wk"):
+        w[k] = (w[k].astype(np.float32) * 30).astype(np.float16)
+    seq = make_prompt(cfg.vocab, 40, 8).numpy()
+    a = oracle.OracleDecoder(cfg, w, 48, layer_window=window)
+    b = oracle.OracleDecoder(cfg, w, 48, layer_window=window)
+    a.prefill(seq[:11])
+    a.prefill(seq[11:30])
+    b.prefill_blocked(seq[:11], block)
+    b.prefill_blocked(seq[11:30], block)
+    assert a.pos == b.pos == 29 and a.pending == b.pending == int(seq[29])
+    ka, va = a.kv_cache()
+    kb, vb = b.kv_cache()
+    assert np.array_equal(ka.view(np.uint16), kb.view(np.uint16))
+    assert np.array_equal(va.view(np.uint16), vb.view(np.uint16))
+    ta, la = a.decode(6, force_tokens=seq[30:36])
+    tb, lb = b.decode(6, force_tokens=seq[30:36])
+    assert np.array_equal(la.view(np.uint32), lb.view(np.uint32))
+    assert np.array_equal(ta, tb)
+
+
+def test_blocked_prefill_rejects_what_it_does_not_cover():
+    cfg = MODELS["tiny"]
+    w = _w(cfg, 0, gains="ones")
+    o = oracle.OracleDecoder(cfg, w, 8)
+    with pytest.raises(ValueError):
+        o.prefill_blocked(np.arange(9, dtype=np.int32), 4)    # cache too small
+    with pytest.raises(ValueError):
+        o.prefill_blocked(np.array([1, cfg.vocab], dtype=np.int32), 4)   # bad token id
+    with pytest.raises(ValueError):
+        o.prefill_blocked(np.arange(4, dtype=np.int32), 0)    # empty block
