@@ -257,7 +257,10 @@ LF_API lf_status lf_create(const lf_config *cfg, const lf_weights *weights, lf_h
  * Accepts NULL. */
 LF_API void lf_destroy(lf_handle *h);
 
-/* Prefill: runs the forward pass of the pending token (if any) and of
+/* Prefill (the per-token decode pass of shivam2003.com, "KOG LaneFormer-2B
+ * & the monokernel", sections "Pillar 3 -- the monokernel runtime" and "The
+ * fused operations, briefly", run once per prompt position without sampling):
+ * runs the forward pass of the pending token (if any) and of
  * tokens_dev[0 .. n-2] at consecutive positions, appending their K and V to
  * the cache, and makes tokens_dev[n-1] the pending token.  No logits are
  * computed.  With lf_config.prefill_block = 0 the passes are repeated decode
@@ -267,7 +270,11 @@ LF_API void lf_destroy(lf_handle *h);
  * these tokens plus the pending one), STATE (latched device error). */
 LF_API lf_status lf_prefill(lf_handle *h, const int32_t *tokens_dev, int32_t n, void *stream);
 
-/* n_steps decode steps in one persistent launch.  Step i runs the forward
+/* n_steps decode steps in one persistent launch (shivam2003.com, "KOG
+ * LaneFormer-2B & the monokernel", section "Pillar 3 -- the monokernel
+ * runtime": the kernel stays resident until the token is produced; here it
+ * stays resident for n_steps tokens, feeding each sampled token to the next
+ * step on the device).  Step i runs the forward
  * pass of the pending token at the current position, chooses a token from
  * its logits (lf_sampling), writes it to out_tokens_dev[i] (device int32
  * [n_steps]) and makes it the pending token.  The position advances by
@@ -334,7 +341,9 @@ LF_API lf_status lf_read_trace(lf_handle *h, uint64_t *host_out, int64_t capacit
  * (row-major, nn.Linear layout), so every buffer in w must stay valid until
  * the call returns.  prompt_dev (device int32 [n_prompt]) and out_tokens_dev
  * (device int32 [n_steps]) belong to the caller; sp works as for lf_decode.
- * cfg->max_seq bounds n_prompt + n_steps; cfg->fault_step is ignored.
+ * The forward passes use positions 0 .. n_prompt + n_steps - 2, so
+ * n_prompt - 1 + n_steps must not exceed cfg->max_seq (the bound of
+ * lf_prefill followed by lf_decode on a handle); cfg->fault_step is ignored.
  *
  * All scratch -- partition, RoPE table, FP16 KV cache, activations, counters,
  * attention partials, sampling candidates -- lives in one file-scope device
@@ -346,8 +355,12 @@ LF_API lf_status lf_read_trace(lf_handle *h, uint64_t *host_out, int64_t capacit
  * The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) and sets the kernel's shared-memory limit; make that
  * first call before any stream capture.  Every call reuses the same array and
- * clears the counters it relies on; calls whose work overlaps on the GPU, or
- * calls from two host threads at once, race on the array: serialise them.
+ * clears the counters it relies on; calls whose work overlaps on the GPU race
+ * on the array.  The host staging buffers of the partition and the RoPE table
+ * are shared by the whole process, so calls from two host threads at once
+ * race even when they use different GPUs: serialise them.  Once a call has
+ * queued work on `stream`, every error return first synchronizes `stream`,
+ * so that no copy or kernel of the failed call still uses the array.
  * The call synchronizes `stream` and returns the device status (LF_OK,
  * LF_ERR_TIMEOUT, or LF_ERR_INVALID_ARG for a token id outside [0, vocab)).
  * Other errors: INVALID_ARG, NOT_SUPPORTED (also: FP8 or MXFP4 weights,

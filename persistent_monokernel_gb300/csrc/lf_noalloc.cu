@@ -17,7 +17,10 @@
 // the device reuses the same array, which keeps the previous call's contents;
 // each call clears the counters and status words it relies on.  Calls whose
 // work overlaps on the GPU race on the array, and so do calls from two host
-// threads at once: serialise them.
+// threads at once -- also on two different GPUs, since the host staging
+// buffers below are shared by the whole process: serialise them.  Once any
+// work is queued, every error return first synchronizes the stream, so that
+// no queued copy or kernel still uses the array when the call returns.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -50,6 +53,16 @@ int g_smem_set[kMaxDevices];        // dynamic shared memory size set for the ke
 // Host staging for the partition and the RoPE table (static: no host allocation either).
 lfk::CtaPlan h_plans[kMaxCtas];
 float2 h_rope[LF_NOALLOC_SCRATCH_BYTES / sizeof(float2)];
+
+// Error return once work that touches the scratch array is queued on `st`:
+// wait for that work first, so that nothing still reads or writes the array
+// when the call returns and the caller may retry at once.  The wait's own
+// error is ignored (the call already failed).
+lf_status drain_and_fail(cudaStream_t st, lf_status s)
+{
+    (void)cudaStreamSynchronize(st);
+    return s;
+}
 
 size_t carve(size_t &off, size_t bytes)
 {
@@ -86,7 +99,9 @@ extern "C" LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_w
     if (cfg->layer_window)
         for (int l = 0; l < cfg->n_layers; ++l)
             if (cfg->layer_window[l] < 0) return LF_ERR_INVALID_ARG;
-    if ((long long)n_prompt + n_steps > cfg->max_seq) return LF_ERR_CAPACITY;
+    // the forward passes use positions 0 .. n_prompt + n_steps - 2 (the bound of
+    // lf_prefill followed by lf_decode on a handle)
+    if ((long long)n_prompt - 1 + n_steps > cfg->max_seq) return LF_ERR_CAPACITY;
 
     lfk::Geo g;
     g.L = cfg->n_layers;
@@ -135,6 +150,7 @@ extern "C" LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_w
     if ((int)rest + 2 * lfk::ATT_CHUNK_BYTES > optin) return LF_ERR_NOT_SUPPORTED;
     int ring = (int)(((unsigned)optin - rest) / 1024u * 1024u);
     while ((int)lfk_smem_bytes(ring, a_floats, b_slots, g.d, lm_rows_max, g.L) > optin) ring -= 1024;
+    if (ring < 2 * lfk::ATT_CHUNK_BYTES) return LF_ERR_NOT_SUPPORTED;   // as lf_create: one K/V sub-block must fit
     const int smem = (int)lfk_smem_bytes(ring, a_floats, b_slots, g.d, lm_rows_max, g.L);
 
     // ---- scratch layout inside the static array
@@ -187,7 +203,7 @@ extern "C" LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_w
     if (e == cudaSuccess) e = cudaMemsetAsync(base + o_status, 0, 4 * 8, st);
     if (e == cudaSuccess && windowed)
         e = cudaMemcpyAsync(base + o_win, cfg->layer_window, sizeof(int) * g.L, cudaMemcpyHostToDevice, st);
-    if (e != cudaSuccess) return LF_ERR_CUDA;
+    if (e != cudaSuccess) return drain_and_fail(st, LF_ERR_CUDA);
 
     lfk::Params p;
     std::memset(&p, 0, sizeof(p));
@@ -240,10 +256,11 @@ extern "C" LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_w
         q.prompt = prompt_dev;
         e = lfk_launch_monokernel_direct(&q, w->wq, w->wk, w->wv, w->wo, w->w_gate, w->w_up, w->w_down, w->lm_head,
                                          smem, st);
-        if (e != cudaSuccess) return e == cudaErrorCooperativeLaunchTooLarge ? LF_ERR_NOT_RESIDENT : LF_ERR_CUDA;
+        if (e != cudaSuccess)
+            return drain_and_fail(st, e == cudaErrorCooperativeLaunchTooLarge ? LF_ERR_NOT_RESIDENT : LF_ERR_CUDA);
     }
     e = cudaMemcpyAsync(p.tok_buf, prompt_dev + (n_prompt - 1), sizeof(int32_t), cudaMemcpyDeviceToDevice, st);
-    if (e != cudaSuccess) return LF_ERR_CUDA;
+    if (e != cudaSuccess) return drain_and_fail(st, LF_ERR_CUDA);
 
     // ---- decode n_steps tokens
     lfk::Params q = p;
@@ -259,13 +276,14 @@ extern "C" LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_w
     q.seed = seed;
     e = lfk_launch_monokernel_direct(&q, w->wq, w->wk, w->wv, w->wo, w->w_gate, w->w_up, w->w_down, w->lm_head,
                                      smem, st);
-    if (e != cudaSuccess) return e == cudaErrorCooperativeLaunchTooLarge ? LF_ERR_NOT_RESIDENT : LF_ERR_CUDA;
+    if (e != cudaSuccess)
+        return drain_and_fail(st, e == cudaErrorCooperativeLaunchTooLarge ? LF_ERR_NOT_RESIDENT : LF_ERR_CUDA);
 
     // ---- wait for the request and report the device status
     unsigned status[4] = {0, 0, 0, 0};
     e = cudaMemcpyAsync(status, p.status, sizeof(status), cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-    if (e != cudaSuccess) return LF_ERR_CUDA;
+    if (e != cudaSuccess) return drain_and_fail(st, LF_ERR_CUDA);
     if (status[0] == (unsigned)lfk::STATUS_TIMEOUT) return LF_ERR_TIMEOUT;
     if (status[0] != 0u) return LF_ERR_INVALID_ARG;
     return LF_OK;
