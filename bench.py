@@ -87,6 +87,22 @@ def prefill_flops(wl, n: int) -> int:
     return 2 * m.n_layers * proj * n + 4 * m.n_heads * m.head_dim * pairs
 
 
+def roofline_tok_s(bytes_per_token: float, bw_gbs: float) -> float:
+    """The bandwidth-bound ceiling of batch-1 decode: tokens/s when every
+    step's bytes stream at bw_gbs (GB/s) and nothing else costs time."""
+    return bw_gbs * 1e9 / bytes_per_token
+
+
+def bandwidth_fraction(tok_s: float, bytes_per_token: float, bw_gbs: float) -> float:
+    """Achieved bytes/s of a decode rate as a fraction of bw_gbs (the
+    memory-bandwidth utilisation of the pages' figures)."""
+    return tok_s * bytes_per_token / (bw_gbs * 1e9)
+
+
+def us_per_token(tok_s: float) -> float:
+    return 1e6 / tok_s
+
+
 def hbm_peak():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -341,6 +357,8 @@ def run_ours(args):
         },
         "hbm_gbs": round(achieved, 1),
         "hbm_frac_of_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
+        "ceiling_tok_s": {"at_8tbs": round(roofline_tok_s(bytes_launch / K, NOMINAL_HBM_GBS), 1),
+                          "at_measured_peak": round(roofline_tok_s(bytes_launch / K, hbm_peak()[0]), 1)},
         "bytes_per_step": round(bytes_launch / K),
         "gpu_launches": 1,
     }
