@@ -3,9 +3,9 @@
     python -m persistent_monokernel_gb300.build
 
 Compiles each .cu translation unit for sm_103a in parallel, then links a
-shared library with the CUDA runtime linked statically and cuBLAS (the
-batched prefill's GEMMs) dynamically, found through an rpath to the
-toolkit's lib64.
+shared library with the CUDA runtime linked statically.  No other library is
+linked: the batched prefill's GEMMs are this library's own tcgen05 kernels,
+and the tensor maps are encoded through the runtime's driver entry point.
 """
 from __future__ import annotations
 
@@ -20,7 +20,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "liblf.so")
-SOURCES = ["lf_kernel.cu", "lf_api.cu", "lf_noalloc.cu", "lf_syncbench.cu", "lf_prefill.cu"]
+SOURCES = ["lf_kernel.cu", "lf_api.cu", "lf_noalloc.cu", "lf_syncbench.cu", "lf_prefill.cu", "lf_gemm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "--expt-relaxed-constexpr"]
@@ -68,9 +68,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     with ThreadPoolExecutor(len(SOURCES)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
     tmp = LIB + f".tmp{os.getpid()}"
-    libdir = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(cc))), "lib64")
-    cmd = [cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs, "-L" + libdir, "-lcublas",
-           "-Xlinker", "-rpath=" + libdir]
+    cmd = [cc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

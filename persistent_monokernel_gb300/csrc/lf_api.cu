@@ -42,6 +42,14 @@ int l2_prefetch_bytes_from_env()
     return (int)kb * 1024;
 }
 
+// Tuning override of the shortest split-KV piece, LF_ATTN_MIN_LEN (positions).
+int attn_min_len_from_env()
+{
+    const char *v = std::getenv("LF_ATTN_MIN_LEN");
+    long n = v ? std::strtol(v, nullptr, 10) : kAttnMinLen;
+    return n < 16 ? 16 : (n > (1 << 20) ? (1 << 20) : (int)n);
+}
+
 }  // namespace
 
 struct lf_handle {
@@ -83,6 +91,7 @@ struct lf_handle {
     int trace_steps = 0;
     int l2_prefetch_bytes = 0;
     int l2_prefetch_last = 0;
+    int attn_min_len = kAttnMinLen;
     // batched prefill (cfg.prefill_block > 0): row-major projection copy,
     // FP8 row scales in the same layout, workspace, token staging, cuBLAS
     int pf_block = 0;
@@ -90,7 +99,7 @@ struct lf_handle {
     float *pf_s = nullptr;
     uint8_t *pf_ws = nullptr;
     int *pf_tok = nullptr;
-    void *cublas = nullptr;
+    lfp_maps pf_maps;              // TMA tensor maps of the prefill GEMM operands
     size_t pf_bytes = 0;
     size_t pf_woff[4] = {}, pf_soff[4] = {};   // [qkv, o, gu, d] element offsets
 };
@@ -110,7 +119,6 @@ void free_all(lf_handle *h)
                     h->stage_in, h->stage_out, h->trace, h->pf_w, h->pf_s, h->pf_ws, h->pf_tok};
     for (void *p : ptrs)
         if (p) cudaFree(p);
-    lfp_cublas_destroy(h->cublas);
 }
 
 lf_status from_cuda(cudaError_t e)
@@ -152,11 +160,47 @@ lf_status validate_config(const lf_config &c)
     return LF_OK;
 }
 
+// The batched prefill's arguments that do not change between calls.
+lfp_args prefill_args(const lf_handle *h)
+{
+    const lfk::Geo &g = h->g;
+    lfp_args a;
+    a.g = g;
+    a.block = h->pf_block;
+    a.n = 0;
+    a.pos0 = 0;
+    a.eps = h->cfg.rms_eps;
+    a.tokens = h->pf_tok;
+    a.embed = h->embed;
+    a.attn_norm = h->attn_norm;
+    a.ffn_norm = h->ffn_norm;
+    a.wqkv = h->pf_w + h->pf_woff[0];
+    a.wo = h->pf_w + h->pf_woff[1];
+    a.wgu = h->pf_w + h->pf_woff[2];
+    a.wd = h->pf_w + h->pf_woff[3];
+    const bool fp8 = h->pf_s != nullptr;
+    a.sqkv = fp8 ? h->pf_s + h->pf_soff[0] : nullptr;
+    a.so = fp8 ? h->pf_s + h->pf_soff[1] : nullptr;
+    a.sgu = fp8 ? h->pf_s + h->pf_soff[2] : nullptr;
+    a.sd = fp8 ? h->pf_s + h->pf_soff[3] : nullptr;
+    a.router = h->router;
+    a.rope = h->rope;
+    a.win = h->win;
+    a.kc = h->kc;
+    a.vc = h->vc;
+    a.status = h->status;
+    a.sms = h->sm_count;
+    a.ws = lfp_carve(h->pf_ws, g, h->pf_block, h->sm_count);
+    return a;
+}
+
 // Batched prefill state: the eight layer projections copied row-major as FP16
 // into four stacked arrays [L, Q+2KV, d] (q, k, v rows), [L, d, Q],
-// [L, 2F, d] (gate rows, then up rows) and [L, d, F] -- FP8 models: the
-// decoded codes, with the row scales gathered into the same row layout --
-// plus the block workspace, a token staging buffer and a cuBLAS handle.
+// [L, 2F, d] (gate and up rows interleaved in blocks of 128 units, so that
+// one 256-row GEMM tile holds a unit's gate and up rows) and [L, d, F] --
+// FP8 models: the decoded codes, with the row scales gathered into the same
+// row order -- plus the block workspace, a token staging buffer and the
+// GEMMs' tensor maps.
 lf_status setup_prefill(lf_handle *h, const lf_weights *w)
 {
     const lfk::Geo &g = h->g;
@@ -187,18 +231,35 @@ lf_status setup_prefill(lf_handle *h, const lf_weights *w)
             if (lo < 104u || hi > 140u) return LF_ERR_NOT_SUPPORTED;
         }
     }
-    const size_t ws_bytes = lfp_workspace_bytes(g, h->pf_block);
+    const size_t ws_bytes = lfp_workspace_bytes(g, h->pf_block, h->sm_count);
     cudaError_t e = dalloc(&h->pf_w, wt);
     if (e == cudaSuccess && fp8) e = dalloc(&h->pf_s, st);
     if (e == cudaSuccess) e = dalloc(&h->pf_ws, ws_bytes);
     if (e == cudaSuccess) e = dalloc(&h->pf_tok, (size_t)g.max_seq);
     if (e != cudaSuccess) return from_cuda(e);
     h->pf_bytes = wt * sizeof(__half) + (fp8 ? st * sizeof(float) : 0) + ws_bytes + (size_t)g.max_seq * sizeof(int);
-    if (lfp_cublas_create(&h->cublas) != 0) {
-        h->cublas = nullptr;
-        return LF_ERR_CUDA;
+    // A [units, cols] matrix (gate or up rows) into the interleaved gate/up
+    // layout: its rows of units 128b .. 128b+127 go to rows 256b + half*128 ..
+    // (elem bytes per value: 2 for the FP16 weights, 4 for the FP8 row scales).
+    auto interleave = [](void *dst, const void *src, size_t units, size_t cols, size_t elem, int half) {
+        const size_t blk = 128 * cols * elem;
+        return cudaMemcpy2D(static_cast<uint8_t *>(dst) + (size_t)half * blk, 2 * blk, src, blk, blk, units / 128,
+                            cudaMemcpyDeviceToDevice);
+    };
+    if (g.E > 0 && e == cudaSuccess) {
+        // each expert's gate and up rows interleaved; the down projections in the caller's layout
+        const size_t ge = Fw * d;
+        for (size_t le = 0; le < L * nexp && e == cudaSuccess; ++le) {
+            __half *dst = h->pf_w + h->pf_woff[2] + le * 2 * ge;
+            e = interleave(dst, static_cast<const __half *>(w->w_gate) + le * ge, Fw, d, sizeof(__half), 0);
+            if (e == cudaSuccess)
+                e = interleave(dst, static_cast<const __half *>(w->w_up) + le * ge, Fw, d, sizeof(__half), 1);
+        }
+        if (e == cudaSuccess)
+            e = cudaMemcpy(h->pf_w + h->pf_woff[3], w->w_down, wlen[3] * sizeof(__half), cudaMemcpyDeviceToDevice);
     }
-    // per matrix: source, rows, cols, destination array, row offset inside a layer
+    // per matrix: source, rows, cols, destination array, row offset inside a
+    // layer (gate/up: which half of the interleaved blocks)
     struct Part {
         const void *src;
         size_t rows, cols;
@@ -206,46 +267,49 @@ lf_status setup_prefill(lf_handle *h, const lf_weights *w)
         size_t row0;
     };
     const Part parts[7] = {{w->wq, Q, d, 0, 0},      {w->wk, KV, d, 0, Q},     {w->wv, KV, d, 0, Q + KV},
-                           {w->wo, d, Q, 1, 0},      {w->w_gate, F, d, 2, 0},  {w->w_up, F, d, 2, F},
+                           {w->wo, d, Q, 1, 0},      {w->w_gate, F, d, 2, 0},  {w->w_up, F, d, 2, 1},
                            {w->w_down, d, F, 3, 0}};
     const size_t arr_rows[4] = {NQKV, d, 2 * F, d};
-    if (g.E > 0 && e == cudaSuccess) {
-        // each expert's gate rows, then its up rows; the down projections in the caller's layout
-        const size_t ge = Fw * d;
-        for (size_t le = 0; le < L * nexp && e == cudaSuccess; ++le) {
-            __half *dst = h->pf_w + h->pf_woff[2] + le * 2 * ge;
-            e = cudaMemcpy(dst, static_cast<const __half *>(w->w_gate) + le * ge, ge * sizeof(__half),
-                           cudaMemcpyDeviceToDevice);
-            if (e == cudaSuccess)
-                e = cudaMemcpy(dst + ge, static_cast<const __half *>(w->w_up) + le * ge, ge * sizeof(__half),
-                               cudaMemcpyDeviceToDevice);
-        }
-        if (e == cudaSuccess)
-            e = cudaMemcpy(h->pf_w + h->pf_woff[3], w->w_down, wlen[3] * sizeof(__half), cudaMemcpyDeviceToDevice);
-    }
+    __half *tmp = nullptr;   // decoded gate/up matrix of one layer before interleaving (FP8, MXFP4)
+    if (g.E == 0 && (fp8 || mx) && e == cudaSuccess) e = dalloc(&tmp, F * d);
     for (int i = 0; i < (g.E > 0 ? 4 : 7) && e == cudaSuccess; ++i) {
         const Part &pt = parts[i];
         const size_t n = pt.rows * pt.cols;
+        const bool gu = pt.arr == 2;
         for (size_t l = 0; l < L && e == cudaSuccess; ++l) {
-            __half *dst = h->pf_w + h->pf_woff[pt.arr] + (l * arr_rows[pt.arr] + pt.row0) * pt.cols;
+            __half *layer = h->pf_w + h->pf_woff[pt.arr] + l * arr_rows[pt.arr] * pt.cols;
+            __half *dst = gu ? tmp : layer + pt.row0 * pt.cols;
             if (mx) {
                 e = lfp_decode_mxfp4(static_cast<const uint8_t *>(pt.src) + l * n / 2,
                                      static_cast<const uint8_t *>(bsc[i]) + l * n / 32, pt.rows, (int)pt.cols, dst,
                                      nullptr);
             } else if (fp8) {
                 e = lfp_decode_e4m3(static_cast<const uint8_t *>(pt.src) + l * n, dst, n, nullptr);
+                const float *ssrc = h->wsc + h->wsc_off[i] + l * pt.rows;
+                float *sl = h->pf_s + h->pf_soff[pt.arr] + l * arr_rows[pt.arr];
                 if (e == cudaSuccess)
-                    e = cudaMemcpy(h->pf_s + h->pf_soff[pt.arr] + l * arr_rows[pt.arr] + pt.row0,
-                                   h->wsc + h->wsc_off[i] + l * pt.rows, pt.rows * sizeof(float),
-                                   cudaMemcpyDeviceToDevice);
+                    e = gu ? interleave(sl, ssrc, pt.rows, 1, sizeof(float), (int)pt.row0)
+                           : cudaMemcpy(sl + pt.row0, ssrc, pt.rows * sizeof(float), cudaMemcpyDeviceToDevice);
+            } else if (gu) {
+                e = interleave(layer, static_cast<const __half *>(pt.src) + l * n, pt.rows, pt.cols, sizeof(__half),
+                               (int)pt.row0);
             } else {
                 e = cudaMemcpy(dst, static_cast<const __half *>(pt.src) + l * n, n * sizeof(__half),
                                cudaMemcpyDeviceToDevice);
             }
+            if (e == cudaSuccess && gu && (fp8 || mx))
+                e = interleave(layer, tmp, pt.rows, pt.cols, sizeof(__half), (int)pt.row0);
         }
     }
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
-    return from_cuda(e);
+    if (tmp) cudaFree(tmp);
+    if (e != cudaSuccess) return from_cuda(e);
+    lfp_args a = prefill_args(h);
+    e = cudaMemset(a.ws.tile_cnt, 0, 1024 * sizeof(unsigned));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return from_cuda(e);
+    if (lfp_make_maps(&a, &h->pf_maps) != 0) return LF_ERR_CUDA;
+    return LF_OK;
 }
 
 lf_status launch(lf_handle *h, const lfk::Params &p, cudaStream_t stream)
@@ -301,7 +365,7 @@ lfk::Params base_params(lf_handle *h)
     p.a_floats = h->a_floats;
     p.b_slots = h->b_slots;
     p.lm_rows_max = h->lm_rows_max;
-    p.attn_min_len = kAttnMinLen;
+    p.attn_min_len = h->attn_min_len;
     p.sched = h->sched;
     p.only_layer = -1;
     p.only_stage = -1;
@@ -407,6 +471,7 @@ lf_status lf_create(const lf_config *cfg, const lf_weights *w, lf_handle **out)
     h->cfg.layer_window = nullptr;   // the caller's array is copied to the device below
     h->l2_prefetch_bytes = l2_prefetch_bytes_from_env();
     h->l2_prefetch_last = std::getenv("LF_L2_PREFETCH_LAST") ? 1 : 0;
+    h->attn_min_len = attn_min_len_from_env();
     lfk::Geo &g = h->g;
     g.L = cfg->n_layers;
     g.d = cfg->d_model;
@@ -640,35 +705,10 @@ lf_status lf_prefill(lf_handle *h, const int32_t *tokens_dev, int32_t n, void *s
             e = cudaMemcpyAsync(h->pf_tok + hp, tokens_dev, sizeof(int32_t) * (size_t)(n - 1),
                                 cudaMemcpyDeviceToDevice, s);
         if (e != cudaSuccess) return from_cuda(e);
-        const lfk::Geo &g = h->g;
-        lfp_args a;
-        a.g = g;
-        a.block = h->pf_block;
+        lfp_args a = prefill_args(h);
         a.n = steps;
         a.pos0 = h->pos;
-        a.eps = h->cfg.rms_eps;
-        a.tokens = h->pf_tok;
-        a.embed = h->embed;
-        a.attn_norm = h->attn_norm;
-        a.ffn_norm = h->ffn_norm;
-        a.wqkv = h->pf_w + h->pf_woff[0];
-        a.wo = h->pf_w + h->pf_woff[1];
-        a.wgu = h->pf_w + h->pf_woff[2];
-        a.wd = h->pf_w + h->pf_woff[3];
-        const bool fp8 = h->pf_s != nullptr;
-        a.sqkv = fp8 ? h->pf_s + h->pf_soff[0] : nullptr;
-        a.so = fp8 ? h->pf_s + h->pf_soff[1] : nullptr;
-        a.sgu = fp8 ? h->pf_s + h->pf_soff[2] : nullptr;
-        a.sd = fp8 ? h->pf_s + h->pf_soff[3] : nullptr;
-        a.router = h->router;
-        a.rope = h->rope;
-        a.win = h->win;
-        a.kc = h->kc;
-        a.vc = h->vc;
-        a.status = h->status;
-        a.cublas = h->cublas;
-        a.ws = lfp_carve(h->pf_ws, g, h->pf_block);
-        if (lfp_run(&a, s) != 0) return LF_ERR_CUDA;
+        if (lfp_run(&a, &h->pf_maps, s) != 0) return LF_ERR_CUDA;
         h->pos += steps;   // the monokernel's counters and epoch are untouched
     } else if (steps > 0) {
         lfk::Params p = base_params(h);

@@ -1,12 +1,21 @@
 // lf_prefill.cu -- batched prefill: the prompt's forward passes over blocks
 // of positions at once instead of one decode step per position.  The
-// projections of a block are dense GEMMs (T positions x rows x columns), so
-// they run on the tensor cores through cuBLAS (FP16 operands, FP32
-// accumulation); the causal attention of the block is a flash-style kernel
-// of warp-level tensor-core fragments over the cached K/V rows; RMSNorm,
-// RoPE, the KV append, SwiGLU and the residual adds are small elementwise
-// kernels.  The decode path stays the monokernel: this only fills the KV
-// cache, the step before it, with the same arithmetic per position.
+// projections of a block are dense GEMMs (T positions x rows x columns) on
+// the sm_103a tensor cores (lf_gemm.cu: tcgen05.mma, TMA-staged operands,
+// TMEM accumulators), each with the elementwise work that follows it fused
+// into its epilogue; the causal attention of the block is a flash-style
+// kernel of warp-level tensor-core fragments over the cached K/V rows.  Per
+// layer and block, five launches:
+//
+//   QKV GEMM   (x g) . Wqkv^T, x the RMSNorm factor, RoPE, q out, K/V into the cache
+//   attention  causal over the cache, output split for the O GEMM
+//   O GEMM     residual add, then the FFN RMSNorm's input (x g_ffn, split) and
+//              its per-tile sums of squares
+//   GU GEMM    x the RMSNorm factor, SiLU(gate) * up, split for the down GEMM
+//   D GEMM     residual add, then the next layer's RMSNorm input the same way
+//
+// The decode path stays the monokernel: this only fills the KV cache, the
+// step before it, with the same arithmetic per position.
 //
 // Numerics follow the decode path: activations are FP32; every projection
 // input is split into an FP16 head and an FP16 remainder (x = hi + lo, about
@@ -15,8 +24,11 @@
 // probabilities are split the same way in the attention products; RMSNorm,
 // RoPE (the same FP32 table), SiLU and the softmax are FP32; K and V are
 // rounded to FP16 (RNE) into the group-swizzled cache rows the decode kernels
-// read.
-#include <cublas_v2.h>
+// read.  The RMSNorm gain multiplies the GEMM input and the factor
+// 1/sqrt(mean(x^2) + eps) the GEMM output (the same product, rounded in a
+// different order); the mean comes from per-128-column partial sums written
+// by the kernel that produced x.
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
@@ -25,6 +37,7 @@
 #include <cmath>
 #include <vector>
 
+#include "lf_gemm.h"
 #include "lf_internal.cuh"
 #include "lf_prefill.h"
 #include "lf_ptx.cuh"
@@ -33,19 +46,7 @@ namespace lfp {
 
 using lfk::Geo;
 
-__device__ __forceinline__ float block_sum(float v, float *red)
-{
-#pragma unroll
-    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (lane == 0) red[w] = v;
-    __syncthreads();
-    float t = 0.f;
-    const int nw = blockDim.x >> 5;
-    for (int i = 0; i < nw; ++i) t += red[i];
-    __syncthreads();
-    return t;
-}
+constexpr int NG = 128;   // columns per partial sum of squares (the O / down GEMM tile width)
 
 __device__ __forceinline__ void split_store(float v, __half *hi, __half *lo, size_t i)
 {
@@ -54,10 +55,35 @@ __device__ __forceinline__ void split_store(float v, __half *hi, __half *lo, siz
     lo[i] = __float2half_rn(v - __half2float(h));
 }
 
-// X[t] = FP32 embedding row of token tok[t].  Ids outside [0, V) read row 0,
-// record STATUS_BAD_TOKEN (where = 400, step = t) and raise the abort flag,
-// as the decode path does, so that the next persistent launch stops at once.
-__global__ void gather_embed(const int *tok, const __half *E, int d, int V, float *X, unsigned *status, int t_base)
+// The next RMSNorm's input for row t of X: X x gain split into Xh / Xl, and
+// the sum of squares of every 128-column group into SS[t][group].  One block
+// of 128 threads per row.
+__device__ __forceinline__ void norm_prep_row(const float *x, const __half *gain, int d, __half *Xh, __half *Xl,
+                                              float *ss, size_t t)
+{
+    __shared__ float red[4];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int g0 = 0; g0 < d; g0 += NG) {
+        const int c = g0 + threadIdx.x;
+        const float v = x[c];
+        split_store(v * __half2float(gain[c]), Xh, Xl, t * d + c);
+        float s = v * v;
+#pragma unroll
+        for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (lane == 0) red[warp] = s;
+        __syncthreads();
+        if (threadIdx.x == 0) ss[t * (d / NG) + g0 / NG] = (red[0] + red[1]) + (red[2] + red[3]);
+        __syncthreads();
+    }
+}
+
+// X[t] = FP32 embedding row of token tok[t], then layer 0's RMSNorm input.
+// Ids outside [0, V) read row 0, record STATUS_BAD_TOKEN (where = 400, step =
+// t) and raise the abort flag, as the decode path does, so that the next
+// persistent launch stops at once.
+__global__ void __launch_bounds__(128) embed_prep(const int *tok, const __half *E, int d, int V, const __half *gain,
+                                                  float *X, __half *Xh, __half *Xl, float *SS, unsigned *status,
+                                                  int t_base)
 {
     const int t = blockIdx.x;
     int id = tok[t];
@@ -70,56 +96,14 @@ __global__ void gather_embed(const int *tok, const __half *E, int d, int V, floa
         if (threadIdx.x == 0) atomicExch(status + 4, 1u);
         id = 0;
     }
-    for (int i = threadIdx.x; i < d; i += blockDim.x) X[(size_t)t * d + i] = __half2float(E[(size_t)id * d + i]);
+    float *x = X + (size_t)t * d;
+    for (int i = threadIdx.x; i < d; i += blockDim.x) x[i] = __half2float(E[(size_t)id * d + i]);
+    __syncthreads();
+    norm_prep_row(x, gain, d, Xh, Xl, SS, (size_t)t);
 }
 
-// RMSNorm of row t times the gain, split into FP16 head and remainder.
-__global__ void rmsnorm_split(const float *X, const __half *gain, int d, float eps, __half *Xh, __half *Xl)
-{
-    __shared__ float red[32];
-    const int t = blockIdx.x;
-    const float *x = X + (size_t)t * d;
-    float ss = 0.f;
-    for (int i = threadIdx.x; i < d; i += blockDim.x) ss = fmaf(x[i], x[i], ss);
-    const float inv = 1.0f / sqrtf(block_sum(ss, red) / (float)d + eps);
-    for (int i = threadIdx.x; i < d; i += blockDim.x)
-        split_store(x[i] * inv * __half2float(gain[i]), Xh, Xl, (size_t)t * d + i);
-}
 
-// Elementwise split of an FP32 array into FP16 head and remainder.
-__global__ void split_f32(const float *A, size_t n, __half *Ah, __half *Al)
-{
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
-        split_store(A[i], Ah, Al, i);
-}
-
-// h[t][r] = SiLU(gate[t][r]) * up[t][r] from the fused [T, 2F] projection, split.
-__global__ void silu_mul_split(const float *GU, int T, int F, __half *Hh, __half *Hl)
-{
-    const size_t n = (size_t)T * F;
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
-        const size_t t = i / F, r = i % F;
-        const float gt = GU[t * 2 * F + r], up = GU[t * 2 * F + F + r];
-        split_store(gt / (1.0f + expf(-gt)) * up, Hh, Hl, i);
-    }
-}
-
-__global__ void resid_add(float *X, const float *Y, size_t n)
-{
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
-        X[i] += Y[i];
-}
-
-// FP8 models: Y[t][c] *= s[c] for the N columns of a [T, ldc] output (the
-// per-row weight scale, applied after the sum as the decode epilogue does).
-__global__ void scale_cols(float *Y, int T, int ldc, int N, const float *s)
-{
-    const size_t n = (size_t)T * N;
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
-        const size_t t = i / N, c = i % N;
-        Y[t * ldc + c] *= s[c];
-    }
-}
+int grid_for(size_t n) { return (int)std::max<size_t>(1, std::min<size_t>((n + 255) / 256, 8 * 1024)); }
 
 __global__ void decode_e4m3(const uint8_t *src, __half *dst, size_t n)
 {
@@ -195,8 +179,8 @@ __global__ void route_tokens(const float *R, int E, int k, int *sel, float *gate
 }
 
 // Per expert (one block each, 256 threads): the (token, slot) pairs routed to
-// it, in token order, as t * 8 + j, and their count.
-__global__ void build_lists(const int *sel, int T, int k, int *list, int *cnt)
+// it, in token order, as t * 8 + j, at list[e * ld ..], and their count.
+__global__ void build_lists(const int *sel, int T, int k, int ld, int *list, int *cnt)
 {
     __shared__ int wsum[8];
     const int e = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -215,88 +199,71 @@ __global__ void build_lists(const int *sel, int T, int k, int *list, int *cnt)
             if (w < warp) before += wsum[w];
             total += wsum[w];
         }
-        if (j >= 0) list[(size_t)e * T + base + before + __popc(m & ((1u << lane) - 1u))] = t * 8 + j;
+        if (j >= 0) list[(size_t)e * ld + base + before + __popc(m & ((1u << lane) - 1u))] = t * 8 + j;
         base += total;
         __syncthreads();
     }
     if (threadIdx.x == 0) cnt[e] = base;
 }
 
-// Row i of the gathered input: the FFN input row of token list[i] / 8.
-__global__ void gather_rows(const __half *Xh, const __half *Xl, const int *list, int d, __half *Gh, __half *Gl)
+
+// Router logits of token t: W_r . (x g), times the RMSNorm factor (the
+// monokernel's order: FP32 dots of the FP16 router rows with x * gain, then
+// the positive scale).  One block of 256 threads per token; warp w takes
+// experts w, w + 8, ...
+__global__ void __launch_bounds__(256) router_logits(const float *X, const __half *gain, const __half *Wr, int E, int d,
+                                                     float eps, float *R)
 {
-    const size_t i = blockIdx.x, t = (size_t)(list[i] >> 3);
+    const int t = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float *x = X + (size_t)t * d;
+    __shared__ float red[8];
+    float ss = 0.f;
+    for (int i = threadIdx.x; i < d; i += blockDim.x) ss = fmaf(x[i], x[i], ss);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    float tot = 0.f;
+    for (int w = 0; w < 8; ++w) tot += red[w];
+    const float inv = 1.0f / sqrtf(tot / (float)d + eps);
+    for (int e = warp; e < E; e += 8) {
+        const __half *row = Wr + (size_t)e * d;
+        float acc = 0.f;
+        for (int i = lane; i < d; i += 32) acc = fmaf(__half2float(row[i]), x[i] * __half2float(gain[i]), acc);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) R[(size_t)t * E + e] = acc * inv;
+    }
+}
+
+// Row i of expert e's gathered GEMM input: the FFN input row (split) of the
+// token of list[e][i]; rows past the expert's count stay untouched.
+__global__ void gather_rows(const __half *Xh, const __half *Xl, const int *list, const int *cnt, int T, int d,
+                            __half *Gh, __half *Gl)
+{
+    const int i = blockIdx.x, e = blockIdx.y;
+    if (i >= cnt[e]) return;
+    const size_t row = (size_t)e * T + i, t = (size_t)(list[row] >> 3);
     for (int c = threadIdx.x; c < d; c += blockDim.x) {
-        Gh[i * d + c] = Xh[t * d + c];
-        Gl[i * d + c] = Xl[t * d + c];
+        Gh[row * d + c] = Xh[t * d + c];
+        Gl[row * d + c] = Xl[t * d + c];
     }
 }
 
-// h = gate * SiLU(g) * u for the n gathered rows of one expert, split.
-__global__ void silu_mul_gate_split(const float *GU, int n, int Fe, const int *list, const float *gatev,
-                                    __half *Hh, __half *Hl)
-{
-    const size_t total = (size_t)n * Fe;
-    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
-        const size_t r = i / Fe, c = i % Fe;
-        const float gt = GU[r * 2 * Fe + c], up = GU[r * 2 * Fe + Fe + c];
-        split_store(gatev[list[r]] * (gt / (1.0f + expf(-gt)) * up), Hh, Hl, i);
-    }
-}
-
-// The expert's output row i goes to its (token, slot) place.
-__global__ void scatter_rows(const float *Y, const int *list, int d, int k, float *Yk)
-{
-    const size_t i = blockIdx.x;
-    const int tj = list[i];
-    float *dst = Yk + ((size_t)(tj >> 3) * k + (tj & 7)) * d;
-    for (int c = threadIdx.x; c < d; c += blockDim.x) dst[c] = Y[i * d + c];
-}
-
-// X[t] += the slots' outputs, summed in slot order.
-__global__ void combine_slots(float *X, const float *Yk, int k, int d)
+// X[t] += the slots' expert outputs (slot order), then the next RMSNorm's
+// input of the row (skipped after the last layer: gain null).
+__global__ void __launch_bounds__(128) combine_prep(float *X, const float *Yk, int k, int d, const __half *gain,
+                                                    __half *Xh, __half *Xl, float *SS)
 {
     const size_t t = blockIdx.x;
+    float *x = X + t * d;
     for (int c = threadIdx.x; c < d; c += blockDim.x) {
         float acc = 0.f;
         for (int j = 0; j < k; ++j) acc += Yk[(t * k + j) * d + c];
-        X[t * d + c] += acc;
+        x[c] += acc;
     }
-}
-
-// RoPE on the q and k heads of row t (rotate-half pairs (j, j + hd/2), the
-// FP32 table), q to Qr, K after RoPE and V rounded to FP16 into the cache at
-// position pos0 + t of layer l.  Thread u: pair unit u of the fused [q; k; v] row.
-__global__ void rope_store(const float *Y, int pos0, int l, Geo g, const float2 *rope, float *Qr, __half *kc,
-                           __half *vc)
-{
-    const int t = blockIdx.x;
-    const int half = g.hd / 2;
-    const int N = g.Q + 2 * g.KV;
-    const int pos = pos0 + t;
-    for (int u = threadIdx.x; u < N / 2; u += blockDim.x) {
-        const int hh = u / half, j = u % half;
-        const float *y = Y + (size_t)t * N + (size_t)hh * g.hd;
-        const float v0 = y[j], v1 = y[j + half];
-        if (hh < g.Hq + g.Hkv) {
-            const float2 cs = rope[(size_t)pos * half + j];
-            const float r0 = v0 * cs.x - v1 * cs.y;
-            const float r1 = v1 * cs.x + v0 * cs.y;
-            if (hh < g.Hq) {
-                float *q = Qr + (size_t)t * g.Q + (size_t)hh * g.hd;
-                q[j] = r0;
-                q[j + half] = r1;
-            } else {
-                __half *kr = kc + (((size_t)l * g.Hkv + (hh - g.Hq)) * g.max_seq + pos) * g.hd;
-                kr[lfk::kv_swz(pos, j)] = __float2half_rn(r0);
-                kr[lfk::kv_swz(pos, j + half)] = __float2half_rn(r1);
-            }
-        } else {
-            __half *vr = vc + (((size_t)l * g.Hkv + (hh - g.Hq - g.Hkv)) * g.max_seq + pos) * g.hd;
-            vr[lfk::kv_swz(pos, j)] = __float2half_rn(v0);
-            vr[lfk::kv_swz(pos, j + half)] = __float2half_rn(v1);
-        }
-    }
+    __syncthreads();
+    if (gain) norm_prep_row(x, gain, d, Xh, Xl, SS, t);
 }
 
 // ------------------------------------------------------------- attention
@@ -329,11 +296,11 @@ constexpr int fa_smem_bytes()
 // loads conflict-free), double-buffered with cp.async; each warp owns 16 query
 // rows and runs, per chunk, S = Q K^T (q as head + remainder: two products),
 // the masked online softmax in FP32 (running max and sum per row), and
-// O += P V (p as head + remainder).  Output rows are FP32, normalised by the
-// final sum.
+// O += P V (p as head + remainder).  Output rows, normalised by the final
+// sum, are stored as FP16 head and remainder: the O projection's GEMM operand.
 template <int HD>
 __global__ void __launch_bounds__(128) attn_flash(const float *Qr, const __half *kc, const __half *vc, int T, int pos0,
-                                                  int l, Geo g, const int *win, float *A)
+                                                  int l, Geo g, const int *win, __half *Ah, __half *Al)
 {
     constexpr int ROW = HD * 2;     // bytes of one FP16 row
     constexpr int KS = HD / 16;     // k-steps of Q K^T
@@ -342,6 +309,7 @@ __global__ void __launch_bounds__(128) attn_flash(const float *Qr, const __half 
     extern __shared__ __align__(128) uint8_t fsm[];
     const uint32_t sqh = lfk::smem_u32(fsm), sql = sqh + FA_BM * ROW;
     const uint32_t sk = sql + FA_BM * ROW, sv = sk + 2 * FA_BN * ROW;
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // launched as a programmatic dependent
     const int blk = gridDim.x - 1 - blockIdx.x;   // the longest rows first
     const int h = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -511,71 +479,37 @@ __global__ void __launch_bounds__(128) attn_flash(const float *Qr, const __half 
 #pragma unroll
     for (int i = 0; i < NO; ++i) {
         const int col = h * HD + i * 8 + 2 * tq;
-        if (rowa < nrow)
-            *reinterpret_cast<float2 *>(A + (size_t)(t0 + rowa) * g.Q + col) = make_float2(o[i][0] * ia, o[i][1] * ia);
-        if (rowb < nrow)
-            *reinterpret_cast<float2 *>(A + (size_t)(t0 + rowb) * g.Q + col) = make_float2(o[i][2] * ib, o[i][3] * ib);
+        __half h0, r0, h1, r1;
+        if (rowa < nrow) {
+            const size_t o0 = (size_t)(t0 + rowa) * g.Q + col;
+            lfk::split_h(o[i][0] * ia, h0, r0);
+            lfk::split_h(o[i][1] * ia, h1, r1);
+            *reinterpret_cast<unsigned *>(Ah + o0) = lfk::pack_h2(h0, h1);
+            *reinterpret_cast<unsigned *>(Al + o0) = lfk::pack_h2(r0, r1);
+        }
+        if (rowb < nrow) {
+            const size_t o1 = (size_t)(t0 + rowb) * g.Q + col;
+            lfk::split_h(o[i][2] * ib, h0, r0);
+            lfk::split_h(o[i][3] * ib, h1, r1);
+            *reinterpret_cast<unsigned *>(Ah + o1) = lfk::pack_h2(h0, h1);
+            *reinterpret_cast<unsigned *>(Al + o1) = lfk::pack_h2(r0, r1);
+        }
     }
 }
 
 // ------------------------------------------------------------- host side
-
-// Y[T x N] (row-major, leading dimension ldc) = X W^T for W [N x K] row-major
-// and X = Xh + Xl [T x K] row-major: two FP16 GEMMs into one FP32 result.
-cublasStatus_t gemm2(cublasHandle_t cb, const __half *W, int N, int K, const __half *Xh, const __half *Xl, int T,
-                     float *Y, int ldc)
-{
-    const float one = 1.0f, zero = 0.0f;
-    cublasStatus_t st = cublasGemmEx(cb, CUBLAS_OP_T, CUBLAS_OP_N, N, T, K, &one, W, CUDA_R_16F, K, Xh, CUDA_R_16F,
-                                     K, &zero, Y, CUDA_R_32F, ldc, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-    if (st != CUBLAS_STATUS_SUCCESS) return st;
-    return cublasGemmEx(cb, CUBLAS_OP_T, CUBLAS_OP_N, N, T, K, &one, W, CUDA_R_16F, K, Xl, CUDA_R_16F, K, &one, Y,
-                        CUDA_R_32F, ldc, CUBLAS_COMPUTE_32F, CUBLAS_GEMM_DEFAULT);
-}
-
-int grid_for(size_t n) { return (int)std::max<size_t>(1, std::min<size_t>((n + 255) / 256, 8 * 1024)); }
-
-// The mixture-of-experts FFN of layer l for the block's T rows (input in
-// w.Xh / w.Xl): router GEMM, routing, then per expert with tokens a gather,
-// the gate/up GEMM, the gated SiLU product, the down GEMM and a scatter to
-// the (token, slot) places; the slots are summed into the residual in order.
-int moe_ffn(const lfp_args *a, cublasHandle_t cb, cudaStream_t s, int l, int T, int *cnt_host)
-{
-    const Geo &g = a->g;
-    const lfp_workspace &w = a->ws;
-    const int E = g.E, k = g.topk, Fe = g.Fe, d = g.d;
-    if (gemm2(cb, a->router + (size_t)l * E * d, E, d, w.Xh, w.Xl, T, w.R, E)) return 3;
-    route_tokens<<<T, 32, 0, s>>>(w.R, E, k, w.sel, w.gate);
-    build_lists<<<E, 256, 0, s>>>(w.sel, T, k, w.list, w.cnt);
-    if (cudaMemcpyAsync(cnt_host, w.cnt, sizeof(int) * E, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-        cudaStreamSynchronize(s) != cudaSuccess)
-        return 1;
-    for (int e = 0; e < E; ++e) {
-        const int n = cnt_host[e];
-        if (n <= 0) continue;
-        const int *lst = w.list + (size_t)e * T;
-        const size_t ex = (size_t)l * E + e;
-        gather_rows<<<n, 256, 0, s>>>(w.Xh, w.Xl, lst, d, w.Xgh, w.Xgl);
-        if (gemm2(cb, a->wgu + ex * 2 * Fe * d, 2 * Fe, d, w.Xgh, w.Xgl, n, w.GU, 2 * Fe)) return 3;
-        silu_mul_gate_split<<<grid_for((size_t)n * Fe), 256, 0, s>>>(w.GU, n, Fe, lst, w.gate, w.Hh, w.Hl);
-        if (gemm2(cb, a->wd + ex * d * Fe, d, Fe, w.Hh, w.Hl, n, w.Y, d)) return 3;
-        scatter_rows<<<n, 256, 0, s>>>(w.Y, lst, d, k, w.Yk);
-    }
-    combine_slots<<<T, 256, 0, s>>>(w.X, w.Yk, k, d);
-    return 0;
-}
 
 size_t align256(size_t b) { return (b + 255) / 256 * 256; }
 
 }  // namespace lfp
 
 // The workspace's parts, carved from `base` (or only sized when base is null).
-static size_t lfp_layout(const lfk::Geo &g, int block, uint8_t *base, lfp_workspace *w)
+static size_t lfp_layout(const lfk::Geo &g, int block, int sms, uint8_t *base, lfp_workspace *w)
 {
     using lfp::align256;
     const size_t T = (size_t)block;
-    const size_t kmax = (size_t)std::max(g.d, std::max(g.Q, g.F));
-    const size_t ymax = (size_t)std::max(g.Q + 2 * g.KV, g.d);
+    const size_t hrows = g.E > 0 ? (size_t)g.E * T : T;   // hidden rows: per expert when routed
+    const size_t hcols = g.E > 0 ? (size_t)g.Fe : (size_t)g.F;
     size_t o = 0;
     auto take = [&](size_t bytes) -> void * {
         void *p = base ? static_cast<void *>(base + o) : nullptr;
@@ -584,56 +518,40 @@ static size_t lfp_layout(const lfk::Geo &g, int block, uint8_t *base, lfp_worksp
     };
     *w = lfp_workspace{};
     w->X = static_cast<float *>(take(T * g.d * 4));
-    w->Xh = static_cast<__half *>(take(T * kmax * 2));
-    w->Xl = static_cast<__half *>(take(T * kmax * 2));
-    w->Y = static_cast<float *>(take(T * ymax * 4));
+    w->Xh = static_cast<__half *>(take(T * g.d * 2));
+    w->Xl = static_cast<__half *>(take(T * g.d * 2));
+    w->SS = static_cast<float *>(take(T * (g.d / lfp::NG) * 4));
     w->Qr = static_cast<float *>(take(T * g.Q * 4));
-    w->A = static_cast<float *>(take(T * g.Q * 4));
-    w->GU = static_cast<float *>(take(T * 2 * g.F * 4));
+    w->Ah = static_cast<__half *>(take(T * g.Q * 2));
+    w->Al = static_cast<__half *>(take(T * g.Q * 2));
+    w->Hh = static_cast<__half *>(take(hrows * hcols * 2));
+    w->Hl = static_cast<__half *>(take(hrows * hcols * 2));
     if (g.E > 0) {
         w->R = static_cast<float *>(take(T * g.E * 4));
         w->sel = static_cast<int *>(take(T * 8 * 4));
         w->gate = static_cast<float *>(take(T * 8 * 4));
         w->list = static_cast<int *>(take((size_t)g.E * T * 4));
         w->cnt = static_cast<int *>(take((size_t)g.E * 4));
-        w->Xgh = static_cast<__half *>(take(T * g.d * 2));
-        w->Xgl = static_cast<__half *>(take(T * g.d * 2));
-        w->Hh = static_cast<__half *>(take(T * g.Fe * 2));
-        w->Hl = static_cast<__half *>(take(T * g.Fe * 2));
+        w->Xgh = static_cast<__half *>(take((size_t)g.E * T * g.d * 2));
+        w->Xgl = static_cast<__half *>(take((size_t)g.E * T * g.d * 2));
         w->Yk = static_cast<float *>(take(T * g.topk * g.d * 4));
     }
+    w->part = static_cast<float *>(take((size_t)sms * 128 * 256 * 4));
+    w->tile_cnt = static_cast<unsigned *>(take(1024 * 4));
     return o;
 }
 
-size_t lfp_workspace_bytes(const lfk::Geo &g, int block)
+size_t lfp_workspace_bytes(const lfk::Geo &g, int block, int sms)
 {
     lfp_workspace w;
-    return lfp_layout(g, block, nullptr, &w);
+    return lfp_layout(g, block, sms, nullptr, &w);
 }
 
-lfp_workspace lfp_carve(void *base, const lfk::Geo &g, int block)
+lfp_workspace lfp_carve(void *base, const lfk::Geo &g, int block, int sms)
 {
     lfp_workspace w;
-    lfp_layout(g, block, static_cast<uint8_t *>(base), &w);
+    lfp_layout(g, block, sms, static_cast<uint8_t *>(base), &w);
     return w;
-}
-
-extern "C" int lfp_cublas_create(void **out)
-{
-    cublasHandle_t h = nullptr;
-    if (cublasCreate(&h) != CUBLAS_STATUS_SUCCESS) return 1;
-    // FP32 accumulation throughout; no reduced-precision split reductions
-    if (cublasSetMathMode(h, CUBLAS_MATH_DISALLOW_REDUCED_PRECISION_REDUCTION) != CUBLAS_STATUS_SUCCESS) {
-        cublasDestroy(h);
-        return 1;
-    }
-    *out = h;
-    return 0;
-}
-
-extern "C" void lfp_cublas_destroy(void *h)
-{
-    if (h) cublasDestroy(static_cast<cublasHandle_t>(h));
 }
 
 extern "C" cudaError_t lfp_decode_e4m3(const uint8_t *src, __half *dst, size_t n, cudaStream_t stream)
@@ -667,55 +585,178 @@ extern "C" cudaError_t lfp_byte_range(const uint8_t *s, size_t n, unsigned *lo, 
     return e;
 }
 
-extern "C" int lfp_run(const lfp_args *a, cudaStream_t s)
+// Tensor maps of the GEMM operands: the workspace's split activations and
+// the four stacked weight arrays.  0 on success.
+extern "C" int lfp_make_maps(const lfp_args *a, lfp_maps *m)
+{
+    const lfk::Geo &g = a->g;
+    const lfp_workspace &w = a->ws;
+    const unsigned long long T = (unsigned long long)a->block, L = (unsigned long long)g.L;
+    const unsigned long long d = g.d, Q = g.Q, NQKV = g.Q + 2 * g.KV;
+    int r = 0;
+    r |= lfg_tensor_map(&m->xh, w.Xh, T, d, lfg::BM);
+    r |= lfg_tensor_map(&m->xl, w.Xl, T, d, lfg::BM);
+    r |= lfg_tensor_map(&m->ah, w.Ah, T, Q, lfg::BM);
+    r |= lfg_tensor_map(&m->al, w.Al, T, Q, lfg::BM);
+    for (int i = 0; i < 2; ++i) {
+        r |= lfg_tensor_map(&m->wqkv[i], a->wqkv, L * NQKV, d, 128 << i);
+        r |= lfg_tensor_map(&m->wo[i], a->wo, L * d, Q, 128 << i);
+    }
+    if (g.E > 0) {
+        const unsigned long long E = g.E, Fe = g.Fe;
+        r |= lfg_tensor_map(&m->hh, w.Hh, E * T, Fe, lfg::BM);
+        r |= lfg_tensor_map(&m->hl, w.Hl, E * T, Fe, lfg::BM);
+        r |= lfg_tensor_map(&m->xgh, w.Xgh, E * T, d, lfg::BM);
+        r |= lfg_tensor_map(&m->xgl, w.Xgl, E * T, d, lfg::BM);
+        r |= lfg_tensor_map(&m->wgu, a->wgu, L * E * 2 * Fe, d, 256);
+        for (int i = 0; i < 2; ++i) r |= lfg_tensor_map(&m->wd[i], a->wd, L * E * d, Fe, 128 << i);
+    } else {
+        const unsigned long long F = g.F;
+        r |= lfg_tensor_map(&m->hh, w.Hh, T, F, lfg::BM);
+        r |= lfg_tensor_map(&m->hl, w.Hl, T, F, lfg::BM);
+        r |= lfg_tensor_map(&m->wgu, a->wgu, L * 2 * F, d, 256);
+        for (int i = 0; i < 2; ++i) r |= lfg_tensor_map(&m->wd[i], a->wd, L * d, F, 128 << i);
+    }
+    return r ? 1 : 0;
+}
+
+extern "C" int lfp_run(const lfp_args *a, const lfp_maps *m, cudaStream_t s)
 {
     using namespace lfp;
     const Geo &g = a->g;
-    cublasHandle_t cb = static_cast<cublasHandle_t>(a->cublas);
-    if (cublasSetStream(cb, s) != CUBLAS_STATUS_SUCCESS) return 2;
-    const int d = g.d, Q = g.Q, F = g.F, NQKV = g.Q + 2 * g.KV;
+    const int d = g.d, NQKV = g.Q + 2 * g.KV;
     const int fa_smem = g.hd == 64 ? fa_smem_bytes<64>() : fa_smem_bytes<128>();
     cudaError_t e = g.hd == 64
                         ? cudaFuncSetAttribute(attn_flash<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, fa_smem)
                         : cudaFuncSetAttribute(attn_flash<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, fa_smem);
     if (e != cudaSuccess) return 1;
     const lfp_workspace &w = a->ws;
-    std::vector<int> cnt_host(g.E > 0 ? g.E : 1);
+    // tile width and split count per product; the weight map whose box matches the width
+    auto plan = [&](lfg::GemmParams &q, int M, bool allow128) {
+        int bn = 256, sp = 1;
+        lfg_plan(M, q.N, q.K, a->sms, allow128 ? 1 : 0, &bn, &sp);
+        q.splits = sp;
+        q.part = w.part;
+        q.tile_cnt = w.tile_cnt;
+        return bn;
+    };
     for (int t0 = 0; t0 < a->n; t0 += a->block) {
         const int T = std::min(a->block, a->n - t0);
         const int pos0 = a->pos0 + t0;
         const dim3 fa_grid((T + FA_BM - 1) / FA_BM, g.Hq);
-        gather_embed<<<T, 256, 0, s>>>(a->tokens + t0, a->embed, d, g.V, w.X, a->status, t0);
+        embed_prep<<<T, 128, 0, s>>>(a->tokens + t0, a->embed, d, g.V, a->attn_norm, w.X, w.Xh, w.Xl, w.SS, a->status,
+                                     t0);
         for (int l = 0; l < g.L; ++l) {
-            // attention block
-            rmsnorm_split<<<T, 256, 0, s>>>(w.X, a->attn_norm + (size_t)l * d, d, a->eps, w.Xh, w.Xl);
-            if (gemm2(cb, a->wqkv + (size_t)l * NQKV * d, NQKV, d, w.Xh, w.Xl, T, w.Y, NQKV)) return 3;
-            if (a->sqkv)
-                scale_cols<<<grid_for((size_t)T * NQKV), 256, 0, s>>>(w.Y, T, NQKV, NQKV, a->sqkv + (size_t)l * NQKV);
-            rope_store<<<T, 256, 0, s>>>(w.Y, pos0, l, g, a->rope, w.Qr, a->kc, a->vc);
-            if (g.hd == 64)
-                attn_flash<64><<<fa_grid, 128, fa_smem, s>>>(w.Qr, a->kc, a->vc, T, pos0, l, g, a->win, w.A);
-            else
-                attn_flash<128><<<fa_grid, 128, fa_smem, s>>>(w.Qr, a->kc, a->vc, T, pos0, l, g, a->win, w.A);
-            split_f32<<<grid_for((size_t)T * Q), 256, 0, s>>>(w.A, (size_t)T * Q, w.Xh, w.Xl);
-            if (gemm2(cb, a->wo + (size_t)l * d * Q, d, Q, w.Xh, w.Xl, T, w.Y, d)) return 3;
-            if (a->so) scale_cols<<<grid_for((size_t)T * d), 256, 0, s>>>(w.Y, T, d, d, a->so + (size_t)l * d);
-            resid_add<<<grid_for((size_t)T * d), 256, 0, s>>>(w.X, w.Y, (size_t)T * d);
-            // SwiGLU block (or the mixture of experts)
-            rmsnorm_split<<<T, 256, 0, s>>>(w.X, a->ffn_norm + (size_t)l * d, d, a->eps, w.Xh, w.Xl);
+            const __half *next_gain = l + 1 < g.L ? a->attn_norm + (size_t)(l + 1) * d : nullptr;
+            lfg::GemmParams p = {};
+            p.M = T;
+            p.g = g;
+            p.eps = a->eps;
+            p.ss_in = w.SS;
+            p.ss_n = d / NG;
+            p.dnorm = d;
+            p.status = a->status;
+            // ---- attention block
+            lfg::GemmParams q = p;
+            q.N = NQKV;
+            q.K = d;
+            q.b_row0 = l * NQKV;
+            q.colscale = a->sqkv ? a->sqkv + (size_t)l * NQKV : nullptr;
+            q.pos0 = pos0;
+            q.layer = l;
+            q.rope = a->rope;
+            q.Qr = w.Qr;
+            q.kc = a->kc;
+            q.vc = a->vc;
+            const int bq = plan(q, T, true);
+            if (lfg_launch(lfg::EPI_QKV, bq, &m->xh, &m->xl, &m->wqkv[bq / 256], &q, 1, 1, s) != cudaSuccess) return 1;
+            {
+                cudaLaunchConfig_t cfg = {};
+                cfg.gridDim = fa_grid;
+                cfg.blockDim = dim3(128);
+                cfg.dynamicSmemBytes = (size_t)fa_smem;
+                cfg.stream = s;
+                cudaLaunchAttribute attr[1];
+                attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+                attr[0].val.programmaticStreamSerializationAllowed = 1;
+                cfg.attrs = attr;
+                cfg.numAttrs = 1;
+                const cudaError_t le =
+                    g.hd == 64 ? cudaLaunchKernelEx(&cfg, attn_flash<64>, (const float *)w.Qr, (const __half *)a->kc,
+                                                    (const __half *)a->vc, T, pos0, l, g, a->win, w.Ah, w.Al)
+                               : cudaLaunchKernelEx(&cfg, attn_flash<128>, (const float *)w.Qr, (const __half *)a->kc,
+                                                    (const __half *)a->vc, T, pos0, l, g, a->win, w.Ah, w.Al);
+                if (le != cudaSuccess) return 1;
+            }
+            lfg::GemmParams o = p;
+            o.N = d;
+            o.K = g.Q;
+            o.b_row0 = l * d;
+            o.colscale = a->so ? a->so + (size_t)l * d : nullptr;
+            o.X = w.X;
+            o.gain_next = a->ffn_norm + (size_t)l * d;
+            o.Xh = w.Xh;
+            o.Xl = w.Xl;
+            o.ss_out = w.SS;
+            const int bo = plan(o, T, true);
+            if (lfg_launch(lfg::EPI_RESID, bo, &m->ah, &m->al, &m->wo[bo / 256], &o, 1, 1, s) != cudaSuccess) return 1;
+            // ---- SwiGLU block
             if (g.E > 0) {
-                const int r = moe_ffn(a, cb, s, l, T, cnt_host.data());
-                if (r) return r;
+                const int E = g.E, k = g.topk, Fe = g.Fe;
+                router_logits<<<T, 256, 0, s>>>(w.X, a->ffn_norm + (size_t)l * d, a->router + (size_t)l * E * d, E, d,
+                                                a->eps, w.R);
+                route_tokens<<<T, 32, 0, s>>>(w.R, E, k, w.sel, w.gate);
+                build_lists<<<E, 256, 0, s>>>(w.sel, T, k, a->block, w.list, w.cnt);
+                gather_rows<<<dim3(T, E), 256, 0, s>>>(w.Xh, w.Xl, w.list, w.cnt, a->block, d, w.Xgh, w.Xgl);
+                lfg::GemmParams u = p;
+                u.M = T;
+                u.N = 2 * Fe;
+                u.K = d;
+                u.a_group_rows = a->block;
+                u.b_row0 = l * E * 2 * Fe;
+                u.cnt = w.cnt;
+                u.list = w.list;
+                u.gatev = w.gate;
+                u.Hh = w.Hh;
+                u.Hl = w.Hl;
+                u.ldh = Fe;
+                if (lfg_launch(lfg::EPI_GU_MOE, 256, &m->xgh, &m->xgl, &m->wgu, &u, E, 1, s) != cudaSuccess) return 1;
+                lfg::GemmParams dn = p;
+                dn.M = T;
+                dn.N = d;
+                dn.K = Fe;
+                dn.a_group_rows = a->block;
+                dn.b_row0 = l * E * d;
+                dn.cnt = w.cnt;
+                dn.list = w.list;
+                dn.Yk = w.Yk;
+                dn.topk = k;
+                if (lfg_launch(lfg::EPI_D_MOE, 128, &m->hh, &m->hl, &m->wd[0], &dn, E, 1, s) != cudaSuccess) return 1;
+                combine_prep<<<T, 128, 0, s>>>(w.X, w.Yk, k, d, next_gain, w.Xh, w.Xl, w.SS);
                 continue;
             }
-            if (gemm2(cb, a->wgu + (size_t)l * 2 * F * d, 2 * F, d, w.Xh, w.Xl, T, w.GU, 2 * F)) return 3;
-            if (a->sgu)
-                scale_cols<<<grid_for((size_t)T * 2 * F), 256, 0, s>>>(w.GU, T, 2 * F, 2 * F,
-                                                                       a->sgu + (size_t)l * 2 * F);
-            silu_mul_split<<<grid_for((size_t)T * F), 256, 0, s>>>(w.GU, T, F, w.Xh, w.Xl);
-            if (gemm2(cb, a->wd + (size_t)l * d * F, d, F, w.Xh, w.Xl, T, w.Y, d)) return 3;
-            if (a->sd) scale_cols<<<grid_for((size_t)T * d), 256, 0, s>>>(w.Y, T, d, d, a->sd + (size_t)l * d);
-            resid_add<<<grid_for((size_t)T * d), 256, 0, s>>>(w.X, w.Y, (size_t)T * d);
+            lfg::GemmParams u = p;
+            u.N = 2 * g.F;
+            u.K = d;
+            u.b_row0 = l * 2 * g.F;
+            u.colscale = a->sgu ? a->sgu + (size_t)l * 2 * g.F : nullptr;
+            u.Hh = w.Hh;
+            u.Hl = w.Hl;
+            u.ldh = g.F;
+            plan(u, T, false);
+            if (lfg_launch(lfg::EPI_GU, 256, &m->xh, &m->xl, &m->wgu, &u, 1, 1, s) != cudaSuccess) return 1;
+            lfg::GemmParams dn = p;
+            dn.N = d;
+            dn.K = g.F;
+            dn.b_row0 = l * d;
+            dn.colscale = a->sd ? a->sd + (size_t)l * d : nullptr;
+            dn.X = w.X;
+            dn.gain_next = next_gain;
+            dn.Xh = w.Xh;
+            dn.Xl = w.Xl;
+            dn.ss_out = w.SS;
+            const int bd = plan(dn, T, true);
+            if (lfg_launch(lfg::EPI_RESID, bd, &m->hh, &m->hl, &m->wd[bd / 256], &dn, 1, 1, s) != cudaSuccess) return 1;
         }
         if (cudaGetLastError() != cudaSuccess) return 1;
     }
