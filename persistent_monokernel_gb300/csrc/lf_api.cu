@@ -30,17 +30,6 @@ namespace {
 
 constexpr int kAttnMinLen = 64;         // fewest positions per split-KV piece
 constexpr long long kDefaultTimeoutNs = 2000000000LL;
-constexpr int kL2PrefetchKB = 0;        // weight-stream lookahead into L2 per CTA (measured: no gain)
-
-// Tuning override of the L2 lookahead, LF_L2_PREFETCH_KB (0 disables it).
-int l2_prefetch_bytes_from_env()
-{
-    const char *v = std::getenv("LF_L2_PREFETCH_KB");
-    long kb = v ? std::strtol(v, nullptr, 10) : kL2PrefetchKB;
-    if (kb < 0) kb = 0;
-    if (kb > 8192) kb = 8192;
-    return (int)kb * 1024;
-}
 
 // Tuning override of the shortest split-KV piece, LF_ATTN_MIN_LEN (positions).
 int attn_min_len_from_env()
@@ -89,8 +78,6 @@ struct lf_handle {
     // optional stage trace
     unsigned long long *trace = nullptr;
     int trace_steps = 0;
-    int l2_prefetch_bytes = 0;
-    int l2_prefetch_last = 0;
     int attn_min_len = kAttnMinLen;
     // batched prefill (cfg.prefill_block > 0): row-major projection copy,
     // FP8 row scales in the same layout, workspace, token staging, cuBLAS
@@ -371,8 +358,6 @@ lfk::Params base_params(lf_handle *h)
     p.only_stage = -1;
     p.trace = h->trace;
     p.trace_steps = h->trace_steps;
-    p.l2_prefetch_bytes = h->l2_prefetch_bytes;
-    p.l2_prefetch_last = h->l2_prefetch_last;
     return p;
 }
 
@@ -469,8 +454,6 @@ lf_status lf_create(const lf_config *cfg, const lf_weights *w, lf_handle **out)
     if (!h) return LF_ERR_OUT_OF_MEMORY;
     h->cfg = *cfg;
     h->cfg.layer_window = nullptr;   // the caller's array is copied to the device below
-    h->l2_prefetch_bytes = l2_prefetch_bytes_from_env();
-    h->l2_prefetch_last = std::getenv("LF_L2_PREFETCH_LAST") ? 1 : 0;
     h->attn_min_len = attn_min_len_from_env();
     lfk::Geo &g = h->g;
     g.L = cfg->n_layers;

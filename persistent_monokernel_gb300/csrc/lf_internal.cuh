@@ -259,9 +259,6 @@ struct Params {
     // optional %globaltimer trace: [step][slot][cta][4] (slot = 5 * layer + stage, LM = 5 * L)
     unsigned long long *trace;
     int trace_steps;
-    // bytes of this CTA's weight stream kept in flight into L2 ahead of the ring (0 = off)
-    int l2_prefetch_bytes;
-    int l2_prefetch_last;        // 1: the lookahead marks lines evict-last, 0: evict-normal
 };
 
 // Trace stamps per (step, slot, CTA), %globaltimer ns.  GEMV stages: consumer

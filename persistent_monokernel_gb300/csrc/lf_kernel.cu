@@ -248,22 +248,6 @@ struct ProdRing {
     unsigned long long alloc = 0, tail_b = 0;
     uint64_t pol = 0;     // weights: read once per token, L2 evict-first
     uint64_t pol_kv = 0;  // KV cache
-    // L2 lookahead over the weight stream, in "virtual" offsets step * token_bytes + offset
-    const uint8_t *stream_base = nullptr;
-    unsigned long long token_bytes = 0, pf_next = 0, pf_limit = 0, pf_dist = 0;
-    uint64_t pol_pf = 0;
-    __device__ void prefetch_to(unsigned long long target)
-    {
-        if (target > pf_limit) target = pf_limit;
-        while (pf_next < target) {
-            const unsigned long long off = pf_next % token_bytes;
-            unsigned long long n = token_bytes - off;
-            if (n > 32768ull) n = 32768ull;
-            if (n > pf_limit - pf_next) n = pf_limit - pf_next;
-            bulk_prefetch_l2(stream_base + off, (unsigned)n, pol_pf);
-            pf_next += n;
-        }
-    }
     // Reserve `bytes` of ring and a ticket; returns the ring offset or -1 on abort.
     __device__ __forceinline__ int reserve(const Ctx &c, unsigned bytes)
     {
@@ -277,6 +261,7 @@ struct ProdRing {
             tail_b = c.chunk_end[tail_n % TICKETS];
             ++tail_n;
         }
+
         c.chunk_end[n % TICKETS] = alloc + bytes;
         int o = (int)off;
         off += bytes;
@@ -1994,9 +1979,6 @@ __device__ __forceinline__ bool produce_tiles(const Ctx &c, ProdRing &pr, int s,
         const unsigned bytes = (unsigned)R * (unsigned)chunk_row_bytes(p.g);
         const int nch = sg.K / KC;
         for (int k = 0; k < nch; ++k) {
-            if (pr.pf_dist)
-                pr.prefetch_to((unsigned long long)step * pr.token_bytes + (unsigned long long)(src - pr.stream_base) +
-                               bytes + pr.pf_dist);
             if (!pr.emit(c, src, bytes)) return false;
             src += bytes;
         }
@@ -2057,16 +2039,6 @@ __device__ void producer(const Ctx &c, const RepackSrc *w)
         const long long ctx_end = (long long)p.pos0 + p.n_steps;
         const long long kv_read = ctx_end * (long long)p.g.L * p.g.KV * 4;   // K + V, FP16, every layer
         pr.pol_kv = kv_read > (128ll << 20) ? policy_evict_first() : policy_evict_normal();
-    }
-    pr.pol_pf = p.l2_prefetch_last ? policy_evict_last() : policy_evict_normal();
-    if (!kDirect && p.only_stage < 0 && p.l2_prefetch_bytes > 0 && g.E == 0) {
-        const CtaPlan &pl = *c.plan;
-        pr.stream_base = p.wstream + pl.base;
-        pr.token_bytes = pl.lm_off;
-        if (p.mode == MODE_DECODE)
-            pr.token_bytes += (unsigned long long)(pl.u1[ST_LM] - pl.u0[ST_LM]) * (g.d / KC) * (unsigned long long)g.crb;
-        pr.pf_limit = pr.token_bytes * (unsigned long long)p.n_steps;
-        pr.pf_dist = (unsigned long long)p.l2_prefetch_bytes;
     }
     bool ok = true;
     const int n_sub = 5 * g.L + (p.mode == MODE_DECODE ? 1 : 0);
