@@ -230,21 +230,25 @@ def workload_desc(wl, K):
 
 # ------------------------------------------------------------------ CPU oracle timing
 
-def time_oracle(cfg, weights_cpu, prompt, budget_s: float, max_steps: int, warmup: int = 1, layer_window=None):
-    """Decode steps of the CPU oracle after a short prompt; returns (tok/s, steps, seconds, threads)."""
+def time_oracle(cfg, weights_cpu, first_token, first_pos, budget_s: float, max_steps: int, warmup: int = 1,
+                layer_window=None, temperature=0.0, top_k=0, seed=0):
+    """Decode steps of the CPU oracle at the GPU run's context: the pending
+    token sits at position first_pos (orc_skip_to: the cache rows before it
+    are left at zero, which changes no step's work), then warm-up steps and a
+    budget-bounded timed run.  Returns (tok/s, steps, seconds, threads)."""
     import oracle
-    n_prompt = len(prompt)
-    cap = n_prompt + warmup + max_steps + 1
+    cap = first_pos + warmup + max_steps + 2
     orc = oracle.OracleDecoder(cfg, weights_cpu, cap, layer_window=layer_window)
-    orc.prefill(prompt)
+    orc.skip_to(first_pos, first_token)
+    samp = (temperature, top_k, seed)
     if warmup:
-        orc.decode(warmup, want_logits=False)
+        orc.decode(warmup, *samp, want_logits=False)
     t0 = time.perf_counter()
-    orc.decode(1, want_logits=False)
+    orc.decode(1, *samp, want_logits=False)
     one = time.perf_counter() - t0
     n = int(max(1, min(max_steps - 1, budget_s / max(one, 1e-6) - 1)))
     t0 = time.perf_counter()
-    orc.decode(n, want_logits=False)
+    orc.decode(n, *samp, want_logits=False)
     dt = time.perf_counter() - t0
     threads = oracle.num_threads()
     orc.close()
@@ -485,16 +489,18 @@ def run_ours(args):
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         wc = {k: v.cpu() for k, v in weights.items()}
-        pr = make_prompt(cfg.vocab, 8, wl.prompt_seed).numpy()
-        tok_s, n, dt, threads = time_oracle(cfg, wc, pr, budget_s=15.0, max_steps=256, layer_window=wl.layer_window)
+        last = int(prompt[-1].item())
+        tok_s, n, dt, threads = time_oracle(cfg, wc, last, first_pos, budget_s=15.0, max_steps=256,
+                                            layer_window=wl.layer_window, temperature=wl.temperature,
+                                            top_k=wl.top_k, seed=wl.sample_seed)
         result["cpu_baseline"] = {
             "value": round(tok_s, 4),
             "unit": "tok/s",
             "cores": threads,
             "kind": "oracle",
-            "sample": f"{n} greedy decode steps of the same decoder after an 8-token prompt "
-                      f"(context 8..{8 + n}; the GPU run decodes at context {wl.prompt_len}..{wl.prompt_len + K}), "
-                      f"{dt:.1f} s on {threads} OpenMP threads",
+            "sample": f"{n} decode steps of the same decoder at the GPU run's context (positions {first_pos}.."
+                      f"{first_pos + n + 1}, after 1 warm-up step; the prompt's cache rows zero-filled by "
+                      f"orc_skip_to, which leaves each step's work unchanged), {dt:.1f} s on {threads} OpenMP threads",
         }
         del wc
 
@@ -524,11 +530,14 @@ def run_reference(args):
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     mk = {"fp8": make_weights_fp8, "mxfp4": make_weights_mxfp4}.get(wl.weights, make_weights)
     wc = {k: v.cpu() for k, v in mk(cfg, wl.weight_seed, device=dev).items()}
-    pr = make_prompt(cfg.vocab, 8, wl.prompt_seed).numpy()
-    tok_s, n, dt, threads = time_oracle(cfg, wc, pr, budget_s=60.0, max_steps=K, warmup=min(W, 3),
-                                        layer_window=wl.layer_window)
-    sample = (f"{n} of the {K} requested decode steps of the same decoder after an 8-token prompt "
-              f"(context 8..{8 + n}), {dt:.1f} s on {threads} OpenMP threads; warm-up {min(W, 3)} steps")
+    first_pos = wl.prompt_len - 1
+    last = int(make_prompt(cfg.vocab, wl.prompt_len, wl.prompt_seed)[-1].item())
+    tok_s, n, dt, threads = time_oracle(cfg, wc, last, first_pos, budget_s=60.0, max_steps=K, warmup=min(W, 3),
+                                        layer_window=wl.layer_window, temperature=wl.temperature, top_k=wl.top_k,
+                                        seed=wl.sample_seed)
+    sample = (f"{n} of the {K} requested decode steps of the same decoder at the workload's context (positions "
+              f"{first_pos}..{first_pos + min(W, 3) + n}; the prompt's cache rows zero-filled by orc_skip_to, which "
+              f"leaves each step's work unchanged), {dt:.1f} s on {threads} OpenMP threads; warm-up {min(W, 3)} steps")
     print(json.dumps({
         "impl": "reference",
         "metric": METRIC,

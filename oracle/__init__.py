@@ -99,6 +99,7 @@ def lib():
             L.orc_forward.argtypes = [C.c_void_p, C.c_int, f32p]
             L.orc_prefill.argtypes = [C.c_void_p, C.POINTER(C.c_int32), C.c_int]
             L.orc_prefill_blocked.argtypes = [C.c_void_p, C.POINTER(C.c_int32), C.c_int, C.c_int]
+            L.orc_skip_to.argtypes = [C.c_void_p, C.c_int, C.c_int]
             L.orc_decode.argtypes = [C.c_void_p, C.c_int, C.c_float, C.c_int, C.c_uint64,
                                      C.POINTER(C.c_int32), C.POINTER(C.c_int32), f32p]
             _lib = L
@@ -342,6 +343,13 @@ class OracleDecoder:
         t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32))
         if lib().orc_prefill_blocked(self._h, _i32(t), t.size, int(block)):
             raise ValueError("orc_prefill_blocked failed (cache full, empty prompt or unsupported model)")
+
+    def skip_to(self, pos: int, token: int):
+        """Timing hook: `token` becomes the pending token at position `pos`
+        without the forward passes before it (their cache rows are left as
+        they are).  For timing decode steps at a given context only."""
+        if lib().orc_skip_to(self._h, int(pos), int(token)):
+            raise ValueError("orc_skip_to: position or token out of range")
 
     def decode(self, n_steps: int, temperature: float = 0.0, top_k: int = 0, seed: int = 0,
                force_tokens=None, want_logits: bool = True):

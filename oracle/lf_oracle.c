@@ -467,6 +467,20 @@ static void orc_project(const orc_model *m, int which, int l, int n_rows, int k_
         orc_matvec(base[which] + off, x, n_rows, k_dim, y);
 }
 
+/* Timing hook: make `token` the pending token at position `pos` without
+ * running the forward passes of positions 0 .. pos-1 (their cache rows keep
+ * what they hold: zeros in a fresh model).  The work of a decode step depends
+ * on its position, not on the cached values, so decode steps after this time
+ * like steps at that context.  Returns 0, or -1 for a position or token out of
+ * range.  Parity tests never call it. */
+ORC_API int orc_skip_to(orc_model *m, int pos, int token)
+{
+    if (pos < 0 || pos >= m->c.max_seq || token < 0 || token >= m->c.vocab) return -1;
+    m->pos = pos;
+    m->pending = token;
+    return 0;
+}
+
 ORC_API void orc_set_windows(orc_model *m, const int *window)
 {
     for (int l = 0; l < m->c.n_layers; ++l) m->window[l] = window ? (window[l] > 0 ? window[l] : 0) : 0;

@@ -287,3 +287,26 @@ def test_blocked_prefill_rejects_what_it_does_not_cover():
         o.prefill_blocked(np.array([1, cfg.vocab], dtype=np.int32), 4)   # bad token id
     with pytest.raises(ValueError):
         o.prefill_blocked(np.arange(4, dtype=np.int32), 0)    # empty block
+
+
+def test_skip_to_is_a_timing_hook_only():
+    """orc_skip_to moves the pending token to a position without running the
+    passes before it; at position 0 that is exactly a one-token prefill, and
+    positions outside the cache are refused."""
+    cfg = MODELS["tiny"]
+    w = _w(cfg, 0, gains="ones")
+    a = oracle.OracleDecoder(cfg, w, 16)
+    a.prefill(np.array([7], dtype=np.int32))
+    ta, la = a.decode(3)
+    b = oracle.OracleDecoder(cfg, w, 16)
+    b.skip_to(0, 7)
+    tb, lb = b.decode(3)
+    assert np.array_equal(la.view(np.uint32), lb.view(np.uint32)) and np.array_equal(ta, tb)
+    c = oracle.OracleDecoder(cfg, w, 16)
+    c.skip_to(12, 3)
+    assert c.pos == 12 and c.pending == 3
+    c.decode(4)                            # positions 12 .. 15
+    with pytest.raises(ValueError):
+        c.skip_to(16, 3)
+    with pytest.raises(ValueError):
+        c.skip_to(0, cfg.vocab)
