@@ -20,7 +20,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "liblf.so")
-SOURCES = ["lf_kernel.cu", "lf_api.cu", "lf_noalloc.cu", "lf_syncbench.cu", "lf_prefill.cu", "lf_gemm.cu"]
+SOURCES = ["lf_kernel.cu", "lf_api.cu", "lf_noalloc.cu", "lf_syncbench.cu", "lf_prefill.cu", "lf_gemm.cu", "lf_attn_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
               "--expt-relaxed-constexpr"]

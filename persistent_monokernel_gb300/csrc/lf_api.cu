@@ -177,6 +177,7 @@ lfp_args prefill_args(const lf_handle *h)
     a.vc = h->vc;
     a.status = h->status;
     a.sms = h->sm_count;
+    a.attn_stamps = h->trace_steps > 0 ? h->trace : nullptr;   // with tracing on: the prefill attention's stamps
     a.ws = lfp_carve(h->pf_ws, g, h->pf_block, h->sm_count);
     return a;
 }
@@ -624,6 +625,10 @@ lf_status lf_create(const lf_config *cfg, const lf_weights *w, lf_handle **out)
     if (e == cudaSuccess) e = cudaMemset(h->counters, 0, h->counters_bytes);
     if (e == cudaSuccess) e = cudaMemset(h->status, 0, 8 * sizeof(unsigned));
     if (e == cudaSuccess) e = cudaMemset(h->tok_buf, 0, sizeof(int));
+    // the cache starts as zeros: rows past the current position are finite when a
+    // prefill attention chunk reads them (their probabilities are 0)
+    if (e == cudaSuccess) e = cudaMemset(h->kc, 0, kv_elems * sizeof(__half));
+    if (e == cudaSuccess) e = cudaMemset(h->vc, 0, kv_elems * sizeof(__half));
     if (e == cudaSuccess && !mxfp4)
         e = lfk_launch_repack(g, P, h->d_plans, w->wq, w->wk, w->wv, w->wo, w->w_gate, w->w_up, w->w_down,
                               w->lm_head, h->wstream, nullptr);

@@ -39,6 +39,11 @@
 
 #include "lf_gemm.h"
 #include "lf_internal.cuh"
+
+extern "C" cudaError_t lfa_launch(const CUtensorMap *tm_k, const CUtensorMap *tm_v, const float *Qr, int T, int pos0,
+                                  int l, lfk::Geo g, const int *win, __half *Ah, __half *Al, unsigned *status,
+                                  unsigned long long *stamps, cudaStream_t stream);
+extern "C" int lfa_cache_map(CUtensorMap *out, const void *cache, unsigned long long rows);
 #include "lf_prefill.h"
 #include "lf_ptx.cuh"
 
@@ -602,6 +607,11 @@ extern "C" int lfp_make_maps(const lfp_args *a, lfp_maps *m)
         r |= lfg_tensor_map(&m->wqkv[i], a->wqkv, L * NQKV, d, 128 << i);
         r |= lfg_tensor_map(&m->wo[i], a->wo, L * d, Q, 128 << i);
     }
+    if (g.hd == 128) {
+        const unsigned long long rows = L * (unsigned long long)g.Hkv * (unsigned long long)g.max_seq;
+        r |= lfa_cache_map(&m->kc, a->kc, rows);
+        r |= lfa_cache_map(&m->vc, a->vc, rows);
+    }
     if (g.E > 0) {
         const unsigned long long E = g.E, Fe = g.Fe;
         r |= lfg_tensor_map(&m->hh, w.Hh, E * T, Fe, lfg::BM);
@@ -670,7 +680,11 @@ extern "C" int lfp_run(const lfp_args *a, const lfp_maps *m, cudaStream_t s)
             q.vc = a->vc;
             const int bq = plan(q, T, true);
             if (lfg_launch(lfg::EPI_QKV, bq, &m->xh, &m->xl, &m->wqkv[bq / 256], &q, 1, 1, s) != cudaSuccess) return 1;
-            {
+            if (g.hd == 128) {
+                if (lfa_launch(&m->kc, &m->vc, w.Qr, T, pos0, l, g, a->win, w.Ah, w.Al, a->status,
+                               l == 1 && t0 == 0 ? a->attn_stamps : nullptr, s) != cudaSuccess)
+                    return 1;
+            } else {
                 cudaLaunchConfig_t cfg = {};
                 cfg.gridDim = fa_grid;
                 cfg.blockDim = dim3(128);
@@ -681,12 +695,9 @@ extern "C" int lfp_run(const lfp_args *a, const lfp_maps *m, cudaStream_t s)
                 attr[0].val.programmaticStreamSerializationAllowed = 1;
                 cfg.attrs = attr;
                 cfg.numAttrs = 1;
-                const cudaError_t le =
-                    g.hd == 64 ? cudaLaunchKernelEx(&cfg, attn_flash<64>, (const float *)w.Qr, (const __half *)a->kc,
-                                                    (const __half *)a->vc, T, pos0, l, g, a->win, w.Ah, w.Al)
-                               : cudaLaunchKernelEx(&cfg, attn_flash<128>, (const float *)w.Qr, (const __half *)a->kc,
-                                                    (const __half *)a->vc, T, pos0, l, g, a->win, w.Ah, w.Al);
-                if (le != cudaSuccess) return 1;
+                if (cudaLaunchKernelEx(&cfg, attn_flash<64>, (const float *)w.Qr, (const __half *)a->kc,
+                                       (const __half *)a->vc, T, pos0, l, g, a->win, w.Ah, w.Al) != cudaSuccess)
+                    return 1;
             }
             lfg::GemmParams o = p;
             o.N = d;

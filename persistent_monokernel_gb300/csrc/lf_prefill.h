@@ -58,6 +58,9 @@ struct lfp_args {
     __half *kc, *vc;            // KV cache, group-swizzled rows
     unsigned *status;           // [8]: status[0..3] error record, status[4] abort flag
     int sms;                    // SMs of the device (GEMM tiling and split-K)
+    // optional per-CTA %globaltimer stamps of layer 1's attention in the first
+    // block ([grid][8]; profiling aid, null = off)
+    unsigned long long *attn_stamps;
     lfp_workspace ws;
 };
 
@@ -66,13 +69,15 @@ struct lfp_args {
 struct lfp_maps {
     CUtensorMap xh, xl, ah, al, hh, hl, xgh, xgl, wgu;
     CUtensorMap wqkv[2], wo[2], wd[2];   // weight boxes of 128 and 256 rows (the two tile widths)
+    CUtensorMap kc, vc;                  // the KV cache as [L * Hkv * max_seq, hd] rows (head_dim 128)
 };
 
 // Builds the tensor maps of a->ws and a->w*.  0 on success.
 extern "C" int lfp_make_maps(const lfp_args *a, lfp_maps *m);
 // Runs the passes on `stream`: five launches per layer and block (the QKV,
-// O, gate/up and down GEMMs with fused epilogues, and the attention), plus the
-// block's embedding gather; a mixture of experts routes, gathers and runs
+// O, gate/up and down GEMMs with fused epilogues, and the attention -- on
+// the tensor cores through tcgen05 for head_dim 128, warp-level MMA
+// fragments for 64), plus the block's embedding gather; a mixture of experts routes, gathers and runs
 // grouped GEMMs sized on the device.  0 on success; 1 a launch failed.
 extern "C" int lfp_run(const lfp_args *a, const lfp_maps *m, cudaStream_t stream);
 // E4M3 codes -> FP16 (exact: every finite E4M3 value is an FP16 value).
