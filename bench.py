@@ -408,7 +408,7 @@ def run_ours(args):
             "tflops_algorithmic": round(tflops, 1),
             "bf16_peak_tflops": tf_peak,
             "frac": round(tflops / tf_peak, 4),
-            "peak_source": f"{tf_kind} cuBLAS bf16 GEMM (MEASURED_PEAKS.json bf16_tflops)" if tf_kind == "measured"
+            "peak_source": f"{tf_kind} bf16 GEMM peak (MEASURED_PEAKS.json bf16_tflops, a cuBLAS run by the driver)" if tf_kind == "measured"
             else "fallback 1.9 PFLOP/s",
             "note": "FP16 tensor-core products with the activations split into an FP16 head and remainder: "
                     "the tensor work is twice the algorithmic FLOPs",

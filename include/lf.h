@@ -125,13 +125,14 @@ typedef struct {
      * decode steps inside the monokernel (one position per step, the
      * weights streamed once per position).  B > 0: batched prefill over
      * blocks of up to B positions (min(B, max_seq)): per layer, the
-     * projections of the whole block as tensor-core GEMMs and a causal
-     * flash-style attention over the cache, the same arithmetic per
-     * position (FP32 activations, FP16 weights and cache).  lf_create then
-     * keeps a row-major FP16 copy of the seven layer projections (FP8
-     * models: the decoded codes; the scales are applied to the sums), a
-     * cuBLAS handle and a workspace that grows with B; lf_info.prefill_bytes
-     * reports them.  lf_generate_noalloc takes 0 only. */
+     * projections of the whole block as the library's tensor-core GEMMs
+     * (tcgen05, with the RMSNorm, RoPE, KV append, SwiGLU and residual work
+     * fused into their epilogues) and a causal flash-style attention over the
+     * cache, the same arithmetic per position (FP32 activations, FP16
+     * weights and cache).  lf_create then keeps a row-major FP16 copy of the
+     * seven layer projections (FP8 models: the decoded codes; the scales are
+     * applied to the sums) and a workspace that grows with B;
+     * lf_info.prefill_bytes reports them.  lf_generate_noalloc takes 0 only. */
     int32_t prefill_block;
     /* Mixture-of-experts FFN (the pages: only the active experts' weights
      * stream per token, shivam2003.com, "Scaling the idea to frontier
@@ -145,10 +146,8 @@ typedef struct {
      * chosen logits, and streams only the chosen experts' rows.  Needs FP16
      * weights, top_k_experts * ffn_dim <= 16384 and a schedule other than
      * LF_SCHED_MULTI_KERNEL.  The batched prefill (prefill_block > 0) routes
-     * the block's tokens the same way and runs one GEMM per expert over the
-     * tokens routed to it; it reads the experts' token counts back to the
-     * host once per layer and block (lf_prefill then synchronizes its
-     * stream). */
+     * the block's tokens the same way and runs grouped GEMMs over the tokens
+     * routed to each expert, sized on the device (no host round trip). */
     int32_t n_experts;
     int32_t top_k_experts;
 } lf_config;
@@ -249,8 +248,8 @@ typedef struct {
  * MXFP4 block scales outside 2^-23 .. 2^13 with prefill_block > 0; an
  * expert configuration outside the limits of lf_config.n_experts),
  * OUT_OF_MEMORY,
- * NOT_RESIDENT, CUDA (also: the cuBLAS handle of the batched prefill could
- * not be created). */
+ * NOT_RESIDENT, CUDA (also: a tensor map of the batched prefill could not
+ * be encoded). */
 LF_API lf_status lf_create(const lf_config *cfg, const lf_weights *weights, lf_handle **out);
 
 /* Release every library-owned allocation.  Synchronizes the device first.
