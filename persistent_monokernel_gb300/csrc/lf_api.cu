@@ -18,7 +18,7 @@ extern "C" cudaError_t lfk_set_smem(int smem_bytes);
 extern "C" cudaError_t lfk_launch_monokernel(const lfk::Params *p, int smem_bytes, cudaStream_t stream,
                                              int cooperative);
 extern "C" cudaError_t lfk_occupancy(int smem_bytes, int *blocks_per_sm);
-extern "C" unsigned lfk_smem_bytes(int ring_bytes, int a_floats, int b_slots, int d, int lm_rows_max, int L);
+extern "C" unsigned lfk_smem_bytes(int ring_bytes, int a_floats, int lm_rows_max, int L);
 extern "C" cudaError_t lfk_launch_mxfp4_interleave(const void *codes, const void *scales, size_t rows, int cols,
                                                    void *out, cudaStream_t stream);
 extern "C" cudaError_t lfk_launch_repack(lfk::Geo g, int P, const lfk::CtaPlan *plans, const void *wq,
@@ -64,7 +64,7 @@ struct lf_handle {
     unsigned long long *lm_part = nullptr;
     int *tok_buf = nullptr, *tok_seq = nullptr;
     unsigned *status = nullptr, *abort_flag = nullptr;
-    int ring_bytes = 0, a_floats = 0, b_slots = 0, lm_rows_max = 0, smem_bytes = 0;
+    int ring_bytes = 0, a_floats = 0, lm_rows_max = 0, smem_bytes = 0;
     // sequence state
     int pos = 0;
     int has_pending = 0;
@@ -106,6 +106,19 @@ void free_all(lf_handle *h)
                     h->stage_in, h->stage_out, h->trace, h->pf_w, h->pf_s, h->pf_ws, h->pf_tok};
     for (void *p : ptrs)
         if (p) cudaFree(p);
+}
+
+// The activations between GEMV stages start as zeros whenever the pass count
+// restarts: a zero carries the parity of no pass 0 value (the tags of
+// lfk::Params::attn, xattn, hbuf, xout).
+cudaError_t clear_activations(lf_handle *h)
+{
+    const lfk::Geo &g = h->g;
+    cudaError_t e = cudaMemset(h->attn, 0, sizeof(float) * (size_t)g.L * g.Q);
+    if (e == cudaSuccess) e = cudaMemset(h->xattn, 0, sizeof(float) * (size_t)g.L * g.d);
+    if (e == cudaSuccess) e = cudaMemset(h->hbuf, 0, sizeof(float) * (size_t)g.L * g.F);
+    if (e == cudaSuccess) e = cudaMemset(h->xout, 0, sizeof(float) * (size_t)g.L * g.d);
+    return e;
 }
 
 lf_status from_cuda(cudaError_t e)
@@ -351,7 +364,6 @@ lfk::Params base_params(lf_handle *h)
     p.fault_step = h->cfg.fault_step;
     p.ring_bytes = h->ring_bytes;
     p.a_floats = h->a_floats;
-    p.b_slots = h->b_slots;
     p.lm_rows_max = h->lm_rows_max;
     p.attn_min_len = h->attn_min_len;
     p.sched = h->sched;
@@ -523,16 +535,16 @@ lf_status lf_create(const lf_config *cfg, const lf_weights *w, lf_handle **out)
 
     // ---- shared memory: everything but the ring, then the largest ring that fits
     h->max_split = std::max(1, P / g.Hkv);
-    lfk::act_sizes(g, h->plans.data(), P, h->max_split, h->a_floats, h->b_slots);
-    const unsigned rest = lfk_smem_bytes(0, h->a_floats, h->b_slots, g.d, lm_rows_max, g.L);
+    h->a_floats = lfk::scratch_floats(g, h->max_split);
+    const unsigned rest = lfk_smem_bytes(0, h->a_floats, lm_rows_max, g.L);
     if ((int)rest + 2 * lfk::ATT_CHUNK_BYTES > optin) {
         delete h;
         return LF_ERR_NOT_SUPPORTED;
     }
     h->ring_bytes = (int)(((unsigned)optin - rest) / 1024u * 1024u);
-    while ((int)lfk_smem_bytes(h->ring_bytes, h->a_floats, h->b_slots, g.d, lm_rows_max, g.L) > optin)
+    while ((int)lfk_smem_bytes(h->ring_bytes, h->a_floats, lm_rows_max, g.L) > optin)
         h->ring_bytes -= 1024;
-    h->smem_bytes = (int)lfk_smem_bytes(h->ring_bytes, h->a_floats, h->b_slots, g.d, lm_rows_max, g.L);
+    h->smem_bytes = (int)lfk_smem_bytes(h->ring_bytes, h->a_floats, lm_rows_max, g.L);
     if (h->ring_bytes < 2 * lfk::ATT_CHUNK_BYTES) {
         delete h;
         return LF_ERR_NOT_SUPPORTED;
@@ -625,6 +637,7 @@ lf_status lf_create(const lf_config *cfg, const lf_weights *w, lf_handle **out)
     if (e == cudaSuccess) e = cudaMemset(h->counters, 0, h->counters_bytes);
     if (e == cudaSuccess) e = cudaMemset(h->status, 0, 8 * sizeof(unsigned));
     if (e == cudaSuccess) e = cudaMemset(h->tok_buf, 0, sizeof(int));
+    if (e == cudaSuccess) e = clear_activations(h);
     // the cache starts as zeros: rows past the current position are finite when a
     // prefill attention chunk reads them (their probabilities are 0)
     if (e == cudaSuccess) e = cudaMemset(h->kc, 0, kv_elems * sizeof(__half));
@@ -772,6 +785,7 @@ lf_status lf_reset(lf_handle *h)
     cudaError_t e = cudaDeviceSynchronize();
     if (e == cudaSuccess) e = cudaMemset(h->counters, 0, h->counters_bytes);
     if (e == cudaSuccess) e = cudaMemset(h->status, 0, 8 * sizeof(unsigned));
+    if (e == cudaSuccess) e = clear_activations(h);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return from_cuda(e);
     h->pos = 0;

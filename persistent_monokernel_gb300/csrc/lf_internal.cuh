@@ -18,10 +18,9 @@ constexpr int TILE_ROWS = 32;         // rows of one GEMV tile (4 per consumer w
 constexpr int NCW = 8;                // consumer warps
 constexpr int NCT = NCW * 32;         // consumer threads
 // Warp roles after the consumers: the producer streams weights into the ring,
-// the loader brings activation slices into shared memory as they become
-// ready, the reducer sums tile partials and runs the stage epilogues.
-constexpr int W_PROD = NCW, W_LOAD = NCW + 1, W_RED = NCW + 2;
-constexpr int NTHREADS = NCT + 96;
+// the reducer sums tile partials and runs the stage epilogues.
+constexpr int W_PROD = NCW, W_RED = NCW + 1;
+constexpr int NTHREADS = NCT + 64;
 constexpr int TICKETS = 32;           // ring slots in flight (mbarrier pairs)
 constexpr int ATT_CHUNK_BYTES = 32768;// K + V bytes of one attention sub-block
 constexpr int MAX_TOPK = 64;
@@ -31,7 +30,6 @@ constexpr int SIG_STRIDE = 8;         // uint32 words between slice readiness co
 constexpr int PART_BUFS = 8;          // rotating per-tile partial-sum buffers of a GEMV stage
 constexpr int PART_STRIDE = TILE_ROWS + 1;  // per warp: 32 row sums + the sum of squares of x
 constexpr int MAX_SLICES = 64;        // 256-element slices of one activation vector (length <= 16384)
-constexpr int B_RING_SLOTS = 32;      // slots of the O / down-projection input ring
 
 enum Stage { ST_QKV = 0, ST_O = 1, ST_GU = 2, ST_D = 3, ST_LM = 4, N_GEMV = 5 };
 enum Mode { MODE_PREFILL = 0, MODE_DECODE = 1 };
@@ -141,27 +139,21 @@ __host__ __device__ inline int attn_first_pos(int pos, int W) { return (W > 0 &&
 // lf_create and lf_reset).  Every slot is a uint32 SIG_STRIDE words apart.
 //   qkvh[h]   RoPE pair-units of head h written by the QKV stage (query heads,
 //             then key heads, then value heads): hd/2 per pass
-//   attn[k]   elements of slice k (256 elements) of the attention output [Q]
-//   xattn[k]  elements of slice k of the residual after attention [d]
-//   h[k]      elements of slice k of SiLU(gate) * up [F]
-//   xout[k]   elements of slice k of the residual after the FFN [d]
-// A GEMV chunk over columns 256k..256k+255 waits only for slice k of its input.
+// Only the attention stage's inputs go by counters (their readers include
+// TMA copies of the K/V rows, which cannot check values); the GEMV stages'
+// inputs are tagged activations (Params::attn, xattn, hbuf, xout).
 struct SigLayout {
-    int qkvh, attn, xattn, h, xout, per_layer;
+    int qkvh, per_layer;
 };
 __host__ __device__ inline SigLayout sig_layout(const Geo &g)
 {
     SigLayout s;
     s.qkvh = 0;
-    s.attn = s.qkvh + g.Hq + 2 * g.Hkv;
-    s.xattn = s.attn + g.Q / KC;
-    s.h = s.xattn + g.d / KC;
-    s.xout = s.h + g.F / KC;
-    s.per_layer = s.xout + g.d / KC;
+    s.per_layer = g.Hq + 2 * g.Hkv;
     return s;
 }
 
-// Attention scratch (floats) in activation buffer A: q of the group [G][hd],
+// Attention scratch (floats) in shared memory: q of the group [G][hd],
 // the staged fresh K and V rows (hd floats' worth of FP16), the states that
 // half of the warps hand to the other half in one round of the merge (4 warps
 // x 8 x ceil(G/2) lanes x hd/4 output values, then [4][8] running maxima and
@@ -175,6 +167,12 @@ __host__ __device__ inline int attn_scratch_floats(const Geo &g, int max_split)
     return piece > combine ? piece : combine;
 }
 
+// The scratch rounded to whole float4s (Params::a_floats).
+__host__ __device__ inline int scratch_floats(const Geo &g, int max_split)
+{
+    return (attn_scratch_floats(g, max_split) + 3) / 4 * 4;
+}
+
 struct CtaPlan {
     int u0[N_GEMV], u1[N_GEMV];
     unsigned long long base;          // byte offset of the stream in the repacked buffer
@@ -182,25 +180,6 @@ struct CtaPlan {
     unsigned long long stage_off[4];  // offset of each stage inside a layer
     unsigned long long lm_off;        // offset of the LM-head tiles from base
 };
-
-// Activation buffer sizes (host side): A holds a d-vector (QKV, gate/up and
-// LM-head inputs) or the attention scratch; B holds the O and down inputs, as
-// a ring of B_RING_SLOTS 256-float slots when every CTA has a single O tile
-// and a single down tile (each slice then has one reader), else as the whole
-// longer input (Q or F).
-inline void act_sizes(const Geo &g, const CtaPlan *plans, int P, int max_split, int &a_floats, int &b_slots)
-{
-    int a = attn_scratch_floats(g, max_split);
-    a = a > g.d ? a : g.d;
-    a_floats = (a + 3) / 4 * 4;
-    const int nb = (g.Q > g.F ? g.Q : g.F) / KC;
-    bool single = true;
-    for (int b = 0; b < P; ++b) {
-        if (tiles_of(plans[b].u1[ST_O] - plans[b].u0[ST_O], 1) > 1) single = false;
-        if (tiles_of(plans[b].u1[ST_D] - plans[b].u0[ST_D], 1) > 1) single = false;
-    }
-    b_slots = single ? (nb < B_RING_SLOTS ? nb : B_RING_SLOTS) : nb;
-}
 
 struct Params {
     Geo g;
@@ -212,6 +191,16 @@ struct Params {
     __half *kc, *vc;             // [L][Hkv][max_seq][hd]
     const float2 *rope;          // [max_seq][hd/2] (cos, sin)
     float *qbuf;                 // [L][Q]   RoPE'd queries
+    // Tagged activations: the lowest mantissa bit of every value holds the
+    // parity of the forward pass that wrote it (pass e: (e & 1) ^ 1, so the
+    // zeros these buffers start from match no pass 0 value).  Their readers
+    // take them straight from global memory, polling until every value they
+    // need carries the current pass's parity: no counter, no writer fence.
+    // Every pass rewrites every value, and every value is read by the same
+    // threads in every pass of a launch: having seen pass e - 1's value, a
+    // thread cannot see an older one (coherence of one location), so a value
+    // of pass e - 2 is never taken for one of pass e; a launch's first pass
+    // is ordered after the previous launch.
     float *attn;                 // [L][Q]   attention output
     float *xattn;                // [L][d]   residual after attention
     float *hbuf;                 // [L][F]   SiLU(gate) * up
@@ -249,8 +238,7 @@ struct Params {
     long long timeout_ns;
     int fault_step;
     int ring_bytes;
-    int a_floats;                // activation buffer A (QKV / gate-up / LM inputs, attention scratch)
-    int b_slots;                 // 256-float slots of activation buffer B (O / down inputs)
+    int a_floats;                // attention scratch (attn_scratch_floats, rounded to 4)
     int lm_rows_max;
     int attn_min_len;
     int sched;
@@ -262,9 +250,9 @@ struct Params {
 };
 
 // Trace stamps per (step, slot, CTA), %globaltimer ns.  GEMV stages: consumer
-// warp 0 entered the stage, its first input slice landed, the loader had
-// issued every slice, the reducer published the last tile, consumer warp 0
-// finished its last chunk (X1), the last tile's partials were complete (X2).
+// warp 0 entered the stage, the first chunk's input values were read, the
+// reducer stored the last tile, consumer warp 0 finished its last chunk (X1),
+// the last tile's partials were complete (X2); TR_LOADED is not used.
 // Attention: entered, inputs ready, K/V positions done (X1), piece partial
 // published (X2), stage done.  The producer adds when it issued the first and
 // the last chunk of the sub-stage (P0, P1).  TR_WAITS is a count: weight

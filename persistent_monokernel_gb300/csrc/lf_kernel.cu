@@ -44,36 +44,29 @@ namespace lfk {
 // ---------------------------------------------------------------- shared memory
 
 struct SmemLayout {
-    unsigned res, full, empty, chunk_end, afull, bfull, gfull, brel, red, hist, misc, plan;
-    unsigned ring, acta, actb, gain, lmkeys, win, total;
+    unsigned res, full, empty, chunk_end, red, hist, misc, plan;
+    unsigned ring, acta, lmkeys, win, total;
 };
 
 __host__ __device__ inline unsigned align_up(unsigned x, unsigned a) { return (x + a - 1) / a * a; }
 
-__host__ __device__ inline SmemLayout smem_layout(int ring_bytes, int a_floats, int b_slots, int d, int lm_rows_max, int L)
+__host__ __device__ inline SmemLayout smem_layout(int ring_bytes, int a_floats, int lm_rows_max, int L)
 {
     // Fixed-size parts first: their offsets are compile-time constants, so
-    // their addresses cost no registers; the ring, the two activation buffers,
-    // the RMSNorm gain row and the LM keys follow at offsets that depend on
-    // the model.
+    // their addresses cost no registers; the ring, the attention scratch and
+    // the LM keys follow at offsets that depend on the model.
     SmemLayout s;
     unsigned o = 0;
     s.res = o;       o = align_up(o + 4u * PART_BUFS * NCW * PART_STRIDE, 128);
     s.full = o;      o += 8u * TICKETS;
     s.empty = o;     o += 8u * TICKETS;
     s.chunk_end = o; o += 8u * TICKETS;
-    s.afull = o;     o += 8u * MAX_SLICES;   // slice k of buffer A landed
-    s.bfull = o;     o += 8u * MAX_SLICES;   // slot j of buffer B landed
-    s.gfull = o;     o += 16u;               // gain row landed
-    s.brel = o;      o = align_up(o + 4u * MAX_SLICES, 16);   // consumer releases of B slots
     s.red = o;       o = align_up(o + 4u * 64u, 16);
     s.hist = o;      o = align_up(o + 4u * 256u, 16);
     s.misc = o;      o = align_up(o + 4u * 64u, 128);
     s.plan = o;      o = align_up(o + (unsigned)sizeof(CtaPlan), 128);
     s.ring = o;      o = align_up(o + (unsigned)ring_bytes, 128);
     s.acta = o;      o = align_up(o + 4u * (unsigned)a_floats, 128);
-    s.actb = o;      o = align_up(o + 4u * KC * (unsigned)b_slots, 128);
-    s.gain = o;      o = align_up(o + 2u * (unsigned)d, 128);
     s.lmkeys = o;    o = align_up(o + 8u * (unsigned)lm_rows_max, 128);
     s.win = o;       o = align_up(o + 4u * (unsigned)L, 128);   // attention window of each layer
     // the GEMV reads whole 8-row blocks: keep 7 rows of readable bytes after the ring
@@ -83,13 +76,12 @@ __host__ __device__ inline SmemLayout smem_layout(int ring_bytes, int a_floats, 
 }
 
 // misc word indices.  M_TCNT + b / M_TRED + b: consumer arrivals at / reducer
-// passes over partial-sum buffer b (cumulative).  M_AREL: consumer warps done
-// with an input in buffer A; M_ASCR: attention stages done with their scratch
-// in buffer A; M_LMDONE: decode steps whose LM-head keys are complete.
+// passes over partial-sum buffer b (cumulative).  M_LMDONE: decode steps
+// whose LM-head keys are complete.
 // Mixture of experts: M_ROUTE counts the expert choices made in this launch;
 // M_SEL + 8 * (l & 1) + j and M_GATE + 8 * (l & 1) + j hold slot j's expert
 // and gate (FP32 bits) of layer l.
-enum { M_FLAG = 0, M_TOKEN = 1, M_DIGIT = 2, M_REMAIN = 3, M_AREL = 4, M_ASCR = 5, M_LMDONE = 6, M_ROUTE = 7,
+enum { M_FLAG = 0, M_TOKEN = 1, M_DIGIT = 2, M_REMAIN = 3, M_LMDONE = 6, M_ROUTE = 7,
        M_TCNT = 16, M_TRED = 24, M_SEL = 32, M_GATE = 48 };
 
 struct Ctx {
@@ -97,14 +89,11 @@ struct Ctx {
     const CtaPlan *plan;  // this CTA's partition, copied to shared memory (global reads
                           // after an ld.acquire miss L1 and cost an L2 round trip)
     uint8_t *ring;
-    float *acta, *actb;
-    __half *gain;
+    float *acta;      // attention scratch
     unsigned long long *lmkeys;
     float *res;
     uint64_t *full, *empty;
     unsigned long long *chunk_end;
-    uint64_t *afull, *bfull, *gfull;
-    unsigned *brel;
     float *red;
     unsigned *hist;
     unsigned *misc;
@@ -354,6 +343,36 @@ __device__ __forceinline__ float gumbel_dev(unsigned long long seed, int pos, in
     return -logf(-logf(u));
 }
 
+// ---------------------------------------------------------------- tagged activations
+
+// The parity a value of forward pass e carries in its lowest mantissa bit
+// (pass 0 carries 1, so the zero-filled buffers of a fresh or reset handle
+// never pass for pass 0's values).
+__device__ __forceinline__ unsigned pass_tag(unsigned e) { return (e & 1u) ^ 1u; }
+__device__ __forceinline__ float tag_value(float v, unsigned tag) { return __uint_as_float((__float_as_uint(v) & ~1u) | tag); }
+// Stores v with the tag (a relaxed gpu-scope store: the readers poll it with
+// relaxed gpu-scope loads).
+__device__ __forceinline__ void st_tagged(float *dst, float v, unsigned tag)
+{
+    asm volatile("st.relaxed.gpu.global.f32 [%0], %1;" ::"l"(dst), "f"(tag_value(v, tag)) : "memory");
+}
+__device__ __forceinline__ bool tagged_ok(float v, unsigned tag) { return (__float_as_uint(v) & 1u) == tag; }
+__device__ __forceinline__ float4 ld_relaxed_f4(const float *ptr)
+{
+    float4 v;
+    asm volatile("ld.relaxed.gpu.global.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(ptr)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ float ld_relaxed_f(const float *ptr)
+{
+    float v;
+    asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(ptr) : "memory");
+    return v;
+}
+
 // ---------------------------------------------------------------- stage plumbing
 
 __device__ __forceinline__ unsigned *sig_ptr(const Params &p, int l, int idx)
@@ -375,6 +394,51 @@ __device__ __forceinline__ bool wait_smem_ge(const Params &p, const unsigned *w,
             if (t0 == 0) t0 = now;
             else if ((long long)(now - t0) > p.timeout_ns) {
                 raise_error(p, STATUS_TIMEOUT, where, layer, step);
+                return false;
+            }
+        }
+    }
+}
+
+// Warp-wide poll of 8 tagged values per lane (columns 8 lane .. 8 lane + 7
+// of a 256-element slice at src) until every value of the warp carries
+// `tag`; the values arrive in xa, xb.  Returns false on timeout or abort.
+__device__ bool poll_slice(const Params &p, const float *src, unsigned tag, float4 &xa, float4 &xb, unsigned where,
+                           int l, int step)
+{
+    unsigned long long t0 = 0;
+    for (unsigned it = 0;; ++it) {
+        xa = ld_relaxed_f4(src);
+        xb = ld_relaxed_f4(src + 4);
+        const bool ok = tagged_ok(xa.x, tag) && tagged_ok(xa.y, tag) && tagged_ok(xa.z, tag) &&
+                        tagged_ok(xa.w, tag) && tagged_ok(xb.x, tag) && tagged_ok(xb.y, tag) &&
+                        tagged_ok(xb.z, tag) && tagged_ok(xb.w, tag);
+        if (__all_sync(0xffffffffu, ok)) return true;
+        if ((it & 15u) == 15u) {
+            bool stop = ld_relaxed(p.abort_flag) != 0u;
+            const unsigned long long now = globaltimer_ns();
+            if (t0 == 0) t0 = now;
+            else if (!stop && (long long)(now - t0) > p.timeout_ns) {
+                if ((threadIdx.x & 31) == 0) raise_error(p, STATUS_TIMEOUT, where, l, step);
+                stop = true;
+            }
+            if (__any_sync(0xffffffffu, stop)) return false;
+        }
+    }
+}
+// The same for one tagged value (one thread).
+__device__ bool poll_value(const Params &p, const float *src, unsigned tag, float &v, unsigned where, int l, int step)
+{
+    unsigned long long t0 = 0;
+    for (unsigned it = 0;; ++it) {
+        v = ld_relaxed_f(src);
+        if (tagged_ok(v, tag)) return true;
+        if ((it & 15u) == 15u) {
+            if (ld_relaxed(p.abort_flag)) return false;
+            const unsigned long long now = globaltimer_ns();
+            if (t0 == 0) t0 = now;
+            else if ((long long)(now - t0) > p.timeout_ns) {
+                raise_error(p, STATUS_TIMEOUT, where, l, step);
                 return false;
             }
         }
@@ -460,58 +524,42 @@ __device__ __forceinline__ int stage_of(int sid)
 }
 
 // Input of a GEMV stage: the FP32 vector (null for layer 0's QKV, which reads
-// the FP16 embedding row of the step's token), the RMSNorm gain row (null for
-// the O and down projections), the readiness counter of input slice 0 (slice
-// k at + k * SIG_STRIDE), and which activation buffer holds it: B for the O
-// and down projections, A otherwise.
+// the FP16 embedding row of the step's token) and the RMSNorm gain row (null
+// for the O and down projections).  The vector's values are tagged with the
+// pass that wrote them (see pass_tag).
 struct StageIn {
     const float *src32;
     const __half *gain;
-    unsigned *sig;
-    bool bufb;
 };
 
 __device__ __forceinline__ StageIn stage_input(const Params &p, int s, int l)
 {
     const Geo &g = p.g;
-    const SigLayout sl = sig_layout(g);
     StageIn in;
     in.src32 = nullptr;
     in.gain = nullptr;
-    in.sig = nullptr;
-    in.bufb = false;
     if (s == ST_QKV) {
         in.gain = p.attn_norm + (size_t)l * g.d;
-        if (l > 0) {
-            in.src32 = p.xout + (size_t)(l - 1) * g.d;
-            in.sig = sig_ptr(p, l - 1, sl.xout);
-        }
+        if (l > 0) in.src32 = p.xout + (size_t)(l - 1) * g.d;
     } else if (s == ST_O) {
         in.src32 = p.attn + (size_t)l * g.Q;
-        in.sig = sig_ptr(p, l, sl.attn);
-        in.bufb = true;
     } else if (s == ST_GU) {
         in.src32 = p.xattn + (size_t)l * g.d;
-        in.sig = sig_ptr(p, l, sl.xattn);
         in.gain = p.ffn_norm + (size_t)l * g.d;
     } else if (s == ST_D) {
         in.src32 = p.hbuf + (size_t)l * g.F;
-        in.sig = sig_ptr(p, l, sl.h);
-        in.bufb = true;
     } else {
         in.src32 = p.xout + (size_t)(g.L - 1) * g.d;
-        in.sig = sig_ptr(p, g.L - 1, sl.xout);
         in.gain = p.final_norm;
     }
     return in;
 }
 
 // A warp's position in the CTA's sequence of sub-stages, advanced identically
-// by the consumer warps, the loader and the reducer: tiles passed (the
-// partial-sum buffer sequence), fills of buffer A, phases of buffer B's slots,
-// inputs of buffer A handed back by the consumers, attention stages passed.
+// by the consumer warps and the reducer: tiles passed (the partial-sum buffer
+// sequence) and, with a mixture of experts, expert choices made.
 struct PipeState {
-    unsigned seq = 0, afill = 0, bphase = 0, a_uses = 0, attn_uses = 0, routes = 0;
+    unsigned seq = 0, routes = 0;
 };
 
 // Token fed to forward pass `step` (decode: after its counter was acquired).
@@ -551,153 +599,6 @@ __device__ __forceinline__ float row_scale(const Params &p, int s, int l, int un
     case ST_GU: return __ldg(p.wsc[part ? 5 : 4] + (size_t)l * g.F + unit);
     case ST_D: return __ldg(p.wsc[6] + (size_t)l * g.d + unit);
     default: return __ldg(p.wsc[7] + unit);
-    }
-}
-
-// ---------------------------------------------------------------- loader warp
-
-// Brings each GEMV stage's input into shared memory, one 256-element slice at
-// a time, as soon as the slice's readiness counter shows it complete (flag
-// schedule), after the grid barrier (barrier schedule) or at once (multi-kernel
-// schedule).  Buffer A (QKV, gate/up and LM-head inputs) holds the whole
-// vector: every tile of those stages reads every slice.  Buffer B (O and down
-// inputs, one tile per CTA) is a ring of b_slots slots: slice k goes to slot
-// k mod b_slots once the consumer of the slot's previous slice released it;
-// slots without a slice in a round get a plain arrival, so that every slot's
-// mbarrier advances one phase per round.  The RMSNorm gain row of the A
-// stages goes to its own area.  Lanes work on different slices in parallel.
-__device__ void loader(const Ctx &c)
-{
-    const Params &p = *c.p;
-    const Geo &g = p.g;
-    const CtaPlan &pl = *c.plan;
-    const bool decode = p.mode == MODE_DECODE;
-    const int n_sub = 5 * g.L + (decode ? 1 : 0);
-    const uint64_t pol = policy_evict_normal();
-    const uint64_t pol_gain = policy_evict_last();
-    PipeState ps;
-    unsigned bexp[2] = {0u, 0u};     // releases of B slots lane and lane + 32 owed before their next fill
-    // slots this lane armed last (for the drain after an abort): A slots lane
-    // and lane + 32 (bits of a_mask) in fill a_par, B slots in phase b_ph[h],
-    // the gain row (lane 0) in fill g_par
-    unsigned a_mask = 0u, a_par = 0u, g_par = 0u, b_ph[2] = {0u, 0u};
-    bool g_arm = false, b_arm[2] = {false, false};
-    bool ok = true;
-    for (int step = 0; step < p.n_steps && ok; ++step) {
-        const unsigned e = p.epoch0 + (unsigned)step;
-        for (int k = 0; k < n_sub && ok; ++k) {
-            const bool lm = k == 5 * g.L;
-            const int l = lm ? g.L - 1 : k / 5;
-            const int sid = lm ? SID_LM : k % 5;
-            if (!stage_active(p, l, sid)) continue;
-            if (sid == SID_ATTN) {
-                ps.attn_uses++;
-                continue;
-            }
-            const int s = stage_of(sid);
-            const StageGeom sg = stage_geom(g, s);
-            const StageIn in = stage_input(p, s, l);
-            const int n = sg.K / KC;
-            const bool flags = p.sched == SCHED_FLAGS;
-            // ---- barrier schedule: the whole previous sub-stage, everywhere
-            if (p.sched == SCHED_GRID) {
-                unsigned idx;
-                if (c.lane == 0 && grid_barrier_before(p, step, l, sid, idx))
-                    ok = wait_counter(p, p.gbar, (idx + 1u) * (unsigned)p.P, 130, l, step);
-                ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
-                if (!ok) break;
-            }
-            if (!in.bufb) {
-                // ---- buffer A: every consumer warp is done with its previous
-                // input and the attention stages with their scratch
-                if (c.lane == 0)
-                    ok = wait_smem_ge(p, &c.misc[M_AREL], (unsigned)NCW * ps.a_uses, 131, l, step) &&
-                         wait_smem_ge(p, &c.misc[M_ASCR], ps.attn_uses, 132, l, step);
-                ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
-                if (!ok) break;
-                ps.a_uses++;
-                a_mask = 0u;
-                a_par = ps.afill & 1u;
-                if (c.lane == 0) {
-                    mbar_arrive_expect_tx(c.gfull, 2u * (unsigned)g.d);
-                    bulk_g2s(c.gain, in.gain, 2u * (unsigned)g.d, c.gfull, pol_gain);
-                    g_arm = true;
-                    g_par = a_par;
-                }
-                if (!in.src32) {
-                    // layer 0: the FP16 embedding row of the step's token
-                    int tok = 0;
-                    if (c.lane == 0) {
-                        if (flags && decode && step > 0)
-                            ok = wait_counter(p, p.tok_cnt, p.tok_base + (unsigned)step, 133, l, step);
-                        if (ok) tok = step_token(p, step);
-                    }
-                    ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
-                    tok = __shfl_sync(0xffffffffu, tok, 0);
-                    if (!ok) break;
-                    const __half *row = p.embed + (size_t)tok * g.d;
-                    for (int kk = c.lane; kk < n; kk += 32) {
-                        mbar_arrive_expect_tx(c.afull + kk, 2u * KC);
-                        bulk_g2s(c.acta + (size_t)kk * (KC / 2), row + (size_t)kk * KC, 2u * KC, c.afull + kk, pol);
-                        a_mask |= 1u << (kk >> 5);
-                    }
-                } else {
-                    for (int kk = c.lane; kk < n && ok; kk += 32) {
-                        if (flags) ok = wait_counter(p, in.sig + (size_t)kk * SIG_STRIDE, (unsigned)KC * (e + 1u), 134, l, step);
-                        if (!ok) break;
-                        fence_proxy_async_global();
-                        mbar_arrive_expect_tx(c.afull + kk, 4u * KC);
-                        bulk_g2s(c.acta + (size_t)kk * KC, in.src32 + (size_t)kk * KC, 4u * KC, c.afull + kk, pol);
-                        a_mask |= 1u << (kk >> 5);
-                    }
-                }
-                ps.afill++;
-            } else {
-                // ---- buffer B: slots in rounds
-                const int bs = p.b_slots;
-                const int nt = tiles_of(pl.u1[s] - pl.u0[s], sg.rows_per_unit);
-                const int rounds = ceil_div(n, bs);
-                for (int r = 0; r < rounds && ok; ++r) {
-                    for (int h = 0; h < 2 && ok; ++h) {
-                        const int j = c.lane + 32 * h;
-                        if (j >= bs) break;
-                        const int kk = r * bs + j;
-                        ok = wait_smem_ge(p, c.brel + j, bexp[h], 135, l, step);
-                        if (!ok) break;
-                        if (kk < n) {
-                            if (flags) ok = wait_counter(p, in.sig + (size_t)kk * SIG_STRIDE, (unsigned)KC * (e + 1u), 136, l, step);
-                            if (!ok) break;
-                            fence_proxy_async_global();
-                            mbar_arrive_expect_tx(c.bfull + j, 4u * KC);
-                            bulk_g2s(c.actb + (size_t)j * KC, in.src32 + (size_t)kk * KC, 4u * KC, c.bfull + j, pol);
-                            bexp[h] += (unsigned)nt;
-                            b_arm[h] = true;
-                            b_ph[h] = (ps.bphase + (unsigned)r) & 1u;
-                        } else {
-                            mbar_arrive(c.bfull + j);
-                        }
-                    }
-                }
-                ps.bphase += (unsigned)rounds;
-            }
-            ok = __all_sync(0xffffffffu, ok);
-            if (c.lane == 0) trace_mark_producer(c, step, k, TR_LOADED);
-        }
-    }
-    if (!ok) {
-        // No bulk copy may still be writing shared memory when the CTA exits:
-        // wait (bounded) until the last copy into each slot this lane armed
-        // has landed.
-        const unsigned long long t0 = globaltimer_ns();
-        auto settle = [&](uint64_t *bar, unsigned par) {
-            while (!mbar_try_wait(bar, par))
-                if ((long long)(globaltimer_ns() - t0) > p.timeout_ns) return;
-        };
-        for (int h = 0; h < 2; ++h) {
-            if (a_mask & (1u << h)) settle(c.afull + c.lane + 32 * h, a_par);
-            if (b_arm[h]) settle(c.bfull + c.lane + 32 * h, b_ph[h]);
-        }
-        if (g_arm) settle(c.gfull, g_par);
     }
 }
 
@@ -870,13 +771,14 @@ __device__ __forceinline__ float2 h2f(unsigned w) { return __half22float2(*reint
 
 // Consumer side of a GEMV stage.  Chunk j of the stage (tile by tile, column
 // group by column group, as the producer streams them) belongs to warp
-// j mod NCW.  Before a chunk the warp waits only for the input slice of its
-// column group, takes the lane's 8 input values, adds their squares to the
-// RMSNorm sum (tile 0 covers every slice once) and applies the gain.  After
+// j mod NCW.  Before a chunk the warp reads the lane's 8 input values of the
+// chunk's column group in place, polling until all carry the pass's tag (no
+// counter, no staging copy), adds their squares to the RMSNorm sum (tile 0
+// covers every slice once) and applies the gain.  After
 // each tile the warp reduces its 32 row sums over the lanes and hands them to
 // the reducer through a rotating partial-sum buffer.
 // Mixture of experts: every CTA chooses the layer's active experts itself,
-// from the gate/up stage's input it has just loaded (the pages: only the
+// from the gate/up stage's input, read in place (the pages: only the
 // active experts' weights stream per token), so the choice costs no grid-wide
 // hop.  Warp w forms the router logits of experts w, w + 8, ... as FP32 dot
 // products of the FP16 router rows with x * gain (the RMSNorm factor is a
@@ -889,28 +791,30 @@ __device__ __forceinline__ bool route_experts(const Ctx &c, PipeState &ps, int l
 {
     const Params &p = *c.p;
     const Geo &g = p.g;
-    const unsigned apar = ps.afill & 1u;
+    const unsigned tag = pass_tag(p.epoch0 + (unsigned)step);
+    const float *xsrc = p.xattn + (size_t)l * g.d;
+    const __half *gsrc = p.ffn_norm + (size_t)l * g.d;
     bool fail = ab;
-    if (!fail && !mbar_try_wait(c.gfull, apar)) fail = !wait_mbar(p, c.gfull, apar, 140);
-    for (int k = 0; k < g.d / KC && !fail; ++k)
-        if (!mbar_try_wait(c.afull + k, apar)) fail = !wait_mbar(p, c.afull + k, apar, 141);
-    fail = __any_sync(0xffffffffu, fail);
     float *logit = reinterpret_cast<float *>(c.hist);
     float ss = 0.f;
     if (!fail) {
         const __half *wr = p.router + (size_t)l * g.E * g.d;
-        for (int e = c.warp; e < g.E; e += NCW) {
+        for (int e = c.warp; e < g.E && !fail; e += NCW) {
             const __half *row = wr + (size_t)e * g.d;
             float acc = 0.f;
             for (int i = c.lane * 8; i < g.d; i += 256) {
-                float4 xa = lds_f4(smem_u32(c.acta + i)), xb = lds_f4(smem_u32(c.acta + i + 4));
+                float4 xa, xb;
+                if (!poll_slice(p, xsrc + i, tag, xa, xb, 141, l, step)) {
+                    fail = true;
+                    break;
+                }
                 if (e == 0) {
                     ss = fmaf(xa.x, xa.x, ss); ss = fmaf(xa.y, xa.y, ss);
                     ss = fmaf(xa.z, xa.z, ss); ss = fmaf(xa.w, xa.w, ss);
                     ss = fmaf(xb.x, xb.x, ss); ss = fmaf(xb.y, xb.y, ss);
                     ss = fmaf(xb.z, xb.z, ss); ss = fmaf(xb.w, xb.w, ss);
                 }
-                const uint4 gv = lds_u4(smem_u32(c.gain + i));
+                const uint4 gv = __ldg(reinterpret_cast<const uint4 *>(gsrc + i));
                 const float2 g0 = h2f(gv.x), g1 = h2f(gv.y), g2 = h2f(gv.z), g3 = h2f(gv.w);
                 xa.x *= g0.x; xa.y *= g0.y; xa.z *= g1.x; xa.w *= g1.y;
                 xb.x *= g2.x; xb.y *= g2.y; xb.z *= g3.x; xb.w *= g3.y;
@@ -976,16 +880,22 @@ __device__ __forceinline__ bool stage_gemv(const Ctx &c, ConsRing &rc, PipeState
     const bool fp16 = in.src32 == nullptr;
     const bool norm = in.gain != nullptr;
     const int tslot = s == ST_LM ? 5 * g.L : 5 * l + (s == ST_QKV ? 0 : s + 1);
-    const uint32_t xbase = smem_u32(in.bufb ? (const void *)c.actb : (const void *)c.acta) +
-                           (uint32_t)c.lane * (fp16 ? 16u : 32u);
-    const uint32_t gbase = smem_u32(c.gain) + (uint32_t)c.lane * 16u;
     const int nslices = sg.K / KC;
-    const int bs = p.b_slots;
-    const unsigned apar = ps.afill & 1u;
-    if (norm && !ab) {
-        bool fail = false;
-        if (!mbar_try_wait(c.gfull, apar)) fail = !wait_mbar(p, c.gfull, apar, 120);
-        ab = __any_sync(0xffffffffu, fail);
+    const unsigned tag = pass_tag(p.epoch0 + (unsigned)step);
+    // layer 0's QKV: the embedding row of the step's token, read in place
+    const __half *emb_row = nullptr;
+    if (fp16 && !ab) {
+        int tok = 0;
+        bool ok = true;
+        if (c.lane == 0) {
+            if (p.mode == MODE_DECODE && step > 0 && p.sched == SCHED_FLAGS)
+                ok = wait_counter(p, p.tok_cnt, p.tok_base + (unsigned)step, 133, l, step);
+            if (ok) tok = step_token(p, step);
+        }
+        ok = __shfl_sync(0xffffffffu, (int)ok, 0) != 0;
+        tok = __shfl_sync(0xffffffffu, tok, 0);
+        if (!ok) ab = true;
+        emb_row = p.embed + (size_t)tok * g.d;
     }
     const int u0 = pl.u0[s], n = pl.u1[s] - u0;
     const int nt = tiles_of(n, sg.rows_per_unit);
@@ -1010,39 +920,21 @@ __device__ __forceinline__ bool stage_gemv(const Ctx &c, ConsRing &rc, PipeState
                 rc.skip(c, bytes);
                 continue;
             }
-            // the input slice: buffer A slot k, or buffer B slot k mod bs in round k / bs
-            uint64_t *bar;
-            unsigned par;
-            uint32_t xaddr;
-            if (in.bufb) {
-                const int j = k % bs;
-                bar = c.bfull + j;
-                par = (ps.bphase + (unsigned)(k / bs)) & 1u;
-                xaddr = xbase + (uint32_t)j * 4u * KC;
-            } else {
-                bar = c.afull + k;
-                par = apar;
-                xaddr = xbase + (uint32_t)k * (fp16 ? 2u : 4u) * KC;
-            }
-            bool fail = false;
-            if (!mbar_try_wait(bar, par)) fail = !wait_mbar(p, bar, par, 121);
-            if (__any_sync(0xffffffffu, fail)) {
+            // the lane's 8 input values, straight from global memory: fixed
+            // (the embedding row) or polled until they carry this pass's tag
+            float4 xa, xb;
+            if (fp16) {
+                const uint4 hv = __ldg(reinterpret_cast<const uint4 *>(emb_row + (size_t)k * KC) + c.lane);
+                const float2 f0 = h2f(hv.x), f1 = h2f(hv.y), f2 = h2f(hv.z), f3 = h2f(hv.w);
+                xa = make_float4(f0.x, f0.y, f1.x, f1.y);
+                xb = make_float4(f2.x, f2.y, f3.x, f3.y);
+            } else if (!poll_slice(p, in.src32 + (size_t)k * KC + c.lane * 8, tag, xa, xb, 121, l, step)) {
                 ab = true;
                 break;
             }
             if (first) {
                 trace_mark(c, step, tslot, TR_READY);
                 first = false;
-            }
-            float4 xa, xb;
-            if (fp16) {
-                const uint4 hv = lds_u4(xaddr);
-                const float2 f0 = h2f(hv.x), f1 = h2f(hv.y), f2 = h2f(hv.z), f3 = h2f(hv.w);
-                xa = make_float4(f0.x, f0.y, f1.x, f1.y);
-                xb = make_float4(f2.x, f2.y, f3.x, f3.y);
-            } else {
-                xa = lds_f4(xaddr);
-                xb = lds_f4(xaddr + 16u);
             }
             if (norm) {
                 if (jt == 0) {
@@ -1051,7 +943,7 @@ __device__ __forceinline__ bool stage_gemv(const Ctx &c, ConsRing &rc, PipeState
                     ss = fmaf(xb.x, xb.x, ss); ss = fmaf(xb.y, xb.y, ss);
                     ss = fmaf(xb.z, xb.z, ss); ss = fmaf(xb.w, xb.w, ss);
                 }
-                const uint4 gv = lds_u4(gbase + (uint32_t)k * 2u * KC);
+                const uint4 gv = __ldg(reinterpret_cast<const uint4 *>(in.gain + (size_t)k * KC) + c.lane);
                 const float2 g0 = h2f(gv.x), g1 = h2f(gv.y), g2 = h2f(gv.z), g3 = h2f(gv.w);
                 xa.x *= g0.x; xa.y *= g0.y; xa.z *= g1.x; xa.w *= g1.y;
                 xb.x *= g2.x; xb.y *= g2.y; xb.z *= g3.x; xb.w *= g3.y;
@@ -1063,10 +955,6 @@ __device__ __forceinline__ bool stage_gemv(const Ctx &c, ConsRing &rc, PipeState
             else gemv_chunk(c, ch, R, xa, xb, acc);
             mine = true;
             rc.release_own(c);
-            if (in.bufb) {
-                __syncwarp();
-                if (c.lane == 0) atomicAdd(c.brel + (k % bs), 1u);
-            }
         }
         if (ab) break;
         // ---- per-warp row sums -> partial buffer of this tile
@@ -1093,20 +981,13 @@ __device__ __forceinline__ bool stage_gemv(const Ctx &c, ConsRing &rc, PipeState
     }
     if (ab) return true;
     if (c.warp == 0 && c.lane == 0) trace_mark_producer(c, step, tslot, TR_X1);
-    if (in.bufb) {
-        ps.bphase += (unsigned)ceil_div(nslices, bs);
-    } else {
-        ps.afill++;
-        __syncwarp();
-        if (c.lane == 0) atomicAdd(&c.misc[M_AREL], 1u);
-    }
     return false;
 }
 
 // Reducer side of a GEMV stage: for each tile, in the consumers' order, wait
-// for the eight warps' partials, sum them in warp order, run the stage
-// epilogue (lane i: unit a + i; pair stages: rows i and i + nu) and count the
-// outputs in the readiness counters of the slices (or heads) they belong to.
+// for the eight warps' partials, sum them in warp order and run the stage
+// epilogue (lane i: unit a + i; pair stages: rows i and i + nu): QKV outputs
+// are counted in their heads' readiness counters, the others stored tagged.
 template <bool MOE>
 __device__ __forceinline__ bool reduce_stage(const Ctx &c, PipeState &ps, int s, int l, int step, bool ab)
 {
@@ -1134,6 +1015,8 @@ __device__ __forceinline__ bool reduce_stage(const Ctx &c, PipeState &ps, int s,
         ps.routes++;
     }
     float inv = 1.f;
+    const unsigned tag = pass_tag(p.epoch0 + (unsigned)step);
+    bool rfail = false;
     for (int jt = 0; jt < nslot * nt; ++jt) {
         const int t = MOE ? jt % nt : jt, slot = MOE ? jt / nt : 0;
         int a, bnd;
@@ -1155,11 +1038,14 @@ __device__ __forceinline__ bool reduce_stage(const Ctx &c, PipeState &ps, int s,
         if (s == ST_QKV) {
             const int half = g.hd / 2;
             if (u / half < g.Hq + g.Hkv) pre = __ldg(p.rope + (size_t)pos * half + u % half);
-        } else if (s == ST_O) {
-            pre.x = (l == 0) ? __half2float(p.embed[(size_t)tok * g.d + u]) : __ldcg(p.xout + (size_t)(l - 1) * g.d + u);
-        } else if (s == ST_D) {
-            pre.x = __ldcg(p.xattn + (size_t)l * g.d + u);
+        } else if (s == ST_O && l == 0) {
+            pre.x = __half2float(p.embed[(size_t)tok * g.d + u]);
+        } else if (s == ST_O || s == ST_D) {
+            // the residual, tagged: this pass's value (in place long before: the stage consumed it)
+            const float *src = s == ST_O ? p.xout + (size_t)(l - 1) * g.d + u : p.xattn + (size_t)l * g.d + u;
+            if (!poll_value(p, src, tag, pre.x, 114, l, step)) rfail = true;
         }
+        if (__any_sync(0xffffffffu, rfail)) return true;
         bool ok = true;
         if (c.lane == 0) ok = wait_smem_ge(p, &c.misc[M_TCNT + buf], (use + 1u) * NCW, 111, l, step);
         if (!__shfl_sync(0xffffffffu, (int)ok, 0)) return true;
@@ -1213,16 +1099,18 @@ __device__ __forceinline__ bool reduce_stage(const Ctx &c, PipeState &ps, int s,
                 }
                 if (hh >= g.Hq) fence_proxy_async_global();   // K/V rows are read by TMA in later steps
             } else if (s == ST_O) {
-                p.xattn[(size_t)l * g.d + u] = pre.x + sum;
+                const float v = pre.x + sum;
+                st_tagged(p.xattn + (size_t)l * g.d + u, v, tag);
             } else if (s == ST_GU) {
                 const float gt = sum * inv, up = partner * inv;
                 float hv = gt / (1.0f + expf(-gt)) * up;
                 if (moe)   // slot j's gate weights its expert's hidden units
                     hv *= __uint_as_float(*reinterpret_cast<const volatile unsigned *>(
                         &c.misc[M_GATE + 8 * (l & 1) + slot]));
-                p.hbuf[(size_t)l * g.F + (size_t)slot * g.Fe + u] = hv;
+                st_tagged(p.hbuf + (size_t)l * g.F + (size_t)slot * g.Fe + u, hv, tag);
             } else if (s == ST_D) {
-                p.xout[(size_t)l * g.d + u] = pre.x + sum;
+                const float v = pre.x + sum;
+                st_tagged(p.xout + (size_t)l * g.d + u, v, tag);
             } else {
                 const float logit = sum * inv;
                 if (p.debug_logits) p.debug_logits[(size_t)step * g.V + u] = logit;
@@ -1233,11 +1121,12 @@ __device__ __forceinline__ bool reduce_stage(const Ctx &c, PipeState &ps, int s,
             }
         }
         __syncwarp();
-        if (c.lane == 0 && s != ST_LM && !withhold) {
-            if (s == ST_QKV) publish_range(sig_ptr(p, l, sl.qkvh), a, nu, g.hd / 2);
-            else if (s == ST_O) publish_range(sig_ptr(p, l, sl.xattn), a, nu, KC);
-            else if (s == ST_GU) publish_range(sig_ptr(p, l, sl.h), slot * g.Fe + a, nu, KC);
-            else publish_range(sig_ptr(p, l, sl.xout), a, nu, KC);
+        // q, k, v go to the attention stage by counters (their consumers are
+        // the attention pieces and the TMA copies of the K/V rows); the other
+        // outputs are tagged and need none
+        if (s == ST_QKV) {
+            __syncwarp();
+            if (c.lane == 0 && !withhold) publish_range(sig_ptr(p, l, sl.qkvh), a, nu, g.hd / 2);
         }
     }
     if (c.lane == 0) {
@@ -1649,13 +1538,13 @@ __device__ __forceinline__ bool attn_piece(const Ctx &c, ConsRing &rc, int l, in
             M0 = B0;
             M1 = B1;
         }
-        if (e0 < n_el) p.attn[(size_t)l * g.Q + (size_t)hq0 * HD + e0] = n0 / d0;
-        if (e1 < n_el) p.attn[(size_t)l * g.Q + (size_t)hq0 * HD + e1] = n1 / d1;
+        const unsigned tg = pass_tag(p.epoch0 + (unsigned)step);
+        if (e0 < n_el) st_tagged(p.attn + (size_t)l * g.Q + (size_t)hq0 * HD + e0, n0 / d0, tg);
+        if (e1 < n_el) st_tagged(p.attn + (size_t)l * g.Q + (size_t)hq0 * HD + e1, n1 / d1, tg);
     }
-    // ---- count the group's G x hd outputs in the attention-output slices
-    if (cons_sync_or(ab)) return true;
-    if (c.tid == 0) publish_range(sig_ptr(p, l, sig_layout(g).attn), hq0 * HD, G * HD, KC);
-    return false;
+    // the outputs are tagged (no count); the barrier keeps the (m, l) table in
+    // the scratch until every thread has read it
+    return cons_sync_or(ab);
 }
 
 // ---------------------------------------------------------------- LM head selection
@@ -1831,12 +1720,29 @@ __device__ void consumer(const Ctx &c)
     const bool ab = false;
     const bool decode = p.mode == MODE_DECODE;
     const int n_sub = 5 * g.L + (decode ? 1 : 0);
+    // A GEMV stage has no consumer barrier, so a warp without chunks in it
+    // may run ahead to the next point where the consumer warps meet (a named
+    // barrier, which cannot time out).  A warp whose GEMV stage gives up (the
+    // abort flag is then set) therefore does not exit at once: it walks on to
+    // that next meeting point and joins it with the abort bit, so that every
+    // warp leaves there, or reaches the end if none is left.
+    bool failed = false;
     for (int step = 0; step < p.n_steps; ++step) {
         for (int k = 0; k < n_sub; ++k) {
             const bool lm = k == 5 * g.L;
             const int l = lm ? g.L - 1 : k / 5;
             const int sid = lm ? SID_LM : k % 5;
             if (!stage_active(p, l, sid)) continue;
+            if (failed) {
+                unsigned idx;
+                const bool meets = sid == SID_ATTN || lm || (MOE && sid == SID_GU) ||
+                                   (p.sched == SCHED_GRID && grid_barrier_before(p, step, l, sid, idx));
+                if (meets) {
+                    (void)cons_sync_or(true);
+                    return;
+                }
+                continue;
+            }
             trace_mark(c, step, k, TR_ENTER);
             if (sid == SID_ATTN) {
                 // barrier schedule: the whole QKV stage, everywhere (the flag
@@ -1856,17 +1762,26 @@ __device__ void consumer(const Ctx &c)
                                                     : attn_piece<64>(c, rc, l, step, gkv, cp, w0, sp, ab);
                     if (stop) return;
                 }
-                // hand the scratch in buffer A back to the loader
+                // every CTA's consumers meet once per attention stage, with or
+                // without pieces (a meeting point of the walk after a failure)
                 if (cons_sync_or(ab)) return;
-                if (c.tid == 0) {
-                    __threadfence_block();
-                    atomicAdd(&c.misc[M_ASCR], 1u);
-                }
                 if (p.sched == SCHED_GRID && cons_grid_arrive(c, ab)) return;
                 trace_mark(c, step, k, TR_DONE);
             } else {
+                // barrier schedule: the whole previous sub-stage, everywhere
+                unsigned idx;
+                if (p.sched == SCHED_GRID && grid_barrier_before(p, step, l, sid, idx)) {
+                    if (cons_wait(c, p.gbar, (idx + 1u) * (unsigned)p.P, 3, l, step, ab)) return;
+                }
                 if (MOE && sid == SID_GU && route_experts(c, ps, l, step, ab)) return;
-                if (stage_gemv<FMT, MOE>(c, rc, ps, stage_of(sid), l, step, ab)) return;
+                if (stage_gemv<FMT, MOE>(c, rc, ps, stage_of(sid), l, step, ab)) {
+                    if (lm) {   // the other warps meet after the LM head's tiles
+                        (void)cons_sync_or(true);
+                        return;
+                    }
+                    failed = true;
+                    continue;
+                }
                 if (lm) {
                     // the reducer's keys of every LM-head tile of this CTA
                     bool fail = false;
@@ -2106,22 +2021,16 @@ template <bool kDirect, int FMT, bool MOE = false>
 __device__ __forceinline__ void monokernel_body(const Params &p, const RepackSrc *w)
 {
     extern __shared__ __align__(128) uint8_t smem[];
-    const SmemLayout L = smem_layout(p.ring_bytes, p.a_floats, p.b_slots, p.g.d, p.lm_rows_max, p.g.L);
+    const SmemLayout L = smem_layout(p.ring_bytes, p.a_floats, p.lm_rows_max, p.g.L);
     Ctx c;
     c.p = &p;
     c.ring = smem + L.ring;
     c.acta = reinterpret_cast<float *>(smem + L.acta);
-    c.actb = reinterpret_cast<float *>(smem + L.actb);
-    c.gain = reinterpret_cast<__half *>(smem + L.gain);
     c.lmkeys = reinterpret_cast<unsigned long long *>(smem + L.lmkeys);
     c.res = reinterpret_cast<float *>(smem + L.res);
     c.full = reinterpret_cast<uint64_t *>(smem + L.full);
     c.empty = reinterpret_cast<uint64_t *>(smem + L.empty);
     c.chunk_end = reinterpret_cast<unsigned long long *>(smem + L.chunk_end);
-    c.afull = reinterpret_cast<uint64_t *>(smem + L.afull);
-    c.bfull = reinterpret_cast<uint64_t *>(smem + L.bfull);
-    c.gfull = reinterpret_cast<uint64_t *>(smem + L.gfull);
-    c.brel = reinterpret_cast<unsigned *>(smem + L.brel);
     c.red = reinterpret_cast<float *>(smem + L.red);
     c.hist = reinterpret_cast<unsigned *>(smem + L.hist);
     c.misc = reinterpret_cast<unsigned *>(smem + L.misc);
@@ -2141,23 +2050,13 @@ __device__ __forceinline__ void monokernel_body(const Params &p, const RepackSrc
             mbar_init(&c.full[i], 1);
             mbar_init(&c.empty[i], NCW);
         }
-        for (int i = 0; i < MAX_SLICES; ++i) {
-            mbar_init(&c.afull[i], 1);
-            mbar_init(&c.bfull[i], 1);
-        }
-        mbar_init(c.gfull, 1);
         mbar_fence_init();
         *plan_s = p.plans[blockIdx.x];
         for (int i = 0; i < 64; ++i) c.misc[i] = 0u;
-        for (int i = 0; i < MAX_SLICES; ++i) c.brel[i] = 0u;
     }
     __syncthreads();
     if (c.warp == W_PROD) {
         if (c.lane == 0) producer<kDirect, MOE>(c, w);
-        return;
-    }
-    if (c.warp == W_LOAD) {
-        loader(c);
         return;
     }
     if (c.warp == W_RED) {
@@ -2304,9 +2203,9 @@ extern "C" cudaError_t lfk_occupancy(int smem_bytes, int *blocks_per_sm)
                                                         (size_t)smem_bytes);
 }
 
-extern "C" unsigned lfk_smem_bytes(int ring_bytes, int a_floats, int b_slots, int d, int lm_rows_max, int L)
+extern "C" unsigned lfk_smem_bytes(int ring_bytes, int a_floats, int lm_rows_max, int L)
 {
-    return lfk::smem_layout(ring_bytes, a_floats, b_slots, d, lm_rows_max, L).total;
+    return lfk::smem_layout(ring_bytes, a_floats, lm_rows_max, L).total;
 }
 
 extern "C" cudaError_t lfk_launch_repack(lfk::Geo g, int P, const lfk::CtaPlan *plans, const void *wq, const void *wk,

@@ -29,7 +29,7 @@
 #include "../../include/lf.h"
 #include "lf_internal.cuh"
 
-extern "C" unsigned lfk_smem_bytes(int ring_bytes, int a_floats, int b_slots, int d, int lm_rows_max, int L);
+extern "C" unsigned lfk_smem_bytes(int ring_bytes, int a_floats, int lm_rows_max, int L);
 extern "C" cudaError_t lfk_set_smem_direct(int smem_bytes);
 extern "C" cudaError_t lfk_launch_monokernel_direct(const lfk::Params *p, const void *wq, const void *wk,
                                                     const void *wv, const void *wo, const void *wg, const void *wu,
@@ -144,14 +144,13 @@ extern "C" LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_w
         lm_rows_max = n_lm > lm_rows_max ? n_lm : lm_rows_max;
     }
     const int max_split = P / g.Hkv > 1 ? P / g.Hkv : 1;
-    int a_floats = 0, b_slots = 0;
-    lfk::act_sizes(g, h_plans, P, max_split, a_floats, b_slots);
-    const unsigned rest = lfk_smem_bytes(0, a_floats, b_slots, g.d, lm_rows_max, g.L);
+    const int a_floats = lfk::scratch_floats(g, max_split);
+    const unsigned rest = lfk_smem_bytes(0, a_floats, lm_rows_max, g.L);
     if ((int)rest + 2 * lfk::ATT_CHUNK_BYTES > optin) return LF_ERR_NOT_SUPPORTED;
     int ring = (int)(((unsigned)optin - rest) / 1024u * 1024u);
-    while ((int)lfk_smem_bytes(ring, a_floats, b_slots, g.d, lm_rows_max, g.L) > optin) ring -= 1024;
+    while ((int)lfk_smem_bytes(ring, a_floats, lm_rows_max, g.L) > optin) ring -= 1024;
     if (ring < 2 * lfk::ATT_CHUNK_BYTES) return LF_ERR_NOT_SUPPORTED;   // as lf_create: one K/V sub-block must fit
-    const int smem = (int)lfk_smem_bytes(ring, a_floats, b_slots, g.d, lm_rows_max, g.L);
+    const int smem = (int)lfk_smem_bytes(ring, a_floats, lm_rows_max, g.L);
 
     // ---- scratch layout inside the static array
     const size_t kv_elems = (size_t)g.L * g.Hkv * (size_t)g.max_seq * g.hd;
@@ -201,6 +200,11 @@ extern "C" LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_w
     if (e == cudaSuccess) e = cudaMemcpyAsync(base + o_rope, h_rope, sizeof(float2) * rope_elems, cudaMemcpyHostToDevice, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(base + o_cnt, 0, 4 * cnt_words, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(base + o_status, 0, 4 * 8, st);
+    // the pass count restarts at 0: the activations between GEMV stages start as zeros
+    if (e == cudaSuccess) e = cudaMemsetAsync(base + o_attn, 0, 4ull * g.L * g.Q, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(base + o_xattn, 0, 4ull * g.L * g.d, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(base + o_h, 0, 4ull * g.L * g.F, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(base + o_xout, 0, 4ull * g.L * g.d, st);
     if (e == cudaSuccess && windowed)
         e = cudaMemcpyAsync(base + o_win, cfg->layer_window, sizeof(int) * g.L, cudaMemcpyHostToDevice, st);
     if (e != cudaSuccess) return drain_and_fail(st, LF_ERR_CUDA);
@@ -241,7 +245,6 @@ extern "C" LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_w
     p.fault_step = -1;
     p.ring_bytes = ring;
     p.a_floats = a_floats;
-    p.b_slots = b_slots;
     p.lm_rows_max = lm_rows_max;
     p.attn_min_len = kAttnMinLen;
     p.sched = lfk::SCHED_FLAGS;
