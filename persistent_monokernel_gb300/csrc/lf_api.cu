@@ -53,6 +53,7 @@ struct lf_handle {
     __half *kc = nullptr, *vc = nullptr;
     float2 *rope = nullptr;
     float *qbuf = nullptr, *attn = nullptr, *xattn = nullptr, *hbuf = nullptr, *xout = nullptr, *apart = nullptr;
+    float *kvf = nullptr;
     int *win = nullptr;            // [L] attention window per layer, or null (every layer: the whole cache)
     const __half *router = nullptr;  // mixture of experts: the caller's [L][E][d] router rows (read in place)
     float *wsc = nullptr;          // FP8 weights: copies of the eight per-row scale arrays, back to back
@@ -102,7 +103,7 @@ cudaError_t dalloc(T **p, size_t count)
 void free_all(lf_handle *h)
 {
     void *ptrs[] = {h->d_plans, h->wstream, h->kc, h->vc, h->rope, h->qbuf, h->attn, h->xattn, h->hbuf,
-                    h->xout, h->apart, h->win, h->wsc, h->counters, h->lm_part, h->tok_buf, h->tok_seq, h->status,
+                    h->xout, h->apart, h->kvf, h->win, h->wsc, h->counters, h->lm_part, h->tok_buf, h->tok_seq, h->status,
                     h->stage_in, h->stage_out, h->trace, h->pf_w, h->pf_s, h->pf_ws, h->pf_tok};
     for (void *p : ptrs)
         if (p) cudaFree(p);
@@ -115,6 +116,8 @@ cudaError_t clear_activations(lf_handle *h)
 {
     const lfk::Geo &g = h->g;
     cudaError_t e = cudaMemset(h->attn, 0, sizeof(float) * (size_t)g.L * g.Q);
+    if (e == cudaSuccess) e = cudaMemset(h->qbuf, 0, sizeof(float) * (size_t)g.L * g.Q);
+    if (e == cudaSuccess) e = cudaMemset(h->kvf, 0, sizeof(float) * (size_t)g.L * 2 * g.KV);
     if (e == cudaSuccess) e = cudaMemset(h->xattn, 0, sizeof(float) * (size_t)g.L * g.d);
     if (e == cudaSuccess) e = cudaMemset(h->hbuf, 0, sizeof(float) * (size_t)g.L * g.F);
     if (e == cudaSuccess) e = cudaMemset(h->xout, 0, sizeof(float) * (size_t)g.L * g.d);
@@ -346,6 +349,7 @@ lfk::Params base_params(lf_handle *h)
     p.hbuf = h->hbuf;
     p.xout = h->xout;
     p.apart = h->apart;
+    p.kvf = h->kvf;
     p.win = h->win;
     p.router = h->router;
     for (int i = 0; i < 8; ++i) p.wsc[i] = h->wsc ? h->wsc + h->wsc_off[i] : nullptr;
@@ -575,6 +579,7 @@ lf_status lf_create(const lf_config *cfg, const lf_weights *w, lf_handle **out)
         (e = dalloc(&h->hbuf, (size_t)g.L * g.F)) != cudaSuccess ||
         (e = dalloc(&h->xout, (size_t)g.L * g.d)) != cudaSuccess ||
         (e = dalloc(&h->apart, (size_t)g.L * g.Hq * h->max_split * (g.hd + 2))) != cudaSuccess ||
+        (e = dalloc(&h->kvf, (size_t)g.L * 2 * g.KV)) != cudaSuccess ||
         (e = dalloc(&h->counters, n_words)) != cudaSuccess ||
         (e = dalloc(&h->lm_part, (size_t)P * lfk::MAX_TOPK)) != cudaSuccess ||
         (e = dalloc(&h->tok_buf, 1)) != cudaSuccess || (e = dalloc(&h->tok_seq, (size_t)g.max_seq)) != cudaSuccess ||

@@ -167,10 +167,14 @@ __host__ __device__ inline int attn_scratch_floats(const Geo &g, int max_split)
     return piece > combine ? piece : combine;
 }
 
-// The scratch rounded to whole float4s (Params::a_floats).
+// The shared-memory scratch (Params::a_floats): the attention's, or with a
+// mixture of experts at least the FFN input the router stages (d floats);
+// rounded to whole float4s.
 __host__ __device__ inline int scratch_floats(const Geo &g, int max_split)
 {
-    return (attn_scratch_floats(g, max_split) + 3) / 4 * 4;
+    int a = attn_scratch_floats(g, max_split);
+    if (g.E > 0 && g.d > a) a = g.d;
+    return (a + 3) / 4 * 4;
 }
 
 struct CtaPlan {
@@ -190,7 +194,7 @@ struct Params {
     const __half *embed, *attn_norm, *ffn_norm, *final_norm;
     __half *kc, *vc;             // [L][Hkv][max_seq][hd]
     const float2 *rope;          // [max_seq][hd/2] (cos, sin)
-    float *qbuf;                 // [L][Q]   RoPE'd queries
+    float *qbuf;                 // [L][Q]   RoPE'd queries (tagged, see below)
     // Tagged activations: the lowest mantissa bit of every value holds the
     // parity of the forward pass that wrote it (pass e: (e & 1) ^ 1, so the
     // zeros these buffers start from match no pass 0 value).  Their readers
@@ -205,6 +209,8 @@ struct Params {
     float *xattn;                // [L][d]   residual after attention
     float *hbuf;                 // [L][F]   SiLU(gate) * up
     float *xout;                 // [L][d]   residual after FFN
+    float *kvf;                  // [L][2][Hkv][hd] this pass's K and V rows (tagged FP32 copies of
+                                 // the FP16 values the cache holds) for the attention's fresh position
     float *apart;                // [L][Hq][max_split][hd + 2]  (o[hd], m, l) per piece
     const int *win;              // [L] attention window per layer in positions (0: whole cache), or null
     // FP8 weights (g.fmt == FMT_FP8): per-row FP32 scales of wq, wk, wv, wo, w_gate,

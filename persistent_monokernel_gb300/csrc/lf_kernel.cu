@@ -445,6 +445,25 @@ __device__ bool poll_value(const Params &p, const float *src, unsigned tag, floa
     }
 }
 
+// The same for four tagged values (one thread).
+__device__ bool poll_f4(const Params &p, const float *src, unsigned tag, float4 &v, unsigned where, int l, int step)
+{
+    unsigned long long t0 = 0;
+    for (unsigned it = 0;; ++it) {
+        v = ld_relaxed_f4(src);
+        if (tagged_ok(v.x, tag) && tagged_ok(v.y, tag) && tagged_ok(v.z, tag) && tagged_ok(v.w, tag)) return true;
+        if ((it & 15u) == 15u) {
+            if (ld_relaxed(p.abort_flag)) return false;
+            const unsigned long long now = globaltimer_ns();
+            if (t0 == 0) t0 = now;
+            else if ((long long)(now - t0) > p.timeout_ns) {
+                raise_error(p, STATUS_TIMEOUT, where, l, step);
+                return false;
+            }
+        }
+    }
+}
+
 // Count the outputs [e0, e0 + n) of a stage in the readiness counters of the
 // groups of `per` elements they fall in (`base`: counter of group 0).  Called
 // by one lane after __syncwarp or a barrier; the single gpu-scope fence turns
@@ -794,35 +813,43 @@ __device__ __forceinline__ bool route_experts(const Ctx &c, PipeState &ps, int l
     const unsigned tag = pass_tag(p.epoch0 + (unsigned)step);
     const float *xsrc = p.xattn + (size_t)l * g.d;
     const __half *gsrc = p.ffn_norm + (size_t)l * g.d;
+    // the FFN input, staged in the attention scratch (free during the FFN):
+    // slice k by warp k mod NCW, so that each warp waits for at most a few
+    // slices and the polls of the eight warps overlap
+    float *xs = c.acta;
     bool fail = ab;
+    for (int k = c.warp; k < g.d / KC && !fail; k += NCW) {
+        float4 xa, xb;
+        if (!poll_slice(p, xsrc + (size_t)k * KC + c.lane * 8, tag, xa, xb, 141, l, step)) {
+            fail = true;
+            break;
+        }
+        reinterpret_cast<float4 *>(xs + (size_t)k * KC + c.lane * 8)[0] = xa;
+        reinterpret_cast<float4 *>(xs + (size_t)k * KC + c.lane * 8)[1] = xb;
+    }
+    if (cons_sync_or(fail)) return true;
     float *logit = reinterpret_cast<float *>(c.hist);
     float ss = 0.f;
-    if (!fail) {
-        const __half *wr = p.router + (size_t)l * g.E * g.d;
-        for (int e = c.warp; e < g.E && !fail; e += NCW) {
-            const __half *row = wr + (size_t)e * g.d;
-            float acc = 0.f;
-            for (int i = c.lane * 8; i < g.d; i += 256) {
-                float4 xa, xb;
-                if (!poll_slice(p, xsrc + i, tag, xa, xb, 141, l, step)) {
-                    fail = true;
-                    break;
-                }
-                if (e == 0) {
-                    ss = fmaf(xa.x, xa.x, ss); ss = fmaf(xa.y, xa.y, ss);
-                    ss = fmaf(xa.z, xa.z, ss); ss = fmaf(xa.w, xa.w, ss);
-                    ss = fmaf(xb.x, xb.x, ss); ss = fmaf(xb.y, xb.y, ss);
-                    ss = fmaf(xb.z, xb.z, ss); ss = fmaf(xb.w, xb.w, ss);
-                }
-                const uint4 gv = __ldg(reinterpret_cast<const uint4 *>(gsrc + i));
-                const float2 g0 = h2f(gv.x), g1 = h2f(gv.y), g2 = h2f(gv.z), g3 = h2f(gv.w);
-                xa.x *= g0.x; xa.y *= g0.y; xa.z *= g1.x; xa.w *= g1.y;
-                xb.x *= g2.x; xb.y *= g2.y; xb.z *= g3.x; xb.w *= g3.y;
-                acc = dot8(__ldg(reinterpret_cast<const uint4 *>(row + i)), xa, xb, acc);
+    const __half *wr = p.router + (size_t)l * g.E * g.d;
+    for (int e = c.warp; e < g.E; e += NCW) {
+        const __half *row = wr + (size_t)e * g.d;
+        float acc = 0.f;
+        for (int i = c.lane * 8; i < g.d; i += 256) {
+            float4 xa = lds_f4(smem_u32(xs + i)), xb = lds_f4(smem_u32(xs + i + 4));
+            if (e == 0) {
+                ss = fmaf(xa.x, xa.x, ss); ss = fmaf(xa.y, xa.y, ss);
+                ss = fmaf(xa.z, xa.z, ss); ss = fmaf(xa.w, xa.w, ss);
+                ss = fmaf(xb.x, xb.x, ss); ss = fmaf(xb.y, xb.y, ss);
+                ss = fmaf(xb.z, xb.z, ss); ss = fmaf(xb.w, xb.w, ss);
             }
-            acc = warp_sum(acc);
-            if (c.lane == 0) logit[e] = acc;
+            const uint4 gv = __ldg(reinterpret_cast<const uint4 *>(gsrc + i));
+            const float2 g0 = h2f(gv.x), g1 = h2f(gv.y), g2 = h2f(gv.z), g3 = h2f(gv.w);
+            xa.x *= g0.x; xa.y *= g0.y; xa.z *= g1.x; xa.w *= g1.y;
+            xb.x *= g2.x; xb.y *= g2.y; xb.z *= g3.x; xb.w *= g3.y;
+            acc = dot8(__ldg(reinterpret_cast<const uint4 *>(row + i)), xa, xb, acc);
         }
+        acc = warp_sum(acc);
+        if (c.lane == 0) logit[e] = acc;
     }
     if (cons_sync_or(fail)) return true;
     if (c.warp == 0) {
@@ -920,6 +947,10 @@ __device__ __forceinline__ bool stage_gemv(const Ctx &c, ConsRing &rc, PipeState
                 rc.skip(c, bytes);
                 continue;
             }
+            // the gain first (it does not depend on the input: its load
+            // overlaps the poll)
+            uint4 gv = make_uint4(0u, 0u, 0u, 0u);
+            if (norm) gv = __ldg(reinterpret_cast<const uint4 *>(in.gain + (size_t)k * KC) + c.lane);
             // the lane's 8 input values, straight from global memory: fixed
             // (the embedding row) or polled until they carry this pass's tag
             float4 xa, xb;
@@ -943,7 +974,6 @@ __device__ __forceinline__ bool stage_gemv(const Ctx &c, ConsRing &rc, PipeState
                     ss = fmaf(xb.x, xb.x, ss); ss = fmaf(xb.y, xb.y, ss);
                     ss = fmaf(xb.z, xb.z, ss); ss = fmaf(xb.w, xb.w, ss);
                 }
-                const uint4 gv = __ldg(reinterpret_cast<const uint4 *>(in.gain + (size_t)k * KC) + c.lane);
                 const float2 g0 = h2f(gv.x), g1 = h2f(gv.y), g2 = h2f(gv.z), g3 = h2f(gv.w);
                 xa.x *= g0.x; xa.y *= g0.y; xa.z *= g1.x; xa.w *= g1.y;
                 xb.x *= g2.x; xb.y *= g2.y; xb.z *= g3.x; xb.w *= g3.y;
@@ -1077,25 +1107,37 @@ __device__ __forceinline__ bool reduce_stage(const Ctx &c, PipeState &ps, int s,
                 const int half = g.hd / 2;
                 const int hh = u / half, j = u % half;
                 const float v0 = sum * inv, v1 = partner * inv;
+                // q (tagged), and the K/V cache row (FP16) plus its tagged
+                // FP32 copy in kvf, which the attention reads for this position
                 if (hh < g.Hq + g.Hkv) {
                     const float2 cs = pre;
                     const float r0 = v0 * cs.x - v1 * cs.y;
                     const float r1 = v1 * cs.x + v0 * cs.y;
                     if (hh < g.Hq) {
                         float *q = p.qbuf + (size_t)l * g.Q + (size_t)hh * g.hd;
-                        q[j] = r0;
-                        q[j + half] = r1;
+                        if (!withhold) {
+                            st_tagged(q + j, r0, tag);
+                            st_tagged(q + j + half, r1, tag);
+                        }
                     } else {
                         const int kvh = hh - g.Hq;
                         __half *kr = p.kc + (((size_t)l * g.Hkv + kvh) * g.max_seq + pos) * g.hd;
-                        kr[kv_swz(pos, j)] = __float2half_rn(r0);
-                        kr[kv_swz(pos, j + half)] = __float2half_rn(r1);
+                        const __half k0 = __float2half_rn(r0), k1 = __float2half_rn(r1);
+                        kr[kv_swz(pos, j)] = k0;
+                        kr[kv_swz(pos, j + half)] = k1;
+                        float *kf = p.kvf + ((size_t)l * 2 * g.Hkv + kvh) * g.hd;
+                        st_tagged(kf + j, __half2float(k0), tag);
+                        st_tagged(kf + j + half, __half2float(k1), tag);
                     }
                 } else {
                     const int kvh = hh - g.Hq - g.Hkv;
                     __half *vr = p.vc + (((size_t)l * g.Hkv + kvh) * g.max_seq + pos) * g.hd;
-                    vr[kv_swz(pos, j)] = __float2half_rn(v0);
-                    vr[kv_swz(pos, j + half)] = __float2half_rn(v1);
+                    const __half w0 = __float2half_rn(v0), w1 = __float2half_rn(v1);
+                    vr[kv_swz(pos, j)] = w0;
+                    vr[kv_swz(pos, j + half)] = w1;
+                    float *vf = p.kvf + ((size_t)(l * 2 + 1) * g.Hkv + kvh) * g.hd;
+                    st_tagged(vf + j, __half2float(w0), tag);
+                    st_tagged(vf + j + half, __half2float(w1), tag);
                 }
                 if (hh >= g.Hq) fence_proxy_async_global();   // K/V rows are read by TMA in later steps
             } else if (s == ST_O) {
@@ -1212,9 +1254,11 @@ __device__ __forceinline__ bool attn_piece(const Ctx &c, ConsRing &rc, int l, in
     uint4 *qfr = reinterpret_cast<uint4 *>(wml + 2 * (NCW / 2) * 8);   // [KS][32 lanes] q fragments
     const size_t kvbase = ((size_t)l * g.Hkv + gkv) * g.max_seq;
     const bool has_fresh = pos >= j0 && pos < j1;
-    // ---- flag schedule: wait for the query heads of the group and the key and
-    // value heads of gkv (this step's QKV outputs), one thread per counter
-    if (p.sched == SCHED_FLAGS) {
+    // ---- this step's q of the group's heads and (the piece holding position
+    // pos) the fresh K and V rows of gkv: tagged, polled in place.  The
+    // monokernel prefill first waits for the heads' readiness counters (its
+    // passes are not ordered by a token chain); decode needs no counter.
+    if (p.sched == SCHED_FLAGS && p.mode == MODE_PREFILL) {
         const SigLayout sl = sig_layout(g);
         const unsigned target = (unsigned)H2 * (p.epoch0 + (unsigned)step + 1u);
         if (c.tid < G + 2 && !ab) {
@@ -1224,17 +1268,24 @@ __device__ __forceinline__ bool attn_piece(const Ctx &c, ConsRing &rc, int l, in
         if (cons_sync_or(ab)) return true;
     }
     if (!ab) {
+        const unsigned tag = pass_tag(p.epoch0 + (unsigned)step);
         const float *qsrc = p.qbuf + (size_t)l * g.Q + (size_t)hq0 * HD;
-        for (int i = c.tid; i < G * HD / 4; i += NCT)
-            reinterpret_cast<float4 *>(qs)[i] = __ldcg(reinterpret_cast<const float4 *>(qsrc) + i);
+        for (int i = c.tid; i < G * HD / 4 && !ab; i += NCT) {
+            float4 v;
+            if (!poll_f4(p, qsrc + 4 * i, tag, v, 140, l, step)) ab = true;
+            reinterpret_cast<float4 *>(qs)[i] = v;
+        }
         if (has_fresh) {
-            // the cache row is group-swizzled: stage it in plain order
-            const unsigned *ksrc = reinterpret_cast<const unsigned *>(p.kc + (kvbase + pos) * HD);
-            const unsigned *vsrc = reinterpret_cast<const unsigned *>(p.vc + (kvbase + pos) * HD);
-            for (int i = c.tid; i < H2; i += NCT) {
-                const int ph = kv_swz(pos, 2 * i) >> 1;
-                reinterpret_cast<unsigned *>(fresh)[i] = __ldcg(ksrc + ph);
-                reinterpret_cast<unsigned *>(fresh)[H2 + i] = __ldcg(vsrc + ph);
+            // K then V as FP16 in plain order (the values are FP16 already:
+            // the conversion is exact and clears the tag)
+            for (int i = c.tid; i < HD / 2 && !ab; i += NCT) {
+                const int r = (4 * i) / HD, e = (4 * i) % HD;   // r 0: K, 1: V
+                const float *src = p.kvf + ((size_t)(l * 2 + r) * g.Hkv + gkv) * HD + e;
+                float4 v;
+                if (!poll_f4(p, src, tag, v, 142, l, step)) ab = true;
+                __half2 *dst = reinterpret_cast<__half2 *>(fresh) + (r * HD + e) / 2;
+                dst[0] = __floats2half2_rn(v.x, v.y);
+                dst[1] = __floats2half2_rn(v.z, v.w);
             }
         }
     }

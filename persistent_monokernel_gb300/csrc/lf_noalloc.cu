@@ -166,6 +166,7 @@ extern "C" LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_w
     const size_t o_xattn = carve(off, 4ull * g.L * g.d), o_h = carve(off, 4ull * g.L * g.F);
     const size_t o_xout = carve(off, 4ull * g.L * g.d);
     const size_t o_apart = carve(off, 4ull * g.L * g.Hq * max_split * (g.hd + 2));
+    const size_t o_kvf = carve(off, 4ull * g.L * 2 * g.KV);
     const size_t o_cnt = carve(off, 4 * cnt_words);
     const size_t o_lm = carve(off, 8ull * P * lfk::MAX_TOPK);
     const size_t o_tok = carve(off, 4ull * (1 + g.max_seq));
@@ -202,6 +203,8 @@ extern "C" LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_w
     if (e == cudaSuccess) e = cudaMemsetAsync(base + o_status, 0, 4 * 8, st);
     // the pass count restarts at 0: the activations between GEMV stages start as zeros
     if (e == cudaSuccess) e = cudaMemsetAsync(base + o_attn, 0, 4ull * g.L * g.Q, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(base + o_q, 0, 4ull * g.L * g.Q, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(base + o_kvf, 0, 4ull * g.L * 2 * g.KV, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(base + o_xattn, 0, 4ull * g.L * g.d, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(base + o_h, 0, 4ull * g.L * g.F, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(base + o_xout, 0, 4ull * g.L * g.d, st);
@@ -228,6 +231,7 @@ extern "C" LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_w
     p.hbuf = reinterpret_cast<float *>(base + o_h);
     p.xout = reinterpret_cast<float *>(base + o_xout);
     p.apart = reinterpret_cast<float *>(base + o_apart);
+    p.kvf = reinterpret_cast<float *>(base + o_kvf);
     p.win = windowed ? reinterpret_cast<const int *>(base + o_win) : nullptr;
     p.max_split = max_split;
     unsigned *cnt = reinterpret_cast<unsigned *>(base + o_cnt);
