@@ -1252,7 +1252,6 @@ __device__ __forceinline__ bool attn_piece(const Ctx &c, ConsRing &rc, int l, in
     float *ws = qs + G * HD + HD;                       // [4][8 * TT][HD / 4] outputs, then [4][8] m and l
     float *wml = ws + (NCW / 2) * 8 * TT * (HD / 4);
     uint4 *qfr = reinterpret_cast<uint4 *>(wml + 2 * (NCW / 2) * 8);   // [KS][32 lanes] q fragments
-    const size_t kvbase = ((size_t)l * g.Hkv + gkv) * g.max_seq;
     const bool has_fresh = pos >= j0 && pos < j1;
     // ---- this step's q of the group's heads and (the piece holding position
     // pos) the fresh K and V rows of gkv: tagged, polled in place.  The
