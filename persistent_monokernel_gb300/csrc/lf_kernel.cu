@@ -414,6 +414,10 @@ __device__ bool poll_slice(const Params &p, const float *src, unsigned tag, floa
                         tagged_ok(xa.w, tag) && tagged_ok(xb.x, tag) && tagged_ok(xb.y, tag) &&
                         tagged_ok(xb.z, tag) && tagged_ok(xb.w, tag);
         if (__all_sync(0xffffffffu, ok)) return true;
+        // after two misses, back off briefly: warps that ran ahead of their
+        // input (no chunk in a stage) would otherwise keep L2 busy with polls
+        // that the stages still being computed wait behind
+        if (it >= 2) __nanosleep(64);
         if ((it & 15u) == 15u) {
             bool stop = ld_relaxed(p.abort_flag) != 0u;
             const unsigned long long now = globaltimer_ns();
