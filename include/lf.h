@@ -352,8 +352,10 @@ LF_API lf_status lf_read_trace(lf_handle *h, uint64_t *host_out, int64_t capacit
  * bytes) is rejected with LF_ERR_CAPACITY before any work is queued.
  *
  * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) and sets the kernel's shared-memory limit; make that
- * first call before any stream capture.  Every call reuses the same array and
+ * (cudaGetSymbolAddress) and sets the kernel's shared-memory limit.  Every
+ * call copies from pageable host memory and synchronizes `stream`, so no call
+ * can be captured into a CUDA graph: a call on a capturing stream returns
+ * LF_ERR_NOT_SUPPORTED before any work is queued.  Every call reuses the same array and
  * clears the counters it relies on; calls whose work overlaps on the GPU race
  * on the array.  The host staging buffers of the partition and the RoPE table
  * are shared by the whole process, so calls from two host threads at once
@@ -363,7 +365,7 @@ LF_API lf_status lf_read_trace(lf_handle *h, uint64_t *host_out, int64_t capacit
  * The call synchronizes `stream` and returns the device status (LF_OK,
  * LF_ERR_TIMEOUT, or LF_ERR_INVALID_ARG for a token id outside [0, vocab)).
  * Other errors: INVALID_ARG, NOT_SUPPORTED (also: FP8 or MXFP4 weights,
- * prefill_block other than 0, or a mixture of experts), CAPACITY,
+ * prefill_block other than 0, a mixture of experts, a capturing stream), CAPACITY,
  * NOT_RESIDENT, CUDA. */
 LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_weights *w, const int32_t *prompt_dev,
                                      int32_t n_prompt, int32_t n_steps, const lf_sampling *sp, uint64_t seed,

@@ -99,6 +99,12 @@ extern "C" LF_API lf_status lf_generate_noalloc(const lf_config *cfg, const lf_w
     if (cfg->layer_window)
         for (int l = 0; l < cfg->n_layers; ++l)
             if (cfg->layer_window[l] < 0) return LF_ERR_INVALID_ARG;
+    {
+        // pageable copies and a stream synchronize cannot be captured: refuse a capturing stream up front
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(static_cast<cudaStream_t>(stream), &cs) != cudaSuccess) return LF_ERR_CUDA;
+        if (cs != cudaStreamCaptureStatusNone) return LF_ERR_NOT_SUPPORTED;
+    }
     // the forward passes use positions 0 .. n_prompt + n_steps - 2 (the bound of
     // lf_prefill followed by lf_decode on a handle)
     if ((long long)n_prompt - 1 + n_steps > cfg->max_seq) return LF_ERR_CAPACITY;

@@ -97,3 +97,28 @@ def test_noalloc_rejects_requests_beyond_its_scratch(pm):
     st = pm.lib().lf_generate_noalloc(C.byref(cfg), C.byref(w), int(prompt.data_ptr()), 8, 4, C.byref(sp), 0,
                                       int(out.data_ptr()), int(torch.cuda.current_stream().cuda_stream))
     assert st == 3   # LF_ERR_CAPACITY
+
+
+def test_noalloc_refuses_a_capturing_stream(pm):
+    """Every call copies from pageable host memory and synchronizes its
+    stream, which a CUDA graph capture cannot hold: on a capturing stream the
+    call returns LF_ERR_NOT_SUPPORTED before it queues any work."""
+    wl = WORKLOADS["tiny"]
+    m = wl.model
+    weights = make_weights(m, wl.weight_seed, device="cuda")
+    cfg = _cfg(pm, m, 64)
+    w = pm.lf_weights(*[int(weights[n].data_ptr()) for n in pm.WEIGHT_FIELDS])
+    prompt = make_prompt(m.vocab, 8, 1).cuda()
+    out = torch.empty(4, dtype=torch.int32, device="cuda")
+    sp = pm.lf_sampling(0.0, 0, None, None)
+    side = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(side):
+        graph.capture_begin()
+        try:
+            st = pm.lib().lf_generate_noalloc(C.byref(cfg), C.byref(w), int(prompt.data_ptr()), 8, 4, C.byref(sp), 0,
+                                              int(out.data_ptr()), int(side.cuda_stream))
+        finally:
+            graph.capture_end()
+    assert st == 7   # LF_ERR_NOT_SUPPORTED
