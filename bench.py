@@ -49,8 +49,10 @@ def parse_args():
     ap.add_argument("--no-ablations", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--prefill-block", type=int, default=1024,
-                    help="positions per batched-prefill pass (0: prefill as repeated decode steps)")
+    ap.add_argument("--prefill-block", type=int, default=-1,
+                    help="positions per batched-prefill pass (0: prefill as repeated decode steps; "
+                         "-1: the library's choice, the largest multiple of 128 up to 1024 whose attention grid "
+                         "fills its waves of SMs well)")
     return ap.parse_args()
 
 

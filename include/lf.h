@@ -46,6 +46,7 @@ extern "C" {
 
 #define LF_ABI_VERSION 6
 #define LF_MAX_TOP_K 64          /* largest top_k that lf_decode accepts (besides 0) */
+#define LF_PREFILL_AUTO (-1)     /* lf_config.prefill_block: batched prefill, block size chosen by the library */
 
 typedef enum {
     LF_OK = 0,
@@ -132,7 +133,13 @@ typedef struct {
      * weights and cache).  lf_create then keeps a row-major FP16 copy of the
      * seven layer projections (FP8 models: the decoded codes; the scales are
      * applied to the sums) and a workspace that grows with B;
-     * lf_info.prefill_bytes reports them.  lf_generate_noalloc takes 0 only. */
+     * lf_info.prefill_bytes reports them.  B = LF_PREFILL_AUTO: batched, with
+     * the library's choice of B (lf_info.prefill_block reports it): the
+     * largest multiple of 128 up to 1024 (and at most max_seq) whose causal
+     * attention grid -- one CTA per 128 query rows and query head, one CTA per
+     * SM at a time -- fills its waves to at least 80 % of the best such
+     * block's fill (896 for 20 heads on 152 SMs, 1024 for 16 or 32).
+     * lf_generate_noalloc takes 0 only. */
     int32_t prefill_block;
     /* Mixture-of-experts FFN (the pages: only the active experts' weights
      * stream per token, shivam2003.com, "Scaling the idea to frontier
@@ -242,7 +249,7 @@ typedef struct {
  * repack kernel on the legacy default stream and synchronizes.  On success
  * *out receives a handle with no pending token at position 0.
  * Errors: INVALID_ARG (NULL or not 16-byte aligned weight pointers,
- * non-positive sizes, a negative window or prefill_block), NOT_SUPPORTED
+ * non-positive sizes, a negative window, prefill_block below LF_PREFILL_AUTO), NOT_SUPPORTED
  * (shape: head_dim other than 64 or 128, d_model, n_heads*head_dim or
  * ffn_dim not a multiple of 256 or above 16384; an unknown weight_format;
  * MXFP4 block scales outside 2^-23 .. 2^13 with prefill_block > 0; an

@@ -19,6 +19,7 @@ STATUS_NAMES = {0: "LF_OK", 1: "LF_ERR_INVALID_ARG", 2: "LF_ERR_OUT_OF_MEMORY", 
                 8: "LF_ERR_STATE"}
 SCHED_FLAGS, SCHED_GRID_BARRIER, SCHED_MULTI_KERNEL = 0, 1, 2
 MAX_TOP_K = 64
+PREFILL_AUTO = -1   # lf_config.prefill_block: batched prefill, block size chosen by the library (LF_PREFILL_AUTO)
 TRACE_STAMPS = 9
 
 # Every symbol include/lf.h declares.

@@ -80,7 +80,7 @@ struct lf_handle {
     unsigned long long *trace = nullptr;
     int trace_steps = 0;
     int attn_min_len = kAttnMinLen;
-    // batched prefill (cfg.prefill_block > 0): row-major projection copy,
+    // batched prefill (cfg.prefill_block != 0): row-major projection copy,
     // FP8 row scales in the same layout, workspace, token staging, cuBLAS
     int pf_block = 0;
     __half *pf_w = nullptr;
@@ -150,7 +150,7 @@ lf_status validate_config(const lf_config &c)
     if (c.weight_format != LF_WEIGHTS_FP16 && c.weight_format != LF_WEIGHTS_FP8_E4M3 &&
         c.weight_format != LF_WEIGHTS_MXFP4)
         return LF_ERR_NOT_SUPPORTED;
-    if (c.prefill_block < 0) return LF_ERR_INVALID_ARG;
+    if (c.prefill_block < LF_PREFILL_AUTO) return LF_ERR_INVALID_ARG;
     if (c.n_experts < 0 || c.top_k_experts < 0) return LF_ERR_INVALID_ARG;
     if (c.n_experts > 0) {
         // mixture of experts: up to 64 experts, 1..8 active, FP16 weights
@@ -208,7 +208,29 @@ lfp_args prefill_args(const lf_handle *h)
 lf_status setup_prefill(lf_handle *h, const lf_weights *w)
 {
     const lfk::Geo &g = h->g;
-    h->pf_block = std::min(h->cfg.prefill_block, g.max_seq);
+    int block = h->cfg.prefill_block;
+    if (block == LF_PREFILL_AUTO) {
+        // The attention of a block runs (block / 128) x Hq CTAs, one per SM at a
+        // time: the fraction of its waves' SM slots those fill is
+        // n / (ceil(n / SMs) * SMs).  Take the largest block (a multiple of
+        // 128, at most 1,024: larger blocks make better GEMMs) whose fill is at
+        // least 80 % of the best block's.
+        const int sms = std::max(1, h->sm_count);
+        auto fill = [&](int b) {
+            const long long n = (long long)(b / 128) * g.Hq;
+            const long long waves = (n + sms - 1) / sms;
+            return (double)n / (double)(waves * sms);
+        };
+        double best = 0.0;
+        for (int b = 128; b <= 1024; b += 128) best = std::max(best, fill(b));
+        block = 128;
+        for (int b = 1024; b >= 128; b -= 128)
+            if (fill(b) >= 0.8 * best) {
+                block = b;
+                break;
+            }
+    }
+    h->pf_block = std::min(block, g.max_seq);
     const size_t L = g.L, d = g.d, Q = g.Q, KV = g.KV, F = g.F, NQKV = Q + 2 * KV;
     // mixture of experts: gate/up [L][E][2 Fe][d] and down [L][E][d][Fe]
     const size_t nexp = (size_t)lfk::n_expert_parts(g), Fw = g.E > 0 ? (size_t)g.Fe : F;
@@ -675,7 +697,7 @@ lf_status lf_create(const lf_config *cfg, const lf_weights *w, lf_handle **out)
         delete h;
         return from_cuda(e);
     }
-    if (cfg->prefill_block > 0) {
+    if (cfg->prefill_block != 0) {
         st = setup_prefill(h, w);
         if (st != LF_OK) {
             free_all(h);

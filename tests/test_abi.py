@@ -77,8 +77,8 @@ def test_create_rejects_bad_arguments_before_touching_the_gpu(pm):
     assert L.lf_create(C.byref(cfg), C.byref(w8), C.byref(h)) == 1
     cfg = pm.lf_config(**good)
     assert L.lf_create(C.byref(cfg), C.byref(w8), C.byref(h)) == 1
-    # a negative prefill block
-    cfg = pm.lf_config(**{**good, "prefill_block": -1})
+    # a prefill block below LF_PREFILL_AUTO (-1)
+    cfg = pm.lf_config(**{**good, "prefill_block": -2})
     assert L.lf_create(C.byref(cfg), C.byref(w), C.byref(h)) == 1
     # MXFP4: every block-scale pointer is needed (any byte address); no batched prefill
     cfg = pm.lf_config(**{**good, "weight_format": pm.WEIGHTS_MXFP4})

@@ -147,3 +147,33 @@ def test_full_size_2p3b_long_prompt_batched_equals_stepwise(pm):
     (t0, l0), (t1, l1) = out
     compare_logits(l1, l0)
     check_tokens(t1, l0, 0.0, 0, 0, plen - 1)
+
+
+def test_automatic_prefill_block_fits_the_attention_in_one_wave(pm):
+    """prefill_block = LF_PREFILL_AUTO: the library picks the largest multiple
+    of 128 up to 1024 whose attention grid ((block / 128) x heads CTAs) fills
+    its waves of SMs to at least 80 % of the best such block's (896 for 20
+    heads on 152 SMs), and the batched prefill it runs, here over two blocks,
+    still matches the oracle."""
+    cfg = ModelConfig("auto-20h", 1, 768, 20, 5, 128, 1024, 3000)
+    n, prompt_len = 8, 960
+    dec, orc, _ = _setup(pm, cfg, 71, prompt_len + n + 1, pm.PREFILL_AUTO)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+
+    def fill(b):
+        k = b // 128 * cfg.n_heads
+        return k / (-(-k // sms) * sms)
+
+    best = max(fill(b) for b in range(128, 1025, 128))
+    want = next(b for b in range(1024, 127, -128) if fill(b) >= 0.8 * best)
+    assert dec.info()["prefill_block"] == min(want, prompt_len + n + 1)
+    if sms == 152:
+        assert want == 896
+    prompt = make_prompt(cfg.vocab, prompt_len, 72)
+    force = make_prompt(cfg.vocab, n, 73)
+    dec.prefill(prompt.cuda())
+    toks, lg = _forced_decode(dec, cfg, n, force)
+    orc.prefill(prompt.numpy())
+    _, ref = orc.decode(n, force_tokens=force.numpy())
+    compare_logits(lg, ref)
+    check_tokens(toks, ref, 0.0, 0, 0, prompt_len - 1)
