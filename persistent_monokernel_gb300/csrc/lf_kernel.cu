@@ -334,6 +334,31 @@ __device__ __forceinline__ float dot8(uint4 w, float4 xa, float4 xb, float acc)
     return acc;
 }
 
+// Packed FP32 arithmetic for the weight chunks: rows r and r + 1 share one
+// fma.rn.f32x2 per column (the .x half carries row r, the .y half row r + 1),
+// so a lane issues half the FMA instructions while each row keeps its own
+// chain of single-rounded FMAs in column order.  fa / fb: the lane's 8 decoded
+// weights of the two rows (column pairs), xd: the 8 input values, each
+// duplicated into both halves.
+__device__ __forceinline__ float2 h2f2(unsigned w) { return __half22float2(*reinterpret_cast<const __half2 *>(&w)); }
+__device__ __forceinline__ void dup8(const float4 &xa, const float4 &xb, float2 (&xd)[8])
+{
+    xd[0] = make_float2(xa.x, xa.x); xd[1] = make_float2(xa.y, xa.y);
+    xd[2] = make_float2(xa.z, xa.z); xd[3] = make_float2(xa.w, xa.w);
+    xd[4] = make_float2(xb.x, xb.x); xd[5] = make_float2(xb.y, xb.y);
+    xd[6] = make_float2(xb.z, xb.z); xd[7] = make_float2(xb.w, xb.w);
+}
+__device__ __forceinline__ float2 dot8_pair(const float2 (&fa)[4], const float2 (&fb)[4], const float2 (&xd)[8],
+                                            float2 acc)
+{
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        acc = __ffma2_rn(make_float2(fa[i].x, fb[i].x), xd[2 * i], acc);
+        acc = __ffma2_rn(make_float2(fa[i].y, fb[i].y), xd[2 * i + 1], acc);
+    }
+    return acc;
+}
+
 __device__ __forceinline__ float gumbel_dev(unsigned long long seed, int pos, int i)
 {
     uint4 r = philox4x32_10(make_uint4((unsigned)i >> 2, (unsigned)pos, 0u, 0u),
@@ -629,12 +654,15 @@ __device__ __forceinline__ float row_scale(const Params &p, int s, int l, int un
 
 // One weight chunk (R rows x 256 columns, row-major, R <= 32) consumed by one
 // warp: lane l holds the 8 input values of columns 8l..8l+7 (xa, xb) and
-// accumulates all R rows, so each lane carries R independent FMA chains.
+// accumulates all R rows, so each lane carries R independent FMA chains
+// (advanced two rows per packed FMA).
 __device__ __forceinline__ void gemv_chunk(const Ctx &c, const uint8_t *ch, int R, const float4 &xa, const float4 &xb,
                                            float (&acc)[TILE_ROWS])
 {
     // 32-bit shared addresses: the lane's 16 bytes of row r sit at chunk + r * 512 + lane * 16.
     const uint32_t a0 = smem_u32(ch) + (uint32_t)c.lane * 16u;
+    float2 xd[8];
+    dup8(xa, xb, xd);
     // Rows in blocks of 8 at constant offsets: one branch per block, so the 8
     // loads issue together and the 8 FMA chains interleave.  The last block
     // may read up to 7 rows past the chunk (inside the ring, or in the slack
@@ -647,33 +675,26 @@ __device__ __forceinline__ void gemv_chunk(const Ctx &c, const uint8_t *ch, int 
 #pragma unroll
             for (int r = 0; r < 8; ++r) wv[r] = lds_u4(a0 + (uint32_t)(rb + r) * KC_BYTES);
 #pragma unroll
-            for (int r = 0; r < 8; ++r) acc[rb + r] = dot8(wv[r], xa, xb, acc[rb + r]);
+            for (int r = 0; r < 8; r += 2) {
+                const float2 fa[4] = {h2f2(wv[r].x), h2f2(wv[r].y), h2f2(wv[r].z), h2f2(wv[r].w)};
+                const float2 fb[4] = {h2f2(wv[r + 1].x), h2f2(wv[r + 1].y), h2f2(wv[r + 1].z), h2f2(wv[r + 1].w)};
+                const float2 o = dot8_pair(fa, fb, xd, make_float2(acc[rb + r], acc[rb + r + 1]));
+                acc[rb + r] = o.x;
+                acc[rb + r + 1] = o.y;
+            }
         }
     }
 }
 
 // The same for an FP8 chunk (R rows x 256 E4M3 codes, 256 bytes per row): lane
 // l's 8 bytes of row r are decoded pairwise to FP16 (cvt.rn.f16x2.e4m3x2) and
-// then to FP32 before the FMAs; the row's scale is applied to the finished sum.
+// then to FP32 before the (packed) FMAs; the row's scale is applied to the
+// finished sum.
 __device__ __forceinline__ float2 e4m3x2_f2(unsigned short v)
 {
     unsigned h;
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(v));
     return __half22float2(*reinterpret_cast<const __half2 *>(&h));
-}
-__device__ __forceinline__ float dot8_fp8(uint2 w, const float4 &xa, const float4 &xb, float acc)
-{
-    const float2 f0 = e4m3x2_f2((unsigned short)(w.x & 0xFFFFu)), f1 = e4m3x2_f2((unsigned short)(w.x >> 16));
-    const float2 f2 = e4m3x2_f2((unsigned short)(w.y & 0xFFFFu)), f3 = e4m3x2_f2((unsigned short)(w.y >> 16));
-    acc = fmaf(f0.x, xa.x, acc);
-    acc = fmaf(f0.y, xa.y, acc);
-    acc = fmaf(f1.x, xa.z, acc);
-    acc = fmaf(f1.y, xa.w, acc);
-    acc = fmaf(f2.x, xb.x, acc);
-    acc = fmaf(f2.y, xb.y, acc);
-    acc = fmaf(f3.x, xb.z, acc);
-    acc = fmaf(f3.y, xb.w, acc);
-    return acc;
 }
 __device__ __forceinline__ uint2 lds_u2(uint32_t a)
 {
@@ -686,6 +707,8 @@ __device__ __forceinline__ void gemv_chunk_fp8(const Ctx &c, const uint8_t *ch, 
 {
     constexpr uint32_t RB = KC;                        // bytes of one row
     const uint32_t a0 = smem_u32(ch) + (uint32_t)c.lane * 8u;
+    float2 xd[8];
+    dup8(xa, xb, xd);
 #pragma unroll
     for (int rb = 0; rb < TILE_ROWS; rb += 8) {
         if (rb < R) {
@@ -693,7 +716,19 @@ __device__ __forceinline__ void gemv_chunk_fp8(const Ctx &c, const uint8_t *ch, 
 #pragma unroll
             for (int r = 0; r < 8; ++r) wv[r] = lds_u2(a0 + (uint32_t)(rb + r) * RB);
 #pragma unroll
-            for (int r = 0; r < 8; ++r) acc[rb + r] = dot8_fp8(wv[r], xa, xb, acc[rb + r]);
+            for (int r = 0; r < 8; r += 2) {
+                const float2 fa[4] = {e4m3x2_f2((unsigned short)(wv[r].x & 0xFFFFu)),
+                                      e4m3x2_f2((unsigned short)(wv[r].x >> 16)),
+                                      e4m3x2_f2((unsigned short)(wv[r].y & 0xFFFFu)),
+                                      e4m3x2_f2((unsigned short)(wv[r].y >> 16))};
+                const float2 fb[4] = {e4m3x2_f2((unsigned short)(wv[r + 1].x & 0xFFFFu)),
+                                      e4m3x2_f2((unsigned short)(wv[r + 1].x >> 16)),
+                                      e4m3x2_f2((unsigned short)(wv[r + 1].y & 0xFFFFu)),
+                                      e4m3x2_f2((unsigned short)(wv[r + 1].y >> 16))};
+                const float2 o = dot8_pair(fa, fb, xd, make_float2(acc[rb + r], acc[rb + r + 1]));
+                acc[rb + r] = o.x;
+                acc[rb + r + 1] = o.y;
+            }
         }
     }
 }
@@ -721,23 +756,25 @@ __device__ __forceinline__ float e8m0_f(unsigned e)
 {
     return e == 0u ? __uint_as_float(0x00400000u) : e == 255u ? __uint_as_float(0x7FC00000u) : __uint_as_float(e << 23);
 }
-__device__ __forceinline__ float dot8_mxfp4(unsigned w, unsigned sc, const float4 &xa, const float4 &xb, float acc)
+// Rows r and r + 1 (codes wa / wb, block scales sa / sb) with packed FMAs:
+// per row the product of column 0, seven FMAs, then the scaled partial joins
+// the accumulator.
+__device__ __forceinline__ float2 dot8_mxfp4_pair(unsigned wa, unsigned sa, unsigned wb, unsigned sb,
+                                                  const float2 (&xd)[8], float2 acc)
 {
-    unsigned h0, h1, h2, h3;
-    e2m1x8_h2(w, h0, h1, h2, h3);
-    const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&h0));
-    const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&h1));
-    const float2 f2 = __half22float2(*reinterpret_cast<const __half2 *>(&h2));
-    const float2 f3 = __half22float2(*reinterpret_cast<const __half2 *>(&h3));
-    float part = f0.x * xa.x;
-    part = fmaf(f0.y, xa.y, part);
-    part = fmaf(f1.x, xa.z, part);
-    part = fmaf(f1.y, xa.w, part);
-    part = fmaf(f2.x, xb.x, part);
-    part = fmaf(f2.y, xb.y, part);
-    part = fmaf(f3.x, xb.z, part);
-    part = fmaf(f3.y, xb.w, part);
-    return fmaf(part, e8m0_f(sc), acc);
+    unsigned a0, a1, a2, a3, b0, b1, b2, b3;
+    e2m1x8_h2(wa, a0, a1, a2, a3);
+    e2m1x8_h2(wb, b0, b1, b2, b3);
+    const float2 fa[4] = {h2f2(a0), h2f2(a1), h2f2(a2), h2f2(a3)};
+    const float2 fb[4] = {h2f2(b0), h2f2(b1), h2f2(b2), h2f2(b3)};
+    float2 part = __fmul2_rn(make_float2(fa[0].x, fb[0].x), xd[0]);
+    part = __ffma2_rn(make_float2(fa[0].y, fb[0].y), xd[1], part);
+#pragma unroll
+    for (int i = 1; i < 4; ++i) {
+        part = __ffma2_rn(make_float2(fa[i].x, fb[i].x), xd[2 * i], part);
+        part = __ffma2_rn(make_float2(fa[i].y, fb[i].y), xd[2 * i + 1], part);
+    }
+    return __ffma2_rn(part, make_float2(e8m0_f(sa), e8m0_f(sb)), acc);
 }
 __device__ __forceinline__ unsigned lds_u32(uint32_t a)
 {
@@ -757,6 +794,8 @@ __device__ __forceinline__ void gemv_chunk_mxfp4(const Ctx &c, const uint8_t *ch
     constexpr uint32_t RB = fmt_crb(FMT_MXFP4);        // bytes of one row
     const uint32_t a0 = smem_u32(ch) + (uint32_t)c.lane * 4u;
     const uint32_t s0 = smem_u32(ch) + 128u + (uint32_t)(c.lane >> 2);
+    float2 xd[8];
+    dup8(xa, xb, xd);
 #pragma unroll
     for (int rb = 0; rb < TILE_ROWS; rb += 8) {
         if (rb < R) {
@@ -767,7 +806,12 @@ __device__ __forceinline__ void gemv_chunk_mxfp4(const Ctx &c, const uint8_t *ch
                 sv[r] = lds_u8(s0 + (uint32_t)(rb + r) * RB);
             }
 #pragma unroll
-            for (int r = 0; r < 8; ++r) acc[rb + r] = dot8_mxfp4(wv[r], sv[r], xa, xb, acc[rb + r]);
+            for (int r = 0; r < 8; r += 2) {
+                const float2 o = dot8_mxfp4_pair(wv[r], sv[r], wv[r + 1], sv[r + 1], xd,
+                                                 make_float2(acc[rb + r], acc[rb + r + 1]));
+                acc[rb + r] = o.x;
+                acc[rb + r + 1] = o.y;
+            }
         }
     }
 }
