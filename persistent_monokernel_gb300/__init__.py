@@ -242,7 +242,8 @@ class Decoder:
         _check(lib().lf_enable_trace(self._h, int(max_steps)), "lf_enable_trace")
 
     def read_trace(self):
-        """Stage trace as a uint64 array [steps, slots, ctas, 6] (ns stamps)."""
+        """Stage trace as a uint64 array [steps, slots, ctas, TRACE_STAMPS] (ns stamps; the last field
+        is a count of weight chunks that had not landed when first asked for)."""
         import numpy as np
         n = C.c_int64()
         _check(lib().lf_read_trace(self._h, None, 0, C.byref(n)), "lf_read_trace")
